@@ -1,0 +1,353 @@
+"""CPU oracle for the replica-integrity scan.
+
+TEST INFRASTRUCTURE ONLY.  The product package never imports this module;
+only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg do.  It shares no code with the CUDA path.
+
+Sources (web pages on silent data corruption):
+  [AWS]   "Detecting and recovering from silent data corruption on Amazon
+          SageMaker HyperPod" (AWS Machine Learning Blog).
+  [AEGIS] "Safeguarding LLM Training at Scale: Online SDC Detection and
+          Insights from 35 Million GPU Hours" (review page).
+
+The element loops live in ``sdc_oracle.c`` (plain scalar C, compiled with gcc
+on first use); the vote and the exact rounding of the sum of squares are plain
+Python.  Every function takes host numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+import threading
+from collections import Counter
+from concurrent.futures import ThreadPoolExecutor
+from fractions import Fraction
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sdc_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+
+# dtype codes of the oracle's C file (its own numbering)
+DTYPE_CODES = {"f32": 1, "bf16": 2, "f16": 3}
+ESIZE = {"f32": 4, "bf16": 2, "f16": 2}
+_QMIN = -149
+_NBINS = 270
+FLT_MAX = 3.4028234663852886e38
+
+_lib = None
+_lib_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile sdc_oracle.c into oracle/_build/liboracle.so (gcc, -O2).
+
+    ``-ffp-contract=off`` keeps every float operation a separately rounded
+    IEEE operation (no fused multiply-add), as the average's definition needs.
+    """
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+           "-fno-fast-math", "-Wall", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lib_lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            u64p = ctypes.POINTER(ctypes.c_uint64)
+            lib.oracle_fingerprint.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint32,
+                                               ctypes.c_uint64, u64p]
+            lib.oracle_fingerprint.restype = ctypes.c_int
+            lib.oracle_xorsum.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint32, u64p]
+            lib.oracle_xorsum.restype = ctypes.c_int
+            lib.oracle_grad_stats.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint32,
+                                              u64p, u64p]
+            lib.oracle_grad_stats.restype = ctypes.c_int
+            lib.oracle_average.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_uint32,
+                                           ctypes.c_uint64, ctypes.c_uint32, ctypes.c_void_p]
+            lib.oracle_average.restype = ctypes.c_int
+            lib.oracle_round_f32.argtypes = [ctypes.c_float, ctypes.c_uint32]
+            lib.oracle_round_f32.restype = ctypes.c_uint32
+            _lib = lib
+    return _lib
+
+
+def _as_bytes(a: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    return a
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def _slices(numel: int, threads: int, min_slice: int = 1 << 22):
+    """Consecutive element slices [lo, hi) used to spread one loop over threads."""
+    if threads <= 1 or numel <= min_slice:
+        return [(0, numel)]
+    n = min(threads * 4, max(1, numel // min_slice))
+    step = -(-numel // n)
+    return [(lo, min(numel, lo + step)) for lo in range(0, numel, step)]
+
+
+# --------------------------------------------------------------------------
+# Fingerprint  ([AWS] "Compare by fingerprint")
+# --------------------------------------------------------------------------
+def fingerprint(a: np.ndarray, threads: int = 1) -> tuple[int, int]:
+    """(S, W) of one tensor: S = sum of widened raw bits, W = sum of (index+1)*bits.
+
+    Both mod 2^64, returned as Python ints in [0, 2^64).  ``a`` is any
+    contiguous numpy array; its itemsize selects the bit view.  With
+    ``threads > 1`` the tensor is walked in consecutive slices (each weighted
+    by its global index, as the page's chunk loop does) on a thread pool and
+    the slices' sums are added mod 2^64.
+    """
+    lib = _load()
+    a = _as_bytes(a)
+    esize = a.itemsize
+    numel = a.size
+    base = _ptr(a)
+
+    def run(lo_hi):
+        lo, hi = lo_hi
+        out = (ctypes.c_uint64 * 2)()
+        rc = lib.oracle_fingerprint(base + lo * esize, hi - lo, esize, lo, out)
+        if rc != 0:
+            raise ValueError(f"bad element size {esize}")
+        return out[0], out[1]
+
+    parts = _map(run, _slices(numel, threads), threads)
+    s = sum(p[0] for p in parts) % (1 << 64)
+    w = sum(p[1] for p in parts) % (1 << 64)
+    return s, w
+
+
+def xorsum(a: np.ndarray, threads: int = 1) -> int:
+    """XOR of every element's raw bits, zero-extended to 64 bits ([AEGIS] sec. 4)."""
+    lib = _load()
+    a = _as_bytes(a)
+    esize = a.itemsize
+    base = _ptr(a)
+
+    def run(lo_hi):
+        lo, hi = lo_hi
+        out = ctypes.c_uint64()
+        if lib.oracle_xorsum(base + lo * esize, hi - lo, esize, ctypes.byref(out)) != 0:
+            raise ValueError(f"bad element size {esize}")
+        return out.value
+
+    x = 0
+    for p in _map(run, _slices(a.size, threads), threads):
+        x ^= p
+    return x
+
+
+def xorsum_compare(a: list[int], b: list[int]) -> tuple[list[int], list[int]]:
+    """Pairwise compare of two xorsum lists: (mismatch flags, a XOR b)."""
+    mism = [1 if x != y else 0 for x, y in zip(a, b)]
+    diff = [x ^ y for x, y in zip(a, b)]
+    return mism, diff
+
+
+def _map(fn, items, threads):
+    if threads <= 1 or len(items) == 1:
+        return [fn(it) for it in items]
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        return list(ex.map(fn, items))
+
+
+# --------------------------------------------------------------------------
+# Gradient statistics  ([AWS] "Check 1: NaN/Inf gradients, before and after
+# the all-reduce"; "Decide what the alarm means")
+# --------------------------------------------------------------------------
+def exact_sum_from_bins(bins: np.ndarray) -> float:
+    """Correctly rounded double of sum_b bins[b] * 4^(b + QMIN).
+
+    ``bins`` is a (NBINS, 2) uint64 array of 128-bit integers (lo, hi).  The
+    sum is formed exactly with rationals and rounded once (Fraction -> float
+    rounds to nearest, ties to even).
+    """
+    total = Fraction(0)
+    for b in range(_NBINS):
+        v = int(bins[b, 0]) | (int(bins[b, 1]) << 64)
+        if v:
+            total += Fraction(v) * Fraction(2) ** (2 * (b + _QMIN))
+    return float(total)
+
+
+def grad_stats(a: np.ndarray, dtype: str, threads: int = 1) -> dict:
+    """Non-finite counts and exact sum of squares of one gradient buffer.
+
+    Returns n_nan, n_inf, n_big (finite, x^2 > FLT_MAX), n_elems,
+    sumsq_finite (exact sum of x^2 over finite x, rounded once to double),
+    norm (NaN if any NaN, else +Inf if any Inf, else sqrt(sumsq_finite)) and
+    nonfinite_fp32 (the page's float32 flag: any NaN/Inf, or a squared norm
+    above FLT_MAX, i.e. a norm above ~1.8e19).
+    ``a`` holds the raw elements (uint16 for bf16/f16, float32/uint32 for f32).
+    """
+    if np.asarray(a).itemsize != ESIZE[dtype]:
+        raise ValueError("element size does not match dtype")
+    return grad_stats_multi([a], [dtype], threads)
+
+
+def finish_stats(n_nan: int, n_inf: int, n_big: int, n_elems: int, sumsq: float) -> dict:
+    """Derived fields of a stats record (norm with IEEE propagation, fp32 flag)."""
+    if n_nan:
+        norm = math.nan
+    elif n_inf:
+        norm = math.inf
+    else:
+        norm = math.sqrt(sumsq)
+    nonfinite = 1 if (n_nan or n_inf or sumsq > FLT_MAX) else 0
+    return {"n_nan": n_nan, "n_inf": n_inf, "n_big": n_big, "n_elems": n_elems,
+            "sumsq_finite": sumsq, "norm": norm, "nonfinite_fp32": nonfinite}
+
+
+def grad_stats_multi(arrays: list[np.ndarray], dtypes: list[str], threads: int = 1) -> dict:
+    """Stats of one replica made of several tensors, summed exactly once.
+
+    All tensors' squares go into one set of exponent bins, so the result is
+    the exact sum over every finite element of every tensor, rounded once.
+    """
+    lib = _load()
+    counts = np.zeros(3, dtype=np.uint64)
+    acc = [0] * _NBINS
+    n = 0
+    lock = threading.Lock()
+
+    def run(item):
+        a, dt, lo, hi = item
+        c = np.zeros(3, dtype=np.uint64)
+        bins = np.zeros((_NBINS, 2), dtype=np.uint64)
+        lib.oracle_grad_stats(_ptr(a) + lo * a.itemsize, hi - lo, DTYPE_CODES[dt],
+                              c.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)),
+                              bins.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)))
+        with lock:
+            counts[:] += c
+            for b in np.nonzero(bins[:, 0] | bins[:, 1])[0]:
+                acc[b] += int(bins[b, 0]) | (int(bins[b, 1]) << 64)
+
+    items = []
+    for a, dt in zip(arrays, dtypes):
+        a = _as_bytes(a)
+        n += a.size
+        for lo, hi in _slices(a.size, threads):
+            items.append((a, dt, lo, hi))
+    _map(run, items, threads)
+    merged = np.zeros((_NBINS, 2), dtype=np.uint64)
+    for b in range(_NBINS):
+        merged[b, 0] = acc[b] & ((1 << 64) - 1)
+        merged[b, 1] = acc[b] >> 64
+    return finish_stats(int(counts[0]), int(counts[1]), int(counts[2]), n,
+                        exact_sum_from_bins(merged))
+
+
+# --------------------------------------------------------------------------
+# Average of local gradients  ([AWS] "Step 1: Detect", worked example)
+# --------------------------------------------------------------------------
+def average(bufs: list[np.ndarray], dtype: str, threads: int = 1) -> np.ndarray:
+    """float32 sum in buffer order, / n, rounded to dtype (ties to even); NaN canonical."""
+    lib = _load()
+    code = DTYPE_CODES[dtype]
+    bufs = [_as_bytes(b) for b in bufs]
+    numel = bufs[0].size
+    for b in bufs:
+        if b.size != numel or b.itemsize != ESIZE[dtype]:
+            raise ValueError("buffers disagree in size")
+    out = np.empty(numel, dtype=np.uint32 if dtype == "f32" else np.uint16)
+    es = ESIZE[dtype]
+
+    def run(lo_hi):
+        lo, hi = lo_hi
+        ptrs = (ctypes.c_void_p * len(bufs))(*[_ptr(b) + lo * es for b in bufs])
+        rc = lib.oracle_average(ptrs, len(bufs), hi - lo, code, _ptr(out) + lo * es)
+        if rc != 0:
+            raise ValueError("bad arguments")
+
+    _map(run, _slices(numel, threads), threads)
+    return out
+
+
+def round_f32(x: float, dtype: str) -> int:
+    """Bits of float32 x rounded to bf16/f16 by the oracle's own rounding."""
+    return int(_load().oracle_round_f32(ctypes.c_float(x), DTYPE_CODES[dtype]))
+
+
+# --------------------------------------------------------------------------
+# Strict-majority vote  ([AWS] "Check 3: Weight fingerprints, after the
+# optimizer step")
+# --------------------------------------------------------------------------
+SUSPECT_AGREE = -1
+SUSPECT_SEVERAL = -2
+SUSPECT_NO_MAJORITY = -3
+
+
+def vote(table) -> tuple[list[int], list[int], dict]:
+    """Per-tensor vote over R replicas' fingerprints.
+
+    ``table[r][k]`` is replica r's fingerprint (a tuple) of tensor k.  For each
+    tensor whose copies do not all agree, the most common fingerprint is a
+    strict majority only if it is held by more than half of the R copies; a
+    replica is a suspect when its copy differs from that majority.  Returns
+    (suspect, mask, summary):
+      suspect[k]: -1 all agree, r if exactly replica r differs, -2 if several
+                  differ from a majority, -3 if there is no strict majority;
+      mask[k]:    bit r set when replica r differs from the majority
+                  (0 when all agree or there is no majority);
+      summary:    diverged (any tensor differs), no_majority (some differing
+                  tensor lacks a strict majority), suspect_mask (union of the
+                  masks of tensors that have a majority).
+    """
+    R = len(table)
+    T = len(table[0]) if R else 0
+    suspect = [SUSPECT_AGREE] * T
+    mask = [0] * T
+    diverged = False
+    no_majority = False
+    union = 0
+    for k in range(T):
+        copies = [tuple(table[r][k]) for r in range(R)]
+        if all(c == copies[0] for c in copies):
+            continue
+        diverged = True
+        value, count = Counter(copies).most_common(1)[0]
+        if 2 * count <= R:
+            suspect[k] = SUSPECT_NO_MAJORITY
+            no_majority = True
+            continue
+        odd = [r for r, c in enumerate(copies) if c != value]
+        m = 0
+        for r in odd:
+            m |= 1 << r
+        mask[k] = m
+        suspect[k] = odd[0] if len(odd) == 1 else SUSPECT_SEVERAL
+        union |= m
+    return suspect, mask, {"diverged": int(diverged), "no_majority": int(no_majority),
+                           "suspect_mask": union}
+
+
+def pages_verdict(summary: dict) -> dict:
+    """The page's result dict from a vote summary.
+
+    No divergence -> {"diverged": False, "suspects": []}; any differing tensor
+    without a strict majority -> {"diverged": True, "suspects": None};
+    otherwise the sorted replicas that differ from a majority somewhere.
+    """
+    if not summary["diverged"]:
+        return {"diverged": False, "suspects": []}
+    if summary["no_majority"]:
+        return {"diverged": True, "suspects": None}
+    m = summary["suspect_mask"]
+    return {"diverged": True, "suspects": [r for r in range(64) if (m >> r) & 1]}
