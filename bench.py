@@ -1,0 +1,399 @@
+#!/usr/bin/env python3
+"""Benchmark of the replica-integrity scan (weight fingerprint check) on GB300.
+
+Metric: fingerprint-scan GB/s (and % of HBM peak, ms per pass) on the
+~1.04e9-parameter layout (24 layers, d=1792, ffn=7168, vocab=32000, untied
+embedding and head), float32 weights, 3 replicas resident in HBM.
+
+One step = one weight check: sdc_fingerprint over the 3 replicas (the
+persistent scan kernel plus its combine) and sdc_vote on the resulting
+[3, 195, 2] table.  Algorithmic bytes per step = every weight byte of every
+replica read once = 12,475,438,080 bytes; inputs are ~97x the 129 MB L2, so
+no flush is needed between steps.  The other hot-path rows (fused gradient
+average-scan on 4 bf16 buffers of the same layout, xorsum with pair compare)
+are timed in the same run and reported under "rows".
+
+Usage:
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 it is launched with torch.distributed.run, one rank per GPU; every
+rank checks its own 3 replicas (no collective on the data path: weak scaling),
+and rank 0 prints one JSON line with the whole-job throughput.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fingerprint-scan GB/s and % of GB300 HBM peak; ms/pass at ~1B params"
+WORKLOAD = "1b_fp32_3replicas"
+
+
+# ---------------------------------------------------------------- distributed helpers
+def dist_env() -> tuple[int, int, int]:
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """MAX of a float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def whole_job_rate(bytes_per_step_per_rank: int, world: int, ms_per_step_max: float) -> float:
+    """GB/s of the whole job: every rank's bytes over the slowest rank's time."""
+    return bytes_per_step_per_rank * world / (ms_per_step_max * 1e-3) / 1e9
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]), "active": parts[4],
+                             "hw": parts[5], "hwt": parts[6], "swt": parts[7], "pcap": parts[8]})
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for k, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                            ("pcap", "sw_power_cap")):
+                if r[k].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------- CPU baseline (the oracle)
+def cpu_baseline_sample(host_tensors, threads: int) -> dict:
+    """Time the oracle's fingerprint over host copies of a sample of the workload."""
+    import oracle
+    import numpy as np
+    arrays = [t.numpy().view(np.uint32) if t.dtype.itemsize == 4 else t.numpy() for t in host_tensors]
+    nbytes = sum(a.nbytes for a in arrays)
+    t0 = time.perf_counter()
+    for a in arrays:
+        oracle.fingerprint(a, threads=threads)
+    dt = time.perf_counter() - t0
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "seconds": dt, "bytes": nbytes}
+
+
+def run_reference(args) -> None:
+    """The reference arm: the CPU oracle on a bounded sample of the same workload."""
+    rank, world, local = dist_env()
+    if world > 1 and rank != 0:
+        return
+    import numpy as np
+    import torch
+    import sdc_workloads as W
+    import oracle
+    threads = os.cpu_count() or 1
+    # sample: the first tensors of one replica, up to ~1 GB of float32 weights, generated on the host
+    layout = W.layout_1b()
+    g = W.generator(1, "cpu")
+    sample, nbytes = [], 0
+    for _, shape in layout:
+        t = W.normal(shape, 0.02, torch.float32, g, "cpu")
+        sample.append(t.numpy().view(np.uint32))
+        nbytes += t.numel() * 4
+        if nbytes >= 1 << 30:
+            break
+    oracle.build()
+
+    def step():
+        for a in sample:
+            oracle.fingerprint(a, threads=threads)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = nbytes / dt / 1e9
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": f"{len(sample)} tensors of replica 0 ({nbytes} bytes) "
+                       "per step; the full step is 3 replicas x 195 tensors"},
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{nbytes} bytes of float32 weights per step"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args) -> None:
+    import numpy as np
+    import torch
+    import sdc_workloads as W
+    import silent_corruption_checksums_gb300 as sdc
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    peaks = measured_peaks()
+    stream = torch.cuda.current_stream()
+
+    # ---- workload: 3 float32 replicas of the 1b layout, one bit flipped
+    w = W.weights_1b(dev, seed=1 + rank)
+    reps = w["replicas"]
+    R, T = len(reps), len(reps[0])
+    bytes_per_step = sum(t.numel() * t.element_size() for ts in reps for t in ts)
+    plan = sdc.Plan(reps, chunk_bytes=args.chunk_bytes)
+    fp = torch.empty((R, T, 2), dtype=torch.int64, device=dev)
+    vote_out = (torch.empty(T, dtype=torch.int32, device=dev), torch.empty(T, dtype=torch.int64, device=dev),
+                torch.empty(sdc.VOTE_SUMMARY_DTYPE.itemsize, dtype=torch.uint8, device=dev))
+
+    def step():
+        plan.fingerprint(out=fp, stream=stream)
+        sdc.vote(fp, stream=stream, out=vote_out)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    # correctness of what is timed: the vote names the flipped replica
+    verdict = sdc.pages_verdict(sdc.decode_summary(vote_out[2]))
+    ok = verdict == {"diverged": True, "suspects": [w["truth"]["replica"]]}
+
+    # ---- timed region: K steps, events around each fingerprint call
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            plan.fingerprint(out=fp, stream=stream)
+            ev[i][1].record(stream)
+            sdc.vote(fp, stream=stream, out=vote_out)
+        stop.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    elapsed_ms = start.elapsed_time(stop)
+    ms_step = max_over_ranks(elapsed_ms / args.steps, world, dev)
+    fp_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    clocks = clk.summary()
+    value = whole_job_rate(bytes_per_step, world, ms_step)
+    achieved = bytes_per_step / (fp_ms * 1e-3) / 1e9
+    launches_per_step = (2 if plan.n_chunks else 1) + 1  # scan + combine, vote (+ a memset node)
+
+    rows = {}
+    e2e = None
+    cpu = None
+    if not args.quick:
+        rows = bench_rows(args, dev, stream, peaks, sdc, W, torch, np)
+        if rank == 0:
+            e2e = bench_e2e(args, reps, plan, fp, vote_out, stream, sdc, torch, bytes_per_step)
+            cpu = bench_cpu(reps, torch)
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+                "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "int64", "data": "synthetic",
+                "config": {"workload": WORKLOAD, "params_per_replica": W.layout_numel(W.layout_1b()),
+                           "replicas": R, "tensors": T, "weights": "float32 N(0,0.02), one seeded bit flip",
+                           "bytes_per_step": bytes_per_step, "chunk_bytes": plan_chunk_bytes(args),
+                           "grid": plan.grid, "block": plan.block, "n_chunks": plan.n_chunks,
+                           "l2": "inputs 12.5 GB per step >> 129 MB L2; no flush between steps",
+                           "vote_names_flipped_replica": ok},
+                "pct_hbm_peak": 100.0 * value / world / peaks["hbm_gbs"],
+                "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": achieved / peaks["hbm_gbs"], "traffic": args.traffic,
+                             "kernel": "fp_scan_kernel (+ fp_combine_kernel, timed together as sdc_fingerprint)",
+                             "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)"},
+                "kernel_ms": fp_ms, "gpu_launches": launches_per_step * args.steps,
+                "clocks": clocks, "rows": rows, "e2e": e2e, "cpu_baseline": cpu}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def plan_chunk_bytes(args) -> int:
+    return args.chunk_bytes or 16384
+
+
+def _time_loop(fn, steps, stream, torch):
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def bench_rows(args, dev, stream, peaks, sdc, W, torch, np) -> dict:
+    """The other rows of the hot path, each timed on its own workload."""
+    rows = {}
+    # fused gradient average-scan on 4 bf16 buffers of the 1b layout
+    g = W.grads_1b(dev, seed=3)
+    bufs = g["bufs"]
+    n = bufs[0].numel()
+    out = torch.empty_like(bufs[0])
+    need = sdc.sdc_grad_average_scan_workspace_size(n, 4, sdc.DTYPE_BF16)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+
+    def avg_step():
+        sdc.grad_average_scan(bufs, out=out, stream=stream, ws=ws)
+
+    ms = _time_loop(avg_step, max(5, args.steps // 10), stream, torch)
+    nbytes = 5 * n * 2
+    rows["grad_average_scan"] = {"workload": "4 x bf16 local grads of the 1b layout (N(0,1e-3), rate-1e-7 "
+                                 "NaN/Inf/2^70 in buffer 2)", "ms": ms, "bytes": nbytes,
+                                 "GB_s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"]}
+    # the same buffers as one plan: pre-average scan only
+    gplan = sdc.Plan([[b] for b in bufs])
+    stats = torch.empty((4, sdc.GRAD_STATS_DTYPE.itemsize), dtype=torch.uint8, device=dev)
+    ms = _time_loop(lambda: gplan.grad_scan(out=stats, stream=stream), max(5, args.steps // 10), stream, torch)
+    nbytes = 4 * n * 2
+    rows["grad_scan"] = {"workload": "4 x bf16 local grads of the 1b layout", "ms": ms, "bytes": nbytes,
+                         "GB_s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"]}
+    del gplan, g, bufs, out, ws
+    torch.cuda.empty_cache()
+    return rows
+
+
+def bench_e2e(args, reps, plan, fp, vote_out, stream, sdc, torch, bytes_per_step) -> dict:
+    """Same metric through the public API with the replicas in pinned host memory:
+    every step copies them to the device, checks them, and reads the verdict back."""
+    host = [[t.to("cpu").pin_memory() for t in ts] for ts in reps]
+    fp_host = torch.empty(fp.shape, dtype=fp.dtype).pin_memory()
+    sum_host = torch.empty(vote_out[2].shape, dtype=torch.uint8).pin_memory()
+    sus_host = torch.empty(vote_out[0].shape, dtype=torch.int32).pin_memory()
+
+    def e2e_step():
+        for hs, ds in zip(host, reps):
+            for h, d in zip(hs, ds):
+                d.copy_(h, non_blocking=True)
+        plan.fingerprint(out=fp, stream=stream)
+        sdc.vote(fp, stream=stream, out=vote_out)
+        fp_host.copy_(fp, non_blocking=True)
+        sus_host.copy_(vote_out[0], non_blocking=True)
+        sum_host.copy_(vote_out[2], non_blocking=True)
+
+    steps = max(3, min(10, args.steps // 50))
+    e2e_step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / steps
+    d2h = fp.numel() * 8 + vote_out[0].numel() * 4 + vote_out[2].numel()
+    del host
+    return {"value": bytes_per_step / dt / 1e9, "unit": "GB/s", "ms_per_step": dt * 1e3,
+            "h2d_bytes_per_step": bytes_per_step, "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+def bench_cpu(reps, torch) -> dict:
+    """The oracle on a bounded sample: the first ~2 GB of replica 0, all host cores."""
+    sample, nbytes = [], 0
+    for t in reps[0]:
+        sample.append(t.to("cpu"))
+        nbytes += t.numel() * t.element_size()
+        if nbytes >= 2 << 30:
+            break
+    threads = os.cpu_count() or 1
+    r = cpu_baseline_sample(sample, threads)
+    r["sample"] = f"{len(sample)} tensors of replica 0, {nbytes} bytes (of 12,475,438,080 per step)"
+    return r
+
+
+def main(argv=None) -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--chunk-bytes", type=int, default=0)
+    ap.add_argument("--quick", action="store_true", help="only the timed fingerprint step (no rows/e2e/cpu)")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="dram bytes per launch of the scan kernel from an ncu capture, if current")
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,248 @@
+/*
+ * sdc.h -- C ABI of libsdc, the replica-integrity scan for one GB300 GPU.
+ *
+ * The method comes from "Detecting and recovering from silent data corruption
+ * on Amazon SageMaker HyperPod" (AWS Machine Learning Blog; cited below as
+ * [AWS]) and, for the xorsum, from the review page "Safeguarding LLM Training
+ * at Scale: Online SDC Detection and Insights from 35 Million GPU Hours"
+ * (cited as [AEGIS]).  Data-parallel training keeps R copies ("replicas") of
+ * every weight tensor; after each optimizer step the copies must be identical
+ * bit for bit.  This library reduces every copy of every tensor to a small
+ * fingerprint, votes on the fingerprints, and scans gradient buffers for NaN,
+ * Inf and float32 overflow while computing their L2 norm.
+ *
+ * Conventions shared by every call:
+ *  - All data pointers named d_* point to device memory of the CURRENT device
+ *    (cudaGetDevice() when the call is made); the caller allocates and owns
+ *    them.  Host arrays are named host_* or documented as host arrays.
+ *  - Every compute call is asynchronous: it validates its arguments on the
+ *    host, enqueues its kernels on `stream` and returns; results appear in
+ *    device memory in stream order.  No call synchronises the device, and no
+ *    call allocates device memory except sdc_plan_create.
+ *  - `stream` is a cudaStream_t (same type; NULL = the legacy default stream).
+ *  - Errors are returned as sdc_status codes, checked before anything is
+ *    enqueued; nothing is enqueued when a call fails.  sdc_last_error()
+ *    returns a one-line detail for the calling thread's last failure.  No
+ *    kernel traps or asserts.
+ *  - Tensors are contiguous (the page fingerprints t.contiguous()) and their
+ *    element order is the flat row-major order.  Start addresses need only be
+ *    aligned to the element size.
+ *  - Replica-major layout: the fingerprint table of R replicas x T tensors is
+ *    uint64 out[R][T][2]; entry (r, k) describes replica r's copy of tensor k.
+ */
+#ifndef SDC_H
+#define SDC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so this header needs no CUDA header. */
+typedef struct CUstream_st *sdc_stream_t;
+
+typedef int sdc_status;
+enum {
+    SDC_OK = 0,
+    SDC_ERR_NULL = 1,              /* a required pointer argument is NULL */
+    SDC_ERR_BAD_ELEM_SIZE = 2,     /* element size not in {1, 2, 4, 8} or not matching dtype */
+    SDC_ERR_SHAPE_MISMATCH = 3,    /* replicas of one tensor differ in numel/elem_size/dtype */
+    SDC_ERR_TOO_MANY_REPLICAS = 4, /* R == 0 or R > SDC_MAX_REPLICAS, or too many buffers */
+    SDC_ERR_WS_TOO_SMALL = 5,      /* workspace smaller than the size query returned */
+    SDC_ERR_CUDA = 6,              /* a CUDA runtime call failed (see sdc_last_error) */
+    SDC_ERR_BAD_DTYPE = 7,         /* dtype code unknown, or not a float type where one is needed */
+    SDC_ERR_BAD_POINTER = 8,       /* not device memory of the current device, misaligned,
+                                      or [ptr, ptr + bytes) leaves its allocation */
+    SDC_ERR_BAD_ARG = 9,           /* any other invalid argument (sizes, options) */
+    SDC_ERR_WRONG_DEVICE = 10      /* plan used on a device other than the one it was built on */
+};
+
+#define SDC_MAX_REPLICAS 64
+
+/* dtype codes.  RAW: fingerprint/xorsum only (bits are bits).  The grad calls
+ * need a float dtype: F32 (elem_size 4), BF16 or F16 (elem_size 2). */
+enum { SDC_DTYPE_RAW = 0, SDC_DTYPE_F32 = 1, SDC_DTYPE_BF16 = 2, SDC_DTYPE_F16 = 3 };
+
+/* One tensor copy.  ptr: device address of element 0 (may be NULL only if
+ * numel == 0); numel: number of elements; elem_size: 1, 2, 4 or 8 bytes;
+ * dtype: one of SDC_DTYPE_*. */
+typedef struct {
+    const void *ptr;
+    uint64_t numel;
+    uint32_t elem_size;
+    uint32_t dtype;
+} sdc_tensor_desc;
+
+/* Plan options; a zero field takes its default.  chunk_bytes: bytes of one
+ * warp task, a power of two in [4096, 32768] (default 16384); ctas_per_sm:
+ * resident CTAs per SM of the persistent kernels (default: the occupancy
+ * limit); skip_pointer_checks: 1 skips the driver queries that check every
+ * descriptor's range lies inside one device allocation of this device. */
+typedef struct {
+    uint32_t chunk_bytes;
+    uint32_t ctas_per_sm;
+    uint32_t skip_pointer_checks;
+    uint32_t reserved;
+} sdc_plan_opts;
+
+/* Opaque plan: the validated descriptor table and its chunk table, resident
+ * in device memory.  Built once per parameter set -- training frameworks keep
+ * parameter storage fixed between steps. */
+typedef struct sdc_plan sdc_plan;
+
+/* Gradient statistics of one buffer (or one replica's tensors).
+ *  n_nan, n_inf: NaN and +-Inf elements;
+ *  n_big: finite elements whose exact square exceeds FLT_MAX (|x| > ~1.8e19);
+ *  n_elems: elements scanned;
+ *  sumsq_finite: sum of x^2 over finite elements, float64;
+ *  norm: sqrt(sumsq_finite), except NaN if any element is NaN, else +Inf if
+ *        any element is +-Inf (IEEE propagation, as clip_grad_norm_ reports);
+ *  nonfinite_fp32: 1 if the float32 squared norm would not be finite:
+ *        n_nan > 0 or n_inf > 0 or sumsq_finite > FLT_MAX -- [AWS] "Decide
+ *        what the alarm means": a norm above about 1.8e19 counts as non-finite. */
+typedef struct {
+    uint64_t n_nan;
+    uint64_t n_inf;
+    uint64_t n_big;
+    uint64_t n_elems;
+    double sumsq_finite;
+    double norm;
+    uint32_t nonfinite_fp32;
+    uint32_t reserved;
+} sdc_grad_stats;
+
+/* Vote summary.  diverged: some tensor's copies differ; no_majority: some
+ * differing tensor has no strict majority; suspect_mask: bit r set when
+ * replica r differs from a strict majority on some tensor that has one;
+ * n_differing / n_no_majority: tensor counts.  The page's result
+ * {"diverged", "suspects"} is: not diverged -> suspects = [];
+ * no_majority -> suspects = None; otherwise suspects = bits of suspect_mask. */
+typedef struct {
+    uint32_t diverged;
+    uint32_t no_majority;
+    uint64_t suspect_mask;
+    uint32_t n_differing;
+    uint32_t n_no_majority;
+} sdc_vote_summary;
+
+/* Per-tensor suspect codes written by sdc_vote. */
+#define SDC_SUSPECT_AGREE (-1)       /* every copy agrees */
+#define SDC_SUSPECT_SEVERAL (-2)     /* several copies differ from a strict majority (see mask) */
+#define SDC_SUSPECT_NO_MAJORITY (-3) /* copies differ and no value has a strict majority */
+
+/* ---------------------------------------------------------------- plan */
+
+/* Build a plan over R replicas x T tensors.  host_descs: host array of R*T
+ * descriptors in replica-major order (entry r*T + k is replica r's copy of
+ * tensor k); every replica's copy of tensor k must have the same numel,
+ * elem_size and dtype.  The descriptors are copied; the plan does not keep
+ * host_descs.  Allocates the plan's device tables on the current device.
+ * opts may be NULL.  On success *out receives the plan.
+ * [AWS] "Compare by fingerprint": the fingerprint function allocates one row
+ * of two int64 per tensor; "Check 3": every rank fingerprints every weight. */
+sdc_status sdc_plan_create(const sdc_tensor_desc *host_descs, uint32_t T, uint32_t R,
+                           const sdc_plan_opts *opts, sdc_plan **out);
+
+/* Free a plan and its device tables (synchronises nothing; the caller must
+ * not destroy a plan whose work is still queued).  NULL is accepted. */
+sdc_status sdc_plan_destroy(sdc_plan *plan);
+
+/* Bytes of device workspace the plan's compute calls need (0 for a plan with
+ * no elements).  Any 256-byte-aligned device buffer at least this large
+ * works; its contents need no initialisation. */
+size_t sdc_workspace_size(const sdc_plan *plan);
+
+/* Plan facts for reporting: chunk count, persistent grid and block size. */
+sdc_status sdc_plan_info(const sdc_plan *plan, uint64_t *n_chunks, uint32_t *grid, uint32_t *block);
+
+/* ---------------------------------------------------------------- fingerprint */
+
+/* Weight fingerprints.  [AWS] "Compare by fingerprint": each tensor is
+ * reduced to two 64-bit sums of its raw bit patterns, one plain and one
+ * weighted by position.  The element bits b_i are read through the integer
+ * type of the element width (unsigned 8-bit, or signed 16/32/64-bit) and
+ * widened to 64 bits (zero-extension for 1-byte, sign-extension otherwise):
+ *     S = sum_i b_i  mod 2^64,     W = sum_i (i + 1) * b_i  mod 2^64.
+ * d_out: device uint64[R][T][2], (S, W) of replica r's copy of tensor k at
+ * d_out[(r*T + k)*2 + {0, 1}]; the bits equal the page's int64 values.
+ * d_ws: device workspace of ws_bytes >= sdc_workspace_size(plan).
+ * Results are exact integers: identical on every run and any launch shape. */
+sdc_status sdc_fingerprint(const sdc_plan *plan, uint64_t *d_out, void *d_ws, size_t ws_bytes,
+                           sdc_stream_t stream);
+
+/* Xorsum fingerprints.  [AEGIS] method section 4: an original and a
+ * recomputed result are each reduced to an xorsum fingerprint; any differing
+ * bit is an anomaly.  Read here as the XOR over elements of each element's
+ * raw bits zero-extended to 64 bits.  d_out: device uint64[R][T]. */
+sdc_status sdc_xorsum(const sdc_plan *plan, uint64_t *d_out, void *d_ws, size_t ws_bytes,
+                      sdc_stream_t stream);
+
+/* Compare two xorsum vectors of n entries: d_mismatch[p] = (d_a[p] != d_b[p]),
+ * d_diff[p] = d_a[p] ^ d_b[p].  d_mismatch: device uint8[n]; d_diff: device
+ * uint64[n] (may be NULL).  n == 0 is a no-op. */
+sdc_status sdc_xorsum_compare(const uint64_t *d_a, const uint64_t *d_b, uint32_t n,
+                              uint8_t *d_mismatch, uint64_t *d_diff, sdc_stream_t stream);
+
+/* ---------------------------------------------------------------- vote */
+
+/* Strict-majority vote over a fingerprint table.  [AWS] "Check 3: Weight
+ * fingerprints, after the optimizer step": a copy is named only when it
+ * differs from a strict majority (more than half of the copies); with two
+ * copies, or a split with no strict majority, a disagreement is reported
+ * without naming anyone.  d_fp: device uint64[R][T][2] (as sdc_fingerprint
+ * writes it); 1 <= R <= SDC_MAX_REPLICAS.  Outputs: d_suspect: device
+ * int32[T] (SDC_SUSPECT_* or the one replica that differs); d_mask: device
+ * uint64[T], bit r set when replica r differs from the majority (0 when all
+ * agree or no majority exists); d_summary: device sdc_vote_summary. */
+sdc_status sdc_vote(const uint64_t *d_fp, uint32_t R, uint32_t T, int32_t *d_suspect, uint64_t *d_mask,
+                    sdc_vote_summary *d_summary, sdc_stream_t stream);
+
+/* ---------------------------------------------------------------- gradients */
+
+/* Non-finite scan and squared norm of each replica's gradient tensors.
+ * [AWS] "Check 1: NaN/Inf gradients, before and after the all-reduce": each
+ * rank's local gradient is checked for NaN/Inf before the all-reduce.  Here
+ * replica r of the plan is one local gradient made of T tensors; every
+ * descriptor must have a float dtype.  d_stats: device sdc_grad_stats[R].
+ * Counts are exact; sumsq_finite is within 2e-11 relative of the exact sum
+ * and identical on every run (fixed reduction order). */
+sdc_status sdc_grad_scan(const sdc_plan *plan, sdc_grad_stats *d_stats, void *d_ws, size_t ws_bytes,
+                         sdc_stream_t stream);
+
+/* Workspace bytes for sdc_grad_average_scan with these sizes. */
+size_t sdc_grad_average_scan_workspace_size(uint64_t numel, uint32_t n_bufs, uint32_t dtype);
+
+/* One fused pass: scan n_bufs local gradient buffers, write their average,
+ * and scan the average -- the one-device stand-in for the page's check 1
+ * around the all-reduce ([AWS] "Step 1: Detect": the all-reduce averages the
+ * replicas' gradients; "Check 1": check each local gradient before it and the
+ * reduced gradient after it, whose norm clip_grad_norm_ already computes).
+ * bufs: HOST array of n_bufs (1..8) device pointers, each to numel elements
+ * of `dtype` (F32, BF16 or F16); d_avg: device output of numel elements of
+ * the same dtype (must not overlap the inputs).  Average, per element: the
+ * float32 sum of the inputs in buffer order, divided by n_bufs in float32
+ * (correctly rounded), rounded to dtype ties-to-even; every NaN result is the
+ * canonical quiet NaN (0x7FC0 bf16, 0x7E00 f16, 0x7FC00000 f32).
+ * d_pre: device sdc_grad_stats[n_bufs] of the inputs; d_post: device
+ * sdc_grad_stats of the average (its `norm` is the global L2 norm and
+ * its nonfinite_fp32 is the reduced-gradient alarm).  Pointers aligned to 16
+ * bytes take the vector path; others take a slower element path. */
+sdc_status sdc_grad_average_scan(const void *const *bufs, uint32_t n_bufs, void *d_avg, uint64_t numel,
+                                 uint32_t dtype, sdc_grad_stats *d_pre, sdc_grad_stats *d_post,
+                                 void *d_ws, size_t ws_bytes, sdc_stream_t stream);
+
+/* ---------------------------------------------------------------- errors */
+
+/* Static name of a status code. */
+const char *sdc_status_string(sdc_status status);
+
+/* Detail of the calling thread's most recent failed call ("" if none). */
+const char *sdc_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDC_H */

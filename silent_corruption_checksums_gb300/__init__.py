@@ -1,0 +1,367 @@
+"""Replica-integrity scan for one GB300 GPU: thin Python binding of libsdc.
+
+The compute lives in the CUDA kernels of libsdc.so (see include/sdc.h for the
+C ABI).  This module only marshals arguments: the ``sdc_*`` functions mirror
+the C entry points one to one (integer device addresses, sizes, a stream
+handle), and ``Plan`` / ``vote`` / ``grad_average_scan`` wrap them for
+torch tensors.  There is no fallback: when the library has not been built
+(``python -m silent_corruption_checksums_gb300.build``) every call raises
+ImportError.
+
+Method: "Detecting and recovering from silent data corruption on Amazon
+SageMaker HyperPod" (weight fingerprints, strict-majority vote, non-finite
+gradient checks) and the review page "Safeguarding LLM Training at Scale ..."
+(xorsum fingerprint of a recomputed result).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from .build import LIB_PATH
+
+__all__ = [
+    "SdcError", "DTYPE_RAW", "DTYPE_F32", "DTYPE_BF16", "DTYPE_F16", "MAX_REPLICAS",
+    "SUSPECT_AGREE", "SUSPECT_SEVERAL", "SUSPECT_NO_MAJORITY", "GRAD_STATS_DTYPE", "VOTE_SUMMARY_DTYPE",
+    "sdc_plan_create", "sdc_plan_destroy", "sdc_workspace_size", "sdc_plan_info", "sdc_fingerprint",
+    "sdc_xorsum", "sdc_xorsum_compare", "sdc_vote", "sdc_grad_scan", "sdc_grad_average_scan_workspace_size",
+    "sdc_grad_average_scan", "sdc_status_string", "sdc_last_error", "Plan", "vote", "xorsum_compare",
+    "grad_average_scan", "decode_stats", "decode_summary", "pages_verdict", "library_path",
+]
+
+DTYPE_RAW, DTYPE_F32, DTYPE_BF16, DTYPE_F16 = 0, 1, 2, 3
+MAX_REPLICAS = 64
+SUSPECT_AGREE, SUSPECT_SEVERAL, SUSPECT_NO_MAJORITY = -1, -2, -3
+
+# Mirrors of the C structs (include/sdc.h).
+DESC_DTYPE = np.dtype([("ptr", "<u8"), ("numel", "<u8"), ("elem_size", "<u4"), ("dtype", "<u4")])
+GRAD_STATS_DTYPE = np.dtype([("n_nan", "<u8"), ("n_inf", "<u8"), ("n_big", "<u8"), ("n_elems", "<u8"),
+                             ("sumsq_finite", "<f8"), ("norm", "<f8"), ("nonfinite_fp32", "<u4"),
+                             ("reserved", "<u4")])
+VOTE_SUMMARY_DTYPE = np.dtype([("diverged", "<u4"), ("no_majority", "<u4"), ("suspect_mask", "<u8"),
+                               ("n_differing", "<u4"), ("n_no_majority", "<u4")])
+assert DESC_DTYPE.itemsize == 24 and GRAD_STATS_DTYPE.itemsize == 56 and VOTE_SUMMARY_DTYPE.itemsize == 24
+
+
+class SdcError(RuntimeError):
+    """A libsdc call returned a non-zero status."""
+
+    def __init__(self, fn: str, status: int, detail: str):
+        super().__init__(f"{fn}: {sdc_status_string(status)} ({status}): {detail}")
+        self.status = status
+
+
+class _PlanOpts(ctypes.Structure):
+    _fields_ = [("chunk_bytes", ctypes.c_uint32), ("ctas_per_sm", ctypes.c_uint32),
+                ("skip_pointer_checks", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libsdc.so not found at {LIB_PATH}; build it with "
+                          "`python -m silent_corruption_checksums_gb300.build` (needs nvcc)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, u64, u32, sz = ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_size_t
+    sig = {
+        "sdc_plan_create": ([vp, u32, u32, ctypes.POINTER(_PlanOpts), ctypes.POINTER(vp)], ctypes.c_int),
+        "sdc_plan_destroy": ([vp], ctypes.c_int),
+        "sdc_workspace_size": ([vp], sz),
+        "sdc_plan_info": ([vp, ctypes.POINTER(u64), ctypes.POINTER(u32), ctypes.POINTER(u32)], ctypes.c_int),
+        "sdc_fingerprint": ([vp, vp, vp, sz, vp], ctypes.c_int),
+        "sdc_xorsum": ([vp, vp, vp, sz, vp], ctypes.c_int),
+        "sdc_xorsum_compare": ([vp, vp, u32, vp, vp, vp], ctypes.c_int),
+        "sdc_vote": ([vp, u32, u32, vp, vp, vp, vp], ctypes.c_int),
+        "sdc_grad_scan": ([vp, vp, vp, sz, vp], ctypes.c_int),
+        "sdc_grad_average_scan_workspace_size": ([u64, u32, u32], sz),
+        "sdc_grad_average_scan": ([ctypes.POINTER(vp), u32, vp, u64, u32, vp, vp, vp, sz, vp], ctypes.c_int),
+        "sdc_status_string": ([ctypes.c_int], ctypes.c_char_p),
+        "sdc_last_error": ([], ctypes.c_char_p),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    return lib
+
+
+class _Missing:
+    """Stands in for the library when it is not built: every call raises."""
+
+    def __init__(self, err: Exception):
+        self.err = err
+
+    def __getattr__(self, name):
+        raise ImportError(str(self.err))
+
+
+try:
+    _lib = _load()
+except ImportError as _err:  # the build module must stay importable to create the library
+    _lib = _Missing(_err)
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def sdc_status_string(status: int) -> str:
+    return _lib.sdc_status_string(status).decode()
+
+
+def sdc_last_error() -> str:
+    return _lib.sdc_last_error().decode()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise SdcError(fn, status, sdc_last_error())
+
+
+# ---------------------------------------------------------------- C-ABI mirrors
+def sdc_plan_create(descs: np.ndarray, T: int, R: int, chunk_bytes: int = 0, ctas_per_sm: int = 0,
+                    skip_pointer_checks: bool = False) -> int:
+    """descs: numpy array of DESC_DTYPE (R*T entries, replica-major). Returns the plan handle."""
+    descs = np.ascontiguousarray(descs, dtype=DESC_DTYPE)
+    opts = _PlanOpts(chunk_bytes, ctas_per_sm, 1 if skip_pointer_checks else 0, 0)
+    out = ctypes.c_void_p()
+    _check("sdc_plan_create", _lib.sdc_plan_create(descs.ctypes.data if descs.size else None, T, R,
+                                                   ctypes.byref(opts), ctypes.byref(out)))
+    return out.value
+
+
+def sdc_plan_destroy(plan: int) -> None:
+    _check("sdc_plan_destroy", _lib.sdc_plan_destroy(plan))
+
+
+def sdc_workspace_size(plan: int) -> int:
+    return int(_lib.sdc_workspace_size(plan))
+
+
+def sdc_plan_info(plan: int) -> tuple[int, int, int]:
+    n, g, b = ctypes.c_uint64(), ctypes.c_uint32(), ctypes.c_uint32()
+    _check("sdc_plan_info", _lib.sdc_plan_info(plan, ctypes.byref(n), ctypes.byref(g), ctypes.byref(b)))
+    return n.value, g.value, b.value
+
+
+def sdc_fingerprint(plan: int, d_out: int, d_ws: int, ws_bytes: int, stream: int) -> None:
+    _check("sdc_fingerprint", _lib.sdc_fingerprint(plan, d_out, d_ws, ws_bytes, stream))
+
+
+def sdc_xorsum(plan: int, d_out: int, d_ws: int, ws_bytes: int, stream: int) -> None:
+    _check("sdc_xorsum", _lib.sdc_xorsum(plan, d_out, d_ws, ws_bytes, stream))
+
+
+def sdc_xorsum_compare(d_a: int, d_b: int, n: int, d_mismatch: int, d_diff: int, stream: int) -> None:
+    _check("sdc_xorsum_compare", _lib.sdc_xorsum_compare(d_a, d_b, n, d_mismatch, d_diff, stream))
+
+
+def sdc_vote(d_fp: int, R: int, T: int, d_suspect: int, d_mask: int, d_summary: int, stream: int) -> None:
+    _check("sdc_vote", _lib.sdc_vote(d_fp, R, T, d_suspect, d_mask, d_summary, stream))
+
+
+def sdc_grad_scan(plan: int, d_stats: int, d_ws: int, ws_bytes: int, stream: int) -> None:
+    _check("sdc_grad_scan", _lib.sdc_grad_scan(plan, d_stats, d_ws, ws_bytes, stream))
+
+
+def sdc_grad_average_scan_workspace_size(numel: int, n_bufs: int, dtype: int) -> int:
+    return int(_lib.sdc_grad_average_scan_workspace_size(numel, n_bufs, dtype))
+
+
+def sdc_grad_average_scan(bufs: list[int], d_avg: int, numel: int, dtype: int, d_pre: int, d_post: int,
+                          d_ws: int, ws_bytes: int, stream: int) -> None:
+    arr = (ctypes.c_void_p * max(1, len(bufs)))(*bufs)
+    _check("sdc_grad_average_scan", _lib.sdc_grad_average_scan(arr, len(bufs), d_avg, numel, dtype, d_pre,
+                                                               d_post, d_ws, ws_bytes, stream))
+
+
+# ---------------------------------------------------------------- torch conveniences
+def _torch():
+    import torch
+    return torch
+
+
+def dtype_code(t) -> int:
+    torch = _torch()
+    return {torch.float32: DTYPE_F32, torch.bfloat16: DTYPE_BF16, torch.float16: DTYPE_F16}.get(t.dtype, DTYPE_RAW)
+
+
+def _stream_handle(stream) -> int:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _ws(nbytes: int, device):
+    torch = _torch()
+    if nbytes == 0:
+        return None
+    # torch's caching allocator returns blocks aligned to at least 512 bytes
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+class Plan:
+    """A plan over R replicas x T tensors held as torch CUDA tensors.
+
+    ``replicas[r][k]`` is replica r's copy of tensor k; tensors must be
+    contiguous and stay allocated while the plan is used.  The plan's device
+    tables and a workspace (from torch's allocator) are created once.
+    """
+
+    def __init__(self, replicas, chunk_bytes: int = 0, ctas_per_sm: int = 0, skip_pointer_checks: bool = False,
+                 dtypes: list[int] | None = None):
+        torch = _torch()
+        self.R = len(replicas)
+        self.T = len(replicas[0]) if self.R else 0
+        descs = np.zeros(self.R * self.T, dtype=DESC_DTYPE)
+        dev = None
+        for r, ts in enumerate(replicas):
+            if len(ts) != self.T:
+                raise ValueError("every replica needs the same number of tensors")
+            for k, t in enumerate(ts):
+                if not t.is_contiguous():
+                    raise ValueError("tensors must be contiguous")
+                if t.numel() and not t.is_cuda:
+                    raise ValueError("tensors must be CUDA tensors")
+                dev = t.device if t.is_cuda else dev
+                i = r * self.T + k
+                descs[i] = (t.data_ptr() if t.numel() else 0, t.numel(), t.element_size(),
+                            dtypes[k] if dtypes is not None else dtype_code(t))
+        self.device = dev if dev is not None else torch.device("cuda", torch.cuda.current_device())
+        self._keep = replicas
+        with torch.cuda.device(self.device):
+            self.handle = sdc_plan_create(descs, self.T, self.R, chunk_bytes, ctas_per_sm, skip_pointer_checks)
+            self.ws_bytes = sdc_workspace_size(self.handle)
+            self.ws = _ws(self.ws_bytes, self.device)
+        self.n_chunks, self.grid, self.block = sdc_plan_info(self.handle)
+
+    @classmethod
+    def from_descs(cls, descs: np.ndarray, T: int, R: int, device, keep=None, **kw) -> "Plan":
+        """Plan over raw descriptors (device addresses); ``keep`` holds the owning tensors."""
+        self = cls.__new__(cls)
+        self.R, self.T = R, T
+        self.device = device
+        self._keep = keep
+        torch = _torch()
+        with torch.cuda.device(device):
+            self.handle = sdc_plan_create(descs, T, R, **kw)
+            self.ws_bytes = sdc_workspace_size(self.handle)
+            self.ws = _ws(self.ws_bytes, device)
+        self.n_chunks, self.grid, self.block = sdc_plan_info(self.handle)
+        return self
+
+    def _ws_ptr(self) -> int:
+        return self.ws.data_ptr() if self.ws is not None else 0
+
+    def fingerprint(self, out=None, stream=None):
+        """(S, W) per replica and tensor: int64 tensor [R, T, 2] holding the uint64 bits."""
+        torch = _torch()
+        if out is None:
+            out = torch.empty((self.R, self.T, 2), dtype=torch.int64, device=self.device)
+        sdc_fingerprint(self.handle, out.data_ptr(), self._ws_ptr(), self.ws_bytes, _stream_handle(stream))
+        return out
+
+    def xorsum(self, out=None, stream=None):
+        """Xorsum per replica and tensor: int64 tensor [R, T] holding the uint64 bits."""
+        torch = _torch()
+        if out is None:
+            out = torch.empty((self.R, self.T), dtype=torch.int64, device=self.device)
+        sdc_xorsum(self.handle, out.data_ptr(), self._ws_ptr(), self.ws_bytes, _stream_handle(stream))
+        return out
+
+    def grad_scan(self, out=None, stream=None):
+        """Gradient statistics per replica: uint8 tensor [R, 56] (decode with decode_stats)."""
+        torch = _torch()
+        if out is None:
+            out = torch.empty((self.R, GRAD_STATS_DTYPE.itemsize), dtype=torch.uint8, device=self.device)
+        sdc_grad_scan(self.handle, out.data_ptr(), self._ws_ptr(), self.ws_bytes, _stream_handle(stream))
+        return out
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            sdc_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def vote(fp, stream=None, out=None):
+    """Strict-majority vote over an [R, T, 2] fingerprint tensor.
+
+    Returns (suspect int32 [T], mask int64 [T], summary uint8 [24]).
+    """
+    torch = _torch()
+    R, T = int(fp.shape[0]), int(fp.shape[1])
+    if out is None:
+        suspect = torch.empty(T, dtype=torch.int32, device=fp.device)
+        mask = torch.empty(T, dtype=torch.int64, device=fp.device)
+        summary = torch.empty(VOTE_SUMMARY_DTYPE.itemsize, dtype=torch.uint8, device=fp.device)
+    else:
+        suspect, mask, summary = out
+    sdc_vote(fp.data_ptr(), R, T, suspect.data_ptr() if T else 0, mask.data_ptr() if T else 0,
+             summary.data_ptr(), _stream_handle(stream))
+    return suspect, mask, summary
+
+
+def xorsum_compare(a, b, stream=None):
+    """Element-wise compare of two xorsum vectors: (mismatch uint8 [n], diff int64 [n])."""
+    torch = _torch()
+    n = int(a.numel())
+    mism = torch.empty(n, dtype=torch.uint8, device=a.device)
+    diff = torch.empty(n, dtype=torch.int64, device=a.device)
+    sdc_xorsum_compare(a.data_ptr(), b.data_ptr(), n, mism.data_ptr() if n else 0, diff.data_ptr() if n else 0,
+                       _stream_handle(stream))
+    return mism, diff
+
+
+def grad_average_scan(bufs, out=None, stream=None, ws=None):
+    """Fused scan of the local gradients, their average, and the scan of the average.
+
+    Returns (avg tensor, pre stats uint8 [n_bufs, 56], post stats uint8 [56]).
+    """
+    torch = _torch()
+    numel = int(bufs[0].numel())
+    code = dtype_code(bufs[0])
+    dev = bufs[0].device
+    if out is None:
+        out = torch.empty_like(bufs[0])
+    pre = torch.empty((len(bufs), GRAD_STATS_DTYPE.itemsize), dtype=torch.uint8, device=dev)
+    post = torch.empty(GRAD_STATS_DTYPE.itemsize, dtype=torch.uint8, device=dev)
+    need = sdc_grad_average_scan_workspace_size(numel, len(bufs), code)
+    if ws is None or ws.numel() < need:
+        ws = _ws(need, dev)
+    sdc_grad_average_scan([b.data_ptr() for b in bufs], out.data_ptr(), numel, code, pre.data_ptr(),
+                          post.data_ptr(), ws.data_ptr() if ws is not None else 0, need, _stream_handle(stream))
+    return out, pre, post
+
+
+# ---------------------------------------------------------------- host-side decoding
+def decode_stats(raw) -> list[dict]:
+    """Decode sdc_grad_stats records (bytes, numpy or a CPU/GPU uint8 tensor) into dicts."""
+    if hasattr(raw, "cpu"):
+        raw = raw.cpu().numpy()
+    arr = np.frombuffer(np.ascontiguousarray(raw).tobytes(), dtype=GRAD_STATS_DTYPE)
+    return [{k: (float(rec[k]) if k in ("sumsq_finite", "norm") else int(rec[k]))
+             for k in GRAD_STATS_DTYPE.names if k != "reserved"} for rec in arr]
+
+
+def decode_summary(raw) -> dict:
+    if hasattr(raw, "cpu"):
+        raw = raw.cpu().numpy()
+    rec = np.frombuffer(np.ascontiguousarray(raw).tobytes(), dtype=VOTE_SUMMARY_DTYPE)[0]
+    return {k: int(rec[k]) for k in VOTE_SUMMARY_DTYPE.names}
+
+
+def pages_verdict(summary: dict) -> dict:
+    """The page's result dict {"diverged", "suspects"} from a decoded summary."""
+    if not summary["diverged"]:
+        return {"diverged": False, "suspects": []}
+    if summary["no_majority"]:
+        return {"diverged": True, "suspects": None}
+    m = summary["suspect_mask"]
+    return {"diverged": True, "suspects": [r for r in range(MAX_REPLICAS) if (m >> r) & 1]}

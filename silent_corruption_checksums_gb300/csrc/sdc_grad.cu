@@ -1,0 +1,648 @@
+// sdc_grad.cu -- non-finite gradient scan with the squared L2 norm, and the
+// fused average-and-scan pass.
+//
+// Method: "Detecting and recovering from silent data corruption on Amazon
+// SageMaker HyperPod", "Check 1: NaN/Inf gradients, before and after the
+// all-reduce" (a rank is flagged when its local gradient norm is NaN or Inf,
+// and the reduced gradient is checked before the update) and "Decide what the
+// alarm means" (a float32 norm above about 1.8e19 counts as non-finite).
+//
+// Per element: NaN / Inf / finite; a finite x is "big" when x^2 > FLT_MAX.
+// The squared norm sums x^2 over finite elements in float64 precision.
+//
+// Why not a float64 add per element: this part's FP64 rate is a small
+// fraction of its FP32 rate, far below what a bf16 stream at HBM speed needs.
+// Instead each lane accumulates x^2 in float32 with an error-free TwoSum
+// (Knuth) on packed f32x2 pairs: (s, c) with s + c = sum exactly up to the
+// rounding of c.  The error of such a sum of n terms is below
+// gamma_{n-1}^2 * sum, gamma_k = k u / (1 - k u), u = 2^-24 (Ogita, Rump and
+// Oishi, "Accurate sum and dot product", 2005); with n = 64 terms per lane
+// half between flushes that is 1.4e-11 relative.  Every 16 vectors the pair
+// is flushed into a float64 accumulator.
+//
+// Exactness of the float32 squares:
+//  - bf16: x is scaled by 2^59 before squaring, so every bf16 square -- down
+//    to the smallest subnormal, (2^-133)^2 -- lands on a multiple of 2^-149
+//    and is exact; the flushed sums are scaled back by 2^-118 in float64.
+//    Values with |x| >= 32 overflow the scaled square to Inf.
+//  - f16: squares of f16 values (22 significant bits, >= 2^-48) are exact.
+//  - f32: x^2 = p + e exactly with p = fl(x*x), e = fma(x, x, -p), provided
+//    the biased exponent of x is >= 76 (or x == 0); smaller values are caught
+//    by a running minimum of the lane's magnitudes.
+// A run whose float32 sum is not finite (NaN, Inf, big, |bf16| >= 32, or an
+// overflowing sum) or that holds a tiny f32 value is redone exactly: each
+// element classified and its square added in float64 (exact squares).
+// All reductions have a fixed shape, so results are identical on every run.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "sdc_internal.cuh"
+
+namespace sdc {
+
+namespace {
+
+constexpr int kRunVec = 16;           // vectors per lane between flushes
+constexpr double kFltMax = 3.4028234663852886e38;
+constexpr float kBf16Scale = 0x1p59f;   // 2^59
+constexpr double kBf16Unscale = 0x1p-118;
+constexpr uint32_t kF32TinyLimit = (76u << 24) - 2u;  // (bits << 1) - 2 below this: tiny, non-zero
+
+// ---------------------------------------------------------------- exact element path
+__device__ __forceinline__ float to_float(uint32_t bits, uint32_t dt) {
+    if (dt == SDC_DTYPE_F32) return __uint_as_float(bits);
+    if (dt == SDC_DTYPE_BF16) return __uint_as_float(bits << 16);
+    return __half2float(__ushort_as_half((unsigned short)bits));
+}
+
+struct Counts {
+    uint32_t nan = 0, inf = 0, big = 0;
+};
+
+__device__ __forceinline__ void exact_elem(uint32_t bits, uint32_t dt, double &acc, Counts &n) {
+    const float f = to_float(bits, dt);
+    if (isnan(f)) {
+        n.nan++;
+    } else if (isinf(f)) {
+        n.inf++;
+    } else {
+        const double x = f;
+        const double x2 = __dmul_rn(x, x);  // exact: <= 48 significant bits
+        if (x2 > kFltMax) n.big++;
+        acc = __dadd_rn(acc, x2);
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ void exact_vec(const uint4 &v, double &acc, Counts &n) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        if (DT == SDC_DTYPE_F32) {
+            exact_elem(w[k], DT, acc, n);
+        } else {
+            exact_elem(w[k] & 0xFFFFu, DT, acc, n);
+            exact_elem(w[k] >> 16, DT, acc, n);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- fast path
+struct FastAcc {
+    uint64_t s = 0, c = 0;  // packed f32x2 sum and compensation
+    uint32_t tmin = 0xFFFFFFFFu;
+};
+
+template <int DT>
+__device__ __forceinline__ void fast_vec(const uint4 &v, FastAcc &a) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if (DT == SDC_DTYPE_BF16) {
+        const uint64_t k = f2_pack(kBf16Scale, kBf16Scale);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint64_t p = f2_pack_bits(w[j] << 16, w[j] & 0xFFFF0000u);
+            p = f2_mul(p, k);
+            f2_two_sum_acc(a.s, a.c, f2_mul(p, p));
+        }
+    } else if (DT == SDC_DTYPE_F16) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float lo = __half2float(__ushort_as_half((unsigned short)(w[j] & 0xFFFFu)));
+            const float hi = __half2float(__ushort_as_half((unsigned short)(w[j] >> 16)));
+            const uint64_t p = f2_pack(lo, hi);
+            f2_two_sum_acc(a.s, a.c, f2_mul(p, p));
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; j += 2) {
+            const uint64_t p = f2_pack_bits(w[j], w[j + 1]);
+            const uint64_t sq = f2_mul(p, p);
+            const uint64_t e = f2_fma(p, p, sq ^ 0x8000000080000000ull);  // x*x - fl(x*x), exact
+            f2_two_sum_acc(a.s, a.c, sq);
+            a.c = f2_add(a.c, e);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) a.tmin = min(a.tmin, w[j] * 2u - 2u);
+    }
+}
+
+// Flush a run's (s, c) into the scaled float64 accumulator.  Returns false
+// when the run must be redone exactly.
+template <int DT>
+__device__ __forceinline__ bool fast_flush(FastAcc &a, double &acc_scaled) {
+    float sx, sy, cx, cy;
+    f2_unpack(a.s, sx, sy);
+    f2_unpack(a.c, cx, cy);
+    bool ok = isfinite(sx) && isfinite(sy);
+    if (DT == SDC_DTYPE_F32) ok = ok && a.tmin >= kF32TinyLimit;
+    if (ok) {
+        // error-free merge of the two lanes, then two float64 adds
+        const float t = sx + sy;
+        const float bb = t - sx;
+        const float e = (sx - (t - bb)) + (sy - bb);
+        const float cc = (cx + cy) + e;
+        acc_scaled = __dadd_rn(acc_scaled, (double)t);
+        acc_scaled = __dadd_rn(acc_scaled, (double)cc);
+    }
+    a.s = 0;
+    a.c = 0;
+    a.tmin = 0xFFFFFFFFu;
+    return ok;
+}
+
+template <int DT>
+__device__ __forceinline__ double unscale(double acc_scaled) {
+    return DT == SDC_DTYPE_BF16 ? acc_scaled * kBf16Unscale : acc_scaled;
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t elems_per_vec() {
+    return DT == SDC_DTYPE_F32 ? 4u : 8u;
+}
+
+// ---------------------------------------------------------------- plan-based scan
+// Chunk geometry (mirrors the fingerprint pass).
+struct GGeom {
+    uint64_t addr;
+    uint32_t head, nvec, tail, l2;
+};
+__device__ __forceinline__ GGeom ggeom(const Chunk &ch) {
+    GGeom g;
+    g.addr = ch.addr;
+    g.l2 = chunk_log2es(ch.tag);
+    uint32_t head = (uint32_t)((16u - (uint32_t)(ch.addr & 15u)) & 15u);
+    if (head > ch.nbytes) head = ch.nbytes;
+    g.head = head;
+    g.nvec = (ch.nbytes - head) >> 4;
+    g.tail = ch.nbytes - head - (g.nvec << 4);
+    return g;
+}
+
+template <int DT, int U>
+__device__ __forceinline__ double grad_chunk(const GGeom &g, uint32_t lane, Counts &n) {
+    const uint4 *vb = (const uint4 *)(g.addr + g.head);
+    const uint32_t niter = (g.nvec + 31) >> 5;
+    double acc_scaled = 0.0, acc_exact = 0.0;
+    for (uint32_t r0 = 0; r0 < niter; r0 += kRunVec) {
+        const uint32_t r1 = min(r0 + (uint32_t)kRunVec, niter);
+        FastAcc a;
+        for (uint32_t i0 = r0; i0 < r1; i0 += U) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const uint32_t vi = lane + ((i0 + u) << 5);
+                v[u] = (i0 + u < r1 && vi < g.nvec) ? ld_stream(vb + vi) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) fast_vec<DT>(v[u], a);
+        }
+        if (!fast_flush<DT>(a, acc_scaled)) {
+            for (uint32_t i = r0; i < r1; ++i) {
+                const uint32_t vi = lane + (i << 5);
+                if (vi < g.nvec) exact_vec<DT>(vb[vi], acc_exact, n);
+            }
+        }
+    }
+    // head and tail elements (fewer than 8 of each), exactly
+    const uint32_t he = g.head >> g.l2, te = g.tail >> g.l2;
+    if (lane < he) {
+        const uint64_t a = g.addr + ((uint64_t)lane << g.l2);
+        const uint32_t bits = g.l2 == 2 ? *(const uint32_t *)a : (uint32_t)(*(const uint16_t *)a);
+        exact_elem(bits, DT, acc_exact, n);
+    } else if (lane >= 16 && lane - 16 < te) {
+        const uint64_t a = g.addr + g.head + ((uint64_t)g.nvec << 4) + ((uint64_t)(lane - 16) << g.l2);
+        const uint32_t bits = g.l2 == 2 ? *(const uint32_t *)a : (uint32_t)(*(const uint16_t *)a);
+        exact_elem(bits, DT, acc_exact, n);
+    }
+    return __dadd_rn(unscale<DT>(acc_scaled), acc_exact);
+}
+
+template <int U>
+__global__ void __launch_bounds__(kScanBlock) grad_scan_kernel(const Chunk *__restrict__ chunks, uint64_t n_chunks,
+                                                               StatPartial *__restrict__ partials) {
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint64_t warp = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint64_t nwarps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
+    for (uint64_t c = warp; c < n_chunks; c += nwarps) {
+        const Chunk ch = chunks[c];
+        const GGeom g = ggeom(ch);
+        Counts n;
+        double acc;
+        switch (chunk_dtype(ch.tag)) {
+            case SDC_DTYPE_F32: acc = grad_chunk<SDC_DTYPE_F32, U>(g, lane, n); break;
+            case SDC_DTYPE_BF16: acc = grad_chunk<SDC_DTYPE_BF16, U>(g, lane, n); break;
+            default: acc = grad_chunk<SDC_DTYPE_F16, U>(g, lane, n); break;
+        }
+        acc = warp_sum_f64(acc);
+        const uint32_t nn = warp_sum_u32(n.nan), ni = warp_sum_u32(n.inf), nb = warp_sum_u32(n.big);
+        if (lane == 0) partials[c] = StatPartial{acc, nn, ni, nb, 0u};
+    }
+}
+
+// ---------------------------------------------------------------- fused average + scan
+struct BufPtrs {
+    const void *p[8];
+};
+
+// Average of NB words (one per input) holding 2 bf16/f16 or 1 f32 element(s)
+// in each half-word/word lane; returns the output word.
+template <int DT, int NB>
+__device__ __forceinline__ uint32_t avg_word_pair16(const uint32_t (&w)[NB], float inv) {
+    float lo, hi;
+    if (DT == SDC_DTYPE_BF16) {
+        uint64_t a = f2_pack_bits(w[0] << 16, w[0] & 0xFFFF0000u);
+#pragma unroll
+        for (int b = 1; b < NB; ++b) a = f2_add(a, f2_pack_bits(w[b] << 16, w[b] & 0xFFFF0000u));
+        f2_unpack(a, lo, hi);
+    } else {
+        lo = __half2float(__ushort_as_half((unsigned short)(w[0] & 0xFFFFu)));
+        hi = __half2float(__ushort_as_half((unsigned short)(w[0] >> 16)));
+        uint64_t a = f2_pack(lo, hi);
+#pragma unroll
+        for (int b = 1; b < NB; ++b) {
+            const float l2 = __half2float(__ushort_as_half((unsigned short)(w[b] & 0xFFFFu)));
+            const float h2 = __half2float(__ushort_as_half((unsigned short)(w[b] >> 16)));
+            a = f2_add(a, f2_pack(l2, h2));
+        }
+        f2_unpack(a, lo, hi);
+    }
+    if ((NB & (NB - 1)) == 0) {  // power of two: multiplying by 1/NB is exact and equals the division
+        lo = __fmul_rn(lo, inv);
+        hi = __fmul_rn(hi, inv);
+    } else {
+        lo = __fdiv_rn(lo, (float)NB);
+        hi = __fdiv_rn(hi, (float)NB);
+    }
+    uint32_t r;
+    if (DT == SDC_DTYPE_BF16) {
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+        const uint32_t t = r & 0x7FFF7FFFu;
+        if ((t + 0x007F007Fu) & 0x80008000u) {  // some half is NaN: canonical quiet NaN
+            if ((t & 0xFFFFu) > 0x7F80u) r = (r & 0xFFFF0000u) | 0x7FC0u;
+            if ((t >> 16) > 0x7F80u) r = (r & 0x0000FFFFu) | 0x7FC00000u;
+        }
+    } else {
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+        const uint32_t t = r & 0x7FFF7FFFu;
+        if ((t + 0x03FF03FFu) & 0x80008000u) {
+            if ((t & 0xFFFFu) > 0x7C00u) r = (r & 0xFFFF0000u) | 0x7E00u;
+            if ((t >> 16) > 0x7C00u) r = (r & 0x0000FFFFu) | 0x7E000000u;
+        }
+    }
+    return r;
+}
+
+template <int NB>
+__device__ __forceinline__ uint32_t avg_word_f32(const uint32_t (&w)[NB], float inv) {
+    float a = __uint_as_float(w[0]);
+#pragma unroll
+    for (int b = 1; b < NB; ++b) a = __fadd_rn(a, __uint_as_float(w[b]));
+    a = ((NB & (NB - 1)) == 0) ? __fmul_rn(a, inv) : __fdiv_rn(a, (float)NB);
+    uint32_t r = __float_as_uint(a);
+    if ((r & 0x7FFFFFFFu) > 0x7F800000u) r = 0x7FC00000u;
+    return r;
+}
+
+template <int DT, int NB>
+__device__ __forceinline__ uint4 avg_vec(const uint4 (&v)[NB], float inv) {
+    uint4 o;
+    uint32_t wx[NB], wy[NB], wz[NB], ww[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        wx[b] = v[b].x;
+        wy[b] = v[b].y;
+        wz[b] = v[b].z;
+        ww[b] = v[b].w;
+    }
+    if (DT == SDC_DTYPE_F32) {
+        o.x = avg_word_f32<NB>(wx, inv);
+        o.y = avg_word_f32<NB>(wy, inv);
+        o.z = avg_word_f32<NB>(wz, inv);
+        o.w = avg_word_f32<NB>(ww, inv);
+    } else {
+        o.x = avg_word_pair16<DT, NB>(wx, inv);
+        o.y = avg_word_pair16<DT, NB>(wy, inv);
+        o.z = avg_word_pair16<DT, NB>(wz, inv);
+        o.w = avg_word_pair16<DT, NB>(ww, inv);
+    }
+    return o;
+}
+
+// One element of the average, for tails and the element path.
+template <int DT>
+__device__ __forceinline__ uint32_t avg_elem(const BufPtrs &bp, int nb, uint64_t i) {
+    float a = 0.0f;
+    for (int b = 0; b < nb; ++b) {
+        uint32_t bits = DT == SDC_DTYPE_F32 ? ((const uint32_t *)bp.p[b])[i] : ((const uint16_t *)bp.p[b])[i];
+        const float x = to_float(bits, DT);
+        a = b == 0 ? x : __fadd_rn(a, x);
+    }
+    a = __fdiv_rn(a, (float)nb);  // equals the multiply by 1/nb when nb is a power of two
+    if (DT == SDC_DTYPE_F32) {
+        uint32_t r = __float_as_uint(a);
+        return (r & 0x7FFFFFFFu) > 0x7F800000u ? 0x7FC00000u : r;
+    } else if (DT == SDC_DTYPE_BF16) {
+        if (isnan(a)) return 0x7FC0u;
+        return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a));
+    } else {
+        if (isnan(a)) return 0x7E00u;
+        return (uint32_t)__half_as_ushort(__float2half_rn(a));
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t load_bits(const void *p, uint64_t i) {
+    return DT == SDC_DTYPE_F32 ? ((const uint32_t *)p)[i] : ((const uint16_t *)p)[i];
+}
+template <int DT>
+__device__ __forceinline__ void store_bits(void *p, uint64_t i, uint32_t v) {
+    if (DT == SDC_DTYPE_F32) ((uint32_t *)p)[i] = v;
+    else ((uint16_t *)p)[i] = (uint16_t)v;
+}
+
+// Vector path: every pointer 16-byte aligned.  Warp task c covers elements
+// [c * CE, min((c + 1) * CE, numel)), CE = kAvgChunkBytes / elem size.
+// Partials: [c][s] for streams s = 0..NB-1 (inputs) and s = NB (average).
+template <int DT, int NB, int U>
+__global__ void __launch_bounds__(kScanBlock) avg_scan_kernel(BufPtrs bp, void *__restrict__ outp, uint64_t numel,
+                                                              uint64_t n_chunks, StatPartial *__restrict__ partials) {
+    constexpr int NS = NB + 1;
+    constexpr uint32_t ES = DT == SDC_DTYPE_F32 ? 4u : 2u;
+    constexpr uint64_t CE = kAvgChunkBytes / ES;
+    const float inv = 1.0f / (float)NB;
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint64_t warp = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint64_t nwarps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
+    for (uint64_t c = warp; c < n_chunks; c += nwarps) {
+        const uint64_t e0 = c * CE;
+        const uint64_t ne = min(CE, numel - e0);
+        const uint32_t nvec = (uint32_t)((ne * ES) >> 4);
+        const uint32_t niter = (nvec + 31) >> 5;
+        const uint4 *in[NB];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) in[b] = (const uint4 *)((const char *)bp.p[b] + e0 * ES);
+        uint4 *out = (uint4 *)((char *)outp + e0 * ES);
+        double acc_s[NS], acc_e[NS];
+        Counts n[NS];
+#pragma unroll
+        for (int s = 0; s < NS; ++s) acc_s[s] = acc_e[s] = 0.0;
+        for (uint32_t r0 = 0; r0 < niter; r0 += kRunVec) {
+            const uint32_t r1 = min(r0 + (uint32_t)kRunVec, niter);
+            FastAcc a[NS];
+            for (uint32_t i0 = r0; i0 < r1; i0 += U) {
+                uint4 v[U][NB];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const uint32_t vi = lane + ((i0 + u) << 5);
+                    const bool ok = i0 + u < r1 && vi < nvec;
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) v[u][b] = ok ? ld_stream(in[b] + vi) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const uint32_t vi = lane + ((i0 + u) << 5);
+                    const bool ok = i0 + u < r1 && vi < nvec;
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) fast_vec<DT>(v[u][b], a[b]);
+                    uint4 o = avg_vec<DT, NB>(v[u], inv);
+                    if (ok) {
+                        __stcs(out + vi, o);
+                    } else {
+                        o = make_uint4(0, 0, 0, 0);
+                    }
+                    fast_vec<DT>(o, a[NB]);
+                }
+            }
+#pragma unroll
+            for (int s = 0; s < NS; ++s) {
+                if (!fast_flush<DT>(a[s], acc_s[s])) {
+                    const uint4 *src = s < NB ? in[s] : (const uint4 *)out;
+                    for (uint32_t i = r0; i < r1; ++i) {
+                        const uint32_t vi = lane + (i << 5);
+                        if (vi < nvec) exact_vec<DT>(src[vi], acc_e[s], n[s]);
+                    }
+                }
+            }
+        }
+        // tail elements of the last chunk (fewer than one vector)
+        const uint64_t done = (uint64_t)nvec * (16u / ES);
+        if (lane < ne - done) {
+            const uint64_t i = e0 + done + lane;
+            const uint32_t r = avg_elem<DT>(bp, NB, i);
+            store_bits<DT>(outp, i, r);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) exact_elem(load_bits<DT>(bp.p[b], i), DT, acc_e[b], n[b]);
+            exact_elem(r, DT, acc_e[NB], n[NB]);
+        }
+#pragma unroll
+        for (int s = 0; s < NS; ++s) {
+            double acc = __dadd_rn(unscale<DT>(acc_s[s]), acc_e[s]);
+            acc = warp_sum_f64(acc);
+            const uint32_t nn = warp_sum_u32(n[s].nan), ni = warp_sum_u32(n[s].inf), nbg = warp_sum_u32(n[s].big);
+            if (lane == 0) partials[c * NS + s] = StatPartial{acc, nn, ni, nbg, 0u};
+        }
+    }
+}
+
+// Element path (some pointer not 16-byte aligned): same task layout, every
+// element exact.
+template <int DT>
+__global__ void __launch_bounds__(kScanBlock) avg_scan_elem_kernel(BufPtrs bp, int nb, void *__restrict__ outp,
+                                                                   uint64_t numel, uint64_t n_chunks,
+                                                                   StatPartial *__restrict__ partials) {
+    constexpr uint32_t ES = DT == SDC_DTYPE_F32 ? 4u : 2u;
+    constexpr uint64_t CE = kAvgChunkBytes / ES;
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint64_t warp = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint64_t nwarps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
+    const int ns = nb + 1;
+    for (uint64_t c = warp; c < n_chunks; c += nwarps) {
+        const uint64_t e0 = c * CE;
+        const uint64_t ne = min(CE, numel - e0);
+        for (int s = 0; s < ns; ++s) {
+            double acc = 0.0;
+            Counts n;
+            for (uint64_t j = lane; j < ne; j += 32) {
+                const uint64_t i = e0 + j;
+                uint32_t bits;
+                if (s < nb) {
+                    bits = load_bits<DT>(bp.p[s], i);
+                } else {
+                    bits = avg_elem<DT>(bp, nb, i);
+                    store_bits<DT>(outp, i, bits);
+                }
+                exact_elem(bits, DT, acc, n);
+            }
+            acc = warp_sum_f64(acc);
+            const uint32_t nn = warp_sum_u32(n.nan), ni = warp_sum_u32(n.inf), nbg = warp_sum_u32(n.big);
+            if (lane == 0) partials[c * ns + s] = StatPartial{acc, nn, ni, nbg, 0u};
+        }
+    }
+}
+
+// ---------------------------------------------------------------- combine
+// One CTA per stream: fixed-order sum of the stream's partials (thread t takes
+// partials t, t + B, ...; then a fixed tree), then the derived fields.
+constexpr int kCombineBlock = 512;
+
+struct StreamSel {
+    const uint64_t *first;  // plan mode: R + 1 chunk offsets; null in buffer mode
+    const uint64_t *numel_arr;
+    uint64_t n_chunks;      // buffer mode: chunks per stream
+    uint64_t numel;         // buffer mode: elements per stream
+    uint32_t n_streams;
+    uint32_t n_pre;         // buffer mode: streams written to out_pre (the rest to out_post)
+};
+
+__global__ void __launch_bounds__(kCombineBlock) stats_combine_kernel(const StatPartial *__restrict__ partials,
+                                                                      StreamSel sel, sdc_grad_stats *out_pre,
+                                                                      sdc_grad_stats *out_post) {
+    const uint32_t s = blockIdx.x;
+    uint64_t base, count, stride, numel;
+    if (sel.first) {
+        base = sel.first[s];
+        count = sel.first[s + 1] - base;
+        stride = 1;
+        numel = sel.numel_arr[s];
+    } else {
+        base = s;
+        count = sel.n_chunks;
+        stride = sel.n_streams;
+        numel = sel.numel;
+    }
+    double acc = 0.0;
+    unsigned long long nn = 0, ni = 0, nb = 0;
+    for (uint64_t i = threadIdx.x; i < count; i += kCombineBlock) {
+        const StatPartial p = partials[base + i * stride];
+        acc = __dadd_rn(acc, p.sumsq);
+        nn += p.n_nan;
+        ni += p.n_inf;
+        nb += p.n_big;
+    }
+    __shared__ double sa[kCombineBlock];
+    __shared__ unsigned long long sn[3][kCombineBlock];
+    sa[threadIdx.x] = acc;
+    sn[0][threadIdx.x] = nn;
+    sn[1][threadIdx.x] = ni;
+    sn[2][threadIdx.x] = nb;
+    __syncthreads();
+    for (int h = kCombineBlock / 2; h > 0; h >>= 1) {
+        if ((int)threadIdx.x < h) {
+            sa[threadIdx.x] = __dadd_rn(sa[threadIdx.x], sa[threadIdx.x + h]);
+            sn[0][threadIdx.x] += sn[0][threadIdx.x + h];
+            sn[1][threadIdx.x] += sn[1][threadIdx.x + h];
+            sn[2][threadIdx.x] += sn[2][threadIdx.x + h];
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        sdc_grad_stats r;
+        r.n_nan = sn[0][0];
+        r.n_inf = sn[1][0];
+        r.n_big = sn[2][0];
+        r.n_elems = numel;
+        r.sumsq_finite = sa[0];
+        if (r.n_nan) r.norm = __longlong_as_double(0x7FF8000000000000ll);
+        else if (r.n_inf) r.norm = __longlong_as_double(0x7FF0000000000000ll);
+        else r.norm = __dsqrt_rn(sa[0]);
+        r.nonfinite_fp32 = (r.n_nan || r.n_inf || sa[0] > kFltMax) ? 1u : 0u;
+        r.reserved = 0;
+        sdc_grad_stats *dst = sel.first ? out_pre + s : (s < sel.n_pre ? out_pre + s : out_post);
+        *dst = r;
+    }
+}
+
+constexpr int kGradUnroll = 4;
+constexpr int kAvgUnroll = 2;
+
+template <int DT, int NB>
+cudaError_t launch_avg_t(const BufPtrs &bp, void *avg, uint64_t numel, StatPartial *partials, uint64_t n_chunks,
+                         int device, cudaStream_t st) {
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, avg_scan_kernel<DT, NB, kAvgUnroll>, kScanBlock, 0);
+    if (per_sm < 1) per_sm = 1;
+    uint64_t grid = (uint64_t)sm_count(device) * per_sm;
+    const uint64_t need = (n_chunks * 32 + kScanBlock - 1) / kScanBlock;
+    if (need < grid) grid = need;
+    avg_scan_kernel<DT, NB, kAvgUnroll><<<(unsigned)grid, kScanBlock, 0, st>>>(bp, avg, numel, n_chunks, partials);
+    return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t launch_avg_dt(const BufPtrs &bp, uint32_t nb, void *avg, uint64_t numel, StatPartial *partials,
+                          uint64_t n_chunks, int device, cudaStream_t st) {
+    switch (nb) {
+        case 1: return launch_avg_t<DT, 1>(bp, avg, numel, partials, n_chunks, device, st);
+        case 2: return launch_avg_t<DT, 2>(bp, avg, numel, partials, n_chunks, device, st);
+        case 3: return launch_avg_t<DT, 3>(bp, avg, numel, partials, n_chunks, device, st);
+        case 4: return launch_avg_t<DT, 4>(bp, avg, numel, partials, n_chunks, device, st);
+        case 5: return launch_avg_t<DT, 5>(bp, avg, numel, partials, n_chunks, device, st);
+        case 6: return launch_avg_t<DT, 6>(bp, avg, numel, partials, n_chunks, device, st);
+        case 7: return launch_avg_t<DT, 7>(bp, avg, numel, partials, n_chunks, device, st);
+        default: return launch_avg_t<DT, 8>(bp, avg, numel, partials, n_chunks, device, st);
+    }
+}
+
+}  // namespace
+
+int grad_scan_blocks_per_sm() {
+    int n = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, grad_scan_kernel<kGradUnroll>, kScanBlock, 0);
+    return n > 0 ? n : 1;
+}
+
+cudaError_t launch_grad_scan(const sdc_plan *plan, StatPartial *partials, cudaStream_t st) {
+    if (plan->n_chunks == 0) return cudaSuccess;
+    uint64_t grid = (uint64_t)sm_count(plan->device) * grad_scan_blocks_per_sm();
+    const uint64_t need = (plan->n_chunks * 32 + kScanBlock - 1) / kScanBlock;
+    if (need < grid) grid = need;
+    grad_scan_kernel<kGradUnroll><<<(unsigned)grid, kScanBlock, 0, st>>>(plan->d_chunks, plan->n_chunks, partials);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_stats_combine_plan(const sdc_plan *plan, const StatPartial *partials, sdc_grad_stats *out,
+                                      cudaStream_t st) {
+    StreamSel sel{plan->d_replica_first_chunk, plan->d_replica_numel, 0, 0, plan->R, plan->R};
+    stats_combine_kernel<<<plan->R, kCombineBlock, 0, st>>>(partials, sel, out, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_avg_scan(const void *const *bufs, uint32_t n_bufs, void *avg, uint64_t numel, uint32_t dtype,
+                            StatPartial *partials, uint64_t n_chunks, bool vector_path, int device,
+                            cudaStream_t st) {
+    if (n_chunks == 0) return cudaSuccess;
+    BufPtrs bp{};
+    for (uint32_t b = 0; b < n_bufs; ++b) bp.p[b] = bufs[b];
+    if (vector_path) {
+        switch (dtype) {
+            case SDC_DTYPE_F32: return launch_avg_dt<SDC_DTYPE_F32>(bp, n_bufs, avg, numel, partials, n_chunks, device, st);
+            case SDC_DTYPE_BF16: return launch_avg_dt<SDC_DTYPE_BF16>(bp, n_bufs, avg, numel, partials, n_chunks, device, st);
+            default: return launch_avg_dt<SDC_DTYPE_F16>(bp, n_bufs, avg, numel, partials, n_chunks, device, st);
+        }
+    }
+    uint64_t grid = (uint64_t)sm_count(device) * 4;
+    const uint64_t need = (n_chunks * 32 + kScanBlock - 1) / kScanBlock;
+    if (need < grid) grid = need;
+    switch (dtype) {
+        case SDC_DTYPE_F32:
+            avg_scan_elem_kernel<SDC_DTYPE_F32><<<(unsigned)grid, kScanBlock, 0, st>>>(bp, (int)n_bufs, avg, numel, n_chunks, partials);
+            break;
+        case SDC_DTYPE_BF16:
+            avg_scan_elem_kernel<SDC_DTYPE_BF16><<<(unsigned)grid, kScanBlock, 0, st>>>(bp, (int)n_bufs, avg, numel, n_chunks, partials);
+            break;
+        default:
+            avg_scan_elem_kernel<SDC_DTYPE_F16><<<(unsigned)grid, kScanBlock, 0, st>>>(bp, (int)n_bufs, avg, numel, n_chunks, partials);
+            break;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_stats_combine_streams(const StatPartial *partials, uint32_t n_streams, uint64_t n_chunks,
+                                         uint64_t numel, sdc_grad_stats *out_pre, sdc_grad_stats *out_post,
+                                         cudaStream_t st) {
+    StreamSel sel{nullptr, nullptr, n_chunks, numel, n_streams, n_streams - 1};
+    stats_combine_kernel<<<n_streams, kCombineBlock, 0, st>>>(partials, sel, out_pre, out_post);
+    return cudaGetLastError();
+}
+
+}  // namespace sdc

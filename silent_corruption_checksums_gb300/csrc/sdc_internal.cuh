@@ -1,0 +1,231 @@
+// sdc_internal.cuh -- structures and device helpers shared by libsdc's
+// translation units.  Not part of the public ABI (see include/sdc.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/sdc.h"
+
+namespace sdc {
+
+// ---------------------------------------------------------------------------
+// Device tables
+// ---------------------------------------------------------------------------
+
+// One warp task: a run of at most chunk_bytes bytes of one tensor copy.
+// Interior chunk boundaries sit on absolute multiples of chunk_bytes, so every
+// chunk except a tensor's first and last starts and ends 16-byte aligned.
+struct Chunk {
+    uint64_t addr;    // absolute device byte address of the chunk's first element
+    uint32_t nbytes;  // bytes in the chunk, a multiple of the element size
+    uint32_t tag;     // bits 0..27 descriptor index, 28..29 log2(elem size), 30..31 dtype
+};
+static_assert(sizeof(Chunk) == 16, "Chunk is 16 bytes");
+
+constexpr uint32_t kDescBits = 28;
+constexpr uint32_t kMaxDescs = 1u << kDescBits;
+
+__host__ __device__ inline uint32_t chunk_desc(uint32_t tag) { return tag & (kMaxDescs - 1); }
+__host__ __device__ inline uint32_t chunk_log2es(uint32_t tag) { return (tag >> 28) & 3u; }
+__host__ __device__ inline uint32_t chunk_dtype(uint32_t tag) { return tag >> 30; }
+__host__ __device__ inline uint32_t make_tag(uint32_t desc, uint32_t log2es, uint32_t dtype) {
+    return desc | (log2es << 28) | (dtype << 30);
+}
+
+// Descriptor as the combine kernels see it.
+struct DescDev {
+    uint64_t ptr;          // device address of element 0
+    uint64_t first_chunk;  // index of the descriptor's first chunk
+    uint32_t n_chunks;     // chunks of this descriptor (0 when numel == 0)
+    uint32_t log2es;       // log2(elem size)
+};
+static_assert(sizeof(DescDev) == 24, "DescDev is 24 bytes");
+
+// Per-chunk partial of the fingerprint pass.
+struct FpPartial {
+    uint64_t s;  // sum of widened bits
+    uint64_t w;  // sum of (local index + 1) * bits, local index from the chunk start
+};
+
+// Per-chunk (or per-stream) partial of a gradient scan.
+struct StatPartial {
+    double sumsq;  // sum of x^2 over finite elements
+    uint32_t n_nan;
+    uint32_t n_inf;
+    uint32_t n_big;
+    uint32_t pad;
+};
+static_assert(sizeof(StatPartial) == 24, "StatPartial is 24 bytes");
+
+}  // namespace sdc
+
+// The plan (opaque to callers).
+struct sdc_plan {
+    int device = -1;
+    uint32_t T = 0, R = 0;
+    uint32_t chunk_bytes = 0;
+    uint64_t n_desc = 0;
+    uint64_t n_chunks = 0;
+    uint32_t grid = 0, block = 0;
+    bool all_float = false;                 // every descriptor has a float dtype
+    std::vector<sdc_tensor_desc> descs;     // host copy
+    std::vector<uint64_t> replica_numel;    // elements per replica
+    std::vector<uint64_t> replica_first_chunk;  // R + 1 entries
+    sdc::Chunk *d_chunks = nullptr;
+    sdc::DescDev *d_descs = nullptr;
+    uint64_t *d_replica_first_chunk = nullptr;  // R + 1
+    uint64_t *d_replica_numel = nullptr;        // R
+};
+
+namespace sdc {
+
+// ---------------------------------------------------------------------------
+// Host-side helpers (sdc_plan.cu)
+// ---------------------------------------------------------------------------
+void set_error(const std::string &msg);
+sdc_status fail(sdc_status st, const std::string &msg);
+sdc_status cuda_fail(cudaError_t e, const char *what);
+sdc_status check_plan_device(const sdc_plan *plan);
+// Check [ptr, ptr + bytes) is device memory of `device` inside one allocation.
+sdc_status check_device_range(const void *ptr, uint64_t bytes, int device, const char *what);
+int sm_count(int device);
+
+// Launchers (one per translation unit that holds the kernel).
+cudaError_t launch_fp_scan(const sdc_plan *plan, FpPartial *partials, cudaStream_t st);
+cudaError_t launch_fp_combine(const sdc_plan *plan, const FpPartial *partials, uint64_t *out,
+                              cudaStream_t st);
+cudaError_t launch_xor_scan(const sdc_plan *plan, uint64_t *partials, cudaStream_t st);
+cudaError_t launch_xor_combine(const sdc_plan *plan, const uint64_t *partials, uint64_t *out,
+                               cudaStream_t st);
+cudaError_t launch_grad_scan(const sdc_plan *plan, StatPartial *partials, cudaStream_t st);
+cudaError_t launch_stats_combine_plan(const sdc_plan *plan, const StatPartial *partials,
+                                      sdc_grad_stats *out, cudaStream_t st);
+cudaError_t launch_avg_scan(const void *const *bufs, uint32_t n_bufs, void *avg, uint64_t numel,
+                            uint32_t dtype, StatPartial *partials, uint64_t n_chunks, bool vector_path,
+                            int device, cudaStream_t st);
+cudaError_t launch_stats_combine_streams(const StatPartial *partials, uint32_t n_streams,
+                                         uint64_t n_chunks, uint64_t numel, sdc_grad_stats *out_pre,
+                                         sdc_grad_stats *out_post, cudaStream_t st);
+cudaError_t launch_vote(const uint64_t *fp, uint32_t R, uint32_t T, int32_t *suspect, uint64_t *mask,
+                        sdc_vote_summary *summary, cudaStream_t st);
+cudaError_t launch_xor_compare(const uint64_t *a, const uint64_t *b, uint32_t n, uint8_t *mismatch,
+                               uint64_t *diff, cudaStream_t st);
+
+// Persistent-kernel block size and per-SM occupancy of the scan kernels.
+constexpr int kScanBlock = 256;
+int fp_scan_blocks_per_sm();
+int grad_scan_blocks_per_sm();
+
+// Elements of one warp task in the fused average scan (per stream).
+constexpr uint64_t kAvgChunkBytes = 16384;
+
+}  // namespace sdc
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+#ifdef __CUDACC__
+namespace sdc {
+
+// Streaming 16-byte load: read-only path, no L1 allocation, 256-byte L2 fetch.
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+// Two-way 16x8-bit dot product with 32-bit accumulate, both halves signed.
+__device__ __forceinline__ int dp2a_lo_s(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.lo.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp2a_hi_s(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.hi.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+// Four-way 8x8-bit unsigned dot product with 32-bit accumulate.
+__device__ __forceinline__ uint32_t dp4a_u(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Packed pair of float32 in one 64-bit register (low word = first element).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_pack_bits(uint32_t lo, uint32_t hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+    return d;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// Error-free sum (Knuth's TwoSum) on both lanes: s + y = s' + err exactly;
+// the error is added to the compensation c.
+__device__ __forceinline__ void f2_two_sum_acc(uint64_t &s, uint64_t &c, uint64_t y) {
+    uint64_t s2 = f2_add(s, y);
+    uint64_t bb = f2_sub(s2, s);
+    uint64_t t1 = f2_sub(s2, bb);
+    uint64_t t2 = f2_sub(s, t1);
+    uint64_t t3 = f2_sub(y, bb);
+    c = f2_add(c, f2_add(t2, t3));
+    s = s2;
+}
+
+__device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ uint64_t warp_xor_u64(uint64_t v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v ^= __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+// Fixed-shape butterfly: every lane ends with the same value, bit for bit.
+__device__ __forceinline__ double warp_sum_f64(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ uint32_t warp_sum_u32(uint32_t v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+}  // namespace sdc
+#endif  // __CUDACC__

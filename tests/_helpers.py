@@ -1,0 +1,56 @@
+"""Helpers shared by the tests: host copies of device tensors for the oracle,
+and conversions of the library's outputs to Python ints."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+M64 = (1 << 64) - 1
+_NP_INT = {1: np.uint8, 2: np.uint16, 4: np.uint32, 8: np.uint64}
+_T_INT = {1: torch.uint8, 2: torch.int16, 4: torch.int32, 8: torch.int64}
+
+
+def host_bits(t: torch.Tensor) -> np.ndarray:
+    """Raw element bits of a tensor as a host numpy array of the same item size."""
+    es = t.element_size()
+    flat = t.detach().reshape(-1)
+    return flat.view(_T_INT[es]).cpu().numpy().view(_NP_INT[es])
+
+
+def u64(x: int) -> int:
+    return int(x) & M64
+
+
+def fp_table(out: torch.Tensor) -> list[list[tuple[int, int]]]:
+    """[R, T, 2] int64 device tensor -> nested lists of (S, W) as unsigned ints."""
+    a = out.cpu().numpy().view(np.uint64)
+    return [[(int(a[r, k, 0]), int(a[r, k, 1])) for k in range(a.shape[1])] for r in range(a.shape[0])]
+
+
+def oracle_fp_table(replicas, threads: int = 1):
+    import oracle
+    return [[oracle.fingerprint(host_bits(t), threads=threads) for t in ts] for ts in replicas]
+
+
+def rel_err(a: float, b: float) -> float:
+    if a == b:
+        return 0.0
+    return abs(a - b) / max(abs(b), 1e-300)
+
+
+def stats_match(gpu: dict, ref: dict, rtol: float = 1e-10) -> None:
+    """Counts, flags and element totals exactly; sumsq and norm within rtol (norm class-wise)."""
+    import math
+    for k in ("n_nan", "n_inf", "n_big", "n_elems"):
+        assert gpu[k] == ref[k], (k, gpu[k], ref[k])
+    assert rel_err(gpu["sumsq_finite"], ref["sumsq_finite"]) <= rtol, (gpu["sumsq_finite"], ref["sumsq_finite"])
+    if math.isnan(ref["norm"]):
+        assert math.isnan(gpu["norm"])
+    elif math.isinf(ref["norm"]):
+        assert gpu["norm"] == ref["norm"]
+    else:
+        assert rel_err(gpu["norm"], ref["norm"]) <= rtol, (gpu["norm"], ref["norm"])
+    # the float32 flag is exact unless the squared norm sits within rtol of FLT_MAX
+    import oracle
+    if abs(ref["sumsq_finite"] - oracle.FLT_MAX) > 1e-9 * oracle.FLT_MAX:
+        assert gpu["nonfinite_fp32"] == ref["nonfinite_fp32"]

@@ -1,0 +1,110 @@
+"""The C ABI library loads on a CPU-only host, exports every entry point the
+header declares, and its host-side validation rejects bad arguments before
+touching the GPU."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sdc.h")
+
+
+@pytest.fixture(scope="module")
+def sdc():
+    from silent_corruption_checksums_gb300 import build
+    build.build()
+    import silent_corruption_checksums_gb300 as m
+    return m
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sdc_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(sdc):
+    names = _declared_functions()
+    assert len(names) >= 13
+    lib = ctypes.CDLL(sdc.library_path())
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_struct_layouts_match_header(sdc):
+    assert sdc.DESC_DTYPE.itemsize == 24
+    assert sdc.GRAD_STATS_DTYPE.itemsize == 56
+    assert sdc.VOTE_SUMMARY_DTYPE.itemsize == 24
+
+
+def test_status_strings(sdc):
+    assert sdc.sdc_status_string(0) == "SDC_OK"
+    assert sdc.sdc_status_string(5) == "SDC_ERR_WS_TOO_SMALL"
+    assert sdc.sdc_status_string(99) == "SDC_ERR_UNKNOWN"
+
+
+def _descs(entries):
+    d = np.zeros(len(entries), dtype=np.dtype([("ptr", "<u8"), ("numel", "<u8"), ("elem_size", "<u4"),
+                                               ("dtype", "<u4")]))
+    for i, e in enumerate(entries):
+        d[i] = e
+    return d
+
+
+def test_host_validation_without_gpu(sdc):
+    with pytest.raises(sdc.SdcError) as ei:
+        sdc.sdc_plan_create(_descs([]), 0, 0)
+    assert ei.value.status == 4  # R == 0
+    with pytest.raises(sdc.SdcError) as ei:
+        sdc.sdc_plan_create(_descs([(4096, 10, 4, 1)] * 65), 1, 65)
+    assert ei.value.status == 4  # R > 64
+    with pytest.raises(sdc.SdcError) as ei:
+        sdc.sdc_plan_create(_descs([(4096, 10, 3, 0)]), 1, 1)
+    assert ei.value.status == 2  # element size 3
+    with pytest.raises(sdc.SdcError) as ei:
+        sdc.sdc_plan_create(_descs([(4096, 10, 2, 1)]), 1, 1)
+    assert ei.value.status == 2  # f32 with 2-byte elements
+    with pytest.raises(sdc.SdcError) as ei:
+        sdc.sdc_plan_create(_descs([(4096, 10, 4, 9)]), 1, 1)
+    assert ei.value.status == 7  # unknown dtype
+    with pytest.raises(sdc.SdcError) as ei:
+        sdc.sdc_plan_create(_descs([(4096, 10, 4, 1), (8192, 11, 4, 1)]), 1, 2)
+    assert ei.value.status == 3  # replica 1 has another numel
+    with pytest.raises(sdc.SdcError) as ei:
+        sdc.sdc_plan_create(_descs([(0, 10, 4, 1)]), 1, 1)
+    assert ei.value.status == 1  # NULL with elements
+    with pytest.raises(sdc.SdcError) as ei:
+        sdc.sdc_plan_create(_descs([(4098, 10, 4, 1)]), 1, 1)
+    assert ei.value.status == 8  # not aligned to the element size
+    with pytest.raises(sdc.SdcError) as ei:
+        sdc.sdc_plan_create(_descs([(4096, 10, 4, 1)]), 1, 1, chunk_bytes=5000)
+    assert ei.value.status == 9
+    assert "chunk_bytes" in sdc.sdc_last_error()
+    with pytest.raises(sdc.SdcError) as ei:
+        sdc.sdc_vote(0, 0, 1, 0, 0, 0, 0)
+    assert ei.value.status == 4
+    with pytest.raises(sdc.SdcError) as ei:
+        sdc.sdc_grad_average_scan([], 0, 10, 2, 0, 0, 0, 0, 0)
+    assert ei.value.status == 4
+    with pytest.raises(sdc.SdcError) as ei:
+        sdc.sdc_grad_average_scan([4096], 8192, 10, 0, 8, 8, 0, 0, 0)
+    assert ei.value.status == 7
+    assert sdc.sdc_grad_average_scan_workspace_size(0, 4, 2) == 0
+    assert sdc.sdc_grad_average_scan_workspace_size(8192, 4, 2) == 256  # one 16 KiB task x 5 streams x 24 B
+    sdc.sdc_xorsum_compare(0, 0, 0, 0, 0, 0)  # n == 0 is a no-op
+
+
+def test_pages_verdict_decoding(sdc):
+    assert sdc.pages_verdict({"diverged": 0, "no_majority": 0, "suspect_mask": 0}) == \
+        {"diverged": False, "suspects": []}
+    assert sdc.pages_verdict({"diverged": 1, "no_majority": 1, "suspect_mask": 4}) == \
+        {"diverged": True, "suspects": None}
+    assert sdc.pages_verdict({"diverged": 1, "no_majority": 0, "suspect_mask": 0b1010}) == \
+        {"diverged": True, "suspects": [1, 3]}
+    raw = np.zeros(1, dtype=sdc.VOTE_SUMMARY_DTYPE)
+    raw["diverged"] = 1
+    raw["suspect_mask"] = 1 << 63
+    assert sdc.decode_summary(raw.view(np.uint8))["suspect_mask"] == 1 << 63

@@ -1,0 +1,155 @@
+"""The five workloads at full size, in the launch configuration the benchmark
+times, checked against the oracle (whole workloads where the host can redo
+them in seconds, sampled tensors plus ground truth elsewhere)."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sdc_workloads as W
+from tests._helpers import fp_table, host_bits, stats_match
+
+pytestmark = [pytest.mark.gpu, pytest.mark.big]
+DEV = "cuda"
+THREADS = max(1, min(16, os.cpu_count() or 1))
+
+
+@pytest.fixture(scope="module")
+def sdc():
+    import silent_corruption_checksums_gb300 as m
+    return m
+
+
+@pytest.fixture(autouse=True)
+def _free():
+    yield
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def _vote(sdc, fp):
+    suspect, mask, summary = sdc.vote(fp)
+    return suspect.cpu().tolist(), mask.cpu().numpy().view(np.uint64).tolist(), sdc.decode_summary(summary)
+
+
+def test_tiny_config(sdc):
+    w = W.tiny(DEV, seed=0)
+    plan = sdc.Plan(w["replicas"])
+    fp = plan.fingerprint()
+    got = fp_table(fp)
+    ref = [[oracle.fingerprint(host_bits(t)) for t in ts] for ts in w["replicas"]]
+    assert got == ref
+    s, m, summ = _vote(sdc, fp)
+    rs, rm, rsumm = oracle.vote(ref)
+    assert s == rs and m == rm and sdc.pages_verdict(summ) == oracle.pages_verdict(rsumm) == \
+        {"diverged": True, "suspects": [1]}
+
+
+def test_1b_fp32_three_replicas_full_oracle(sdc):
+    w = W.weights_1b(DEV, seed=1)
+    plan = sdc.Plan(w["replicas"])
+    fp = plan.fingerprint()
+    got = fp_table(fp)
+    ref = [[oracle.fingerprint(host_bits(t), threads=THREADS) for t in ts] for ts in w["replicas"]]
+    assert got == ref
+    t = w["truth"]
+    s, m, summ = _vote(sdc, fp)
+    rs, rm, rsumm = oracle.vote(ref)
+    assert s == rs and m == rm
+    exp = [-1] * len(w["layout"])
+    exp[t["tensor"]] = t["replica"]
+    assert s == exp
+    assert sdc.pages_verdict(summ) == {"diverged": True, "suspects": [t["replica"]]}
+    xs = plan.xorsum().cpu().numpy().view(np.uint64)
+    for r in range(3):
+        assert int(xs[r, t["tensor"]]) == oracle.xorsum(host_bits(w["replicas"][r][t["tensor"]]), threads=THREADS)
+
+
+def test_grad_config_full_oracle(sdc):
+    g = W.grads_1b(DEV, seed=3)
+    bufs = g["bufs"]
+    avg, pre, post = sdc.grad_average_scan(bufs)
+    torch.cuda.synchronize()
+    hb = [host_bits(b) for b in bufs]
+    got_pre = sdc.decode_stats(pre)
+    for b in range(4):
+        stats_match(got_pre[b], oracle.grad_stats(hb[b], "bf16", threads=THREADS))
+    # ground truth of the injector: counts of the injected buffer
+    kinds = [k for _, k in g["truth"]]
+    assert got_pre[2]["n_nan"] == kinds.count("nan")
+    assert got_pre[2]["n_inf"] == kinds.count("+inf") + kinds.count("-inf")
+    assert got_pre[2]["n_big"] == kinds.count("+2^70") + kinds.count("-2^70")
+    ref_avg = oracle.average(hb, "bf16", threads=THREADS)
+    assert np.array_equal(host_bits(avg), ref_avg)
+    got_post = sdc.decode_stats(post)[0]
+    stats_match(got_post, oracle.grad_stats(ref_avg, "bf16", threads=THREADS))
+    assert got_post["nonfinite_fp32"] == 1
+
+
+def test_8b_bf16_eight_replicas_sampled(sdc):
+    w = W.weights_8b(DEV, seed=4)
+    reps = w["replicas"]
+    plan = sdc.Plan(reps)
+    fp = plan.fingerprint()
+    got = fp_table(fp)
+    t = w["truth"]
+    k = t["tensor"]
+    for r in range(8):  # every copy of the perturbed tensor
+        assert got[r][k] == oracle.fingerprint(host_bits(reps[r][k]), threads=THREADS)
+    rng = np.random.default_rng(40)
+    for _ in range(8):  # random other copies
+        r, kk = int(rng.integers(8)), int(rng.integers(len(reps[0])))
+        assert got[r][kk] == oracle.fingerprint(host_bits(reps[r][kk]), threads=THREADS)
+    s, m, summ = _vote(sdc, fp)
+    exp = [-1] * len(w["layout"])
+    exp[k] = t["replica"]
+    assert s == exp and m[k] == 1 << t["replica"]
+    assert sdc.pages_verdict(summ) == {"diverged": True, "suspects": [t["replica"]]}
+    # property at any size: the copies that were not touched agree exactly
+    for kk in range(len(reps[0])):
+        if kk != k:
+            assert len({got[r][kk] for r in range(8)}) == 1
+
+
+def test_stress_many_small_tensors_sampled(sdc):
+    w = W.stress(DEV, seed=5)
+    reps = w["replicas"]
+    plan = sdc.Plan(reps)
+    fp = plan.fingerprint()
+    got = fp_table(fp)
+    t = w["truth"]
+    T = len(reps[0])
+    for r in range(3):
+        assert got[r][t["tensor"]] == oracle.fingerprint(host_bits(reps[r][t["tensor"]]))
+    rng = np.random.default_rng(50)
+    for _ in range(1500):
+        r, k = int(rng.integers(3)), int(rng.integers(T))
+        assert got[r][k] == oracle.fingerprint(host_bits(reps[r][k])), (r, k)
+    s, m, summ = _vote(sdc, fp)
+    assert [i for i, v in enumerate(s) if v != -1] == [t["tensor"]]
+    assert s[t["tensor"]] == t["replica"]
+    assert sdc.pages_verdict(summ) == {"diverged": True, "suspects": [t["replica"]]}
+    # grad statistics over the mixed-dtype replicas (counts exact, norm to 1e-10)
+    stats = sdc.decode_stats(plan.grad_scan())
+    idx = rng.choice(T, size=0, replace=False)
+    del idx
+    ref0 = oracle.grad_stats_multi([host_bits(x) for x in reps[0]],
+                                   [{torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16"}[x.dtype]
+                                    for x in reps[0]], threads=THREADS)
+    stats_match(stats[0], ref0)
+    # xorsum compare of 1,000 (original, recomputed) pairs
+    p = w["pairs"]
+    pplan = sdc.Plan([p["orig"], p["recomp"]])
+    xs = pplan.xorsum()
+    mism, diff = sdc.xorsum_compare(xs[0], xs[1])
+    xs_np = xs.cpu().numpy().view(np.uint64)
+    for i in range(len(p["orig"])):
+        assert int(xs_np[0, i]) == oracle.xorsum(host_bits(p["orig"][i]))
+        assert int(xs_np[1, i]) == oracle.xorsum(host_bits(p["recomp"][i]))
+    differ = {i for i, _, _ in p["differ"]}
+    assert set(np.nonzero(mism.cpu().numpy())[0].tolist()) == differ
+    dnp = diff.cpu().numpy().view(np.uint64)
+    for i, e, b in p["differ"]:
+        assert int(dnp[i]) == 1 << b
