@@ -125,6 +125,20 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
+def scan_traffic(layers: int):
+    """DRAM bytes per launch of the scan kernel from the committed ncu summary,
+    scaled to this workload, or None when the kernel source changed since."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "fp_scan_traffic.json")
+    src = os.path.join(ROOT, "silent_corruption_checksums_gb300", "csrc", "sdc_fp.cu")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("source_sha256") != hashlib.sha256(open(src, "rb").read()).hexdigest():
+        return None
+    return d["dram_bytes_per_launch"] * d.get("scale_to_full", 1.0) if layers == 24 else None
+
+
 def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -210,7 +224,7 @@ def run_ours(args) -> None:
     stream = torch.cuda.current_stream()
 
     # ---- workload: 3 float32 replicas of the 1b layout, one bit flipped
-    w = W.weights_1b(dev, seed=1 + rank)
+    w = W.weights_1b(dev, seed=1 + rank, n_layers=args.layers)
     reps = w["replicas"]
     R, T = len(reps), len(reps[0])
     bytes_per_step = sum(t.numel() * t.element_size() for ts in reps for t in ts)
@@ -265,7 +279,8 @@ def run_ours(args) -> None:
         line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
                 "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "int64", "data": "synthetic",
-                "config": {"workload": WORKLOAD, "params_per_replica": W.layout_numel(W.layout_1b()),
+                "config": {"workload": WORKLOAD if args.layers == 24 else f"{WORKLOAD}_{args.layers}layers",
+                           "params_per_replica": W.layout_numel(w["layout"]),
                            "replicas": R, "tensors": T, "weights": "float32 N(0,0.02), one seeded bit flip",
                            "bytes_per_step": bytes_per_step, "chunk_bytes": plan_chunk_bytes(args),
                            "grid": plan.grid, "block": plan.block, "n_chunks": plan.n_chunks,
@@ -273,7 +288,8 @@ def run_ours(args) -> None:
                            "vote_names_flipped_replica": ok},
                 "pct_hbm_peak": 100.0 * value / world / peaks["hbm_gbs"],
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                             "frac": achieved / peaks["hbm_gbs"], "traffic": args.traffic,
+                             "frac": achieved / peaks["hbm_gbs"],
+                             "traffic": args.traffic if args.traffic is not None else scan_traffic(args.layers),
                              "kernel": "fp_scan_kernel (+ fp_combine_kernel, timed together as sdc_fingerprint)",
                              "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)"},
                 "kernel_ms": fp_ms, "gpu_launches": launches_per_step * args.steps,
@@ -386,6 +402,8 @@ def main(argv=None) -> None:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--chunk-bytes", type=int, default=0)
     ap.add_argument("--quick", action="store_true", help="only the timed fingerprint step (no rows/e2e/cpu)")
+    ap.add_argument("--layers", type=int, default=24,
+                    help="decoder layers of the 1b layout (24 = the benchmark workload; fewer for profiling)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per launch of the scan kernel from an ncu capture, if current")
     args = ap.parse_args(argv)

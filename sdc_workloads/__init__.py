@@ -31,8 +31,8 @@ import numpy as np
 import torch
 
 # ---------------------------------------------------------------- layouts
-def layout_1b() -> list[tuple[str, tuple[int, ...]]]:
-    d, ffn, vocab, layers = 1792, 7168, 32000, 24
+def layout_1b(layers: int = 24) -> list[tuple[str, tuple[int, ...]]]:
+    d, ffn, vocab = 1792, 7168, 32000
     out = [("embed", (vocab, d))]
     for i in range(layers):
         out += [(f"l{i}.q", (d, d)), (f"l{i}.k", (d, d)), (f"l{i}.v", (d, d)), (f"l{i}.o", (d, d)),
@@ -123,8 +123,8 @@ def weights(layout, n_replicas: int, dtype, std: float, device, seed: int) -> li
     return reps
 
 
-def weights_1b(device, seed: int = 1, n_replicas: int = 3) -> dict:
-    layout = layout_1b()
+def weights_1b(device, seed: int = 1, n_replicas: int = 3, n_layers: int = 24) -> dict:
+    layout = layout_1b(n_layers)
     reps = weights(layout, n_replicas, torch.float32, 0.02, device, seed)
     rng = np.random.default_rng(seed)
     r = int(rng.integers(n_replicas))

@@ -87,13 +87,20 @@ def _load() -> ctypes.CDLL:
 
 
 class _Missing:
-    """Stands in for the library when it is not built: every call raises."""
+    """Stands in for the library until it is built: each use retries the load
+    (the build step may have produced it since import) and raises if it is
+    still missing."""
 
     def __init__(self, err: Exception):
         self.err = err
 
     def __getattr__(self, name):
-        raise ImportError(str(self.err))
+        global _lib
+        try:
+            _lib = _load()
+        except ImportError as e:
+            raise ImportError(str(e)) from None
+        return getattr(_lib, name)
 
 
 try:
