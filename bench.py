@@ -208,12 +208,27 @@ def run_reference(args) -> None:
 
 
 # ---------------------------------------------------------------- our arm
+def run_only_row(args) -> None:
+    """Time one row alone (profiling helper): prints a small JSON line."""
+    import numpy as np
+    import torch
+    import sdc_workloads as W
+    import silent_corruption_checksums_gb300 as sdc
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    rows = bench_rows(args, dev, torch.cuda.current_stream(), measured_peaks(), sdc, W, torch, np,
+                      only=args.only)
+    print(json.dumps({"only": args.only, "layers": args.layers, "rows": rows}), flush=True)
+
+
 def run_ours(args) -> None:
     import numpy as np
     import torch
     import sdc_workloads as W
     import silent_corruption_checksums_gb300 as sdc
 
+    if args.only:
+        return run_only_row(args)
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -317,11 +332,11 @@ def _time_loop(fn, steps, stream, torch):
     return a.elapsed_time(b) / steps
 
 
-def bench_rows(args, dev, stream, peaks, sdc, W, torch, np) -> dict:
+def bench_rows(args, dev, stream, peaks, sdc, W, torch, np, only=None) -> dict:
     """The other rows of the hot path, each timed on its own workload."""
     rows = {}
     # fused gradient average-scan on 4 bf16 buffers of the 1b layout
-    g = W.grads_1b(dev, seed=3)
+    g = W.grads_flat(W.layout_numel(W.layout_1b(args.layers)), 4, torch.bfloat16, 1e-3, dev, seed=3)
     bufs = g["bufs"]
     n = bufs[0].numel()
     out = torch.empty_like(bufs[0])
@@ -331,19 +346,41 @@ def bench_rows(args, dev, stream, peaks, sdc, W, torch, np) -> dict:
     def avg_step():
         sdc.grad_average_scan(bufs, out=out, stream=stream, ws=ws)
 
-    ms = _time_loop(avg_step, max(5, args.steps // 10), stream, torch)
+    ms = _time_loop(avg_step, max(5, args.steps // 10), stream, torch) if only in (None, "grad_average_scan") \
+        else None
     nbytes = 5 * n * 2
-    rows["grad_average_scan"] = {"workload": "4 x bf16 local grads of the 1b layout (N(0,1e-3), rate-1e-7 "
-                                 "NaN/Inf/2^70 in buffer 2)", "ms": ms, "bytes": nbytes,
-                                 "GB_s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"]}
+    if ms is not None:
+        rows["grad_average_scan"] = {"workload": "4 x bf16 local grads of the 1b layout (N(0,1e-3), rate-1e-7 "
+                                     "NaN/Inf/2^70 in buffer 2)", "ms": ms, "bytes": nbytes,
+                                     "GB_s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"]}
     # the same buffers as one plan: pre-average scan only
-    gplan = sdc.Plan([[b] for b in bufs])
-    stats = torch.empty((4, sdc.GRAD_STATS_DTYPE.itemsize), dtype=torch.uint8, device=dev)
-    ms = _time_loop(lambda: gplan.grad_scan(out=stats, stream=stream), max(5, args.steps // 10), stream, torch)
-    nbytes = 4 * n * 2
-    rows["grad_scan"] = {"workload": "4 x bf16 local grads of the 1b layout", "ms": ms, "bytes": nbytes,
-                         "GB_s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"]}
-    del gplan, g, bufs, out, ws
+    if only in (None, "grad_scan"):
+        gplan = sdc.Plan([[b] for b in bufs])
+        stats = torch.empty((4, sdc.GRAD_STATS_DTYPE.itemsize), dtype=torch.uint8, device=dev)
+        ms = _time_loop(lambda: gplan.grad_scan(out=stats, stream=stream), max(5, args.steps // 10), stream,
+                        torch)
+        nbytes = 4 * n * 2
+        rows["grad_scan"] = {"workload": "4 x bf16 local grads of the 1b layout", "ms": ms, "bytes": nbytes,
+                             "GB_s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"]}
+        del gplan
+    if only in (None, "xorsum"):
+        # xorsum + pair compare of 4 bf16 buffers against copies (original vs recomputed)
+        rec = [b.clone() for b in bufs]
+        W.xor_element(rec[1], 12345, 1 << 3)
+        xplan = sdc.Plan([list(bufs), rec])
+        xo = torch.empty((2, 4), dtype=torch.int64, device=dev)
+
+        def xor_step():
+            xplan.xorsum(out=xo, stream=stream)
+            sdc.xorsum_compare(xo[0], xo[1], stream=stream)
+
+        ms = _time_loop(xor_step, max(5, args.steps // 10), stream, torch)
+        nbytes = 8 * n * 2
+        rows["xorsum"] = {"workload": "xorsum of 4 bf16 grad buffers and their recomputed copies + compare",
+                          "ms": ms, "bytes": nbytes, "GB_s": nbytes / ms / 1e6,
+                          "frac_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"]}
+        del xplan, rec
+    del g, bufs, out, ws
     torch.cuda.empty_cache()
     return rows
 
@@ -402,6 +439,8 @@ def main(argv=None) -> None:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--chunk-bytes", type=int, default=0)
     ap.add_argument("--quick", action="store_true", help="only the timed fingerprint step (no rows/e2e/cpu)")
+    ap.add_argument("--only", choices=["grad_average_scan", "grad_scan", "xorsum"], default=None,
+                    help="time one row alone (profiling)")
     ap.add_argument("--layers", type=int, default=24,
                     help="decoder layers of the 1b layout (24 = the benchmark workload; fewer for profiling)")
     ap.add_argument("--traffic", type=float, default=None,

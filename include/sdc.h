@@ -149,9 +149,10 @@ sdc_status sdc_plan_create(const sdc_tensor_desc *host_descs, uint32_t T, uint32
  * not destroy a plan whose work is still queued).  NULL is accepted. */
 sdc_status sdc_plan_destroy(sdc_plan *plan);
 
-/* Bytes of device workspace the plan's compute calls need (0 for a plan with
- * no elements).  Any 256-byte-aligned device buffer at least this large
- * works; its contents need no initialisation. */
+/* Bytes of device workspace the plan's compute calls need: per-chunk partials
+ * plus the group sums of the statistics combine.  Any 256-byte-aligned device
+ * buffer at least this large works; its contents need no initialisation.
+ * Calls that share one workspace must not overlap on the GPU. */
 size_t sdc_workspace_size(const sdc_plan *plan);
 
 /* Plan facts for reporting: chunk count, persistent grid and block size. */
@@ -211,7 +212,8 @@ sdc_status sdc_vote(const uint64_t *d_fp, uint32_t R, uint32_t T, int32_t *d_sus
 sdc_status sdc_grad_scan(const sdc_plan *plan, sdc_grad_stats *d_stats, void *d_ws, size_t ws_bytes,
                          sdc_stream_t stream);
 
-/* Workspace bytes for sdc_grad_average_scan with these sizes. */
+/* Workspace bytes for sdc_grad_average_scan with these sizes (0 when n_bufs or
+ * dtype is invalid). */
 size_t sdc_grad_average_scan_workspace_size(uint64_t numel, uint32_t n_bufs, uint32_t dtype);
 
 /* One fused pass: scan n_bufs local gradient buffers, write their average,

@@ -10,8 +10,9 @@
 // A persistent grid of warps walks the chunk table; each warp reads its chunk
 // with coalesced 16-byte streaming loads (512 contiguous bytes per warp
 // instruction), reduces in registers and with shuffles, and writes one
-// partial.  A second kernel combines the partials per descriptor, in integer
-// arithmetic, so the result is exact and independent of the launch shape.
+// partial.  A second kernel, parallel over chunks, combines the partials per
+// descriptor in integer arithmetic, so the result is exact and independent of
+// the launch shape.
 //
 // Position weights without a 64-bit multiply per element: for a chunk whose
 // first element has tensor index o, W = sum_j (o + j + 1) b_j
@@ -244,28 +245,43 @@ __global__ void __launch_bounds__(kScanBlock) fp_scan_kernel(const Chunk *__rest
     }
 }
 
-// One warp per descriptor: S = sum S_c, W = sum (W_c + o_c S_c), o_c = the
-// chunk's first tensor index.  Writes (0, 0) for empty descriptors.
-__global__ void fp_combine_kernel(const DescDev *__restrict__ descs, uint64_t n_desc, const Chunk *__restrict__ chunks,
-                                  const FpPartial *__restrict__ partials, uint64_t *__restrict__ out) {
+// Second pass, parallel over chunks: thread i turns chunk i's partial into
+// its tensor-level contribution (S_c, W_c + o_c S_c), o_c = the chunk's first
+// tensor index; a segmented warp scan sums the contributions of each run of
+// chunks that belong to one descriptor (the chunk table is in descriptor
+// order), and the last lane of each run adds the run's sums to the output
+// with one 64-bit atomic per sum.  Integer addition mod 2^64 is associative
+// and commutative, so the result is exact and the same on every run.
+// `out` must be zeroed first (descriptors without chunks stay (0, 0)).
+__global__ void fp_combine_kernel(const Chunk *__restrict__ chunks, uint64_t n_chunks,
+                                  const DescDev *__restrict__ descs, const FpPartial *__restrict__ partials,
+                                  unsigned long long *__restrict__ out) {
     const uint32_t lane = threadIdx.x & 31u;
-    const uint64_t warp = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const uint64_t nwarps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
-    for (uint64_t d = warp; d < n_desc; d += nwarps) {
-        const DescDev dd = descs[d];
-        uint64_t S = 0, W = 0;
-        for (uint64_t c = dd.first_chunk + lane; c < dd.first_chunk + dd.n_chunks; c += 32) {
-            const FpPartial p = partials[c];
-            const uint64_t o = (chunks[c].addr - dd.ptr) >> dd.log2es;
-            S += p.s;
-            W += p.w + o * p.s;
+    const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    uint32_t d = 0xFFFFFFFFu;
+    uint64_t S = 0, W = 0;
+    if (i < n_chunks) {
+        const Chunk ch = chunks[i];
+        const FpPartial p = partials[i];
+        d = chunk_desc(ch.tag);
+        const uint64_t o = (ch.addr - descs[d].ptr) >> chunk_log2es(ch.tag);
+        S = p.s;
+        W = p.w + o * p.s;
+    }
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint64_t s_up = __shfl_up_sync(0xffffffffu, S, off);
+        const uint64_t w_up = __shfl_up_sync(0xffffffffu, W, off);
+        const uint32_t d_up = __shfl_up_sync(0xffffffffu, d, off);
+        if (lane >= (uint32_t)off && d_up == d) {
+            S += s_up;
+            W += w_up;
         }
-        S = warp_sum_u64(S);
-        W = warp_sum_u64(W);
-        if (lane == 0) {
-            out[2 * d] = S;
-            out[2 * d + 1] = W;
-        }
+    }
+    const uint32_t d_next = __shfl_down_sync(0xffffffffu, d, 1);
+    if (d != 0xFFFFFFFFu && (lane == 31u || d_next != d)) {
+        atomicAdd(out + 2ull * d, (unsigned long long)S);
+        atomicAdd(out + 2ull * d + 1, (unsigned long long)W);
     }
 }
 
@@ -311,28 +327,28 @@ __global__ void __launch_bounds__(kScanBlock) xor_scan_kernel(const Chunk *__res
     }
 }
 
-__global__ void xor_combine_kernel(const DescDev *__restrict__ descs, uint64_t n_desc,
-                                   const uint64_t *__restrict__ partials, uint64_t *__restrict__ out) {
+// Same second pass for the xorsum: XOR is associative and commutative.
+__global__ void xor_combine_kernel(const Chunk *__restrict__ chunks, uint64_t n_chunks,
+                                   const uint64_t *__restrict__ partials, unsigned long long *__restrict__ out) {
     const uint32_t lane = threadIdx.x & 31u;
-    const uint64_t warp = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const uint64_t nwarps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
-    for (uint64_t d = warp; d < n_desc; d += nwarps) {
-        const DescDev dd = descs[d];
-        uint64_t X = 0;
-        for (uint64_t c = dd.first_chunk + lane; c < dd.first_chunk + dd.n_chunks; c += 32) X ^= partials[c];
-        X = warp_xor_u64(X);
-        if (lane == 0) out[d] = X;
+    const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    uint32_t d = 0xFFFFFFFFu;
+    uint64_t X = 0;
+    if (i < n_chunks) {
+        d = chunk_desc(chunks[i].tag);
+        X = partials[i];
     }
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint64_t x_up = __shfl_up_sync(0xffffffffu, X, off);
+        const uint32_t d_up = __shfl_up_sync(0xffffffffu, d, off);
+        if (lane >= (uint32_t)off && d_up == d) X ^= x_up;
+    }
+    const uint32_t d_next = __shfl_down_sync(0xffffffffu, d, 1);
+    if (d != 0xFFFFFFFFu && (lane == 31u || d_next != d)) atomicXor(out + d, (unsigned long long)X);
 }
 
 constexpr int kFpUnroll = 4;
-
-int combine_grid(uint64_t n_desc, int device) {
-    const uint64_t warps = n_desc;
-    const uint64_t blocks = (warps * 32 + 255) / 256;
-    const uint64_t cap = (uint64_t)sm_count(device) * 8;
-    return (int)(blocks < cap ? (blocks ? blocks : 1) : cap);
-}
 
 }  // namespace
 
@@ -350,8 +366,11 @@ cudaError_t launch_fp_scan(const sdc_plan *plan, FpPartial *partials, cudaStream
 
 cudaError_t launch_fp_combine(const sdc_plan *plan, const FpPartial *partials, uint64_t *out, cudaStream_t st) {
     if (plan->n_desc == 0) return cudaSuccess;
-    fp_combine_kernel<<<combine_grid(plan->n_desc, plan->device), 256, 0, st>>>(plan->d_descs, plan->n_desc,
-                                                                               plan->d_chunks, partials, out);
+    cudaError_t e = cudaMemsetAsync(out, 0, plan->n_desc * 2 * sizeof(uint64_t), st);
+    if (e != cudaSuccess || plan->n_chunks == 0) return e;
+    const unsigned blocks = (unsigned)((plan->n_chunks + 255) / 256);
+    fp_combine_kernel<<<blocks, 256, 0, st>>>(plan->d_chunks, plan->n_chunks, plan->d_descs, partials,
+                                              (unsigned long long *)out);
     return cudaGetLastError();
 }
 
@@ -363,8 +382,11 @@ cudaError_t launch_xor_scan(const sdc_plan *plan, uint64_t *partials, cudaStream
 
 cudaError_t launch_xor_combine(const sdc_plan *plan, const uint64_t *partials, uint64_t *out, cudaStream_t st) {
     if (plan->n_desc == 0) return cudaSuccess;
-    xor_combine_kernel<<<combine_grid(plan->n_desc, plan->device), 256, 0, st>>>(plan->d_descs, plan->n_desc,
-                                                                                partials, out);
+    cudaError_t e = cudaMemsetAsync(out, 0, plan->n_desc * sizeof(uint64_t), st);
+    if (e != cudaSuccess || plan->n_chunks == 0) return e;
+    const unsigned blocks = (unsigned)((plan->n_chunks + 255) / 256);
+    xor_combine_kernel<<<blocks, 256, 0, st>>>(plan->d_chunks, plan->n_chunks, partials,
+                                               (unsigned long long *)out);
     return cudaGetLastError();
 }
 

@@ -362,7 +362,7 @@ __device__ __forceinline__ void store_bits(void *p, uint64_t i, uint32_t v) {
 
 // Vector path: every pointer 16-byte aligned.  Warp task c covers elements
 // [c * CE, min((c + 1) * CE, numel)), CE = kAvgChunkBytes / elem size.
-// Partials: [c][s] for streams s = 0..NB-1 (inputs) and s = NB (average).
+// Partials: [s][c] for streams s = 0..NB-1 (inputs) and s = NB (average).
 template <int DT, int NB, int U>
 __global__ void __launch_bounds__(kScanBlock) avg_scan_kernel(BufPtrs bp, void *__restrict__ outp, uint64_t numel,
                                                               uint64_t n_chunks, StatPartial *__restrict__ partials) {
@@ -439,7 +439,7 @@ __global__ void __launch_bounds__(kScanBlock) avg_scan_kernel(BufPtrs bp, void *
             double acc = __dadd_rn(unscale<DT>(acc_s[s]), acc_e[s]);
             acc = warp_sum_f64(acc);
             const uint32_t nn = warp_sum_u32(n[s].nan), ni = warp_sum_u32(n[s].inf), nbg = warp_sum_u32(n[s].big);
-            if (lane == 0) partials[c * NS + s] = StatPartial{acc, nn, ni, nbg, 0u};
+            if (lane == 0) partials[(uint64_t)s * n_chunks + c] = StatPartial{acc, nn, ni, nbg, 0u};
         }
     }
 }
@@ -475,56 +475,52 @@ __global__ void __launch_bounds__(kScanBlock) avg_scan_elem_kernel(BufPtrs bp, i
             }
             acc = warp_sum_f64(acc);
             const uint32_t nn = warp_sum_u32(n.nan), ni = warp_sum_u32(n.inf), nbg = warp_sum_u32(n.big);
-            if (lane == 0) partials[c * ns + s] = StatPartial{acc, nn, ni, nbg, 0u};
+            if (lane == 0) partials[(uint64_t)s * n_chunks + c] = StatPartial{acc, nn, ni, nbg, 0u};
         }
     }
 }
 
 // ---------------------------------------------------------------- combine
-// One CTA per stream: fixed-order sum of the stream's partials (thread t takes
-// partials t, t + B, ...; then a fixed tree), then the derived fields.
-constexpr int kCombineBlock = 512;
+// Two fixed-shape passes per stream, so the float64 sum has the same
+// association on every run whatever the grid: pass 1 splits a stream's
+// partials into kGroups contiguous ranges (range bounds depend only on the
+// count), one CTA per (stream, group) summing its range in a fixed order
+// (thread t takes t, t + B, ...; then a fixed tree); pass 2 sums the kGroups
+// group results of each stream in a fixed tree and writes the derived fields.
+constexpr int kCombineBlock = 256;
 
 struct StreamSel {
     const uint64_t *first;  // plan mode: R + 1 chunk offsets; null in buffer mode
     const uint64_t *numel_arr;
-    uint64_t n_chunks;      // buffer mode: chunks per stream
+    uint64_t n_chunks;      // buffer mode: chunks per stream (partials are stream-major)
     uint64_t numel;         // buffer mode: elements per stream
     uint32_t n_streams;
     uint32_t n_pre;         // buffer mode: streams written to out_pre (the rest to out_post)
 };
 
-__global__ void __launch_bounds__(kCombineBlock) stats_combine_kernel(const StatPartial *__restrict__ partials,
-                                                                      StreamSel sel, sdc_grad_stats *out_pre,
-                                                                      sdc_grad_stats *out_post) {
-    const uint32_t s = blockIdx.x;
-    uint64_t base, count, stride, numel;
+__device__ __forceinline__ void stream_range(const StreamSel &sel, uint32_t s, uint64_t &base, uint64_t &count) {
     if (sel.first) {
         base = sel.first[s];
         count = sel.first[s + 1] - base;
-        stride = 1;
-        numel = sel.numel_arr[s];
     } else {
-        base = s;
+        base = (uint64_t)s * sel.n_chunks;
         count = sel.n_chunks;
-        stride = sel.n_streams;
-        numel = sel.numel;
     }
-    double acc = 0.0;
-    unsigned long long nn = 0, ni = 0, nb = 0;
-    for (uint64_t i = threadIdx.x; i < count; i += kCombineBlock) {
-        const StatPartial p = partials[base + i * stride];
-        acc = __dadd_rn(acc, p.sumsq);
-        nn += p.n_nan;
-        ni += p.n_inf;
-        nb += p.n_big;
-    }
+}
+
+struct Acc {
+    double sum;
+    unsigned long long nan, inf, big;
+};
+
+// Fixed-shape block reduction of one Acc per thread; result valid in thread 0.
+__device__ __forceinline__ Acc block_reduce(Acc a) {
     __shared__ double sa[kCombineBlock];
     __shared__ unsigned long long sn[3][kCombineBlock];
-    sa[threadIdx.x] = acc;
-    sn[0][threadIdx.x] = nn;
-    sn[1][threadIdx.x] = ni;
-    sn[2][threadIdx.x] = nb;
+    sa[threadIdx.x] = a.sum;
+    sn[0][threadIdx.x] = a.nan;
+    sn[1][threadIdx.x] = a.inf;
+    sn[2][threadIdx.x] = a.big;
     __syncthreads();
     for (int h = kCombineBlock / 2; h > 0; h >>= 1) {
         if ((int)threadIdx.x < h) {
@@ -535,21 +531,65 @@ __global__ void __launch_bounds__(kCombineBlock) stats_combine_kernel(const Stat
         }
         __syncthreads();
     }
+    return Acc{sa[0], sn[0][0], sn[1][0], sn[2][0]};
+}
+
+__global__ void __launch_bounds__(kCombineBlock) stats_combine1_kernel(const StatPartial *__restrict__ partials,
+                                                                       StreamSel sel, StatPartial *__restrict__ groups) {
+    const uint32_t s = blockIdx.y, g = blockIdx.x;
+    uint64_t base, count;
+    stream_range(sel, s, base, count);
+    const uint64_t lo = base + count * g / kStatGroups, hi = base + count * (g + 1) / kStatGroups;
+    Acc a{0.0, 0, 0, 0};
+    for (uint64_t i = lo + threadIdx.x; i < hi; i += kCombineBlock) {
+        const StatPartial p = partials[i];
+        a.sum = __dadd_rn(a.sum, p.sumsq);
+        a.nan += p.n_nan;
+        a.inf += p.n_inf;
+        a.big += p.n_big;
+    }
+    a = block_reduce(a);
+    if (threadIdx.x == 0)
+        groups[(uint64_t)s * kStatGroups + g] = StatPartial{a.sum, (uint32_t)a.nan, (uint32_t)a.inf, (uint32_t)a.big, 0u};
+}
+
+__global__ void __launch_bounds__(kCombineBlock) stats_combine2_kernel(const StatPartial *__restrict__ groups,
+                                                                       StreamSel sel, sdc_grad_stats *out_pre,
+                                                                       sdc_grad_stats *out_post) {
+    const uint32_t s = blockIdx.x;
+    Acc a{0.0, 0, 0, 0};
+    for (uint32_t g = threadIdx.x; g < kStatGroups; g += kCombineBlock) {
+        const StatPartial p = groups[(uint64_t)s * kStatGroups + g];
+        a.sum = __dadd_rn(a.sum, p.sumsq);
+        a.nan += p.n_nan;
+        a.inf += p.n_inf;
+        a.big += p.n_big;
+    }
+    a = block_reduce(a);
     if (threadIdx.x == 0) {
         sdc_grad_stats r;
-        r.n_nan = sn[0][0];
-        r.n_inf = sn[1][0];
-        r.n_big = sn[2][0];
-        r.n_elems = numel;
-        r.sumsq_finite = sa[0];
+        r.n_nan = a.nan;
+        r.n_inf = a.inf;
+        r.n_big = a.big;
+        r.n_elems = sel.first ? sel.numel_arr[s] : sel.numel;
+        r.sumsq_finite = a.sum;
         if (r.n_nan) r.norm = __longlong_as_double(0x7FF8000000000000ll);
         else if (r.n_inf) r.norm = __longlong_as_double(0x7FF0000000000000ll);
-        else r.norm = __dsqrt_rn(sa[0]);
-        r.nonfinite_fp32 = (r.n_nan || r.n_inf || sa[0] > kFltMax) ? 1u : 0u;
+        else r.norm = __dsqrt_rn(a.sum);
+        r.nonfinite_fp32 = (r.n_nan || r.n_inf || a.sum > kFltMax) ? 1u : 0u;
         r.reserved = 0;
         sdc_grad_stats *dst = sel.first ? out_pre + s : (s < sel.n_pre ? out_pre + s : out_post);
         *dst = r;
     }
+}
+
+cudaError_t launch_combine(const StatPartial *partials, StatPartial *groups, const StreamSel &sel,
+                           sdc_grad_stats *out_pre, sdc_grad_stats *out_post, cudaStream_t st) {
+    stats_combine1_kernel<<<dim3(kStatGroups, sel.n_streams), kCombineBlock, 0, st>>>(partials, sel, groups);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    stats_combine2_kernel<<<sel.n_streams, kCombineBlock, 0, st>>>(groups, sel, out_pre, out_post);
+    return cudaGetLastError();
 }
 
 constexpr int kGradUnroll = 4;
@@ -600,11 +640,10 @@ cudaError_t launch_grad_scan(const sdc_plan *plan, StatPartial *partials, cudaSt
     return cudaGetLastError();
 }
 
-cudaError_t launch_stats_combine_plan(const sdc_plan *plan, const StatPartial *partials, sdc_grad_stats *out,
-                                      cudaStream_t st) {
+cudaError_t launch_stats_combine_plan(const sdc_plan *plan, const StatPartial *partials, StatPartial *groups,
+                                      sdc_grad_stats *out, cudaStream_t st) {
     StreamSel sel{plan->d_replica_first_chunk, plan->d_replica_numel, 0, 0, plan->R, plan->R};
-    stats_combine_kernel<<<plan->R, kCombineBlock, 0, st>>>(partials, sel, out, out);
-    return cudaGetLastError();
+    return launch_combine(partials, groups, sel, out, out, st);
 }
 
 cudaError_t launch_avg_scan(const void *const *bufs, uint32_t n_bufs, void *avg, uint64_t numel, uint32_t dtype,
@@ -637,12 +676,11 @@ cudaError_t launch_avg_scan(const void *const *bufs, uint32_t n_bufs, void *avg,
     return cudaGetLastError();
 }
 
-cudaError_t launch_stats_combine_streams(const StatPartial *partials, uint32_t n_streams, uint64_t n_chunks,
-                                         uint64_t numel, sdc_grad_stats *out_pre, sdc_grad_stats *out_post,
-                                         cudaStream_t st) {
+cudaError_t launch_stats_combine_streams(const StatPartial *partials, StatPartial *groups, uint32_t n_streams,
+                                         uint64_t n_chunks, uint64_t numel, sdc_grad_stats *out_pre,
+                                         sdc_grad_stats *out_post, cudaStream_t st) {
     StreamSel sel{nullptr, nullptr, n_chunks, numel, n_streams, n_streams - 1};
-    stats_combine_kernel<<<n_streams, kCombineBlock, 0, st>>>(partials, sel, out_pre, out_post);
-    return cudaGetLastError();
+    return launch_combine(partials, groups, sel, out_pre, out_post, st);
 }
 
 }  // namespace sdc

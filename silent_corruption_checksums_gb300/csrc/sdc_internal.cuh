@@ -102,12 +102,12 @@ cudaError_t launch_xor_scan(const sdc_plan *plan, uint64_t *partials, cudaStream
 cudaError_t launch_xor_combine(const sdc_plan *plan, const uint64_t *partials, uint64_t *out,
                                cudaStream_t st);
 cudaError_t launch_grad_scan(const sdc_plan *plan, StatPartial *partials, cudaStream_t st);
-cudaError_t launch_stats_combine_plan(const sdc_plan *plan, const StatPartial *partials,
+cudaError_t launch_stats_combine_plan(const sdc_plan *plan, const StatPartial *partials, StatPartial *groups,
                                       sdc_grad_stats *out, cudaStream_t st);
 cudaError_t launch_avg_scan(const void *const *bufs, uint32_t n_bufs, void *avg, uint64_t numel,
                             uint32_t dtype, StatPartial *partials, uint64_t n_chunks, bool vector_path,
                             int device, cudaStream_t st);
-cudaError_t launch_stats_combine_streams(const StatPartial *partials, uint32_t n_streams,
+cudaError_t launch_stats_combine_streams(const StatPartial *partials, StatPartial *groups, uint32_t n_streams,
                                          uint64_t n_chunks, uint64_t numel, sdc_grad_stats *out_pre,
                                          sdc_grad_stats *out_post, cudaStream_t st);
 cudaError_t launch_vote(const uint64_t *fp, uint32_t R, uint32_t T, int32_t *suspect, uint64_t *mask,
@@ -120,8 +120,10 @@ constexpr int kScanBlock = 256;
 int fp_scan_blocks_per_sm();
 int grad_scan_blocks_per_sm();
 
-// Elements of one warp task in the fused average scan (per stream).
+// Bytes of one warp task in the fused average scan (per stream).
 constexpr uint64_t kAvgChunkBytes = 16384;
+// Fixed number of first-pass groups per stream in the statistics combine.
+constexpr uint32_t kStatGroups = 128;
 
 }  // namespace sdc
 
