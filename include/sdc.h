@@ -235,6 +235,32 @@ sdc_status sdc_grad_average_scan(const void *const *bufs, uint32_t n_bufs, void 
                                  uint32_t dtype, sdc_grad_stats *d_pre, sdc_grad_stats *d_post,
                                  void *d_ws, size_t ws_bytes, sdc_stream_t stream);
 
+/* Size of the library's fixed device scratch used by
+ * sdc_grad_average_scan_noalloc (16 MiB on every GPU that loads libsdc). */
+#define SDC_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* sdc_grad_average_scan without a workspace argument and without any device
+ * allocation.  (The pages have no counterpart: this is an interface choice of
+ * this library, not a step of the method.)  It is for callers that cannot
+ * call cudaMalloc or take memory from a caching allocator -- code running in
+ * a host callback or inside an allocator's hooks, a tool injected into a job
+ * whose device memory is owned and capped by another framework -- but still
+ * want the non-finite scan and average of their gradient buffers.
+ * Arguments, results and errors are those of sdc_grad_average_scan.  The
+ * scratch is a fixed __device__ array of SDC_NOALLOC_SCRATCH_BYTES inside the
+ * library: sizes whose sdc_grad_average_scan_workspace_size(numel, n_bufs,
+ * dtype) exceeds it are rejected with SDC_ERR_BAD_ARG and a message giving
+ * the limit (with 4 bf16 buffers that is about 1.14e9 elements).  The first
+ * call on each device looks up the array's device address (a
+ * cudaGetSymbolAddress with that device current) and caches it; make that
+ * first call before any stream capture.  All calls share the one array and
+ * it keeps the last call's contents (nothing in it needs to start at zero):
+ * calls whose GPU work overlaps -- on different streams, or from several host
+ * threads -- race on it and must be ordered by the caller. */
+sdc_status sdc_grad_average_scan_noalloc(const void *const *bufs, uint32_t n_bufs, void *d_avg, uint64_t numel,
+                                         uint32_t dtype, sdc_grad_stats *d_pre, sdc_grad_stats *d_post,
+                                         sdc_stream_t stream);
+
 /* ---------------------------------------------------------------- errors */
 
 /* Static name of a status code. */

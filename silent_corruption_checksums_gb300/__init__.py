@@ -20,14 +20,14 @@ import os
 
 import numpy as np
 
-from .build import LIB_PATH
+from .build import LIB_PATH, is_stale
 
 __all__ = [
     "SdcError", "DTYPE_RAW", "DTYPE_F32", "DTYPE_BF16", "DTYPE_F16", "MAX_REPLICAS",
     "SUSPECT_AGREE", "SUSPECT_SEVERAL", "SUSPECT_NO_MAJORITY", "GRAD_STATS_DTYPE", "VOTE_SUMMARY_DTYPE",
     "sdc_plan_create", "sdc_plan_destroy", "sdc_workspace_size", "sdc_plan_info", "sdc_fingerprint",
     "sdc_xorsum", "sdc_xorsum_compare", "sdc_vote", "sdc_grad_scan", "sdc_grad_average_scan_workspace_size",
-    "sdc_grad_average_scan", "sdc_status_string", "sdc_last_error", "Plan", "vote", "xorsum_compare",
+    "sdc_grad_average_scan", "sdc_grad_average_scan_noalloc", "NOALLOC_SCRATCH_BYTES", "sdc_status_string", "sdc_last_error", "Plan", "vote", "xorsum_compare",
     "grad_average_scan", "decode_stats", "decode_summary", "pages_verdict", "library_path",
 ]
 
@@ -62,6 +62,9 @@ def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"libsdc.so not found at {LIB_PATH}; build it with "
                           "`python -m silent_corruption_checksums_gb300.build` (needs nvcc)")
+    if is_stale():
+        raise ImportError(f"libsdc.so at {LIB_PATH} is older than its sources; rebuild it with "
+                          "`python -m silent_corruption_checksums_gb300.build`")
     lib = ctypes.CDLL(LIB_PATH)
     vp, u64, u32, sz = ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_size_t
     sig = {
@@ -76,6 +79,7 @@ def _load() -> ctypes.CDLL:
         "sdc_grad_scan": ([vp, vp, vp, sz, vp], ctypes.c_int),
         "sdc_grad_average_scan_workspace_size": ([u64, u32, u32], sz),
         "sdc_grad_average_scan": ([ctypes.POINTER(vp), u32, vp, u64, u32, vp, vp, vp, sz, vp], ctypes.c_int),
+        "sdc_grad_average_scan_noalloc": ([ctypes.POINTER(vp), u32, vp, u64, u32, vp, vp, vp], ctypes.c_int),
         "sdc_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "sdc_last_error": ([], ctypes.c_char_p),
     }
@@ -181,6 +185,17 @@ def sdc_grad_average_scan(bufs: list[int], d_avg: int, numel: int, dtype: int, d
     arr = (ctypes.c_void_p * max(1, len(bufs)))(*bufs)
     _check("sdc_grad_average_scan", _lib.sdc_grad_average_scan(arr, len(bufs), d_avg, numel, dtype, d_pre,
                                                                d_post, d_ws, ws_bytes, stream))
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def sdc_grad_average_scan_noalloc(bufs: list[int], d_avg: int, numel: int, dtype: int, d_pre: int, d_post: int,
+                                  stream: int) -> None:
+    """The average-scan on the library's fixed device scratch (no workspace, no allocation)."""
+    arr = (ctypes.c_void_p * max(1, len(bufs)))(*bufs)
+    _check("sdc_grad_average_scan_noalloc", _lib.sdc_grad_average_scan_noalloc(arr, len(bufs), d_avg, numel, dtype,
+                                                                               d_pre, d_post, stream))
 
 
 # ---------------------------------------------------------------- torch conveniences
