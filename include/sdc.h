@@ -101,10 +101,7 @@ typedef struct sdc_plan sdc_plan;
  *        any element is +-Inf (IEEE propagation, as clip_grad_norm_ reports);
  *  nonfinite_fp32: 1 if the float32 squared norm would not be finite:
  *        n_nan > 0 or n_inf > 0 or sumsq_finite > FLT_MAX -- [AWS] "Decide
- *        what the alarm means": a norm above about 1.8e19 counts as non-finite;
- *  aborted: 0 normally; 1 if a kernel of the call gave up waiting for its own
- *        staged copies (a bounded wait ran out) -- the other fields are then
- *        incomplete and the call should be treated as failed. */
+ *        what the alarm means": a norm above about 1.8e19 counts as non-finite. */
 typedef struct {
     uint64_t n_nan;
     uint64_t n_inf;
@@ -113,7 +110,7 @@ typedef struct {
     double sumsq_finite;
     double norm;
     uint32_t nonfinite_fp32;
-    uint32_t aborted;
+    uint32_t reserved;
 } sdc_grad_stats;
 
 /* Vote summary.  diverged: some tensor's copies differ; no_majority: some

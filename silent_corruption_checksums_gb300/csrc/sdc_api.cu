@@ -148,9 +148,9 @@ sdc_status check_ws(const void *ws, size_t ws_bytes, size_t need) {
 
 // Workspace: per-chunk partials, then the statistics combine's group sums.
 size_t plan_partials_bytes(const sdc_plan *p) { return round_up((size_t)p->n_chunks * sizeof(StatPartial), 256); }
-size_t plan_groups_bytes(const sdc_plan *p) { return round_up((size_t)p->R * kStatGroups * sizeof(StatPartial), 256); }
-// ... and one 256-byte slot holding the call's abort flag.
-size_t plan_ws_bytes(const sdc_plan *p) { return plan_partials_bytes(p) + plan_groups_bytes(p) + 256; }
+size_t plan_ws_bytes(const sdc_plan *p) {
+    return plan_partials_bytes(p) + round_up((size_t)p->R * kStatGroups * sizeof(StatPartial), 256);
+}
 
 size_t avg_chunks(uint64_t numel, uint32_t dtype) {
     const uint64_t es = dtype == SDC_DTYPE_F32 ? 4 : 2;
@@ -419,10 +419,8 @@ sdc_status sdc_grad_scan(const sdc_plan *plan, sdc_grad_stats *d_stats, void *d_
     cudaStream_t s = (cudaStream_t)stream;
     StatPartial *part = (StatPartial *)d_ws;
     StatPartial *groups = (StatPartial *)((char *)d_ws + plan_partials_bytes(plan));
-    int *err = (int *)((char *)d_ws + plan_partials_bytes(plan) + plan_groups_bytes(plan));
-    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int), s);
-    if (e == cudaSuccess) e = launch_grad_scan(plan, part, err, s);
-    if (e == cudaSuccess) e = launch_stats_combine_plan(plan, part, groups, err, d_stats, s);
+    cudaError_t e = launch_grad_scan(plan, part, s);
+    if (e == cudaSuccess) e = launch_stats_combine_plan(plan, part, groups, d_stats, s);
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_grad_scan launch");
 }
 
@@ -431,7 +429,7 @@ size_t sdc_grad_average_scan_workspace_size(uint64_t numel, uint32_t n_bufs, uin
     if (dtype != SDC_DTYPE_F32 && dtype != SDC_DTYPE_BF16 && dtype != SDC_DTYPE_F16) return 0;
     const size_t nc = avg_chunks(numel, dtype);
     return round_up(nc * (n_bufs + 1) * sizeof(StatPartial), 256) +
-           round_up((size_t)(n_bufs + 1) * kStatGroups * sizeof(StatPartial), 256) + 256;
+           round_up((size_t)(n_bufs + 1) * kStatGroups * sizeof(StatPartial), 256);
 }
 
 sdc_status sdc_grad_average_scan(const void *const *bufs, uint32_t n_bufs, void *d_avg, uint64_t numel,
@@ -466,14 +464,9 @@ sdc_status sdc_grad_average_scan(const void *const *bufs, uint32_t n_bufs, void 
     if (st != SDC_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     StatPartial *part = (StatPartial *)d_ws;
-    const size_t part_bytes = round_up(nc * (n_bufs + 1) * sizeof(StatPartial), 256);
-    StatPartial *groups = (StatPartial *)((char *)d_ws + part_bytes);
-    int *err = (int *)((char *)d_ws + part_bytes +
-                       round_up((size_t)(n_bufs + 1) * kStatGroups * sizeof(StatPartial), 256));
-    e = cudaMemsetAsync(err, 0, sizeof(int), s);
-    if (e == cudaSuccess) e = launch_avg_scan(bufs, n_bufs, d_avg, numel, dtype, part, nc, aligned, err, dev, s);
-    if (e == cudaSuccess)
-        e = launch_stats_combine_streams(part, groups, err, n_bufs + 1, nc, numel, d_pre, d_post, s);
+    StatPartial *groups = (StatPartial *)((char *)d_ws + round_up(nc * (n_bufs + 1) * sizeof(StatPartial), 256));
+    e = launch_avg_scan(bufs, n_bufs, d_avg, numel, dtype, part, nc, aligned, dev, s);
+    if (e == cudaSuccess) e = launch_stats_combine_streams(part, groups, n_bufs + 1, nc, numel, d_pre, d_post, s);
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_grad_average_scan launch");
 }
 

@@ -33,9 +33,6 @@
 // overflowing sum) or that holds a tiny f32 value is redone exactly: each
 // element classified and its square added in float64 (exact squares).
 // All reductions have a fixed shape, so results are identical on every run.
-// Data reaches the warps through warp-private rings of bulk-copy stages (see
-// avg_scan_kernel); a wait that gives up sets the call's abort flag, which the
-// combine reports in sdc_grad_stats.aborted.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -181,77 +178,23 @@ __device__ __forceinline__ GGeom ggeom(const Chunk &ch) {
     return g;
 }
 
-// Warp-private ring of bulk-copy stages over the warp's chunks of a plan
-// (one 512-byte slice of a chunk's aligned body per stage).
-constexpr int kGRing = 8;
-constexpr uint32_t kGSlice = 512;
-
-struct GradRing {
-    uint32_t ring, bars;     // shared addresses of the stages and their mbarriers
-    uint64_t pc, nwarps, n_chunks, issued, consumed;
-    uint32_t pi;
-    GGeom pg;                // geometry of chunk pc (lane 0)
-    uint64_t pg_of;          // chunk whose geometry pg holds
-    const Chunk *chunks;
-
-    __device__ void produce() {
-        while (pc < n_chunks) {
-            if (pg_of != pc) {
-                pg = ggeom(chunks[pc]);
-                pg_of = pc;
-            }
-            if (pi < ((pg.nvec + 31) >> 5)) {
-                const uint32_t q = (uint32_t)(issued % kGRing);
-                const uint32_t bytes = min(kGSlice, (pg.nvec - (pi << 5)) * 16u);
-                const uint32_t mb = bars + 8 * q;
-                fence_proxy_async_smem();
-                mbar_arrive_expect_tx(mb, bytes);
-                bulk_g2s(ring + q * kGSlice, (const char *)(pg.addr + pg.head) + (uint64_t)pi * kGSlice, bytes, mb);
-                ++pi;
-                ++issued;
-                return;
-            }
-            pc += nwarps;
-            pi = 0;
-        }
-    }
-    // Wait for the next stage; false (uniform over the warp) if the wait gave up.
-    __device__ bool wait_next(uint32_t &q) {
-        q = (uint32_t)(consumed % kGRing);
-        const bool got = mbar_wait(bars + 8 * q, (uint32_t)((consumed / kGRing) & 1));
-        return !__any_sync(0xffffffffu, !got);
-    }
-    __device__ void release(uint32_t lane) {
-        __syncwarp();
-        ++consumed;
-        if (lane == 0) produce();
-    }
-    __device__ void abandon(uint32_t lane, int *err) {
-        if (lane == 0) {
-            atomicOr(err, 1);
-            for (uint64_t k = consumed; k < issued; ++k)
-                mbar_wait(bars + 8 * (uint32_t)(k % kGRing), (uint32_t)((k / kGRing) & 1));
-        }
-        __syncwarp();
-    }
-};
-
-// One chunk of a gradient scan from the ring; returns false if a wait gave up.
-template <int DT>
-__device__ __forceinline__ bool grad_chunk(const GGeom &g, uint32_t lane, GradRing &rg, double &acc_out, Counts &n) {
+template <int DT, int U>
+__device__ __forceinline__ double grad_chunk(const GGeom &g, uint32_t lane, Counts &n) {
     const uint4 *vb = (const uint4 *)(g.addr + g.head);
     const uint32_t niter = (g.nvec + 31) >> 5;
     double acc_scaled = 0.0, acc_exact = 0.0;
     for (uint32_t r0 = 0; r0 < niter; r0 += kRunVec) {
         const uint32_t r1 = min(r0 + (uint32_t)kRunVec, niter);
         FastAcc a;
-        for (uint32_t i = r0; i < r1; ++i) {
-            uint32_t q;
-            if (!rg.wait_next(q)) return false;
-            const uint32_t vi = lane + (i << 5);
-            const uint4 v = vi < g.nvec ? ld_shared_v4(rg.ring + q * kGSlice + lane * 16u) : make_uint4(0, 0, 0, 0);
-            rg.release(lane);
-            fast_vec<DT>(v, a);
+        for (uint32_t i0 = r0; i0 < r1; i0 += U) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const uint32_t vi = lane + ((i0 + u) << 5);
+                v[u] = (i0 + u < r1 && vi < g.nvec) ? ld_stream(vb + vi) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) fast_vec<DT>(v[u], a);
         }
         if (!fast_flush<DT>(a, acc_scaled)) {
             for (uint32_t i = r0; i < r1; ++i) {
@@ -271,49 +214,24 @@ __device__ __forceinline__ bool grad_chunk(const GGeom &g, uint32_t lane, GradRi
         const uint32_t bits = g.l2 == 2 ? *(const uint32_t *)a : (uint32_t)(*(const uint16_t *)a);
         exact_elem(bits, DT, acc_exact, n);
     }
-    acc_out = __dadd_rn(unscale<DT>(acc_scaled), acc_exact);
-    return true;
+    return __dadd_rn(unscale<DT>(acc_scaled), acc_exact);
 }
 
-constexpr uint32_t grad_warp_smem() { return kGRing * kGSlice + kGRing * 8; }
-
+template <int U>
 __global__ void __launch_bounds__(kScanBlock) grad_scan_kernel(const Chunk *__restrict__ chunks, uint64_t n_chunks,
-                                                               StatPartial *__restrict__ partials, int *__restrict__ err) {
-    extern __shared__ __align__(128) unsigned char smem[];
-    const uint32_t lane = threadIdx.x & 31u, wib = threadIdx.x >> 5;
-    GradRing rg;
-    rg.ring = smem_addr(smem + wib * (kGRing * kGSlice));
-    rg.bars = smem_addr(smem + (blockDim.x >> 5) * (kGRing * kGSlice)) + wib * (kGRing * 8);
-    if (lane == 0) {
-        for (int q = 0; q < kGRing; ++q) mbar_init(rg.bars + 8 * q, 1);
-        fence_mbar_init();
-    }
-    __syncwarp();
+                                                               StatPartial *__restrict__ partials) {
+    const uint32_t lane = threadIdx.x & 31u;
     const uint64_t warp = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    rg.nwarps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
-    rg.n_chunks = n_chunks;
-    rg.chunks = chunks;
-    rg.pc = warp;
-    rg.pi = 0;
-    rg.pg_of = ~0ull;
-    rg.issued = rg.consumed = 0;
-    if (lane == 0)
-        for (int k = 0; k < kGRing; ++k) rg.produce();
-    __syncwarp();
-    for (uint64_t c = warp; c < n_chunks; c += rg.nwarps) {
+    const uint64_t nwarps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
+    for (uint64_t c = warp; c < n_chunks; c += nwarps) {
         const Chunk ch = chunks[c];
         const GGeom g = ggeom(ch);
         Counts n;
-        double acc = 0.0;
-        bool ok;
+        double acc;
         switch (chunk_dtype(ch.tag)) {
-            case SDC_DTYPE_F32: ok = grad_chunk<SDC_DTYPE_F32>(g, lane, rg, acc, n); break;
-            case SDC_DTYPE_BF16: ok = grad_chunk<SDC_DTYPE_BF16>(g, lane, rg, acc, n); break;
-            default: ok = grad_chunk<SDC_DTYPE_F16>(g, lane, rg, acc, n); break;
-        }
-        if (!ok) {
-            rg.abandon(lane, err);
-            return;
+            case SDC_DTYPE_F32: acc = grad_chunk<SDC_DTYPE_F32, U>(g, lane, n); break;
+            case SDC_DTYPE_BF16: acc = grad_chunk<SDC_DTYPE_BF16, U>(g, lane, n); break;
+            default: acc = grad_chunk<SDC_DTYPE_F16, U>(g, lane, n); break;
         }
         acc = warp_sum_f64(acc);
         const uint32_t nn = warp_sum_u32(n.nan), ni = warp_sum_u32(n.inf), nb = warp_sum_u32(n.big);
@@ -445,86 +363,16 @@ __device__ __forceinline__ void store_bits(void *p, uint64_t i, uint32_t v) {
 // Vector path: every pointer 16-byte aligned.  Warp task c covers elements
 // [c * CE, min((c + 1) * CE, numel)), CE = kAvgChunkBytes / elem size.
 // Partials: [s][c] for streams s = 0..NB-1 (inputs) and s = NB (average).
-//
-// Data movement: each warp owns a ring of kRing shared-memory stages; stage
-// k holds one 512-byte slice (one 16-byte vector per lane) of every input for
-// the warp's k-th iteration, filled by NB bulk copies (cp.async.bulk) that
-// complete on the stage's mbarrier.  Lane 0 refills a stage as soon as the
-// warp has read it, so up to kRing - 1 iterations of every input are in
-// flight while the warp computes -- memory latency is hidden without extra
-// registers.  The lane -> vector mapping, the run boundaries and the flush
-// points are those of a plain load loop, so the results do not depend on the
-// staging.
-constexpr int kRing = 6;
-constexpr uint32_t kSlice = 512;  // bytes of one stream in one stage
-
-template <int NB>
-constexpr uint32_t avg_warp_smem() {
-    return kRing * NB * kSlice + kRing * 8;
-}
-
-template <int DT, int NB>
+template <int DT, int NB, int U>
 __global__ void __launch_bounds__(kScanBlock) avg_scan_kernel(BufPtrs bp, void *__restrict__ outp, uint64_t numel,
-                                                              uint64_t n_chunks, StatPartial *__restrict__ partials,
-                                                              int *__restrict__ err) {
+                                                              uint64_t n_chunks, StatPartial *__restrict__ partials) {
     constexpr int NS = NB + 1;
     constexpr uint32_t ES = DT == SDC_DTYPE_F32 ? 4u : 2u;
     constexpr uint64_t CE = kAvgChunkBytes / ES;
-    constexpr uint32_t STAGE = NB * kSlice;
-    extern __shared__ __align__(128) unsigned char smem[];
     const float inv = 1.0f / (float)NB;
-    const uint32_t lane = threadIdx.x & 31u, wib = threadIdx.x >> 5;
-    const uint32_t ring = smem_addr(smem + wib * (kRing * STAGE));
-    const uint32_t bars = smem_addr(smem + (blockDim.x >> 5) * (kRing * STAGE)) + wib * (kRing * 8);
-    if (lane == 0) {
-        for (int q = 0; q < kRing; ++q) mbar_init(bars + 8 * q, 1);
-        fence_mbar_init();
-    }
-    __syncwarp();
+    const uint32_t lane = threadIdx.x & 31u;
     const uint64_t warp = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const uint64_t nwarps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
-
-    // producer cursor (used by lane 0): next chunk and iteration to stage
-    uint64_t pc = warp, issued = 0, consumed = 0;
-    uint32_t pi = 0;
-    auto vecs_of = [&](uint64_t c) -> uint32_t {
-        const uint64_t ne = min(CE, numel - c * CE);
-        return (uint32_t)((ne * ES) >> 4);
-    };
-    auto produce = [&]() {
-        while (pc < n_chunks) {
-            const uint32_t nv = vecs_of(pc);
-            if (pi < ((nv + 31) >> 5)) {
-                const uint32_t q = (uint32_t)(issued % kRing);
-                const uint32_t bytes = min(kSlice, (nv - (pi << 5)) * 16u);
-                const uint32_t mb = bars + 8 * q;
-                const uint64_t off = pc * CE * ES + (uint64_t)pi * kSlice;
-                fence_proxy_async_smem();
-                mbar_arrive_expect_tx(mb, NB * bytes);
-#pragma unroll
-                for (int b = 0; b < NB; ++b)
-                    bulk_g2s(ring + q * STAGE + b * kSlice, (const char *)bp.p[b] + off, bytes, mb);
-                ++pi;
-                ++issued;
-                return;
-            }
-            pc += nwarps;
-            pi = 0;
-        }
-    };
-    // give up: flag the error, let the copies already issued land, stop
-    auto abandon = [&]() {
-        if (lane == 0) {
-            atomicOr(err, 1);
-            for (uint64_t k = consumed; k < issued; ++k)
-                mbar_wait(bars + 8 * (uint32_t)(k % kRing), (uint32_t)((k / kRing) & 1));
-        }
-        __syncwarp();
-    };
-    if (lane == 0)
-        for (int k = 0; k < kRing; ++k) produce();
-    __syncwarp();
-
     for (uint64_t c = warp; c < n_chunks; c += nwarps) {
         const uint64_t e0 = c * CE;
         const uint64_t ne = min(CE, numel - e0);
@@ -541,31 +389,29 @@ __global__ void __launch_bounds__(kScanBlock) avg_scan_kernel(BufPtrs bp, void *
         for (uint32_t r0 = 0; r0 < niter; r0 += kRunVec) {
             const uint32_t r1 = min(r0 + (uint32_t)kRunVec, niter);
             FastAcc a[NS];
-            for (uint32_t i = r0; i < r1; ++i) {
-                const uint32_t q = (uint32_t)(consumed % kRing);
-                const bool got = mbar_wait(bars + 8 * q, (uint32_t)((consumed / kRing) & 1));
-                if (__any_sync(0xffffffffu, !got)) {
-                    abandon();
-                    return;
-                }
-                const uint32_t vi = lane + (i << 5);
-                const bool ok = vi < nvec;
-                uint4 v[NB];
+            for (uint32_t i0 = r0; i0 < r1; i0 += U) {
+                uint4 v[U][NB];
 #pragma unroll
-                for (int b = 0; b < NB; ++b)
-                    v[b] = ok ? ld_shared_v4(ring + q * STAGE + b * kSlice + lane * 16u) : make_uint4(0, 0, 0, 0);
-                __syncwarp();
-                ++consumed;
-                if (lane == 0) produce();  // refill the stage just read
+                for (int u = 0; u < U; ++u) {
+                    const uint32_t vi = lane + ((i0 + u) << 5);
+                    const bool ok = i0 + u < r1 && vi < nvec;
 #pragma unroll
-                for (int b = 0; b < NB; ++b) fast_vec<DT>(v[b], a[b]);
-                uint4 o = avg_vec<DT, NB>(v, inv);
-                if (ok) {
-                    __stcs(out + vi, o);
-                } else {
-                    o = make_uint4(0, 0, 0, 0);
+                    for (int b = 0; b < NB; ++b) v[u][b] = ok ? ld_stream(in[b] + vi) : make_uint4(0, 0, 0, 0);
                 }
-                fast_vec<DT>(o, a[NB]);
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const uint32_t vi = lane + ((i0 + u) << 5);
+                    const bool ok = i0 + u < r1 && vi < nvec;
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) fast_vec<DT>(v[u][b], a[b]);
+                    uint4 o = avg_vec<DT, NB>(v[u], inv);
+                    if (ok) {
+                        __stcs(out + vi, o);
+                    } else {
+                        o = make_uint4(0, 0, 0, 0);
+                    }
+                    fast_vec<DT>(o, a[NB]);
+                }
             }
 #pragma unroll
             for (int s = 0; s < NS; ++s) {
@@ -708,8 +554,7 @@ __global__ void __launch_bounds__(kCombineBlock) stats_combine1_kernel(const Sta
 }
 
 __global__ void __launch_bounds__(kCombineBlock) stats_combine2_kernel(const StatPartial *__restrict__ groups,
-                                                                       StreamSel sel, const int *__restrict__ err,
-                                                                       sdc_grad_stats *out_pre,
+                                                                       StreamSel sel, sdc_grad_stats *out_pre,
                                                                        sdc_grad_stats *out_post) {
     const uint32_t s = blockIdx.x;
     Acc a{0.0, 0, 0, 0};
@@ -732,89 +577,86 @@ __global__ void __launch_bounds__(kCombineBlock) stats_combine2_kernel(const Sta
         else if (r.n_inf) r.norm = __longlong_as_double(0x7FF0000000000000ll);
         else r.norm = __dsqrt_rn(a.sum);
         r.nonfinite_fp32 = (r.n_nan || r.n_inf || a.sum > kFltMax) ? 1u : 0u;
-        r.aborted = *err != 0 ? 1u : 0u;
+        r.reserved = 0;
         sdc_grad_stats *dst = sel.first ? out_pre + s : (s < sel.n_pre ? out_pre + s : out_post);
         *dst = r;
     }
 }
 
-cudaError_t launch_combine(const StatPartial *partials, StatPartial *groups, const StreamSel &sel, const int *err,
+cudaError_t launch_combine(const StatPartial *partials, StatPartial *groups, const StreamSel &sel,
                            sdc_grad_stats *out_pre, sdc_grad_stats *out_post, cudaStream_t st) {
     stats_combine1_kernel<<<dim3(kStatGroups, sel.n_streams), kCombineBlock, 0, st>>>(partials, sel, groups);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    stats_combine2_kernel<<<sel.n_streams, kCombineBlock, 0, st>>>(groups, sel, err, out_pre, out_post);
+    stats_combine2_kernel<<<sel.n_streams, kCombineBlock, 0, st>>>(groups, sel, out_pre, out_post);
     return cudaGetLastError();
 }
 
+constexpr int kGradUnroll = 4;
+constexpr int kAvgUnroll = 2;
 
 template <int DT, int NB>
 cudaError_t launch_avg_t(const BufPtrs &bp, void *avg, uint64_t numel, StatPartial *partials, uint64_t n_chunks,
-                         int *err, int device, cudaStream_t st) {
-    const int smem = (kScanBlock / 32) * (int)avg_warp_smem<NB>();
-    cudaError_t e = cudaFuncSetAttribute(avg_scan_kernel<DT, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
+                         int device, cudaStream_t st) {
     int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, avg_scan_kernel<DT, NB>, kScanBlock, smem);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, avg_scan_kernel<DT, NB, kAvgUnroll>, kScanBlock, 0);
     if (per_sm < 1) per_sm = 1;
     uint64_t grid = (uint64_t)sm_count(device) * per_sm;
     const uint64_t need = (n_chunks * 32 + kScanBlock - 1) / kScanBlock;
     if (need < grid) grid = need;
-    avg_scan_kernel<DT, NB><<<(unsigned)grid, kScanBlock, smem, st>>>(bp, avg, numel, n_chunks, partials, err);
+    avg_scan_kernel<DT, NB, kAvgUnroll><<<(unsigned)grid, kScanBlock, 0, st>>>(bp, avg, numel, n_chunks, partials);
     return cudaGetLastError();
 }
 
 template <int DT>
 cudaError_t launch_avg_dt(const BufPtrs &bp, uint32_t nb, void *avg, uint64_t numel, StatPartial *partials,
-                          uint64_t n_chunks, int *err, int device, cudaStream_t st) {
+                          uint64_t n_chunks, int device, cudaStream_t st) {
     switch (nb) {
-        case 1: return launch_avg_t<DT, 1>(bp, avg, numel, partials, n_chunks, err, device, st);
-        case 2: return launch_avg_t<DT, 2>(bp, avg, numel, partials, n_chunks, err, device, st);
-        case 3: return launch_avg_t<DT, 3>(bp, avg, numel, partials, n_chunks, err, device, st);
-        case 4: return launch_avg_t<DT, 4>(bp, avg, numel, partials, n_chunks, err, device, st);
-        case 5: return launch_avg_t<DT, 5>(bp, avg, numel, partials, n_chunks, err, device, st);
-        case 6: return launch_avg_t<DT, 6>(bp, avg, numel, partials, n_chunks, err, device, st);
-        case 7: return launch_avg_t<DT, 7>(bp, avg, numel, partials, n_chunks, err, device, st);
-        default: return launch_avg_t<DT, 8>(bp, avg, numel, partials, n_chunks, err, device, st);
+        case 1: return launch_avg_t<DT, 1>(bp, avg, numel, partials, n_chunks, device, st);
+        case 2: return launch_avg_t<DT, 2>(bp, avg, numel, partials, n_chunks, device, st);
+        case 3: return launch_avg_t<DT, 3>(bp, avg, numel, partials, n_chunks, device, st);
+        case 4: return launch_avg_t<DT, 4>(bp, avg, numel, partials, n_chunks, device, st);
+        case 5: return launch_avg_t<DT, 5>(bp, avg, numel, partials, n_chunks, device, st);
+        case 6: return launch_avg_t<DT, 6>(bp, avg, numel, partials, n_chunks, device, st);
+        case 7: return launch_avg_t<DT, 7>(bp, avg, numel, partials, n_chunks, device, st);
+        default: return launch_avg_t<DT, 8>(bp, avg, numel, partials, n_chunks, device, st);
     }
 }
 
 }  // namespace
 
 int grad_scan_blocks_per_sm() {
-    const int smem = (kScanBlock / 32) * (int)grad_warp_smem();
     int n = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, grad_scan_kernel, kScanBlock, smem);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, grad_scan_kernel<kGradUnroll>, kScanBlock, 0);
     return n > 0 ? n : 1;
 }
 
-cudaError_t launch_grad_scan(const sdc_plan *plan, StatPartial *partials, int *err, cudaStream_t st) {
+cudaError_t launch_grad_scan(const sdc_plan *plan, StatPartial *partials, cudaStream_t st) {
     if (plan->n_chunks == 0) return cudaSuccess;
-    const int smem = (kScanBlock / 32) * (int)grad_warp_smem();
     uint64_t grid = (uint64_t)sm_count(plan->device) * grad_scan_blocks_per_sm();
     const uint64_t need = (plan->n_chunks * 32 + kScanBlock - 1) / kScanBlock;
     if (need < grid) grid = need;
-    grad_scan_kernel<<<(unsigned)grid, kScanBlock, smem, st>>>(plan->d_chunks, plan->n_chunks, partials, err);
+    grad_scan_kernel<kGradUnroll><<<(unsigned)grid, kScanBlock, 0, st>>>(plan->d_chunks, plan->n_chunks, partials);
     return cudaGetLastError();
 }
 
 cudaError_t launch_stats_combine_plan(const sdc_plan *plan, const StatPartial *partials, StatPartial *groups,
-                                      const int *err, sdc_grad_stats *out, cudaStream_t st) {
+                                      sdc_grad_stats *out, cudaStream_t st) {
     StreamSel sel{plan->d_replica_first_chunk, plan->d_replica_numel, 0, 0, plan->R, plan->R};
-    return launch_combine(partials, groups, sel, err, out, out, st);
+    return launch_combine(partials, groups, sel, out, out, st);
 }
 
 cudaError_t launch_avg_scan(const void *const *bufs, uint32_t n_bufs, void *avg, uint64_t numel, uint32_t dtype,
-                            StatPartial *partials, uint64_t n_chunks, bool vector_path, int *err, int device,
+                            StatPartial *partials, uint64_t n_chunks, bool vector_path, int device,
                             cudaStream_t st) {
     if (n_chunks == 0) return cudaSuccess;
     BufPtrs bp{};
     for (uint32_t b = 0; b < n_bufs; ++b) bp.p[b] = bufs[b];
     if (vector_path) {
         switch (dtype) {
-            case SDC_DTYPE_F32: return launch_avg_dt<SDC_DTYPE_F32>(bp, n_bufs, avg, numel, partials, n_chunks, err, device, st);
-            case SDC_DTYPE_BF16: return launch_avg_dt<SDC_DTYPE_BF16>(bp, n_bufs, avg, numel, partials, n_chunks, err, device, st);
-            default: return launch_avg_dt<SDC_DTYPE_F16>(bp, n_bufs, avg, numel, partials, n_chunks, err, device, st);
+            case SDC_DTYPE_F32: return launch_avg_dt<SDC_DTYPE_F32>(bp, n_bufs, avg, numel, partials, n_chunks, device, st);
+            case SDC_DTYPE_BF16: return launch_avg_dt<SDC_DTYPE_BF16>(bp, n_bufs, avg, numel, partials, n_chunks, device, st);
+            default: return launch_avg_dt<SDC_DTYPE_F16>(bp, n_bufs, avg, numel, partials, n_chunks, device, st);
         }
     }
     uint64_t grid = (uint64_t)sm_count(device) * 4;
@@ -834,11 +676,11 @@ cudaError_t launch_avg_scan(const void *const *bufs, uint32_t n_bufs, void *avg,
     return cudaGetLastError();
 }
 
-cudaError_t launch_stats_combine_streams(const StatPartial *partials, StatPartial *groups, const int *err,
-                                         uint32_t n_streams, uint64_t n_chunks, uint64_t numel,
-                                         sdc_grad_stats *out_pre, sdc_grad_stats *out_post, cudaStream_t st) {
+cudaError_t launch_stats_combine_streams(const StatPartial *partials, StatPartial *groups, uint32_t n_streams,
+                                         uint64_t n_chunks, uint64_t numel, sdc_grad_stats *out_pre,
+                                         sdc_grad_stats *out_post, cudaStream_t st) {
     StreamSel sel{nullptr, nullptr, n_chunks, numel, n_streams, n_streams - 1};
-    return launch_combine(partials, groups, sel, err, out_pre, out_post, st);
+    return launch_combine(partials, groups, sel, out_pre, out_post, st);
 }
 
 }  // namespace sdc
