@@ -101,10 +101,7 @@ typedef struct sdc_plan sdc_plan;
  *        any element is +-Inf (IEEE propagation, as clip_grad_norm_ reports);
  *  nonfinite_fp32: 1 if the float32 squared norm would not be finite:
  *        n_nan > 0 or n_inf > 0 or sumsq_finite > FLT_MAX -- [AWS] "Decide
- *        what the alarm means": a norm above about 1.8e19 counts as non-finite;
- *  aborted: 0 normally; 1 if a kernel of the call gave up one of its bounded
- *        waits for its own staged copies -- the other fields are then
- *        incomplete and the call must be treated as failed. */
+ *        what the alarm means": a norm above about 1.8e19 counts as non-finite. */
 typedef struct {
     uint64_t n_nan;
     uint64_t n_inf;
@@ -113,7 +110,7 @@ typedef struct {
     double sumsq_finite;
     double norm;
     uint32_t nonfinite_fp32;
-    uint32_t aborted;
+    uint32_t reserved;
 } sdc_grad_stats;
 
 /* Vote summary.  diverged: some tensor's copies differ; no_majority: some
@@ -253,7 +250,7 @@ sdc_status sdc_grad_average_scan(const void *const *bufs, uint32_t n_bufs, void 
  * scratch is a fixed __device__ array of SDC_NOALLOC_SCRATCH_BYTES inside the
  * library: sizes whose sdc_grad_average_scan_workspace_size(numel, n_bufs,
  * dtype) exceeds it are rejected with SDC_ERR_BAD_ARG and a message giving
- * the limit (with 4 bf16 buffers that is about 9.1e9 elements).  The first
+ * the limit (with 4 bf16 buffers that is about 1.14e9 elements).  The first
  * call on each device looks up the array's device address (a
  * cudaGetSymbolAddress with that device current) and caches it; make that
  * first call before any stream capture.  All calls share the one array and

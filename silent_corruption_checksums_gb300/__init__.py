@@ -39,7 +39,7 @@ SUSPECT_AGREE, SUSPECT_SEVERAL, SUSPECT_NO_MAJORITY = -1, -2, -3
 DESC_DTYPE = np.dtype([("ptr", "<u8"), ("numel", "<u8"), ("elem_size", "<u4"), ("dtype", "<u4")])
 GRAD_STATS_DTYPE = np.dtype([("n_nan", "<u8"), ("n_inf", "<u8"), ("n_big", "<u8"), ("n_elems", "<u8"),
                              ("sumsq_finite", "<f8"), ("norm", "<f8"), ("nonfinite_fp32", "<u4"),
-                             ("aborted", "<u4")])
+                             ("reserved", "<u4")])
 VOTE_SUMMARY_DTYPE = np.dtype([("diverged", "<u4"), ("no_majority", "<u4"), ("suspect_mask", "<u8"),
                                ("n_differing", "<u4"), ("n_no_majority", "<u4")])
 assert DESC_DTYPE.itemsize == 24 and GRAD_STATS_DTYPE.itemsize == 56 and VOTE_SUMMARY_DTYPE.itemsize == 24
@@ -369,7 +369,7 @@ def decode_stats(raw) -> list[dict]:
         raw = raw.cpu().numpy()
     arr = np.frombuffer(np.ascontiguousarray(raw).tobytes(), dtype=GRAD_STATS_DTYPE)
     return [{k: (float(rec[k]) if k in ("sumsq_finite", "norm") else int(rec[k]))
-             for k in GRAD_STATS_DTYPE.names} for rec in arr]
+             for k in GRAD_STATS_DTYPE.names if k != "reserved"} for rec in arr]
 
 
 def decode_summary(raw) -> dict:

@@ -429,7 +429,7 @@ size_t sdc_grad_average_scan_workspace_size(uint64_t numel, uint32_t n_bufs, uin
     if (dtype != SDC_DTYPE_F32 && dtype != SDC_DTYPE_BF16 && dtype != SDC_DTYPE_F16) return 0;
     const size_t nc = avg_chunks(numel, dtype);
     return round_up(nc * (n_bufs + 1) * sizeof(StatPartial), 256) +
-           round_up((size_t)(n_bufs + 1) * kStatGroups * sizeof(StatPartial), 256) + 256;  // + abort flag
+           round_up((size_t)(n_bufs + 1) * kStatGroups * sizeof(StatPartial), 256);
 }
 
 sdc_status sdc_grad_average_scan(const void *const *bufs, uint32_t n_bufs, void *d_avg, uint64_t numel,
@@ -464,14 +464,9 @@ sdc_status sdc_grad_average_scan(const void *const *bufs, uint32_t n_bufs, void 
     if (st != SDC_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     StatPartial *part = (StatPartial *)d_ws;
-    const size_t part_bytes = round_up(nc * (n_bufs + 1) * sizeof(StatPartial), 256);
-    StatPartial *groups = (StatPartial *)((char *)d_ws + part_bytes);
-    int *err = (int *)((char *)d_ws + part_bytes +
-                       round_up((size_t)(n_bufs + 1) * kStatGroups * sizeof(StatPartial), 256));
-    e = cudaMemsetAsync(err, 0, sizeof(int), s);
-    if (e == cudaSuccess) e = launch_avg_scan(bufs, n_bufs, d_avg, numel, dtype, part, nc, aligned, err, dev, s);
-    if (e == cudaSuccess)
-        e = launch_stats_combine_streams(part, groups, err, n_bufs + 1, nc, numel, d_pre, d_post, s);
+    StatPartial *groups = (StatPartial *)((char *)d_ws + round_up(nc * (n_bufs + 1) * sizeof(StatPartial), 256));
+    e = launch_avg_scan(bufs, n_bufs, d_avg, numel, dtype, part, nc, aligned, dev, s);
+    if (e == cudaSuccess) e = launch_stats_combine_streams(part, groups, n_bufs + 1, nc, numel, d_pre, d_post, s);
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_grad_average_scan launch");
 }
 

@@ -183,9 +183,6 @@ __device__ __forceinline__ double grad_chunk(const GGeom &g, uint32_t lane, Coun
     const uint4 *vb = (const uint4 *)(g.addr + g.head);
     const uint32_t niter = (g.nvec + 31) >> 5;
     double acc_scaled = 0.0, acc_exact = 0.0;
-    // one bulk L2 prefetch of the chunk's aligned body: the later runs of the
-    // chunk then load from L2 while this run computes
-    if (lane == 0 && g.nvec) prefetch_l2_bulk(vb, g.nvec * 16u);
     for (uint32_t r0 = 0; r0 < niter; r0 += kRunVec) {
         const uint32_t r1 = min(r0 + (uint32_t)kRunVec, niter);
         FastAcc a;
@@ -363,199 +360,87 @@ __device__ __forceinline__ void store_bits(void *p, uint64_t i, uint32_t v) {
     else ((uint16_t *)p)[i] = (uint16_t)v;
 }
 
-// Vector path (every pointer 16-byte aligned), one CTA per task at a time.
-//
-// Task t covers elements [t * CE, min((t + 1) * CE, numel)) of every stream,
-// CE = kAvgChunkBytes / elem size (128 KiB of each stream).  A task is 16
-// stages; stage j of a task holds, for each input, the 8 KiB slice j of the
-// task's aligned bytes.  Warp kAvgConsumerWarps (the producer) streams the
-// slices into a ring of kAvgRing<NB> shared-memory stages with one
-// cp.async.bulk per input per stage (8 KiB copies: the copy engine issues few,
-// large requests), each stage completing on its `full` mbarrier; the 16
-// consumer warps read a stage (consumer thread t takes the vector at byte
-// t * 16 of every slice), release it on its `empty` mbarrier, and compute.
-// So up to kAvgRing - 1 stages of every input are in flight while the
-// consumers compute, and the consumers never wait on HBM latency.
-//
-// Per task, consumer thread t handles vectors j * 512 + t (j = 0..15) of each
-// stream: one run of the TwoSum accumulation, flushed at the task's end.  The
-// task's partial per stream is the fixed-order sum over warps of the warp
-// butterflies, so it does not depend on the grid.  Partials: [s][t] for the
-// NB inputs (s < NB) and the average (s = NB).
-//
-// Waits are bounded.  A consumer warp whose wait gives up flags `err`, stops
-// touching data, and keeps taking part in every barrier so that no warp is
-// left waiting; the producer flags, stops issuing and waits (bounded) for its
-// copies in flight.
-constexpr int kAvgConsumerWarps = 16;
-constexpr int kAvgConsumers = kAvgConsumerWarps * 32;
-constexpr int kAvgThreads = kAvgConsumers + 32;
-constexpr uint32_t kAvgSlice = kAvgConsumers * 16;  // bytes of one input in one stage
-constexpr uint32_t kAvgStagesPerTask = (uint32_t)(kAvgChunkBytes / kAvgSlice);
-static_assert(kAvgStagesPerTask == (uint32_t)kRunVec, "one accumulation run per task");
-
-template <int NB>
-constexpr int avg_ring() {
-    return (196608 / (NB * (int)kAvgSlice)) > 8 ? 8 : ((196608 / (NB * (int)kAvgSlice)) < 2 ? 2 : 196608 / (NB * (int)kAvgSlice));
-}
-template <int NB>
-constexpr uint32_t avg_smem_bytes() {
-    // ring | full[ring] | empty[ring] | per-warp sums and counts of each stream
-    return (uint32_t)avg_ring<NB>() * NB * kAvgSlice + 16u * avg_ring<NB>() +
-           (uint32_t)kAvgConsumerWarps * (NB + 1) * (8 + 12);
-}
-
-template <int DT, int NB>
-__global__ void __launch_bounds__(kAvgThreads, 1) avg_scan_kernel(BufPtrs bp, void *__restrict__ outp, uint64_t numel,
-                                                                  uint64_t n_tasks, StatPartial *__restrict__ partials,
-                                                                  int *__restrict__ err) {
+// Vector path: every pointer 16-byte aligned.  Warp task c covers elements
+// [c * CE, min((c + 1) * CE, numel)), CE = kAvgChunkBytes / elem size.
+// Partials: [s][c] for streams s = 0..NB-1 (inputs) and s = NB (average).
+template <int DT, int NB, int U>
+__global__ void __launch_bounds__(kScanBlock) avg_scan_kernel(BufPtrs bp, void *__restrict__ outp, uint64_t numel,
+                                                              uint64_t n_chunks, StatPartial *__restrict__ partials) {
     constexpr int NS = NB + 1;
-    constexpr int RING = avg_ring<NB>();
     constexpr uint32_t ES = DT == SDC_DTYPE_F32 ? 4u : 2u;
     constexpr uint64_t CE = kAvgChunkBytes / ES;
-    constexpr uint32_t STAGE = NB * kAvgSlice;
-    extern __shared__ __align__(128) unsigned char smem[];
-    const uint32_t ring = smem_addr(smem);
-    const uint32_t full = ring + RING * STAGE, empty = full + 8 * RING;
-    double *red_acc = (double *)(smem + RING * STAGE + 16 * RING);             // [warp][NS]
-    uint32_t *red_cnt = (uint32_t *)(red_acc + kAvgConsumerWarps * NS);       // [warp][NS][3]
-    const uint32_t tid = threadIdx.x, wid = tid >> 5, lane = tid & 31u;
-    if (tid == 0) {
-        for (int q = 0; q < RING; ++q) {
-            mbar_init(full + 8 * q, 1);
-            mbar_init(empty + 8 * q, kAvgConsumerWarps);
-        }
-        fence_mbar_init();
-    }
-    __syncthreads();
-    const uint64_t total_bytes = numel * ES;
-    auto task_vec_bytes = [&](uint64_t t) -> uint64_t {
-        const uint64_t left = total_bytes - t * kAvgChunkBytes;
-        return (left < kAvgChunkBytes ? left : kAvgChunkBytes) & ~15ull;
-    };
-
-    if (wid == kAvgConsumerWarps) {  // ------------------------------ producer
-        if (lane == 0) {
-            uint64_t it = 0;
-            bool failed = false;
-            for (uint64_t t = blockIdx.x; t < n_tasks && !failed; t += gridDim.x) {
-                const uint64_t tb = task_vec_bytes(t);
-                for (uint64_t off = 0; off < tb; off += kAvgSlice, ++it) {
-                    const uint32_t q = (uint32_t)(it % RING);
-                    const uint64_t k = it / RING;
-                    if (k > 0 && !mbar_wait(empty + 8 * q, (uint32_t)((k - 1) & 1))) {
-                        atomicOr(err, 1);
-                        failed = true;
-                        break;
-                    }
-                    const uint32_t bytes = (uint32_t)(tb - off < kAvgSlice ? tb - off : kAvgSlice);
-                    mbar_arrive_expect_tx(full + 8 * q, NB * bytes);
-#pragma unroll
-                    for (int b = 0; b < NB; ++b)
-                        bulk_g2s(ring + q * STAGE + b * kAvgSlice, (const char *)bp.p[b] + t * kAvgChunkBytes + off,
-                                 bytes, full + 8 * q);
-                }
-            }
-            if (failed) {  // let the copies already issued land before leaving
-                const uint64_t first = it > (uint64_t)RING ? it - RING : 0;
-                for (uint64_t k = first; k < it; ++k)
-                    mbar_wait(full + 8 * (uint32_t)(k % RING), (uint32_t)((k / RING) & 1));
-            }
-        }
-        return;
-    }
-
-    // ---------------------------------------------------------------- consumers
     const float inv = 1.0f / (float)NB;
-    uint64_t it = 0;
-    bool failed = false;
-    for (uint64_t t = blockIdx.x; t < n_tasks; t += gridDim.x) {
-        const uint64_t e0 = t * CE;
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint64_t warp = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint64_t nwarps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
+    for (uint64_t c = warp; c < n_chunks; c += nwarps) {
+        const uint64_t e0 = c * CE;
         const uint64_t ne = min(CE, numel - e0);
-        const uint32_t nvec = (uint32_t)(task_vec_bytes(t) >> 4);
-        const uint32_t nst = (nvec + kAvgConsumers - 1) / kAvgConsumers;
+        const uint32_t nvec = (uint32_t)((ne * ES) >> 4);
+        const uint32_t niter = (nvec + 31) >> 5;
         const uint4 *in[NB];
 #pragma unroll
         for (int b = 0; b < NB; ++b) in[b] = (const uint4 *)((const char *)bp.p[b] + e0 * ES);
         uint4 *out = (uint4 *)((char *)outp + e0 * ES);
         double acc_s[NS], acc_e[NS];
         Counts n[NS];
-        FastAcc a[NS];
 #pragma unroll
         for (int s = 0; s < NS; ++s) acc_s[s] = acc_e[s] = 0.0;
-        for (uint32_t j = 0; j < nst; ++j, ++it) {
-            const uint32_t q = (uint32_t)(it % RING);
-            if (!failed) {
-                const bool got = mbar_wait(full + 8 * q, (uint32_t)((it / RING) & 1));
-                if (__any_sync(0xffffffffu, !got)) {
-                    failed = true;
-                    if (lane == 0) atomicOr(err, 1);
+        for (uint32_t r0 = 0; r0 < niter; r0 += kRunVec) {
+            const uint32_t r1 = min(r0 + (uint32_t)kRunVec, niter);
+            FastAcc a[NS];
+            for (uint32_t i0 = r0; i0 < r1; i0 += U) {
+                uint4 v[U][NB];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const uint32_t vi = lane + ((i0 + u) << 5);
+                    const bool ok = i0 + u < r1 && vi < nvec;
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) v[u][b] = ok ? ld_stream(in[b] + vi) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const uint32_t vi = lane + ((i0 + u) << 5);
+                    const bool ok = i0 + u < r1 && vi < nvec;
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) fast_vec<DT>(v[u][b], a[b]);
+                    uint4 o = avg_vec<DT, NB>(v[u], inv);
+                    if (ok) {
+                        __stcs(out + vi, o);
+                    } else {
+                        o = make_uint4(0, 0, 0, 0);
+                    }
+                    fast_vec<DT>(o, a[NB]);
                 }
             }
-            const uint32_t vi = j * kAvgConsumers + tid;
-            const bool ok = !failed && vi < nvec;
-            uint4 v[NB];
 #pragma unroll
-            for (int b = 0; b < NB; ++b)
-                v[b] = ok ? ld_shared_v4(ring + q * STAGE + b * kAvgSlice + tid * 16u) : make_uint4(0, 0, 0, 0);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty + 8 * q);  // stage read: the producer may refill it
-#pragma unroll
-            for (int b = 0; b < NB; ++b) fast_vec<DT>(v[b], a[b]);
-            uint4 o = avg_vec<DT, NB>(v, inv);
-            if (ok) {
-                __stcs(out + vi, o);
-            } else {
-                o = make_uint4(0, 0, 0, 0);
-            }
-            fast_vec<DT>(o, a[NB]);
-        }
-#pragma unroll
-        for (int s = 0; s < NS; ++s) {
-            if (!fast_flush<DT>(a[s], acc_s[s]) && !failed) {
-                const uint4 *src = s < NB ? in[s] : (const uint4 *)out;
-                for (uint32_t j = 0; j < nst; ++j) {
-                    const uint32_t vi = j * kAvgConsumers + tid;
-                    if (vi < nvec) exact_vec<DT>(src[vi], acc_e[s], n[s]);
+            for (int s = 0; s < NS; ++s) {
+                if (!fast_flush<DT>(a[s], acc_s[s])) {
+                    const uint4 *src = s < NB ? in[s] : (const uint4 *)out;
+                    for (uint32_t i = r0; i < r1; ++i) {
+                        const uint32_t vi = lane + (i << 5);
+                        if (vi < nvec) exact_vec<DT>(src[vi], acc_e[s], n[s]);
+                    }
                 }
             }
         }
-        // tail elements of the last task (fewer than one vector)
+        // tail elements of the last chunk (fewer than one vector)
         const uint64_t done = (uint64_t)nvec * (16u / ES);
-        if (!failed && tid < ne - done) {
-            const uint64_t i = e0 + done + tid;
+        if (lane < ne - done) {
+            const uint64_t i = e0 + done + lane;
             const uint32_t r = avg_elem<DT>(bp, NB, i);
             store_bits<DT>(outp, i, r);
 #pragma unroll
             for (int b = 0; b < NB; ++b) exact_elem(load_bits<DT>(bp.p[b], i), DT, acc_e[b], n[b]);
             exact_elem(r, DT, acc_e[NB], n[NB]);
         }
-        // task partials: warp butterflies, then warps 0..15 in order
 #pragma unroll
         for (int s = 0; s < NS; ++s) {
-            const double acc = warp_sum_f64(__dadd_rn(unscale<DT>(acc_s[s]), acc_e[s]));
+            double acc = __dadd_rn(unscale<DT>(acc_s[s]), acc_e[s]);
+            acc = warp_sum_f64(acc);
             const uint32_t nn = warp_sum_u32(n[s].nan), ni = warp_sum_u32(n[s].inf), nbg = warp_sum_u32(n[s].big);
-            if (lane == 0) {
-                red_acc[wid * NS + s] = acc;
-                red_cnt[(wid * NS + s) * 3 + 0] = nn;
-                red_cnt[(wid * NS + s) * 3 + 1] = ni;
-                red_cnt[(wid * NS + s) * 3 + 2] = nbg;
-            }
+            if (lane == 0) partials[(uint64_t)s * n_chunks + c] = StatPartial{acc, nn, ni, nbg, 0u};
         }
-        consumer_sync(kAvgConsumers);
-        if (tid < (uint32_t)NS) {
-            const int s = (int)tid;
-            double acc = 0.0;
-            uint32_t nn = 0, ni = 0, nbg = 0;
-            for (int w = 0; w < kAvgConsumerWarps; ++w) {
-                acc = __dadd_rn(acc, red_acc[w * NS + s]);
-                nn += red_cnt[(w * NS + s) * 3 + 0];
-                ni += red_cnt[(w * NS + s) * 3 + 1];
-                nbg += red_cnt[(w * NS + s) * 3 + 2];
-            }
-            partials[(uint64_t)s * n_tasks + t] = StatPartial{acc, nn, ni, nbg, 0u};
-        }
-        consumer_sync(kAvgConsumers);
     }
 }
 
@@ -669,8 +554,7 @@ __global__ void __launch_bounds__(kCombineBlock) stats_combine1_kernel(const Sta
 }
 
 __global__ void __launch_bounds__(kCombineBlock) stats_combine2_kernel(const StatPartial *__restrict__ groups,
-                                                                       StreamSel sel, const int *__restrict__ err,
-                                                                       sdc_grad_stats *out_pre,
+                                                                       StreamSel sel, sdc_grad_stats *out_pre,
                                                                        sdc_grad_stats *out_post) {
     const uint32_t s = blockIdx.x;
     Acc a{0.0, 0, 0, 0};
@@ -693,47 +577,49 @@ __global__ void __launch_bounds__(kCombineBlock) stats_combine2_kernel(const Sta
         else if (r.n_inf) r.norm = __longlong_as_double(0x7FF0000000000000ll);
         else r.norm = __dsqrt_rn(a.sum);
         r.nonfinite_fp32 = (r.n_nan || r.n_inf || a.sum > kFltMax) ? 1u : 0u;
-        r.aborted = (err != nullptr && *err != 0) ? 1u : 0u;
+        r.reserved = 0;
         sdc_grad_stats *dst = sel.first ? out_pre + s : (s < sel.n_pre ? out_pre + s : out_post);
         *dst = r;
     }
 }
 
-cudaError_t launch_combine(const StatPartial *partials, StatPartial *groups, const StreamSel &sel, const int *err,
+cudaError_t launch_combine(const StatPartial *partials, StatPartial *groups, const StreamSel &sel,
                            sdc_grad_stats *out_pre, sdc_grad_stats *out_post, cudaStream_t st) {
     stats_combine1_kernel<<<dim3(kStatGroups, sel.n_streams), kCombineBlock, 0, st>>>(partials, sel, groups);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    stats_combine2_kernel<<<sel.n_streams, kCombineBlock, 0, st>>>(groups, sel, err, out_pre, out_post);
+    stats_combine2_kernel<<<sel.n_streams, kCombineBlock, 0, st>>>(groups, sel, out_pre, out_post);
     return cudaGetLastError();
 }
 
 constexpr int kGradUnroll = 4;
+constexpr int kAvgUnroll = 2;
 
 template <int DT, int NB>
-cudaError_t launch_avg_t(const BufPtrs &bp, void *avg, uint64_t numel, StatPartial *partials, uint64_t n_tasks,
-                         int *err, int device, cudaStream_t st) {
-    const int smem = (int)avg_smem_bytes<NB>();
-    cudaError_t e = cudaFuncSetAttribute(avg_scan_kernel<DT, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    uint64_t grid = (uint64_t)sm_count(device);  // one CTA (16 consumer warps + a producer) per SM
-    if (n_tasks < grid) grid = n_tasks;
-    avg_scan_kernel<DT, NB><<<(unsigned)grid, kAvgThreads, smem, st>>>(bp, avg, numel, n_tasks, partials, err);
+cudaError_t launch_avg_t(const BufPtrs &bp, void *avg, uint64_t numel, StatPartial *partials, uint64_t n_chunks,
+                         int device, cudaStream_t st) {
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, avg_scan_kernel<DT, NB, kAvgUnroll>, kScanBlock, 0);
+    if (per_sm < 1) per_sm = 1;
+    uint64_t grid = (uint64_t)sm_count(device) * per_sm;
+    const uint64_t need = (n_chunks * 32 + kScanBlock - 1) / kScanBlock;
+    if (need < grid) grid = need;
+    avg_scan_kernel<DT, NB, kAvgUnroll><<<(unsigned)grid, kScanBlock, 0, st>>>(bp, avg, numel, n_chunks, partials);
     return cudaGetLastError();
 }
 
 template <int DT>
 cudaError_t launch_avg_dt(const BufPtrs &bp, uint32_t nb, void *avg, uint64_t numel, StatPartial *partials,
-                          uint64_t n_tasks, int *err, int device, cudaStream_t st) {
+                          uint64_t n_chunks, int device, cudaStream_t st) {
     switch (nb) {
-        case 1: return launch_avg_t<DT, 1>(bp, avg, numel, partials, n_tasks, err, device, st);
-        case 2: return launch_avg_t<DT, 2>(bp, avg, numel, partials, n_tasks, err, device, st);
-        case 3: return launch_avg_t<DT, 3>(bp, avg, numel, partials, n_tasks, err, device, st);
-        case 4: return launch_avg_t<DT, 4>(bp, avg, numel, partials, n_tasks, err, device, st);
-        case 5: return launch_avg_t<DT, 5>(bp, avg, numel, partials, n_tasks, err, device, st);
-        case 6: return launch_avg_t<DT, 6>(bp, avg, numel, partials, n_tasks, err, device, st);
-        case 7: return launch_avg_t<DT, 7>(bp, avg, numel, partials, n_tasks, err, device, st);
-        default: return launch_avg_t<DT, 8>(bp, avg, numel, partials, n_tasks, err, device, st);
+        case 1: return launch_avg_t<DT, 1>(bp, avg, numel, partials, n_chunks, device, st);
+        case 2: return launch_avg_t<DT, 2>(bp, avg, numel, partials, n_chunks, device, st);
+        case 3: return launch_avg_t<DT, 3>(bp, avg, numel, partials, n_chunks, device, st);
+        case 4: return launch_avg_t<DT, 4>(bp, avg, numel, partials, n_chunks, device, st);
+        case 5: return launch_avg_t<DT, 5>(bp, avg, numel, partials, n_chunks, device, st);
+        case 6: return launch_avg_t<DT, 6>(bp, avg, numel, partials, n_chunks, device, st);
+        case 7: return launch_avg_t<DT, 7>(bp, avg, numel, partials, n_chunks, device, st);
+        default: return launch_avg_t<DT, 8>(bp, avg, numel, partials, n_chunks, device, st);
     }
 }
 
@@ -757,20 +643,20 @@ cudaError_t launch_grad_scan(const sdc_plan *plan, StatPartial *partials, cudaSt
 cudaError_t launch_stats_combine_plan(const sdc_plan *plan, const StatPartial *partials, StatPartial *groups,
                                       sdc_grad_stats *out, cudaStream_t st) {
     StreamSel sel{plan->d_replica_first_chunk, plan->d_replica_numel, 0, 0, plan->R, plan->R};
-    return launch_combine(partials, groups, sel, nullptr, out, out, st);
+    return launch_combine(partials, groups, sel, out, out, st);
 }
 
 cudaError_t launch_avg_scan(const void *const *bufs, uint32_t n_bufs, void *avg, uint64_t numel, uint32_t dtype,
-                            StatPartial *partials, uint64_t n_chunks, bool vector_path, int *err, int device,
+                            StatPartial *partials, uint64_t n_chunks, bool vector_path, int device,
                             cudaStream_t st) {
     if (n_chunks == 0) return cudaSuccess;
     BufPtrs bp{};
     for (uint32_t b = 0; b < n_bufs; ++b) bp.p[b] = bufs[b];
     if (vector_path) {
         switch (dtype) {
-            case SDC_DTYPE_F32: return launch_avg_dt<SDC_DTYPE_F32>(bp, n_bufs, avg, numel, partials, n_chunks, err, device, st);
-            case SDC_DTYPE_BF16: return launch_avg_dt<SDC_DTYPE_BF16>(bp, n_bufs, avg, numel, partials, n_chunks, err, device, st);
-            default: return launch_avg_dt<SDC_DTYPE_F16>(bp, n_bufs, avg, numel, partials, n_chunks, err, device, st);
+            case SDC_DTYPE_F32: return launch_avg_dt<SDC_DTYPE_F32>(bp, n_bufs, avg, numel, partials, n_chunks, device, st);
+            case SDC_DTYPE_BF16: return launch_avg_dt<SDC_DTYPE_BF16>(bp, n_bufs, avg, numel, partials, n_chunks, device, st);
+            default: return launch_avg_dt<SDC_DTYPE_F16>(bp, n_bufs, avg, numel, partials, n_chunks, device, st);
         }
     }
     uint64_t grid = (uint64_t)sm_count(device) * 4;
@@ -790,11 +676,11 @@ cudaError_t launch_avg_scan(const void *const *bufs, uint32_t n_bufs, void *avg,
     return cudaGetLastError();
 }
 
-cudaError_t launch_stats_combine_streams(const StatPartial *partials, StatPartial *groups, const int *err,
-                                         uint32_t n_streams, uint64_t n_chunks, uint64_t numel,
-                                         sdc_grad_stats *out_pre, sdc_grad_stats *out_post, cudaStream_t st) {
+cudaError_t launch_stats_combine_streams(const StatPartial *partials, StatPartial *groups, uint32_t n_streams,
+                                         uint64_t n_chunks, uint64_t numel, sdc_grad_stats *out_pre,
+                                         sdc_grad_stats *out_post, cudaStream_t st) {
     StreamSel sel{nullptr, nullptr, n_chunks, numel, n_streams, n_streams - 1};
-    return launch_combine(partials, groups, sel, err, out_pre, out_post, st);
+    return launch_combine(partials, groups, sel, out_pre, out_post, st);
 }
 
 }  // namespace sdc

@@ -106,10 +106,10 @@ cudaError_t launch_stats_combine_plan(const sdc_plan *plan, const StatPartial *p
                                       sdc_grad_stats *out, cudaStream_t st);
 cudaError_t launch_avg_scan(const void *const *bufs, uint32_t n_bufs, void *avg, uint64_t numel,
                             uint32_t dtype, StatPartial *partials, uint64_t n_chunks, bool vector_path,
-                            int *err, int device, cudaStream_t st);
-cudaError_t launch_stats_combine_streams(const StatPartial *partials, StatPartial *groups, const int *err,
-                                         uint32_t n_streams, uint64_t n_chunks, uint64_t numel,
-                                         sdc_grad_stats *out_pre, sdc_grad_stats *out_post, cudaStream_t st);
+                            int device, cudaStream_t st);
+cudaError_t launch_stats_combine_streams(const StatPartial *partials, StatPartial *groups, uint32_t n_streams,
+                                         uint64_t n_chunks, uint64_t numel, sdc_grad_stats *out_pre,
+                                         sdc_grad_stats *out_post, cudaStream_t st);
 cudaError_t launch_vote(const uint64_t *fp, uint32_t R, uint32_t T, int32_t *suspect, uint64_t *mask,
                         sdc_vote_summary *summary, cudaStream_t st);
 cudaError_t launch_xor_compare(const uint64_t *a, const uint64_t *b, uint32_t n, uint8_t *mismatch,
@@ -120,9 +120,8 @@ constexpr int kScanBlock = 256;
 int fp_scan_blocks_per_sm();
 int grad_scan_blocks_per_sm();
 
-// Bytes of one task of the fused average scan (per stream): 16 stages of
-// 8 KiB, one CTA of 16 consumer warps per task.
-constexpr uint64_t kAvgChunkBytes = 131072;
+// Bytes of one warp task in the fused average scan (per stream).
+constexpr uint64_t kAvgChunkBytes = 16384;
 // Fixed number of first-pass groups per stream in the statistics combine.
 constexpr uint32_t kStatGroups = 128;
 
@@ -141,12 +140,6 @@ __device__ __forceinline__ uint4 ld_stream(const void *p) {
         : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
         : "l"(p));
     return r;
-}
-
-// Bulk prefetch of [p, p + bytes) into L2 (p 16-byte aligned, bytes a
-// multiple of 16); no data is returned and no completion is tracked.
-__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // Two-way 16x8-bit dot product with 32-bit accumulate, both halves signed.
@@ -212,55 +205,6 @@ __device__ __forceinline__ void f2_two_sum_acc(uint64_t &s, uint64_t &c, uint64_
     uint64_t t3 = f2_sub(y, bb);
     c = f2_add(c, f2_add(t2, t3));
     s = s2;
-}
-
-// ---------------------------------------------------------------- bulk copies (TMA) and mbarriers
-// Every wait on a barrier is bounded: after kSpinLimit polls the caller
-// records an error instead of waiting on, so no kernel can hang on one.
-constexpr uint32_t kSpinLimit = 1u << 22;
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-__device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mbar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
-__device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mbar) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t mbar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t mbar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(mbar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Bounded wait for the completion of the barrier phase with parity `parity`
-// (returns at once if that phase has already completed).
-__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
-    for (uint32_t i = 0; i < kSpinLimit; ++i)
-        if (mbar_try_wait(mbar, parity)) return true;
-    return false;
-}
-// Global -> shared bulk copy of `bytes` (a multiple of 16; both addresses
-// 16-byte aligned), completing its bytes on `mbar`.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t mbar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(mbar)
-                 : "memory");
-}
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-    uint4 r;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(addr));
-    return r;
-}
-// Barrier over the consumer warps only (named barrier 1).
-__device__ __forceinline__ void consumer_sync(uint32_t nthreads) {
-    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 
 __device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
