@@ -183,6 +183,9 @@ __device__ __forceinline__ double grad_chunk(const GGeom &g, uint32_t lane, Coun
     const uint4 *vb = (const uint4 *)(g.addr + g.head);
     const uint32_t niter = (g.nvec + 31) >> 5;
     double acc_scaled = 0.0, acc_exact = 0.0;
+    // one bulk L2 prefetch of the chunk's aligned body: the later runs of the
+    // chunk then load from L2 while this run computes
+    if (lane == 0 && g.nvec) prefetch_l2_bulk(vb, g.nvec * 16u);
     for (uint32_t r0 = 0; r0 < niter; r0 += kRunVec) {
         const uint32_t r1 = min(r0 + (uint32_t)kRunVec, niter);
         FastAcc a;

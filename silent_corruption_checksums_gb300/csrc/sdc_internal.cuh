@@ -142,6 +142,12 @@ __device__ __forceinline__ uint4 ld_stream(const void *p) {
     return r;
 }
 
+// Bulk prefetch of [p, p + bytes) into L2 (p 16-byte aligned, bytes a
+// multiple of 16); no data is returned and no completion is tracked.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // Two-way 16x8-bit dot product with 32-bit accumulate, both halves signed.
 __device__ __forceinline__ int dp2a_lo_s(uint32_t a, uint32_t b, int c) {
     int d;
@@ -195,15 +201,20 @@ __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
     return d;
 }
 
-// Error-free sum (Knuth's TwoSum) on both lanes: s + y = s' + err exactly;
-// the error is added to the compensation c.
+// Error-free accumulation of a non-negative term on both lanes:
+// s + y = s' + err exactly, and err is added to the compensation c.
+// Dekker's Fast2Sum (s' = a + b, err = b - (s' - a)) is exact when |a| >= |b|;
+// with s, y >= 0 the larger of the two is the larger bit pattern, so the
+// ordering is two integer max/min per lane (integer pipe) and the floating
+// point cost is four packed operations instead of TwoSum's seven.
+// Requires s >= 0 and y >= 0 (NaN/Inf propagate into s).
 __device__ __forceinline__ void f2_two_sum_acc(uint64_t &s, uint64_t &c, uint64_t y) {
-    uint64_t s2 = f2_add(s, y);
-    uint64_t bb = f2_sub(s2, s);
-    uint64_t t1 = f2_sub(s2, bb);
-    uint64_t t2 = f2_sub(s, t1);
-    uint64_t t3 = f2_sub(y, bb);
-    c = f2_add(c, f2_add(t2, t3));
+    const uint32_t s0 = (uint32_t)s, s1 = (uint32_t)(s >> 32), y0 = (uint32_t)y, y1 = (uint32_t)(y >> 32);
+    const uint64_t big = f2_pack_bits(max(s0, y0), max(s1, y1));
+    const uint64_t small = f2_pack_bits(min(s0, y0), min(s1, y1));
+    const uint64_t s2 = f2_add(big, small);
+    const uint64_t err = f2_sub(small, f2_sub(s2, big));
+    c = f2_add(c, err);
     s = s2;
 }
 
