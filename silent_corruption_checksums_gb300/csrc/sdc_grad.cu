@@ -393,6 +393,15 @@ __global__ void __launch_bounds__(kScanBlock) avg_scan_kernel(BufPtrs bp, void *
             const uint32_t r1 = min(r0 + (uint32_t)kRunVec, niter);
             FastAcc a[NS];
             for (uint32_t i0 = r0; i0 < r1; i0 += U) {
+                // L2 prefetch of the batch after next: lanes 0, 8, 16, 24 touch the
+                // four 128-byte lines of each input's 512-byte warp slice
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const uint32_t vi = lane + ((i0 + 2 * U + u) << 5);
+                    if ((lane & 7u) == 0 && vi < nvec)
+#pragma unroll
+                        for (int b = 0; b < NB; ++b) prefetch_l2(in[b] + vi);
+                }
                 uint4 v[U][NB];
 #pragma unroll
                 for (int u = 0; u < U; ++u) {

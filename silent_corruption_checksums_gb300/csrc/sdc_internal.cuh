@@ -148,6 +148,9 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) 
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
+// Prefetch the line holding p into L2.
+__device__ __forceinline__ void prefetch_l2(const void *p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
 // Two-way 16x8-bit dot product with 32-bit accumulate, both halves signed.
 __device__ __forceinline__ int dp2a_lo_s(uint32_t a, uint32_t b, int c) {
     int d;
