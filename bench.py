@@ -335,6 +335,8 @@ def _time_loop(fn, steps, stream, torch):
 def bench_rows(args, dev, stream, peaks, sdc, W, torch, np, only=None) -> dict:
     """The other rows of the hot path, each timed on its own workload."""
     rows = {}
+    if only in ("fingerprint_8b", "fingerprint_stress"):
+        return bench_big_rows(args, dev, stream, peaks, sdc, W, torch, only)
     # fused gradient average-scan on 4 bf16 buffers of the 1b layout
     g = W.grads_flat(W.layout_numel(W.layout_1b(args.layers)), 4, torch.bfloat16, 1e-3, dev, seed=3)
     bufs = g["bufs"]
@@ -382,7 +384,60 @@ def bench_rows(args, dev, stream, peaks, sdc, W, torch, np, only=None) -> dict:
         del xplan, rec
     del g, bufs, out, ws
     torch.cuda.empty_cache()
+    if not getattr(args, "no_big_rows", False):
+        rows.update(bench_big_rows(args, dev, stream, peaks, sdc, W, torch, only))
     return rows
+
+
+def bench_big_rows(args, dev, stream, peaks, sdc, W, torch, only) -> dict:
+    """Fingerprint rows on the 8b and stress workloads (tens of GB each)."""
+    rows = {}
+    if only in (None, "fingerprint_8b"):
+        rows["fingerprint_8b"] = bench_fp_row(
+            W.weights_8b(dev, seed=4)["replicas"], "8b bf16 layout (T=291), 8 replicas, 16-element perturbation",
+            args, stream, peaks, sdc, torch)
+    if only in (None, "fingerprint_stress"):
+        w = W.stress(dev, seed=5)
+        rows["fingerprint_stress"] = bench_fp_row(
+            w["replicas"], "100,000 tensors (1..1e6 elements, fp32/bf16/fp16, element-aligned packing), 3 replicas",
+            args, stream, peaks, sdc, torch)
+        p = w["pairs"]
+        xplan = sdc.Plan([p["orig"], p["recomp"]])
+        xo = torch.empty((2, len(p["orig"])), dtype=torch.int64, device=dev)
+
+        def xs_step():
+            xplan.xorsum(out=xo, stream=stream)
+            sdc.xorsum_compare(xo[0], xo[1], stream=stream)
+
+        ms = _time_loop(xs_step, 20, stream, torch)
+        nbytes = sum(t.numel() * t.element_size() for t in p["orig"]) * 2
+        rows["xorsum_pairs_stress"] = {"workload": "1,000 (original, recomputed) pairs, sizes 1..1e6, half with a "
+                                       "one-bit difference: xorsum + compare", "ms": ms, "bytes": nbytes,
+                                       "GB_s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"]}
+        del w, xplan, p
+        torch.cuda.empty_cache()
+    return rows
+
+
+def bench_fp_row(reps, workload, args, stream, peaks, sdc, torch) -> dict:
+    """Fingerprint + vote over a replica set: ms per pass and GB/s of element bytes."""
+    plan = sdc.Plan(reps)
+    R, T = len(reps), len(reps[0])
+    fp = torch.empty((R, T, 2), dtype=torch.int64, device=plan.device)
+    vo = (torch.empty(T, dtype=torch.int32, device=plan.device), torch.empty(T, dtype=torch.int64, device=plan.device),
+          torch.empty(sdc.VOTE_SUMMARY_DTYPE.itemsize, dtype=torch.uint8, device=plan.device))
+
+    def step():
+        plan.fingerprint(out=fp, stream=stream)
+        sdc.vote(fp, stream=stream, out=vo)
+
+    ms = _time_loop(step, 20, stream, torch)
+    nbytes = sum(t.numel() * t.element_size() for ts in reps for t in ts)
+    verdict = sdc.pages_verdict(sdc.decode_summary(vo[2]))
+    n_chunks = plan.n_chunks
+    del plan
+    return {"workload": workload, "ms": ms, "bytes": nbytes, "GB_s": nbytes / ms / 1e6,
+            "frac_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"], "n_chunks": n_chunks, "verdict": verdict}
 
 
 def bench_e2e(args, reps, plan, fp, vote_out, stream, sdc, torch, bytes_per_step) -> dict:
@@ -393,10 +448,22 @@ def bench_e2e(args, reps, plan, fp, vote_out, stream, sdc, torch, bytes_per_step
     sum_host = torch.empty(vote_out[2].shape, dtype=torch.uint8).pin_memory()
     sus_host = torch.empty(vote_out[0].shape, dtype=torch.int32).pin_memory()
 
+    # the host-to-device copies are spread round-robin over four copy streams
+    # (several copy engines in parallel), joined into the compute stream
+    copy_streams = [torch.cuda.Stream() for _ in range(4)]
+    pairs = [(h, d) for hs, ds in zip(host, reps) for h, d in zip(hs, ds)]
+
     def e2e_step():
-        for hs, ds in zip(host, reps):
-            for h, d in zip(hs, ds):
+        start_ev = torch.cuda.Event()
+        start_ev.record(stream)
+        for i, (h, d) in enumerate(pairs):
+            cs = copy_streams[i % len(copy_streams)]
+            if i < len(copy_streams):
+                cs.wait_event(start_ev)
+            with torch.cuda.stream(cs):
                 d.copy_(h, non_blocking=True)
+        for cs in copy_streams:
+            stream.wait_stream(cs)
         plan.fingerprint(out=fp, stream=stream)
         sdc.vote(fp, stream=stream, out=vote_out)
         fp_host.copy_(fp, non_blocking=True)
@@ -439,7 +506,9 @@ def main(argv=None) -> None:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--chunk-bytes", type=int, default=0)
     ap.add_argument("--quick", action="store_true", help="only the timed fingerprint step (no rows/e2e/cpu)")
-    ap.add_argument("--only", choices=["grad_average_scan", "grad_scan", "xorsum"], default=None,
+    ap.add_argument("--no-big-rows", action="store_true", help="skip the 8b and stress rows")
+    ap.add_argument("--only", choices=["grad_average_scan", "grad_scan", "xorsum", "fingerprint_8b",
+                                       "fingerprint_stress"], default=None,
                     help="time one row alone (profiling)")
     ap.add_argument("--layers", type=int, default=24,
                     help="decoder layers of the 1b layout (24 = the benchmark workload; fewer for profiling)")
