@@ -448,22 +448,10 @@ def bench_e2e(args, reps, plan, fp, vote_out, stream, sdc, torch, bytes_per_step
     sum_host = torch.empty(vote_out[2].shape, dtype=torch.uint8).pin_memory()
     sus_host = torch.empty(vote_out[0].shape, dtype=torch.int32).pin_memory()
 
-    # the host-to-device copies are spread round-robin over four copy streams
-    # (several copy engines in parallel), joined into the compute stream
-    copy_streams = [torch.cuda.Stream() for _ in range(4)]
-    pairs = [(h, d) for hs, ds in zip(host, reps) for h, d in zip(hs, ds)]
-
     def e2e_step():
-        start_ev = torch.cuda.Event()
-        start_ev.record(stream)
-        for i, (h, d) in enumerate(pairs):
-            cs = copy_streams[i % len(copy_streams)]
-            if i < len(copy_streams):
-                cs.wait_event(start_ev)
-            with torch.cuda.stream(cs):
+        for hs, ds in zip(host, reps):
+            for h, d in zip(hs, ds):
                 d.copy_(h, non_blocking=True)
-        for cs in copy_streams:
-            stream.wait_stream(cs)
         plan.fingerprint(out=fp, stream=stream)
         sdc.vote(fp, stream=stream, out=vote_out)
         fp_host.copy_(fp, non_blocking=True)
