@@ -351,3 +351,30 @@ def pages_verdict(summary: dict) -> dict:
         return {"diverged": True, "suspects": None}
     m = summary["suspect_mask"]
     return {"diverged": True, "suspects": [r for r in range(64) if (m >> r) & 1]}
+
+
+# --------------------------------------------------------------------------
+# Ring replay audit  ([AWS] "Check 2: Ring replay, before the optimizer step")
+# --------------------------------------------------------------------------
+def ring_pairs(table, offset: int) -> list[tuple[int, int]]:
+    """Mismatched (target, replayer) pairs of a ring audit table.
+
+    ``table[r]`` is rank r's pair of rows (own result, replay of its target);
+    rank r replays rank (r + offset) % n.  A pair mismatches when the target's
+    own result differs from the replayer's replay.  Listed by replayer.
+    """
+    n = len(table)
+    out = []
+    for r in range(n):
+        t = (r + offset) % n
+        if list(table[t][0]) != list(table[r][1]):
+            out.append((t, r))
+    return out
+
+
+def localize(pairs: list[tuple[int, int]]) -> tuple[list[int], list[tuple[int, int]]]:
+    """Culprits (ranks counted in two or more mismatched pairs) and the pairs touching none of them."""
+    hits = Counter(x for p in pairs for x in p)
+    culprits = sorted(r for r, c in hits.items() if c >= 2)
+    ambiguous = [p for p in pairs if not (set(p) & set(culprits))]
+    return culprits, ambiguous

@@ -28,7 +28,7 @@ __all__ = [
     "sdc_plan_create", "sdc_plan_destroy", "sdc_workspace_size", "sdc_plan_info", "sdc_fingerprint",
     "sdc_xorsum", "sdc_xorsum_compare", "sdc_vote", "sdc_grad_scan", "sdc_grad_average_scan_workspace_size",
     "sdc_grad_average_scan", "sdc_grad_average_scan_noalloc", "NOALLOC_SCRATCH_BYTES", "sdc_status_string", "sdc_last_error", "Plan", "vote", "xorsum_compare",
-    "grad_average_scan", "decode_stats", "decode_summary", "pages_verdict", "library_path",
+    "grad_average_scan", "ring_audit", "ring_result", "sdc_ring_audit", "RING_SUMMARY_DTYPE", "decode_stats", "decode_summary", "pages_verdict", "library_path",
 ]
 
 DTYPE_RAW, DTYPE_F32, DTYPE_BF16, DTYPE_F16 = 0, 1, 2, 3
@@ -40,6 +40,8 @@ DESC_DTYPE = np.dtype([("ptr", "<u8"), ("numel", "<u8"), ("elem_size", "<u4"), (
 GRAD_STATS_DTYPE = np.dtype([("n_nan", "<u8"), ("n_inf", "<u8"), ("n_big", "<u8"), ("n_elems", "<u8"),
                              ("sumsq_finite", "<f8"), ("norm", "<f8"), ("nonfinite_fp32", "<u4"),
                              ("reserved", "<u4")])
+RING_SUMMARY_DTYPE = np.dtype([("n_pairs", "<u4"), ("n_culprits", "<u4"), ("n_ambiguous", "<u4"),
+                               ("reserved", "<u4")])
 VOTE_SUMMARY_DTYPE = np.dtype([("diverged", "<u4"), ("no_majority", "<u4"), ("suspect_mask", "<u8"),
                                ("n_differing", "<u4"), ("n_no_majority", "<u4")])
 assert DESC_DTYPE.itemsize == 24 and GRAD_STATS_DTYPE.itemsize == 56 and VOTE_SUMMARY_DTYPE.itemsize == 24
@@ -80,6 +82,7 @@ def _load() -> ctypes.CDLL:
         "sdc_grad_average_scan_workspace_size": ([u64, u32, u32], sz),
         "sdc_grad_average_scan": ([ctypes.POINTER(vp), u32, vp, u64, u32, vp, vp, vp, sz, vp], ctypes.c_int),
         "sdc_grad_average_scan_noalloc": ([ctypes.POINTER(vp), u32, vp, u64, u32, vp, vp, vp], ctypes.c_int),
+        "sdc_ring_audit": ([vp, u32, u32, u32, vp, vp, vp, vp, vp, vp], ctypes.c_int),
         "sdc_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "sdc_last_error": ([], ctypes.c_char_p),
     }
@@ -185,6 +188,12 @@ def sdc_grad_average_scan(bufs: list[int], d_avg: int, numel: int, dtype: int, d
     arr = (ctypes.c_void_p * max(1, len(bufs)))(*bufs)
     _check("sdc_grad_average_scan", _lib.sdc_grad_average_scan(arr, len(bufs), d_avg, numel, dtype, d_pre,
                                                                d_post, d_ws, ws_bytes, stream))
+
+
+def sdc_ring_audit(d_table: int, n: int, L: int, offset: int, d_mismatch: int, d_hits: int, d_culprit: int,
+                   d_ambiguous: int, d_summary: int, stream: int) -> None:
+    _check("sdc_ring_audit", _lib.sdc_ring_audit(d_table, n, L, offset, d_mismatch, d_hits, d_culprit, d_ambiguous,
+                                                 d_summary, stream))
 
 
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -328,6 +337,37 @@ def vote(fp, stream=None, out=None):
     sdc_vote(fp.data_ptr(), R, T, suspect.data_ptr() if T else 0, mask.data_ptr() if T else 0,
              summary.data_ptr(), _stream_handle(stream))
     return suspect, mask, summary
+
+
+def ring_audit(table, offset: int, stream=None):
+    """Ring replay audit on an [n, 2, L] int64 table (row 0 own result, row 1 replay of the target).
+
+    Returns (mismatch uint8 [n], hits int32 [n], culprit uint8 [n], ambiguous uint8 [n], summary uint8 [16]),
+    mismatch/ambiguous indexed by the replayer r of pair ((r + offset) % n, r).
+    """
+    torch = _torch()
+    n, L = int(table.shape[0]), int(table.shape[2])
+    dev = table.device
+    mism = torch.empty(n, dtype=torch.uint8, device=dev)
+    hits = torch.empty(n, dtype=torch.int32, device=dev)
+    cul = torch.empty(n, dtype=torch.uint8, device=dev)
+    amb = torch.empty(n, dtype=torch.uint8, device=dev)
+    summ = torch.empty(RING_SUMMARY_DTYPE.itemsize, dtype=torch.uint8, device=dev)
+    z = lambda t: t.data_ptr() if n else 0
+    sdc_ring_audit(table.data_ptr() if table.numel() else 0, n, L, offset, z(mism), z(hits), z(cul), z(amb),
+                   summ.data_ptr(), _stream_handle(stream))
+    return mism, hits, cul, amb, summ
+
+
+def ring_result(mism, culprit, offset: int) -> dict:
+    """Host view of a ring audit: the page's mismatched pairs (target, replayer), culprits, ambiguous pairs."""
+    m = mism.cpu().tolist()
+    n = len(m)
+    c = culprit.cpu().tolist()
+    pairs = [((r + offset) % n, r) for r in range(n) if m[r]]
+    culprits = sorted(r for r in range(n) if c[r])
+    ambiguous = [p for p in pairs if not (set(p) & set(culprits))]
+    return {"pairs": pairs, "culprits": culprits, "ambiguous": ambiguous}
 
 
 def xorsum_compare(a, b, stream=None):

@@ -112,6 +112,9 @@ cudaError_t launch_stats_combine_streams(const StatPartial *partials, StatPartia
                                          sdc_grad_stats *out_post, cudaStream_t st);
 cudaError_t launch_vote(const uint64_t *fp, uint32_t R, uint32_t T, int32_t *suspect, uint64_t *mask,
                         sdc_vote_summary *summary, cudaStream_t st);
+cudaError_t launch_ring_audit(const uint64_t *table, uint32_t n, uint32_t L, uint32_t offset, uint8_t *mismatch,
+                              uint32_t *hits, uint8_t *culprit, uint8_t *ambiguous, sdc_ring_summary *summary,
+                              int device, cudaStream_t st);
 cudaError_t launch_xor_compare(const uint64_t *a, const uint64_t *b, uint32_t n, uint8_t *mismatch,
                                uint64_t *diff, cudaStream_t st);
 
