@@ -78,6 +78,11 @@ def _load():
             lib.oracle_average.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_uint32,
                                            ctypes.c_uint64, ctypes.c_uint32, ctypes.c_void_p]
             lib.oracle_average.restype = ctypes.c_int
+            fl = ctypes.c_float
+            lib.oracle_adamw.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32, ctypes.c_void_p,
+                                         ctypes.c_void_p, ctypes.c_uint64, fl, ctypes.c_int, fl, fl, fl, fl, fl,
+                                         fl, fl]
+            lib.oracle_adamw.restype = ctypes.c_int
             lib.oracle_round_f32.argtypes = [ctypes.c_float, ctypes.c_uint32]
             lib.oracle_round_f32.restype = ctypes.c_uint32
             _lib = lib
@@ -378,3 +383,47 @@ def localize(pairs: list[tuple[int, int]]) -> tuple[list[int], list[tuple[int, i
     culprits = sorted(r for r, c in hits.items() if c >= 2)
     ambiguous = [p for p in pairs if not (set(p) & set(culprits))]
     return culprits, ambiguous
+
+
+# --------------------------------------------------------------------------
+# Clip + AdamW step  ([AWS] "Use case: Testing the checks on SageMaker
+# HyperPod" hyperparameters; `train()` clip, reduced-gradient gate and step)
+# --------------------------------------------------------------------------
+def adamw_scalars(lr: float, beta1: float, beta2: float, eps: float, weight_decay: float, step: int) -> dict:
+    """float32 scalars of one AdamW step: each formed in double from the float32 inputs, rounded once."""
+    f = lambda x: float(np.float32(x))
+    lr, beta1, beta2, eps, wd = f(lr), f(beta1), f(beta2), f(eps), f(weight_decay)
+    return {"decay": f(1.0 - lr * wd), "omb1": f(1.0 - beta1), "beta2": beta2, "omb2": f(1.0 - beta2),
+            "bc2s": f(math.sqrt(1.0 - math.pow(beta2, step))), "eps": eps,
+            "step_size": f(lr / (1.0 - math.pow(beta1, step)))}
+
+
+def clip_coef(norm: float, max_norm: float) -> float:
+    """clip_grad_norm_'s coefficient in float32: min(1, max_norm / (norm + 1e-6))."""
+    n32 = np.float32(norm)
+    c = np.float32(np.float32(max_norm) / np.float32(n32 + np.float32(1e-6)))
+    return float(min(c, np.float32(1.0)))
+
+
+def adamw_step(p: np.ndarray, grad: np.ndarray, gdtype: str, m: np.ndarray, v: np.ndarray, hp: dict,
+               post_stats: dict | None) -> bool:
+    """One gated, clipped AdamW step on float32 host arrays, in place.
+
+    ``hp``: lr, beta1, beta2, eps, weight_decay, max_grad_norm, step, clip.  When
+    ``post_stats`` (the reduced gradient's stats) raise the float32 alarm, nothing is
+    updated and False is returned, as the page's train() skips the step.
+    """
+    if post_stats is not None and post_stats["nonfinite_fp32"]:
+        return False
+    k = adamw_scalars(hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], hp["weight_decay"], hp["step"])
+    use = 1 if (hp.get("clip") and post_stats is not None) else 0
+    coef = clip_coef(post_stats["norm"], hp["max_grad_norm"]) if use else 1.0
+    for a in (p, m, v):
+        assert a.dtype == np.float32 and a.flags["C_CONTIGUOUS"]
+    g = np.ascontiguousarray(grad)
+    rc = _load().oracle_adamw(p.ctypes.data, g.ctypes.data, DTYPE_CODES[gdtype], m.ctypes.data, v.ctypes.data,
+                              p.size, coef, use, k["decay"], k["omb1"], k["beta2"], k["omb2"], k["bc2s"], k["eps"],
+                              k["step_size"])
+    if rc != 0:
+        raise ValueError("bad grad dtype")
+    return True

@@ -288,3 +288,46 @@ uint32_t oracle_round_f32(float x, uint32_t dtype)
     if (dtype == ORACLE_BF16) return round_to_format(x, 7, 8, -126, 127);
     return round_to_format(x, 10, 5, -14, 15);
 }
+
+/* ------------------------------------------------------------------------ */
+/* One AdamW step with gradient clipping, in place.                          */
+/* [AWS] "Use case: Testing the checks on SageMaker HyperPod": AdamW with     */
+/* betas (0.9, 0.95), weight decay 0.1, gradient clipping at 1.0; `train()`   */
+/* clips (clip_grad_norm_), skips the step when the reduced gradient is not   */
+/* finite, else steps.  The pages fix no float arithmetic; the reading here   */
+/* is this sequence of separately rounded float32 operations (decoupled       */
+/* weight decay, bias-corrected moments), with the scalars already rounded    */
+/* to float32 by the caller:                                                  */
+/*   g  = grad * coef                       (coef == 1: g = grad)            */
+/*   p  = p * decay                         decay = 1 - lr * wd               */
+/*   m  = m + omb1 * (g - m)                omb1 = 1 - beta1                  */
+/*   v  = v * beta2 + (g * g) * omb2        omb2 = 1 - beta2                  */
+/*   d  = sqrt(v) / bc2s + eps              bc2s = sqrt(1 - beta2^t)          */
+/*   p  = p - step_size * (m / d)           step_size = lr / (1 - beta1^t)    */
+/* grad dtype: 1 = float32, 2 = bfloat16, 3 = float16 (this file's codes).    */
+/* ------------------------------------------------------------------------ */
+int oracle_adamw(float *p, const void *grad, uint32_t gdtype, float *m, float *v, uint64_t n, float coef,
+                 int use_coef, float decay, float omb1, float beta2, float omb2, float bc2s, float eps,
+                 float step_size)
+{
+    const unsigned char *g8 = (const unsigned char *)grad;
+    if (gdtype != ORACLE_F32 && gdtype != ORACLE_BF16 && gdtype != ORACLE_F16) return -1;
+    for (uint64_t i = 0; i < n; ++i) {
+        volatile float g = load_as_float(g8, i, gdtype);
+        if (use_coef) g = g * coef;
+        volatile float pp = p[i] * decay;
+        volatile float diff = g - m[i];
+        volatile float mm = m[i] + omb1 * diff;
+        volatile float g2 = g * g;
+        volatile float t2 = g2 * omb2;
+        volatile float vv = v[i] * beta2 + t2;
+        volatile float r = sqrtf(vv);
+        volatile float den = r / bc2s + eps;
+        volatile float q = mm / den;
+        volatile float upd = step_size * q;
+        p[i] = pp - upd;
+        m[i] = mm;
+        v[i] = vv;
+    }
+    return 0;
+}
