@@ -28,7 +28,8 @@ __all__ = [
     "sdc_plan_create", "sdc_plan_destroy", "sdc_workspace_size", "sdc_plan_info", "sdc_fingerprint",
     "sdc_xorsum", "sdc_xorsum_compare", "sdc_vote", "sdc_grad_scan", "sdc_grad_average_scan_workspace_size",
     "sdc_grad_average_scan", "sdc_grad_average_scan_noalloc", "NOALLOC_SCRATCH_BYTES", "sdc_status_string", "sdc_last_error", "Plan", "vote", "xorsum_compare",
-    "grad_average_scan", "ring_audit", "ring_result", "sdc_ring_audit", "RING_SUMMARY_DTYPE", "decode_stats", "decode_summary", "pages_verdict", "library_path",
+    "grad_average_scan", "AdamWFingerprint", "AdamWHparams", "sdc_opt_state_create", "sdc_opt_state_destroy",
+    "sdc_adamw_fingerprint", "ring_audit", "ring_result", "sdc_ring_audit", "RING_SUMMARY_DTYPE", "decode_stats", "decode_summary", "pages_verdict", "library_path",
 ]
 
 DTYPE_RAW, DTYPE_F32, DTYPE_BF16, DTYPE_F16 = 0, 1, 2, 3
@@ -53,6 +54,12 @@ class SdcError(RuntimeError):
     def __init__(self, fn: str, status: int, detail: str):
         super().__init__(f"{fn}: {sdc_status_string(status)} ({status}): {detail}")
         self.status = status
+
+
+class AdamWHparams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float), ("eps", ctypes.c_float),
+                ("weight_decay", ctypes.c_float), ("max_grad_norm", ctypes.c_float), ("step", ctypes.c_uint32),
+                ("clip", ctypes.c_uint32)]
 
 
 class _PlanOpts(ctypes.Structure):
@@ -83,6 +90,10 @@ def _load() -> ctypes.CDLL:
         "sdc_grad_average_scan": ([ctypes.POINTER(vp), u32, vp, u64, u32, vp, vp, vp, sz, vp], ctypes.c_int),
         "sdc_grad_average_scan_noalloc": ([ctypes.POINTER(vp), u32, vp, u64, u32, vp, vp, vp], ctypes.c_int),
         "sdc_ring_audit": ([vp, u32, u32, u32, vp, vp, vp, vp, vp, vp], ctypes.c_int),
+        "sdc_opt_state_create": ([vp, ctypes.POINTER(vp), u32, ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                  ctypes.POINTER(vp)], ctypes.c_int),
+        "sdc_opt_state_destroy": ([vp], ctypes.c_int),
+        "sdc_adamw_fingerprint": ([vp, vp, ctypes.POINTER(AdamWHparams), vp, vp, vp, sz, vp], ctypes.c_int),
         "sdc_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "sdc_last_error": ([], ctypes.c_char_p),
     }
@@ -194,6 +205,25 @@ def sdc_ring_audit(d_table: int, n: int, L: int, offset: int, d_mismatch: int, d
                    d_ambiguous: int, d_summary: int, stream: int) -> None:
     _check("sdc_ring_audit", _lib.sdc_ring_audit(d_table, n, L, offset, d_mismatch, d_hits, d_culprit, d_ambiguous,
                                                  d_summary, stream))
+
+
+def sdc_opt_state_create(plan: int, grads: list[int], grad_dtype: int, exp_avg: list[int],
+                         exp_avg_sq: list[int]) -> int:
+    arr = lambda xs: (ctypes.c_void_p * max(1, len(xs)))(*xs)
+    out = ctypes.c_void_p()
+    _check("sdc_opt_state_create", _lib.sdc_opt_state_create(plan, arr(grads), grad_dtype, arr(exp_avg),
+                                                             arr(exp_avg_sq), ctypes.byref(out)))
+    return out.value
+
+
+def sdc_opt_state_destroy(state: int) -> None:
+    _check("sdc_opt_state_destroy", _lib.sdc_opt_state_destroy(state))
+
+
+def sdc_adamw_fingerprint(plan: int, state: int, hp: AdamWHparams, d_post: int, d_fp_out: int, d_ws: int,
+                          ws_bytes: int, stream: int) -> None:
+    _check("sdc_adamw_fingerprint", _lib.sdc_adamw_fingerprint(plan, state, ctypes.byref(hp), d_post, d_fp_out, d_ws,
+                                                               ws_bytes, stream))
 
 
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -312,6 +342,43 @@ class Plan:
     def close(self) -> None:
         if getattr(self, "handle", None):
             sdc_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class AdamWFingerprint:
+    """Clip + AdamW step + fingerprint of the written weights for a Plan of F32 weights.
+
+    ``grads``: T tensors (the averaged gradient, shared by the replicas);
+    ``exp_avg``/``exp_avg_sq``: R x T float32 tensors.
+    """
+
+    def __init__(self, plan: "Plan", grads, exp_avg, exp_avg_sq):
+        self.plan = plan
+        self._keep = (grads, exp_avg, exp_avg_sq)
+        gd = dtype_code(grads[0]) if grads else DTYPE_F32
+        flat = lambda xss: [t.data_ptr() if t.numel() else 0 for ts in xss for t in ts]
+        self.handle = sdc_opt_state_create(plan.handle, [g.data_ptr() if g.numel() else 0 for g in grads], gd,
+                                           flat(exp_avg), flat(exp_avg_sq))
+
+    def step(self, hp: dict, post=None, out=None, stream=None):
+        torch = _torch()
+        if out is None:
+            out = torch.empty((self.plan.R, self.plan.T, 2), dtype=torch.int64, device=self.plan.device)
+        h = AdamWHparams(hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], hp["weight_decay"],
+                         hp.get("max_grad_norm", 1.0), hp["step"], 1 if hp.get("clip") else 0)
+        sdc_adamw_fingerprint(self.plan.handle, self.handle, h, post.data_ptr() if post is not None else 0,
+                              out.data_ptr(), self.plan._ws_ptr(), self.plan.ws_bytes, _stream_handle(stream))
+        return out
+
+    def close(self):
+        if getattr(self, "handle", None):
+            sdc_opt_state_destroy(self.handle)
             self.handle = None
 
     def __del__(self):
