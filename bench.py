@@ -365,6 +365,8 @@ def bench_rows(args, dev, stream, peaks, sdc, W, torch, np, only=None) -> dict:
         rows["grad_scan"] = {"workload": "4 x bf16 local grads of the 1b layout", "ms": ms, "bytes": nbytes,
                              "GB_s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"]}
         del gplan
+    if only in (None, "adamw_fingerprint"):
+        rows.update(bench_adamw_row(args, dev, stream, peaks, sdc, W, torch))
     if only in (None, "xorsum"):
         # xorsum + pair compare of 4 bf16 buffers against copies (original vs recomputed)
         rec = [b.clone() for b in bufs]
@@ -387,6 +389,34 @@ def bench_rows(args, dev, stream, peaks, sdc, W, torch, np, only=None) -> dict:
     if not getattr(args, "no_big_rows", False):
         rows.update(bench_big_rows(args, dev, stream, peaks, sdc, W, torch, only))
     return rows
+
+
+def bench_adamw_row(args, dev, stream, peaks, sdc, W, torch) -> dict:
+    """Fused clip + AdamW step + fingerprint on one fp32 replica of the 1b layout, bf16 averaged gradient."""
+    layout = W.layout_1b(args.layers)
+    gen = W.generator(21, dev)
+    weights = [[W.normal(s, 0.02, torch.float32, gen, dev) for _, s in layout]]
+    grads = [W.normal(s, 1e-3, torch.bfloat16, gen, dev) for _, s in layout]
+    m = [[torch.zeros(s, dtype=torch.float32, device=dev) for _, s in layout]]
+    v = [[torch.zeros(s, dtype=torch.float32, device=dev) for _, s in layout]]
+    plan = sdc.Plan(weights)
+    opt = sdc.AdamWFingerprint(plan, grads, m, v)
+    fp = torch.empty((1, len(layout), 2), dtype=torch.int64, device=dev)
+    hp = {"lr": 3e-4, "beta1": 0.9, "beta2": 0.95, "eps": 1e-8, "weight_decay": 0.1, "max_grad_norm": 1.0,
+          "step": 1, "clip": 0}
+    ms = _time_loop(lambda: opt.step(hp, out=fp, stream=stream), max(5, args.steps // 20), stream, torch)
+    ms_fp = _time_loop(lambda: plan.fingerprint(out=fp, stream=stream), max(5, args.steps // 20), stream, torch)
+    n = W.layout_numel(layout)
+    nbytes = n * (4 + 2 + 4 + 4 + 4 + 4 + 4)  # read p, g(bf16), m, v; write p, m, v
+    out = {"adamw_fingerprint": {"workload": "1 fp32 replica of the 1b layout, bf16 averaged gradient, fp32 moments: "
+                                 "AdamW step + fingerprint of the written weights in one pass",
+                                 "ms": ms, "bytes": nbytes, "GB_s": nbytes / ms / 1e6,
+                                 "frac_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"],
+                                 "separate_fingerprint_reread_ms": ms_fp}}
+    opt.close()
+    del plan, weights, grads, m, v
+    torch.cuda.empty_cache()
+    return out
 
 
 def bench_big_rows(args, dev, stream, peaks, sdc, W, torch, only) -> dict:
@@ -496,7 +526,7 @@ def main(argv=None) -> None:
     ap.add_argument("--quick", action="store_true", help="only the timed fingerprint step (no rows/e2e/cpu)")
     ap.add_argument("--no-big-rows", action="store_true", help="skip the 8b and stress rows")
     ap.add_argument("--only", choices=["grad_average_scan", "grad_scan", "xorsum", "fingerprint_8b",
-                                       "fingerprint_stress"], default=None,
+                                       "fingerprint_stress", "adamw_fingerprint"], default=None,
                     help="time one row alone (profiling)")
     ap.add_argument("--layers", type=int, default=24,
                     help="decoder layers of the 1b layout (24 = the benchmark workload; fewer for profiling)")

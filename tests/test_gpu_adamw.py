@@ -32,9 +32,20 @@ def _setup(R, sizes, gdtype, seed, misalign_moments=False):
             t = t.abs() * 1e-3
         return t[1:] if misalign_moments else t[:n]
 
-    m = [[moment(n, False) for n in sizes] for _ in range(R)]
-    v = [[moment(n, True) for n in sizes] for _ in range(R)]
+    m0 = [moment(n, False) for n in sizes]
+    v0 = [moment(n, True) for n in sizes]
+    # data-parallel replicas hold identical optimizer states (copies keep the views' alignment)
+    m = [m0] + [[_same_alignment_copy(t) for t in m0] for _ in range(R - 1)]
+    v = [v0] + [[_same_alignment_copy(t) for t in v0] for _ in range(R - 1)]
     return weights, grads, m, v
+
+
+def _same_alignment_copy(t):
+    off = (t.data_ptr() % 16) // 4
+    buf = torch.empty(t.numel() + off, dtype=t.dtype, device=t.device)
+    out = buf[off:]
+    out.copy_(t)
+    return out
 
 
 def _oracle_step(weights, grads, m, v, hp, post):
