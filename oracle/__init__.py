@@ -10,6 +10,9 @@ Sources (web pages on silent data corruption):
   [AEGIS] "Safeguarding LLM Training at Scale: Online SDC Detection and
           Insights from 35 Million GPU Hours" (review page).
 
+The GEMM checksum functions at the end are plain numpy in float64; their
+parity with the tensor-core kernel is up to the rounding bound they state.
+
 The element loops live in ``sdc_oracle.c`` (plain scalar C, compiled with gcc
 on first use); the vote and the exact rounding of the sum of squares are plain
 Python.  Every function takes host numpy arrays.
@@ -427,3 +430,64 @@ def adamw_step(p: np.ndarray, grad: np.ndarray, gdtype: str, m: np.ndarray, v: n
     if rc != 0:
         raise ValueError("bad grad dtype")
     return True
+
+
+# --------------------------------------------------------------------------
+# GEMM checksum  ([AEGIS] method section 2: (AB)1 against A(B1), the checksum
+# taken from the float32 accumulator before the bfloat16 output is rounded)
+# --------------------------------------------------------------------------
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bfloat16 bit patterns (uint16) -> float64, exactly."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def abft_product(A_bits: np.ndarray, W_bits: np.ndarray) -> np.ndarray:
+    """C = A . W^T in float64 for bf16 A [M, K] and W [N, K] (K contiguous in both).
+
+    Every product of two bf16 values is exact in float64; the K-term sums round at
+    most K * 2^-53 of sum_k |a| |w|, far below the float32 accumulation error the
+    check bounds."""
+    return bf16_to_f64(A_bits) @ bf16_to_f64(W_bits).T
+
+
+def abft_row_checksum(C: np.ndarray) -> np.ndarray:
+    """(AB)1: each output row summed."""
+    return C.sum(axis=1)
+
+
+def abft_reference(A_bits: np.ndarray, W_bits: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """A(B1) and the magnitude sum_k |A[i,k]| sum_j |W[j,k]| of each row, float64.
+
+    B1 for C = A W^T is W^T 1: the column sums of W over its N rows."""
+    A = bf16_to_f64(A_bits)
+    W = bf16_to_f64(W_bits)
+    w1 = W.sum(axis=0)
+    wabs = np.abs(W).sum(axis=0)
+    return A @ w1, np.abs(A) @ wabs
+
+
+def abft_bound(mag: np.ndarray, N: int, K: int) -> np.ndarray:
+    """Rounding bound of a row checksum taken from a float32 accumulator.
+
+    Each of the K float32 accumulation steps of one output may lose up to two
+    units in the last place of its partial sum (g = K 2^-22 per output to first
+    order, g^2 beyond it); the float64 sums of the check lose (N + K + 64) 2^-52
+    of the magnitude; subnormals flushed to zero lose 2^-126 per product and per
+    step."""
+    g = K * 2.0 ** -22
+    return (g * (1.0 + g) + (N + K + 64) * 2.0 ** -52) * np.asarray(mag, dtype=np.float64) + 2.0 * K * N * 2.0 ** -126
+
+
+def abft_verify(rowsum: np.ndarray, A_bits: np.ndarray, W_bits: np.ndarray, tol_scale: float = 1.0) -> dict:
+    """The check of one GEMM: residual = checksum - A(W^T 1), the bound, and the
+    row flags (a row is flagged unless |residual| <= tol_scale * bound, so a NaN
+    residual flags)."""
+    M, K = A_bits.shape
+    N = W_bits.shape[0]
+    ref, mag = abft_reference(A_bits, W_bits)
+    residual = np.asarray(rowsum, dtype=np.float64) - ref
+    bound = abft_bound(mag, N, K)
+    with np.errstate(invalid="ignore"):
+        flag = ~(np.abs(residual) <= tol_scale * bound)
+    return {"residual": residual, "bound": bound, "flag": flag.astype(np.uint8), "n_flagged": int(flag.sum())}

@@ -17,6 +17,12 @@ Workloads (sizes follow the parameter layouts below):
   8b        Llama-style layout (32 layers, d=4096, 8 kv heads of 128,
             ffn=14336, vocab=128256), bf16 N(0, 0.02), 8 replicas; one
             replica gets 16 elements XORed with non-zero 16-bit masks.
+  gemm      a linear layer's forward product C = A W^T: A [M, K] bf16 N(0, 1)
+            activations, W [N, K] bf16 N(0, 0.02) weights; the benchmark
+            shape is the 8b layout's MLP up-projection (M = 8192 tokens,
+            N = 14336, K = 4096).  A fault is planted by XORing bits of chosen
+            elements of a copy of A (the operand as a faulty unit would read
+            it), the clean A being the reference.
   stress    100,000 tensors, numel = floor(exp(U(0, ln(1e6 + 1)))), dtype
             uniform over float32/bf16/float16, packed per replica in one flat
             buffer (element-aligned starts), 3 replicas with one bit flip;
@@ -250,3 +256,28 @@ def stress(device, seed: int = 5, n_tensors: int = 100_000, n_replicas: int = 3,
     return {"replicas": reps, "flats": flats, "numel": numel, "dtypes": dt,
             "truth": {"replica": r, "tensor": k, "element": e, "bit": bit},
             "pairs": {"orig": orig, "recomp": recomp, "flats": (pflat, rflat), "differ": pair_truth}}
+
+
+GEMM_8B_UP = (8192, 14336, 4096)  # tokens, ffn, d of the 8b layout
+
+
+def gemm_operands(M: int, N: int, K: int, device, seed: int = 6, a_std: float = 1.0, w_std: float = 0.02) -> dict:
+    """Seeded bf16 A [M, K] (activations) and W [N, K] (weights)."""
+    gen = generator(seed, device)
+    A = normal((M, K), a_std, torch.bfloat16, gen, device)
+    W = normal((N, K), w_std, torch.bfloat16, gen, device)
+    return {"A": A, "W": W}
+
+
+def gemm_fault(A: torch.Tensor, rows: list[int], seed: int = 7, mask: int = 0x4000) -> tuple[torch.Tensor, list]:
+    """A copy of A with one seeded element of each listed row XORed with `mask`
+    (default: the top exponent bit of a bf16).  Returns (faulty A, [(row, col)])."""
+    rng = np.random.default_rng(seed)
+    Af = A.clone()
+    K = A.shape[1]
+    where = []
+    for r in rows:
+        c = int(rng.integers(0, K))
+        xor_element(Af, r * K + c, mask)
+        where.append((int(r), c))
+    return Af, where

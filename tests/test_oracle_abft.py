@@ -1,0 +1,169 @@
+"""Pins of the oracle's GEMM checksum.
+
+Source: "Safeguarding LLM Training at Scale: Online SDC Detection and Insights
+from 35 Million GPU Hours" (review page), method section 2: the matrix checksum
+compares (AB)1 with A(B1), the checksum taken from the float32 accumulator
+before the bfloat16 output is rounded.  Here the product is C = A W^T (a linear
+layer's forward pass), so B1 = W^T 1.
+
+Each pin is independent of the oracle's own arithmetic: pure-Python integer and
+Fraction brute force, closed forms for planted operand faults, and an emulation
+of float32 accumulation (round-to-nearest and truncating, per step and per
+16-wide block) against which the rounding bound must hold.
+"""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+
+
+def _bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 values that are exact in bfloat16 -> their bit patterns."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    assert np.all(b & 0xFFFF == 0), "value not exact in bf16"
+    return (b >> 16).astype(np.uint16)
+
+
+def _bf16_round(x: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 bit patterns, round to nearest even (finite inputs)."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    b = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
+    return b.astype(np.uint16)
+
+
+def _int_operands(M, N, K, seed, lo=-16, hi=16):
+    rng = np.random.default_rng(seed)
+    A = rng.integers(lo, hi + 1, size=(M, K))
+    W = rng.integers(lo, hi + 1, size=(N, K))
+    return A, W, _bf16_bits(A.astype(np.float32)), _bf16_bits(W.astype(np.float32))
+
+
+def test_bf16_decode_fixed_patterns():
+    bits = np.array([0x3F80, 0xC000, 0x0000, 0x8000, 0x7F80, 0xFF80, 0x0001, 0x4049], dtype=np.uint16)
+    v = oracle.bf16_to_f64(bits)
+    assert list(v[:6]) == [1.0, -2.0, 0.0, -0.0, np.inf, -np.inf]
+    assert v[6] == 2.0 ** -133  # smallest subnormal
+    assert v[7] == 3.140625  # 0x4049: 1.5703125 * 2
+    assert np.isnan(oracle.bf16_to_f64(np.array([0x7FC0], dtype=np.uint16))[0])
+
+
+def test_product_matches_fraction_brute_force():
+    # non-square shapes so a transposed operand cannot pass; dyadic values exact in bf16
+    M, N, K = 3, 5, 7
+    rng = np.random.default_rng(1)
+    A = (rng.integers(-255, 256, size=(M, K)) * 2.0 ** rng.integers(-20, 20, size=(M, K))).astype(np.float32)
+    W = (rng.integers(-255, 256, size=(N, K)) * 2.0 ** rng.integers(-20, 20, size=(N, K))).astype(np.float32)
+    Ab, Wb = _bf16_bits(A), _bf16_bits(W)
+    C = oracle.abft_product(Ab, Wb)
+    assert C.shape == (M, N)
+    for i in range(M):
+        for j in range(N):
+            exact = sum(Fraction(float(A[i, k])) * Fraction(float(W[j, k])) for k in range(K))
+            assert abs(Fraction(C[i, j]) - exact) <= Fraction(K) * Fraction(2) ** -52 * sum(
+                abs(Fraction(float(A[i, k])) * Fraction(float(W[j, k]))) for k in range(K))
+
+
+def test_checksum_identity_on_integers():
+    # integer data: every sum is exact, so (A W^T) 1 == A (W^T 1) holds with equality
+    M, N, K = 16, 24, 40
+    A, W, Ab, Wb = _int_operands(M, N, K, 2)
+    rowsum = oracle.abft_row_checksum(oracle.abft_product(Ab, Wb))
+    ref, mag = oracle.abft_reference(Ab, Wb)
+    brute = [sum(int(A[i, k]) * int(W[j, k]) for j in range(N) for k in range(K)) for i in range(M)]
+    brute_mag = [sum(abs(int(A[i, k])) * abs(int(W[j, k])) for j in range(N) for k in range(K)) for i in range(M)]
+    assert list(rowsum) == brute
+    assert list(ref) == brute
+    assert list(mag) == brute_mag
+    v = oracle.abft_verify(rowsum, Ab, Wb)
+    assert v["n_flagged"] == 0 and np.all(v["residual"] == 0)
+
+
+@pytest.mark.parametrize("delta", [1, -3, 7])
+def test_planted_operand_fault_closed_form(delta):
+    # the GEMM reads A' = A + delta e_(i,k); the check uses A: the residual of row i
+    # is delta * sum_j W[j, k] and every other row's is zero
+    M, N, K = 8, 12, 20
+    A, W, Ab, Wb = _int_operands(M, N, K, 3, lo=-8, hi=8)
+    i, k = 5, 11
+    Af = A.copy()
+    Af[i, k] += delta
+    rowsum = oracle.abft_row_checksum(oracle.abft_product(_bf16_bits(Af.astype(np.float32)), Wb))
+    v = oracle.abft_verify(rowsum, Ab, Wb, tol_scale=1.0)
+    expect = np.zeros(M)
+    expect[i] = delta * int(W[:, k].sum())
+    assert np.array_equal(v["residual"], expect)
+    # integers: the bound is far below 1, so the row flags exactly when the column sum is non-zero
+    assert v["n_flagged"] == int(W[:, k].sum() != 0)
+    assert v["flag"][i] == int(W[:, k].sum() != 0)
+
+
+def _emulate_fp32(Af: np.ndarray, Wf: np.ndarray, mode: str) -> np.ndarray:
+    """float32 accumulators of A W^T: per-step round-to-nearest, per-step truncation,
+    or 16-wide blocks summed exactly then truncated into the accumulator."""
+    M, K = Af.shape
+    N = Wf.shape[0]
+    acc = np.zeros((M, N), dtype=np.float64)
+
+    def trunc32(x):
+        r = x.astype(np.float32).astype(np.float64)
+        over = np.abs(r) > np.abs(x)
+        r[over] = np.nextafter(r[over].astype(np.float32), np.float32(0)).astype(np.float64)
+        return r
+
+    if mode == "block16":
+        for k0 in range(0, K, 16):
+            blk = acc + Af[:, k0:k0 + 16] @ Wf[:, k0:k0 + 16].T
+            acc = trunc32(blk)
+        return acc
+    for k in range(K):
+        x = acc + np.outer(Af[:, k], Wf[:, k])  # the product of two bf16 is exact in float64
+        acc = x.astype(np.float32).astype(np.float64) if mode == "rn" else trunc32(x)
+    return acc
+
+
+@pytest.mark.parametrize("mode", ["rn", "trunc", "block16"])
+@pytest.mark.parametrize("dist", ["normal", "positive", "dominant", "wide"])
+def test_bound_covers_float32_accumulation(mode, dist):
+    M, N, K = 8, 32, 512
+    rng = np.random.default_rng(4)
+    if dist == "normal":
+        A32 = rng.standard_normal((M, K)).astype(np.float32)
+        W32 = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    elif dist == "positive":  # no cancellation: partial sums grow, rounding errors add up
+        A32 = rng.uniform(0.5, 1.0, (M, K)).astype(np.float32)
+        W32 = rng.uniform(0.5, 1.0, (N, K)).astype(np.float32)
+    elif dist == "dominant":  # positive, over 12 binades, one large first term: every later
+        # product is added to a partial sum whose unit in the last place exceeds its low bits
+        A32 = (rng.uniform(0.5, 1.0, (M, K)) * 2.0 ** -rng.integers(0, 12, (M, K))).astype(np.float32)
+        W32 = (rng.uniform(0.5, 1.0, (N, K)) * 2.0 ** -rng.integers(0, 12, (N, K))).astype(np.float32)
+        A32[:, 0], W32[:, 0] = 2.0 ** 10, 2.0 ** 4
+    else:  # magnitudes over 40 binades
+        A32 = (rng.standard_normal((M, K)) * 2.0 ** rng.integers(-20, 20, (M, K))).astype(np.float32)
+        W32 = (rng.standard_normal((N, K)) * 2.0 ** rng.integers(-20, 20, (N, K))).astype(np.float32)
+    Ab, Wb = _bf16_round(A32), _bf16_round(W32)
+    acc = _emulate_fp32(oracle.bf16_to_f64(Ab), oracle.bf16_to_f64(Wb), mode)
+    v = oracle.abft_verify(acc.sum(axis=1), Ab, Wb, tol_scale=1.0)
+    assert v["n_flagged"] == 0
+    ratio = np.max(np.abs(v["residual"]) / v["bound"])
+    assert ratio <= 1.0
+    # not vacuous: to first order the bound is K 2^-22 of the magnitude
+    _, mag = oracle.abft_reference(Ab, Wb)
+    assert np.all(v["bound"] <= 1.01 * K * 2.0 ** -22 * mag + 1e-30)
+    if dist == "dominant" and mode == "trunc":
+        assert ratio > 0.05  # one-sided truncation errors add up to a sizeable share of the bound
+
+
+def test_flag_rule_edges():
+    # A = 0: reference and magnitude vanish and the bound is its subnormal term 2 K N 2^-126
+    M, N, K = 4, 8, 16
+    Ab = np.zeros((M, K), dtype=np.uint16)
+    Wb = _bf16_round(np.ones((N, K), np.float32))
+    b = 2.0 * K * N * 2.0 ** -126
+    rowsum = np.array([b, 2 * b, np.nan, -np.inf])
+    v = oracle.abft_verify(rowsum, Ab, Wb, tol_scale=1.0)
+    assert np.all(v["bound"] == b)
+    assert list(v["flag"]) == [0, 1, 1, 1]  # equality passes; NaN and infinities flag
+    v = oracle.abft_verify(rowsum, Ab, Wb, tol_scale=2.0)
+    assert list(v["flag"]) == [0, 0, 1, 1]
