@@ -252,6 +252,47 @@ sdc_status sdc_adamw_fingerprint(const sdc_plan *plan, const sdc_opt_state *stat
                                  const sdc_grad_stats *d_post, uint64_t *d_fp_out, void *d_ws, size_t ws_bytes,
                                  sdc_stream_t stream);
 
+/* ---------------------------------------------------------------- GEMM checksums (AEGIS) */
+
+/* Counts written by sdc_abft_verify. */
+typedef struct {
+    uint32_t n_flagged;  /* rows whose checksum residual exceeds tol_scale x bound */
+    uint32_t reserved;
+} sdc_abft_summary;
+
+/* Workspace bytes of sdc_abft_gemm / sdc_abft_verify (one buffer may serve both
+ * when they are ordered on one stream). */
+size_t sdc_abft_workspace_size(uint32_t M, uint32_t N, uint32_t K);
+
+/* The checksum sensor: C = A . W^T on the tensor cores (tcgen05, accumulator
+ * in TMEM, operands staged by TMA) with each output row's checksum formed
+ * from the float32 accumulator before the bfloat16 store.  [AEGIS] method
+ * section 2: compare (AB)1 with A(B1), with the checksum taken from the fp32
+ * accumulator inside the kernel.  d_A: device bf16 [M][K]; d_W: device bf16
+ * [N][K] (both row-major, K contiguous, 16-byte aligned); d_C: device bf16
+ * [M][N].  M a multiple of 128, N of 256, K of 64.  d_rowsum: device double
+ * [M], sum over j of the fp32 accumulator of C[i][j] (summed in float64, tile
+ * partials in a fixed order); d_aborted: device uint32, 1 if a bounded wait
+ * of the GEMM gave up (results then invalid). */
+sdc_status sdc_abft_gemm(const void *d_A, const void *d_W, void *d_C, uint32_t M, uint32_t N, uint32_t K,
+                         double *d_rowsum, uint32_t *d_aborted, void *d_ws, size_t ws_bytes, sdc_stream_t stream);
+
+/* The checksum verifier: per row, the reference A(W^T 1) in float64, the
+ * residual d_residual[i] = d_rowsum[i] - reference, the rounding bound
+ * d_bound[i] = (g (1 + g) + (N + K + 64) 2^-52) mag + 2 K N 2^-126 with
+ * g = K 2^-22 and mag = sum_k |A[i][k]| sum_j |W[j][k]| (each float32
+ * accumulation step may lose two units in the last place of its partial sum,
+ * the float64 sums of the check and flushed subnormals are covered, so a
+ * correct product stays inside it), and d_flag[i] = 1 unless
+ * |residual| <= tol_scale * bound (a NaN residual flags; tol_scale > 0; the
+ * page's adaptive threshold has no published constants).  d_summary counts
+ * the flagged rows.  Same shapes and workspace as sdc_abft_gemm; K <= 2^20.
+ * Errors: SDC_ERR_BAD_ARG for shapes, SDC_ERR_BAD_POINTER for misalignment,
+ * SDC_ERR_WS_TOO_SMALL, SDC_ERR_WRONG_DEVICE. */
+sdc_status sdc_abft_verify(const void *d_A, const void *d_W, uint32_t M, uint32_t N, uint32_t K, const double *d_rowsum,
+                           float tol_scale, double *d_residual, double *d_bound, uint8_t *d_flag,
+                           sdc_abft_summary *d_summary, void *d_ws, size_t ws_bytes, sdc_stream_t stream);
+
 /* ---------------------------------------------------------------- ring replay audit */
 
 /* Counts written by sdc_ring_audit. */

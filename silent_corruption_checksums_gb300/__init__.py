@@ -94,6 +94,9 @@ def _load() -> ctypes.CDLL:
                                   ctypes.POINTER(vp)], ctypes.c_int),
         "sdc_opt_state_destroy": ([vp], ctypes.c_int),
         "sdc_adamw_fingerprint": ([vp, vp, ctypes.POINTER(AdamWHparams), vp, vp, vp, sz, vp], ctypes.c_int),
+        "sdc_abft_workspace_size": ([u32, u32, u32], sz),
+        "sdc_abft_gemm": ([vp, vp, vp, u32, u32, u32, vp, vp, vp, sz, vp], ctypes.c_int),
+        "sdc_abft_verify": ([vp, vp, u32, u32, u32, vp, ctypes.c_float, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
         "sdc_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "sdc_last_error": ([], ctypes.c_char_p),
     }
@@ -235,6 +238,21 @@ def sdc_grad_average_scan_noalloc(bufs: list[int], d_avg: int, numel: int, dtype
     arr = (ctypes.c_void_p * max(1, len(bufs)))(*bufs)
     _check("sdc_grad_average_scan_noalloc", _lib.sdc_grad_average_scan_noalloc(arr, len(bufs), d_avg, numel, dtype,
                                                                                d_pre, d_post, stream))
+
+
+def sdc_abft_workspace_size(M: int, N: int, K: int) -> int:
+    return int(_lib.sdc_abft_workspace_size(M, N, K))
+
+
+def sdc_abft_gemm(d_A: int, d_W: int, d_C: int, M: int, N: int, K: int, d_rowsum: int, d_aborted: int, d_ws: int,
+                  ws_bytes: int, stream: int) -> None:
+    _check("sdc_abft_gemm", _lib.sdc_abft_gemm(d_A, d_W, d_C, M, N, K, d_rowsum, d_aborted, d_ws, ws_bytes, stream))
+
+
+def sdc_abft_verify(d_A: int, d_W: int, M: int, N: int, K: int, d_rowsum: int, tol_scale: float, d_residual: int,
+                    d_bound: int, d_flag: int, d_summary: int, d_ws: int, ws_bytes: int, stream: int) -> None:
+    _check("sdc_abft_verify", _lib.sdc_abft_verify(d_A, d_W, M, N, K, d_rowsum, tol_scale, d_residual, d_bound,
+                                                   d_flag, d_summary, d_ws, ws_bytes, stream))
 
 
 # ---------------------------------------------------------------- torch conveniences
@@ -467,6 +485,51 @@ def grad_average_scan(bufs, out=None, stream=None, ws=None):
     sdc_grad_average_scan([b.data_ptr() for b in bufs], out.data_ptr(), numel, code, pre.data_ptr(),
                           post.data_ptr(), ws.data_ptr() if ws is not None else 0, need, _stream_handle(stream))
     return out, pre, post
+
+
+class AbftGemm:
+    """C = A . W^T on the tensor cores with the per-row accumulator checksum, and
+    its check against A (W^T 1).  A: bf16 [M, K], W: bf16 [N, K], both contiguous
+    CUDA tensors; M a multiple of 128, N of 256, K of 64.  Output and scratch
+    buffers are allocated once per shape and reused by every call."""
+
+    def __init__(self, M: int, N: int, K: int, device):
+        torch = _torch()
+        self.M, self.N, self.K = M, N, K
+        self.C = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+        self.rowsum = torch.empty(M, dtype=torch.float64, device=device)
+        self.aborted = torch.zeros(1, dtype=torch.int32, device=device)
+        self.residual = torch.empty(M, dtype=torch.float64, device=device)
+        self.bound = torch.empty(M, dtype=torch.float64, device=device)
+        self.flag = torch.empty(M, dtype=torch.uint8, device=device)
+        self.summary = torch.zeros(2, dtype=torch.int32, device=device)
+        self.ws_bytes = sdc_abft_workspace_size(M, N, K)
+        self.ws = _ws(self.ws_bytes, device)
+
+    def _shape(self, A, W):
+        if tuple(A.shape) != (self.M, self.K) or tuple(W.shape) != (self.N, self.K):
+            raise ValueError(f"expected A [{self.M}, {self.K}] and W [{self.N}, {self.K}]")
+
+    def gemm(self, A, W, stream=None):
+        """The GEMM and its row checksums (self.C, self.rowsum; self.aborted != 0 if a wait gave up)."""
+        self._shape(A, W)
+        sdc_abft_gemm(A.data_ptr(), W.data_ptr(), self.C.data_ptr(), self.M, self.N, self.K, self.rowsum.data_ptr(),
+                      self.aborted.data_ptr(), self.ws.data_ptr(), self.ws_bytes, _stream_handle(stream))
+        return self.C
+
+    def verify(self, A, W, tol_scale: float = 1.0, rowsum=None, stream=None):
+        """The check (self.residual, self.bound, self.flag, self.summary[0] = flagged rows)."""
+        self._shape(A, W)
+        rs = self.rowsum if rowsum is None else rowsum
+        sdc_abft_verify(A.data_ptr(), W.data_ptr(), self.M, self.N, self.K, rs.data_ptr(), tol_scale,
+                        self.residual.data_ptr(), self.bound.data_ptr(), self.flag.data_ptr(),
+                        self.summary.data_ptr(), self.ws.data_ptr(), self.ws_bytes, _stream_handle(stream))
+        return self.flag
+
+    def __call__(self, A, W, tol_scale: float = 1.0, stream=None):
+        self.gemm(A, W, stream)
+        self.verify(A, W, tol_scale, stream=stream)
+        return self.C
 
 
 # ---------------------------------------------------------------- host-side decoding

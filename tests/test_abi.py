@@ -97,6 +97,20 @@ def test_host_validation_without_gpu(sdc):
     assert sdc.sdc_grad_average_scan_workspace_size(8192, 4, 2) == 256 + 5 * 128 * 24
     assert sdc.sdc_grad_average_scan_workspace_size(8192, 9, 2) == 0  # more than 8 buffers
     sdc.sdc_xorsum_compare(0, 0, 0, 0, 0, 0)  # n == 0 is a no-op
+    # GEMM checksum: operands checked, then shapes, before any CUDA call
+    with pytest.raises(sdc.SdcError) as ei:
+        sdc.sdc_abft_gemm(0, 4096, 8192, 128, 256, 64, 0, 0, 0, 0, 0)
+    assert ei.value.status == 1
+    for M, N, K in [(100, 256, 64), (128, 200, 64), (128, 256, 48), (0, 256, 64), (128, 256, 1 << 21)]:
+        with pytest.raises(sdc.SdcError) as ei:
+            sdc.sdc_abft_gemm(4096, 8192, 16384, M, N, K, 0, 0, 0, 0, 0)
+        assert ei.value.status == 9, (M, N, K)
+        with pytest.raises(sdc.SdcError) as ei:
+            sdc.sdc_abft_verify(4096, 8192, M, N, K, 0, 1.0, 0, 0, 0, 0, 0, 0, 0)
+        assert ei.value.status == 9, (M, N, K)
+    # tile partials (N/256 per row) + two K-long float64 column sums + the abort word, each rounded to 256
+    assert sdc.sdc_abft_workspace_size(128, 512, 64) == 2048 + 2 * 512 + 256
+    assert sdc.sdc_abft_workspace_size(1000, 256, 100) == 8192 + 2 * 1024 + 256
 
 
 def test_pages_verdict_decoding(sdc):

@@ -1,0 +1,143 @@
+"""GPU GEMM with the in-kernel row checksum versus the oracle.
+
+Source: "Safeguarding LLM Training at Scale: Online SDC Detection and Insights
+from 35 Million GPU Hours" (review page), method section 2.  The product C and
+the row checksums come from the tensor cores' float32 accumulator, whose
+summation order is the hardware's, so they are compared with the oracle's
+exact product within the rounding bound; the check's bound, residual and
+flags are compared with the oracle's on the kernel's checksums.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sdc_workloads as W
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+# one tile; K-blocks past the 4-stage ring (phase wrap); several tiles each way; a larger case
+SHAPES = [(128, 256, 64), (256, 512, 320), (384, 768, 1024), (1024, 2048, 4096)]
+
+
+@pytest.fixture(scope="module")
+def sdc():
+    import silent_corruption_checksums_gb300 as m
+    return m
+
+
+def _bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _elem_error_bound(Ab, Wb, K):
+    """Per-element bound on |float32 accumulator - exact| (the row bound's first and third terms)."""
+    mag = np.abs(oracle.bf16_to_f64(Ab)) @ np.abs(oracle.bf16_to_f64(Wb)).T
+    g = K * 2.0 ** -22
+    return g * (1.0 + g) * mag + 2.0 * K * 2.0 ** -126
+
+
+def _check_clean(g, Ab, Wb, M, N, K):
+    exact = oracle.abft_product(Ab, Wb)
+    e = _elem_error_bound(Ab, Wb, K)
+    C = g.C.float().cpu().numpy().astype(np.float64)
+    # round-to-nearest into bf16 moves a value by at most 2^-8 of itself (2^-134 if subnormal)
+    tol = 2.0 ** -8 * (np.abs(exact) + e) + e + 2.0 ** -134
+    assert np.all(np.abs(C - exact) <= tol), np.max(np.abs(C - exact) / tol)
+    rs = g.rowsum.cpu().numpy()
+    _, mag = oracle.abft_reference(Ab, Wb)
+    bound = oracle.abft_bound(mag, N, K)
+    assert np.all(np.abs(rs - oracle.abft_row_checksum(exact)) <= bound)
+    v = oracle.abft_verify(rs, Ab, Wb, tol_scale=1.0)
+    np.testing.assert_allclose(g.bound.cpu().numpy(), v["bound"], rtol=1e-12, atol=0)
+    # the two sides sum the reference in different orders: float64 rounding of the magnitude
+    res = g.residual.cpu().numpy()
+    assert np.all(np.abs(res - v["residual"]) <= (N + K + 64) * 2.0 ** -52 * mag)
+    assert np.all(g.flag.cpu().numpy() == 0) and v["n_flagged"] == 0
+    assert int(g.summary[0]) == 0
+    assert int(g.aborted[0]) == 0
+    return float(np.max(np.abs(res) / v["bound"]))
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_gemm_checksum_parity(sdc, M, N, K):
+    ops = W.gemm_operands(M, N, K, DEV, seed=M + N + K)
+    g = sdc.AbftGemm(M, N, K, DEV)
+    g(ops["A"], ops["W"])
+    torch.cuda.synchronize()
+    ratio = _check_clean(g, _bits(ops["A"]), _bits(ops["W"]), M, N, K)
+    assert ratio < 0.5  # the float32 rounding noise is far inside the bound
+
+
+def test_matches_torch_matmul(sdc):
+    # the same product from cuBLAS: both round a float32 accumulation to bf16, in
+    # different orders, so they agree within two bf16 units of the accumulator bound
+    M, N, K = 512, 1024, 2048
+    ops = W.gemm_operands(M, N, K, DEV, seed=21)
+    g = sdc.AbftGemm(M, N, K, DEV)
+    C = g(ops["A"], ops["W"]).float().cpu().numpy().astype(np.float64)
+    ref = (ops["A"] @ ops["W"].t()).float().cpu().numpy().astype(np.float64)
+    e = _elem_error_bound(_bits(ops["A"]), _bits(ops["W"]), K)
+    assert np.all(np.abs(C - ref) <= 2.0 ** -7 * (np.abs(ref) + 2 * e) + 2 * e + 2.0 ** -133)
+
+
+def test_deterministic_and_reusable(sdc):
+    M, N, K = 256, 512, 1024
+    ops = W.gemm_operands(M, N, K, DEV, seed=22)
+    g = sdc.AbftGemm(M, N, K, DEV)
+    g(ops["A"], ops["W"])
+    C0, rs0 = g.C.clone(), g.rowsum.clone()
+    for _ in range(3):
+        g(ops["A"], ops["W"])
+        assert torch.equal(g.C, C0)
+        assert torch.equal(g.rowsum.view(torch.int64), rs0.view(torch.int64))
+    # a second shape on the same stream
+    ops2 = W.gemm_operands(128, 256, 128, DEV, seed=23)
+    g2 = sdc.AbftGemm(128, 256, 128, DEV)
+    g2(ops2["A"], ops2["W"])
+    torch.cuda.synchronize()
+    _check_clean(g2, _bits(ops2["A"]), _bits(ops2["W"]), 128, 256, 128)
+
+
+@pytest.mark.parametrize("mask", [0x4000, 0x2000, 0x0080])
+def test_operand_fault_flags_its_rows(sdc, mask):
+    # the GEMM reads a corrupted A (one element of each planted row XORed with `mask`),
+    # the check uses the clean A: rows whose exact residual is clearly above the bound
+    # flag, rows with no fault do not
+    M, N, K = 512, 1024, 1024
+    ops = W.gemm_operands(M, N, K, DEV, seed=24)
+    A, Wt = ops["A"], ops["W"]
+    rows = [0, 3, 100, 257, 384, 511]
+    Af, where = W.gemm_fault(A, rows, seed=mask, mask=mask)
+    g = sdc.AbftGemm(M, N, K, DEV)
+    g.gemm(Af, Wt)
+    g.verify(A, Wt, tol_scale=1.0)
+    torch.cuda.synchronize()
+    Ab, Afb, Wb = _bits(A), _bits(Af), _bits(Wt)
+    with np.errstate(invalid="ignore", over="ignore"):
+        exact_rs = oracle.abft_row_checksum(oracle.abft_product(Afb, Wb))
+    v = oracle.abft_verify(exact_rs, Ab, Wb, tol_scale=1.0)
+    flag = g.flag.cpu().numpy()
+    clear = (np.abs(v["residual"]) > 2.0 * v["bound"]) | np.isnan(v["residual"])
+    clean = v["residual"] == 0
+    assert np.all(flag[clear] == 1)
+    assert np.all(flag[clean] == 0)
+    assert set(np.nonzero(~clean)[0]) <= set(rows)
+    assert int(g.summary[0]) == int(flag.sum())
+    if mask == 0x4000:  # the top exponent bit: NaN, infinities or values near 2^128
+        assert int(clear.sum()) >= 4
+
+
+def test_rejects_misaligned_and_short_workspace(sdc):
+    M, N, K = 128, 256, 64
+    ops = W.gemm_operands(M, N, K + 8, DEV, seed=25)
+    g = sdc.AbftGemm(M, N, K, DEV)
+    A_odd = ops["A"].view(-1)[1:1 + M * K]  # 2-byte offset
+    with pytest.raises(sdc.SdcError) as ei:
+        sdc.sdc_abft_gemm(A_odd.data_ptr(), ops["W"].data_ptr(), g.C.data_ptr(), M, N, K, g.rowsum.data_ptr(),
+                          g.aborted.data_ptr(), g.ws.data_ptr(), g.ws_bytes, 0)
+    assert ei.value.status == 8
+    with pytest.raises(sdc.SdcError) as ei:
+        sdc.sdc_abft_gemm(ops["A"].data_ptr(), ops["W"].data_ptr(), g.C.data_ptr(), M, N, K, g.rowsum.data_ptr(),
+                          g.aborted.data_ptr(), g.ws.data_ptr(), g.ws_bytes - 256, 0)
+    assert ei.value.status == 5
