@@ -279,11 +279,11 @@ sdc_status sdc_abft_gemm(const void *d_A, const void *d_W, void *d_C, uint32_t M
 
 /* The checksum verifier: per row, the reference A(W^T 1) in float64, the
  * residual d_residual[i] = d_rowsum[i] - reference, the rounding bound
- * d_bound[i] = (g (1 + g) + (N + K + 64) 2^-52) mag + 2 K N 2^-126 with
+ * d_bound[i] = (g (1 + g) + (N + K + 64) 2^-44) mag + 2 K N 2^-126 with
  * g = K 2^-22 and mag = sum_k |A[i][k]| sum_j |W[j][k]| (each float32
- * accumulation step may lose two units in the last place of its partial sum,
- * the float64 sums of the check and flushed subnormals are covered, so a
- * correct product stays inside it), and d_flag[i] = 1 unless
+ * accumulation step may lose two units in the last place of its partial sum;
+ * the check's own sums, carried as float32 pairs, and flushed subnormals are
+ * covered; so a correct product stays inside it), and d_flag[i] = 1 unless
  * |residual| <= tol_scale * bound (a NaN residual flags; tol_scale > 0; the
  * page's adaptive threshold has no published constants).  d_summary counts
  * the flagged rows.  Same shapes and workspace as sdc_abft_gemm; K <= 2^20.

@@ -472,11 +472,11 @@ def abft_bound(mag: np.ndarray, N: int, K: int) -> np.ndarray:
 
     Each of the K float32 accumulation steps of one output may lose up to two
     units in the last place of its partial sum (g = K 2^-22 per output to first
-    order, g^2 beyond it); the float64 sums of the check lose (N + K + 64) 2^-52
-    of the magnitude; subnormals flushed to zero lose 2^-126 per product and per
-    step."""
+    order, g^2 beyond it); the sums of the check, carried as float32 pairs of
+    about 48 bits, lose at most (N + K + 64) 2^-44 of the magnitude; subnormals
+    flushed to zero lose 2^-126 per product and per step."""
     g = K * 2.0 ** -22
-    return (g * (1.0 + g) + (N + K + 64) * 2.0 ** -52) * np.asarray(mag, dtype=np.float64) + 2.0 * K * N * 2.0 ** -126
+    return (g * (1.0 + g) + (N + K + 64) * 2.0 ** -44) * np.asarray(mag, dtype=np.float64) + 2.0 * K * N * 2.0 ** -126
 
 
 def abft_verify(rowsum: np.ndarray, A_bits: np.ndarray, W_bits: np.ndarray, tol_scale: float = 1.0) -> dict:

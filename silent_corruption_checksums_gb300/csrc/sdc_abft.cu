@@ -1,5 +1,6 @@
 // sdc_abft.cu -- a bf16 GEMM on the 5th-generation tensor cores whose
-// epilogue checksums every output row from the float32 accumulator.
+// epilogue checksums every output row from the float32 accumulator, and the
+// check of those checksums.
 //
 // "Safeguarding LLM Training at Scale: Online SDC Detection and Insights from
 // 35 Million GPU Hours" (review page), method section 2: the classic matrix
@@ -9,33 +10,41 @@
 //
 // Here C[M, N] = A[M, K] . W[N, K]^T (the forward product of a linear layer,
 // both operands K-contiguous), bf16 in, fp32 accumulate, bf16 out.  Row i's
-// checksum sum_j acc[i, j] is summed in float64 from the TMEM accumulator by
-// the epilogue (one partial per 256-column tile, reduced in a fixed order);
-// the reference A (W^T 1) comes from a column-sum and a float64 row dot
-// product.  A row whose residual exceeds tol_scale times a bound on the
-// rounding error is flagged.  With mag = sum_k |A[i, k]| * sum_j |W[j, k]| and
-// g = K * 2^-22 the bound is
-//   g (1 + g) mag  +  (N + K + 64) 2^-52 mag  +  2 K N 2^-126:
+// checksum sum_j acc[i, j] is summed by the epilogue from the TMEM accumulator
+// (one partial per 256-column tile, reduced in a fixed order); the reference
+// A (W^T 1) comes from a column-sum and a row dot product.  A row whose
+// residual exceeds tol_scale times a bound on the rounding error is flagged.
+// With mag = sum_k |A[i, k]| * sum_j |W[j, k]| and g = K * 2^-22 the bound is
+//   g (1 + g) mag  +  (N + K + 64) 2^-44 mag  +  2 K N 2^-126:
 // the first term lets each of the K float32 accumulation steps of an output
 // lose up to two units in the last place of its partial sum's magnitude (so it
 // holds for round-to-nearest and for truncating adders alike), the second
-// covers the float64 sums of the check, the third subnormals flushed to zero.
-// A clean product is thus not flagged with tol_scale >= 1; AEGIS adapts its
-// threshold online and the page gives no constants, so the residual is
-// returned too.
+// covers the sums of the check (float32 pairs, ~2^-48 per step), the third
+// subnormals flushed to zero.  A clean product is thus not flagged with
+// tol_scale >= 1; AEGIS adapts its threshold online and the page gives no
+// constants, so the residual is returned too.
 //
-// Kernel layout (one 128 x 256 output tile per CTA, 6 warps):
-//   warp 0 lane 0: TMA producer -- per 64-wide K block, 8 + 8 tiled bulk
-//     tensor copies (boxes of 8 K-elements x 128 or 256 rows) lay A and W out
-//     in the tensor core's core-matrix order (no swizzle) in one of kStages
-//     shared-memory stages, completing on the stage's `full` mbarrier;
+// The check's sums run on float32 pairs (an error-free TwoSum, products split
+// with a fused multiply-add) rather than float64: this GPU's float64 rate is a
+// small fraction of its float32 rate, and a pair carries ~48 bits, far more
+// than the check needs.
+//
+// GEMM kernel (persistent, one CTA per SM, 6 warps, 128 x 256 output tiles):
+//   warp 0 lane 0: TMA producer -- per 64-wide K block one tiled bulk tensor
+//     copy of A (64 x 128) and one of W (64 x 256) into a kStages-deep ring of
+//     shared-memory stages, 128-byte swizzled (the tensor core's canonical
+//     K-major layout), completing on the stage's `full` mbarrier;
 //   warp 1 lane 0: MMA issuer -- 4 tcgen05.mma (M=128, N=256, K=16) per stage
-//     into a 256-column TMEM accumulator, tcgen05.commit releases the stage
-//     (`empty`) and, after the last block, signals the epilogue (`acc`);
+//     into one of two 256-column TMEM accumulators; tcgen05.commit frees the
+//     stage (`empty`) and, after a tile's last block, hands the accumulator to
+//     the epilogue (`tfull`);
 //   warps 2..5: epilogue -- each thread owns one row (TMEM lane), reads its
-//     256 fp32 accumulators with tcgen05.ld, sums them in float64, rounds to
-//     bf16 and stores.
-// Every wait is bounded; a wait that gives up sets the call's abort flag.
+//     256 fp32 accumulators with tcgen05.ld, sums them (float32 pair), rounds
+//     to bf16 and stores, then frees the accumulator (`tempty`), so the
+//     epilogue of one tile overlaps the main loop of the next.
+// Every wait is bounded; a wait that gives up sets the call's abort flag, and
+// the block still waits (bounded) for its copies and MMAs in flight and frees
+// its TMEM before it exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -45,21 +54,31 @@
 
 namespace sdc {
 
+int sm_count(int device);
+
 namespace {
 
 constexpr uint32_t kBM = 128, kBN = 256, kBK = 64;
 constexpr int kStages = 4;
 constexpr uint32_t kStageA = kBM * kBK * 2;  // 16 KiB
 constexpr uint32_t kStageW = kBN * kBK * 2;  // 32 KiB
+constexpr uint32_t kAccCols = 256;           // one accumulator; two are allocated
 constexpr uint32_t kGemmThreads = 192;
-constexpr uint32_t kGemmSmem = kStages * (kStageA + kStageW) + 2048;  // + alignment slack, barriers, TMEM slot
+constexpr uint32_t kNumBars = 2 * kStages + 5;  // full[S], empty[S], tfull[2], tempty[2], done
+constexpr uint32_t kGemmSmem = kStages * (kStageA + kStageW) + 1024 + 8 * kNumBars + 16;
 constexpr uint32_t kMaxK = 1u << 20;
+constexpr uint32_t kMaxSlabs = 64;
+constexpr uint32_t kCheckRows = 4;  // rows per warp in the check
 
-// Shared-memory matrix descriptor, no swizzle: start address, the byte stride
-// between core matrices along K (lbo) and along M/N (sbo), version 1.
-__device__ __forceinline__ uint64_t umma_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte swizzled
+// layout: rows of 128 bytes (64 bf16 of K), 8-row atoms of 1 KiB stacked at a
+// stride of 1 KiB (the stride field), version 1, layout type 2 (128-byte
+// swizzle).  The leading-dimension field is unused by this layout (the MMA's
+// K extent, 32 bytes, lies inside one swizzle row); a K16 step advances the
+// start address by 32 bytes inside the atom.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t addr) {
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
 // Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
@@ -92,6 +111,7 @@ __device__ __forceinline__ void tc_mma(uint32_t tmem, uint64_t da, uint64_t db, 
         : "memory");
 }
 
+// 32 consecutive fp32 columns of this thread's TMEM lane (no wait).
 __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -102,7 +122,41 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr)
         : "memory");
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------- float32 pairs
+// s + c holds a sum to ~48 bits: TwoSum makes each addition's rounding error
+// exact, and the errors gather in c.
+__device__ __forceinline__ void pair_add(float &s, float &c, float x) {
+    const float t = __fadd_rn(s, x);
+    const float bp = __fsub_rn(t, s);
+    const float e = __fadd_rn(__fsub_rn(s, __fsub_rn(t, bp)), __fsub_rn(x, bp));
+    s = t;
+    c = __fadd_rn(c, e);
+}
+// s + c += a * (h + l), the product's rounding error recovered with a fused multiply-add.
+__device__ __forceinline__ void pair_fma(float &s, float &c, float a, float h, float l) {
+    const float p = __fmul_rn(a, h);
+    const float e = __fmaf_rn(a, h, -p);
+    pair_add(s, c, p);
+    c = __fmaf_rn(a, l, __fadd_rn(c, e));
+}
+
+// Converts 32 accumulators to bf16 (round to nearest even), stores them at
+// dst (64 bytes, 16-byte aligned) and adds them to the row's pair sum.
+__device__ __forceinline__ void epilogue_chunk(const uint32_t (&r)[32], __nv_bfloat16 *dst, float &s, float &c) {
+    uint32_t packed[16];
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        const float lo = __uint_as_float(r[j]), hi = __uint_as_float(r[j + 1]);
+        pair_add(s, c, lo);
+        pair_add(s, c, hi);
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed[j / 2]) : "f"(hi), "f"(lo));
+    }
+    uint4 *d = (uint4 *)dst;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) d[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
 }
 
 __global__ void __launch_bounds__(kGemmThreads, 1)
@@ -111,18 +165,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                      int *__restrict__ err) {
     extern __shared__ __align__(1024) unsigned char smem[];
     const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
-    const uint32_t tile_n = blockIdx.x, tile_m = blockIdx.y;
     const uint32_t base = smem_addr(smem), pad = ((base + 1023u) & ~1023u) - base;
-    const uint32_t sA = base + pad;                 // kStages x 16 KiB, 1 KiB aligned
-    const uint32_t sW = sA + kStages * kStageA;     // kStages x 32 KiB
-    const uint32_t bars = sW + kStages * kStageW;   // full[S], empty[S], acc
-    uint32_t *tmem_slot = (uint32_t *)(smem + pad + kStages * (kStageA + kStageW) + 8 * (2 * kStages + 1));
-    const uint32_t full = bars, empty = bars + 8 * kStages, acc = bars + 16 * kStages;
-    const uint32_t nkb = K / kBK;
+    const uint32_t sA = base + pad;                // kStages x 16 KiB, 1 KiB aligned (the swizzle atom)
+    const uint32_t sW = sA + kStages * kStageA;    // kStages x 32 KiB
+    const uint32_t bars = sW + kStages * kStageW;  // full[S], empty[S], tfull[2], tempty[2], done
+    const uint32_t full = bars, empty = bars + 8 * kStages, tfull = bars + 16 * kStages, tempty = tfull + 16,
+                   done = tempty + 16;
+    uint32_t *tmem_slot = (uint32_t *)(smem + pad + kStages * (kStageA + kStageW) + 8 * kNumBars);
+    const uint32_t tiles_m = M / kBM, n_tiles = tiles_m * (N / kBN), nkb = K / kBK;
 
-    if (warp == 1) {  // the MMA warp owns the accumulator's TMEM columns
+    if (warp == 1) {  // the MMA warp owns both accumulators' TMEM columns
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
-                     "r"(kBN)
+                     "r"(2 * kAccCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -131,7 +185,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(full + 8 * s, 1);
             mbar_init(empty + 8 * s, 1);
         }
-        mbar_init(acc, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull + 8 * b, 1);
+            mbar_init(tempty + 8 * b, 4);  // one arrival per epilogue warp
+        }
+        mbar_init(done, 1);
         fence_mbar_init();
     }
     tc_fence_before();
@@ -142,104 +200,97 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {  // ------------------------------------------ TMA producer
-            uint32_t issued = 0;
-            for (uint32_t kb = 0; kb < nkb && ok; ++kb) {
-                const uint32_t s = kb % kStages;
-                if (kb >= (uint32_t)kStages && !mbar_wait(empty + 8 * s, ((kb / kStages) - 1) & 1)) {
-                    ok = false;
-                    break;
-                }
-                issued = kb + 1;
-                mbar_arrive_expect_tx(full + 8 * s, kStageA + kStageW);
-                for (uint32_t j = 0; j < kBK / 8; ++j) {
-                    const int32_t k0 = (int32_t)(kb * kBK + 8 * j);
-                    tma_load_2d(sA + s * kStageA + j * (kBM * 16), &mapA, k0, (int32_t)(tile_m * kBM), full + 8 * s);
-                    tma_load_2d(sW + s * kStageW + j * (kBN * 16), &mapW, k0, (int32_t)(tile_n * kBN), full + 8 * s);
+            uint32_t it = 0;
+            for (uint32_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+                const int32_t row_a = (int32_t)((t % tiles_m) * kBM), row_w = (int32_t)((t / tiles_m) * kBN);
+                for (uint32_t kb = 0; kb < nkb; ++kb, ++it) {
+                    const uint32_t s = it % kStages;
+                    if (it >= (uint32_t)kStages && !mbar_wait(empty + 8 * s, ((it / kStages) - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full + 8 * s, kStageA + kStageW);
+                    tma_load_2d(sA + s * kStageA, &mapA, (int32_t)(kb * kBK), row_a, full + 8 * s);
+                    tma_load_2d(sW + s * kStageW, &mapW, (int32_t)(kb * kBK), row_w, full + 8 * s);
                 }
             }
             // Let no copy land in shared memory after the block has left: wait
             // (bounded) for the last stages issued to complete.
-            const uint32_t first = issued > (uint32_t)kStages ? issued - kStages : 0;
-            for (uint32_t kb = first; kb < issued; ++kb)
-                if (!mbar_wait(full + 8 * (kb % kStages), (kb / kStages) & 1)) ok = false;
+            const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0;
+            for (uint32_t j = first; j < it; ++j)
+                if (!mbar_wait(full + 8 * (j % kStages), (j / kStages) & 1)) ok = false;
             if (!ok) atomicOr(err, 1);
         }
     } else if (warp == 1) {
         if (lane == 0) {  // ------------------------------------------ MMA issuer
             constexpr uint32_t idesc = umma_idesc(kBM, kBN);
-            for (uint32_t kb = 0; kb < nkb && ok; ++kb) {
-                const uint32_t s = kb % kStages;
-                if (!mbar_wait(full + 8 * s, (kb / kStages) & 1)) {
+            uint32_t it = 0, lt = 0;
+            for (uint32_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++lt) {
+                const uint32_t b = lt & 1u;
+                if (lt >= 2 && !mbar_wait(tempty + 8 * b, ((lt >> 1) - 1) & 1)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                for (uint32_t ks = 0; ks < kBK / 16; ++ks) {
-                    // one K16 step = two core-matrix columns: 2 x (rows x 16 B)
-                    const uint64_t da = umma_desc(sA + s * kStageA + ks * 2 * (kBM * 16), kBM * 16, 128);
-                    const uint64_t dw = umma_desc(sW + s * kStageW + ks * 2 * (kBN * 16), kBN * 16, 128);
-                    tc_mma(tmem, da, dw, idesc, (kb | ks) != 0 ? 1u : 0u);
+                const uint32_t d = tmem + b * kAccCols;
+                for (uint32_t kb = 0; kb < nkb; ++kb, ++it) {
+                    const uint32_t s = it % kStages;
+                    if (!mbar_wait(full + 8 * s, (it / kStages) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (uint32_t ks = 0; ks < kBK / 16; ++ks)
+                        tc_mma(d, umma_desc_sw128(sA + s * kStageA + ks * 32), umma_desc_sw128(sW + s * kStageW + ks * 32),
+                               idesc, (kb | ks) != 0 ? 1u : 0u);
+                    tc_commit(empty + 8 * s);  // the stage is free once these MMAs have read it
                 }
-                tc_commit(empty + 8 * s);  // the stage is free once these MMAs have read it
+                if (ok) tc_commit(tfull + 8 * b);
             }
-            // Always signal: the barrier then tracks every MMA this thread
-            // issued, and the TMEM owner waits on it before freeing.
-            tc_commit(acc);
+            // Tracks every MMA this thread issued; the TMEM owner waits on it before freeing.
+            tc_commit(done);
             if (!ok) atomicOr(err, 1);
         }
     } else {  // ------------------------------------------------------- epilogue
-        const uint32_t quarter = warp & 3u;  // TMEM lanes this warp may read
-        const uint32_t row = tile_m * kBM + quarter * 32 + lane;
-        const bool got = mbar_wait(acc, 0);
-        if (__any_sync(0xffffffffu, !got)) {
-            if (lane == 0) atomicOr(err, 1);
-        } else {
-            tc_fence_after();
-            double rs = 0.0;
-            __nv_bfloat16 *crow = C + (uint64_t)row * N + tile_n * kBN;
-            for (uint32_t c = 0; c < kBN; c += 32) {
-                uint32_t r[32];
-                tc_ld32(tmem + ((quarter * 32) << 16) + c, r);
-                uint32_t packed[16];
-#pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                    const float lo = __uint_as_float(r[j]), hi = __uint_as_float(r[j + 1]);
-                    rs = __dadd_rn(rs, (double)lo);
-                    rs = __dadd_rn(rs, (double)hi);
-                    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed[j / 2]) : "f"(hi), "f"(lo));
-                }
-                uint4 *dst = (uint4 *)(crow + c);
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+        const uint32_t quarter = warp & 3u;  // the TMEM lanes this warp may read
+        const uint32_t lane_base = (quarter * 32) << 16;
+        uint32_t lt = 0;
+        for (uint32_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++lt) {
+            const uint32_t b = lt & 1u;
+            const bool got = mbar_wait(tfull + 8 * b, (lt >> 1) & 1);
+            if (__any_sync(0xffffffffu, !got)) {
+                if (lane == 0) atomicOr(err, 1);
+                break;
             }
-            rowsum_part[(uint64_t)tile_n * M + row] = rs;
+            tc_fence_after();
+            const uint32_t tile_n = t / tiles_m;
+            const uint32_t row = (t % tiles_m) * kBM + quarter * 32 + lane;
+            __nv_bfloat16 *crow = C + (uint64_t)row * N + (uint64_t)tile_n * kBN;
+            const uint32_t acc = tmem + lane_base + b * kAccCols;
+            float s = 0.0f, c = 0.0f;
+            for (uint32_t c0 = 0; c0 < kBN; c0 += 64) {
+                uint32_t r0[32], r1[32];
+                tc_ld32(acc + c0, r0);
+                tc_ld32(acc + c0 + 32, r1);
+                tc_wait_ld();
+                epilogue_chunk(r0, crow + c0, s, c);
+                epilogue_chunk(r1, crow + c0 + 32, s, c);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tempty + 8 * b) : "memory");
+            rowsum_part[(uint64_t)tile_n * M + row] = (double)s + (double)c;
         }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
-        if (lane == 0 && !mbar_wait(acc, 0)) atomicOr(err, 1);
+        if (lane == 0 && !mbar_wait(done, 0)) atomicOr(err, 1);
         __syncwarp();
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kBN) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * kAccCols) : "memory");
     }
-}
-
-// w1[k] = sum_j W[j, k] and wabs[k] = sum_j |W[j, k]| in float64, one thread per k
-// column, rows in order.
-__global__ void abft_colsum_kernel(const __nv_bfloat16 *__restrict__ W, uint32_t N, uint32_t K, double *__restrict__ w1,
-                                   double *__restrict__ wabs) {
-    const uint32_t k = blockIdx.x * blockDim.x + threadIdx.x;
-    if (k >= K) return;
-    double s = 0.0, a = 0.0;
-    for (uint32_t j = 0; j < N; ++j) {
-        const double x = (double)__bfloat162float(W[(uint64_t)j * K + k]);
-        s = __dadd_rn(s, x);
-        a = __dadd_rn(a, fabs(x));
-    }
-    w1[k] = s;
-    wabs[k] = a;
 }
 
 // Row checksums: the tile partials of each row summed in tile order.
@@ -252,40 +303,127 @@ __global__ void abft_rowsum_kernel(const double *__restrict__ rowsum_part, uint3
     rowsum[i] = cs;
 }
 
-// Per row: the reference A (W^T 1), the rounding bound, the residual against
-// the accumulator checksum, and the flag.  One warp per row.
-__global__ void abft_check_kernel(const __nv_bfloat16 *__restrict__ A, uint32_t M, uint32_t N, uint32_t K,
-                                  const double *__restrict__ rowsum, const double *__restrict__ w1,
-                                  const double *__restrict__ wabs, float tol_scale, double *__restrict__ residual,
-                                  double *__restrict__ bound, uint8_t *__restrict__ flag,
-                                  sdc_abft_summary *__restrict__ summary) {
-    const uint32_t lane = threadIdx.x & 31u;
-    const uint64_t warp = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (warp >= M) return;
-    const uint32_t i = (uint32_t)warp;
-    double ref = 0.0, mag = 0.0;
-    for (uint32_t k = lane; k < K; k += 32) {
-        const double a = (double)__bfloat162float(A[(uint64_t)i * K + k]);
-        ref = fma(a, w1[k], ref);
-        mag = fma(fabs(a), wabs[k], mag);
+__global__ void abft_finish_kernel(const int *__restrict__ err, uint32_t *__restrict__ aborted) {
+    *aborted = *err != 0 ? 1u : 0u;
+}
+
+// ---------------------------------------------------------------- the check
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Column sums of W over one slab of its rows: block (x, y) covers columns
+// 256x .. 256x + 255 (8 per lane, one 16-byte load per row) and slab y; the 8
+// warps take the slab's rows in turn.  Writes slabs[y][k] = {sum_j W[j, k],
+// sum_j |W[j, k]|} in float64, warps combined in order.
+__global__ void __launch_bounds__(256) abft_colsum_slab_kernel(const __nv_bfloat16 *__restrict__ W, uint32_t N,
+                                                               uint32_t K, uint32_t n_slabs,
+                                                               double2 *__restrict__ slabs) {
+    __shared__ double2 part[8][256];
+    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+    const uint32_t k = blockIdx.x * 256 + lane * 8;
+    const uint32_t j0 = (uint32_t)((uint64_t)blockIdx.y * N / n_slabs),
+                   j1 = (uint32_t)((uint64_t)(blockIdx.y + 1) * N / n_slabs);
+    float s[8], c[8], sa[8], ca[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) s[q] = c[q] = sa[q] = ca[q] = 0.0f;
+    if (k < K) {
+        for (uint32_t j = j0 + warp; j < j1; j += 8) {
+            const uint4 v = ld_stream(W + (uint64_t)j * K + k);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float x0 = bf16_lo(w[q]), x1 = bf16_hi(w[q]);
+                pair_add(s[2 * q], c[2 * q], x0);
+                pair_add(s[2 * q + 1], c[2 * q + 1], x1);
+                pair_add(sa[2 * q], ca[2 * q], fabsf(x0));
+                pair_add(sa[2 * q + 1], ca[2 * q + 1], fabsf(x1));
+            }
+        }
     }
-    ref = warp_sum_f64(ref);
-    mag = warp_sum_f64(mag);
-    if (lane == 0) {
-        const double cs = rowsum[i];
-        const double g = (double)K * 0x1p-22;
-        const double b = (g * (1.0 + g) + (double)(N + K + 64) * 0x1p-52) * mag + 2.0 * (double)K * (double)N * 0x1p-126;
-        const double d = cs - ref;
-        residual[i] = d;
-        bound[i] = b;
-        const uint8_t f = fabs(d) <= (double)tol_scale * b ? 0 : 1;  // NaN flags
-        flag[i] = f;
-        if (f) atomicAdd(&summary->n_flagged, 1u);
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        part[warp][lane * 8 + q] = make_double2((double)s[q] + (double)c[q], (double)sa[q] + (double)ca[q]);
+    __syncthreads();
+    const uint32_t kk = blockIdx.x * 256 + threadIdx.x;
+    if (kk < K) {
+        double2 acc = part[0][threadIdx.x];
+        for (int w = 1; w < 8; ++w) {
+            acc.x = __dadd_rn(acc.x, part[w][threadIdx.x].x);
+            acc.y = __dadd_rn(acc.y, part[w][threadIdx.x].y);
+        }
+        slabs[(uint64_t)blockIdx.y * K + kk] = acc;
     }
 }
 
-__global__ void abft_finish_kernel(const int *__restrict__ err, uint32_t *__restrict__ aborted) {
-    *aborted = *err != 0 ? 1u : 0u;
+// The slabs summed in order: wcol[k] = {W^T 1, |W|^T 1} in float64 and, for the
+// check, each split into a float32 pair wsplit[k] = {hi, lo, hi_abs, lo_abs}.
+__global__ void abft_colsum_final_kernel(const double2 *__restrict__ slabs, uint32_t K, uint32_t n_slabs,
+                                         double2 *__restrict__ wcol, float4 *__restrict__ wsplit) {
+    const uint32_t k = blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= K) return;
+    double a = 0.0, b = 0.0;
+    for (uint32_t y = 0; y < n_slabs; ++y) {
+        const double2 p = slabs[(uint64_t)y * K + k];
+        a = __dadd_rn(a, p.x);
+        b = __dadd_rn(b, p.y);
+    }
+    wcol[k] = make_double2(a, b);
+    const float ah = (float)a, bh = (float)b;
+    wsplit[k] = make_float4(ah, (float)(a - (double)ah), bh, (float)(b - (double)bh));
+}
+
+// Per row: the reference A (W^T 1) and the magnitude |A| (|W|^T 1) as float32
+// pairs, the bound, the residual against the accumulator checksum, and the
+// flag.  One warp per kCheckRows rows (each column pair loaded once for them),
+// lanes over 8-column vectors.
+__global__ void __launch_bounds__(256) abft_check_kernel(const __nv_bfloat16 *__restrict__ A, uint32_t M, uint32_t N,
+                                                         uint32_t K, const double *__restrict__ rowsum,
+                                                         const float4 *__restrict__ wsplit, float tol_scale,
+                                                         double *__restrict__ residual, double *__restrict__ bound,
+                                                         uint8_t *__restrict__ flag,
+                                                         sdc_abft_summary *__restrict__ summary) {
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint64_t warp = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint64_t row0 = warp * kCheckRows;
+    if (row0 >= M) return;  // M is a multiple of 128, so all kCheckRows rows exist
+    float rs[kCheckRows], rc[kCheckRows], ms[kCheckRows], mc[kCheckRows];
+#pragma unroll
+    for (uint32_t r = 0; r < kCheckRows; ++r) rs[r] = rc[r] = ms[r] = mc[r] = 0.0f;
+    for (uint32_t v = lane; v < K / 8; v += 32) {
+        float4 w[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) w[q] = wsplit[v * 8 + q];
+#pragma unroll
+        for (uint32_t r = 0; r < kCheckRows; ++r) {
+            const uint4 av = ld_stream(A + (row0 + r) * K + (uint64_t)v * 8);
+            const uint32_t a4[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float a0 = bf16_lo(a4[q]), a1 = bf16_hi(a4[q]);
+                pair_fma(rs[r], rc[r], a0, w[2 * q].x, w[2 * q].y);
+                pair_fma(rs[r], rc[r], a1, w[2 * q + 1].x, w[2 * q + 1].y);
+                pair_fma(ms[r], mc[r], fabsf(a0), w[2 * q].z, w[2 * q].w);
+                pair_fma(ms[r], mc[r], fabsf(a1), w[2 * q + 1].z, w[2 * q + 1].w);
+            }
+        }
+    }
+#pragma unroll
+    for (uint32_t r = 0; r < kCheckRows; ++r) {
+        const double ref = warp_sum_f64((double)rs[r] + (double)rc[r]);
+        const double mag = warp_sum_f64((double)ms[r] + (double)mc[r]);
+        if (lane == 0) {
+            const uint64_t i = row0 + r;
+            const double g = (double)K * 0x1p-22;
+            const double b =
+                (g * (1.0 + g) + (double)(N + K + 64) * 0x1p-44) * mag + 2.0 * (double)K * (double)N * 0x1p-126;
+            const double d = rowsum[i] - ref;
+            residual[i] = d;
+            bound[i] = b;
+            const uint8_t f = fabs(d) <= (double)tol_scale * b ? 0 : 1;  // NaN flags
+            flag[i] = f;
+            if (f) atomicAdd(&summary->n_flagged, 1u);
+        }
+    }
 }
 
 typedef CUresult (*PFN_encodeTiled)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -306,22 +444,40 @@ PFN_encodeTiled encode_fn() {
     return fn;
 }
 
-// 2-D map over a [rows, K] bf16 matrix: boxes of 8 K-elements (16 bytes) x box_rows.
+// 2-D map over a [rows, K] bf16 matrix: boxes of 64 K-elements (128 bytes) x
+// box_rows, 128-byte swizzled in shared memory.
 sdc_status make_map(CUtensorMap *map, const void *ptr, uint32_t rows, uint32_t K, uint32_t box_rows) {
     PFN_encodeTiled fn = encode_fn();
     if (!fn) return fail(SDC_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
     const cuuint64_t dims[2] = {K, rows};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {8, box_rows};
+    const cuuint32_t box[2] = {kBK, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(SDC_ERR_CUDA, "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
     return SDC_OK;
 }
 
 size_t round_up256(size_t x) { return (x + 255) / 256 * 256; }
+
+uint32_t n_slabs_for(uint32_t N) { return N / 128 < kMaxSlabs ? N / 128 : kMaxSlabs; }
+
+// Workspace: tile partials [N/256][M] | wcol [K] | wsplit [K] | slabs [n_slabs][K] | abort word.
+struct AbftWs {
+    size_t part, wcol, wsplit, slabs, err, total;
+};
+AbftWs abft_ws(uint32_t M, uint32_t N, uint32_t K) {
+    AbftWs w;
+    w.part = 0;
+    w.wcol = round_up256((size_t)(N / kBN) * M * sizeof(double));
+    w.wsplit = w.wcol + round_up256((size_t)K * sizeof(double2));
+    w.slabs = w.wsplit + round_up256((size_t)K * sizeof(float4));
+    w.err = w.slabs + round_up256((size_t)n_slabs_for(N) * K * sizeof(double2));
+    w.total = w.err + 256;
+    return w;
+}
 
 }  // namespace
 
@@ -331,10 +487,7 @@ using namespace sdc;
 
 extern "C" {
 
-size_t sdc_abft_workspace_size(uint32_t M, uint32_t N, uint32_t K) {
-    const size_t tiles_n = N / kBN;
-    return round_up256(tiles_n * M * sizeof(double)) + 2 * round_up256((size_t)K * sizeof(double)) + 256;
-}
+size_t sdc_abft_workspace_size(uint32_t M, uint32_t N, uint32_t K) { return abft_ws(M, N, K).total; }
 
 static sdc_status abft_args(const void *d_A, const void *d_W, uint32_t M, uint32_t N, uint32_t K, void *d_ws,
                             size_t ws_bytes, int *dev) {
@@ -366,18 +519,19 @@ sdc_status sdc_abft_gemm(const void *d_A, const void *d_W, void *d_C, uint32_t M
     st = make_map(&mapA, d_A, M, K, kBM);
     if (st == SDC_OK) st = make_map(&mapW, d_W, N, K, kBN);
     if (st != SDC_OK) return st;
-    const uint32_t tiles_n = N / kBN;
-    double *part = (double *)d_ws;
-    int *err = (int *)((char *)d_ws + round_up256((size_t)tiles_n * M * sizeof(double)) +
-                       2 * round_up256((size_t)K * sizeof(double)));
+    const AbftWs w = abft_ws(M, N, K);
+    double *part = (double *)((char *)d_ws + w.part);
+    int *err = (int *)((char *)d_ws + w.err);
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int), s);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(abft_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_gemm setup");
-    abft_gemm_kernel<<<dim3(tiles_n, M / kBM), kGemmThreads, kGemmSmem, s>>>(mapA, mapW, (__nv_bfloat16 *)d_C, M, N, K,
-                                                                           part, err);
-    abft_rowsum_kernel<<<(M + 255) / 256, 256, 0, s>>>(part, M, tiles_n, d_rowsum);
+    const uint32_t n_tiles = (M / kBM) * (N / kBN);
+    const uint32_t sms = (uint32_t)sm_count(dev);
+    const uint32_t grid = n_tiles < sms ? n_tiles : sms;
+    abft_gemm_kernel<<<grid, kGemmThreads, kGemmSmem, s>>>(mapA, mapW, (__nv_bfloat16 *)d_C, M, N, K, part, err);
+    abft_rowsum_kernel<<<(M + 255) / 256, 256, 0, s>>>(part, M, N / kBN, d_rowsum);
     abft_finish_kernel<<<1, 1, 0, s>>>(err, d_aborted);
     e = cudaGetLastError();
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_abft_gemm launch");
@@ -391,15 +545,20 @@ sdc_status sdc_abft_verify(const void *d_A, const void *d_W, uint32_t M, uint32_
     if (st != SDC_OK) return st;
     if (!d_rowsum || !d_residual || !d_bound || !d_flag || !d_summary) return fail(SDC_ERR_NULL, "NULL output");
     if (!(tol_scale > 0.0f)) return fail(SDC_ERR_BAD_ARG, "tol_scale must be positive");
-    const uint32_t tiles_n = N / kBN;
-    double *w1 = (double *)((char *)d_ws + round_up256((size_t)tiles_n * M * sizeof(double)));
-    double *wabs = (double *)((char *)w1 + round_up256((size_t)K * sizeof(double)));
+    const AbftWs w = abft_ws(M, N, K);
+    double2 *wcol = (double2 *)((char *)d_ws + w.wcol);
+    float4 *wsplit = (float4 *)((char *)d_ws + w.wsplit);
+    double2 *slabs = (double2 *)((char *)d_ws + w.slabs);
+    const uint32_t n_slabs = n_slabs_for(N);
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = cudaMemsetAsync(d_summary, 0, sizeof(sdc_abft_summary), s);
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_verify setup");
-    abft_colsum_kernel<<<(K + 255) / 256, 256, 0, s>>>((const __nv_bfloat16 *)d_W, N, K, w1, wabs);
-    abft_check_kernel<<<(unsigned)(((uint64_t)M * 32 + 255) / 256), 256, 0, s>>>(
-        (const __nv_bfloat16 *)d_A, M, N, K, d_rowsum, w1, wabs, tol_scale, d_residual, d_bound, d_flag, d_summary);
+    abft_colsum_slab_kernel<<<dim3((K + 255) / 256, n_slabs), 256, 0, s>>>((const __nv_bfloat16 *)d_W, N, K, n_slabs,
+                                                                           slabs);
+    abft_colsum_final_kernel<<<(K + 255) / 256, 256, 0, s>>>(slabs, K, n_slabs, wcol, wsplit);
+    const uint64_t warps = M / kCheckRows;
+    abft_check_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(
+        (const __nv_bfloat16 *)d_A, M, N, K, d_rowsum, wsplit, tol_scale, d_residual, d_bound, d_flag, d_summary);
     e = cudaGetLastError();
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_abft_verify launch");
 }

@@ -108,9 +108,11 @@ def test_host_validation_without_gpu(sdc):
         with pytest.raises(sdc.SdcError) as ei:
             sdc.sdc_abft_verify(4096, 8192, M, N, K, 0, 1.0, 0, 0, 0, 0, 0, 0, 0)
         assert ei.value.status == 9, (M, N, K)
-    # tile partials (N/256 per row) + two K-long float64 column sums + the abort word, each rounded to 256
-    assert sdc.sdc_abft_workspace_size(128, 512, 64) == 2048 + 2 * 512 + 256
-    assert sdc.sdc_abft_workspace_size(1000, 256, 100) == 8192 + 2 * 1024 + 256
+    # tile partials (N/256 per row), K column-sum pairs (float64), K split pairs (float32),
+    # min(64, N/128) slabs of K float64 pairs, the abort word; each rounded up to 256 bytes
+    assert sdc.sdc_abft_workspace_size(128, 512, 64) == 2048 + 1024 + 1024 + 4 * 64 * 16 + 256
+    assert sdc.sdc_abft_workspace_size(1000, 256, 100) == 8192 + 1792 + 1792 + 3328 + 256
+    assert sdc.sdc_abft_workspace_size(128, 16384, 64) == 64 * 128 * 8 + 1024 + 1024 + 64 * 64 * 16 + 256
 
 
 def test_pages_verdict_decoding(sdc):
