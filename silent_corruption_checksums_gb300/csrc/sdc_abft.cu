@@ -159,10 +159,24 @@ __device__ __forceinline__ void epilogue_chunk(const uint32_t (&r)[32], __nv_bfl
     for (int q = 0; q < 4; ++q) d[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
 }
 
+// Tile t of the schedule -> (tile row, tile column).  Tiles go in bands of
+// band_m tile rows; inside a band the row index runs fastest, so the CTAs in
+// flight share a few W tiles while the band's rows of A (sized on the host to
+// stay resident in L2) are reused by every column of the band.
+__device__ __forceinline__ void tile_coords(uint32_t t, uint32_t tiles_m, uint32_t tiles_n, uint32_t band_m,
+                                            uint32_t &tm, uint32_t &tn) {
+    const uint32_t band_tiles = band_m * tiles_n;
+    const uint32_t band = t / band_tiles, r = t - band * band_tiles;
+    const uint32_t m0 = band * band_m;
+    const uint32_t bm = tiles_m - m0 < band_m ? tiles_m - m0 : band_m;
+    tm = m0 + r % bm;
+    tn = r / bm;
+}
+
 __global__ void __launch_bounds__(kGemmThreads, 1)
     abft_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapW,
-                     __nv_bfloat16 *__restrict__ C, uint32_t M, uint32_t N, uint32_t K, double *__restrict__ rowsum_part,
-                     int *__restrict__ err) {
+                     __nv_bfloat16 *__restrict__ C, uint32_t M, uint32_t N, uint32_t K, uint32_t band_m,
+                     double *__restrict__ rowsum_part, int *__restrict__ err) {
     extern __shared__ __align__(1024) unsigned char smem[];
     const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
     const uint32_t base = smem_addr(smem), pad = ((base + 1023u) & ~1023u) - base;
@@ -172,7 +186,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t full = bars, empty = bars + 8 * kStages, tfull = bars + 16 * kStages, tempty = tfull + 16,
                    done = tempty + 16;
     uint32_t *tmem_slot = (uint32_t *)(smem + pad + kStages * (kStageA + kStageW) + 8 * kNumBars);
-    const uint32_t tiles_m = M / kBM, n_tiles = tiles_m * (N / kBN), nkb = K / kBK;
+    const uint32_t tiles_m = M / kBM, tiles_n = N / kBN, n_tiles = tiles_m * tiles_n, nkb = K / kBK;
 
     if (warp == 1) {  // the MMA warp owns both accumulators' TMEM columns
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
@@ -202,7 +216,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (lane == 0) {  // ------------------------------------------ TMA producer
             uint32_t it = 0;
             for (uint32_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-                const int32_t row_a = (int32_t)((t % tiles_m) * kBM), row_w = (int32_t)((t / tiles_m) * kBN);
+                uint32_t tm, tn;
+                tile_coords(t, tiles_m, tiles_n, band_m, tm, tn);
+                const int32_t row_a = (int32_t)(tm * kBM), row_w = (int32_t)(tn * kBN);
                 for (uint32_t kb = 0; kb < nkb; ++kb, ++it) {
                     const uint32_t s = it % kStages;
                     if (it >= (uint32_t)kStages && !mbar_wait(empty + 8 * s, ((it / kStages) - 1) & 1)) {
@@ -264,8 +280,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 break;
             }
             tc_fence_after();
-            const uint32_t tile_n = t / tiles_m;
-            const uint32_t row = (t % tiles_m) * kBM + quarter * 32 + lane;
+            uint32_t tm, tile_n;
+            tile_coords(t, tiles_m, tiles_n, band_m, tm, tile_n);
+            const uint32_t row = tm * kBM + quarter * 32 + lane;
             __nv_bfloat16 *crow = C + (uint64_t)row * N + (uint64_t)tile_n * kBN;
             const uint32_t acc = tmem + lane_base + b * kAccCols;
             float s = 0.0f, c = 0.0f;
@@ -530,7 +547,11 @@ sdc_status sdc_abft_gemm(const void *d_A, const void *d_W, void *d_C, uint32_t M
     const uint32_t n_tiles = (M / kBM) * (N / kBN);
     const uint32_t sms = (uint32_t)sm_count(dev);
     const uint32_t grid = n_tiles < sms ? n_tiles : sms;
-    abft_gemm_kernel<<<grid, kGemmThreads, kGemmSmem, s>>>(mapA, mapW, (__nv_bfloat16 *)d_C, M, N, K, part, err);
+    // A band of tile rows holds about 24 MiB of A, a fraction of the 126 MiB L2.
+    uint32_t band_m = (uint32_t)((24u << 20) / ((size_t)kBM * K * 2));
+    band_m = band_m < 1 ? 1 : (band_m > M / kBM ? M / kBM : band_m);
+    abft_gemm_kernel<<<grid, kGemmThreads, kGemmSmem, s>>>(mapA, mapW, (__nv_bfloat16 *)d_C, M, N, K, band_m, part,
+                                                           err);
     abft_rowsum_kernel<<<(M + 255) / 256, 256, 0, s>>>(part, M, N / kBN, d_rowsum);
     abft_finish_kernel<<<1, 1, 0, s>>>(err, d_aborted);
     e = cudaGetLastError();
