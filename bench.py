@@ -143,8 +143,9 @@ def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
-    return {"hbm_gbs": 6800.0, "source": "fallback"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d.get("bf16_tflops", 1900.0)),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
 # ---------------------------------------------------------------- CPU baseline (the oracle)
@@ -337,6 +338,8 @@ def bench_rows(args, dev, stream, peaks, sdc, W, torch, np, only=None) -> dict:
     rows = {}
     if only in ("fingerprint_8b", "fingerprint_stress"):
         return bench_big_rows(args, dev, stream, peaks, sdc, W, torch, only)
+    if only == "abft_gemm":
+        return bench_abft_row(args, dev, stream, peaks, sdc, W, torch)
     # fused gradient average-scan on 4 bf16 buffers of the 1b layout
     g = W.grads_flat(W.layout_numel(W.layout_1b(args.layers)), 4, torch.bfloat16, 1e-3, dev, seed=3)
     bufs = g["bufs"]
@@ -386,6 +389,8 @@ def bench_rows(args, dev, stream, peaks, sdc, W, torch, np, only=None) -> dict:
         del xplan, rec
     del g, bufs, out, ws
     torch.cuda.empty_cache()
+    if only in (None, "abft_gemm"):
+        rows.update(bench_abft_row(args, dev, stream, peaks, sdc, W, torch))
     if not getattr(args, "no_big_rows", False):
         rows.update(bench_big_rows(args, dev, stream, peaks, sdc, W, torch, only))
     return rows
@@ -415,6 +420,37 @@ def bench_adamw_row(args, dev, stream, peaks, sdc, W, torch) -> dict:
                                  "separate_fingerprint_reread_ms": ms_fp}}
     opt.close()
     del plan, weights, grads, m, v
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_abft_row(args, dev, stream, peaks, sdc, W, torch) -> dict:
+    """GEMM with the in-kernel accumulator row checksum (the sensor) and its check (the
+    verifier) on the 8b layout's MLP up-projection, with cuBLAS's plain GEMM beside it."""
+    M, N, K = W.GEMM_8B_UP
+    ops = W.gemm_operands(M, N, K, dev, seed=6)
+    A, Wt = ops["A"], ops["W"]
+    g = sdc.AbftGemm(M, N, K, dev)
+    reps = max(10, args.steps // 10)
+    ms_gemm = _time_loop(lambda: g.gemm(A, Wt, stream=stream), reps, stream, torch)
+    ms_verify = _time_loop(lambda: g.verify(A, Wt, stream=stream), reps, stream, torch)
+    ms_cublas = _time_loop(lambda: torch.matmul(A, Wt.t()), reps, stream, torch)
+    torch.cuda.synchronize()
+    flops = 2.0 * M * N * K
+    tf = flops / (ms_gemm * 1e-3) / 1e12
+    vbytes = (M + N) * K * 2
+    out = {"abft_gemm": {"workload": f"C = A W^T, bf16, M={M} tokens x N={N} x K={K} (8b MLP up-projection), "
+                         "A N(0,1), W N(0,0.02); row checksum from the fp32 accumulator + check vs A(W^T 1)",
+                         "gemm_ms": ms_gemm, "tflops": tf, "frac_bf16_peak": tf / peaks["bf16_tflops"],
+                         "peak_tflops": peaks["bf16_tflops"],
+                         "peak_kind": f"burst bf16 (MEASURED_PEAKS.json bf16_tflops, {peaks['source']})",
+                         "verify_ms": ms_verify, "verify_GB_s": vbytes / ms_verify / 1e6,
+                         "verify_frac_hbm": vbytes / ms_verify / 1e6 / peaks["hbm_gbs"],
+                         "cublas_plain_gemm_ms": ms_cublas,
+                         "cublas_tflops": flops / (ms_cublas * 1e-3) / 1e12,
+                         "clean_rows_flagged": int(g.summary[0]), "aborted": int(g.aborted[0]),
+                         "max_residual_over_bound": float((g.residual.abs() / g.bound).max())}}
+    del g, ops, A, Wt
     torch.cuda.empty_cache()
     return out
 
@@ -525,7 +561,7 @@ def main(argv=None) -> None:
     ap.add_argument("--chunk-bytes", type=int, default=0)
     ap.add_argument("--quick", action="store_true", help="only the timed fingerprint step (no rows/e2e/cpu)")
     ap.add_argument("--no-big-rows", action="store_true", help="skip the 8b and stress rows")
-    ap.add_argument("--only", choices=["grad_average_scan", "grad_scan", "xorsum", "fingerprint_8b",
+    ap.add_argument("--only", choices=["grad_average_scan", "grad_scan", "xorsum", "abft_gemm", "fingerprint_8b",
                                        "fingerprint_stress", "adamw_fingerprint"], default=None,
                     help="time one row alone (profiling)")
     ap.add_argument("--layers", type=int, default=24,
