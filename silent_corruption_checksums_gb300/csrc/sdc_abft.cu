@@ -68,7 +68,8 @@ constexpr uint32_t kNumBars = 2 * kStages + 5;  // full[S], empty[S], tfull[2], 
 constexpr uint32_t kGemmSmem = kStages * (kStageA + kStageW) + 1024 + 8 * kNumBars + 16;
 constexpr uint32_t kMaxK = 1u << 20;
 constexpr uint32_t kMaxSlabs = 64;
-constexpr uint32_t kCheckRows = 4;  // rows per warp in the check
+constexpr uint32_t kCheckRows = 4;     // rows per block of the check
+constexpr uint32_t kCheckThreads = 64;  // threads per block of the check
 
 // Shared-memory matrix descriptor of a K-major operand in the 128-byte swizzled
 // layout: rows of 128 bytes (64 bf16 of K), 8-row atoms of 1 KiB stacked at a
@@ -141,6 +142,12 @@ __device__ __forceinline__ void pair_fma(float &s, float &c, float a, float h, f
     const float e = __fmaf_rn(a, h, -p);
     pair_add(s, c, p);
     c = __fmaf_rn(a, l, __fadd_rn(c, e));
+}
+
+// Merges the pair (s2, c2) into (s, c).
+__device__ __forceinline__ void pair_merge(float &s, float &c, float s2, float c2) {
+    pair_add(s, c, s2);
+    c = __fadd_rn(c, c2);
 }
 
 // Converts 32 accumulators to bf16 (round to nearest even), stores them at
@@ -310,18 +317,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 }
 
-// Row checksums: the tile partials of each row summed in tile order.
+// Row checksums: the tile partials of each row summed in tile order; thread 0
+// also publishes the GEMM's abort flag.
 __global__ void abft_rowsum_kernel(const double *__restrict__ rowsum_part, uint32_t M, uint32_t n_tiles,
-                                   double *__restrict__ rowsum) {
+                                   double *__restrict__ rowsum, const int *__restrict__ err,
+                                   uint32_t *__restrict__ aborted) {
     const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i == 0) *aborted = *err != 0 ? 1u : 0u;
     if (i >= M) return;
     double cs = 0.0;
+#pragma unroll 8
     for (uint32_t t = 0; t < n_tiles; ++t) cs = __dadd_rn(cs, rowsum_part[(uint64_t)t * M + i]);
     rowsum[i] = cs;
-}
-
-__global__ void abft_finish_kernel(const int *__restrict__ err, uint32_t *__restrict__ aborted) {
-    *aborted = *err != 0 ? 1u : 0u;
 }
 
 // ---------------------------------------------------------------- the check
@@ -330,12 +337,12 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 
 // Column sums of W over one slab of its rows: block (x, y) covers columns
 // 256x .. 256x + 255 (8 per lane, one 16-byte load per row) and slab y; the 8
-// warps take the slab's rows in turn.  Writes slabs[y][k] = {sum_j W[j, k],
-// sum_j |W[j, k]|} in float64, warps combined in order.
+// warps take the slab's rows in turn.  Writes slabs[y][k] = the float32 pairs
+// of sum_j W[j, k] and sum_j |W[j, k]|, warps merged in order.
 __global__ void __launch_bounds__(256) abft_colsum_slab_kernel(const __nv_bfloat16 *__restrict__ W, uint32_t N,
                                                                uint32_t K, uint32_t n_slabs,
-                                                               double2 *__restrict__ slabs) {
-    __shared__ double2 part[8][256];
+                                                               float4 *__restrict__ slabs) {
+    __shared__ float4 part[8][256];
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
     const uint32_t k = blockIdx.x * 256 + lane * 8;
     const uint32_t j0 = (uint32_t)((uint64_t)blockIdx.y * N / n_slabs),
@@ -343,77 +350,108 @@ __global__ void __launch_bounds__(256) abft_colsum_slab_kernel(const __nv_bfloat
     float s[8], c[8], sa[8], ca[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) s[q] = c[q] = sa[q] = ca[q] = 0.0f;
-    if (k < K) {
-        for (uint32_t j = j0 + warp; j < j1; j += 8) {
-            const uint4 v = ld_stream(W + (uint64_t)j * K + k);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    auto add_row = [&](const uint4 v) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float x0 = bf16_lo(w[q]), x1 = bf16_hi(w[q]);
-                pair_add(s[2 * q], c[2 * q], x0);
-                pair_add(s[2 * q + 1], c[2 * q + 1], x1);
-                pair_add(sa[2 * q], ca[2 * q], fabsf(x0));
-                pair_add(sa[2 * q + 1], ca[2 * q + 1], fabsf(x1));
-            }
+        for (int q = 0; q < 4; ++q) {
+            const float x0 = bf16_lo(w[q]), x1 = bf16_hi(w[q]);
+            pair_add(s[2 * q], c[2 * q], x0);
+            pair_add(s[2 * q + 1], c[2 * q + 1], x1);
+            pair_add(sa[2 * q], ca[2 * q], fabsf(x0));
+            pair_add(sa[2 * q + 1], ca[2 * q + 1], fabsf(x1));
         }
+    };
+    if (k < K) {
+        uint32_t j = j0 + warp;
+        for (; j + 24 < j1; j += 32) {  // four rows in flight per lane, added in row order
+            const uint4 v0 = ld_stream(W + (uint64_t)j * K + k), v1 = ld_stream(W + (uint64_t)(j + 8) * K + k),
+                        v2 = ld_stream(W + (uint64_t)(j + 16) * K + k), v3 = ld_stream(W + (uint64_t)(j + 24) * K + k);
+            add_row(v0);
+            add_row(v1);
+            add_row(v2);
+            add_row(v3);
+        }
+        for (; j < j1; j += 8) add_row(ld_stream(W + (uint64_t)j * K + k));
     }
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
-        part[warp][lane * 8 + q] = make_double2((double)s[q] + (double)c[q], (double)sa[q] + (double)ca[q]);
+    for (int q = 0; q < 8; ++q) part[warp][lane * 8 + q] = make_float4(s[q], c[q], sa[q], ca[q]);
     __syncthreads();
     const uint32_t kk = blockIdx.x * 256 + threadIdx.x;
     if (kk < K) {
-        double2 acc = part[0][threadIdx.x];
+        float4 acc = part[0][threadIdx.x];
         for (int w = 1; w < 8; ++w) {
-            acc.x = __dadd_rn(acc.x, part[w][threadIdx.x].x);
-            acc.y = __dadd_rn(acc.y, part[w][threadIdx.x].y);
+            const float4 q = part[w][threadIdx.x];
+            pair_merge(acc.x, acc.y, q.x, q.y);
+            pair_merge(acc.z, acc.w, q.z, q.w);
         }
         slabs[(uint64_t)blockIdx.y * K + kk] = acc;
     }
 }
 
-// The slabs summed in order: wcol[k] = {W^T 1, |W|^T 1} in float64 and, for the
-// check, each split into a float32 pair wsplit[k] = {hi, lo, hi_abs, lo_abs}.
-__global__ void abft_colsum_final_kernel(const double2 *__restrict__ slabs, uint32_t K, uint32_t n_slabs,
-                                         double2 *__restrict__ wcol, float4 *__restrict__ wsplit) {
-    const uint32_t k = blockIdx.x * blockDim.x + threadIdx.x;
-    if (k >= K) return;
-    double a = 0.0, b = 0.0;
-    for (uint32_t y = 0; y < n_slabs; ++y) {
-        const double2 p = slabs[(uint64_t)y * K + k];
-        a = __dadd_rn(a, p.x);
-        b = __dadd_rn(b, p.y);
+// The slabs merged: for the check, W^T 1 and |W|^T 1 as normalised float32
+// pairs wsplit[k] = {hi, lo, hi_abs, lo_abs} (hi the float nearest the pair's
+// sum), and wcol[k] = the same values in float64.  Block = 32 columns (one per
+// lane) x 8 warps; warp w merges slabs w, w + 8, ... in order, then the warps'
+// pairs are merged in warp order (a fixed order: the result is reproducible).
+__global__ void __launch_bounds__(256) abft_colsum_final_kernel(const float4 *__restrict__ slabs, uint32_t K,
+                                                                uint32_t n_slabs, double2 *__restrict__ wcol,
+                                                                float4 *__restrict__ wsplit) {
+    __shared__ float4 part[8][32];
+    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+    const uint32_t k = blockIdx.x * 32 + lane;
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (k < K) {
+#pragma unroll 8
+        for (uint32_t y = warp; y < n_slabs; y += 8) {
+            const float4 q = slabs[(uint64_t)y * K + k];
+            pair_merge(acc.x, acc.y, q.x, q.y);
+            pair_merge(acc.z, acc.w, q.z, q.w);
+        }
     }
-    wcol[k] = make_double2(a, b);
-    const float ah = (float)a, bh = (float)b;
-    wsplit[k] = make_float4(ah, (float)(a - (double)ah), bh, (float)(b - (double)bh));
+    part[warp][lane] = acc;
+    __syncthreads();
+    if (warp != 0 || k >= K) return;
+    for (int w = 1; w < 8; ++w) {
+        const float4 q = part[w][lane];
+        pair_merge(acc.x, acc.y, q.x, q.y);
+        pair_merge(acc.z, acc.w, q.z, q.w);
+    }
+    float h = 0.0f, l = 0.0f, ha = 0.0f, la = 0.0f;  // renormalise: TwoSum of the two parts
+    pair_add(h, l, acc.x);
+    pair_add(h, l, acc.y);
+    pair_add(ha, la, acc.z);
+    pair_add(ha, la, acc.w);
+    wsplit[k] = make_float4(h, l, ha, la);
+    wcol[k] = make_double2((double)h + (double)l, (double)ha + (double)la);
 }
 
 // Per row: the reference A (W^T 1) and the magnitude |A| (|W|^T 1) as float32
 // pairs, the bound, the residual against the accumulator checksum, and the
-// flag.  One warp per kCheckRows rows (each column pair loaded once for them),
-// lanes over 8-column vectors.
-__global__ void __launch_bounds__(256) abft_check_kernel(const __nv_bfloat16 *__restrict__ A, uint32_t M, uint32_t N,
+// flag.  One block of kCheckThreads threads per kCheckRows rows: the threads stride over
+// the 8-column vectors (each column pair loaded once for all the rows), then
+// the pairs are merged across lanes (butterfly) and across warps (in order).
+__global__ void __launch_bounds__(kCheckThreads) abft_check_kernel(const __nv_bfloat16 *__restrict__ A, uint32_t M, uint32_t N,
                                                          uint32_t K, const double *__restrict__ rowsum,
                                                          const float4 *__restrict__ wsplit, float tol_scale,
                                                          double *__restrict__ residual, double *__restrict__ bound,
                                                          uint8_t *__restrict__ flag,
                                                          sdc_abft_summary *__restrict__ summary) {
-    const uint32_t lane = threadIdx.x & 31u;
-    const uint64_t warp = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const uint64_t row0 = warp * kCheckRows;
-    if (row0 >= M) return;  // M is a multiple of 128, so all kCheckRows rows exist
+    __shared__ float4 red[kCheckThreads / 32][kCheckRows];
+    const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
+    const uint64_t row0 = (uint64_t)blockIdx.x * kCheckRows;  // M is a multiple of 128: all rows exist
     float rs[kCheckRows], rc[kCheckRows], ms[kCheckRows], mc[kCheckRows];
 #pragma unroll
     for (uint32_t r = 0; r < kCheckRows; ++r) rs[r] = rc[r] = ms[r] = mc[r] = 0.0f;
-    for (uint32_t v = lane; v < K / 8; v += 32) {
+    for (uint32_t v = tid; v < K / 8; v += kCheckThreads) {
         float4 w[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) w[q] = wsplit[v * 8 + q];
+        uint4 av[kCheckRows];
+#pragma unroll
+        for (uint32_t r = 0; r < kCheckRows; ++r) av[r] = ld_stream(A + (row0 + r) * K + (uint64_t)v * 8);
 #pragma unroll
         for (uint32_t r = 0; r < kCheckRows; ++r) {
-            const uint4 av = ld_stream(A + (row0 + r) * K + (uint64_t)v * 8);
-            const uint32_t a4[4] = {av.x, av.y, av.z, av.w};
+            const uint32_t a4[4] = {av[r].x, av[r].y, av[r].z, av[r].w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const float a0 = bf16_lo(a4[q]), a1 = bf16_hi(a4[q]);
@@ -426,20 +464,33 @@ __global__ void __launch_bounds__(256) abft_check_kernel(const __nv_bfloat16 *__
     }
 #pragma unroll
     for (uint32_t r = 0; r < kCheckRows; ++r) {
-        const double ref = warp_sum_f64((double)rs[r] + (double)rc[r]);
-        const double mag = warp_sum_f64((double)ms[r] + (double)mc[r]);
-        if (lane == 0) {
-            const uint64_t i = row0 + r;
-            const double g = (double)K * 0x1p-22;
-            const double b =
-                (g * (1.0 + g) + (double)(N + K + 64) * 0x1p-44) * mag + 2.0 * (double)K * (double)N * 0x1p-126;
-            const double d = rowsum[i] - ref;
-            residual[i] = d;
-            bound[i] = b;
-            const uint8_t f = fabs(d) <= (double)tol_scale * b ? 0 : 1;  // NaN flags
-            flag[i] = f;
-            if (f) atomicAdd(&summary->n_flagged, 1u);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float s2 = __shfl_xor_sync(0xffffffffu, rs[r], off), c2 = __shfl_xor_sync(0xffffffffu, rc[r], off);
+            const float t2 = __shfl_xor_sync(0xffffffffu, ms[r], off), d2 = __shfl_xor_sync(0xffffffffu, mc[r], off);
+            pair_merge(rs[r], rc[r], s2, c2);
+            pair_merge(ms[r], mc[r], t2, d2);
         }
+        if (lane == 0) red[warp][r] = make_float4(rs[r], rc[r], ms[r], mc[r]);
+    }
+    __syncthreads();
+    if (tid < kCheckRows) {
+        float4 p = red[0][tid];
+        for (uint32_t w = 1; w < kCheckThreads / 32; ++w) {
+            const float4 q = red[w][tid];
+            pair_merge(p.x, p.y, q.x, q.y);
+            pair_merge(p.z, p.w, q.z, q.w);
+        }
+        const double ref = (double)p.x + (double)p.y, mag = (double)p.z + (double)p.w;
+        const uint64_t i = row0 + tid;
+        const double g = (double)K * 0x1p-22;
+        const double b = (g * (1.0 + g) + (double)(N + K + 64) * 0x1p-44) * mag + 2.0 * (double)K * (double)N * 0x1p-126;
+        const double d = rowsum[i] - ref;
+        residual[i] = d;
+        bound[i] = b;
+        const uint8_t f = fabs(d) <= (double)tol_scale * b ? 0 : 1;  // NaN flags
+        flag[i] = f;
+        if (f) atomicAdd(&summary->n_flagged, 1u);
     }
 }
 
@@ -491,7 +542,7 @@ AbftWs abft_ws(uint32_t M, uint32_t N, uint32_t K) {
     w.wcol = round_up256((size_t)(N / kBN) * M * sizeof(double));
     w.wsplit = w.wcol + round_up256((size_t)K * sizeof(double2));
     w.slabs = w.wsplit + round_up256((size_t)K * sizeof(float4));
-    w.err = w.slabs + round_up256((size_t)n_slabs_for(N) * K * sizeof(double2));
+    w.err = w.slabs + round_up256((size_t)n_slabs_for(N) * K * sizeof(float4));
     w.total = w.err + 256;
     return w;
 }
@@ -552,8 +603,7 @@ sdc_status sdc_abft_gemm(const void *d_A, const void *d_W, void *d_C, uint32_t M
     band_m = band_m < 1 ? 1 : (band_m > M / kBM ? M / kBM : band_m);
     abft_gemm_kernel<<<grid, kGemmThreads, kGemmSmem, s>>>(mapA, mapW, (__nv_bfloat16 *)d_C, M, N, K, band_m, part,
                                                            err);
-    abft_rowsum_kernel<<<(M + 255) / 256, 256, 0, s>>>(part, M, N / kBN, d_rowsum);
-    abft_finish_kernel<<<1, 1, 0, s>>>(err, d_aborted);
+    abft_rowsum_kernel<<<(M + 63) / 64, 64, 0, s>>>(part, M, N / kBN, d_rowsum, err, d_aborted);
     e = cudaGetLastError();
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_abft_gemm launch");
 }
@@ -569,16 +619,15 @@ sdc_status sdc_abft_verify(const void *d_A, const void *d_W, uint32_t M, uint32_
     const AbftWs w = abft_ws(M, N, K);
     double2 *wcol = (double2 *)((char *)d_ws + w.wcol);
     float4 *wsplit = (float4 *)((char *)d_ws + w.wsplit);
-    double2 *slabs = (double2 *)((char *)d_ws + w.slabs);
+    float4 *slabs = (float4 *)((char *)d_ws + w.slabs);
     const uint32_t n_slabs = n_slabs_for(N);
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = cudaMemsetAsync(d_summary, 0, sizeof(sdc_abft_summary), s);
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_verify setup");
     abft_colsum_slab_kernel<<<dim3((K + 255) / 256, n_slabs), 256, 0, s>>>((const __nv_bfloat16 *)d_W, N, K, n_slabs,
                                                                            slabs);
-    abft_colsum_final_kernel<<<(K + 255) / 256, 256, 0, s>>>(slabs, K, n_slabs, wcol, wsplit);
-    const uint64_t warps = M / kCheckRows;
-    abft_check_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(
+    abft_colsum_final_kernel<<<(K + 31) / 32, 256, 0, s>>>(slabs, K, n_slabs, wcol, wsplit);
+    abft_check_kernel<<<M / kCheckRows, kCheckThreads, 0, s>>>(
         (const __nv_bfloat16 *)d_A, M, N, K, d_rowsum, wsplit, tol_scale, d_residual, d_bound, d_flag, d_summary);
     e = cudaGetLastError();
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_abft_verify launch");
