@@ -10,8 +10,9 @@ Sources (web pages on silent data corruption):
   [AEGIS] "Safeguarding LLM Training at Scale: Online SDC Detection and
           Insights from 35 Million GPU Hours" (review page).
 
-The GEMM checksum functions at the end are plain numpy in float64; their
-parity with the tensor-core kernel is up to the rounding bound they state.
+The GEMM checksum and attention-invariant functions at the end are plain numpy
+in float64; their parity with the tensor-core kernels is up to the rounding
+bounds they state.
 
 The element loops live in ``sdc_oracle.c`` (plain scalar C, compiled with gcc
 on first use); the vote and the exact rounding of the sum of squares are plain
@@ -488,6 +489,52 @@ def abft_verify(rowsum: np.ndarray, A_bits: np.ndarray, W_bits: np.ndarray, tol_
     ref, mag = abft_reference(A_bits, W_bits)
     residual = np.asarray(rowsum, dtype=np.float64) - ref
     bound = abft_bound(mag, N, K)
+    with np.errstate(invalid="ignore"):
+        flag = ~(np.abs(residual) <= tol_scale * bound)
+    return {"residual": residual, "bound": bound, "flag": flag.astype(np.uint8), "n_flagged": int(flag.sum())}
+
+
+# --------------------------------------------------------------------------
+# Attention invariant  ([AEGIS] method section 3: in the attention backward
+# dV = P^T dO and every row of the softmax P sums to 1, so 1^T dV = 1^T dO;
+# the column sums of dV come from its float32 accumulator)
+# --------------------------------------------------------------------------
+def attn_probs(Q_bits: np.ndarray, K_bits: np.ndarray, lse: np.ndarray, scale: float, causal: bool) -> np.ndarray:
+    """P [L, L] of one head, rebuilt as the backward does: exp(scale Q K^T - lse) with
+    the forward's log-sum-exp per query row; causal masks key j > query i to 0."""
+    S = bf16_to_f64(Q_bits) @ bf16_to_f64(K_bits).T
+    P = np.exp(S * float(np.float32(scale)) - np.asarray(lse, dtype=np.float64)[:, None])
+    if causal:
+        P = np.tril(P)
+    return P
+
+
+def attn_dv(P: np.ndarray, dO_bits: np.ndarray) -> np.ndarray:
+    """dV = P^T dO of one head, float64."""
+    return P.T @ bf16_to_f64(dO_bits)
+
+
+def attn_bound(abs_colsum_do: np.ndarray, L: int) -> np.ndarray:
+    """Bound on |1^T dV - 1^T dO| per column for a backward that rounds P to bf16
+    and accumulates dV in float32 over the L query rows.
+
+    Each probability may be off by 2^-8 of itself (its bf16 rounding, 2^-9, plus up
+    to 2^-9 for the recomputed scores, the exponential and the forward's float32
+    log-sum-exp), so a row of P sums to 1 within 2^-8 (1 + 2^-7); each float32
+    accumulation step may lose two units in the last place of its partial sum
+    (g = L 2^-22); the column sums themselves are float32 pairs (2^-40)."""
+    g = L * 2.0 ** -22
+    rho = 1.0 + 2.0 ** -7
+    return (2.0 ** -8 * rho + g * (1.0 + g) * rho + 2.0 ** -40) * np.asarray(abs_colsum_do, dtype=np.float64) + 2.0 ** -100
+
+
+def attn_invariant(colsum_dv: np.ndarray, dO_bits: np.ndarray, tol_scale: float = 1.0) -> dict:
+    """The invariant of one head: residual[c] = colsum_dv[c] - sum_i dO[i, c], the bound,
+    and the column flags (flagged unless |residual| <= tol_scale * bound; NaN flags)."""
+    dO = bf16_to_f64(dO_bits)
+    L = dO.shape[0]
+    residual = np.asarray(colsum_dv, dtype=np.float64) - dO.sum(axis=0)
+    bound = attn_bound(np.abs(dO).sum(axis=0), L)
     with np.errstate(invalid="ignore"):
         flag = ~(np.abs(residual) <= tol_scale * bound)
     return {"residual": residual, "bound": bound, "flag": flag.astype(np.uint8), "n_flagged": int(flag.sum())}
