@@ -293,6 +293,44 @@ sdc_status sdc_abft_verify(const void *d_A, const void *d_W, uint32_t M, uint32_
                            float tol_scale, double *d_residual, double *d_bound, uint8_t *d_flag,
                            sdc_abft_summary *d_summary, void *d_ws, size_t ws_bytes, sdc_stream_t stream);
 
+/* ---------------------------------------------------------------- attention invariant (AEGIS) */
+
+/* Workspace bytes of sdc_attn_dv_check (0 unless D == 128). */
+size_t sdc_attn_workspace_size(uint32_t BH, uint32_t L, uint32_t D);
+
+/* The dV half of the attention backward with the invariant 1^T dV = 1^T dO.
+ * [AEGIS] method section 3: dV = P^T dO and every row of the softmax P sums
+ * to 1, so dV's column sums (taken from the float32 accumulator) equal dO's;
+ * P is rebuilt from Q K^T, the softmax and the forward's log-sum-exp, so an
+ * upstream error that breaks the row sums breaks the invariant too.
+ *
+ * Inputs (device): d_Q, d_K, d_dO bf16 [BH][L][D] (BH heads, L tokens, row-
+ * major, 16-byte aligned); d_lse float [BH][L], the forward's natural-log
+ * log-sum-exp of scale * q_i . k_j over the keys each query attends; scale
+ * (> 0, e.g. 1/sqrt(D)); causal (1: query i attends keys j <= i).  D must be
+ * 128 and L a positive multiple of 128.
+ * Computes P[i][j] = exp(scale q_i . k_j - lse_i) (bf16 for the product, as a
+ * flash-attention backward does), d_dV = P^T dO (bf16 [BH][L][D], float32
+ * accumulation on the tensor cores), and per head h and column c:
+ *   d_colsum_dv[h][c] = sum_j of dV's float32 accumulator [j][c],
+ *   d_colsum_do[h][c] = sum_i dO[i][c],
+ *   d_residual = colsum_dv - colsum_do,
+ *   d_bound = (2^-8 rho + g (1 + g) rho + 2^-40) sum_i |dO[i][c]| + 2^-100,
+ *     g = L 2^-22, rho = 1 + 2^-7 (each probability within 2^-8 of itself:
+ *     its bf16 rounding and up to 2^-9 for the recomputed scores, exp and the
+ *     float32 log-sum-exp; each float32 accumulation step within two ulps),
+ *   d_flag[h][c] = 1 unless |residual| <= tol_scale * bound (NaN flags),
+ * all double/uint8 [BH][D]; d_summary counts the flagged columns; *d_aborted
+ * = 1 if a bounded wait gave up (results then invalid).
+ * Errors: SDC_ERR_NULL, SDC_ERR_BAD_ARG (shapes, scale, tol_scale, causal),
+ * SDC_ERR_BAD_POINTER (alignment), SDC_ERR_WRONG_DEVICE, SDC_ERR_WS_TOO_SMALL.
+ * The workspace (256-byte aligned) holds dO^T and per-block partial sums. */
+sdc_status sdc_attn_dv_check(const void *d_Q, const void *d_K, const void *d_dO, const float *d_lse, uint32_t BH,
+                             uint32_t L, uint32_t D, float scale, uint32_t causal, float tol_scale, void *d_dV,
+                             double *d_colsum_dv, double *d_colsum_do, double *d_residual, double *d_bound,
+                             uint8_t *d_flag, sdc_abft_summary *d_summary, uint32_t *d_aborted, void *d_ws,
+                             size_t ws_bytes, sdc_stream_t stream);
+
 /* ---------------------------------------------------------------- ring replay audit */
 
 /* Counts written by sdc_ring_audit. */

@@ -23,6 +23,12 @@ Workloads (sizes follow the parameter layouts below):
             N = 14336, K = 4096).  A fault is planted by XORing bits of chosen
             elements of a copy of A (the operand as a faulty unit would read
             it), the clean A being the reference.
+  attn      one attention layer's backward inputs: BH heads of L tokens, head
+            dimension 128, Q, K, dO bf16 N(0, 1), scale 1/sqrt(128), and the
+            forward's log-sum-exp (torch.logsumexp of the float32 scores, the
+            causal mask applied) as float32; the benchmark shape is the 8b
+            layout's 32 heads at L = 4096, causal.  Faults are planted in a
+            copy of an input (a shifted log-sum-exp row, an XORed element of K).
   stress    100,000 tensors, numel = floor(exp(U(0, ln(1e6 + 1)))), dtype
             uniform over float32/bf16/float16, packed per replica in one flat
             buffer (element-aligned starts), 3 replicas with one bit flip;
@@ -281,3 +287,23 @@ def gemm_fault(A: torch.Tensor, rows: list[int], seed: int = 7, mask: int = 0x40
         xor_element(Af, r * K + c, mask)
         where.append((int(r), c))
     return Af, where
+
+
+ATTN_8B = (32, 4096)  # heads, tokens (head dimension 128)
+
+
+def attn_inputs(BH: int, L: int, device, seed: int = 8, causal: bool = True, D: int = 128) -> dict:
+    """Seeded Q, K, dO (bf16 [BH, L, D]) and the forward's float32 log-sum-exp [BH, L]."""
+    gen = generator(seed, device)
+    Q = normal((BH, L, D), 1.0, torch.bfloat16, gen, device)
+    K = normal((BH, L, D), 1.0, torch.bfloat16, gen, device)
+    dO = normal((BH, L, D), 1.0, torch.bfloat16, gen, device)
+    scale = 1.0 / math.sqrt(D)
+    lse = torch.empty((BH, L), dtype=torch.float32, device=device)
+    mask = torch.ones((L, L), dtype=torch.bool, device=device).triu(1) if causal else None
+    for h in range(BH):  # the forward's softmax statistics, one head at a time
+        s = (Q[h].float() @ K[h].float().t()) * scale
+        if mask is not None:
+            s.masked_fill_(mask, float("-inf"))
+        lse[h] = torch.logsumexp(s, dim=-1)
+    return {"Q": Q, "K": K, "dO": dO, "lse": lse, "scale": scale, "causal": causal}

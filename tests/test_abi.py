@@ -112,6 +112,21 @@ def test_host_validation_without_gpu(sdc):
     # min(64, N/128) slabs of K float64 pairs, the abort word; each rounded up to 256 bytes
     assert sdc.sdc_abft_workspace_size(128, 512, 64) == 2048 + 1024 + 1024 + 4 * 64 * 16 + 256
     assert sdc.sdc_abft_workspace_size(1000, 256, 100) == 8192 + 1792 + 1792 + 3328 + 256
+    # attention invariant: inputs checked, then shapes and scalars, before any CUDA call
+    fake = [4096, 8192, 12288, 16384]
+    outs = [20480 + 4096 * i for i in range(8)]
+    with pytest.raises(sdc.SdcError) as ei:
+        sdc.sdc_attn_dv_check(0, *fake[1:], 1, 128, 128, 0.088, 0, 1.0, *outs, 0, 0, 0)
+    assert ei.value.status == 1
+    for BH, L, D, scale, causal, tol in [(1, 128, 64, 0.088, 0, 1.0), (1, 100, 128, 0.088, 0, 1.0),
+                                         (0, 128, 128, 0.088, 0, 1.0), (1, 128, 128, -1.0, 0, 1.0),
+                                         (1, 128, 128, 0.088, 2, 1.0), (1, 128, 128, 0.088, 0, 0.0)]:
+        with pytest.raises(sdc.SdcError) as ei:
+            sdc.sdc_attn_dv_check(*fake, BH, L, D, scale, causal, tol, *outs, 0, 0, 0)
+        assert ei.value.status == 9, (BH, L, D, scale, causal, tol)
+    # dO^T, dO partials (float4 per block and column), dV partials (float2), the abort word
+    assert sdc.sdc_attn_workspace_size(2, 256, 128) == 2 * 128 * 256 * 2 + 2 * 2 * 128 * 16 + 2 * 2 * 128 * 8 + 256
+    assert sdc.sdc_attn_workspace_size(2, 256, 64) == 0
     assert sdc.sdc_abft_workspace_size(128, 16384, 64) == 64 * 128 * 8 + 1024 + 1024 + 64 * 64 * 16 + 256
 
 
