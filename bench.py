@@ -340,6 +340,8 @@ def bench_rows(args, dev, stream, peaks, sdc, W, torch, np, only=None) -> dict:
         return bench_big_rows(args, dev, stream, peaks, sdc, W, torch, only)
     if only == "abft_gemm":
         return bench_abft_row(args, dev, stream, peaks, sdc, W, torch)
+    if only == "attn_invariant":
+        return bench_attn_row(args, dev, stream, peaks, sdc, W, torch)
     # fused gradient average-scan on 4 bf16 buffers of the 1b layout
     g = W.grads_flat(W.layout_numel(W.layout_1b(args.layers)), 4, torch.bfloat16, 1e-3, dev, seed=3)
     bufs = g["bufs"]
@@ -391,6 +393,8 @@ def bench_rows(args, dev, stream, peaks, sdc, W, torch, np, only=None) -> dict:
     torch.cuda.empty_cache()
     if only in (None, "abft_gemm"):
         rows.update(bench_abft_row(args, dev, stream, peaks, sdc, W, torch))
+    if only in (None, "attn_invariant"):
+        rows.update(bench_attn_row(args, dev, stream, peaks, sdc, W, torch))
     if not getattr(args, "no_big_rows", False):
         rows.update(bench_big_rows(args, dev, stream, peaks, sdc, W, torch, only))
     return rows
@@ -451,6 +455,34 @@ def bench_abft_row(args, dev, stream, peaks, sdc, W, torch) -> dict:
                          "clean_rows_flagged": int(g.summary[0]), "aborted": int(g.aborted[0]),
                          "max_residual_over_bound": float((g.residual.abs() / g.bound).max())}}
     del g, ops, A, Wt
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_attn_row(args, dev, stream, peaks, sdc, W, torch) -> dict:
+    """The dV half of the attention backward with the invariant 1^T dV = 1^T dO, on the 8b
+    layout's 32 heads of 128 at 4,096 tokens, causal; torch's fused backward (dQ, dK, dV) beside it."""
+    BH, L = W.ATTN_8B
+    x = W.attn_inputs(BH, L, dev, seed=8, causal=True)
+    a = sdc.AttnDvCheck(BH, L, dev)
+    reps = max(10, args.steps // 10)
+    ms = _time_loop(lambda: a(x["Q"], x["K"], x["dO"], x["lse"], x["scale"], True, stream=stream), reps, stream,
+                    torch)
+    torch.cuda.synchronize()
+    flops = 2 * 2.0 * L * L * 128 * BH * 0.5  # S^T = K Q^T and dV = P^T dO over the causal half
+    tf = flops / (ms * 1e-3) / 1e12
+    q, k, v = (t.unsqueeze(0).clone().requires_grad_(True) for t in (x["Q"], x["K"], x["dO"]))
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True)
+    g = x["dO"].unsqueeze(0)
+    ms_ref = _time_loop(lambda: torch.autograd.grad(o, (q, k, v), g, retain_graph=True), reps, stream, torch)
+    out = {"attn_invariant": {"workload": f"{BH} heads x {L} tokens x 128, causal, bf16 Q/K/dO N(0,1), fp32 "
+                              "log-sum-exp: dV = P^T dO (P rebuilt from Q K^T and the log-sum-exp) + 1^T dV vs 1^T dO",
+                              "ms": ms, "tflops": tf, "frac_bf16_peak": tf / peaks["bf16_tflops"],
+                              "peak_tflops": peaks["bf16_tflops"],
+                              "clean_columns_flagged": int(a.summary[0]), "aborted": int(a.aborted[0]),
+                              "max_residual_over_bound": float((a.residual.abs() / a.bound).max()),
+                              "torch_fused_backward_dq_dk_dv_ms": ms_ref}}
+    del a, x, q, k, v, o
     torch.cuda.empty_cache()
     return out
 
@@ -561,7 +593,8 @@ def main(argv=None) -> None:
     ap.add_argument("--chunk-bytes", type=int, default=0)
     ap.add_argument("--quick", action="store_true", help="only the timed fingerprint step (no rows/e2e/cpu)")
     ap.add_argument("--no-big-rows", action="store_true", help="skip the 8b and stress rows")
-    ap.add_argument("--only", choices=["grad_average_scan", "grad_scan", "xorsum", "abft_gemm", "fingerprint_8b",
+    ap.add_argument("--only", choices=["grad_average_scan", "grad_scan", "xorsum", "abft_gemm", "attn_invariant",
+                                       "fingerprint_8b",
                                        "fingerprint_stress", "adamw_fingerprint"], default=None,
                     help="time one row alone (profiling)")
     ap.add_argument("--layers", type=int, default=24,
