@@ -469,7 +469,8 @@ def abft_reference(A_bits: np.ndarray, W_bits: np.ndarray) -> tuple[np.ndarray, 
 
 
 def abft_bound(mag: np.ndarray, N: int, K: int) -> np.ndarray:
-    """Rounding bound of a row checksum taken from a float32 accumulator.
+    """Rounding bound of a checksum of N outputs taken from their float32 accumulators
+    (N: the columns a row checksum sums, or the rows a column checksum sums).
 
     Each of the K float32 accumulation steps of one output may lose up to two
     units in the last place of its partial sum (g = K 2^-22 per output to first
@@ -478,6 +479,26 @@ def abft_bound(mag: np.ndarray, N: int, K: int) -> np.ndarray:
     flushed to zero lose 2^-126 per product and per step."""
     g = K * 2.0 ** -22
     return (g * (1.0 + g) + (N + K + 64) * 2.0 ** -44) * np.asarray(mag, dtype=np.float64) + 2.0 * K * N * 2.0 ** -126
+
+
+def abft_reference_cols(A_bits: np.ndarray, W_bits: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """(1^T A) W^T and the magnitude sum_k (sum_i |A[i,k]|) |W[j,k]| of each output column, float64:
+    the column side of the check (the page's row + column configuration)."""
+    A = bf16_to_f64(A_bits)
+    W = bf16_to_f64(W_bits)
+    return W @ A.sum(axis=0), np.abs(W) @ np.abs(A).sum(axis=0)
+
+
+def abft_verify_cols(colsum: np.ndarray, A_bits: np.ndarray, W_bits: np.ndarray, tol_scale: float = 1.0) -> dict:
+    """The column check: residual = 1^T C (accumulator) - (1^T A) W^T per column, its bound (the
+    row bound with the M summed rows in place of the N summed columns), the column flags."""
+    M, K = A_bits.shape
+    ref, mag = abft_reference_cols(A_bits, W_bits)
+    residual = np.asarray(colsum, dtype=np.float64) - ref
+    bound = abft_bound(mag, M, K)
+    with np.errstate(invalid="ignore"):
+        flag = ~(np.abs(residual) <= tol_scale * bound)
+    return {"residual": residual, "bound": bound, "flag": flag.astype(np.uint8), "n_flagged": int(flag.sum())}
 
 
 def abft_verify(rowsum: np.ndarray, A_bits: np.ndarray, W_bits: np.ndarray, tol_scale: float = 1.0) -> dict:

@@ -167,3 +167,40 @@ def test_flag_rule_edges():
     assert list(v["flag"]) == [0, 1, 1, 1]  # equality passes; NaN and infinities flag
     v = oracle.abft_verify(rowsum, Ab, Wb, tol_scale=2.0)
     assert list(v["flag"]) == [0, 0, 1, 1]
+
+
+def test_column_identity_and_planted_weight_fault():
+    # 1^T (A W^T) = (1^T A) W^T exactly on integers; a fault in W's row j (the GEMM reads
+    # W' = W + delta e_(j,k), the check uses W) moves column j's residual by delta sum_i A[i, k]
+    M, N, K = 12, 10, 18
+    A, W, Ab, Wb = _int_operands(M, N, K, 7, lo=-8, hi=8)
+    colsum = oracle.abft_product(Ab, Wb).sum(axis=0)
+    brute = [sum(int(A[i, k]) * int(W[j, k]) for i in range(M) for k in range(K)) for j in range(N)]
+    assert list(colsum) == brute
+    v = oracle.abft_verify_cols(colsum, Ab, Wb)
+    assert v["n_flagged"] == 0 and np.all(v["residual"] == 0)
+    j, k, delta = 4, 9, 5
+    Wf = W.copy()
+    Wf[j, k] += delta
+    colsum_f = oracle.abft_product(Ab, _bf16_bits(Wf.astype(np.float32))).sum(axis=0)
+    v = oracle.abft_verify_cols(colsum_f, Ab, Wb)
+    expect = np.zeros(N)
+    expect[j] = delta * int(A[:, k].sum())
+    assert np.array_equal(v["residual"], expect)
+    # the row check sees the same fault spread over every row: delta A[i, k] on row i
+    vr = oracle.abft_verify(oracle.abft_product(Ab, _bf16_bits(Wf.astype(np.float32))).sum(axis=1), Ab, Wb)
+    assert np.array_equal(vr["residual"], delta * A[:, k].astype(float))
+
+
+@pytest.mark.parametrize("mode", ["rn", "trunc", "block16"])
+def test_column_bound_covers_float32_accumulation(mode):
+    M, N, K = 32, 8, 512
+    rng = np.random.default_rng(8)
+    A32 = (rng.uniform(0.5, 1.0, (M, K)) * 2.0 ** -rng.integers(0, 12, (M, K))).astype(np.float32)
+    W32 = (rng.uniform(0.5, 1.0, (N, K)) * 2.0 ** -rng.integers(0, 12, (N, K))).astype(np.float32)
+    A32[:, 0], W32[:, 0] = 2.0 ** 10, 2.0 ** 4
+    Ab, Wb = _bf16_round(A32), _bf16_round(W32)
+    acc = _emulate_fp32(oracle.bf16_to_f64(Ab), oracle.bf16_to_f64(Wb), mode)
+    v = oracle.abft_verify_cols(acc.sum(axis=0), Ab, Wb)
+    assert v["n_flagged"] == 0
+    assert np.max(np.abs(v["residual"]) / v["bound"]) <= 1.0
