@@ -438,6 +438,9 @@ def bench_abft_row(args, dev, stream, peaks, sdc, W, torch) -> dict:
     reps = max(10, args.steps // 10)
     ms_gemm = _time_loop(lambda: g.gemm(A, Wt, stream=stream), reps, stream, torch)
     ms_verify = _time_loop(lambda: g.verify(A, Wt, stream=stream), reps, stream, torch)
+    gc = sdc.AbftGemm(M, N, K, dev, columns=True)  # the row + column configuration
+    ms_gemm_rc = _time_loop(lambda: gc.gemm(A, Wt, stream=stream), reps, stream, torch)
+    ms_verify_rc = _time_loop(lambda: gc.verify(A, Wt, stream=stream), reps, stream, torch)
     ms_cublas = _time_loop(lambda: torch.matmul(A, Wt.t()), reps, stream, torch)
     torch.cuda.synchronize()
     flops = 2.0 * M * N * K
@@ -450,11 +453,14 @@ def bench_abft_row(args, dev, stream, peaks, sdc, W, torch) -> dict:
                          "peak_kind": f"burst bf16 (MEASURED_PEAKS.json bf16_tflops, {peaks['source']})",
                          "verify_ms": ms_verify, "verify_GB_s": vbytes / ms_verify / 1e6,
                          "verify_frac_hbm": vbytes / ms_verify / 1e6 / peaks["hbm_gbs"],
+                         "row_col_gemm_ms": ms_gemm_rc, "row_col_tflops": flops / (ms_gemm_rc * 1e-3) / 1e12,
+                         "row_col_over_row_only": ms_gemm_rc / ms_gemm - 1.0, "row_col_verify_ms": ms_verify_rc,
+                         "row_col_clean_flagged": [int(gc.summary[0]), int(gc.summary[1])],
                          "cublas_plain_gemm_ms": ms_cublas,
                          "cublas_tflops": flops / (ms_cublas * 1e-3) / 1e12,
                          "clean_rows_flagged": int(g.summary[0]), "aborted": int(g.aborted[0]),
                          "max_residual_over_bound": float((g.residual.abs() / g.bound).max())}}
-    del g, ops, A, Wt
+    del g, gc, ops, A, Wt
     torch.cuda.empty_cache()
     return out
 

@@ -254,10 +254,10 @@ sdc_status sdc_adamw_fingerprint(const sdc_plan *plan, const sdc_opt_state *stat
 
 /* ---------------------------------------------------------------- GEMM checksums (AEGIS) */
 
-/* Counts written by sdc_abft_verify. */
+/* Counts written by sdc_abft_verify and sdc_attn_dv_check. */
 typedef struct {
-    uint32_t n_flagged;  /* rows whose checksum residual exceeds tol_scale x bound */
-    uint32_t reserved;
+    uint32_t n_flagged;      /* GEMM: flagged rows; attention: flagged (head, column) pairs */
+    uint32_t n_flagged_cols; /* GEMM: flagged columns (0 without the column check); attention: 0 */
 } sdc_abft_summary;
 
 /* Workspace bytes of sdc_abft_gemm / sdc_abft_verify (one buffer may serve both
@@ -271,11 +271,15 @@ size_t sdc_abft_workspace_size(uint32_t M, uint32_t N, uint32_t K);
  * accumulator inside the kernel.  d_A: device bf16 [M][K]; d_W: device bf16
  * [N][K] (both row-major, K contiguous, 16-byte aligned); d_C: device bf16
  * [M][N].  M a multiple of 128, N of 256, K of 64.  d_rowsum: device double
- * [M], sum over j of the fp32 accumulator of C[i][j] (summed in float64, tile
- * partials in a fixed order); d_aborted: device uint32, 1 if a bounded wait
- * of the GEMM gave up (results then invalid). */
+ * [M], sum over j of the fp32 accumulator of C[i][j] (float32 pairs per
+ * 256-column tile, tile partials added in a fixed order in float64).
+ * d_colsum: NULL, or device double [N] for the page's row + column
+ * configuration: sum over i of the fp32 accumulator of C[i][j] (float32 pairs
+ * per 32 rows, partials added in a fixed order).  d_aborted: device uint32,
+ * 1 if a bounded wait of the GEMM gave up (results then invalid). */
 sdc_status sdc_abft_gemm(const void *d_A, const void *d_W, void *d_C, uint32_t M, uint32_t N, uint32_t K,
-                         double *d_rowsum, uint32_t *d_aborted, void *d_ws, size_t ws_bytes, sdc_stream_t stream);
+                         double *d_rowsum, double *d_colsum, uint32_t *d_aborted, void *d_ws, size_t ws_bytes,
+                         sdc_stream_t stream);
 
 /* The checksum verifier: per row, the reference A(W^T 1) in float64, the
  * residual d_residual[i] = d_rowsum[i] - reference, the rounding bound
@@ -285,12 +289,18 @@ sdc_status sdc_abft_gemm(const void *d_A, const void *d_W, void *d_C, uint32_t M
  * the check's own sums, carried as float32 pairs, and flushed subnormals are
  * covered; so a correct product stays inside it), and d_flag[i] = 1 unless
  * |residual| <= tol_scale * bound (a NaN residual flags; tol_scale > 0; the
- * page's adaptive threshold has no published constants).  d_summary counts
- * the flagged rows.  Same shapes and workspace as sdc_abft_gemm; K <= 2^20.
+ * page's adaptive threshold has no published constants).  With d_colsum
+ * (from sdc_abft_gemm) the columns are checked too, against (1^T A) W^T:
+ * d_residual_col[j], d_bound_col[j] (the same bound with M, the rows summed,
+ * in place of N and mag = sum_k sum_i |A[i][k]| |W[j][k]|) and d_flag_col[j];
+ * with d_colsum NULL the three column outputs are not touched.  d_summary
+ * counts the flagged rows and columns.  Same shapes and workspace as
+ * sdc_abft_gemm; K <= 2^20.
  * Errors: SDC_ERR_BAD_ARG for shapes, SDC_ERR_BAD_POINTER for misalignment,
  * SDC_ERR_WS_TOO_SMALL, SDC_ERR_WRONG_DEVICE. */
 sdc_status sdc_abft_verify(const void *d_A, const void *d_W, uint32_t M, uint32_t N, uint32_t K, const double *d_rowsum,
-                           float tol_scale, double *d_residual, double *d_bound, uint8_t *d_flag,
+                           const double *d_colsum, float tol_scale, double *d_residual, double *d_bound,
+                           uint8_t *d_flag, double *d_residual_col, double *d_bound_col, uint8_t *d_flag_col,
                            sdc_abft_summary *d_summary, void *d_ws, size_t ws_bytes, sdc_stream_t stream);
 
 /* ---------------------------------------------------------------- attention invariant (AEGIS) */

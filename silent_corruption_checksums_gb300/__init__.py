@@ -95,8 +95,9 @@ def _load() -> ctypes.CDLL:
         "sdc_opt_state_destroy": ([vp], ctypes.c_int),
         "sdc_adamw_fingerprint": ([vp, vp, ctypes.POINTER(AdamWHparams), vp, vp, vp, sz, vp], ctypes.c_int),
         "sdc_abft_workspace_size": ([u32, u32, u32], sz),
-        "sdc_abft_gemm": ([vp, vp, vp, u32, u32, u32, vp, vp, vp, sz, vp], ctypes.c_int),
-        "sdc_abft_verify": ([vp, vp, u32, u32, u32, vp, ctypes.c_float, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
+        "sdc_abft_gemm": ([vp, vp, vp, u32, u32, u32, vp, vp, vp, vp, sz, vp], ctypes.c_int),
+        "sdc_abft_verify": ([vp, vp, u32, u32, u32, vp, vp, ctypes.c_float, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
+                            ctypes.c_int),
         "sdc_attn_workspace_size": ([u32, u32, u32], sz),
         "sdc_attn_dv_check": ([vp, vp, vp, vp, u32, u32, u32, ctypes.c_float, u32, ctypes.c_float, vp, vp, vp, vp,
                                vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
@@ -247,15 +248,19 @@ def sdc_abft_workspace_size(M: int, N: int, K: int) -> int:
     return int(_lib.sdc_abft_workspace_size(M, N, K))
 
 
-def sdc_abft_gemm(d_A: int, d_W: int, d_C: int, M: int, N: int, K: int, d_rowsum: int, d_aborted: int, d_ws: int,
-                  ws_bytes: int, stream: int) -> None:
-    _check("sdc_abft_gemm", _lib.sdc_abft_gemm(d_A, d_W, d_C, M, N, K, d_rowsum, d_aborted, d_ws, ws_bytes, stream))
+def sdc_abft_gemm(d_A: int, d_W: int, d_C: int, M: int, N: int, K: int, d_rowsum: int, d_colsum: int,
+                  d_aborted: int, d_ws: int, ws_bytes: int, stream: int) -> None:
+    _check("sdc_abft_gemm", _lib.sdc_abft_gemm(d_A, d_W, d_C, M, N, K, d_rowsum, d_colsum or None, d_aborted, d_ws,
+                                               ws_bytes, stream))
 
 
-def sdc_abft_verify(d_A: int, d_W: int, M: int, N: int, K: int, d_rowsum: int, tol_scale: float, d_residual: int,
-                    d_bound: int, d_flag: int, d_summary: int, d_ws: int, ws_bytes: int, stream: int) -> None:
-    _check("sdc_abft_verify", _lib.sdc_abft_verify(d_A, d_W, M, N, K, d_rowsum, tol_scale, d_residual, d_bound,
-                                                   d_flag, d_summary, d_ws, ws_bytes, stream))
+def sdc_abft_verify(d_A: int, d_W: int, M: int, N: int, K: int, d_rowsum: int, d_colsum: int, tol_scale: float,
+                    d_residual: int, d_bound: int, d_flag: int, d_residual_col: int, d_bound_col: int,
+                    d_flag_col: int, d_summary: int, d_ws: int, ws_bytes: int, stream: int) -> None:
+    _check("sdc_abft_verify", _lib.sdc_abft_verify(d_A, d_W, M, N, K, d_rowsum, d_colsum or None, tol_scale,
+                                                   d_residual, d_bound, d_flag, d_residual_col or None,
+                                                   d_bound_col or None, d_flag_col or None, d_summary, d_ws,
+                                                   ws_bytes, stream))
 
 
 def sdc_attn_workspace_size(BH: int, L: int, D: int) -> int:
@@ -503,12 +508,13 @@ def grad_average_scan(bufs, out=None, stream=None, ws=None):
 
 
 class AbftGemm:
-    """C = A . W^T on the tensor cores with the per-row accumulator checksum, and
-    its check against A (W^T 1).  A: bf16 [M, K], W: bf16 [N, K], both contiguous
-    CUDA tensors; M a multiple of 128, N of 256, K of 64.  Output and scratch
-    buffers are allocated once per shape and reused by every call."""
+    """C = A . W^T on the tensor cores with the per-row accumulator checksum (and,
+    with columns=True, the per-column one: the row + column configuration), and
+    its check against A (W^T 1) (and (1^T A) W^T).  A: bf16 [M, K], W: bf16 [N, K],
+    both contiguous CUDA tensors; M a multiple of 128, N of 256, K of 64.  Output
+    and scratch buffers are allocated once per shape and reused by every call."""
 
-    def __init__(self, M: int, N: int, K: int, device):
+    def __init__(self, M: int, N: int, K: int, device, columns: bool = False):
         torch = _torch()
         self.M, self.N, self.K = M, N, K
         self.C = torch.empty((M, N), dtype=torch.bfloat16, device=device)
@@ -518,8 +524,17 @@ class AbftGemm:
         self.bound = torch.empty(M, dtype=torch.float64, device=device)
         self.flag = torch.empty(M, dtype=torch.uint8, device=device)
         self.summary = torch.zeros(2, dtype=torch.int32, device=device)
+        self.columns = columns
+        if columns:
+            self.colsum = torch.empty(N, dtype=torch.float64, device=device)
+            self.residual_col = torch.empty(N, dtype=torch.float64, device=device)
+            self.bound_col = torch.empty(N, dtype=torch.float64, device=device)
+            self.flag_col = torch.empty(N, dtype=torch.uint8, device=device)
         self.ws_bytes = sdc_abft_workspace_size(M, N, K)
         self.ws = _ws(self.ws_bytes, device)
+
+    def _ptr(self, name):
+        return getattr(self, name).data_ptr() if self.columns else 0
 
     def _shape(self, A, W):
         if tuple(A.shape) != (self.M, self.K) or tuple(W.shape) != (self.N, self.K):
@@ -529,15 +544,18 @@ class AbftGemm:
         """The GEMM and its row checksums (self.C, self.rowsum; self.aborted != 0 if a wait gave up)."""
         self._shape(A, W)
         sdc_abft_gemm(A.data_ptr(), W.data_ptr(), self.C.data_ptr(), self.M, self.N, self.K, self.rowsum.data_ptr(),
-                      self.aborted.data_ptr(), self.ws.data_ptr(), self.ws_bytes, _stream_handle(stream))
+                      self._ptr("colsum"), self.aborted.data_ptr(), self.ws.data_ptr(), self.ws_bytes,
+                      _stream_handle(stream))
         return self.C
 
     def verify(self, A, W, tol_scale: float = 1.0, rowsum=None, stream=None):
-        """The check (self.residual, self.bound, self.flag, self.summary[0] = flagged rows)."""
+        """The check (self.residual, self.bound, self.flag, self.summary[0] = flagged rows; with
+        columns, self.residual_col, self.bound_col, self.flag_col, self.summary[1] = flagged columns)."""
         self._shape(A, W)
         rs = self.rowsum if rowsum is None else rowsum
-        sdc_abft_verify(A.data_ptr(), W.data_ptr(), self.M, self.N, self.K, rs.data_ptr(), tol_scale,
-                        self.residual.data_ptr(), self.bound.data_ptr(), self.flag.data_ptr(),
+        sdc_abft_verify(A.data_ptr(), W.data_ptr(), self.M, self.N, self.K, rs.data_ptr(), self._ptr("colsum"),
+                        tol_scale, self.residual.data_ptr(), self.bound.data_ptr(), self.flag.data_ptr(),
+                        self._ptr("residual_col"), self._ptr("bound_col"), self._ptr("flag_col"),
                         self.summary.data_ptr(), self.ws.data_ptr(), self.ws_bytes, _stream_handle(stream))
         return self.flag
 

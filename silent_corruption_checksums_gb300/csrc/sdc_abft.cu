@@ -67,6 +67,8 @@ constexpr uint32_t kAccCols = 256;           // one accumulator; two are allocat
 constexpr uint32_t kGemmThreads = 192;
 constexpr uint32_t kNumBars = 2 * kStages + 5;  // full[S], empty[S], tfull[2], tempty[2], done
 constexpr uint32_t kGemmSmem = kStages * (kStageA + kStageW) + 1024 + 8 * kNumBars + 16;
+constexpr uint32_t kColTileFloats = 32 * 33;  // one epilogue warp's column-sum tile (row pitch 33)
+constexpr uint32_t kGemmSmemCols = kGemmSmem + 4 * kColTileFloats * 4;
 constexpr uint32_t kMaxK = 1u << 20;
 constexpr uint32_t kMaxSlabs = 64;
 constexpr uint32_t kCheckRows = 4;     // rows per block of the check
@@ -102,10 +104,27 @@ __device__ __forceinline__ void tile_coords(uint32_t t, uint32_t tiles_m, uint32
     tn = r / bm;
 }
 
+// The sum over the warp's 32 rows (lanes) of 32 accumulator columns: the warp
+// writes its 32 x 32 block into its own padded shared-memory tile (row pitch
+// 33 words: conflict-free both ways), then lane k sums column k in row order as
+// a float32 pair.  Each column is summed by one lane in a fixed order, so the
+// result is reproducible.
+__device__ __forceinline__ double warp_column_sum(const uint32_t (&r)[32], uint32_t lane, float *tile) {
+#pragma unroll
+    for (int k = 0; k < 32; ++k) tile[lane * 33 + k] = __uint_as_float(r[k]);
+    __syncwarp();
+    float s = 0.0f, c = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) pair_add(s, c, tile[i * 33 + lane]);
+    __syncwarp();  // the tile is reused by the next chunk
+    return (double)s + (double)c;
+}
+
+template <bool kCols>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     abft_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapW,
                      __nv_bfloat16 *__restrict__ C, uint32_t M, uint32_t N, uint32_t K, uint32_t band_m,
-                     double *__restrict__ rowsum_part, int *__restrict__ err) {
+                     double *__restrict__ rowsum_part, double *__restrict__ colsum_part, int *__restrict__ err) {
     extern __shared__ __align__(1024) unsigned char smem[];
     const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
     const uint32_t base = smem_addr(smem), pad = ((base + 1023u) & ~1023u) - base;
@@ -200,6 +219,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else {  // ------------------------------------------------------- epilogue
         const uint32_t quarter = warp & 3u;  // the TMEM lanes this warp may read
         const uint32_t lane_base = (quarter * 32) << 16;
+        float *coltile = (float *)(smem + pad + kStages * (kStageA + kStageW) + 8 * kNumBars + 16) + quarter * kColTileFloats;
         uint32_t lt = 0;
         for (uint32_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++lt) {
             const uint32_t b = lt & 1u;
@@ -215,6 +235,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             __nv_bfloat16 *crow = C + (uint64_t)row * N + (uint64_t)tile_n * kBN;
             const uint32_t acc = tmem + lane_base + b * kAccCols;
             float s = 0.0f, c = 0.0f;
+            // column partials of this warp's 32 rows: [4 tile_m + quarter][N]
+            double *cpart = colsum_part + ((uint64_t)tm * 4 + quarter) * N + (uint64_t)tile_n * kBN + lane;
             for (uint32_t c0 = 0; c0 < kBN; c0 += 64) {
                 uint32_t r0[32], r1[32];
                 tc_ld32(acc + c0, r0);
@@ -222,6 +244,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 tc_wait_ld();
                 epilogue_chunk(r0, crow + c0, s, c);
                 epilogue_chunk(r1, crow + c0 + 32, s, c);
+                if (kCols) {
+                    cpart[c0] = warp_column_sum(r0, lane, coltile);
+                    cpart[c0 + 32] = warp_column_sum(r1, lane, coltile);
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -239,18 +265,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 }
 
-// Row checksums: the tile partials of each row summed in tile order; thread 0
-// also publishes the GEMM's abort flag.
-__global__ void abft_rowsum_kernel(const double *__restrict__ rowsum_part, uint32_t M, uint32_t n_tiles,
-                                   double *__restrict__ rowsum, const int *__restrict__ err,
-                                   uint32_t *__restrict__ aborted) {
-    const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i == 0) *aborted = *err != 0 ? 1u : 0u;
-    if (i >= M) return;
-    double cs = 0.0;
-#pragma unroll 8
-    for (uint32_t t = 0; t < n_tiles; ++t) cs = __dadd_rn(cs, rowsum_part[(uint64_t)t * M + i]);
-    rowsum[i] = cs;
+// out[j] = sum over p < count of parts[p * n + j] (row checksums from the tile
+// partials, or column checksums from the 32-row partials), in a fixed order:
+// block = 32 outputs (one per lane) x 8 warps; warp w sums the partials
+// p = w, w + 8, ... in turn, then the 8 warp sums are added in warp order.
+// Thread 0 also publishes the GEMM's abort flag when `aborted` is given.
+__global__ void __launch_bounds__(256) abft_sum_parts_kernel(const double *__restrict__ parts, uint32_t n,
+                                                             uint32_t count, double *__restrict__ out,
+                                                             const int *__restrict__ err,
+                                                             uint32_t *__restrict__ aborted) {
+    __shared__ double part[8][32];
+    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+    const uint32_t j = blockIdx.x * 32 + lane;
+    if (aborted && blockIdx.x == 0 && threadIdx.x == 0) *aborted = *err != 0 ? 1u : 0u;
+    double acc = 0.0;
+    if (j < n) {
+#pragma unroll 4
+        for (uint32_t p = warp; p < count; p += 8) acc = __dadd_rn(acc, parts[(uint64_t)p * n + j]);
+    }
+    part[warp][lane] = acc;
+    __syncthreads();
+    if (warp == 0 && j < n) {
+        double t = part[0][lane];
+        for (int w = 1; w < 8; ++w) t = __dadd_rn(t, part[w][lane]);
+        out[j] = t;
+    }
 }
 
 // ---------------------------------------------------------------- the check
@@ -345,17 +384,17 @@ __global__ void __launch_bounds__(256) abft_colsum_final_kernel(const float4 *__
     wcol[k] = make_double2((double)h + (double)l, (double)ha + (double)la);
 }
 
-// Per row: the reference A (W^T 1) and the magnitude |A| (|W|^T 1) as float32
-// pairs, the bound, the residual against the accumulator checksum, and the
-// flag.  One block of kCheckThreads threads per kCheckRows rows: the threads stride over
+// Per row of X (A for the row check, W for the column check): the reference
+// X . split (A (W^T 1), or W (A^T 1)) and the magnitude |X| . split_abs as
+// float32 pairs, the bound over n_sum summed outputs, the residual against the
+// accumulator checksum, and the flag.  One block of kCheckThreads threads per kCheckRows rows: the threads stride over
 // the 8-column vectors (each column pair loaded once for all the rows), then
 // the pairs are merged across lanes (butterfly) and across warps (in order).
-__global__ void __launch_bounds__(kCheckThreads) abft_check_kernel(const __nv_bfloat16 *__restrict__ A, uint32_t M, uint32_t N,
+__global__ void __launch_bounds__(kCheckThreads) abft_check_kernel(const __nv_bfloat16 *__restrict__ A, uint32_t n_sum,
                                                          uint32_t K, const double *__restrict__ rowsum,
                                                          const float4 *__restrict__ wsplit, float tol_scale,
                                                          double *__restrict__ residual, double *__restrict__ bound,
-                                                         uint8_t *__restrict__ flag,
-                                                         sdc_abft_summary *__restrict__ summary) {
+                                                         uint8_t *__restrict__ flag, uint32_t *__restrict__ n_flagged) {
     __shared__ float4 red[kCheckThreads / 32][kCheckRows];
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
     const uint64_t row0 = (uint64_t)blockIdx.x * kCheckRows;  // M is a multiple of 128: all rows exist
@@ -404,13 +443,14 @@ __global__ void __launch_bounds__(kCheckThreads) abft_check_kernel(const __nv_bf
         const double ref = (double)p.x + (double)p.y, mag = (double)p.z + (double)p.w;
         const uint64_t i = row0 + tid;
         const double g = (double)K * 0x1p-22;
-        const double b = (g * (1.0 + g) + (double)(N + K + 64) * 0x1p-44) * mag + 2.0 * (double)K * (double)N * 0x1p-126;
+        const double b =
+            (g * (1.0 + g) + (double)(n_sum + K + 64) * 0x1p-44) * mag + 2.0 * (double)K * (double)n_sum * 0x1p-126;
         const double d = rowsum[i] - ref;
         residual[i] = d;
         bound[i] = b;
         const uint8_t f = fabs(d) <= (double)tol_scale * b ? 0 : 1;  // NaN flags
         flag[i] = f;
-        if (f) atomicAdd(&summary->n_flagged, 1u);
+        if (f) atomicAdd(n_flagged, 1u);
     }
 }
 
@@ -418,17 +458,23 @@ size_t round_up256(size_t x) { return (x + 255) / 256 * 256; }
 
 uint32_t n_slabs_for(uint32_t N) { return N / 128 < kMaxSlabs ? N / 128 : kMaxSlabs; }
 
-// Workspace: tile partials [N/256][M] | wcol [K] | wsplit [K] | slabs [n_slabs][K] | abort word.
+// Workspace: row partials [N/256][M] | column partials [M/32][N] | W's column sums
+// wcol [K] and their pair split wsplit [K] | A's, acol [K] and asplit [K] |
+// slabs [max(n_slabs(N), n_slabs(M))][K] (used for W, then for A) | abort word.
 struct AbftWs {
-    size_t part, wcol, wsplit, slabs, err, total;
+    size_t part, cpart, wcol, wsplit, acol, asplit, slabs, err, total;
 };
 AbftWs abft_ws(uint32_t M, uint32_t N, uint32_t K) {
     AbftWs w;
+    const size_t ns = n_slabs_for(N) > n_slabs_for(M) ? n_slabs_for(N) : n_slabs_for(M);
     w.part = 0;
-    w.wcol = round_up256((size_t)(N / kBN) * M * sizeof(double));
+    w.cpart = round_up256((size_t)(N / kBN) * M * sizeof(double));
+    w.wcol = w.cpart + round_up256((size_t)(M / 32) * N * sizeof(double));
     w.wsplit = w.wcol + round_up256((size_t)K * sizeof(double2));
-    w.slabs = w.wsplit + round_up256((size_t)K * sizeof(float4));
-    w.err = w.slabs + round_up256((size_t)n_slabs_for(N) * K * sizeof(float4));
+    w.acol = w.wsplit + round_up256((size_t)K * sizeof(float4));
+    w.asplit = w.acol + round_up256((size_t)K * sizeof(double2));
+    w.slabs = w.asplit + round_up256((size_t)K * sizeof(float4));
+    w.err = w.slabs + round_up256(ns * K * sizeof(float4));
     w.total = w.err + 256;
     return w;
 }
@@ -461,7 +507,8 @@ static sdc_status abft_args(const void *d_A, const void *d_W, uint32_t M, uint32
 }
 
 sdc_status sdc_abft_gemm(const void *d_A, const void *d_W, void *d_C, uint32_t M, uint32_t N, uint32_t K,
-                         double *d_rowsum, uint32_t *d_aborted, void *d_ws, size_t ws_bytes, sdc_stream_t stream) {
+                         double *d_rowsum, double *d_colsum, uint32_t *d_aborted, void *d_ws, size_t ws_bytes,
+                         sdc_stream_t stream) {
     int dev = -1;
     sdc_status st = abft_args(d_A, d_W, M, N, K, d_ws, ws_bytes, &dev);
     if (st != SDC_OK) return st;
@@ -475,11 +522,14 @@ sdc_status sdc_abft_gemm(const void *d_A, const void *d_W, void *d_C, uint32_t M
     if (st != SDC_OK) return st;
     const AbftWs w = abft_ws(M, N, K);
     double *part = (double *)((char *)d_ws + w.part);
+    double *cpart = (double *)((char *)d_ws + w.cpart);
     int *err = (int *)((char *)d_ws + w.err);
     cudaStream_t s = (cudaStream_t)stream;
+    const bool cols = d_colsum != nullptr;
+    auto kernel = cols ? abft_gemm_kernel<true> : abft_gemm_kernel<false>;
     cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int), s);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(abft_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
+    const uint32_t smem_bytes = cols ? kGemmSmemCols : kGemmSmem;
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_gemm setup");
     const uint32_t n_tiles = (M / kBM) * (N / kBN);
     const uint32_t sms = (uint32_t)sm_count(dev);
@@ -487,34 +537,47 @@ sdc_status sdc_abft_gemm(const void *d_A, const void *d_W, void *d_C, uint32_t M
     // A band of tile rows holds about 24 MiB of A, a fraction of the 126 MiB L2.
     uint32_t band_m = (uint32_t)((24u << 20) / ((size_t)kBM * K * 2));
     band_m = band_m < 1 ? 1 : (band_m > M / kBM ? M / kBM : band_m);
-    abft_gemm_kernel<<<grid, kGemmThreads, kGemmSmem, s>>>(mapA, mapW, (__nv_bfloat16 *)d_C, M, N, K, band_m, part,
-                                                           err);
-    abft_rowsum_kernel<<<(M + 63) / 64, 64, 0, s>>>(part, M, N / kBN, d_rowsum, err, d_aborted);
+    kernel<<<grid, kGemmThreads, smem_bytes, s>>>(mapA, mapW, (__nv_bfloat16 *)d_C, M, N, K, band_m, part, cpart, err);
+    abft_sum_parts_kernel<<<(M + 31) / 32, 256, 0, s>>>(part, M, N / kBN, d_rowsum, err, d_aborted);
+    if (cols) abft_sum_parts_kernel<<<(N + 31) / 32, 256, 0, s>>>(cpart, N, M / 32, d_colsum, nullptr, nullptr);
     e = cudaGetLastError();
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_abft_gemm launch");
 }
 
 sdc_status sdc_abft_verify(const void *d_A, const void *d_W, uint32_t M, uint32_t N, uint32_t K, const double *d_rowsum,
-                           float tol_scale, double *d_residual, double *d_bound, uint8_t *d_flag,
+                           const double *d_colsum, float tol_scale, double *d_residual, double *d_bound,
+                           uint8_t *d_flag, double *d_residual_col, double *d_bound_col, uint8_t *d_flag_col,
                            sdc_abft_summary *d_summary, void *d_ws, size_t ws_bytes, sdc_stream_t stream) {
     int dev = -1;
     sdc_status st = abft_args(d_A, d_W, M, N, K, d_ws, ws_bytes, &dev);
     if (st != SDC_OK) return st;
     if (!d_rowsum || !d_residual || !d_bound || !d_flag || !d_summary) return fail(SDC_ERR_NULL, "NULL output");
+    const bool cols = d_colsum != nullptr;
+    if (cols && (!d_residual_col || !d_bound_col || !d_flag_col)) return fail(SDC_ERR_NULL, "NULL column output");
     if (!(tol_scale > 0.0f)) return fail(SDC_ERR_BAD_ARG, "tol_scale must be positive");
     const AbftWs w = abft_ws(M, N, K);
-    double2 *wcol = (double2 *)((char *)d_ws + w.wcol);
-    float4 *wsplit = (float4 *)((char *)d_ws + w.wsplit);
+    double2 *wcol = (double2 *)((char *)d_ws + w.wcol), *acol = (double2 *)((char *)d_ws + w.acol);
+    float4 *wsplit = (float4 *)((char *)d_ws + w.wsplit), *asplit = (float4 *)((char *)d_ws + w.asplit);
     float4 *slabs = (float4 *)((char *)d_ws + w.slabs);
-    const uint32_t n_slabs = n_slabs_for(N);
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = cudaMemsetAsync(d_summary, 0, sizeof(sdc_abft_summary), s);
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_verify setup");
-    abft_colsum_slab_kernel<<<dim3((K + 255) / 256, n_slabs), 256, 0, s>>>((const __nv_bfloat16 *)d_W, N, K, n_slabs,
-                                                                           slabs);
-    abft_colsum_final_kernel<<<(K + 31) / 32, 256, 0, s>>>(slabs, K, n_slabs, wcol, wsplit);
-    abft_check_kernel<<<M / kCheckRows, kCheckThreads, 0, s>>>(
-        (const __nv_bfloat16 *)d_A, M, N, K, d_rowsum, wsplit, tol_scale, d_residual, d_bound, d_flag, d_summary);
+    // rows: A (W^T 1) over the N columns each row checksum sums
+    const uint32_t nsw = n_slabs_for(N);
+    abft_colsum_slab_kernel<<<dim3((K + 255) / 256, nsw), 256, 0, s>>>((const __nv_bfloat16 *)d_W, N, K, nsw, slabs);
+    abft_colsum_final_kernel<<<(K + 31) / 32, 256, 0, s>>>(slabs, K, nsw, wcol, wsplit);
+    abft_check_kernel<<<M / kCheckRows, kCheckThreads, 0, s>>>((const __nv_bfloat16 *)d_A, N, K, d_rowsum, wsplit,
+                                                               tol_scale, d_residual, d_bound, d_flag,
+                                                               &d_summary->n_flagged);
+    if (cols) {  // columns: W (A^T 1) over the M rows each column checksum sums
+        const uint32_t nsa = n_slabs_for(M);
+        abft_colsum_slab_kernel<<<dim3((K + 255) / 256, nsa), 256, 0, s>>>((const __nv_bfloat16 *)d_A, M, K, nsa,
+                                                                          slabs);
+        abft_colsum_final_kernel<<<(K + 31) / 32, 256, 0, s>>>(slabs, K, nsa, acol, asplit);
+        abft_check_kernel<<<N / kCheckRows, kCheckThreads, 0, s>>>((const __nv_bfloat16 *)d_W, M, K, d_colsum, asplit,
+                                                                   tol_scale, d_residual_col, d_bound_col, d_flag_col,
+                                                                   &d_summary->n_flagged_cols);
+    }
     e = cudaGetLastError();
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_abft_verify launch");
 }

@@ -99,19 +99,20 @@ def test_host_validation_without_gpu(sdc):
     sdc.sdc_xorsum_compare(0, 0, 0, 0, 0, 0)  # n == 0 is a no-op
     # GEMM checksum: operands checked, then shapes, before any CUDA call
     with pytest.raises(sdc.SdcError) as ei:
-        sdc.sdc_abft_gemm(0, 4096, 8192, 128, 256, 64, 0, 0, 0, 0, 0)
+        sdc.sdc_abft_gemm(0, 4096, 8192, 128, 256, 64, 0, 0, 0, 0, 0, 0)
     assert ei.value.status == 1
     for M, N, K in [(100, 256, 64), (128, 200, 64), (128, 256, 48), (0, 256, 64), (128, 256, 1 << 21)]:
         with pytest.raises(sdc.SdcError) as ei:
-            sdc.sdc_abft_gemm(4096, 8192, 16384, M, N, K, 0, 0, 0, 0, 0)
+            sdc.sdc_abft_gemm(4096, 8192, 16384, M, N, K, 0, 0, 0, 0, 0, 0)
         assert ei.value.status == 9, (M, N, K)
         with pytest.raises(sdc.SdcError) as ei:
-            sdc.sdc_abft_verify(4096, 8192, M, N, K, 0, 1.0, 0, 0, 0, 0, 0, 0, 0)
+            sdc.sdc_abft_verify(4096, 8192, M, N, K, 0, 0, 1.0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0)
         assert ei.value.status == 9, (M, N, K)
-    # tile partials (N/256 per row), K column-sum pairs (float64), K split pairs (float32),
-    # min(64, N/128) slabs of K float64 pairs, the abort word; each rounded up to 256 bytes
-    assert sdc.sdc_abft_workspace_size(128, 512, 64) == 2048 + 1024 + 1024 + 4 * 64 * 16 + 256
-    assert sdc.sdc_abft_workspace_size(1000, 256, 100) == 8192 + 1792 + 1792 + 3328 + 256
+    # row partials (N/256 per row), column partials (M/32 per column), W's and A's column sums
+    # (K float64 pairs) and their float32 pair splits (K x 16 bytes), max(min(64, N/128),
+    # min(64, M/128)) slabs of K x 16 bytes, the abort word; each rounded up to 256 bytes
+    assert sdc.sdc_abft_workspace_size(128, 512, 64) == 2048 + 4 * 512 * 8 + 4 * 1024 + 4 * 64 * 16 + 256
+    assert sdc.sdc_abft_workspace_size(1000, 256, 100) == 8192 + 31 * 256 * 8 + 4 * 1792 + 11264 + 256
     # attention invariant: inputs checked, then shapes and scalars, before any CUDA call
     fake = [4096, 8192, 12288, 16384]
     outs = [20480 + 4096 * i for i in range(8)]
@@ -124,10 +125,13 @@ def test_host_validation_without_gpu(sdc):
         with pytest.raises(sdc.SdcError) as ei:
             sdc.sdc_attn_dv_check(*fake, BH, L, D, scale, causal, tol, *outs, 0, 0, 0)
         assert ei.value.status == 9, (BH, L, D, scale, causal, tol)
-    # dO^T, dO partials (float4 per block and column), dV partials (float2), the abort word
-    assert sdc.sdc_attn_workspace_size(2, 256, 128) == 2 * 128 * 256 * 2 + 2 * 2 * 128 * 16 + 2 * 2 * 128 * 8 + 256
+    # dO^T, dO partials (float4 per block and column), dV partials (float2), lse log2(e)
+    # (a float per token), the abort word
+    assert sdc.sdc_attn_workspace_size(2, 256, 128) == (2 * 128 * 256 * 2 + 2 * 2 * 128 * 16 + 2 * 2 * 128 * 8
+                                                        + 2 * 256 * 4 + 256)
     assert sdc.sdc_attn_workspace_size(2, 256, 64) == 0
-    assert sdc.sdc_abft_workspace_size(128, 16384, 64) == 64 * 128 * 8 + 1024 + 1024 + 64 * 64 * 16 + 256
+    assert sdc.sdc_abft_workspace_size(128, 16384, 64) == (64 * 128 * 8 + 4 * 16384 * 8 + 4 * 1024 + 64 * 64 * 16
+                                                           + 256)
 
 
 def test_pages_verdict_decoding(sdc):
