@@ -71,7 +71,7 @@ constexpr uint32_t kColTileFloats = 32 * 33;  // one epilogue warp's column-sum 
 constexpr uint32_t kGemmSmemCols = kGemmSmem + 4 * kColTileFloats * 4;
 constexpr uint32_t kMaxK = 1u << 20;
 constexpr uint32_t kMaxSlabs = 64;
-constexpr uint32_t kCheckRows = 4;     // rows per block of the check
+constexpr uint32_t kCheckRows = 8;     // rows per block of the check
 constexpr uint32_t kCheckThreads = 64;  // threads per block of the check
 
 // Converts 32 accumulators to bf16 (round to nearest even), stores them at
@@ -306,23 +306,27 @@ __global__ void __launch_bounds__(256) abft_colsum_slab_kernel(const __nv_bfloat
     const uint32_t k = blockIdx.x * 256 + lane * 8;
     const uint32_t j0 = (uint32_t)((uint64_t)blockIdx.y * N / n_slabs),
                    j1 = (uint32_t)((uint64_t)(blockIdx.y + 1) * N / n_slabs);
-    float s[8], c[8], sa[8], ca[8];
+    // columns 2q and 2q + 1 of the lane's 8 share packed registers
+    uint64_t s[4], c[4], sa[4], ca[4];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) s[q] = c[q] = sa[q] = ca[q] = 0.0f;
+    for (int q = 0; q < 4; ++q) s[q] = c[q] = sa[q] = ca[q] = 0ull;
     auto add_row = [&](const uint4 v) {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const float x0 = bf16_lo(w[q]), x1 = bf16_hi(w[q]);
-            pair_add(s[2 * q], c[2 * q], x0);
-            pair_add(s[2 * q + 1], c[2 * q + 1], x1);
-            pair_add(sa[2 * q], ca[2 * q], fabsf(x0));
-            pair_add(sa[2 * q + 1], ca[2 * q + 1], fabsf(x1));
+            const uint64_t x = f2_pack_bits(w[q] << 16, w[q] & 0xFFFF0000u);
+            pair2_add(s[q], c[q], x);
+            pair2_add(sa[q], ca[q], x & kF2Abs);
         }
     };
     if (k < K) {
         uint32_t j = j0 + warp;
         for (; j + 24 < j1; j += 32) {  // four rows in flight per lane, added in row order
+            if ((lane & 7u) == 0) {  // the next four rows into L2: lanes 0, 8, 16, 24 touch the warp's 4 lines
+#pragma unroll
+                for (uint32_t d = 32; d < 64; d += 8)
+                    if (j + d < j1) prefetch_l2(W + (uint64_t)(j + d) * K + k);
+            }
             const uint4 v0 = ld_stream(W + (uint64_t)j * K + k), v1 = ld_stream(W + (uint64_t)(j + 8) * K + k),
                         v2 = ld_stream(W + (uint64_t)(j + 16) * K + k), v3 = ld_stream(W + (uint64_t)(j + 24) * K + k);
             add_row(v0);
@@ -333,7 +337,15 @@ __global__ void __launch_bounds__(256) abft_colsum_slab_kernel(const __nv_bfloat
         for (; j < j1; j += 8) add_row(ld_stream(W + (uint64_t)j * K + k));
     }
 #pragma unroll
-    for (int q = 0; q < 8; ++q) part[warp][lane * 8 + q] = make_float4(s[q], c[q], sa[q], ca[q]);
+    for (int q = 0; q < 4; ++q) {
+        float s0, s1, c0, c1, a0, a1, e0, e1;
+        f2_unpack(s[q], s0, s1);
+        f2_unpack(c[q], c0, c1);
+        f2_unpack(sa[q], a0, a1);
+        f2_unpack(ca[q], e0, e1);
+        part[warp][lane * 8 + 2 * q] = make_float4(s0, c0, a0, e0);
+        part[warp][lane * 8 + 2 * q + 1] = make_float4(s1, c1, a1, e1);
+    }
     __syncthreads();
     const uint32_t kk = blockIdx.x * 256 + threadIdx.x;
     if (kk < K) {
@@ -398,28 +410,40 @@ __global__ void __launch_bounds__(kCheckThreads) abft_check_kernel(const __nv_bf
     __shared__ float4 red[kCheckThreads / 32][kCheckRows];
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
     const uint64_t row0 = (uint64_t)blockIdx.x * kCheckRows;  // M is a multiple of 128: all rows exist
-    float rs[kCheckRows], rc[kCheckRows], ms[kCheckRows], mc[kCheckRows];
+    // rows (0, 1) and (2, 3) share packed registers
+    uint64_t rs2[kCheckRows / 2], rc2[kCheckRows / 2], ms2[kCheckRows / 2], mc2[kCheckRows / 2];
 #pragma unroll
-    for (uint32_t r = 0; r < kCheckRows; ++r) rs[r] = rc[r] = ms[r] = mc[r] = 0.0f;
+    for (uint32_t r = 0; r < kCheckRows / 2; ++r) rs2[r] = rc2[r] = ms2[r] = mc2[r] = 0ull;
     for (uint32_t v = tid; v < K / 8; v += kCheckThreads) {
-        float4 w[8];
+        if ((lane & 7u) == 0 && v + kCheckThreads < K / 8) {  // the next vectors of every row into L2
 #pragma unroll
-        for (int q = 0; q < 8; ++q) w[q] = wsplit[v * 8 + q];
+            for (uint32_t r = 0; r < kCheckRows; ++r) prefetch_l2(A + (row0 + r) * K + (uint64_t)(v + kCheckThreads) * 8);
+        }
         uint4 av[kCheckRows];
 #pragma unroll
         for (uint32_t r = 0; r < kCheckRows; ++r) av[r] = ld_stream(A + (row0 + r) * K + (uint64_t)v * 8);
 #pragma unroll
-        for (uint32_t r = 0; r < kCheckRows; ++r) {
-            const uint32_t a4[4] = {av[r].x, av[r].y, av[r].z, av[r].w};
+        for (int q = 0; q < 8; ++q) {  // column 8 v + q
+            const float4 w = wsplit[v * 8 + q];
+            const uint64_t h2 = f2_pack(w.x, w.x), l2 = f2_pack(w.y, w.y);
+            const uint64_t ha2 = f2_pack(w.z, w.z), la2 = f2_pack(w.w, w.w);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float a0 = bf16_lo(a4[q]), a1 = bf16_hi(a4[q]);
-                pair_fma(rs[r], rc[r], a0, w[2 * q].x, w[2 * q].y);
-                pair_fma(rs[r], rc[r], a1, w[2 * q + 1].x, w[2 * q + 1].y);
-                pair_fma(ms[r], mc[r], fabsf(a0), w[2 * q].z, w[2 * q].w);
-                pair_fma(ms[r], mc[r], fabsf(a1), w[2 * q + 1].z, w[2 * q + 1].w);
+            for (uint32_t rp = 0; rp < kCheckRows / 2; ++rp) {
+                const uint32_t w0 = (&av[2 * rp].x)[q >> 1], w1 = (&av[2 * rp + 1].x)[q >> 1];
+                const uint64_t a2 = (q & 1) ? f2_pack_bits(w0 & 0xFFFF0000u, w1 & 0xFFFF0000u)
+                                            : f2_pack_bits(w0 << 16, w1 << 16);
+                pair2_fma(rs2[rp], rc2[rp], a2, h2, l2);
+                pair2_fma(ms2[rp], mc2[rp], a2 & kF2Abs, ha2, la2);
             }
         }
+    }
+    float rs[kCheckRows], rc[kCheckRows], ms[kCheckRows], mc[kCheckRows];
+#pragma unroll
+    for (uint32_t rp = 0; rp < kCheckRows / 2; ++rp) {
+        f2_unpack(rs2[rp], rs[2 * rp], rs[2 * rp + 1]);
+        f2_unpack(rc2[rp], rc[2 * rp], rc[2 * rp + 1]);
+        f2_unpack(ms2[rp], ms[2 * rp], ms[2 * rp + 1]);
+        f2_unpack(mc2[rp], mc[2 * rp], mc[2 * rp + 1]);
     }
 #pragma unroll
     for (uint32_t r = 0; r < kCheckRows; ++r) {
@@ -456,17 +480,26 @@ __global__ void __launch_bounds__(kCheckThreads) abft_check_kernel(const __nv_bf
 
 size_t round_up256(size_t x) { return (x + 255) / 256 * 256; }
 
-uint32_t n_slabs_for(uint32_t N) { return N / 128 < kMaxSlabs ? N / 128 : kMaxSlabs; }
+// Row slabs of a column sum over `rows` rows of K columns: about 608 blocks in all
+// (4 resident blocks on each of 152 SMs: one wave), at most kMaxSlabs, at least
+// 8 rows per slab.  A function of the shapes only, so the workspace size is too.
+uint32_t n_slabs_for(uint32_t rows, uint32_t K) {
+    const uint32_t col_blocks = (K + 255) / 256;
+    uint32_t n = 608 / col_blocks;
+    if (n > kMaxSlabs) n = kMaxSlabs;
+    if (n > rows / 8) n = rows / 8;
+    return n < 1 ? 1 : n;
+}
 
 // Workspace: row partials [N/256][M] | column partials [M/32][N] | W's column sums
 // wcol [K] and their pair split wsplit [K] | A's, acol [K] and asplit [K] |
-// slabs [max(n_slabs(N), n_slabs(M))][K] (used for W, then for A) | abort word.
+// slabs [max(n_slabs(N, K), n_slabs(M, K))][K] (used for W, then for A) | abort word.
 struct AbftWs {
     size_t part, cpart, wcol, wsplit, acol, asplit, slabs, err, total;
 };
 AbftWs abft_ws(uint32_t M, uint32_t N, uint32_t K) {
     AbftWs w;
-    const size_t ns = n_slabs_for(N) > n_slabs_for(M) ? n_slabs_for(N) : n_slabs_for(M);
+    const size_t ns = n_slabs_for(N, K) > n_slabs_for(M, K) ? n_slabs_for(N, K) : n_slabs_for(M, K);
     w.part = 0;
     w.cpart = round_up256((size_t)(N / kBN) * M * sizeof(double));
     w.wcol = w.cpart + round_up256((size_t)(M / 32) * N * sizeof(double));
@@ -563,14 +596,14 @@ sdc_status sdc_abft_verify(const void *d_A, const void *d_W, uint32_t M, uint32_
     cudaError_t e = cudaMemsetAsync(d_summary, 0, sizeof(sdc_abft_summary), s);
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_verify setup");
     // rows: A (W^T 1) over the N columns each row checksum sums
-    const uint32_t nsw = n_slabs_for(N);
+    const uint32_t nsw = n_slabs_for(N, K);
     abft_colsum_slab_kernel<<<dim3((K + 255) / 256, nsw), 256, 0, s>>>((const __nv_bfloat16 *)d_W, N, K, nsw, slabs);
     abft_colsum_final_kernel<<<(K + 31) / 32, 256, 0, s>>>(slabs, K, nsw, wcol, wsplit);
     abft_check_kernel<<<M / kCheckRows, kCheckThreads, 0, s>>>((const __nv_bfloat16 *)d_A, N, K, d_rowsum, wsplit,
                                                                tol_scale, d_residual, d_bound, d_flag,
                                                                &d_summary->n_flagged);
     if (cols) {  // columns: W (A^T 1) over the M rows each column checksum sums
-        const uint32_t nsa = n_slabs_for(M);
+        const uint32_t nsa = n_slabs_for(M, K);
         abft_colsum_slab_kernel<<<dim3((K + 255) / 256, nsa), 256, 0, s>>>((const __nv_bfloat16 *)d_A, M, K, nsa,
                                                                           slabs);
         abft_colsum_final_kernel<<<(K + 31) / 32, 256, 0, s>>>(slabs, K, nsa, acol, asplit);

@@ -146,6 +146,23 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Two float32 pairs at once, one in each half of packed f32x2 registers: the
+// same TwoSum and product splitting as pair_add / pair_fma.
+constexpr uint64_t kF2Sign = 0x8000000080000000ull, kF2Abs = 0x7FFFFFFF7FFFFFFFull;
+__device__ __forceinline__ void pair2_add(uint64_t &s, uint64_t &c, uint64_t x) {
+    const uint64_t t = f2_add(s, x);
+    const uint64_t bp = f2_sub(t, s);
+    const uint64_t e = f2_add(f2_sub(s, f2_sub(t, bp)), f2_sub(x, bp));
+    s = t;
+    c = f2_add(c, e);
+}
+__device__ __forceinline__ void pair2_fma(uint64_t &s, uint64_t &c, uint64_t a, uint64_t h, uint64_t l) {
+    const uint64_t p = f2_mul(a, h);
+    const uint64_t e = f2_fma(a, h, p ^ kF2Sign);  // a h - fl(a h), exact
+    pair2_add(s, c, p);
+    c = f2_fma(a, l, f2_add(c, e));
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

@@ -109,10 +109,11 @@ def test_host_validation_without_gpu(sdc):
             sdc.sdc_abft_verify(4096, 8192, M, N, K, 0, 0, 1.0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0)
         assert ei.value.status == 9, (M, N, K)
     # row partials (N/256 per row), column partials (M/32 per column), W's and A's column sums
-    # (K float64 pairs) and their float32 pair splits (K x 16 bytes), max(min(64, N/128),
-    # min(64, M/128)) slabs of K x 16 bytes, the abort word; each rounded up to 256 bytes
-    assert sdc.sdc_abft_workspace_size(128, 512, 64) == 2048 + 4 * 512 * 8 + 4 * 1024 + 4 * 64 * 16 + 256
-    assert sdc.sdc_abft_workspace_size(1000, 256, 100) == 8192 + 31 * 256 * 8 + 4 * 1792 + 11264 + 256
+    # (K float64 pairs) and their float32 pair splits (K x 16 bytes), slabs of K x 16 bytes for the
+    # larger of the two column sums (slabs = min(608 / ceil(K / 256), 64, rows / 8)), the abort
+    # word; each rounded up to 256 bytes
+    assert sdc.sdc_abft_workspace_size(128, 512, 64) == 2048 + 4 * 512 * 8 + 4 * 1024 + 64 * 64 * 16 + 256
+    assert sdc.sdc_abft_workspace_size(1000, 256, 100) == 8192 + 31 * 256 * 8 + 4 * 1792 + 64 * 100 * 16 + 256
     # attention invariant: inputs checked, then shapes and scalars, before any CUDA call
     fake = [4096, 8192, 12288, 16384]
     outs = [20480 + 4096 * i for i in range(8)]
