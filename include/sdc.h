@@ -341,6 +341,18 @@ sdc_status sdc_attn_dv_check(const void *d_Q, const void *d_K, const void *d_dO,
                              uint8_t *d_flag, sdc_abft_summary *d_summary, uint32_t *d_aborted, void *d_ws,
                              size_t ws_bytes, sdc_stream_t stream);
 
+/* ---------------------------------------------------------------- self-test */
+
+/* Self-test of the bounded barrier wait with which the TMA / tensor-core
+ * kernels (sdc_abft_gemm, sdc_attn_dv_check) turn a stall into an abort flag
+ * instead of a hang.  No page counterpart: it tests this library's own
+ * failure handling.  One thread waits up to `polls` polls (1 .. 2^24) on a
+ * shared-memory barrier phase that nothing completes, then completes it itself
+ * and waits again.  *d_status (device uint32) = bit 0: the first wait gave up;
+ * bit 1: the second wait succeeded; 3 is the correct outcome.  The kernel ends
+ * in every case. */
+sdc_status sdc_selftest_bounded_wait(uint32_t polls, uint32_t *d_status, sdc_stream_t stream);
+
 /* ---------------------------------------------------------------- ring replay audit */
 
 /* Counts written by sdc_ring_audit. */

@@ -101,6 +101,7 @@ def _load() -> ctypes.CDLL:
         "sdc_attn_workspace_size": ([u32, u32, u32], sz),
         "sdc_attn_dv_check": ([vp, vp, vp, vp, u32, u32, u32, ctypes.c_float, u32, ctypes.c_float, vp, vp, vp, vp,
                                vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
+        "sdc_selftest_bounded_wait": ([u32, vp, vp], ctypes.c_int),
         "sdc_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "sdc_last_error": ([], ctypes.c_char_p),
     }
@@ -273,6 +274,10 @@ def sdc_attn_dv_check(d_Q: int, d_K: int, d_dO: int, d_lse: int, BH: int, L: int
     _check("sdc_attn_dv_check", _lib.sdc_attn_dv_check(d_Q, d_K, d_dO, d_lse, BH, L, D, scale, causal, tol_scale,
                                                        d_dV, d_colsum_dv, d_colsum_do, d_residual, d_bound, d_flag,
                                                        d_summary, d_aborted, d_ws, ws_bytes, stream))
+
+
+def sdc_selftest_bounded_wait(polls: int, d_status: int, stream: int) -> None:
+    _check("sdc_selftest_bounded_wait", _lib.sdc_selftest_bounded_wait(polls, d_status, stream))
 
 
 # ---------------------------------------------------------------- torch conveniences

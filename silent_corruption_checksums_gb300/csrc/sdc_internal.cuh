@@ -250,7 +250,11 @@ __device__ __forceinline__ uint32_t warp_sum_u32(uint32_t v) {
 // Shared-memory barriers that TMA copies and tcgen05.commit signal.  Every
 // wait is bounded: after kSpinLimit polls the caller records an error and
 // stops, so no kernel can hang on a barrier.
-constexpr uint32_t kSpinLimit = 1u << 22;
+// A poll that finds the phase incomplete suspends the thread for ~3.76 us on
+// GB300 (measured with sdc_selftest_bounded_wait), so 2^18 polls give up after
+// about one second: far longer than any wait of these kernels (at most one
+// tile's main loop, milliseconds), short enough to end a stall promptly.
+constexpr uint32_t kSpinLimit = 1u << 18;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 __device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count) {
@@ -269,9 +273,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t mbar, uint32_t parity) {
         : "memory");
     return done != 0;
 }
-// Bounded wait for the completion of phase `parity` of a barrier.
-__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
-    for (uint32_t i = 0; i < kSpinLimit; ++i)
+// Bounded wait for the completion of phase `parity` of a barrier: at most
+// `limit` polls (kSpinLimit unless given); false when it gave up.
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, uint32_t limit = kSpinLimit) {
+    for (uint32_t i = 0; i < limit; ++i)
         if (mbar_try_wait(mbar, parity)) return true;
     return false;
 }

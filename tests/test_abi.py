@@ -114,6 +114,14 @@ def test_host_validation_without_gpu(sdc):
     # word; each rounded up to 256 bytes
     assert sdc.sdc_abft_workspace_size(128, 512, 64) == 2048 + 4 * 512 * 8 + 4 * 1024 + 64 * 64 * 16 + 256
     assert sdc.sdc_abft_workspace_size(1000, 256, 100) == 8192 + 31 * 256 * 8 + 4 * 1792 + 64 * 100 * 16 + 256
+    # bounded-wait self-test: arguments checked before the launch
+    with pytest.raises(sdc.SdcError) as ei:
+        sdc.sdc_selftest_bounded_wait(10, 0, 0)
+    assert ei.value.status == 1
+    for polls in (0, 1 << 25):
+        with pytest.raises(sdc.SdcError) as ei:
+            sdc.sdc_selftest_bounded_wait(polls, 4096, 0)
+        assert ei.value.status == 9
     # attention invariant: inputs checked, then shapes and scalars, before any CUDA call
     fake = [4096, 8192, 12288, 16384]
     outs = [20480 + 4096 * i for i in range(8)]
