@@ -499,13 +499,18 @@ def bench_big_rows(args, dev, stream, peaks, sdc, W, torch, only) -> dict:
     """Fingerprint rows on the 8b and stress workloads (tens of GB each)."""
     rows = {}
     if only in (None, "fingerprint_8b"):
+        L8, R8 = getattr(args, "layers_8b", 32), getattr(args, "replicas_8b", 8)
+        w8 = W.weights_8b(dev, seed=4, n_replicas=R8, n_layers=L8)
         rows["fingerprint_8b"] = bench_fp_row(
-            W.weights_8b(dev, seed=4)["replicas"], "8b bf16 layout (T=291), 8 replicas, 16-element perturbation",
-            args, stream, peaks, sdc, torch)
+            w8["replicas"], f"8b bf16 layout (T={len(w8['layout'])}, {L8} layers), {R8} replicas, 16-element "
+            "perturbation", args, stream, peaks, sdc, torch)
+        del w8
+        torch.cuda.empty_cache()
     if only in (None, "fingerprint_stress"):
-        w = W.stress(dev, seed=5)
+        nt = getattr(args, "stress_tensors", 100_000)
+        w = W.stress(dev, seed=5, n_tensors=nt)
         rows["fingerprint_stress"] = bench_fp_row(
-            w["replicas"], "100,000 tensors (1..1e6 elements, fp32/bf16/fp16, element-aligned packing), 3 replicas",
+            w["replicas"], f"{nt:,} tensors (1..1e6 elements, fp32/bf16/fp16, element-aligned packing), 3 replicas",
             args, stream, peaks, sdc, torch)
         p = w["pairs"]
         xplan = sdc.Plan([p["orig"], p["recomp"]])
@@ -653,6 +658,11 @@ def main(argv=None) -> None:
                                        "fingerprint_8b",
                                        "fingerprint_stress", "adamw_fingerprint"], default=None,
                     help="time one row alone (profiling)")
+    ap.add_argument("--layers-8b", type=int, default=32,
+                    help="decoder layers of the 8b layout (32 = the benchmark workload; fewer for profiling)")
+    ap.add_argument("--replicas-8b", type=int, default=8, help="replicas of the 8b row (8; fewer for profiling)")
+    ap.add_argument("--stress-tensors", type=int, default=100_000,
+                    help="tensors of the stress row (100,000; fewer for profiling)")
     ap.add_argument("--layers", type=int, default=24,
                     help="decoder layers of the 1b layout (24 = the benchmark workload; fewer for profiling)")
     ap.add_argument("--traffic", type=float, default=None,

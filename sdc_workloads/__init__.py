@@ -53,8 +53,8 @@ def layout_1b(layers: int = 24) -> list[tuple[str, tuple[int, ...]]]:
     return out
 
 
-def layout_8b() -> list[tuple[str, tuple[int, ...]]]:
-    d, kv, ffn, vocab, layers = 4096, 1024, 14336, 128256, 32
+def layout_8b(layers: int = 32) -> list[tuple[str, tuple[int, ...]]]:
+    d, kv, ffn, vocab = 4096, 1024, 14336, 128256
     out = [("embed", (vocab, d))]
     for i in range(layers):
         out += [(f"l{i}.q", (d, d)), (f"l{i}.k", (kv, d)), (f"l{i}.v", (kv, d)), (f"l{i}.o", (d, d)),
@@ -175,8 +175,8 @@ def grads_1b(device, seed: int = 3) -> dict:
     return grads_flat(layout_numel(layout_1b()), 4, torch.bfloat16, 1e-3, device, seed)
 
 
-def weights_8b(device, seed: int = 4, n_replicas: int = 8) -> dict:
-    layout = layout_8b()
+def weights_8b(device, seed: int = 4, n_replicas: int = 8, n_layers: int = 32) -> dict:
+    layout = layout_8b(n_layers)
     reps = weights(layout, n_replicas, torch.bfloat16, 0.02, device, seed)
     rng = np.random.default_rng(seed)
     r = int(rng.integers(n_replicas))
