@@ -632,16 +632,23 @@ class E2E:
 
 
 def bench_cpu(reps, torch) -> dict:
-    """The oracle on a bounded sample: the first ~2 GB of replica 0, all host cores."""
-    sample, nbytes = [], 0
-    for t in reps[0]:
-        sample.append(t.to("cpu"))
-        nbytes += t.numel() * t.element_size()
-        if nbytes >= 2 << 30:
-            break
+    """The oracle on the whole step's bytes (all replicas, all host cores: about 20
+    core-seconds), plus a single-threaded figure on the first ~1 GB of replica 0."""
+    host = [[t.to("cpu") for t in ts] for ts in reps]
+    nbytes = sum(t.numel() * t.element_size() for ts in host for t in ts)
     threads = os.cpu_count() or 1
-    r = cpu_baseline_sample(sample, threads)
-    r["sample"] = f"{len(sample)} tensors of replica 0, {nbytes} bytes (of 12,475,438,080 per step)"
+    r = cpu_baseline_sample([t for ts in host for t in ts], threads)
+    r["sample"] = f"the whole step: {len(host)} replicas x {len(host[0])} tensors, {nbytes} bytes"
+    one, nb1 = [], 0
+    for t in host[0]:
+        one.append(t)
+        nb1 += t.numel() * t.element_size()
+        if nb1 >= 1 << 30:
+            break
+    st = cpu_baseline_sample(one, 1)
+    r["single_thread"] = {"value": st["value"], "unit": "GB/s", "cores": 1, "seconds": st["seconds"],
+                          "sample": f"{len(one)} tensors of replica 0, {nb1} bytes"}
+    del host
     return r
 
 
