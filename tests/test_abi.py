@@ -154,3 +154,17 @@ def test_pages_verdict_decoding(sdc):
     raw["diverged"] = 1
     raw["suspect_mask"] = 1 << 63
     assert sdc.decode_summary(raw.view(np.uint8))["suspect_mask"] == 1 << 63
+
+
+def test_binding_signatures_match_header(sdc):
+    # every entry point of include/sdc.h has a ctypes signature of the same arity
+    import silent_corruption_checksums_gb300 as m
+    hdr = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    decls = re.findall(r"\n(?:sdc_status|size_t|const char \*|void)\s+\*?(sdc_\w+)\s*\(([^;]*?)\);", hdr)
+    assert len(decls) >= 20
+    lib = m._load()
+    for name, args in decls:
+        n_c = 0 if args.strip() in ("", "void") else args.count(",") + 1
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None, name
+        assert len(fn.argtypes) == n_c, (name, n_c, len(fn.argtypes))
