@@ -153,3 +153,60 @@ def test_stress_many_small_tensors_sampled(sdc):
     dnp = diff.cpu().numpy().view(np.uint64)
     for i, e, b in p["differ"]:
         assert int(dnp[i]) == 1 << b
+
+
+def _bf16_bits(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def test_gemm_checksum_bench_shape(sdc):
+    # the benchmark's GEMM (8b MLP up-projection, 8192 x 14336 x 4096, rows + columns, the same
+    # seed) in its launch configuration; sampled rows and columns against the oracle one by one
+    M, N, K = W.GEMM_8B_UP
+    ops = W.gemm_operands(M, N, K, DEV, seed=6)
+    g = sdc.AbftGemm(M, N, K, DEV, columns=True)
+    g(ops["A"], ops["W"])
+    torch.cuda.synchronize()
+    assert int(g.aborted[0]) == 0
+    assert int(g.summary[0]) == 0 and int(g.summary[1]) == 0  # no clean row or column flagged
+    A64 = oracle.bf16_to_f64(_bf16_bits(ops["A"]))
+    W64 = oracle.bf16_to_f64(_bf16_bits(ops["W"]))
+    rng = np.random.default_rng(61)
+    gk = K * 2.0 ** -22
+    rows = np.sort(rng.choice(M, 12, replace=False))
+    exact = A64[rows] @ W64.T
+    e = gk * (1 + gk) * (np.abs(A64[rows]) @ np.abs(W64).T) + 2.0 * K * 2.0 ** -126
+    C = g.C[torch.as_tensor(rows, device=DEV)].float().cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(C - exact) <= 2.0 ** -8 * (np.abs(exact) + e) + e + 2.0 ** -134)
+    bound_r = oracle.abft_bound(np.abs(A64[rows]) @ np.abs(W64).sum(axis=0), N, K)
+    rs = g.rowsum.cpu().numpy()[rows]
+    assert np.all(np.abs(rs - exact.sum(axis=1)) <= bound_r)
+    np.testing.assert_allclose(g.bound.cpu().numpy()[rows], bound_r, rtol=(N + K + 64) * 2.0 ** -44)
+    cols = np.sort(rng.choice(N, 8, replace=False))
+    exact_c = (A64 @ W64[cols].T).sum(axis=0)
+    bound_c = oracle.abft_bound(np.abs(W64[cols]) @ np.abs(A64).sum(axis=0), M, K)
+    assert np.all(np.abs(g.colsum.cpu().numpy()[cols] - exact_c) <= bound_c)
+
+
+def test_attention_invariant_bench_shape(sdc):
+    # the benchmark's attention backward (32 heads x 4096 x 128, causal, the same seed) in its
+    # launch configuration; two sampled heads in full against the oracle, no flag anywhere
+    BH, L = W.ATTN_8B
+    x = W.attn_inputs(BH, L, DEV, seed=8, causal=True)
+    a = sdc.AttnDvCheck(BH, L, DEV)
+    a(x["Q"], x["K"], x["dO"], x["lse"], x["scale"], True)
+    torch.cuda.synchronize()
+    assert int(a.aborted[0]) == 0 and int(a.summary[0]) == 0
+    g = L * 2.0 ** -22
+    eps = 2.0 ** -8 * (1 + 2.0 ** -7) + g * (1 + g) * (1 + 2.0 ** -7)
+    for h in (0, 19):
+        Qb, Kb, dOb = (_bf16_bits(x[k][h]) for k in ("Q", "K", "dO"))
+        P = oracle.attn_probs(Qb, Kb, x["lse"][h].cpu().numpy(), x["scale"], True)
+        exact = oracle.attn_dv(P, dOb)
+        e = eps * (P.T @ np.abs(oracle.bf16_to_f64(dOb)))
+        dV = a.dV[h].float().cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(dV - exact) <= 2.0 ** -8 * (np.abs(exact) + e) + e + 2.0 ** -134)
+        v = oracle.attn_invariant(a.colsum_dv[h].cpu().numpy(), dOb)
+        assert v["n_flagged"] == 0
+        assert np.all(np.abs(a.colsum_dv[h].cpu().numpy() - exact.sum(axis=0)) <= v["bound"])
+        np.testing.assert_allclose(a.bound[h].cpu().numpy(), v["bound"], rtol=2.0 ** -38)
