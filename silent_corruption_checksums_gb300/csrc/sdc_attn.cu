@@ -20,15 +20,18 @@
 //   attn_do_prep_kernel -- dO^T [BH][128][L] for the MMA (both MMA operands
 //     then sit K-major in shared memory), lse log2(e), and float32-pair column
 //     sums of dO and |dO| per 128-row block;
-//   attn_dv_kernel -- one CTA per (head, 128-key block), 18 warps:
+//   attn_dv_kernel -- one CTA per (head, 128-key block), 19 warps:
 //     warp 0 lane 0: TMA -- the K tile once, then per 128-query step the Q
 //       tile into one of two Q stages, freed when the S MMAs have read it, and
 //       the dO^T tile with the step's 128 log-sum-exps (times log2(e)) into one
 //       of two dO stages, freed when the dV MMAs have read it;
-//     warp 1 lane 0: MMA -- S^T = K Q^T (M = keys, N = queries, K = 128) into
-//       one of two 128-column TMEM buffers, issued a step ahead, and
-//       dV += P^T dO (M = keys, N = 128, K = queries) into a third;
-//     warps 2..17: softmax -- two groups of 8 warps take alternate steps; in
+//     warp 1 lane 0: S^T = K Q^T (M = keys, N = queries, K = 128) into one of
+//       two 128-column TMEM buffers, as soon as a Q tile and a buffer are free;
+//     warp 2 lane 0: dV += P^T dO (M = keys, N = 128, K = queries) into a
+//       third.  Two issuing threads: one thread's tcgen05.mma issue rate, not
+//       the tensor pipe, bounds products with N = 128, and the two products
+//       share no TMEM, meeting only at barriers;
+//     warps 3..18: softmax -- two groups of 8 warps take alternate steps; in
 //       a group each thread owns one key (a TMEM lane) and 64 of the step's
 //       queries (two warps per lane quarter), reads those 64 scores,
 //       forms exp2(s scale log2(e) - lse log2(e)) (masked when causal), rounds
@@ -59,14 +62,15 @@ constexpr uint32_t kLStages = 16;    // log-sum-exps of a step (512 bytes): free
 // lane quarter each take 64 of the step's 128 queries.
 constexpr uint32_t kSoftWarps = 16;
 constexpr uint32_t kGroupWarps = kSoftWarps / 2;
-constexpr uint32_t kAttnThreads = 64 + 32 * kSoftWarps;
+constexpr uint32_t kSoftBase = 3;  // warps 0-2: TMA, S^T issuer, dV issuer
+constexpr uint32_t kAttnThreads = 32 * kSoftBase + 32 * kSoftWarps;
 // Barriers: kfull, qfull/qempty[kQStages], dfull/dempty[kDStages], lfull/lempty[kLStages],
-// sfull/sempty[2], pfull/pempty[2], dvfull.  Each input has its own ring and is freed by its last
+// sfull/sempty[2], pfull/pempty[2], dvfull, sdone.  Each input has its own ring and is freed by its last
 // reader, so every copy is issued steps before it is needed and no chain of a step waits on a copy.
 constexpr uint32_t kBarK = 0, kBarQF = 1, kBarQE = kBarQF + kQStages, kBarDF = kBarQE + kQStages,
                    kBarDE = kBarDF + kDStages, kBarLF = kBarDE + kDStages, kBarLE = kBarLF + kLStages,
                    kBarSF = kBarLE + kLStages, kBarSE = kBarSF + 2, kBarPF = kBarSE + 2, kBarPE = kBarPF + 2,
-                   kBarDV = kBarPE + 2, kNumBars = kBarDV + 1;
+                   kBarDV = kBarPE + 2, kBarSD = kBarDV + 1, kNumBars = kBarSD + 1;
 // shared memory: K tile | Q stages | dO^T stages | lse stages | barriers | TMEM slot
 constexpr uint32_t kOffK = 0, kOffQ = kTile, kOffD = kOffQ + kQStages * kTile, kOffLse = kOffD + kDStages * kTile,
                    kOffBar = kOffLse + kLStages * kBlk * 4, kOffSlot = kOffBar + 8 * kNumBars;
@@ -102,7 +106,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t kfull = bar + 8 * kBarK, qfull = bar + 8 * kBarQF, qempty = bar + 8 * kBarQE,
                    dfull = bar + 8 * kBarDF, dempty = bar + 8 * kBarDE, lfull = bar + 8 * kBarLF,
                    lempty = bar + 8 * kBarLE, sfull = bar + 8 * kBarSF, sempty = bar + 8 * kBarSE,
-                   pfull = bar + 8 * kBarPF, pempty = bar + 8 * kBarPE, dvfull = bar + 8 * kBarDV;
+                   pfull = bar + 8 * kBarPF, pempty = bar + 8 * kBarPE, dvfull = bar + 8 * kBarDV,
+                   sdone = bar + 8 * kBarSD;
     uint32_t *tmem_slot = (uint32_t *)(sm + kOffSlot);
     const uint32_t q_first = causal ? kb : 0u, nq = nkb - q_first;
     const uint32_t row0 = bh * L;  // this head's first row in the [BH * L, 128] views
@@ -134,6 +139,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_init(pempty + 8 * i, 1);
         }
         mbar_init(dvfull, 1);
+        mbar_init(sdone, 1);
         fence_mbar_init();
     }
     tc_fence_before();
@@ -187,12 +193,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (!ok) atomicOr(err, 1);
         }
     } else if (warp == 1) {
-        if (lane == 0) {  // ------------------------------------------ MMA issuer
+        if (lane == 0) {  // ------------------------------------------ S^T issuer
             constexpr uint32_t idesc = umma_idesc(kBlk, kBlk);
-            auto issue_s = [&](uint32_t t) -> bool {  // S^T(t) = K Q(t)^T into buffer t & 1
+            if (!mbar_wait(kfull, 0)) ok = false;
+            for (uint32_t t = 0; t < nq && ok; ++t) {  // S^T(t) = K Q(t)^T into buffer t & 1
                 const uint32_t qs = t % kQStages, b = t & 1u;
-                if (!mbar_wait(qfull + 8 * qs, (t / kQStages) & 1)) return false;
-                if (t >= 2 && !mbar_wait(sempty + 8 * b, ((t >> 1) - 1) & 1)) return false;
+                if (!mbar_wait(qfull + 8 * qs, (t / kQStages) & 1) ||
+                    (t >= 2 && !mbar_wait(sempty + 8 * b, ((t >> 1) - 1) & 1))) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
                 const uint32_t sQ = sQ0 + qs * kTile;
 #pragma unroll
@@ -203,15 +213,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
                 tc_commit(sfull + 8 * b);
                 tc_commit(qempty + 8 * qs);
-                return true;
-            };
-            if (!mbar_wait(kfull, 0)) ok = false;
-            if (ok && nq > 0) ok = issue_s(0);
+            }
+            tc_commit(sdone);  // tracks every S^T product this thread issued: the TMEM owner waits on it
+            if (!ok) atomicOr(err, 1);
+        }
+    } else if (warp == 2) {
+        if (lane == 0) {  // ------------------------------------------ dV issuer
+            constexpr uint32_t idesc = umma_idesc(kBlk, kBlk);
             for (uint32_t t = 0; t < nq && ok; ++t) {
-                if (t + 1 < nq && !issue_s(t + 1)) {
-                    ok = false;
-                    break;
-                }
                 const uint32_t ds = t % kDStages, b = t & 1u;
                 if (!mbar_wait(pfull + 8 * b, (t >> 1) & 1) || !mbar_wait(dfull + 8 * ds, (t / kDStages) & 1)) {
                     ok = false;
@@ -228,14 +237,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 tc_commit(pempty + 8 * b);   // P^T buffer b (TMEM) is free once these MMAs have read it
                 tc_commit(dempty + 8 * ds);  // and so is the dO^T stage
             }
-            tc_commit(dvfull);  // tracks every MMA issued: the epilogue and the TMEM owner wait on it
+            tc_commit(dvfull);  // tracks every dV product: the epilogue and the TMEM owner wait on it
             if (!ok) atomicOr(err, 1);
         }
     } else {  // ------------------------------------------------------- softmax + epilogue
         const uint32_t quarter = warp & 3u;       // the TMEM lanes this warp may read
-        const uint32_t part = (warp - 2) >> 2;     // which 32 of dV's columns in the epilogue
-        const uint32_t grp = (warp - 2) / kGroupWarps;        // softmax group: steps grp, grp + 2, ...
-        const uint32_t half = ((warp - 2) % kGroupWarps) >> 2;  // which 64 of a step's queries
+        const uint32_t part = (warp - kSoftBase) >> 2;     // which 32 of dV's columns in the epilogue
+        const uint32_t grp = (warp - kSoftBase) / kGroupWarps;        // softmax group: steps grp, grp + 2, ...
+        const uint32_t half = ((warp - kSoftBase) % kGroupWarps) >> 2;  // which 64 of a step's queries
         const uint32_t j = quarter * 32 + lane;  // this thread's key within the block (its TMEM lane)
         const uint32_t lane_base = (quarter * 32) << 16;
         for (uint32_t t = grp; t < nq; t += 2) {
@@ -310,7 +319,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         named_bar_sync(1, 32 * kSoftWarps);
         // dV's column sums: thread (column c, row quarter rq) sums rows 32 rq .. 32 rq + 31, then
         // the rq = 0 thread merges the others' pairs in order rq = 1, 2, 3
-        const uint32_t c = (tid - 64) & (kHD - 1), rq = (tid - 64) >> 7;
+        const uint32_t c = (tid - 32 * kSoftBase) & (kHD - 1), rq = (tid - 32 * kSoftBase) >> 7;
         float s = 0.0f, e = 0.0f;
         if (ok) {
 #pragma unroll 8
@@ -331,7 +340,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
-        if (lane == 0 && !mbar_wait(dvfull, 0)) atomicOr(err, 1);
+        if (lane == 0 && (!mbar_wait(dvfull, 0) || !mbar_wait(sdone, 0))) atomicOr(err, 1);
         __syncwarp();
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512u) : "memory");
