@@ -20,25 +20,33 @@
 //   attn_do_prep_kernel -- dO^T [BH][128][L] for the MMA (both MMA operands
 //     then sit K-major in shared memory), lse log2(e), and float32-pair column
 //     sums of dO and |dO| per 128-row block;
-//   attn_dv_kernel -- one CTA per (head, 128-key block), 19 warps:
-//     warp 0 lane 0: TMA -- the K tile once, then per 128-query step the Q
-//       tile into one of two Q stages, freed when the S MMAs have read it, and
-//       the dO^T tile with the step's 128 log-sum-exps (times log2(e)) into one
-//       of two dO stages, freed when the dV MMAs have read it;
+//   attn_dv_kernel -- persistent, one CTA per SM; a work item is one
+//     (head, 128-key block), taken from a counter heaviest first (causal:
+//     key block 0 of every head first).  24 warps:
+//     warp 0 lane 0: the work queue and the K, Q and lse copies -- claims
+//       the next item, hands it to the other roles through a 4-slot ring,
+//       copies its K tile into one of two K stages (so the next item's K
+//       arrives while this one runs), then per 128-query step the Q tile and
+//       the step's 128 log-sum-exps (times log2(e)) into their rings;
+//     warp 3 lane 0: the dO^T copies, per step into a ring of their own (one
+//       copy thread per ring: a Q copy never waits behind a dO^T stage);
 //     warp 1 lane 0: S^T = K Q^T (M = keys, N = queries, K = 128) into one of
-//       two 128-column TMEM buffers, as soon as a Q tile and a buffer are free;
-//     warp 2 lane 0: dV += P^T dO (M = keys, N = 128, K = queries) into a
-//       third.  Two issuing threads: one thread's tcgen05.mma issue rate, not
-//       the tensor pipe, bounds products with N = 128, and the two products
-//       share no TMEM, meeting only at barriers;
-//     warps 3..18: softmax -- two groups of 8 warps take alternate steps; in
-//       a group each thread owns one key (a TMEM lane) and 64 of the step's
-//       queries (two warps per lane quarter), reads those 64 scores,
-//       forms exp2(s scale log2(e) - lse log2(e)) (masked when causal), rounds
-//       to bf16 and writes them into its row of P^T in one of two TMEM
-//       buffers, from which the dV product takes its A operand; at the end it reads its 32 columns of
-//       dV's row, stores them as bf16, and the threads sum dV's columns
-//       (float32 pairs) through shared memory;
+//       two 128-column TMEM buffers;
+//     warp 2 lane 0: dV += P^T dO (M = keys, N = 128, K = queries) into one of
+//       two 128-column TMEM accumulators (alternate items), its A operand P^T
+//       read from TMEM.  Two issuing threads: one thread's tcgen05.mma issue
+//       rate, not the tensor pipe, bounds products with N = 128;
+//     warps 4..7: epilogue -- when an item's dV is complete, each thread
+//       stores its key's row as bf16 and the warps sum dV's columns (float32
+//       pairs) through shared memory, while the next item's products run;
+//     warps 8..23: softmax -- each thread owns one key (a TMEM lane) and 32
+//       of the step's queries (four warps per lane quarter), reads those 32
+//       scores, forms exp2(s scale log2(e) - lse log2(e)) (masked when
+//       causal), rounds to bf16 and writes them as its row of P^T over the
+//       first 16 of the columns it read; the S^T buffer is reused once the
+//       dV product has read that P^T.
+//     Every ring stage is freed by its last reader; each wait that usually
+//     finds its phase complete comes before the one that blocks.
 //   attn_invariant_kernel -- per (head, column): the block partials merged in
 //     order, the residual, the bound, the flag.
 // Every wait is bounded; a wait that gives up sets the call's abort flag and
@@ -51,35 +59,47 @@ namespace sdc {
 namespace {
 
 constexpr uint32_t kHD = 128;                    // head dimension
-constexpr uint32_t kBlk = 128;                   // keys per CTA, queries per step
+constexpr uint32_t kBlk = 128;                   // keys per work item, queries per step
 constexpr uint32_t kTile = kBlk * kHD * 2;       // 32 KiB: a [128 x 128] bf16 tile = two 64-column swizzled blocks
 constexpr uint32_t kHalf = kBlk * 128;           // 16 KiB: one 64-column block
-constexpr uint32_t kQStages = 2;     // Q tiles: freed by the S product
-constexpr uint32_t kDStages = 3;     // dO^T tiles: freed by the dV product
-constexpr uint32_t kLStages = 16;    // log-sum-exps of a step (512 bytes): freed by the softmax
-// Two groups of 8 softmax warps take alternate query steps (group g: steps g, g + 2, ...; S^T and
-// P^T buffer g), so one group's latency chain overlaps the other's; in a group, two warps per TMEM
-// lane quarter each take 64 of the step's 128 queries.
-constexpr uint32_t kSoftWarps = 16;
-constexpr uint32_t kGroupWarps = kSoftWarps / 2;
-constexpr uint32_t kSoftBase = 3;  // warps 0-2: TMA, S^T issuer, dV issuer
-constexpr uint32_t kAttnThreads = 32 * kSoftBase + 32 * kSoftWarps;
-// Barriers: kfull, qfull/qempty[kQStages], dfull/dempty[kDStages], lfull/lempty[kLStages],
-// sfull/sempty[2], pfull/pempty[2], dvfull, sdone.  Each input has its own ring and is freed by its last
-// reader, so every copy is issued steps before it is needed and no chain of a step waits on a copy.
-constexpr uint32_t kBarK = 0, kBarQF = 1, kBarQE = kBarQF + kQStages, kBarDF = kBarQE + kQStages,
-                   kBarDE = kBarDF + kDStages, kBarLF = kBarDE + kDStages, kBarLE = kBarLF + kLStages,
-                   kBarSF = kBarLE + kLStages, kBarSE = kBarSF + 2, kBarPF = kBarSE + 2, kBarPE = kBarPF + 2,
-                   kBarDV = kBarPE + 2, kBarSD = kBarDV + 1, kNumBars = kBarSD + 1;
-// shared memory: K tile | Q stages | dO^T stages | lse stages | barriers | TMEM slot
-constexpr uint32_t kOffK = 0, kOffQ = kTile, kOffD = kOffQ + kQStages * kTile, kOffLse = kOffD + kDStages * kTile,
-                   kOffBar = kOffLse + kLStages * kBlk * 4, kOffSlot = kOffBar + 8 * kNumBars;
-// TMEM columns: S^T buffers at 0 and 128 (fp32), dV at 256 (fp32), P^T buffers at 384 and 448
-// (bf16, two per 32-bit column: the A operand of the dV product)
-constexpr uint32_t kColS = 0, kColDv = 256, kColP = 384;
+constexpr uint32_t kKStages = 2;     // K tiles: the next item's loads while this item's S^T products read
+constexpr uint32_t kQStages = 2;     // Q tiles: freed by the S^T product
+constexpr uint32_t kDStages = 2;     // dO^T tiles: freed by the dV product
+constexpr uint32_t kLStages = 8;     // log-sum-exps of a step (512 bytes): freed by the softmax
+constexpr uint32_t kItemSlots = 4;   // work items handed from the TMA thread to the other roles
+constexpr uint32_t kNoItem = 0xFFFFFFFFu;
+// Warps: 0 the work queue and the K, Q and lse copies, 1 S^T issuer, 2 dV issuer, 3 the dO^T copies
+// (two copy threads, so that neither ring's copies wait behind the other's), 4-7 epilogue (one per
+// TMEM lane quarter), then the softmax: kQParts warps per lane quarter, kQPer of a step's queries each.
+constexpr uint32_t kQParts = 4, kQPer = kBlk / kQParts;
+constexpr uint32_t kEpiParts = 1, kEpiCols = kHD / kEpiParts;
+constexpr uint32_t kEpiBase = 4, kEpiWarps = 4 * kEpiParts, kSoftBase = kEpiBase + kEpiWarps, kSoftWarps = 4 * kQParts;
+// TMEM: kSBufs S^T buffers, then kDvBufs dV accumulators, 128 columns each.  More S^T buffers let the
+// S^T product run further ahead of the chain S^T -> softmax -> dV that frees a buffer.
+constexpr uint32_t kSBufs = 2, kDvBufs = 2;
+static_assert((kSBufs + kDvBufs) * kBlk <= 512, "TMEM has 512 columns");
+static_assert(kQPer % 32 == 0, "the softmax reads its scores 32 columns at a time");
+constexpr uint32_t kAttnThreads = 32 * (kSoftBase + kSoftWarps);
+constexpr uint32_t kItemReaders = 3 + kEpiWarps + kSoftWarps;  // issuers, dO^T copier, one per other warp
+// Barriers (each ring indexed by a counter that runs across work items):
+constexpr uint32_t kBarKF = 0, kBarKE = kBarKF + kKStages, kBarQF = kBarKE + kKStages, kBarQE = kBarQF + kQStages,
+                   kBarDF = kBarQE + kQStages, kBarDE = kBarDF + kDStages, kBarLF = kBarDE + kDStages,
+                   kBarLE = kBarLF + kLStages, kBarSF = kBarLE + kLStages, kBarPF = kBarSF + kSBufs,
+                   kBarPE = kBarPF + kSBufs, kBarVF = kBarPE + kSBufs, kBarVE = kBarVF + kDvBufs, kBarIF = kBarVE + kDvBufs, kBarIE = kBarIF + kItemSlots,
+                   kBarSD = kBarIE + kItemSlots, kBarMD = kBarSD + 1, kNumBars = kBarMD + 1;
+// shared memory: K stages | Q stages | dO^T stages | lse stages | epilogue scratch (a padded 32 x 32
+// float tile per epilogue warp) | column partials [4][128] float2 | item slots | barriers | TMEM slot
+constexpr uint32_t kScrPitch = 33;
+constexpr uint32_t kOffK = 0, kOffQ = kOffK + kKStages * kTile, kOffD = kOffQ + kQStages * kTile,
+                   kOffLse = kOffD + kDStages * kTile, kOffScr = kOffLse + kLStages * kBlk * 4,
+                   kOffCp = kOffScr + kEpiWarps * 32 * kScrPitch * 4, kOffItems = kOffCp + 4 * kHD * 8,
+                   kOffBar = kOffItems + 4 * kItemSlots, kOffSlot = kOffBar + 8 * kNumBars;
+// TMEM columns: S^T buffers at 0 and 128 (fp32; the softmax overwrites the first 32 columns of each
+// half with its P^T, bf16 pairs: the dV product's A operand), dV accumulators at 256 and 384
+constexpr uint32_t kColS = 0, kColDv = kSBufs * kBlk;
 constexpr uint32_t kAttnSmem = 1024 + kOffSlot + 16;
-constexpr uint32_t kScratchPitch = kHD + 1;  // float row pitch of the column-sum scratch (conflict-free both ways)
-static_assert(kBlk * kScratchPitch * 4 <= (kQStages + kDStages) * kTile, "column-sum scratch must fit in the stages");
+static_assert(kAttnSmem <= 232448, "shared memory per block");
+static_assert(kOffBar % 8 == 0, "mbarrier alignment");
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float ex2(float x) {
@@ -88,58 +108,74 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Barrier over `count` threads that also ORs `pred` across them: every warp of the group takes the
+// same branch afterwards.
+__device__ __forceinline__ bool bar_any(uint32_t id, uint32_t count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+// Persistent: one CTA per SM takes (head, key block) items from a counter, heaviest first (item w:
+// key block w / BH of head w % BH; when causal, key block kb meets nkb - kb query blocks).
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_dv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                    const __grid_constant__ CUtensorMap mapDoT, const float *__restrict__ lse2, uint32_t L,
-                   float scale_log2, uint32_t causal, __nv_bfloat16 *__restrict__ dV, float2 *__restrict__ part_dv,
-                   int *__restrict__ err) {
+                   uint32_t BH, float scale_log2, uint32_t causal, __nv_bfloat16 *__restrict__ dV,
+                   float2 *__restrict__ part_dv, int *__restrict__ err, uint32_t *__restrict__ next_item) {
     extern __shared__ __align__(1024) unsigned char smem[];
     const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
-    // grid (heads, key blocks): blocks start in linear order, so every head's key block 0 (the
-    // most query steps when causal) starts first and the light blocks fill the tail
-    const uint32_t bh = blockIdx.x, kb = blockIdx.y, nkb = gridDim.y;
+    const uint32_t nkb = L / kBlk, n_items = BH * nkb;
     const uint32_t base = smem_addr(smem), pad = ((base + 1023u) & ~1023u) - base;
     unsigned char *sm = smem + pad;
     const uint32_t s0 = base + pad;
-    const uint32_t sK = s0 + kOffK, sQ0 = s0 + kOffQ, sD0 = s0 + kOffD, sLse = s0 + kOffLse;
     const uint32_t bar = s0 + kOffBar;
-    const uint32_t kfull = bar + 8 * kBarK, qfull = bar + 8 * kBarQF, qempty = bar + 8 * kBarQE,
-                   dfull = bar + 8 * kBarDF, dempty = bar + 8 * kBarDE, lfull = bar + 8 * kBarLF,
-                   lempty = bar + 8 * kBarLE, sfull = bar + 8 * kBarSF, sempty = bar + 8 * kBarSE,
-                   pfull = bar + 8 * kBarPF, pempty = bar + 8 * kBarPE, dvfull = bar + 8 * kBarDV,
-                   sdone = bar + 8 * kBarSD;
+#define BAR(i) (bar + 8u * (i))
+    volatile uint32_t *items = (volatile uint32_t *)(sm + kOffItems);
     uint32_t *tmem_slot = (uint32_t *)(sm + kOffSlot);
-    const uint32_t q_first = causal ? kb : 0u, nq = nkb - q_first;
-    const uint32_t row0 = bh * L;  // this head's first row in the [BH * L, 128] views
 
-    if (warp == 1) {  // all 512 columns: S^T x 2, dV, P^T x 2
+    if (warp == 1) {  // all 512 columns: S^T x 2, dV x 2
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
                      "r"(512u)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (tid == 0) {
-        mbar_init(kfull, 1);
+        for (uint32_t i = 0; i < kKStages; ++i) {
+            mbar_init(BAR(kBarKF + i), 1);
+            mbar_init(BAR(kBarKE + i), 1);
+        }
         for (uint32_t i = 0; i < kQStages; ++i) {
-            mbar_init(qfull + 8 * i, 1);
-            mbar_init(qempty + 8 * i, 1);
+            mbar_init(BAR(kBarQF + i), 1);
+            mbar_init(BAR(kBarQE + i), 1);
         }
         for (uint32_t i = 0; i < kDStages; ++i) {
-            mbar_init(dfull + 8 * i, 1);
-            mbar_init(dempty + 8 * i, 1);
+            mbar_init(BAR(kBarDF + i), 1);
+            mbar_init(BAR(kBarDE + i), 1);
         }
         for (uint32_t i = 0; i < kLStages; ++i) {
-            mbar_init(lfull + 8 * i, 1);
-            mbar_init(lempty + 8 * i, kGroupWarps);  // stage i serves steps of one parity: one group
+            mbar_init(BAR(kBarLF + i), 1);
+            mbar_init(BAR(kBarLE + i), kSoftWarps);
         }
-        for (uint32_t i = 0; i < 2; ++i) {
-            mbar_init(sfull + 8 * i, 1);
-            mbar_init(sempty + 8 * i, kGroupWarps);  // one arrival per warp of softmax group i
-            mbar_init(pfull + 8 * i, kGroupWarps);
-            mbar_init(pempty + 8 * i, 1);
+        for (uint32_t i = 0; i < kSBufs; ++i) {
+            mbar_init(BAR(kBarSF + i), 1);
+            mbar_init(BAR(kBarPF + i), kSoftWarps);
+            mbar_init(BAR(kBarPE + i), 1);
         }
-        mbar_init(dvfull, 1);
-        mbar_init(sdone, 1);
+        for (uint32_t i = 0; i < kDvBufs; ++i) {
+            mbar_init(BAR(kBarVF + i), 1);
+            mbar_init(BAR(kBarVE + i), kEpiWarps);
+        }
+        for (uint32_t i = 0; i < kItemSlots; ++i) {
+            mbar_init(BAR(kBarIF + i), 1);
+            mbar_init(BAR(kBarIE + i), kItemReaders);
+        }
+        mbar_init(BAR(kBarSD), 1);
+        mbar_init(BAR(kBarMD), 1);
         fence_mbar_init();
     }
     tc_fence_before();
@@ -149,202 +185,318 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     bool ok = true;
 
     if (warp == 0) {
-        if (lane == 0) {  // ------------------------------------------ TMA producer
-            mbar_arrive_expect_tx(kfull, kTile);
-            tma_load_2d(sK, &mapK, 0, (int32_t)(row0 + kb * kBlk), kfull);
-            tma_load_2d(sK + kHalf, &mapK, 64, (int32_t)(row0 + kb * kBlk), kfull);
-            uint32_t tl = 0, tq = 0, td = 0;  // steps whose lse / Q / dO^T copies were issued
-            for (uint32_t t = 0; t < nq && ok; ++t) {
-                const uint32_t qb = q_first + t;
-                const uint32_t ls = t % kLStages, qs = t % kQStages, ds = t % kDStages;
-                if (t >= kLStages && !mbar_wait(lempty + 8 * ls, ((t / kLStages) - 1) & 1)) {
+        if (lane == 0) {  // ------------------------------------------ work queue + TMA
+            uint32_t nk = 0, tl = 0, tq = 0;  // K tiles and steps whose copies were issued
+            for (uint32_t i = 0; ok; ++i) {
+                const uint32_t slot = i % kItemSlots;
+                if (i >= kItemSlots && !mbar_wait(BAR(kBarIE + slot), ((i / kItemSlots) - 1) & 1)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(lfull + 8 * ls, kBlk * 4);
-                bulk_g2s(sLse + ls * kBlk * 4, lse2 + (uint64_t)row0 + qb * kBlk, kBlk * 4, lfull + 8 * ls);
-                tl = t + 1;
-                if (t >= kQStages && !mbar_wait(qempty + 8 * qs, ((t / kQStages) - 1) & 1)) {
+                uint32_t w = atomicAdd(next_item, 1u);
+                if (w >= n_items) w = kNoItem;
+                items[slot] = w;
+                mbar_arrive(BAR(kBarIF + slot));  // release: the readers see the slot after their wait
+                if (w == kNoItem) break;
+                const uint32_t kb = w / BH, bh = w % BH, q_first = causal ? kb : 0u, nq = nkb - q_first;
+                const uint32_t row0 = bh * L;
+                const uint32_t ks = i % kKStages, sK = s0 + kOffK + ks * kTile;
+                if (i >= kKStages && !mbar_wait(BAR(kBarKE + ks), ((i / kKStages) - 1) & 1)) {
                     ok = false;
                     break;
                 }
-                const uint32_t sQ = sQ0 + qs * kTile, sDo = sD0 + ds * kTile;
-                mbar_arrive_expect_tx(qfull + 8 * qs, kTile);
-                tma_load_2d(sQ, &mapQ, 0, (int32_t)(row0 + qb * kBlk), qfull + 8 * qs);
-                tma_load_2d(sQ + kHalf, &mapQ, 64, (int32_t)(row0 + qb * kBlk), qfull + 8 * qs);
-                tq = t + 1;
-                if (t >= kDStages && !mbar_wait(dempty + 8 * ds, ((t / kDStages) - 1) & 1)) {
-                    ok = false;
-                    break;
+                mbar_arrive_expect_tx(BAR(kBarKF + ks), kTile);
+                tma_load_2d(sK, &mapK, 0, (int32_t)(row0 + kb * kBlk), BAR(kBarKF + ks));
+                tma_load_2d(sK + kHalf, &mapK, 64, (int32_t)(row0 + kb * kBlk), BAR(kBarKF + ks));
+                nk = i + 1;
+                for (uint32_t t = 0; t < nq; ++t) {
+                    const uint32_t g = tl, qb = q_first + t;
+                    const uint32_t ls = g % kLStages, qs = g % kQStages;
+                    if (g >= kLStages && !mbar_wait(BAR(kBarLE + ls), ((g / kLStages) - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(BAR(kBarLF + ls), kBlk * 4);
+                    bulk_g2s(s0 + kOffLse + ls * kBlk * 4, lse2 + (uint64_t)row0 + qb * kBlk, kBlk * 4,
+                             BAR(kBarLF + ls));
+                    tl = g + 1;
+                    if (g >= kQStages && !mbar_wait(BAR(kBarQE + qs), ((g / kQStages) - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sQ = s0 + kOffQ + qs * kTile;
+                    mbar_arrive_expect_tx(BAR(kBarQF + qs), kTile);
+                    tma_load_2d(sQ, &mapQ, 0, (int32_t)(row0 + qb * kBlk), BAR(kBarQF + qs));
+                    tma_load_2d(sQ + kHalf, &mapQ, 64, (int32_t)(row0 + qb * kBlk), BAR(kBarQF + qs));
+                    tq = g + 1;
                 }
-                mbar_arrive_expect_tx(dfull + 8 * ds, kTile);
-                tma_load_2d(sDo, &mapDoT, (int32_t)(qb * kBlk), (int32_t)(bh * kHD), dfull + 8 * ds);
-                tma_load_2d(sDo + kHalf, &mapDoT, (int32_t)(qb * kBlk + 64), (int32_t)(bh * kHD), dfull + 8 * ds);
-                td = t + 1;
             }
             // Let no copy land after the block has left: wait (bounded) for the last ones issued.
-            if (!mbar_wait(kfull, 0)) ok = false;
+            for (uint32_t j = nk > kKStages ? nk - kKStages : 0; j < nk; ++j)
+                if (!mbar_wait(BAR(kBarKF + j % kKStages), (j / kKStages) & 1)) ok = false;
             for (uint32_t j = tl > kLStages ? tl - kLStages : 0; j < tl; ++j)
-                if (!mbar_wait(lfull + 8 * (j % kLStages), (j / kLStages) & 1)) ok = false;
+                if (!mbar_wait(BAR(kBarLF + j % kLStages), (j / kLStages) & 1)) ok = false;
             for (uint32_t j = tq > kQStages ? tq - kQStages : 0; j < tq; ++j)
-                if (!mbar_wait(qfull + 8 * (j % kQStages), (j / kQStages) & 1)) ok = false;
+                if (!mbar_wait(BAR(kBarQF + j % kQStages), (j / kQStages) & 1)) ok = false;
+            if (!ok) atomicOr(err, 1);
+        }
+    } else if (warp == 3) {
+        if (lane == 0) {  // ------------------------------------------ dO^T copies
+            uint32_t td = 0;  // steps whose dO^T copies were issued
+            for (uint32_t i = 0; ok; ++i) {
+                const uint32_t slot = i % kItemSlots;
+                if (!mbar_wait(BAR(kBarIF + slot), (i / kItemSlots) & 1)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t w = items[slot];
+                mbar_arrive(BAR(kBarIE + slot));
+                if (w == kNoItem) break;
+                const uint32_t kb = w / BH, bh = w % BH, q_first = causal ? kb : 0u, nq = nkb - q_first;
+                for (uint32_t t = 0; t < nq; ++t) {
+                    const uint32_t g = td, qb = q_first + t, ds = g % kDStages, sDo = s0 + kOffD + ds * kTile;
+                    if (g >= kDStages && !mbar_wait(BAR(kBarDE + ds), ((g / kDStages) - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(BAR(kBarDF + ds), kTile);
+                    tma_load_2d(sDo, &mapDoT, (int32_t)(qb * kBlk), (int32_t)(bh * kHD), BAR(kBarDF + ds));
+                    tma_load_2d(sDo + kHalf, &mapDoT, (int32_t)(qb * kBlk + 64), (int32_t)(bh * kHD),
+                                BAR(kBarDF + ds));
+                    td = g + 1;
+                }
+            }
             for (uint32_t j = td > kDStages ? td - kDStages : 0; j < td; ++j)
-                if (!mbar_wait(dfull + 8 * (j % kDStages), (j / kDStages) & 1)) ok = false;
+                if (!mbar_wait(BAR(kBarDF + j % kDStages), (j / kDStages) & 1)) ok = false;
             if (!ok) atomicOr(err, 1);
         }
     } else if (warp == 1) {
         if (lane == 0) {  // ------------------------------------------ S^T issuer
             constexpr uint32_t idesc = umma_idesc(kBlk, kBlk);
-            if (!mbar_wait(kfull, 0)) ok = false;
-            for (uint32_t t = 0; t < nq && ok; ++t) {  // S^T(t) = K Q(t)^T into buffer t & 1
-                const uint32_t qs = t % kQStages, b = t & 1u;
-                if (!mbar_wait(qfull + 8 * qs, (t / kQStages) & 1) ||
-                    (t >= 2 && !mbar_wait(sempty + 8 * b, ((t >> 1) - 1) & 1))) {
+            uint32_t g = 0;
+            for (uint32_t i = 0; ok; ++i) {
+                const uint32_t slot = i % kItemSlots;
+                if (!mbar_wait(BAR(kBarIF + slot), (i / kItemSlots) & 1)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                const uint32_t sQ = sQ0 + qs * kTile;
-#pragma unroll
-                for (uint32_t ks = 0; ks < kHD / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * kHalf + (ks & 3u) * 32;
-                    tc_mma(tmem + kColS + b * kBlk, umma_desc_sw128(sK + off), umma_desc_sw128(sQ + off), idesc,
-                           ks ? 1u : 0u);
+                const uint32_t w = items[slot];
+                mbar_arrive(BAR(kBarIE + slot));
+                if (w == kNoItem) break;
+                const uint32_t kb = w / BH, nq = nkb - (causal ? kb : 0u);
+                const uint32_t ks = i % kKStages, sK = s0 + kOffK + ks * kTile;
+                if (!mbar_wait(BAR(kBarKF + ks), (i / kKStages) & 1)) {
+                    ok = false;
+                    break;
                 }
-                tc_commit(sfull + 8 * b);
-                tc_commit(qempty + 8 * qs);
+                for (uint32_t t = 0; t < nq; ++t, ++g) {  // S^T(g) = K Q(g)^T into buffer g % kSBufs
+                    const uint32_t qs = g % kQStages, b = g % kSBufs;
+                    // buffer b is free once dV(g - kSBufs) has read the P^T the softmax wrote over it
+                    if (!mbar_wait(BAR(kBarQF + qs), (g / kQStages) & 1) ||
+                        (g >= kSBufs && !mbar_wait(BAR(kBarPE + b), ((g / kSBufs) - 1) & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sQ = s0 + kOffQ + qs * kTile;
+#pragma unroll
+                    for (uint32_t k = 0; k < kHD / 16; ++k) {
+                        const uint32_t off = (k >> 2) * kHalf + (k & 3u) * 32;
+                        tc_mma(tmem + kColS + b * kBlk, umma_desc_sw128(sK + off), umma_desc_sw128(sQ + off), idesc,
+                               k ? 1u : 0u);
+                    }
+                    tc_commit(BAR(kBarSF + b));
+                    tc_commit(BAR(kBarQE + qs));
+                }
+                if (!ok) break;
+                tc_commit(BAR(kBarKE + ks));  // the K stage is free once this item's products have read it
             }
-            tc_commit(sdone);  // tracks every S^T product this thread issued: the TMEM owner waits on it
+            tc_commit(BAR(kBarSD));  // tracks every product this thread issued: the TMEM owner waits on it
             if (!ok) atomicOr(err, 1);
         }
     } else if (warp == 2) {
         if (lane == 0) {  // ------------------------------------------ dV issuer
             constexpr uint32_t idesc = umma_idesc(kBlk, kBlk);
-            for (uint32_t t = 0; t < nq && ok; ++t) {
-                const uint32_t ds = t % kDStages, b = t & 1u;
-                if (!mbar_wait(pfull + 8 * b, (t >> 1) & 1) || !mbar_wait(dfull + 8 * ds, (t / kDStages) & 1)) {
+            uint32_t g = 0;
+            for (uint32_t i = 0; ok; ++i) {
+                const uint32_t slot = i % kItemSlots;
+                if (!mbar_wait(BAR(kBarIF + slot), (i / kItemSlots) & 1)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                const uint32_t sDo = sD0 + ds * kTile;
-#pragma unroll
-                for (uint32_t ks = 0; ks < kBlk / 16; ++ks) {  // 16 queries = 8 TMEM columns of P^T
-                    const uint32_t off = (ks >> 2) * kHalf + (ks & 3u) * 32;
-                    tc_mma_ts(tmem + kColDv, tmem + kColP + b * 64 + ks * 8, umma_desc_sw128(sDo + off), idesc,
-                              (t | ks) != 0 ? 1u : 0u);
+                const uint32_t w = items[slot];
+                mbar_arrive(BAR(kBarIE + slot));
+                if (w == kNoItem) break;
+                const uint32_t kb = w / BH, nq = nkb - (causal ? kb : 0u), db = i % kDvBufs;
+                if (i >= kDvBufs && !mbar_wait(BAR(kBarVE + db), ((i / kDvBufs) - 1) & 1)) {  // its last reader
+                    ok = false;
+                    break;
                 }
-                tc_commit(pempty + 8 * b);   // P^T buffer b (TMEM) is free once these MMAs have read it
-                tc_commit(dempty + 8 * ds);  // and so is the dO^T stage
+                for (uint32_t t = 0; t < nq; ++t, ++g) {
+                    const uint32_t ds = g % kDStages, b = g % kSBufs;
+                    if (!mbar_wait(BAR(kBarDF + ds), (g / kDStages) & 1) ||  // copied steps ahead: first
+                        !mbar_wait(BAR(kBarPF + b), (g / kSBufs) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sDo = s0 + kOffD + ds * kTile;
+#pragma unroll
+                    for (uint32_t k = 0; k < kBlk / 16; ++k) {  // 16 queries = 8 TMEM columns of P^T
+                        const uint32_t off = (k >> 2) * kHalf + (k & 3u) * 32;
+                        // queries 16k .. 16k + 15: softmax part 16k / kQPer wrote them at its first columns
+                        const uint32_t pa = kColS + b * kBlk + (16 * k / kQPer) * kQPer + (16 * k % kQPer) / 2;
+                        tc_mma_ts(tmem + kColDv + db * kBlk, tmem + pa, umma_desc_sw128(sDo + off), idesc,
+                                  (t | k) != 0 ? 1u : 0u);
+                    }
+                    tc_commit(BAR(kBarPE + b));   // S^T buffer b free once these products have read its P^T
+                    tc_commit(BAR(kBarDE + ds));  // and so is the dO^T stage
+                }
+                if (!ok) break;
+                tc_commit(BAR(kBarVF + db));  // the item's dV is complete
             }
-            tc_commit(dvfull);  // tracks every dV product: the epilogue and the TMEM owner wait on it
+            tc_commit(BAR(kBarMD));
             if (!ok) atomicOr(err, 1);
         }
-    } else {  // ------------------------------------------------------- softmax + epilogue
-        const uint32_t quarter = warp & 3u;       // the TMEM lanes this warp may read
-        const uint32_t part = (warp - kSoftBase) >> 2;     // which 32 of dV's columns in the epilogue
-        const uint32_t grp = (warp - kSoftBase) / kGroupWarps;        // softmax group: steps grp, grp + 2, ...
-        const uint32_t half = ((warp - kSoftBase) % kGroupWarps) >> 2;  // which 64 of a step's queries
-        const uint32_t j = quarter * 32 + lane;  // this thread's key within the block (its TMEM lane)
-        const uint32_t lane_base = (quarter * 32) << 16;
-        for (uint32_t t = grp; t < nq; t += 2) {
-            const uint32_t ls = t % kLStages, b = t & 1u, qb = q_first + t;
-            bool got = mbar_wait(sfull + 8 * b, (t >> 1) & 1);
-            if (got) got = mbar_wait(lfull + 8 * ls, (t / kLStages) & 1);  // the step's log-sum-exps
-            if (got && t >= 2) got = mbar_wait(pempty + 8 * b, ((t >> 1) - 1) & 1);
-            if (__any_sync(0xffffffffu, !got)) {
+    } else if (warp < kSoftBase) {  // ------------------------------ epilogue
+        const uint32_t quarter = warp & 3u, j = quarter * 32 + lane, lane_base = (quarter * 32) << 16;
+        float *scr = (float *)(sm + kOffScr) + (warp - kEpiBase) * 32 * kScrPitch;
+        float2 *cpart = (float2 *)(sm + kOffCp);  // [lane quarter][column]
+        for (uint32_t i = 0;; ++i) {
+            const uint32_t slot = i % kItemSlots;
+            bool got = mbar_wait(BAR(kBarIF + slot), (i / kItemSlots) & 1);
+            if (bar_any(2, 32 * kEpiWarps, !got)) {
+                ok = false;
+                break;
+            }
+            const uint32_t w = items[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(kBarIE + slot));
+            if (w == kNoItem) break;
+            const uint32_t kb = w / BH, bh = w % BH, db = i % kDvBufs;
+            got = mbar_wait(BAR(kBarVF + db), (i / kDvBufs) & 1);
+            if (bar_any(2, 32 * kEpiWarps, !got)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t lsa = sLse + ls * kBlk * 4 + half * 64 * 4;  // lse log2(e) of this half's 64 queries
-            const bool diag = causal && qb == kb;
-            uint32_t r[64];
-            tc_ld32(tmem + lane_base + kColS + b * kBlk + half * 64, *(uint32_t(*)[32]) & r[0]);
-            tc_ld32(tmem + lane_base + kColS + b * kBlk + half * 64 + 32, *(uint32_t(*)[32]) & r[32]);
-            tc_wait_ld();
-            uint32_t w[32];  // this thread's 64 probabilities as bf16 pairs: 32 columns of its row of P^T
+            __nv_bfloat16 *drow = dV + ((uint64_t)bh * L + kb * kBlk + j) * kHD;
+#pragma unroll 1
+            for (uint32_t cc = 0; cc < kHD / 32; ++cc) {
+                uint32_t r[32];
+                tc_ld32(tmem + lane_base + kColDv + db * kBlk + cc * 32, r);
+                tc_wait_ld();
+                uint4 *d = (uint4 *)(drow + cc * 32);
 #pragma unroll
-            for (uint32_t g = 0; g < 8; ++g) {  // 8 queries at a time
-                const float4 la = ld_shared_f4(lsa + g * 32), lb = ld_shared_f4(lsa + g * 32 + 16);
-                const float l8[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
+                for (uint32_t v = 0; v < 4; ++v) {
+                    uint32_t p[4];
 #pragma unroll
-                for (uint32_t q = 0; q < 8; q += 2) {
-                    const uint32_t i0 = half * 64 + g * 8 + q;  // query within the step
-                    float p0 = ex2(__fmaf_rn(__uint_as_float(r[g * 8 + q]), scale_log2, -l8[q]));
-                    float p1 = ex2(__fmaf_rn(__uint_as_float(r[g * 8 + q + 1]), scale_log2, -l8[q + 1]));
-                    if (diag) {  // query i attends key j only when i >= j
-                        p0 = i0 >= j ? p0 : 0.0f;
-                        p1 = i0 + 1 >= j ? p1 : 0.0f;
-                    }
-                    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w[g * 4 + q / 2]) : "f"(p1), "f"(p0));
+                    for (uint32_t k = 0; k < 4; ++k)
+                        asm("cvt.rn.bf16x2.f32 %0, %1, %2;"
+                            : "=r"(p[k])
+                            : "f"(__uint_as_float(r[8 * v + 2 * k + 1])), "f"(__uint_as_float(r[8 * v + 2 * k])));
+                    d[v] = make_uint4(p[0], p[1], p[2], p[3]);
                 }
+                // this warp's 32 rows of the chunk's 32 columns, summed in row order (float32 pair)
+#pragma unroll
+                for (uint32_t q = 0; q < 32; ++q) scr[lane * kScrPitch + q] = __uint_as_float(r[q]);
+                __syncwarp();
+                float s = 0.0f, e = 0.0f;
+#pragma unroll 8
+                for (uint32_t rr = 0; rr < 32; ++rr) pair_add(s, e, scr[rr * kScrPitch + lane]);
+                cpart[quarter * kHD + cc * 32 + lane] = make_float2(s, e);
+                __syncwarp();
             }
-            tc_st16(tmem + lane_base + kColP + b * 64 + half * 32, *(const uint32_t(*)[16]) & w[0]);
-            tc_st16(tmem + lane_base + kColP + b * 64 + half * 32 + 16, *(const uint32_t(*)[16]) & w[16]);
-            tc_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(sempty + 8 * b);
-                mbar_arrive(pfull + 8 * b);
-                mbar_arrive(lempty + 8 * ls);
+            if (lane == 0) mbar_arrive(BAR(kBarVE + db));  // the accumulator may take its next item
+            named_bar_sync(2, 32 * kEpiWarps);
+            {  // the lane quarters' partials merged in order: the item's column sums of dV
+                const uint32_t c = (warp - kEpiBase) * 32 + lane;
+                float2 a = cpart[c];
+#pragma unroll
+                for (uint32_t q = 1; q < 4; ++q) pair_merge(a.x, a.y, cpart[q * kHD + c].x, cpart[q * kHD + c].y);
+                part_dv[((uint64_t)bh * nkb + kb) * kHD + c] = a;
             }
+            named_bar_sync(2, 32 * kEpiWarps);
         }
-        // ---- epilogue: dV row j to global as bf16, then dV's column sums
-        const bool got = mbar_wait(dvfull, 0);
-        if (__any_sync(0xffffffffu, !got)) ok = false;
-        float *scratch = (float *)(sm + kOffQ);
-        if (ok) {
-            tc_fence_after();
-            __nv_bfloat16 *drow = dV + ((uint64_t)row0 + kb * kBlk + j) * kHD;
-            uint32_t r[32];
-            tc_ld32(tmem + lane_base + kColDv + part * 32, r);
-            tc_wait_ld();
-            float *srow = scratch + j * kScratchPitch + part * 32;
-#pragma unroll
-            for (uint32_t q = 0; q < 32; ++q) srow[q] = __uint_as_float(r[q]);
-            uint4 *d = (uint4 *)(drow + part * 32);
-#pragma unroll
-            for (uint32_t v = 0; v < 4; ++v) {
-                uint32_t w[4];
-#pragma unroll
-                for (uint32_t k = 0; k < 4; ++k)
-                    asm("cvt.rn.bf16x2.f32 %0, %1, %2;"
-                        : "=r"(w[k])
-                        : "f"(__uint_as_float(r[8 * v + 2 * k + 1])), "f"(__uint_as_float(r[8 * v + 2 * k])));
-                d[v] = make_uint4(w[0], w[1], w[2], w[3]);
+        if (!ok && lane == 0) atomicOr(err, 1);
+    } else {  // ------------------------------------------------------- softmax
+        const uint32_t quarter = warp & 3u;               // the TMEM lanes this warp may access
+        const uint32_t qpart = (warp - kSoftBase) >> 2;   // which kQPer of a step's queries
+        const uint32_t j = quarter * 32 + lane;           // this thread's key within the item (its TMEM lane)
+        const uint32_t lane_base = (quarter * 32) << 16;
+        uint32_t g = 0;
+        for (uint32_t i = 0; ok; ++i) {
+            const uint32_t slot = i % kItemSlots;
+            const bool got_item = mbar_wait(BAR(kBarIF + slot), (i / kItemSlots) & 1);
+            if (__any_sync(0xffffffffu, !got_item)) {
+                ok = false;
+                break;
             }
-        }
-        named_bar_sync(1, 32 * kSoftWarps);
-        // dV's column sums: thread (column c, row quarter rq) sums rows 32 rq .. 32 rq + 31, then
-        // the rq = 0 thread merges the others' pairs in order rq = 1, 2, 3
-        const uint32_t c = (tid - 32 * kSoftBase) & (kHD - 1), rq = (tid - 32 * kSoftBase) >> 7;
-        float s = 0.0f, e = 0.0f;
-        if (ok) {
-#pragma unroll 8
-            for (uint32_t jj = rq * 32; jj < rq * 32 + 32; ++jj) pair_add(s, e, scratch[jj * kScratchPitch + c]);
-        }
-        named_bar_sync(1, 32 * kSoftWarps);  // every thread has read the scratch: reuse its first rows
-        if (rq != 0) {
-            scratch[(rq * kHD + c) * 2] = s;
-            scratch[(rq * kHD + c) * 2 + 1] = e;
-        }
-        named_bar_sync(1, 32 * kSoftWarps);
-        if (rq == 0) {
-            for (uint32_t k = 1; k < 4; ++k) pair_merge(s, e, scratch[(k * kHD + c) * 2], scratch[(k * kHD + c) * 2 + 1]);
-            part_dv[((uint64_t)bh * nkb + kb) * kHD + c] = make_float2(s, e);
+            const uint32_t w = items[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(kBarIE + slot));
+            if (w == kNoItem) break;
+            const uint32_t kb = w / BH, q_first = causal ? kb : 0u, nq = nkb - q_first;
+            for (uint32_t t = 0; t < nq; ++t, ++g) {
+                const uint32_t ls = g % kLStages, b = g % kSBufs, qb = q_first + t;
+                // the step's log-sum-exps (copied steps ahead) first, then the scores: the wait that
+                // blocks comes last, so nothing stands between the scores' arrival and their use
+                bool got = mbar_wait(BAR(kBarLF + ls), (g / kLStages) & 1);
+                if (got) got = mbar_wait(BAR(kBarSF + b), (g / kSBufs) & 1);
+                if (__any_sync(0xffffffffu, !got)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t lsa = s0 + kOffLse + ls * kBlk * 4 + qpart * kQPer * 4;  // lse log2(e) of its queries
+                const bool diag = causal && qb == kb;
+                const uint32_t col = tmem + lane_base + kColS + b * kBlk + qpart * kQPer;
+                uint32_t r[kQPer];
+#pragma unroll
+                for (uint32_t c = 0; c < kQPer / 32; ++c) tc_ld32(col + 32 * c, *(uint32_t(*)[32]) & r[32 * c]);
+                tc_wait_ld();
+                uint32_t pw[kQPer / 2];  // this thread's probabilities as bf16 pairs
+#pragma unroll
+                for (uint32_t q8 = 0; q8 < kQPer / 8; ++q8) {  // 8 queries at a time
+                    const float4 la = ld_shared_f4(lsa + q8 * 32), lb = ld_shared_f4(lsa + q8 * 32 + 16);
+                    const float l8[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
+#pragma unroll
+                    for (uint32_t q = 0; q < 8; q += 2) {
+                        const uint32_t i0 = qpart * kQPer + q8 * 8 + q;  // query within the step
+                        float p0 = ex2(__fmaf_rn(__uint_as_float(r[q8 * 8 + q]), scale_log2, -l8[q]));
+                        float p1 = ex2(__fmaf_rn(__uint_as_float(r[q8 * 8 + q + 1]), scale_log2, -l8[q + 1]));
+                        if (diag) {  // query i attends key j only when i >= j
+                            p0 = i0 >= j ? p0 : 0.0f;
+                            p1 = i0 + 1 >= j ? p1 : 0.0f;
+                        }
+                        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(pw[q8 * 4 + q / 2]) : "f"(p1), "f"(p0));
+                    }
+                }
+                // P^T over the first kQPer / 2 of the columns just read (this thread's own lane and columns)
+#pragma unroll
+                for (uint32_t c = 0; c < kQPer / 32; ++c) tc_st16(col + 16 * c, *(const uint32_t(*)[16]) & pw[16 * c]);
+                tc_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(BAR(kBarPF + b));
+                    mbar_arrive(BAR(kBarLE + ls));
+                }
+            }
         }
         if (!ok && lane == 0) atomicOr(err, 1);
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
-        if (lane == 0 && (!mbar_wait(dvfull, 0) || !mbar_wait(sdone, 0))) atomicOr(err, 1);
+        if (lane == 0 && (!mbar_wait(BAR(kBarMD), 0) || !mbar_wait(BAR(kBarSD), 0))) atomicOr(err, 1);
         __syncwarp();
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512u) : "memory");
     }
+#undef BAR
 }
 
 // dO^T, lse log2(e), and the column sums of dO and |dO| over one block of 128 rows: block
@@ -432,7 +584,8 @@ __global__ void attn_invariant_kernel(const float2 *__restrict__ part_dv, const 
 size_t round_up256(size_t x) { return (x + 255) / 256 * 256; }
 
 // Workspace: dO^T [BH][128][L] bf16 | dO partials [BH][L/128][128] float4 |
-// dV partials [BH][L/128][128] float2 | lse log2(e) [BH][L] float | abort word.
+// dV partials [BH][L/128][128] float2 | lse log2(e) [BH][L] float | abort word and the
+// dV kernel's work counter.
 struct AttnWs {
     size_t dot, pdo, pdv, lse2, err, total;
 };
@@ -502,15 +655,21 @@ sdc_status sdc_attn_dv_check(const void *d_Q, const void *d_K, const void *d_dO,
     if (st == SDC_OK) st = make_map_sw128(&mapDoT, dOT, (uint64_t)BH * kHD, L, kHD);
     if (st != SDC_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
-    e = cudaMemsetAsync(err, 0, sizeof(int), s);
+    uint32_t *next_item = (uint32_t *)(err + 1);  // the work queue's counter, in the abort word's slot
+    int n_sm = 0;
+    e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    const uint32_t n_items = BH * (L / kBlk);
+    const uint32_t grid = n_items < (uint32_t)n_sm ? n_items : (uint32_t)n_sm;
+    e = cudaMemsetAsync(err, 0, 2 * sizeof(int), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(d_summary, 0, sizeof(sdc_abft_summary), s);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(attn_dv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAttnSmem);
     if (e != cudaSuccess) return cuda_fail(e, "sdc_attn_dv_check setup");
     const uint32_t nb = L / kBlk;
     attn_do_prep_kernel<<<dim3(nb, BH), 256, 0, s>>>((const __nv_bfloat16 *)d_dO, d_lse, L, dOT, pdo, lse2);
-    attn_dv_kernel<<<dim3(BH, nb), kAttnThreads, kAttnSmem, s>>>(mapQ, mapK, mapDoT, lse2, L, scale * kLog2e, causal,
-                                                                (__nv_bfloat16 *)d_dV, pdv, err);
+    attn_dv_kernel<<<grid, kAttnThreads, kAttnSmem, s>>>(mapQ, mapK, mapDoT, lse2, L, BH, scale * kLog2e, causal,
+                                                        (__nv_bfloat16 *)d_dV, pdv, err, next_item);
     attn_invariant_kernel<<<(BH * kHD + 127) / 128, 128, 0, s>>>(pdv, pdo, BH, nb, L, tol_scale, d_colsum_dv,
                                                                  d_colsum_do, d_residual, d_bound, d_flag, d_summary,
                                                                  err, d_aborted);
