@@ -17,9 +17,9 @@
 //   invariant per column c: sum_j dV_acc[j, c]  vs  sum_i dO[i, c].
 //
 // Kernels:
-//   attn_do_prep_kernel -- dO^T [BH][128][L] for the MMA (both MMA operands
-//     then sit K-major in shared memory), lse log2(e), and float32-pair column
-//     sums of dO and |dO| per 128-row block;
+//   attn_do_prep_kernel -- lse log2(e), and float32-pair column sums of dO
+//     and |dO| per 128-row block (dO itself feeds the dV product as it is:
+//     its B operand, MN-major);
 //   attn_dv_kernel -- persistent, one CTA per SM; a work item is one
 //     (head, 128-key block), taken from a counter heaviest first (causal:
 //     key block 0 of every head first).  24 warps:
@@ -28,8 +28,8 @@
 //       copies its K tile into one of two K stages (so the next item's K
 //       arrives while this one runs), then per 128-query step the Q tile and
 //       the step's 128 log-sum-exps (times log2(e)) into their rings;
-//     warp 3 lane 0: the dO^T copies, per step into a ring of their own (one
-//       copy thread per ring: a Q copy never waits behind a dO^T stage);
+//     warp 3 lane 0: the dO copies, per step into a ring of their own (one
+//       copy thread per ring: a Q copy never waits behind a dO stage);
 //     warp 1 lane 0: S^T = K Q^T (M = keys, N = queries, K = 128) into one of
 //       two 128-column TMEM buffers;
 //     warp 2 lane 0: dV += P^T dO (M = keys, N = 128, K = queries) into one of
@@ -64,30 +64,29 @@ constexpr uint32_t kTile = kBlk * kHD * 2;       // 32 KiB: a [128 x 128] bf16 t
 constexpr uint32_t kHalf = kBlk * 128;           // 16 KiB: one 64-column block
 constexpr uint32_t kKStages = 2;     // K tiles: the next item's loads while this item's S^T products read
 constexpr uint32_t kQStages = 2;     // Q tiles: freed by the S^T product
-constexpr uint32_t kDStages = 2;     // dO^T tiles: freed by the dV product
+constexpr uint32_t kDStages = 2;     // dO tiles: freed by the dV product
 constexpr uint32_t kLStages = 8;     // log-sum-exps of a step (512 bytes): freed by the softmax
 constexpr uint32_t kItemSlots = 4;   // work items handed from the TMA thread to the other roles
 constexpr uint32_t kNoItem = 0xFFFFFFFFu;
-// Warps: 0 the work queue and the K, Q and lse copies, 1 S^T issuer, 2 dV issuer, 3 the dO^T copies
+// Warps: 0 the work queue and the K, Q and lse copies, 1 S^T issuer, 2 dV issuer, 3 the dO copies
 // (two copy threads, so that neither ring's copies wait behind the other's), 4-7 epilogue (one per
 // TMEM lane quarter), then the softmax: kQParts warps per lane quarter, kQPer of a step's queries each.
 constexpr uint32_t kQParts = 4, kQPer = kBlk / kQParts;
-constexpr uint32_t kEpiParts = 1, kEpiCols = kHD / kEpiParts;
-constexpr uint32_t kEpiBase = 4, kEpiWarps = 4 * kEpiParts, kSoftBase = kEpiBase + kEpiWarps, kSoftWarps = 4 * kQParts;
+constexpr uint32_t kEpiBase = 4, kEpiWarps = 4, kSoftBase = kEpiBase + kEpiWarps, kSoftWarps = 4 * kQParts;
 // TMEM: kSBufs S^T buffers, then kDvBufs dV accumulators, 128 columns each.  More S^T buffers let the
 // S^T product run further ahead of the chain S^T -> softmax -> dV that frees a buffer.
 constexpr uint32_t kSBufs = 2, kDvBufs = 2;
 static_assert((kSBufs + kDvBufs) * kBlk <= 512, "TMEM has 512 columns");
 static_assert(kQPer % 32 == 0, "the softmax reads its scores 32 columns at a time");
 constexpr uint32_t kAttnThreads = 32 * (kSoftBase + kSoftWarps);
-constexpr uint32_t kItemReaders = 3 + kEpiWarps + kSoftWarps;  // issuers, dO^T copier, one per other warp
+constexpr uint32_t kItemReaders = 3 + kEpiWarps + kSoftWarps;  // issuers, dO copier, one per other warp
 // Barriers (each ring indexed by a counter that runs across work items):
 constexpr uint32_t kBarKF = 0, kBarKE = kBarKF + kKStages, kBarQF = kBarKE + kKStages, kBarQE = kBarQF + kQStages,
                    kBarDF = kBarQE + kQStages, kBarDE = kBarDF + kDStages, kBarLF = kBarDE + kDStages,
                    kBarLE = kBarLF + kLStages, kBarSF = kBarLE + kLStages, kBarPF = kBarSF + kSBufs,
                    kBarPE = kBarPF + kSBufs, kBarVF = kBarPE + kSBufs, kBarVE = kBarVF + kDvBufs, kBarIF = kBarVE + kDvBufs, kBarIE = kBarIF + kItemSlots,
                    kBarSD = kBarIE + kItemSlots, kBarMD = kBarSD + 1, kNumBars = kBarMD + 1;
-// shared memory: K stages | Q stages | dO^T stages | lse stages | epilogue scratch (a padded 32 x 32
+// shared memory: K stages | Q stages | dO stages | lse stages | epilogue scratch (a padded 32 x 32
 // float tile per epilogue warp) | column partials [4][128] float2 | item slots | barriers | TMEM slot
 constexpr uint32_t kScrPitch = 33;
 constexpr uint32_t kOffK = 0, kOffQ = kOffK + kKStages * kTile, kOffD = kOffQ + kQStages * kTile,
@@ -124,7 +123,7 @@ __device__ __forceinline__ bool bar_any(uint32_t id, uint32_t count, bool pred) 
 // key block w / BH of head w % BH; when causal, key block kb meets nkb - kb query blocks).
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_dv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
-                   const __grid_constant__ CUtensorMap mapDoT, const float *__restrict__ lse2, uint32_t L,
+                   const __grid_constant__ CUtensorMap mapDo, const float *__restrict__ lse2, uint32_t L,
                    uint32_t BH, float scale_log2, uint32_t causal, __nv_bfloat16 *__restrict__ dV,
                    float2 *__restrict__ part_dv, int *__restrict__ err, uint32_t *__restrict__ next_item) {
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -241,8 +240,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (!ok) atomicOr(err, 1);
         }
     } else if (warp == 3) {
-        if (lane == 0) {  // ------------------------------------------ dO^T copies
-            uint32_t td = 0;  // steps whose dO^T copies were issued
+        if (lane == 0) {  // ------------------------------------------ dO copies
+            uint32_t td = 0;  // steps whose dO copies were issued
             for (uint32_t i = 0; ok; ++i) {
                 const uint32_t slot = i % kItemSlots;
                 if (!mbar_wait(BAR(kBarIF + slot), (i / kItemSlots) & 1)) {
@@ -260,9 +259,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(BAR(kBarDF + ds), kTile);
-                    tma_load_2d(sDo, &mapDoT, (int32_t)(qb * kBlk), (int32_t)(bh * kHD), BAR(kBarDF + ds));
-                    tma_load_2d(sDo + kHalf, &mapDoT, (int32_t)(qb * kBlk + 64), (int32_t)(bh * kHD),
-                                BAR(kBarDF + ds));
+                    // the step's 128 rows of dO, head dimensions 0-63 then 64-127: K rows of the
+                    // MN-major B operand
+                    tma_load_2d(sDo, &mapDo, 0, (int32_t)(bh * L + qb * kBlk), BAR(kBarDF + ds));
+                    tma_load_2d(sDo + kHalf, &mapDo, 64, (int32_t)(bh * L + qb * kBlk), BAR(kBarDF + ds));
                     td = g + 1;
                 }
             }
@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
     } else if (warp == 2) {
         if (lane == 0) {  // ------------------------------------------ dV issuer
-            constexpr uint32_t idesc = umma_idesc(kBlk, kBlk);
+            constexpr uint32_t idesc = umma_idesc_bmn(kBlk, kHD);  // B = dO, MN-major
             uint32_t g = 0;
             for (uint32_t i = 0; ok; ++i) {
                 const uint32_t slot = i % kItemSlots;
@@ -343,14 +343,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const uint32_t sDo = s0 + kOffD + ds * kTile;
 #pragma unroll
                     for (uint32_t k = 0; k < kBlk / 16; ++k) {  // 16 queries = 8 TMEM columns of P^T
-                        const uint32_t off = (k >> 2) * kHalf + (k & 3u) * 32;
-                        // queries 16k .. 16k + 15: softmax part 16k / kQPer wrote them at its first columns
+                        // queries 16k .. 16k + 15: softmax part 16k / kQPer wrote them at its first columns;
+                        // their rows of dO start 16k rows (2 KB) into each 64-column half
                         const uint32_t pa = kColS + b * kBlk + (16 * k / kQPer) * kQPer + (16 * k % kQPer) / 2;
-                        tc_mma_ts(tmem + kColDv + db * kBlk, tmem + pa, umma_desc_sw128(sDo + off), idesc,
-                                  (t | k) != 0 ? 1u : 0u);
+                        tc_mma_ts(tmem + kColDv + db * kBlk, tmem + pa, umma_desc_sw128_mn(sDo + k * 2048, kHalf),
+                                  idesc, (t | k) != 0 ? 1u : 0u);
                     }
                     tc_commit(BAR(kBarPE + b));   // S^T buffer b free once these products have read its P^T
-                    tc_commit(BAR(kBarDE + ds));  // and so is the dO^T stage
+                    tc_commit(BAR(kBarDE + ds));  // and so is the dO stage
                 }
                 if (!ok) break;
                 tc_commit(BAR(kBarVF + db));  // the item's dV is complete
@@ -499,33 +499,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #undef BAR
 }
 
-// dO^T, lse log2(e), and the column sums of dO and |dO| over one block of 128 rows: block
-// (x, y) takes rows 128x .. 128x + 127 of head y.  The tile goes through
-// shared memory (row-major, read back column-wise for the transpose and the
-// sums); part_do[y][x][c] = {pair of sum_i dO[i, c], pair of sum_i |dO[i, c]|}.
+// lse log2(e), and the column sums of dO and |dO| over one block of 128 rows:
+// block (x, y) takes rows 128x .. 128x + 127 of head y.  The tile goes through
+// shared memory (row-major, read back column-wise for the sums);
+// part_do[y][x][c] = {pair of sum_i dO[i, c], pair of sum_i |dO[i, c]|}.
 __global__ void __launch_bounds__(256) attn_do_prep_kernel(const __nv_bfloat16 *__restrict__ dO,
                                                            const float *__restrict__ lse, uint32_t L,
-                                                           __nv_bfloat16 *__restrict__ dOT, float4 *__restrict__ part_do,
-                                                           float *__restrict__ lse2) {
+                                                           float4 *__restrict__ part_do, float *__restrict__ lse2) {
     __shared__ __align__(16) uint16_t tile[kBlk][kHD];
     const uint32_t qb = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
     const uint64_t row0 = (uint64_t)bh * L + (uint64_t)qb * kBlk;
     if (tid < kBlk) lse2[row0 + tid] = lse[row0 + tid] * kLog2e;  // the exponent's offset in base 2
+#pragma unroll
     for (uint32_t v = tid; v < kBlk * kHD / 8; v += 256) {  // 16-byte vectors, row-major
         const uint32_t r = v / (kHD / 8), c8 = v % (kHD / 8);
         *(uint4 *)&tile[r][c8 * 8] = ld_stream(dO + (row0 + r) * kHD + c8 * 8);
     }
     __syncthreads();
-    for (uint32_t v = tid; v < kHD * kBlk / 16; v += 256) {  // dO^T row d, queries 16 q16 .. 16 q16 + 15
-        const uint32_t d = v % kHD, q16 = v / kHD;
-        uint32_t w[8];
-#pragma unroll
-        for (uint32_t k = 0; k < 8; ++k)
-            w[k] = (uint32_t)tile[q16 * 16 + 2 * k][d] | ((uint32_t)tile[q16 * 16 + 2 * k + 1][d] << 16);
-        uint4 *o = (uint4 *)(dOT + ((uint64_t)bh * kHD + d) * L + (uint64_t)qb * kBlk + q16 * 16);  // one 32-byte sector
-        o[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        o[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    }
     // column sums: thread (column c, row half h) sums rows 64h .. 64h + 63 of dO and |dO|
     // (two independent chains); the half-1 pairs are merged into the half-0 ones in that order
     __shared__ float4 half1[kHD];
@@ -583,17 +573,16 @@ __global__ void attn_invariant_kernel(const float2 *__restrict__ part_dv, const 
 
 size_t round_up256(size_t x) { return (x + 255) / 256 * 256; }
 
-// Workspace: dO^T [BH][128][L] bf16 | dO partials [BH][L/128][128] float4 |
+// Workspace: dO partials [BH][L/128][128] float4 |
 // dV partials [BH][L/128][128] float2 | lse log2(e) [BH][L] float | abort word and the
 // dV kernel's work counter.
 struct AttnWs {
-    size_t dot, pdo, pdv, lse2, err, total;
+    size_t pdo, pdv, lse2, err, total;
 };
 AttnWs attn_ws(uint32_t BH, uint32_t L) {
     AttnWs w;
     const size_t nb = L / kBlk;
-    w.dot = 0;
-    w.pdo = round_up256((size_t)BH * kHD * L * 2);
+    w.pdo = 0;
     w.pdv = w.pdo + round_up256((size_t)BH * nb * kHD * sizeof(float4));
     w.lse2 = w.pdv + round_up256((size_t)BH * nb * kHD * sizeof(float2));
     w.err = w.lse2 + round_up256((size_t)BH * L * sizeof(float));
@@ -644,15 +633,14 @@ sdc_status sdc_attn_dv_check(const void *d_Q, const void *d_K, const void *d_dO,
         return fail(SDC_ERR_WS_TOO_SMALL, "workspace smaller than sdc_attn_workspace_size");
     if ((uint64_t)d_ws & 255u) return fail(SDC_ERR_BAD_POINTER, "workspace is not 256-byte aligned");
     const AttnWs w = attn_ws(BH, L);
-    __nv_bfloat16 *dOT = (__nv_bfloat16 *)((char *)d_ws + w.dot);
     float4 *pdo = (float4 *)((char *)d_ws + w.pdo);
     float2 *pdv = (float2 *)((char *)d_ws + w.pdv);
     float *lse2 = (float *)((char *)d_ws + w.lse2);
     int *err = (int *)((char *)d_ws + w.err);
-    CUtensorMap mapQ, mapK, mapDoT;
+    CUtensorMap mapQ, mapK, mapDo;
     st = make_map_sw128(&mapQ, d_Q, (uint64_t)BH * L, kHD, kBlk);
     if (st == SDC_OK) st = make_map_sw128(&mapK, d_K, (uint64_t)BH * L, kHD, kBlk);
-    if (st == SDC_OK) st = make_map_sw128(&mapDoT, dOT, (uint64_t)BH * kHD, L, kHD);
+    if (st == SDC_OK) st = make_map_sw128(&mapDo, d_dO, (uint64_t)BH * L, kHD, kBlk);
     if (st != SDC_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     uint32_t *next_item = (uint32_t *)(err + 1);  // the work queue's counter, in the abort word's slot
@@ -667,8 +655,8 @@ sdc_status sdc_attn_dv_check(const void *d_Q, const void *d_K, const void *d_dO,
         e = cudaFuncSetAttribute(attn_dv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAttnSmem);
     if (e != cudaSuccess) return cuda_fail(e, "sdc_attn_dv_check setup");
     const uint32_t nb = L / kBlk;
-    attn_do_prep_kernel<<<dim3(nb, BH), 256, 0, s>>>((const __nv_bfloat16 *)d_dO, d_lse, L, dOT, pdo, lse2);
-    attn_dv_kernel<<<grid, kAttnThreads, kAttnSmem, s>>>(mapQ, mapK, mapDoT, lse2, L, BH, scale * kLog2e, causal,
+    attn_do_prep_kernel<<<dim3(nb, BH), 256, 0, s>>>((const __nv_bfloat16 *)d_dO, d_lse, L, pdo, lse2);
+    attn_dv_kernel<<<grid, kAttnThreads, kAttnSmem, s>>>(mapQ, mapK, mapDo, lse2, L, BH, scale * kLog2e, causal,
                                                         (__nv_bfloat16 *)d_dV, pdv, err, next_item);
     attn_invariant_kernel<<<(BH * kHD + 127) / 128, 128, 0, s>>>(pdv, pdo, BH, nb, L, tol_scale, d_colsum_dv,
                                                                  d_colsum_do, d_residual, d_bound, d_flag, d_summary,

@@ -29,11 +29,22 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t addr) {
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// Descriptor of an MN-major operand in the 128-byte-swizzled layout: each K row
+// holds 64 bf16 along M or N (128 bytes), 8 consecutive K rows make a 1 KB atom
+// (stride byte offset 1 KB), and blocks of 64 along M or N sit `lbo` bytes
+// apart (leading byte offset).
+__device__ __forceinline__ uint64_t umma_desc_sw128_mn(uint32_t addr, uint32_t lbo) {
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
 // Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
 // K-major, N and M.
 __host__ __device__ constexpr uint32_t umma_idesc(uint32_t m, uint32_t n) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
+// The same with B MN-major (bit 16).
+__host__ __device__ constexpr uint32_t umma_idesc_bmn(uint32_t m, uint32_t n) { return umma_idesc(m, n) | (1u << 16); }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int32_t c0, int32_t c1,
                                             uint32_t mbar) {

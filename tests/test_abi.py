@@ -134,10 +134,9 @@ def test_host_validation_without_gpu(sdc):
         with pytest.raises(sdc.SdcError) as ei:
             sdc.sdc_attn_dv_check(*fake, BH, L, D, scale, causal, tol, *outs, 0, 0, 0)
         assert ei.value.status == 9, (BH, L, D, scale, causal, tol)
-    # dO^T, dO partials (float4 per block and column), dV partials (float2), lse log2(e)
-    # (a float per token), the abort word
-    assert sdc.sdc_attn_workspace_size(2, 256, 128) == (2 * 128 * 256 * 2 + 2 * 2 * 128 * 16 + 2 * 2 * 128 * 8
-                                                        + 2 * 256 * 4 + 256)
+    # dO partials (float4 per block and column), dV partials (float2), lse log2(e) (a float
+    # per token), the abort word and the work counter
+    assert sdc.sdc_attn_workspace_size(2, 256, 128) == (2 * 2 * 128 * 16 + 2 * 2 * 128 * 8 + 2 * 256 * 4 + 256)
     assert sdc.sdc_attn_workspace_size(2, 256, 64) == 0
     assert sdc.sdc_abft_workspace_size(128, 16384, 64) == (64 * 128 * 8 + 4 * 16384 * 8 + 4 * 1024 + 64 * 64 * 16
                                                            + 256)
