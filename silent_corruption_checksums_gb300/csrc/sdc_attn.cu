@@ -47,8 +47,10 @@
 //       dV product has read that P^T.
 //     Every ring stage is freed by its last reader; each wait that usually
 //     finds its phase complete comes before the one that blocks.
-//   attn_invariant_kernel -- per (head, column): the block partials merged in
-//     order, the residual, the bound, the flag.
+//     The item that completes a head (its last key block to finish, in
+//     whichever block) merges the head's partials in order and writes the
+//     invariant per column: dV's and dO's column sums, the residual, the
+//     bound and the flag; the last block to finish publishes the abort word.
 // Every wait is bounded; a wait that gives up sets the call's abort flag and
 // the block still drains its copies and MMAs (bounded) and frees its TMEM.
 #include "sdc_internal.cuh"
@@ -92,7 +94,7 @@ constexpr uint32_t kScrPitch = 33;
 constexpr uint32_t kOffK = 0, kOffQ = kOffK + kKStages * kTile, kOffD = kOffQ + kQStages * kTile,
                    kOffLse = kOffD + kDStages * kTile, kOffScr = kOffLse + kLStages * kBlk * 4,
                    kOffCp = kOffScr + kEpiWarps * 32 * kScrPitch * 4, kOffItems = kOffCp + 4 * kHD * 8,
-                   kOffBar = kOffItems + 4 * kItemSlots, kOffSlot = kOffBar + 8 * kNumBars;
+                   kOffFlag = kOffItems + 4 * kItemSlots, kOffBar = kOffFlag + 8, kOffSlot = kOffBar + 8 * kNumBars;
 // TMEM columns: S^T buffers at 0 and 128 (fp32; the softmax overwrites the first 32 columns of each
 // half with its P^T, bf16 pairs: the dV product's A operand), dV accumulators at 256 and 384
 constexpr uint32_t kColS = 0, kColDv = kSBufs * kBlk;
@@ -119,13 +121,51 @@ __device__ __forceinline__ bool bar_any(uint32_t id, uint32_t count, bool pred) 
     return r != 0;
 }
 
+// The invariant of head bh, column c, once every key block's partial is in part_dv: dV's column
+// sum (the blocks' partials merged in order), dO's and |dO|'s (the prep pass's partials merged in
+// order), the residual, the bound and the flag.
+struct AttnOut {
+    double *colsum_dv, *colsum_do, *residual, *bound;
+    uint8_t *flag;
+    sdc_abft_summary *summary;
+    uint32_t *aborted;
+    float tol_scale;
+};
+__device__ void head_invariant(const float2 *part_dv, const float4 *part_do, uint32_t bh, uint32_t c, uint32_t nb,
+                               uint32_t L, const AttnOut &o) {
+    float vs = 0.0f, vc = 0.0f, os = 0.0f, oc = 0.0f, as = 0.0f, ac = 0.0f;
+#pragma unroll 8
+    for (uint32_t b = 0; b < nb; ++b) {  // L2 reads: other blocks wrote these partials
+        const float2 pv = __ldcg(part_dv + ((uint64_t)bh * nb + b) * kHD + c);
+        const float4 po = __ldcg(part_do + ((uint64_t)bh * nb + b) * kHD + c);
+        pair_merge(vs, vc, pv.x, pv.y);
+        pair_merge(os, oc, po.x, po.y);
+        pair_merge(as, ac, po.z, po.w);
+    }
+    const double dv = (double)vs + (double)vc, dsum = (double)os + (double)oc, dabs = (double)as + (double)ac;
+    const double g = (double)L * 0x1p-22, rho = 1.0 + 0x1p-7;
+    const double bnd = (0x1p-8 * rho + g * (1.0 + g) * rho + 0x1p-40) * dabs + 0x1p-100;
+    const double d = dv - dsum;
+    const uint32_t i = bh * kHD + c;
+    o.colsum_dv[i] = dv;
+    o.colsum_do[i] = dsum;
+    o.residual[i] = d;
+    o.bound[i] = bnd;
+    const uint8_t f = fabs(d) <= (double)o.tol_scale * bnd ? 0 : 1;  // NaN flags
+    o.flag[i] = f;
+    if (f) atomicAdd(&o.summary->n_flagged, 1u);
+}
+
 // Persistent: one CTA per SM takes (head, key block) items from a counter, heaviest first (item w:
 // key block w / BH of head w % BH; when causal, key block kb meets nkb - kb query blocks).
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_dv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                    const __grid_constant__ CUtensorMap mapDo, const float *__restrict__ lse2, uint32_t L,
                    uint32_t BH, float scale_log2, uint32_t causal, __nv_bfloat16 *__restrict__ dV,
-                   float2 *__restrict__ part_dv, int *__restrict__ err, uint32_t *__restrict__ next_item) {
+                   float2 *__restrict__ part_dv, const float4 *__restrict__ part_do, const AttnOut out,
+                   int *__restrict__ err, uint32_t *__restrict__ ctr) {
+    // ctr: [0] the work counter, [1] blocks finished, [3 + h] key blocks of head h finished
+    uint32_t *next_item = ctr;
     extern __shared__ __align__(1024) unsigned char smem[];
     const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
     const uint32_t nkb = L / kBlk, n_items = BH * nkb;
@@ -362,6 +402,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const uint32_t quarter = warp & 3u, j = quarter * 32 + lane, lane_base = (quarter * 32) << 16;
         float *scr = (float *)(sm + kOffScr) + (warp - kEpiBase) * 32 * kScrPitch;
         float2 *cpart = (float2 *)(sm + kOffCp);  // [lane quarter][column]
+        volatile uint32_t *last = (volatile uint32_t *)(sm + kOffFlag);
         for (uint32_t i = 0;; ++i) {
             const uint32_t slot = i % kItemSlots;
             bool got = mbar_wait(BAR(kBarIF + slot), (i / kItemSlots) & 1);
@@ -411,14 +452,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(kBarVE + db));  // the accumulator may take its next item
             named_bar_sync(2, 32 * kEpiWarps);
+            const uint32_t c = (warp - kEpiBase) * 32 + lane;  // one column per epilogue thread
             {  // the lane quarters' partials merged in order: the item's column sums of dV
-                const uint32_t c = (warp - kEpiBase) * 32 + lane;
                 float2 a = cpart[c];
 #pragma unroll
                 for (uint32_t q = 1; q < 4; ++q) pair_merge(a.x, a.y, cpart[q * kHD + c].x, cpart[q * kHD + c].y);
                 part_dv[((uint64_t)bh * nkb + kb) * kHD + c] = a;
             }
+            // the item that completes its head (the head's last key block to finish, in any block)
+            // finishes the head's invariant
+            __threadfence();
             named_bar_sync(2, 32 * kEpiWarps);
+            if (c == 0) *last = atomicAdd(ctr + 3 + bh, 1u) == nkb - 1 ? 1u : 0u;
+            named_bar_sync(2, 32 * kEpiWarps);
+            if (*last) {
+                __threadfence();
+                head_invariant(part_dv, part_do, bh, c, nkb, L, out);
+            }
         }
         if (!ok && lane == 0) atomicOr(err, 1);
     } else {  // ------------------------------------------------------- softmax
@@ -496,6 +546,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512u) : "memory");
     }
+    __syncthreads();
+    if (tid == 0) {  // the last block to finish publishes whether any wait gave up
+        __threadfence();
+        if (atomicAdd(ctr + 1, 1u) == gridDim.x - 1) {
+            __threadfence();
+            *out.aborted = atomicOr(err, 0) != 0 ? 1u : 0u;
+        }
+    }
 #undef BAR
 }
 
@@ -537,45 +595,12 @@ __global__ void __launch_bounds__(256) attn_do_prep_kernel(const __nv_bfloat16 *
     }
 }
 
-// Per (head, column): dV's column sum (block partials merged in order), dO's
-// column sum and |dO|'s, the residual, the bound and the flag.
-__global__ void attn_invariant_kernel(const float2 *__restrict__ part_dv, const float4 *__restrict__ part_do,
-                                      uint32_t BH, uint32_t nb, uint32_t L, float tol_scale,
-                                      double *__restrict__ colsum_dv, double *__restrict__ colsum_do,
-                                      double *__restrict__ residual, double *__restrict__ bound,
-                                      uint8_t *__restrict__ flag, sdc_abft_summary *__restrict__ summary,
-                                      const int *__restrict__ err, uint32_t *__restrict__ aborted) {
-    const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i == 0) *aborted = *err != 0 ? 1u : 0u;
-    if (i >= BH * kHD) return;
-    const uint32_t bh = i / kHD, c = i % kHD;
-    float vs = 0.0f, vc = 0.0f, os = 0.0f, oc = 0.0f, as = 0.0f, ac = 0.0f;
-#pragma unroll 8
-    for (uint32_t b = 0; b < nb; ++b) {
-        const float2 pv = part_dv[((uint64_t)bh * nb + b) * kHD + c];
-        const float4 po = part_do[((uint64_t)bh * nb + b) * kHD + c];
-        pair_merge(vs, vc, pv.x, pv.y);
-        pair_merge(os, oc, po.x, po.y);
-        pair_merge(as, ac, po.z, po.w);
-    }
-    const double dv = (double)vs + (double)vc, dsum = (double)os + (double)oc, dabs = (double)as + (double)ac;
-    const double g = (double)L * 0x1p-22, rho = 1.0 + 0x1p-7;
-    const double b = (0x1p-8 * rho + g * (1.0 + g) * rho + 0x1p-40) * dabs + 0x1p-100;
-    const double d = dv - dsum;
-    colsum_dv[i] = dv;
-    colsum_do[i] = dsum;
-    residual[i] = d;
-    bound[i] = b;
-    const uint8_t f = fabs(d) <= (double)tol_scale * b ? 0 : 1;  // NaN flags
-    flag[i] = f;
-    if (f) atomicAdd(&summary->n_flagged, 1u);
-}
-
 size_t round_up256(size_t x) { return (x + 255) / 256 * 256; }
 
 // Workspace: dO partials [BH][L/128][128] float4 |
-// dV partials [BH][L/128][128] float2 | lse log2(e) [BH][L] float | abort word and the
-// dV kernel's work counter.
+// dV partials [BH][L/128][128] float2 | lse log2(e) [BH][L] float | the abort word, the dV
+// kernel's work counter, its count of finished blocks (one word of padding) and of finished
+// key blocks per head [BH].
 struct AttnWs {
     size_t pdo, pdv, lse2, err, total;
 };
@@ -586,7 +611,7 @@ AttnWs attn_ws(uint32_t BH, uint32_t L) {
     w.pdv = w.pdo + round_up256((size_t)BH * nb * kHD * sizeof(float4));
     w.lse2 = w.pdv + round_up256((size_t)BH * nb * kHD * sizeof(float2));
     w.err = w.lse2 + round_up256((size_t)BH * L * sizeof(float));
-    w.total = w.err + 256;
+    w.total = w.err + round_up256(16 + (size_t)BH * 4);
     return w;
 }
 
@@ -643,24 +668,22 @@ sdc_status sdc_attn_dv_check(const void *d_Q, const void *d_K, const void *d_dO,
     if (st == SDC_OK) st = make_map_sw128(&mapDo, d_dO, (uint64_t)BH * L, kHD, kBlk);
     if (st != SDC_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
-    uint32_t *next_item = (uint32_t *)(err + 1);  // the work queue's counter, in the abort word's slot
+    uint32_t *ctr = (uint32_t *)(err + 1);  // the counters after the abort word
     int n_sm = 0;
     e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
     const uint32_t n_items = BH * (L / kBlk);
     const uint32_t grid = n_items < (uint32_t)n_sm ? n_items : (uint32_t)n_sm;
-    e = cudaMemsetAsync(err, 0, 2 * sizeof(int), s);
+    e = cudaMemsetAsync(err, 0, 16 + (size_t)BH * 4, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(d_summary, 0, sizeof(sdc_abft_summary), s);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(attn_dv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAttnSmem);
     if (e != cudaSuccess) return cuda_fail(e, "sdc_attn_dv_check setup");
     const uint32_t nb = L / kBlk;
+    const AttnOut out{d_colsum_dv, d_colsum_do, d_residual, d_bound, d_flag, d_summary, d_aborted, tol_scale};
     attn_do_prep_kernel<<<dim3(nb, BH), 256, 0, s>>>((const __nv_bfloat16 *)d_dO, d_lse, L, pdo, lse2);
     attn_dv_kernel<<<grid, kAttnThreads, kAttnSmem, s>>>(mapQ, mapK, mapDo, lse2, L, BH, scale * kLog2e, causal,
-                                                        (__nv_bfloat16 *)d_dV, pdv, err, next_item);
-    attn_invariant_kernel<<<(BH * kHD + 127) / 128, 128, 0, s>>>(pdv, pdo, BH, nb, L, tol_scale, d_colsum_dv,
-                                                                 d_colsum_do, d_residual, d_bound, d_flag, d_summary,
-                                                                 err, d_aborted);
+                                                        (__nv_bfloat16 *)d_dV, pdv, pdo, out, err, ctr);
     e = cudaGetLastError();
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_attn_dv_check launch");
 }

@@ -135,8 +135,9 @@ def test_host_validation_without_gpu(sdc):
             sdc.sdc_attn_dv_check(*fake, BH, L, D, scale, causal, tol, *outs, 0, 0, 0)
         assert ei.value.status == 9, (BH, L, D, scale, causal, tol)
     # dO partials (float4 per block and column), dV partials (float2), lse log2(e) (a float
-    # per token), the abort word and the work counter
+    # per token), the abort word and the counters (16 bytes + one word per head, in 256-byte units)
     assert sdc.sdc_attn_workspace_size(2, 256, 128) == (2 * 2 * 128 * 16 + 2 * 2 * 128 * 8 + 2 * 256 * 4 + 256)
+    assert sdc.sdc_attn_workspace_size(64, 128, 128) == (64 * 128 * 16 + 64 * 128 * 8 + 64 * 128 * 4 + 512)
     assert sdc.sdc_attn_workspace_size(2, 256, 64) == 0
     assert sdc.sdc_abft_workspace_size(128, 16384, 64) == (64 * 128 * 8 + 4 * 16384 * 8 + 4 * 1024 + 64 * 64 * 16
                                                            + 256)
