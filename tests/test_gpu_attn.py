@@ -148,3 +148,42 @@ def test_rejects_bad_arguments(sdc):
         with pytest.raises(sdc.SdcError) as ei:
             sdc.sdc_attn_dv_check(*bad)
         assert ei.value.status == status, (i, v)
+
+
+def _check_against_oracle(sdc, x, a, causal):
+    BH = x["Q"].shape[0]
+    Qb, Kb, dOb = _bits(x["Q"]), _bits(x["K"]), _bits(x["dO"])
+    lse = x["lse"].cpu().numpy()
+    dV = a.dV.float().cpu().numpy().astype(np.float64)
+    eps = _eps(x["Q"].shape[1])
+    for h in range(BH):
+        P = oracle.attn_probs(Qb[h], Kb[h], lse[h], x["scale"], causal)
+        exact = oracle.attn_dv(P, dOb[h])
+        e = eps * (P.T @ np.abs(oracle.bf16_to_f64(dOb[h])))
+        assert np.all(np.abs(dV[h] - exact) <= 2.0 ** -8 * (np.abs(exact) + e) + e + 2.0 ** -134), h
+        v = oracle.attn_invariant(a.colsum_dv[h].cpu().numpy(), dOb[h])
+        assert np.all(np.abs(a.colsum_dv[h].cpu().numpy() - exact.sum(axis=0)) <= v["bound"]), h
+        np.testing.assert_allclose(a.bound[h].cpu().numpy(), v["bound"], rtol=2.0 ** -38)
+        assert v["n_flagged"] == 0 and np.all(a.flag[h].cpu().numpy() == 0), h
+
+
+@pytest.mark.parametrize("BH,L", [(151, 128), (152, 128), (153, 128), (1, 2048)])
+def test_work_items_around_the_grid(sdc, BH, L):
+    # (head, key block) items one fewer than, equal to and one more than the persistent grid
+    # (one block per SM on this GPU), and one head split over sixteen items
+    x = W.attn_inputs(BH, L, DEV, seed=35 + BH, causal=True)
+    a = _run(sdc, x)
+    assert int(a.aborted[0]) == 0 and int(a.summary[0]) == 0
+    _check_against_oracle(sdc, x, a, True)
+
+
+def test_counters_reset_between_calls(sdc):
+    # the same object (workspace, counters) called causal, non-causal, causal again
+    xc = W.attn_inputs(3, 512, DEV, seed=36, causal=True)
+    xn = W.attn_inputs(3, 512, DEV, seed=37, causal=False)
+    a = sdc.AttnDvCheck(3, 512, DEV)
+    for x, causal in [(xc, True), (xn, False), (xc, True)]:
+        a(x["Q"], x["K"], x["dO"], x["lse"], x["scale"], causal)
+        torch.cuda.synchronize()
+        assert int(a.aborted[0]) == 0 and int(a.summary[0]) == 0
+        _check_against_oracle(sdc, x, a, causal)
