@@ -24,6 +24,9 @@
  *    enqueued; nothing is enqueued when a call fails.  sdc_last_error()
  *    returns a one-line detail for the calling thread's last failure.  No
  *    kernel traps or asserts.
+ *  - A workspace (d_ws) holds a call's intermediate values and counters,
+ *    which the call resets itself: calls that share one workspace must not
+ *    overlap on the GPU (order them on one stream, or give each its own).
  *  - Tensors are contiguous (the page fingerprints t.contiguous()) and their
  *    element order is the flat row-major order.  Start addresses need only be
  *    aligned to the element size.
