@@ -520,13 +520,15 @@ def abft_verify(rowsum: np.ndarray, A_bits: np.ndarray, W_bits: np.ndarray, tol_
 # dV = P^T dO and every row of the softmax P sums to 1, so 1^T dV = 1^T dO;
 # the column sums of dV come from its float32 accumulator)
 # --------------------------------------------------------------------------
-def attn_probs(Q_bits: np.ndarray, K_bits: np.ndarray, lse: np.ndarray, scale: float, causal: bool) -> np.ndarray:
-    """P [L, L] of one head, rebuilt as the backward does: exp(scale Q K^T - lse) with
-    the forward's log-sum-exp per query row; causal masks key j > query i to 0."""
+def attn_probs(Q_bits: np.ndarray, K_bits: np.ndarray, lse: np.ndarray, scale: float, causal: bool,
+               key0: int = 0) -> np.ndarray:
+    """P [L, n] of one head, rebuilt as the backward does: exp(scale Q K^T - lse) with
+    the forward's log-sum-exp per query row; causal masks key j > query i to 0.  The
+    rows of K_bits are keys key0, key0 + 1, ... (all L keys by default)."""
     S = bf16_to_f64(Q_bits) @ bf16_to_f64(K_bits).T
     P = np.exp(S * float(np.float32(scale)) - np.asarray(lse, dtype=np.float64)[:, None])
     if causal:
-        P = np.tril(P)
+        P = np.tril(P, -key0)  # keeps P[i, jj] where key key0 + jj <= query i
     return P
 
 

@@ -300,10 +300,16 @@ def attn_inputs(BH: int, L: int, device, seed: int = 8, causal: bool = True, D: 
     dO = normal((BH, L, D), 1.0, torch.bfloat16, gen, device)
     scale = 1.0 / math.sqrt(D)
     lse = torch.empty((BH, L), dtype=torch.float32, device=device)
-    mask = torch.ones((L, L), dtype=torch.bool, device=device).triu(1) if causal else None
-    for h in range(BH):  # the forward's softmax statistics, one head at a time
-        s = (Q[h].float() @ K[h].float().t()) * scale
-        if mask is not None:
-            s.masked_fill_(mask, float("-inf"))
-        lse[h] = torch.logsumexp(s, dim=-1)
+    # the forward's softmax statistics, one head at a time; past 8,192 tokens, in blocks of
+    # 4,096 query rows (the whole score matrix of a head would not fit)
+    rows = L if L <= 8192 else 4096
+    for h in range(BH):
+        Kf = K[h].float()
+        for r0 in range(0, L, rows):
+            s = (Q[h, r0:r0 + rows].float() @ Kf.t()) * scale
+            if causal:
+                keys = torch.arange(L, device=device)[None, :]
+                qs = torch.arange(r0, min(L, r0 + rows), device=device)[:, None]
+                s.masked_fill_(keys > qs, float("-inf"))
+            lse[h, r0:r0 + rows] = torch.logsumexp(s, dim=-1)
     return {"Q": Q, "K": K, "dO": dO, "lse": lse, "scale": scale, "causal": causal}

@@ -101,7 +101,8 @@ def test_host_validation_without_gpu(sdc):
     with pytest.raises(sdc.SdcError) as ei:
         sdc.sdc_abft_gemm(0, 4096, 8192, 128, 256, 64, 0, 0, 0, 0, 0, 0)
     assert ei.value.status == 1
-    for M, N, K in [(100, 256, 64), (128, 200, 64), (128, 256, 48), (0, 256, 64), (128, 256, 1 << 21)]:
+    for M, N, K in [(100, 256, 64), (128, 200, 64), (128, 256, 48), (0, 256, 64), (128, 256, (1 << 20) + 64),
+                    (128, 256, 1 << 21)]:
         with pytest.raises(sdc.SdcError) as ei:
             sdc.sdc_abft_gemm(4096, 8192, 16384, M, N, K, 0, 0, 0, 0, 0, 0)
         assert ei.value.status == 9, (M, N, K)

@@ -195,3 +195,19 @@ def test_weight_fault_flags_its_columns(sdc):
     assert set(np.nonzero(~clean)[0]) <= set(cols)
     assert int(clear.sum()) >= 2
     assert int(g.summary[1]) == int(flag.sum())
+
+
+def test_largest_contraction(sdc):
+    # the largest K the kernel accepts (2^20), where the rounding bound is at its loosest
+    # (g = K 2^-22 = 1/4): one tile, rows and columns, against the oracle
+    M, N, K = 128, 256, 1 << 20
+    ops = W.gemm_operands(M, N, K, DEV, seed=41)
+    g = sdc.AbftGemm(M, N, K, DEV, columns=True)
+    g(ops["A"], ops["W"])
+    torch.cuda.synchronize()
+    Ab, Wb = _bits(ops["A"]), _bits(ops["W"])
+    del ops
+    _check_clean(g, Ab, Wb, M, N, K)
+    cs = g.colsum.cpu().numpy()
+    v = oracle.abft_verify_cols(cs, Ab, Wb)
+    assert v["n_flagged"] == 0 and int(g.summary[1]) == 0 and np.all(g.flag_col.cpu().numpy() == 0)

@@ -187,3 +187,27 @@ def test_counters_reset_between_calls(sdc):
         torch.cuda.synchronize()
         assert int(a.aborted[0]) == 0 and int(a.summary[0]) == 0
         _check_against_oracle(sdc, x, a, causal)
+
+
+def test_long_sequence_sampled_keys(sdc):
+    # one head of 65,536 tokens, causal: 512 key blocks of up to 512 query steps; four key
+    # blocks (first, second, middle, last) against the oracle row by row, and the invariant of
+    # every column (the kernel's column sums of dV against the oracle's bound)
+    L = 1 << 16
+    x = W.attn_inputs(1, L, DEV, seed=38, causal=True)
+    a = _run(sdc, x)
+    assert int(a.aborted[0]) == 0 and int(a.summary[0]) == 0
+    Qb, Kb, dOb = _bits(x["Q"])[0], _bits(x["K"])[0], _bits(x["dO"])[0]
+    lse = x["lse"][0].cpu().numpy()
+    absdo = np.abs(oracle.bf16_to_f64(dOb))
+    eps = _eps(L)
+    dV = a.dV[0].float().cpu().numpy().astype(np.float64)
+    for j0 in (0, 128, L // 2, L - 128):
+        P = oracle.attn_probs(Qb, Kb[j0:j0 + 128], lse, x["scale"], True, key0=j0)  # [L, 128]
+        exact = oracle.attn_dv(P, dOb)
+        e = eps * (P.T @ absdo)
+        tol = 2.0 ** -8 * (np.abs(exact) + e) + e + 2.0 ** -134
+        assert np.all(np.abs(dV[j0:j0 + 128] - exact) <= tol), j0
+    v = oracle.attn_invariant(a.colsum_dv[0].cpu().numpy(), dOb)
+    assert v["n_flagged"] == 0 and np.all(a.flag[0].cpu().numpy() == 0)
+    np.testing.assert_allclose(a.bound[0].cpu().numpy(), v["bound"], rtol=2.0 ** -38)

@@ -151,3 +151,17 @@ def test_flag_rule_edges():
     b = 2.0 ** -100
     v = oracle.attn_invariant(np.array([b, 2 * b, np.nan]), dOb)
     assert list(v["flag"]) == [0, 1, 1]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_probs_of_a_key_block_are_columns_of_the_full_matrix(causal):
+    # a block of keys key0 .. key0 + n - 1 gives exactly those columns of P, causal mask included
+    L, D = 40, 8
+    Qb, Kb, dOb, scale, lse = _inputs(L, D, 7, causal)
+    P = oracle.attn_probs(Qb, Kb, lse, scale, causal)
+    for key0, n in [(0, 8), (13, 9), (32, 8)]:
+        Pb = oracle.attn_probs(Qb, Kb[key0:key0 + n], lse, scale, causal, key0=key0)
+        np.testing.assert_allclose(Pb, P[:, key0:key0 + n], rtol=1e-13, atol=0)
+        np.testing.assert_array_equal(Pb == 0, P[:, key0:key0 + n] == 0)
+        if causal:
+            assert np.all(Pb[:key0] == 0)  # no query before the block attends any of its keys
