@@ -604,7 +604,7 @@ cudaError_t launch_combine(const StatPartial *partials, StatPartial *groups, con
     return cudaGetLastError();
 }
 
-constexpr int kGradUnroll = 4;
+constexpr int kGradUnroll = 16;  // a whole run (kRunVec vectors per lane) in flight
 constexpr int kAvgUnroll = 2;
 
 template <int DT, int NB>
