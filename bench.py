@@ -557,11 +557,8 @@ class E2E:
 
     Each replica's tensors sit back to back (256-byte aligned) in one host buffer
     allocated pinned and one device buffer; a step moves them in 256 MiB copies.
-    The host buffers are written by the CPU, as a caller's host data would be, and
-    end with one sequential CPU rewrite of each whole buffer: on this machine pinned
-    memory last written by a device-to-host copy streams back at ~120 GB/s, filled
-    tensor by tensor at ~150 GB/s, and after a whole-buffer CPU rewrite at the
-    link's full 211 GB/s (measured; set-up, outside the timed region).  The plan
+    The host buffers are written by the CPU, as a caller's host data would be
+    (set-up, outside the timed region).  The host link bounds the rate.  The plan
     covers views of the device buffers."""
 
     def __init__(self, args, reps, sdc, torch):
