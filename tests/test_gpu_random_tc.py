@@ -57,11 +57,13 @@ def test_gemm_random(sdc, case):
         assert vc["n_flagged"] == 0 and int(g.summary[1]) == 0 and np.all(g.flag_col.cpu().numpy() == 0)
 
 
-@pytest.mark.parametrize("case", range(6))
+@pytest.mark.parametrize("case", range(14))
 def test_attention_random(sdc, case):
+    # heads and lengths drawn so that the (head, key block) items range from one to a few
+    # hundred: fewer than, about as many as and several times the persistent grid
     rng = np.random.default_rng(3000 + case)
-    BH = int(rng.integers(1, 4))
-    L = 128 * int(rng.integers(1, 7))
+    BH = int(rng.integers(1, 4)) if case < 6 else int(rng.integers(4, 17))
+    L = 128 * int(rng.integers(1, 7)) if case < 6 else 128 * int(rng.integers(4, 17))
     causal = bool(rng.integers(0, 2))
     x = W.attn_inputs(BH, L, DEV, seed=4000 + case, causal=causal)
     a = sdc.AttnDvCheck(BH, L, DEV)
