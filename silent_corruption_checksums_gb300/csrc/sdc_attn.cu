@@ -103,6 +103,13 @@ static_assert(kAttnSmem <= 232448, "shared memory per block");
 static_assert(kOffBar % 8 == 0, "mbarrier alignment");
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Programmatic dependent launch: the prep kernel lets the dV kernel launch at once, and the dV
+// kernel's threads that read the prep's results (lse log2(e), dO's column sums) wait for the prep
+// grid to complete first; its other work (TMEM, barriers, the K and Q copies) overlaps the prep's tail.
+// Without a dependent launch the wait returns at once.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -226,6 +233,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (warp == 0) {
         if (lane == 0) {  // ------------------------------------------ work queue + TMA
             uint32_t nk = 0, tl = 0, tq = 0;  // K tiles and steps whose copies were issued
+            bool prep_done = false;           // the prep grid's lse log2(e) is complete
             for (uint32_t i = 0; ok; ++i) {
                 const uint32_t slot = i % kItemSlots;
                 if (i >= kItemSlots && !mbar_wait(BAR(kBarIE + slot), ((i / kItemSlots) - 1) & 1)) {
@@ -254,6 +262,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     if (g >= kLStages && !mbar_wait(BAR(kBarLE + ls), ((g / kLStages) - 1) & 1)) {
                         ok = false;
                         break;
+                    }
+                    if (!prep_done) {
+                        grid_dep_wait();
+                        prep_done = true;
                     }
                     mbar_arrive_expect_tx(BAR(kBarLF + ls), kBlk * 4);
                     bulk_g2s(s0 + kOffLse + ls * kBlk * 4, lse2 + (uint64_t)row0 + qb * kBlk, kBlk * 4,
@@ -403,6 +415,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         float *scr = (float *)(sm + kOffScr) + (warp - kEpiBase) * 32 * kScrPitch;
         float2 *cpart = (float2 *)(sm + kOffCp);  // [lane quarter][column]
         volatile uint32_t *last = (volatile uint32_t *)(sm + kOffFlag);
+        grid_dep_wait();  // the head invariant reads the prep grid's column sums of dO
         for (uint32_t i = 0;; ++i) {
             const uint32_t slot = i % kItemSlots;
             bool got = mbar_wait(BAR(kBarIF + slot), (i / kItemSlots) & 1);
@@ -565,6 +578,7 @@ __global__ void __launch_bounds__(256) attn_do_prep_kernel(const __nv_bfloat16 *
                                                            const float *__restrict__ lse, uint32_t L,
                                                            float4 *__restrict__ part_do, float *__restrict__ lse2) {
     __shared__ __align__(16) uint16_t tile[kBlk][kHD];
+    grid_dep_launch();  // the dV kernel may start its set-up now
     const uint32_t qb = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
     const uint64_t row0 = (uint64_t)bh * L + (uint64_t)qb * kBlk;
     if (tid < kBlk) lse2[row0 + tid] = lse[row0 + tid] * kLog2e;  // the exponent's offset in base 2
@@ -682,8 +696,19 @@ sdc_status sdc_attn_dv_check(const void *d_Q, const void *d_K, const void *d_dO,
     const uint32_t nb = L / kBlk;
     const AttnOut out{d_colsum_dv, d_colsum_do, d_residual, d_bound, d_flag, d_summary, d_aborted, tol_scale};
     attn_do_prep_kernel<<<dim3(nb, BH), 256, 0, s>>>((const __nv_bfloat16 *)d_dO, d_lse, L, pdo, lse2);
-    attn_dv_kernel<<<grid, kAttnThreads, kAttnSmem, s>>>(mapQ, mapK, mapDo, lse2, L, BH, scale * kLog2e, causal,
-                                                        (__nv_bfloat16 *)d_dV, pdv, pdo, out, err, ctr);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kAttnThreads);
+    cfg.dynamicSmemBytes = kAttnSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start before the prep completes
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, attn_dv_kernel, mapQ, mapK, mapDo, (const float *)lse2, L, BH, scale * kLog2e, causal,
+                           (__nv_bfloat16 *)d_dV, pdv, (const float4 *)pdo, out, err, ctr);
+    if (e != cudaSuccess) return cuda_fail(e, "sdc_attn_dv_check launch");
     e = cudaGetLastError();
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_attn_dv_check launch");
 }
