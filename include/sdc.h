@@ -345,6 +345,25 @@ sdc_status sdc_attn_dv_check(const void *d_Q, const void *d_K, const void *d_dO,
                              uint8_t *d_flag, sdc_abft_summary *d_summary, uint32_t *d_aborted, void *d_ws,
                              size_t ws_bytes, sdc_stream_t stream);
 
+/* The same for grouped-query attention: `group` query heads share each K/V
+ * head (group = 1 is sdc_attn_dv_check).  BH query heads, a multiple of
+ * group; query head h uses K/V head h / group.  d_Q, d_dO bf16 [BH][L][D] and
+ * d_lse float [BH][L] as above; d_K bf16 [BH / group][L][D].  dV of a K/V head
+ * sums over its group's query heads, as the backward of grouped attention
+ * does: d_dV[v] = sum over h in v's group of P_h^T dO_h (bf16 [BH / group][L][D],
+ * float32 accumulation over group * L query rows).  Per K/V head v and column c:
+ *   d_colsum_dv[v][c] = sum_j of dV's float32 accumulator [j][c],
+ *   d_colsum_do[v][c] = sum over h in v's group and i of dO_h[i][c],
+ *   d_residual, d_bound, d_flag as above with g = group L 2^-22 and the sum of
+ *     |dO| over the group, all [BH / group][D].
+ * Errors as above; SDC_ERR_BAD_ARG also when group is 0 or does not divide BH.
+ * The workspace is sdc_attn_workspace_size(BH, L, D). */
+sdc_status sdc_attn_dv_check_grouped(const void *d_Q, const void *d_K, const void *d_dO, const float *d_lse,
+                                     uint32_t BH, uint32_t group, uint32_t L, uint32_t D, float scale, uint32_t causal,
+                                     float tol_scale, void *d_dV, double *d_colsum_dv, double *d_colsum_do,
+                                     double *d_residual, double *d_bound, uint8_t *d_flag, sdc_abft_summary *d_summary,
+                                     uint32_t *d_aborted, void *d_ws, size_t ws_bytes, sdc_stream_t stream);
+
 /* ---------------------------------------------------------------- self-test */
 
 /* Self-test of the bounded barrier wait with which the TMA / tensor-core

@@ -292,11 +292,12 @@ def gemm_fault(A: torch.Tensor, rows: list[int], seed: int = 7, mask: int = 0x40
 ATTN_8B = (32, 4096)  # heads, tokens (head dimension 128)
 
 
-def attn_inputs(BH: int, L: int, device, seed: int = 8, causal: bool = True, D: int = 128) -> dict:
-    """Seeded Q, K, dO (bf16 [BH, L, D]) and the forward's float32 log-sum-exp [BH, L]."""
+def attn_inputs(BH: int, L: int, device, seed: int = 8, causal: bool = True, D: int = 128, group: int = 1) -> dict:
+    """Seeded Q, dO (bf16 [BH, L, D]), K (bf16 [BH / group, L, D]: query head h uses
+    K/V head h / group) and the forward's float32 log-sum-exp [BH, L]."""
     gen = generator(seed, device)
     Q = normal((BH, L, D), 1.0, torch.bfloat16, gen, device)
-    K = normal((BH, L, D), 1.0, torch.bfloat16, gen, device)
+    K = normal((BH // group, L, D), 1.0, torch.bfloat16, gen, device)
     dO = normal((BH, L, D), 1.0, torch.bfloat16, gen, device)
     scale = 1.0 / math.sqrt(D)
     lse = torch.empty((BH, L), dtype=torch.float32, device=device)
@@ -304,7 +305,7 @@ def attn_inputs(BH: int, L: int, device, seed: int = 8, causal: bool = True, D: 
     # 4,096 query rows (the whole score matrix of a head would not fit)
     rows = L if L <= 8192 else 4096
     for h in range(BH):
-        Kf = K[h].float()
+        Kf = K[h // group].float()
         for r0 in range(0, L, rows):
             s = (Q[h, r0:r0 + rows].float() @ Kf.t()) * scale
             if causal:
@@ -312,4 +313,4 @@ def attn_inputs(BH: int, L: int, device, seed: int = 8, causal: bool = True, D: 
                 qs = torch.arange(r0, min(L, r0 + rows), device=device)[:, None]
                 s.masked_fill_(keys > qs, float("-inf"))
             lse[h, r0:r0 + rows] = torch.logsumexp(s, dim=-1)
-    return {"Q": Q, "K": K, "dO": dO, "lse": lse, "scale": scale, "causal": causal}
+    return {"Q": Q, "K": K, "dO": dO, "lse": lse, "scale": scale, "causal": causal, "group": group}

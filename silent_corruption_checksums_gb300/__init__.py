@@ -101,6 +101,8 @@ def _load() -> ctypes.CDLL:
         "sdc_attn_workspace_size": ([u32, u32, u32], sz),
         "sdc_attn_dv_check": ([vp, vp, vp, vp, u32, u32, u32, ctypes.c_float, u32, ctypes.c_float, vp, vp, vp, vp,
                                vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
+        "sdc_attn_dv_check_grouped": ([vp, vp, vp, vp, u32, u32, u32, u32, ctypes.c_float, u32, ctypes.c_float, vp, vp,
+                                       vp, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
         "sdc_selftest_bounded_wait": ([u32, vp, vp], ctypes.c_int),
         "sdc_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "sdc_last_error": ([], ctypes.c_char_p),
@@ -274,6 +276,16 @@ def sdc_attn_dv_check(d_Q: int, d_K: int, d_dO: int, d_lse: int, BH: int, L: int
     _check("sdc_attn_dv_check", _lib.sdc_attn_dv_check(d_Q, d_K, d_dO, d_lse, BH, L, D, scale, causal, tol_scale,
                                                        d_dV, d_colsum_dv, d_colsum_do, d_residual, d_bound, d_flag,
                                                        d_summary, d_aborted, d_ws, ws_bytes, stream))
+
+
+def sdc_attn_dv_check_grouped(d_Q: int, d_K: int, d_dO: int, d_lse: int, BH: int, group: int, L: int, D: int,
+                              scale: float, causal: int, tol_scale: float, d_dV: int, d_colsum_dv: int,
+                              d_colsum_do: int, d_residual: int, d_bound: int, d_flag: int, d_summary: int,
+                              d_aborted: int, d_ws: int, ws_bytes: int, stream: int) -> None:
+    _check("sdc_attn_dv_check_grouped",
+           _lib.sdc_attn_dv_check_grouped(d_Q, d_K, d_dO, d_lse, BH, group, L, D, scale, causal, tol_scale, d_dV,
+                                          d_colsum_dv, d_colsum_do, d_residual, d_bound, d_flag, d_summary, d_aborted,
+                                          d_ws, ws_bytes, stream))
 
 
 def sdc_selftest_bounded_wait(polls: int, d_status: int, stream: int) -> None:
@@ -572,33 +584,40 @@ class AbftGemm:
 
 class AttnDvCheck:
     """The dV half of the attention backward with the invariant 1^T dV = 1^T dO.
-    Q, K, dO: bf16 [BH, L, 128] contiguous CUDA tensors; lse: float32 [BH, L], the
-    forward's log-sum-exp.  Outputs and scratch are allocated once per shape."""
+    Q, dO: bf16 [BH, L, 128] contiguous CUDA tensors; lse: float32 [BH, L], the
+    forward's log-sum-exp; K: bf16 [BH / group, L, 128] (group query heads per K/V
+    head; 1: plain multi-head attention).  dV and the per-column results are per
+    K/V head.  Outputs and scratch are allocated once per shape."""
 
-    def __init__(self, BH: int, L: int, device, D: int = 128):
+    def __init__(self, BH: int, L: int, device, D: int = 128, group: int = 1):
         torch = _torch()
-        self.BH, self.L, self.D = BH, L, D
-        self.dV = torch.empty((BH, L, D), dtype=torch.bfloat16, device=device)
+        if group < 1 or BH % group:
+            raise ValueError("group must divide BH")
+        self.BH, self.L, self.D, self.group = BH, L, D, group
+        kv = BH // group
+        self.dV = torch.empty((kv, L, D), dtype=torch.bfloat16, device=device)
         f64 = dict(dtype=torch.float64, device=device)
-        self.colsum_dv = torch.empty((BH, D), **f64)
-        self.colsum_do = torch.empty((BH, D), **f64)
-        self.residual = torch.empty((BH, D), **f64)
-        self.bound = torch.empty((BH, D), **f64)
-        self.flag = torch.empty((BH, D), dtype=torch.uint8, device=device)
+        self.colsum_dv = torch.empty((kv, D), **f64)
+        self.colsum_do = torch.empty((kv, D), **f64)
+        self.residual = torch.empty((kv, D), **f64)
+        self.bound = torch.empty((kv, D), **f64)
+        self.flag = torch.empty((kv, D), dtype=torch.uint8, device=device)
         self.summary = torch.zeros(2, dtype=torch.int32, device=device)
         self.aborted = torch.zeros(1, dtype=torch.int32, device=device)
         self.ws_bytes = sdc_attn_workspace_size(BH, L, D)
         self.ws = _ws(self.ws_bytes, device)
 
     def __call__(self, Q, K, dO, lse, scale: float, causal: bool, tol_scale: float = 1.0, stream=None):
-        for t in (Q, K, dO):
+        for t in (Q, dO):
             if tuple(t.shape) != (self.BH, self.L, self.D):
-                raise ValueError(f"expected [{self.BH}, {self.L}, {self.D}] tensors")
-        sdc_attn_dv_check(Q.data_ptr(), K.data_ptr(), dO.data_ptr(), lse.data_ptr(), self.BH, self.L, self.D,
-                          scale, int(bool(causal)), tol_scale, self.dV.data_ptr(), self.colsum_dv.data_ptr(),
-                          self.colsum_do.data_ptr(), self.residual.data_ptr(), self.bound.data_ptr(),
-                          self.flag.data_ptr(), self.summary.data_ptr(), self.aborted.data_ptr(),
-                          self.ws.data_ptr(), self.ws_bytes, _stream_handle(stream))
+                raise ValueError(f"expected [{self.BH}, {self.L}, {self.D}] Q and dO")
+        if tuple(K.shape) != (self.BH // self.group, self.L, self.D):
+            raise ValueError(f"expected K [{self.BH // self.group}, {self.L}, {self.D}]")
+        sdc_attn_dv_check_grouped(Q.data_ptr(), K.data_ptr(), dO.data_ptr(), lse.data_ptr(), self.BH, self.group,
+                                  self.L, self.D, scale, int(bool(causal)), tol_scale, self.dV.data_ptr(),
+                                  self.colsum_dv.data_ptr(), self.colsum_do.data_ptr(), self.residual.data_ptr(),
+                                  self.bound.data_ptr(), self.flag.data_ptr(), self.summary.data_ptr(),
+                                  self.aborted.data_ptr(), self.ws.data_ptr(), self.ws_bytes, _stream_handle(stream))
         return self.dV
 
 

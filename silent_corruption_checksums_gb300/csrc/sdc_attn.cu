@@ -10,19 +10,23 @@
 // anywhere along that chain that breaks the row sums also breaks the
 // invariant.  AEGIS takes both sides' column sums from float32 accumulators.
 //
-// Per head (BH heads of L tokens, head dimension 128, Q/K/dO/dV bf16
-// [BH][L][128], the forward's natural-log log-sum-exp float32 [BH][L]):
-//   P[i, j] = exp(scale q_i . k_j - lse_i)   (0 for j > i when causal)
-//   dV[j, :] = sum_i P[i, j] dO[i, :]        (P rounded to bf16, fp32 accumulate)
-//   invariant per column c: sum_j dV_acc[j, c]  vs  sum_i dO[i, c].
+// Per head (BH query heads of L tokens, head dimension 128, Q/dO bf16
+// [BH][L][128], the forward's natural-log log-sum-exp float32 [BH][L]; K/dV
+// bf16 [BH / group][L][128], query head h using K/V head h / group):
+//   P_h[i, j] = exp(scale q_i . k_j - lse_i)          (0 for j > i when causal)
+//   dV[j, :] = sum over the group's heads h and queries i of P_h[i, j] dO_h[i, :]
+//                                                      (P rounded to bf16, fp32 accumulate)
+//   invariant per K/V head and column c: sum_j dV_acc[j, c]  vs  sum_h sum_i dO_h[i, c]
+//   (every row of every P_h sums to 1).  group = 1 is plain multi-head attention.
 //
 // Kernels:
 //   attn_do_prep_kernel -- lse log2(e), and float32-pair column sums of dO
 //     and |dO| per 128-row block (dO itself feeds the dV product as it is:
 //     its B operand, MN-major);
 //   attn_dv_kernel -- persistent, one CTA per SM; a work item is one
-//     (head, 128-key block), taken from a counter heaviest first (causal:
-//     key block 0 of every head first).  24 warps:
+//     (K/V head, 128-key block), taken from a counter heaviest first (causal:
+//     key block 0 of every head first), its steps running over the query
+//     blocks of each of the group's query heads in turn.  24 warps:
 //     warp 0 lane 0: the work queue and the K, Q and lse copies -- claims
 //       the next item, hands it to the other roles through a 4-slot ring,
 //       copies its K tile into one of two K stages (so the next item's K
@@ -138,22 +142,41 @@ struct AttnOut {
     uint32_t *aborted;
     float tol_scale;
 };
-__device__ void head_invariant(const float2 *part_dv, const float4 *part_do, uint32_t bh, uint32_t c, uint32_t nb,
-                               uint32_t L, const AttnOut &o) {
+__device__ void head_invariant(const float2 *part_dv, const float4 *part_do, uint32_t kvh, uint32_t c, uint32_t nb,
+                               uint32_t group, uint32_t L, const AttnOut &o) {
     float vs = 0.0f, vc = 0.0f, os = 0.0f, oc = 0.0f, as = 0.0f, ac = 0.0f;
+    // L2 reads: other blocks wrote these partials
+    if (group == 1) {  // one pass over the key blocks: both partials of block b together
 #pragma unroll 8
-    for (uint32_t b = 0; b < nb; ++b) {  // L2 reads: other blocks wrote these partials
-        const float2 pv = __ldcg(part_dv + ((uint64_t)bh * nb + b) * kHD + c);
-        const float4 po = __ldcg(part_do + ((uint64_t)bh * nb + b) * kHD + c);
-        pair_merge(vs, vc, pv.x, pv.y);
-        pair_merge(os, oc, po.x, po.y);
-        pair_merge(as, ac, po.z, po.w);
+        for (uint32_t b = 0; b < nb; ++b) {
+            const float2 pv = __ldcg(part_dv + ((uint64_t)kvh * nb + b) * kHD + c);
+            const float4 po = __ldcg(part_do + ((uint64_t)kvh * nb + b) * kHD + c);
+            pair_merge(vs, vc, pv.x, pv.y);
+            pair_merge(os, oc, po.x, po.y);
+            pair_merge(as, ac, po.z, po.w);
+        }
+    } else {  // dV's key blocks, then the group's query heads, each over its query blocks, in order
+#pragma unroll 8
+        for (uint32_t b = 0; b < nb; ++b) {
+            const float2 pv = __ldcg(part_dv + ((uint64_t)kvh * nb + b) * kHD + c);
+            pair_merge(vs, vc, pv.x, pv.y);
+        }
+        for (uint32_t h = 0; h < group; ++h) {
+            const float4 *pd = part_do + (uint64_t)(kvh * group + h) * nb * kHD + c;
+#pragma unroll 8
+            for (uint32_t b = 0; b < nb; ++b) {
+                const float4 po = __ldcg(pd + (uint64_t)b * kHD);
+                pair_merge(os, oc, po.x, po.y);
+                pair_merge(as, ac, po.z, po.w);
+            }
+        }
     }
     const double dv = (double)vs + (double)vc, dsum = (double)os + (double)oc, dabs = (double)as + (double)ac;
-    const double g = (double)L * 0x1p-22, rho = 1.0 + 0x1p-7;
+    // dV's accumulation runs over the group's group * L query rows
+    const double g = (double)group * (double)L * 0x1p-22, rho = 1.0 + 0x1p-7;
     const double bnd = (0x1p-8 * rho + g * (1.0 + g) * rho + 0x1p-40) * dabs + 0x1p-100;
     const double d = dv - dsum;
-    const uint32_t i = bh * kHD + c;
+    const uint32_t i = kvh * kHD + c;
     o.colsum_dv[i] = dv;
     o.colsum_do[i] = dsum;
     o.residual[i] = d;
@@ -163,19 +186,20 @@ __device__ void head_invariant(const float2 *part_dv, const float4 *part_do, uin
     if (f) atomicAdd(&o.summary->n_flagged, 1u);
 }
 
-// Persistent: one CTA per SM takes (head, key block) items from a counter, heaviest first (item w:
-// key block w / BH of head w % BH; when causal, key block kb meets nkb - kb query blocks).
+// Persistent: one CTA per SM takes (K/V head, key block) items from a counter, heaviest first (item
+// w: key block w / n_kv of K/V head w % n_kv; when causal, key block kb meets nkb - kb query blocks
+// of each of the group's query heads kvh * group .. kvh * group + group - 1, taken head by head).
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_dv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                    const __grid_constant__ CUtensorMap mapDo, const float *__restrict__ lse2, uint32_t L,
-                   uint32_t BH, float scale_log2, uint32_t causal, __nv_bfloat16 *__restrict__ dV,
+                   uint32_t n_kv, uint32_t group, float scale_log2, uint32_t causal, __nv_bfloat16 *__restrict__ dV,
                    float2 *__restrict__ part_dv, const float4 *__restrict__ part_do, const AttnOut out,
                    int *__restrict__ err, uint32_t *__restrict__ ctr) {
     // ctr: [0] the work counter, [1] blocks finished, [3 + h] key blocks of head h finished
     uint32_t *next_item = ctr;
     extern __shared__ __align__(1024) unsigned char smem[];
     const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
-    const uint32_t nkb = L / kBlk, n_items = BH * nkb;
+    const uint32_t nkb = L / kBlk, n_items = n_kv * nkb;
     const uint32_t base = smem_addr(smem), pad = ((base + 1023u) & ~1023u) - base;
     unsigned char *sm = smem + pad;
     const uint32_t s0 = base + pad;
@@ -245,19 +269,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 items[slot] = w;
                 mbar_arrive(BAR(kBarIF + slot));  // release: the readers see the slot after their wait
                 if (w == kNoItem) break;
-                const uint32_t kb = w / BH, bh = w % BH, q_first = causal ? kb : 0u, nq = nkb - q_first;
-                const uint32_t row0 = bh * L;
+                const uint32_t kb = w / n_kv, kvh = w % n_kv, q_first = causal ? kb : 0u, nq = nkb - q_first;
                 const uint32_t ks = i % kKStages, sK = s0 + kOffK + ks * kTile;
                 if (i >= kKStages && !mbar_wait(BAR(kBarKE + ks), ((i / kKStages) - 1) & 1)) {
                     ok = false;
                     break;
                 }
                 mbar_arrive_expect_tx(BAR(kBarKF + ks), kTile);
-                tma_load_2d(sK, &mapK, 0, (int32_t)(row0 + kb * kBlk), BAR(kBarKF + ks));
-                tma_load_2d(sK + kHalf, &mapK, 64, (int32_t)(row0 + kb * kBlk), BAR(kBarKF + ks));
+                tma_load_2d(sK, &mapK, 0, (int32_t)(kvh * L + kb * kBlk), BAR(kBarKF + ks));
+                tma_load_2d(sK + kHalf, &mapK, 64, (int32_t)(kvh * L + kb * kBlk), BAR(kBarKF + ks));
                 nk = i + 1;
-                for (uint32_t t = 0; t < nq; ++t) {
-                    const uint32_t g = tl, qb = q_first + t;
+                uint32_t qb = q_first, row0 = kvh * group * L;  // the step's query block and head's first row
+                for (uint32_t t = 0; t < group * nq; ++t, ++qb) {
+                    if (qb == nkb) {  // the next query head of the group
+                        qb = q_first;
+                        row0 += L;
+                    }
+                    const uint32_t g = tl;
                     const uint32_t ls = g % kLStages, qs = g % kQStages;
                     if (g >= kLStages && !mbar_wait(BAR(kBarLE + ls), ((g / kLStages) - 1) & 1)) {
                         ok = false;
@@ -303,9 +331,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const uint32_t w = items[slot];
                 mbar_arrive(BAR(kBarIE + slot));
                 if (w == kNoItem) break;
-                const uint32_t kb = w / BH, bh = w % BH, q_first = causal ? kb : 0u, nq = nkb - q_first;
-                for (uint32_t t = 0; t < nq; ++t) {
-                    const uint32_t g = td, qb = q_first + t, ds = g % kDStages, sDo = s0 + kOffD + ds * kTile;
+                const uint32_t kb = w / n_kv, kvh = w % n_kv, q_first = causal ? kb : 0u, nq = nkb - q_first;
+                uint32_t qb = q_first, row0 = kvh * group * L;
+                for (uint32_t t = 0; t < group * nq; ++t, ++qb) {
+                    if (qb == nkb) {
+                        qb = q_first;
+                        row0 += L;
+                    }
+                    const uint32_t g = td, ds = g % kDStages, sDo = s0 + kOffD + ds * kTile;
                     if (g >= kDStages && !mbar_wait(BAR(kBarDE + ds), ((g / kDStages) - 1) & 1)) {
                         ok = false;
                         break;
@@ -313,8 +346,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     mbar_arrive_expect_tx(BAR(kBarDF + ds), kTile);
                     // the step's 128 rows of dO, head dimensions 0-63 then 64-127: K rows of the
                     // MN-major B operand
-                    tma_load_2d(sDo, &mapDo, 0, (int32_t)(bh * L + qb * kBlk), BAR(kBarDF + ds));
-                    tma_load_2d(sDo + kHalf, &mapDo, 64, (int32_t)(bh * L + qb * kBlk), BAR(kBarDF + ds));
+                    tma_load_2d(sDo, &mapDo, 0, (int32_t)(row0 + qb * kBlk), BAR(kBarDF + ds));
+                    tma_load_2d(sDo + kHalf, &mapDo, 64, (int32_t)(row0 + qb * kBlk), BAR(kBarDF + ds));
                     td = g + 1;
                 }
             }
@@ -335,7 +368,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const uint32_t w = items[slot];
                 mbar_arrive(BAR(kBarIE + slot));
                 if (w == kNoItem) break;
-                const uint32_t kb = w / BH, nq = nkb - (causal ? kb : 0u);
+                const uint32_t kb = w / n_kv, nq = group * (nkb - (causal ? kb : 0u));
                 const uint32_t ks = i % kKStages, sK = s0 + kOffK + ks * kTile;
                 if (!mbar_wait(BAR(kBarKF + ks), (i / kKStages) & 1)) {
                     ok = false;
@@ -379,7 +412,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const uint32_t w = items[slot];
                 mbar_arrive(BAR(kBarIE + slot));
                 if (w == kNoItem) break;
-                const uint32_t kb = w / BH, nq = nkb - (causal ? kb : 0u), db = i % kDvBufs;
+                const uint32_t kb = w / n_kv, nq = group * (nkb - (causal ? kb : 0u)), db = i % kDvBufs;
                 if (i >= kDvBufs && !mbar_wait(BAR(kBarVE + db), ((i / kDvBufs) - 1) & 1)) {  // its last reader
                     ok = false;
                     break;
@@ -427,14 +460,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(kBarIE + slot));
             if (w == kNoItem) break;
-            const uint32_t kb = w / BH, bh = w % BH, db = i % kDvBufs;
+            const uint32_t kb = w / n_kv, kvh = w % n_kv, db = i % kDvBufs;
             got = mbar_wait(BAR(kBarVF + db), (i / kDvBufs) & 1);
             if (bar_any(2, 32 * kEpiWarps, !got)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            __nv_bfloat16 *drow = dV + ((uint64_t)bh * L + kb * kBlk + j) * kHD;
+            __nv_bfloat16 *drow = dV + ((uint64_t)kvh * L + kb * kBlk + j) * kHD;
 #pragma unroll 1
             for (uint32_t cc = 0; cc < kHD / 32; ++cc) {
                 uint32_t r[32];
@@ -470,17 +503,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 float2 a = cpart[c];
 #pragma unroll
                 for (uint32_t q = 1; q < 4; ++q) pair_merge(a.x, a.y, cpart[q * kHD + c].x, cpart[q * kHD + c].y);
-                part_dv[((uint64_t)bh * nkb + kb) * kHD + c] = a;
+                part_dv[((uint64_t)kvh * nkb + kb) * kHD + c] = a;
             }
             // the item that completes its head (the head's last key block to finish, in any block)
             // finishes the head's invariant
             __threadfence();
             named_bar_sync(2, 32 * kEpiWarps);
-            if (c == 0) *last = atomicAdd(ctr + 3 + bh, 1u) == nkb - 1 ? 1u : 0u;
+            if (c == 0) *last = atomicAdd(ctr + 3 + kvh, 1u) == nkb - 1 ? 1u : 0u;
             named_bar_sync(2, 32 * kEpiWarps);
             if (*last) {
                 __threadfence();
-                head_invariant(part_dv, part_do, bh, c, nkb, L, out);
+                head_invariant(part_dv, part_do, kvh, c, nkb, group, L, out);
             }
         }
         if (!ok && lane == 0) atomicOr(err, 1);
@@ -501,9 +534,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(kBarIE + slot));
             if (w == kNoItem) break;
-            const uint32_t kb = w / BH, q_first = causal ? kb : 0u, nq = nkb - q_first;
-            for (uint32_t t = 0; t < nq; ++t, ++g) {
-                const uint32_t ls = g % kLStages, b = g % kSBufs, qb = q_first + t;
+            const uint32_t kb = w / n_kv, q_first = causal ? kb : 0u, nq = nkb - q_first;
+            uint32_t qb = q_first;
+            for (uint32_t t = 0; t < group * nq; ++t, ++g, ++qb) {
+                if (qb == nkb) qb = q_first;  // the next query head of the group
+                const uint32_t ls = g % kLStages, b = g % kSBufs;
                 // the step's log-sum-exps (copied steps ahead) first, then the scores: the wait that
                 // blocks comes last, so nothing stands between the scores' arrival and their use
                 bool got = mbar_wait(BAR(kBarLF + ls), (g / kLStages) & 1);
@@ -642,15 +677,17 @@ size_t sdc_attn_workspace_size(uint32_t BH, uint32_t L, uint32_t D) {
     return attn_ws(BH, L).total;
 }
 
-sdc_status sdc_attn_dv_check(const void *d_Q, const void *d_K, const void *d_dO, const float *d_lse, uint32_t BH,
-                             uint32_t L, uint32_t D, float scale, uint32_t causal, float tol_scale, void *d_dV,
-                             double *d_colsum_dv, double *d_colsum_do, double *d_residual, double *d_bound,
-                             uint8_t *d_flag, sdc_abft_summary *d_summary, uint32_t *d_aborted, void *d_ws,
-                             size_t ws_bytes, sdc_stream_t stream) {
+sdc_status sdc_attn_dv_check_grouped(const void *d_Q, const void *d_K, const void *d_dO, const float *d_lse,
+                                     uint32_t BH, uint32_t group, uint32_t L, uint32_t D, float scale, uint32_t causal,
+                                     float tol_scale, void *d_dV, double *d_colsum_dv, double *d_colsum_do,
+                                     double *d_residual, double *d_bound, uint8_t *d_flag, sdc_abft_summary *d_summary,
+                                     uint32_t *d_aborted, void *d_ws, size_t ws_bytes, sdc_stream_t stream) {
     if (!d_Q || !d_K || !d_dO || !d_lse) return fail(SDC_ERR_NULL, "NULL input");
     if (D != kHD) return fail(SDC_ERR_BAD_ARG, "the head dimension D must be 128");
     if (BH == 0 || L == 0 || L % kBlk || (uint64_t)BH * L >= (1ull << 31) || (uint64_t)BH * kHD >= (1ull << 31))
         return fail(SDC_ERR_BAD_ARG, "L must be a positive multiple of 128 and BH * L below 2^31");
+    if (group == 0 || BH % group) return fail(SDC_ERR_BAD_ARG, "group must divide BH");
+    const uint32_t n_kv = BH / group;  // K/V heads
     if (!(scale > 0.0f) || !(scale < 3.0e38f)) return fail(SDC_ERR_BAD_ARG, "scale must be positive and finite");
     if (!(tol_scale > 0.0f)) return fail(SDC_ERR_BAD_ARG, "tol_scale must be positive");
     if (causal > 1) return fail(SDC_ERR_BAD_ARG, "causal must be 0 or 1");
@@ -659,11 +696,11 @@ sdc_status sdc_attn_dv_check(const void *d_Q, const void *d_K, const void *d_dO,
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    const uint64_t tbytes = (uint64_t)BH * L * kHD * 2;
+    const uint64_t tbytes = (uint64_t)BH * L * kHD * 2, kvbytes = (uint64_t)n_kv * L * kHD * 2;
     sdc_status st = check_device_range(d_Q, tbytes, dev, "d_Q");
-    if (st == SDC_OK) st = check_device_range(d_K, tbytes, dev, "d_K");
+    if (st == SDC_OK) st = check_device_range(d_K, kvbytes, dev, "d_K");
     if (st == SDC_OK) st = check_device_range(d_dO, tbytes, dev, "d_dO");
-    if (st == SDC_OK) st = check_device_range(d_dV, tbytes, dev, "d_dV");
+    if (st == SDC_OK) st = check_device_range(d_dV, kvbytes, dev, "d_dV");
     if (st == SDC_OK) st = check_device_range(d_lse, (uint64_t)BH * L * 4, dev, "d_lse");
     if (st != SDC_OK) return st;
     if (((uint64_t)d_Q | (uint64_t)d_K | (uint64_t)d_dO | (uint64_t)d_dV | (uint64_t)d_lse) & 15u)
@@ -678,7 +715,7 @@ sdc_status sdc_attn_dv_check(const void *d_Q, const void *d_K, const void *d_dO,
     int *err = (int *)((char *)d_ws + w.err);
     CUtensorMap mapQ, mapK, mapDo;
     st = make_map_sw128(&mapQ, d_Q, (uint64_t)BH * L, kHD, kBlk);
-    if (st == SDC_OK) st = make_map_sw128(&mapK, d_K, (uint64_t)BH * L, kHD, kBlk);
+    if (st == SDC_OK) st = make_map_sw128(&mapK, d_K, (uint64_t)n_kv * L, kHD, kBlk);
     if (st == SDC_OK) st = make_map_sw128(&mapDo, d_dO, (uint64_t)BH * L, kHD, kBlk);
     if (st != SDC_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
@@ -686,7 +723,7 @@ sdc_status sdc_attn_dv_check(const void *d_Q, const void *d_K, const void *d_dO,
     int n_sm = 0;
     e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-    const uint32_t n_items = BH * (L / kBlk);
+    const uint32_t n_items = n_kv * (L / kBlk);
     const uint32_t grid = n_items < (uint32_t)n_sm ? n_items : (uint32_t)n_sm;
     e = cudaMemsetAsync(err, 0, 16 + (size_t)BH * 4, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(d_summary, 0, sizeof(sdc_abft_summary), s);
@@ -706,11 +743,21 @@ sdc_status sdc_attn_dv_check(const void *d_Q, const void *d_K, const void *d_dO,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, attn_dv_kernel, mapQ, mapK, mapDo, (const float *)lse2, L, BH, scale * kLog2e, causal,
-                           (__nv_bfloat16 *)d_dV, pdv, (const float4 *)pdo, out, err, ctr);
+    e = cudaLaunchKernelEx(&cfg, attn_dv_kernel, mapQ, mapK, mapDo, (const float *)lse2, L, n_kv, group,
+                           scale * kLog2e, causal, (__nv_bfloat16 *)d_dV, pdv, (const float4 *)pdo, out, err, ctr);
     if (e != cudaSuccess) return cuda_fail(e, "sdc_attn_dv_check launch");
     e = cudaGetLastError();
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_attn_dv_check launch");
+}
+
+sdc_status sdc_attn_dv_check(const void *d_Q, const void *d_K, const void *d_dO, const float *d_lse, uint32_t BH,
+                             uint32_t L, uint32_t D, float scale, uint32_t causal, float tol_scale, void *d_dV,
+                             double *d_colsum_dv, double *d_colsum_do, double *d_residual, double *d_bound,
+                             uint8_t *d_flag, sdc_abft_summary *d_summary, uint32_t *d_aborted, void *d_ws,
+                             size_t ws_bytes, sdc_stream_t stream) {
+    return sdc_attn_dv_check_grouped(d_Q, d_K, d_dO, d_lse, BH, 1, L, D, scale, causal, tol_scale, d_dV, d_colsum_dv,
+                                     d_colsum_do, d_residual, d_bound, d_flag, d_summary, d_aborted, d_ws, ws_bytes,
+                                     stream);
 }
 
 }  // extern "C"

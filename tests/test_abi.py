@@ -140,6 +140,13 @@ def test_host_validation_without_gpu(sdc):
     assert sdc.sdc_attn_workspace_size(2, 256, 128) == (2 * 2 * 128 * 16 + 2 * 2 * 128 * 8 + 2 * 256 * 4 + 256)
     assert sdc.sdc_attn_workspace_size(64, 128, 128) == (64 * 128 * 16 + 64 * 128 * 8 + 64 * 128 * 4 + 512)
     assert sdc.sdc_attn_workspace_size(2, 256, 64) == 0
+    # grouped attention: group 0, or a group that does not divide the query heads, is rejected
+    outs = [4096] * 8
+    for BH, group in [(4, 0), (6, 4), (2, 3)]:
+        with pytest.raises(sdc.SdcError) as ei:
+            sdc.sdc_attn_dv_check_grouped(4096, 8192, 16384, 32768, BH, group, 128, 128, 0.088, 0, 1.0, *outs,
+                                          0, 0, 0)
+        assert ei.value.status == 9, (BH, group)
     assert sdc.sdc_abft_workspace_size(128, 16384, 64) == (64 * 128 * 8 + 4 * 16384 * 8 + 4 * 1024 + 64 * 64 * 16
                                                            + 256)
 

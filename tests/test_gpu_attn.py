@@ -211,3 +211,42 @@ def test_long_sequence_sampled_keys(sdc):
     v = oracle.attn_invariant(a.colsum_dv[0].cpu().numpy(), dOb)
     assert v["n_flagged"] == 0 and np.all(a.flag[0].cpu().numpy() == 0)
     np.testing.assert_allclose(a.bound[0].cpu().numpy(), v["bound"], rtol=2.0 ** -38)
+
+
+@pytest.mark.parametrize("BH,group,L,causal", [(8, 4, 512, True), (8, 4, 384, False), (6, 2, 256, True),
+                                               (8, 8, 256, True)])
+def test_grouped_query_attention(sdc, BH, group, L, causal):
+    # group query heads per K/V head (4: the 8b layout's 32 query heads over 8 K/V heads; 8: one
+    # K/V head): dV of a K/V head sums P_h^T dO_h over its group, and its column sums equal the
+    # group's column sums of dO; the oracle stacks the group's rows of P and of dO
+    x = W.attn_inputs(BH, L, DEV, seed=60 + BH + group + L, causal=causal, group=group)
+    a = sdc.AttnDvCheck(BH, L, DEV, group=group)
+    a(x["Q"], x["K"], x["dO"], x["lse"], x["scale"], causal)
+    torch.cuda.synchronize()
+    assert int(a.aborted[0]) == 0 and int(a.summary[0]) == 0
+    Qb, Kb, dOb = _bits(x["Q"]), _bits(x["K"]), _bits(x["dO"])
+    lse = x["lse"].cpu().numpy()
+    dV = a.dV.float().cpu().numpy().astype(np.float64)
+    eps = _eps(group * L)
+    for v in range(BH // group):
+        heads = range(v * group, (v + 1) * group)
+        P = np.vstack([oracle.attn_probs(Qb[h], Kb[v], lse[h], x["scale"], causal) for h in heads])
+        dOs = np.vstack([dOb[h] for h in heads])
+        exact = oracle.attn_dv(P, dOs)
+        e = eps * (P.T @ np.abs(oracle.bf16_to_f64(dOs)))
+        assert np.all(np.abs(dV[v] - exact) <= 2.0 ** -8 * (np.abs(exact) + e) + e + 2.0 ** -134), v
+        inv = oracle.attn_invariant(a.colsum_dv[v].cpu().numpy(), dOs)
+        assert np.all(np.abs(a.colsum_dv[v].cpu().numpy() - exact.sum(axis=0)) <= inv["bound"]), v
+        np.testing.assert_allclose(a.bound[v].cpu().numpy(), inv["bound"], rtol=2.0 ** -38)
+        absd = np.abs(oracle.bf16_to_f64(dOs)).sum(axis=0)
+        assert np.all(np.abs(a.colsum_do[v].cpu().numpy() - oracle.bf16_to_f64(dOs).sum(axis=0)) <= 2.0 ** -40 * absd)
+        assert inv["n_flagged"] == 0 and np.all(a.flag[v].cpu().numpy() == 0), v
+
+
+def test_grouped_rejects_bad_shapes(sdc):
+    with pytest.raises(ValueError):
+        sdc.AttnDvCheck(6, 128, DEV, group=4)
+    x = W.attn_inputs(4, 128, DEV, seed=64, causal=True, group=2)
+    a = sdc.AttnDvCheck(4, 128, DEV, group=2)
+    with pytest.raises(ValueError):  # K of every query head where the group's K/V heads are expected
+        a(x["Q"], x["Q"], x["dO"], x["lse"], x["scale"], True)
