@@ -492,6 +492,21 @@ def bench_attn_row(args, dev, stream, peaks, sdc, W, torch) -> dict:
                               "torch_fused_backward_dq_dk_dv_ms": ms_ref}}
     del a, x, q, k, v, o
     torch.cuda.empty_cache()
+    # the 8b layout's grouped-query form: its 32 query heads over 8 K/V heads, dV per K/V head
+    group = 4
+    x = W.attn_inputs(BH, L, dev, seed=9, causal=True, group=group)
+    a = sdc.AttnDvCheck(BH, L, dev, group=group)
+    ms_g = _time_loop(lambda: a(x["Q"], x["K"], x["dO"], x["lse"], x["scale"], True, stream=stream), reps, stream,
+                      torch)
+    torch.cuda.synchronize()
+    tf_g = flops / (ms_g * 1e-3) / 1e12
+    out["attn_invariant"].update({"grouped_workload": f"{BH} query heads over {BH // group} K/V heads, the same "
+                                                      "shapes and causal mask", "grouped_ms": ms_g,
+                                  "grouped_tflops": tf_g, "grouped_frac_bf16_peak": tf_g / peaks["bf16_tflops"],
+                                  "grouped_clean_columns_flagged": int(a.summary[0]),
+                                  "grouped_aborted": int(a.aborted[0])})
+    del a, x
+    torch.cuda.empty_cache()
     return out
 
 
