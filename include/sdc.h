@@ -273,7 +273,9 @@ size_t sdc_abft_workspace_size(uint32_t M, uint32_t N, uint32_t K);
  * section 2: compare (AB)1 with A(B1), with the checksum taken from the fp32
  * accumulator inside the kernel.  d_A: device bf16 [M][K]; d_W: device bf16
  * [N][K] (both row-major, K contiguous, 16-byte aligned); d_C: device bf16
- * [M][N].  M a multiple of 128, N of 256, K of 64.  d_rowsum: device double
+ * [M][N].  M >= 1; N and K positive multiples of 8 (row strides of 16-byte
+ * multiples), K <= 2^20; tiles past M, N or K are filled with zeros, which add
+ * nothing to C or to a checksum, and only C itself is written.  d_rowsum: device double
  * [M], sum over j of the fp32 accumulator of C[i][j] (float32 pairs per
  * 256-column tile, tile partials added in a fixed order in float64).
  * d_colsum: NULL, or device double [N] for the page's row + column

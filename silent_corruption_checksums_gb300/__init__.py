@@ -528,7 +528,7 @@ class AbftGemm:
     """C = A . W^T on the tensor cores with the per-row accumulator checksum (and,
     with columns=True, the per-column one: the row + column configuration), and
     its check against A (W^T 1) (and (1^T A) W^T).  A: bf16 [M, K], W: bf16 [N, K],
-    both contiguous CUDA tensors; M a multiple of 128, N of 256, K of 64.  Output
+    both contiguous CUDA tensors; M >= 1, N and K multiples of 8, K <= 2^20.  Output
     and scratch buffers are allocated once per shape and reused by every call."""
 
     def __init__(self, M: int, N: int, K: int, device, columns: bool = False):

@@ -76,7 +76,9 @@ constexpr uint32_t kCheckThreads = 64;  // threads per block of the check
 
 // Converts 32 accumulators to bf16 (round to nearest even), stores them at
 // dst (64 bytes, 16-byte aligned) and adds them to the row's pair sum.
-__device__ __forceinline__ void epilogue_chunk(const uint32_t (&r)[32], __nv_bfloat16 *dst, float &s, float &c) {
+// valid: how many of the chunk's 32 columns lie inside C (a multiple of 8; 0 for a row past M)
+__device__ __forceinline__ void epilogue_chunk(const uint32_t (&r)[32], __nv_bfloat16 *dst, float &s, float &c,
+                                               uint32_t valid) {
     uint32_t packed[16];
 #pragma unroll
     for (int j = 0; j < 32; j += 2) {
@@ -87,7 +89,8 @@ __device__ __forceinline__ void epilogue_chunk(const uint32_t (&r)[32], __nv_bfl
     }
     uint4 *d = (uint4 *)dst;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) d[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+    for (uint32_t q = 0; q < 4; ++q)
+        if (8 * q < valid) d[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
 }
 
 // Tile t of the schedule -> (tile row, tile column).  Tiles go in bands of
@@ -165,7 +168,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t full = bars, empty = bars + 8 * kStages, tfull = bars + 16 * kStages, tempty = tfull + 16,
                    done = tempty + 16;
     uint32_t *tmem_slot = (uint32_t *)(smem + pad + kStages * (kStageA + kStageW) + 8 * kNumBars);
-    const uint32_t tiles_m = M / kBM, tiles_n = N / kBN, nkb = K / kBK;
+    // tiles cover C with zeros past M, N and K: the copies fill the rows and columns outside A and
+    // W with zeros, which add nothing to a product or a checksum; the epilogue stores only inside C
+    const uint32_t tiles_m = (M + kBM - 1) / kBM, tiles_n = (N + kBN - 1) / kBN, nkb = (K + kBK - 1) / kBK;
     // work units: tiles, or (with kMc) pairs of vertically adjacent tiles, one per cluster
     const uint32_t rank = kMc ? cluster_rank() : 0u;
     const uint32_t units_m = kMc ? tiles_m / 2 : tiles_m, n_units = units_m * tiles_n;
@@ -278,7 +283,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t tm, tile_n;
             coords(u, tm, tile_n);
             const uint32_t row = tm * kBM + quarter * 32 + lane;
-            __nv_bfloat16 *crow = C + (uint64_t)row * N + (uint64_t)tile_n * kBN;
+            const uint32_t col0 = tile_n * kBN;  // the tile's first column
+            __nv_bfloat16 *crow = C + (uint64_t)row * N + col0;
             const uint32_t acc = tmem + lane_base + b * kAccCols;
             float s = 0.0f, c = 0.0f;
             // column partials of this warp's 32 rows: [4 tile_m + quarter][N]
@@ -288,17 +294,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 tc_ld32(acc + c0, r0);
                 tc_ld32(acc + c0 + 32, r1);
                 tc_wait_ld();
-                epilogue_chunk(r0, crow + c0, s, c);
-                epilogue_chunk(r1, crow + c0 + 32, s, c);
+                // columns of the two chunks inside C (none for a row past M)
+                const uint32_t v0 = row >= M || col0 + c0 >= N ? 0u : min(32u, N - col0 - c0);
+                const uint32_t v1 = row >= M || col0 + c0 + 32 >= N ? 0u : min(32u, N - col0 - c0 - 32);
+                epilogue_chunk(r0, crow + c0, s, c, v0);
+                epilogue_chunk(r1, crow + c0 + 32, s, c, v1);
                 if (kCols) {
-                    cpart[c0] = warp_column_sum(r0, lane, coltile);
-                    cpart[c0 + 32] = warp_column_sum(r1, lane, coltile);
+                    const double cs0 = warp_column_sum(r0, lane, coltile), cs1 = warp_column_sum(r1, lane, coltile);
+                    if (col0 + c0 + lane < N) cpart[c0] = cs0;
+                    if (col0 + c0 + 32 + lane < N) cpart[c0 + 32] = cs1;
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tempty + 8 * b) : "memory");
-            rowsum_part[(uint64_t)tile_n * M + row] = (double)s + (double)c;
+            if (row < M) rowsum_part[(uint64_t)tile_n * M + row] = (double)s + (double)c;
         }
     }
     tc_fence_before();
@@ -451,14 +461,15 @@ __global__ void __launch_bounds__(256) abft_colsum_final_kernel(const float4 *__
 // accumulator checksum, and the flag.  One block of kCheckThreads threads per kCheckRows rows: the threads stride over
 // the 8-column vectors (each column pair loaded once for all the rows), then
 // the pairs are merged across lanes (butterfly) and across warps (in order).
-__global__ void __launch_bounds__(kCheckThreads) abft_check_kernel(const __nv_bfloat16 *__restrict__ A, uint32_t n_sum,
-                                                         uint32_t K, const double *__restrict__ rowsum,
+__global__ void __launch_bounds__(kCheckThreads) abft_check_kernel(const __nv_bfloat16 *__restrict__ A, uint32_t n_rows,
+                                                         uint32_t n_sum, uint32_t K, const double *__restrict__ rowsum,
                                                          const float4 *__restrict__ wsplit, float tol_scale,
                                                          double *__restrict__ residual, double *__restrict__ bound,
                                                          uint8_t *__restrict__ flag, uint32_t *__restrict__ n_flagged) {
     __shared__ float4 red[kCheckThreads / 32][kCheckRows];
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
-    const uint64_t row0 = (uint64_t)blockIdx.x * kCheckRows;  // M is a multiple of 128: all rows exist
+    const uint64_t row0 = (uint64_t)blockIdx.x * kCheckRows;
+    const uint32_t nr = n_rows - (uint32_t)row0 < kCheckRows ? n_rows - (uint32_t)row0 : kCheckRows;  // rows present
     // rows (0, 1) and (2, 3) share packed registers
     uint64_t rs2[kCheckRows / 2], rc2[kCheckRows / 2], ms2[kCheckRows / 2], mc2[kCheckRows / 2];
 #pragma unroll
@@ -466,11 +477,13 @@ __global__ void __launch_bounds__(kCheckThreads) abft_check_kernel(const __nv_bf
     for (uint32_t v = tid; v < K / 8; v += kCheckThreads) {
         if ((lane & 7u) == 0 && v + kCheckThreads < K / 8) {  // the next vectors of every row into L2
 #pragma unroll
-            for (uint32_t r = 0; r < kCheckRows; ++r) prefetch_l2(A + (row0 + r) * K + (uint64_t)(v + kCheckThreads) * 8);
+            for (uint32_t r = 0; r < kCheckRows; ++r)
+                if (r < nr) prefetch_l2(A + (row0 + r) * K + (uint64_t)(v + kCheckThreads) * 8);
         }
         uint4 av[kCheckRows];
 #pragma unroll
-        for (uint32_t r = 0; r < kCheckRows; ++r) av[r] = ld_stream(A + (row0 + r) * K + (uint64_t)v * 8);
+        for (uint32_t r = 0; r < kCheckRows; ++r)
+            av[r] = r < nr ? ld_stream(A + (row0 + r) * K + (uint64_t)v * 8) : make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {  // column 8 v + q
             const float4 w = wsplit[v * 8 + q];
@@ -506,7 +519,7 @@ __global__ void __launch_bounds__(kCheckThreads) abft_check_kernel(const __nv_bf
         if (lane == 0) red[warp][r] = make_float4(rs[r], rc[r], ms[r], mc[r]);
     }
     __syncthreads();
-    if (tid < kCheckRows) {
+    if (tid < nr) {
         float4 p = red[0][tid];
         for (uint32_t w = 1; w < kCheckThreads / 32; ++w) {
             const float4 q = red[w][tid];
@@ -540,7 +553,7 @@ uint32_t n_slabs_for(uint32_t rows, uint32_t K) {
     return n < 1 ? 1 : n;
 }
 
-// Workspace: row partials [N/256][M] | column partials [M/32][N] | W's column sums
+// Workspace: row partials [ceil(N/256)][M] | column partials [4 ceil(M/128)][N] | W's column sums
 // wcol [K] and their pair split wsplit [K] | A's, acol [K] and asplit [K] |
 // slabs [max(n_slabs(N, K), n_slabs(M, K))][K] (used for W, then for A) | abort word.
 struct AbftWs {
@@ -550,8 +563,9 @@ AbftWs abft_ws(uint32_t M, uint32_t N, uint32_t K) {
     AbftWs w;
     const size_t ns = n_slabs_for(N, K) > n_slabs_for(M, K) ? n_slabs_for(N, K) : n_slabs_for(M, K);
     w.part = 0;
-    w.cpart = round_up256((size_t)(N / kBN) * M * sizeof(double));
-    w.wcol = w.cpart + round_up256((size_t)(M / 32) * N * sizeof(double));
+    const size_t tiles_m = (M + kBM - 1) / kBM, tiles_n = (N + kBN - 1) / kBN;
+    w.cpart = round_up256(tiles_n * M * sizeof(double));
+    w.wcol = w.cpart + round_up256(4 * tiles_m * N * sizeof(double));
     w.wsplit = w.wcol + round_up256((size_t)K * sizeof(double2));
     w.acol = w.wsplit + round_up256((size_t)K * sizeof(float4));
     w.asplit = w.acol + round_up256((size_t)K * sizeof(double2));
@@ -574,8 +588,8 @@ size_t sdc_abft_workspace_size(uint32_t M, uint32_t N, uint32_t K) { return abft
 static sdc_status abft_args(const void *d_A, const void *d_W, uint32_t M, uint32_t N, uint32_t K, void *d_ws,
                             size_t ws_bytes, int *dev) {
     if (!d_A || !d_W) return fail(SDC_ERR_NULL, "NULL operand");
-    if (M == 0 || N == 0 || K == 0 || M % kBM || N % kBN || K % kBK || K > kMaxK)
-        return fail(SDC_ERR_BAD_ARG, "M must be a multiple of 128, N of 256 and K of 64 (all > 0, K <= 2^20)");
+    if (M == 0 || N == 0 || K == 0 || N % 8 || K % 8 || K > kMaxK)
+        return fail(SDC_ERR_BAD_ARG, "M must be positive, N and K positive multiples of 8, K <= 2^20");
     cudaError_t e = cudaGetDevice(dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     sdc_status st = check_device_range(d_A, (uint64_t)M * K * 2, *dev, "d_A");
@@ -598,7 +612,7 @@ sdc_status sdc_abft_gemm(const void *d_A, const void *d_W, void *d_C, uint32_t M
     st = check_device_range(d_C, (uint64_t)M * N * 2, dev, "d_C");
     if (st != SDC_OK) return st;
     if ((uint64_t)d_C & 15u) return fail(SDC_ERR_BAD_POINTER, "C must be 16-byte aligned");
-    const uint32_t tiles_m = M / kBM, sms = (uint32_t)sm_count(dev);
+    const uint32_t tiles_m = (M + kBM - 1) / kBM, tiles_n = (N + kBN - 1) / kBN, sms = (uint32_t)sm_count(dev);
     // clusters of two on vertically adjacent tiles (W multicast) when the tile rows pair up
     const bool mc = tiles_m % 2 == 0 && sms >= 2;
     CUtensorMap mapA, mapW;
@@ -617,7 +631,7 @@ sdc_status sdc_abft_gemm(const void *d_A, const void *d_W, void *d_C, uint32_t M
     const uint32_t smem_bytes = cols ? kGemmSmemCols : kGemmSmem;
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_gemm setup");
-    const uint32_t units_m = mc ? tiles_m / 2 : tiles_m, n_units = units_m * (N / kBN);
+    const uint32_t units_m = mc ? tiles_m / 2 : tiles_m, n_units = units_m * tiles_n;
     // one CTA per SM: mc -> one cluster (two CTAs) per SM pair and work unit
     const uint32_t grid = mc ? 2 * (n_units < sms / 2 ? n_units : sms / 2) : (n_units < sms ? n_units : sms);
     // A band of tile rows holds about 24 MiB of A, a fraction of the 126 MiB L2 (in work-unit rows).
@@ -638,8 +652,8 @@ sdc_status sdc_abft_gemm(const void *d_A, const void *d_W, void *d_C, uint32_t M
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, kernel, mapA, mapW, (__nv_bfloat16 *)d_C, M, N, K, band_m, part, cpart, err);
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_gemm launch");
-    abft_sum_parts_kernel<<<(M + 31) / 32, 256, 0, s>>>(part, M, N / kBN, d_rowsum, err, d_aborted);
-    if (cols) abft_sum_parts_kernel<<<(N + 31) / 32, 256, 0, s>>>(cpart, N, M / 32, d_colsum, nullptr, nullptr);
+    abft_sum_parts_kernel<<<(M + 31) / 32, 256, 0, s>>>(part, M, tiles_n, d_rowsum, err, d_aborted);
+    if (cols) abft_sum_parts_kernel<<<(N + 31) / 32, 256, 0, s>>>(cpart, N, 4 * tiles_m, d_colsum, nullptr, nullptr);
     e = cudaGetLastError();
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_abft_gemm launch");
 }
@@ -666,7 +680,8 @@ sdc_status sdc_abft_verify(const void *d_A, const void *d_W, uint32_t M, uint32_
     const uint32_t nsw = n_slabs_for(N, K);
     abft_colsum_slab_kernel<<<dim3((K + 255) / 256, nsw), 256, 0, s>>>((const __nv_bfloat16 *)d_W, N, K, nsw, slabs);
     abft_colsum_final_kernel<<<(K + 31) / 32, 256, 0, s>>>(slabs, K, nsw, wcol, wsplit);
-    abft_check_kernel<<<M / kCheckRows, kCheckThreads, 0, s>>>((const __nv_bfloat16 *)d_A, N, K, d_rowsum, wsplit,
+    abft_check_kernel<<<(M + kCheckRows - 1) / kCheckRows, kCheckThreads, 0, s>>>((const __nv_bfloat16 *)d_A, M, N, K,
+                                                                                d_rowsum, wsplit,
                                                                tol_scale, d_residual, d_bound, d_flag,
                                                                &d_summary->n_flagged);
     if (cols) {  // columns: W (A^T 1) over the M rows each column checksum sums
@@ -674,7 +689,8 @@ sdc_status sdc_abft_verify(const void *d_A, const void *d_W, uint32_t M, uint32_
         abft_colsum_slab_kernel<<<dim3((K + 255) / 256, nsa), 256, 0, s>>>((const __nv_bfloat16 *)d_A, M, K, nsa,
                                                                           slabs);
         abft_colsum_final_kernel<<<(K + 31) / 32, 256, 0, s>>>(slabs, K, nsa, acol, asplit);
-        abft_check_kernel<<<N / kCheckRows, kCheckThreads, 0, s>>>((const __nv_bfloat16 *)d_W, M, K, d_colsum, asplit,
+        abft_check_kernel<<<(N + kCheckRows - 1) / kCheckRows, kCheckThreads, 0, s>>>((const __nv_bfloat16 *)d_W, N, M,
+                                                                                    K, d_colsum, asplit,
                                                                    tol_scale, d_residual_col, d_bound_col, d_flag_col,
                                                                    &d_summary->n_flagged_cols);
     }

@@ -101,20 +101,20 @@ def test_host_validation_without_gpu(sdc):
     with pytest.raises(sdc.SdcError) as ei:
         sdc.sdc_abft_gemm(0, 4096, 8192, 128, 256, 64, 0, 0, 0, 0, 0, 0)
     assert ei.value.status == 1
-    for M, N, K in [(100, 256, 64), (128, 200, 64), (128, 256, 48), (0, 256, 64), (128, 256, (1 << 20) + 64),
-                    (128, 256, 1 << 21)]:
+    for M, N, K in [(100, 260, 64), (128, 200, 60), (0, 256, 64), (128, 0, 64), (128, 256, 0),
+                    (128, 256, (1 << 20) + 8), (128, 256, 1 << 21)]:
         with pytest.raises(sdc.SdcError) as ei:
             sdc.sdc_abft_gemm(4096, 8192, 16384, M, N, K, 0, 0, 0, 0, 0, 0)
         assert ei.value.status == 9, (M, N, K)
         with pytest.raises(sdc.SdcError) as ei:
             sdc.sdc_abft_verify(4096, 8192, M, N, K, 0, 0, 1.0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0)
         assert ei.value.status == 9, (M, N, K)
-    # row partials (N/256 per row), column partials (M/32 per column), W's and A's column sums
+    # row partials (ceil(N/256) per row), column partials (4 ceil(M/128) per column), W's and A's column sums
     # (K float64 pairs) and their float32 pair splits (K x 16 bytes), slabs of K x 16 bytes for the
     # larger of the two column sums (slabs = min(608 / ceil(K / 256), 64, rows / 8)), the abort
     # word; each rounded up to 256 bytes
     assert sdc.sdc_abft_workspace_size(128, 512, 64) == 2048 + 4 * 512 * 8 + 4 * 1024 + 64 * 64 * 16 + 256
-    assert sdc.sdc_abft_workspace_size(1000, 256, 100) == 8192 + 31 * 256 * 8 + 4 * 1792 + 64 * 100 * 16 + 256
+    assert sdc.sdc_abft_workspace_size(1000, 256, 100) == 8192 + 32 * 256 * 8 + 4 * 1792 + 64 * 100 * 16 + 256
     # bounded-wait self-test: arguments checked before the launch
     with pytest.raises(sdc.SdcError) as ei:
         sdc.sdc_selftest_bounded_wait(10, 0, 0)

@@ -211,3 +211,50 @@ def test_largest_contraction(sdc):
     cs = g.colsum.cpu().numpy()
     v = oracle.abft_verify_cols(cs, Ab, Wb)
     assert v["n_flagged"] == 0 and int(g.summary[1]) == 0 and np.all(g.flag_col.cpu().numpy() == 0)
+
+
+RAGGED = [(1, 8, 8), (100, 264, 72), (129, 520, 1000), (200, 776, 4104), (300, 256, 64)]
+
+
+@pytest.mark.parametrize("columns", [False, True])
+@pytest.mark.parametrize("M,N,K", RAGGED)
+def test_ragged_shapes(sdc, M, N, K, columns):
+    # shapes that are not multiples of the 128 x 256 x 64 tiles (any M, N and K multiples of 8): the
+    # copies fill the tiles' rows and columns outside A and W with zeros, the epilogue stores
+    # only inside C; odd and even tile-row counts (with and without the cluster pairs)
+    ops = W.gemm_operands(M, N, K, DEV, seed=70 + M + N + K)
+    g = sdc.AbftGemm(M, N, K, DEV, columns=columns)
+    g(ops["A"], ops["W"])
+    torch.cuda.synchronize()
+    Ab, Wb = _bits(ops["A"]), _bits(ops["W"])
+    _check_clean(g, Ab, Wb, M, N, K)
+    if columns:
+        exact = oracle.abft_product(Ab, Wb)
+        cs = g.colsum.cpu().numpy()
+        v = oracle.abft_verify_cols(cs, Ab, Wb)
+        assert np.all(np.abs(cs - exact.sum(axis=0)) <= v["bound"])
+        assert v["n_flagged"] == 0 and int(g.summary[1]) == 0 and np.all(g.flag_col.cpu().numpy() == 0)
+
+
+@pytest.mark.parametrize("M,N,K", [(100, 264, 72), (129, 520, 1000)])
+def test_ragged_stores_stay_inside_c(sdc, M, N, K):
+    # through the C ABI with C followed by a sentinel region: nothing past M x N is written
+    ops = W.gemm_operands(M, N, K, DEV, seed=80 + M)
+    buf = torch.full((M * N + 8192,), 0x7777, dtype=torch.int16, device=DEV)
+    rowsum = torch.empty(M, dtype=torch.float64, device=DEV)
+    colsum = torch.empty(N, dtype=torch.float64, device=DEV)
+    aborted = torch.zeros(1, dtype=torch.int32, device=DEV)
+    nws = sdc.sdc_abft_workspace_size(M, N, K)
+    ws = torch.empty(nws + 256, dtype=torch.uint8, device=DEV)
+    wsp = (ws.data_ptr() + 255) // 256 * 256
+    sdc.sdc_abft_gemm(ops["A"].data_ptr(), ops["W"].data_ptr(), buf.data_ptr(), M, N, K, rowsum.data_ptr(),
+                      colsum.data_ptr(), aborted.data_ptr(), wsp, nws, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert int(aborted[0]) == 0
+    assert bool((buf[M * N:] == 0x7777).all())
+    g = sdc.AbftGemm(M, N, K, DEV, columns=True)
+    g.gemm(ops["A"], ops["W"])
+    torch.cuda.synchronize()
+    assert torch.equal(buf[:M * N].view(M, N), g.C.view(torch.int16))
+    assert torch.equal(rowsum.view(torch.int64), g.rowsum.view(torch.int64))
+    assert torch.equal(colsum.view(torch.int64), g.colsum.view(torch.int64))
