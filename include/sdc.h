@@ -323,7 +323,8 @@ size_t sdc_attn_workspace_size(uint32_t BH, uint32_t L, uint32_t D);
  * major, 16-byte aligned); d_lse float [BH][L], the forward's natural-log
  * log-sum-exp of scale * q_i . k_j over the keys each query attends; scale
  * (> 0, e.g. 1/sqrt(D)); causal (1: query i attends keys j <= i).  D must be
- * 128 and L a positive multiple of 128.
+ * 128 and L a positive multiple of 4 (the last 128-token block may be
+ * partial: keys and queries past L take no probability).
  * Computes P[i][j] = exp(scale q_i . k_j - lse_i) (bf16 for the product, as a
  * flash-attention backward does), d_dV = P^T dO (bf16 [BH][L][D], float32
  * accumulation on the tensor cores), and per head h and column c:

@@ -57,6 +57,8 @@
 //     bound and the flag; the last block to finish publishes the abort word.
 // Every wait is bounded; a wait that gives up sets the call's abort flag and
 // the block still drains its copies and MMAs (bounded) and frees its TMEM.
+#include <type_traits>
+
 #include "sdc_internal.cuh"
 #include "sdc_tc.cuh"
 
@@ -199,7 +201,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint32_t *next_item = ctr;
     extern __shared__ __align__(1024) unsigned char smem[];
     const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
-    const uint32_t nkb = L / kBlk, n_items = n_kv * nkb;
+    const uint32_t nkb = (L + kBlk - 1) / kBlk, n_items = n_kv * nkb;  // the last block may be partial
     const uint32_t base = smem_addr(smem), pad = ((base + 1023u) & ~1023u) - base;
     unsigned char *sm = smem + pad;
     const uint32_t s0 = base + pad;
@@ -276,14 +278,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     break;
                 }
                 mbar_arrive_expect_tx(BAR(kBarKF + ks), kTile);
-                tma_load_2d(sK, &mapK, 0, (int32_t)(kvh * L + kb * kBlk), BAR(kBarKF + ks));
-                tma_load_2d(sK + kHalf, &mapK, 64, (int32_t)(kvh * L + kb * kBlk), BAR(kBarKF + ks));
+                tma_load_3d(sK, &mapK, 0, (int32_t)(kb * kBlk), (int32_t)kvh, BAR(kBarKF + ks));
+                tma_load_3d(sK + kHalf, &mapK, 64, (int32_t)(kb * kBlk), (int32_t)kvh, BAR(kBarKF + ks));
                 nk = i + 1;
-                uint32_t qb = q_first, row0 = kvh * group * L;  // the step's query block and head's first row
+                uint32_t qb = q_first, qh = kvh * group;  // the step's query block and query head
                 for (uint32_t t = 0; t < group * nq; ++t, ++qb) {
                     if (qb == nkb) {  // the next query head of the group
                         qb = q_first;
-                        row0 += L;
+                        ++qh;
                     }
                     const uint32_t g = tl;
                     const uint32_t ls = g % kLStages, qs = g % kQStages;
@@ -295,8 +297,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         grid_dep_wait();
                         prep_done = true;
                     }
-                    mbar_arrive_expect_tx(BAR(kBarLF + ls), kBlk * 4);
-                    bulk_g2s(s0 + kOffLse + ls * kBlk * 4, lse2 + (uint64_t)row0 + qb * kBlk, kBlk * 4,
+                    // the block's queries inside the sequence (a multiple of 4: 16-byte copies)
+                    const uint32_t lbytes = (L - qb * kBlk < kBlk ? L - qb * kBlk : kBlk) * 4;
+                    mbar_arrive_expect_tx(BAR(kBarLF + ls), lbytes);
+                    bulk_g2s(s0 + kOffLse + ls * kBlk * 4, lse2 + (uint64_t)qh * L + qb * kBlk, lbytes,
                              BAR(kBarLF + ls));
                     tl = g + 1;
                     if (g >= kQStages && !mbar_wait(BAR(kBarQE + qs), ((g / kQStages) - 1) & 1)) {
@@ -305,8 +309,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     }
                     const uint32_t sQ = s0 + kOffQ + qs * kTile;
                     mbar_arrive_expect_tx(BAR(kBarQF + qs), kTile);
-                    tma_load_2d(sQ, &mapQ, 0, (int32_t)(row0 + qb * kBlk), BAR(kBarQF + qs));
-                    tma_load_2d(sQ + kHalf, &mapQ, 64, (int32_t)(row0 + qb * kBlk), BAR(kBarQF + qs));
+                    tma_load_3d(sQ, &mapQ, 0, (int32_t)(qb * kBlk), (int32_t)qh, BAR(kBarQF + qs));
+                    tma_load_3d(sQ + kHalf, &mapQ, 64, (int32_t)(qb * kBlk), (int32_t)qh, BAR(kBarQF + qs));
                     tq = g + 1;
                 }
             }
@@ -332,11 +336,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 mbar_arrive(BAR(kBarIE + slot));
                 if (w == kNoItem) break;
                 const uint32_t kb = w / n_kv, kvh = w % n_kv, q_first = causal ? kb : 0u, nq = nkb - q_first;
-                uint32_t qb = q_first, row0 = kvh * group * L;
+                uint32_t qb = q_first, qh = kvh * group;
                 for (uint32_t t = 0; t < group * nq; ++t, ++qb) {
                     if (qb == nkb) {
                         qb = q_first;
-                        row0 += L;
+                        ++qh;
                     }
                     const uint32_t g = td, ds = g % kDStages, sDo = s0 + kOffD + ds * kTile;
                     if (g >= kDStages && !mbar_wait(BAR(kBarDE + ds), ((g / kDStages) - 1) & 1)) {
@@ -346,8 +350,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     mbar_arrive_expect_tx(BAR(kBarDF + ds), kTile);
                     // the step's 128 rows of dO, head dimensions 0-63 then 64-127: K rows of the
                     // MN-major B operand
-                    tma_load_2d(sDo, &mapDo, 0, (int32_t)(row0 + qb * kBlk), BAR(kBarDF + ds));
-                    tma_load_2d(sDo + kHalf, &mapDo, 64, (int32_t)(row0 + qb * kBlk), BAR(kBarDF + ds));
+                    tma_load_3d(sDo, &mapDo, 0, (int32_t)(qb * kBlk), (int32_t)qh, BAR(kBarDF + ds));
+                    tma_load_3d(sDo + kHalf, &mapDo, 64, (int32_t)(qb * kBlk), (int32_t)qh, BAR(kBarDF + ds));
                     td = g + 1;
                 }
             }
@@ -482,7 +486,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         asm("cvt.rn.bf16x2.f32 %0, %1, %2;"
                             : "=r"(p[k])
                             : "f"(__uint_as_float(r[8 * v + 2 * k + 1])), "f"(__uint_as_float(r[8 * v + 2 * k])));
-                    d[v] = make_uint4(p[0], p[1], p[2], p[3]);
+                    if (kb * kBlk + j < L) d[v] = make_uint4(p[0], p[1], p[2], p[3]);  // keys inside the sequence
                 }
                 // this warp's 32 rows of the chunk's 32 columns, summed in row order (float32 pair)
 #pragma unroll
@@ -535,6 +539,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (lane == 0) mbar_arrive(BAR(kBarIE + slot));
             if (w == kNoItem) break;
             const uint32_t kb = w / n_kv, q_first = causal ? kb : 0u, nq = nkb - q_first;
+            const bool key_ok = kb * kBlk + j < L;  // this thread's key is inside the sequence
             uint32_t qb = q_first;
             for (uint32_t t = 0; t < group * nq; ++t, ++g, ++qb) {
                 if (qb == nkb) qb = q_first;  // the next query head of the group
@@ -549,28 +554,47 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t lsa = s0 + kOffLse + ls * kBlk * 4 + qpart * kQPer * 4;  // lse log2(e) of its queries
+                // steps that need a mask: the causal diagonal block, a partial last query block, a key
+                // past L (a partial last key block)
                 const bool diag = causal && qb == kb;
+                const bool edge = diag || qb * kBlk + kBlk > L || !key_ok;
                 const uint32_t col = tmem + lane_base + kColS + b * kBlk + qpart * kQPer;
                 uint32_t r[kQPer];
 #pragma unroll
                 for (uint32_t c = 0; c < kQPer / 32; ++c) tc_ld32(col + 32 * c, *(uint32_t(*)[32]) & r[32 * c]);
                 tc_wait_ld();
                 uint32_t pw[kQPer / 2];  // this thread's probabilities as bf16 pairs
+                uint32_t mbits = ~0u;    // with a mask: bit q for query qpart * kQPer + q
+                // two copies of the loop, the masked one only for the steps that need it (a mask tested
+                // inside a single loop costs every step)
+                auto probs = [&](auto masked) {
 #pragma unroll
-                for (uint32_t q8 = 0; q8 < kQPer / 8; ++q8) {  // 8 queries at a time
-                    const float4 la = ld_shared_f4(lsa + q8 * 32), lb = ld_shared_f4(lsa + q8 * 32 + 16);
-                    const float l8[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
+                    for (uint32_t q8 = 0; q8 < kQPer / 8; ++q8) {  // 8 queries at a time
+                        const float4 la = ld_shared_f4(lsa + q8 * 32), lb = ld_shared_f4(lsa + q8 * 32 + 16);
+                        const float l8[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
 #pragma unroll
-                    for (uint32_t q = 0; q < 8; q += 2) {
-                        const uint32_t i0 = qpart * kQPer + q8 * 8 + q;  // query within the step
-                        float p0 = ex2(__fmaf_rn(__uint_as_float(r[q8 * 8 + q]), scale_log2, -l8[q]));
-                        float p1 = ex2(__fmaf_rn(__uint_as_float(r[q8 * 8 + q + 1]), scale_log2, -l8[q + 1]));
-                        if (diag) {  // query i attends key j only when i >= j
-                            p0 = i0 >= j ? p0 : 0.0f;
-                            p1 = i0 + 1 >= j ? p1 : 0.0f;
+                        for (uint32_t q = 0; q < 8; q += 2) {
+                            float p0 = ex2(__fmaf_rn(__uint_as_float(r[q8 * 8 + q]), scale_log2, -l8[q]));
+                            float p1 = ex2(__fmaf_rn(__uint_as_float(r[q8 * 8 + q + 1]), scale_log2, -l8[q + 1]));
+                            if constexpr (decltype(masked)::value) {  // selected, not multiplied: a masked
+                                p0 = (mbits >> (q8 * 8 + q)) & 1u ? p0 : 0.0f;       // score may be anything
+                                p1 = (mbits >> (q8 * 8 + q + 1)) & 1u ? p1 : 0.0f;
+                            }
+                            asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(pw[q8 * 4 + q / 2]) : "f"(p1), "f"(p0));
                         }
-                        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(pw[q8 * 4 + q / 2]) : "f"(p1), "f"(p0));
                     }
+                };
+                if (edge) {
+                    // bit q: this thread's query qpart * kQPer + q attends its key (on the diagonal, query
+                    // i >= key j; queries past L, and a key past L, take no probability)
+                    const uint32_t qbase = qpart * kQPer;
+                    mbits = ~0u;
+                    if (diag && j > qbase) mbits = j - qbase >= 32 ? 0u : ~0u << (j - qbase);
+                    const uint32_t q_lim = key_ok ? (L - qb * kBlk < kBlk ? L - qb * kBlk : kBlk) : 0u;
+                    if (q_lim < qbase + 32) mbits &= (1u << (q_lim > qbase ? q_lim - qbase : 0u)) - 1u;
+                    probs(std::true_type{});
+                } else {
+                    probs(std::false_type{});
                 }
                 // P^T over the first kQPer / 2 of the columns just read (this thread's own lane and columns)
 #pragma unroll
@@ -616,11 +640,12 @@ __global__ void __launch_bounds__(256) attn_do_prep_kernel(const __nv_bfloat16 *
     grid_dep_launch();  // the dV kernel may start its set-up now
     const uint32_t qb = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
     const uint64_t row0 = (uint64_t)bh * L + (uint64_t)qb * kBlk;
-    if (tid < kBlk) lse2[row0 + tid] = lse[row0 + tid] * kLog2e;  // the exponent's offset in base 2
+    const uint32_t rows = L - qb * kBlk < kBlk ? L - qb * kBlk : kBlk;  // the block's rows inside the sequence
+    if (tid < rows) lse2[row0 + tid] = lse[row0 + tid] * kLog2e;  // the exponent's offset in base 2
 #pragma unroll
-    for (uint32_t v = tid; v < kBlk * kHD / 8; v += 256) {  // 16-byte vectors, row-major
+    for (uint32_t v = tid; v < kBlk * kHD / 8; v += 256) {  // 16-byte vectors, row-major; zeros past the rows
         const uint32_t r = v / (kHD / 8), c8 = v % (kHD / 8);
-        *(uint4 *)&tile[r][c8 * 8] = ld_stream(dO + (row0 + r) * kHD + c8 * 8);
+        *(uint4 *)&tile[r][c8 * 8] = r < rows ? ld_stream(dO + (row0 + r) * kHD + c8 * 8) : make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
     // column sums: thread (column c, row half h) sums rows 64h .. 64h + 63 of dO and |dO|
@@ -655,7 +680,7 @@ struct AttnWs {
 };
 AttnWs attn_ws(uint32_t BH, uint32_t L) {
     AttnWs w;
-    const size_t nb = L / kBlk;
+    const size_t nb = (L + kBlk - 1) / kBlk;
     w.pdo = 0;
     w.pdv = w.pdo + round_up256((size_t)BH * nb * kHD * sizeof(float4));
     w.lse2 = w.pdv + round_up256((size_t)BH * nb * kHD * sizeof(float2));
@@ -684,8 +709,8 @@ sdc_status sdc_attn_dv_check_grouped(const void *d_Q, const void *d_K, const voi
                                      uint32_t *d_aborted, void *d_ws, size_t ws_bytes, sdc_stream_t stream) {
     if (!d_Q || !d_K || !d_dO || !d_lse) return fail(SDC_ERR_NULL, "NULL input");
     if (D != kHD) return fail(SDC_ERR_BAD_ARG, "the head dimension D must be 128");
-    if (BH == 0 || L == 0 || L % kBlk || (uint64_t)BH * L >= (1ull << 31) || (uint64_t)BH * kHD >= (1ull << 31))
-        return fail(SDC_ERR_BAD_ARG, "L must be a positive multiple of 128 and BH * L below 2^31");
+    if (BH == 0 || L == 0 || L % 4 || (uint64_t)BH * L >= (1ull << 31) || (uint64_t)BH * kHD >= (1ull << 31))
+        return fail(SDC_ERR_BAD_ARG, "L must be a positive multiple of 4 and BH * L below 2^31");
     if (group == 0 || BH % group) return fail(SDC_ERR_BAD_ARG, "group must divide BH");
     const uint32_t n_kv = BH / group;  // K/V heads
     if (!(scale > 0.0f) || !(scale < 3.0e38f)) return fail(SDC_ERR_BAD_ARG, "scale must be positive and finite");
@@ -714,23 +739,24 @@ sdc_status sdc_attn_dv_check_grouped(const void *d_Q, const void *d_K, const voi
     float *lse2 = (float *)((char *)d_ws + w.lse2);
     int *err = (int *)((char *)d_ws + w.err);
     CUtensorMap mapQ, mapK, mapDo;
-    st = make_map_sw128(&mapQ, d_Q, (uint64_t)BH * L, kHD, kBlk);
-    if (st == SDC_OK) st = make_map_sw128(&mapK, d_K, (uint64_t)n_kv * L, kHD, kBlk);
-    if (st == SDC_OK) st = make_map_sw128(&mapDo, d_dO, (uint64_t)BH * L, kHD, kBlk);
+    // one plane per head: a partial last block reads zeros past L, never the next head's rows
+    st = make_map_sw128_3d(&mapQ, d_Q, BH, L, kHD, kBlk);
+    if (st == SDC_OK) st = make_map_sw128_3d(&mapK, d_K, n_kv, L, kHD, kBlk);
+    if (st == SDC_OK) st = make_map_sw128_3d(&mapDo, d_dO, BH, L, kHD, kBlk);
     if (st != SDC_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     uint32_t *ctr = (uint32_t *)(err + 1);  // the counters after the abort word
     int n_sm = 0;
     e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-    const uint32_t n_items = n_kv * (L / kBlk);
+    const uint32_t n_items = n_kv * ((L + kBlk - 1) / kBlk);
     const uint32_t grid = n_items < (uint32_t)n_sm ? n_items : (uint32_t)n_sm;
     e = cudaMemsetAsync(err, 0, 16 + (size_t)BH * 4, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(d_summary, 0, sizeof(sdc_abft_summary), s);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(attn_dv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAttnSmem);
     if (e != cudaSuccess) return cuda_fail(e, "sdc_attn_dv_check setup");
-    const uint32_t nb = L / kBlk;
+    const uint32_t nb = (L + kBlk - 1) / kBlk;
     const AttnOut out{d_colsum_dv, d_colsum_do, d_residual, d_bound, d_flag, d_summary, d_aborted, tol_scale};
     attn_do_prep_kernel<<<dim3(nb, BH), 256, 0, s>>>((const __nv_bfloat16 *)d_dO, d_lse, L, pdo, lse2);
     cudaLaunchConfig_t cfg = {};

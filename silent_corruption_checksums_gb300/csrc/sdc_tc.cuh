@@ -46,6 +46,14 @@ __host__ __device__ constexpr uint32_t umma_idesc(uint32_t m, uint32_t n) {
 // The same with B MN-major (bit 16).
 __host__ __device__ constexpr uint32_t umma_idesc_bmn(uint32_t m, uint32_t n) { return umma_idesc(m, n) | (1u << 16); }
 
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int32_t c0, int32_t c1, int32_t c2,
+                                            uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+            dst),
+        "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(mbar)
+        : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int32_t c0, int32_t c1,
                                             uint32_t mbar) {
     asm volatile(
@@ -193,6 +201,24 @@ inline PFN_encodeTiled encode_fn() {
             fn = (PFN_encodeTiled)p;
     });
     return fn;
+}
+
+// 3-D map over [planes][rows][cols] bf16 (row-major, cols contiguous): boxes
+// of 64 columns x box_rows rows x 1 plane, 128-byte swizzled; rows past `rows`
+// inside a plane read as zeros (the next plane is never reached).
+inline sdc_status make_map_sw128_3d(CUtensorMap *map, const void *ptr, uint64_t planes, uint64_t rows, uint64_t cols,
+                                    uint32_t box_rows) {
+    PFN_encodeTiled fn = encode_fn();
+    if (!fn) return fail(SDC_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    const cuuint64_t dims[3] = {cols, rows, planes};
+    const cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)cols * 2 * rows};
+    const cuuint32_t box[3] = {64, box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(SDC_ERR_CUDA, "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
+    return SDC_OK;
 }
 
 // 2-D map over a row-major [rows, cols] bf16 matrix: boxes of 64 columns

@@ -129,7 +129,7 @@ def test_host_validation_without_gpu(sdc):
     with pytest.raises(sdc.SdcError) as ei:
         sdc.sdc_attn_dv_check(0, *fake[1:], 1, 128, 128, 0.088, 0, 1.0, *outs, 0, 0, 0)
     assert ei.value.status == 1
-    for BH, L, D, scale, causal, tol in [(1, 128, 64, 0.088, 0, 1.0), (1, 100, 128, 0.088, 0, 1.0),
+    for BH, L, D, scale, causal, tol in [(1, 128, 64, 0.088, 0, 1.0), (1, 102, 128, 0.088, 0, 1.0), (1, 0, 128, 0.088, 0, 1.0),
                                          (0, 128, 128, 0.088, 0, 1.0), (1, 128, 128, -1.0, 0, 1.0),
                                          (1, 128, 128, 0.088, 2, 1.0), (1, 128, 128, 0.088, 0, 0.0)]:
         with pytest.raises(sdc.SdcError) as ei:
@@ -139,6 +139,8 @@ def test_host_validation_without_gpu(sdc):
     # per token), the abort word and the counters (16 bytes + one word per head, in 256-byte units)
     assert sdc.sdc_attn_workspace_size(2, 256, 128) == (2 * 2 * 128 * 16 + 2 * 2 * 128 * 8 + 2 * 256 * 4 + 256)
     assert sdc.sdc_attn_workspace_size(64, 128, 128) == (64 * 128 * 16 + 64 * 128 * 8 + 64 * 128 * 4 + 512)
+    # a partial last block counts as a block: 100 tokens take one block of partials
+    assert sdc.sdc_attn_workspace_size(2, 100, 128) == (2 * 128 * 16 + 2 * 128 * 8 + 256 * ((2 * 100 * 4 + 255) // 256) + 256)
     assert sdc.sdc_attn_workspace_size(2, 256, 64) == 0
     # grouped attention: group 0, or a group that does not divide the query heads, is rejected
     outs = [4096] * 8

@@ -141,7 +141,7 @@ def test_rejects_bad_arguments(sdc):
             x["scale"], 0, 1.0, a.dV.data_ptr(), a.colsum_dv.data_ptr(), a.colsum_do.data_ptr(),
             a.residual.data_ptr(), a.bound.data_ptr(), a.flag.data_ptr(), a.summary.data_ptr(),
             a.aborted.data_ptr(), a.ws.data_ptr(), a.ws_bytes, 0]
-    for i, v, status in [(6, 64, 9), (5, 100, 9), (7, math.nan, 9), (8, 2, 9), (19, a.ws_bytes - 256, 5),
+    for i, v, status in [(6, 64, 9), (5, 102, 9), (7, math.nan, 9), (8, 2, 9), (19, a.ws_bytes - 256, 5),
                          (0, x["Q"].data_ptr() + 2, 8)]:
         bad = list(args)
         bad[i] = v
@@ -250,3 +250,42 @@ def test_grouped_rejects_bad_shapes(sdc):
     a = sdc.AttnDvCheck(4, 128, DEV, group=2)
     with pytest.raises(ValueError):  # K of every query head where the group's K/V heads are expected
         a(x["Q"], x["Q"], x["dO"], x["lse"], x["scale"], True)
+
+
+@pytest.mark.parametrize("BH,group,L,causal", [(2, 1, 100, True), (1, 1, 260, False), (3, 1, 1000, True),
+                                               (8, 4, 300, True), (1, 1, 4100, False), (2, 2, 4, True)])
+def test_ragged_lengths(sdc, BH, group, L, causal):
+    # sequence lengths that are not multiples of the 128-token blocks (any multiple of 4): the last
+    # key block and the last query block are partial; the copies read zeros past L inside each
+    # head, and keys and queries past L take no probability
+    x = W.attn_inputs(BH, L, DEV, seed=90 + BH + L, causal=causal, group=group)
+    a = sdc.AttnDvCheck(BH, L, DEV, group=group)
+    a(x["Q"], x["K"], x["dO"], x["lse"], x["scale"], causal)
+    torch.cuda.synchronize()
+    assert int(a.aborted[0]) == 0 and int(a.summary[0]) == 0
+    Qb, Kb, dOb = _bits(x["Q"]), _bits(x["K"]), _bits(x["dO"])
+    lse = x["lse"].cpu().numpy()
+    dV = a.dV.float().cpu().numpy().astype(np.float64)
+    eps = _eps(group * L)
+    for v in range(BH // group):
+        heads = range(v * group, (v + 1) * group)
+        P = np.vstack([oracle.attn_probs(Qb[h], Kb[v], lse[h], x["scale"], causal) for h in heads])
+        dOs = np.vstack([dOb[h] for h in heads])
+        exact = oracle.attn_dv(P, dOs)
+        e = eps * (P.T @ np.abs(oracle.bf16_to_f64(dOs)))
+        assert np.all(np.abs(dV[v] - exact) <= 2.0 ** -8 * (np.abs(exact) + e) + e + 2.0 ** -134), v
+        inv = oracle.attn_invariant(a.colsum_dv[v].cpu().numpy(), dOs)
+        assert np.all(np.abs(a.colsum_dv[v].cpu().numpy() - exact.sum(axis=0)) <= inv["bound"]), v
+        np.testing.assert_allclose(a.bound[v].cpu().numpy(), inv["bound"], rtol=2.0 ** -38)
+        assert inv["n_flagged"] == 0 and np.all(a.flag[v].cpu().numpy() == 0), v
+
+
+def test_length_not_a_multiple_of_4_is_rejected(sdc):
+    x = W.attn_inputs(1, 128, DEV, seed=95, causal=True)
+    a = sdc.AttnDvCheck(1, 128, DEV)
+    with pytest.raises(sdc.SdcError) as ei:
+        sdc.sdc_attn_dv_check(x["Q"].data_ptr(), x["K"].data_ptr(), x["dO"].data_ptr(), x["lse"].data_ptr(), 1, 126,
+                              128, x["scale"], 1, 1.0, a.dV.data_ptr(), a.colsum_dv.data_ptr(), a.colsum_do.data_ptr(),
+                              a.residual.data_ptr(), a.bound.data_ptr(), a.flag.data_ptr(), a.summary.data_ptr(),
+                              a.aborted.data_ptr(), a.ws.data_ptr(), a.ws_bytes, 0)
+    assert ei.value.status == 9
