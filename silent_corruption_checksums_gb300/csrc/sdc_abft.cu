@@ -72,7 +72,7 @@ constexpr uint32_t kGemmSmemCols = kGemmSmem + 4 * kColTileFloats * 4;
 constexpr uint32_t kMaxK = 1u << 20;
 constexpr uint32_t kMaxSlabs = 64;
 constexpr uint32_t kCheckRows = 8;     // rows per block of the check
-constexpr uint32_t kCheckThreads = 64;  // threads per block of the check
+constexpr uint32_t kCheckThreads = 128;  // threads per block of the check
 
 // Converts 32 accumulators to bf16 (round to nearest even), stores them at
 // dst (64 bytes, 16-byte aligned) and adds them to the row's pair sum.
