@@ -359,7 +359,8 @@ sdc_status sdc_attn_dv_check(const void *d_Q, const void *d_K, const void *d_dO,
  *   d_colsum_do[v][c] = sum over h in v's group and i of dO_h[i][c],
  *   d_residual, d_bound, d_flag as above with g = group L 2^-22 and the sum of
  *     |dO| over the group, all [BH / group][D].
- * Errors as above; SDC_ERR_BAD_ARG also when group is 0 or does not divide BH.
+ * Errors as above; SDC_ERR_BAD_ARG also when group is 0 or does not divide BH,
+ * or when group * ceil(L / 128) (the steps of one work item) exceeds 2^19.
  * The workspace is sdc_attn_workspace_size(BH, L, D). */
 sdc_status sdc_attn_dv_check_grouped(const void *d_Q, const void *d_K, const void *d_dO, const float *d_lse,
                                      uint32_t BH, uint32_t group, uint32_t L, uint32_t D, float scale, uint32_t causal,

@@ -713,6 +713,10 @@ sdc_status sdc_attn_dv_check_grouped(const void *d_Q, const void *d_K, const voi
         return fail(SDC_ERR_BAD_ARG, "L must be a positive multiple of 4 and BH * L below 2^31");
     if (group == 0 || BH % group) return fail(SDC_ERR_BAD_ARG, "group must divide BH");
     const uint32_t n_kv = BH / group;  // K/V heads
+    // one work item's steps (group x key blocks) stay well inside a bounded wait (the epilogue waits
+    // for a whole item): 2^19 steps take under a second even on a throttled GPU
+    if ((uint64_t)group * ((L + kBlk - 1) / kBlk) > (1ull << 19))
+        return fail(SDC_ERR_BAD_ARG, "group * ceil(L / 128) must not exceed 2^19");
     if (!(scale > 0.0f) || !(scale < 3.0e38f)) return fail(SDC_ERR_BAD_ARG, "scale must be positive and finite");
     if (!(tol_scale > 0.0f)) return fail(SDC_ERR_BAD_ARG, "tol_scale must be positive");
     if (causal > 1) return fail(SDC_ERR_BAD_ARG, "causal must be 0 or 1");

@@ -149,6 +149,11 @@ def test_host_validation_without_gpu(sdc):
             sdc.sdc_attn_dv_check_grouped(4096, 8192, 16384, 32768, BH, group, 128, 128, 0.088, 0, 1.0, *outs,
                                           0, 0, 0)
         assert ei.value.status == 9, (BH, group)
+    # one work item's steps, group x ceil(L / 128), at most 2^19 (the epilogue's bounded wait)
+    with pytest.raises(sdc.SdcError) as ei:
+        sdc.sdc_attn_dv_check_grouped(4096, 8192, 16384, 32768, 1024, 1024, 65536 + 128, 128, 0.088, 0, 1.0, *outs,
+                                      0, 0, 0)
+    assert ei.value.status == 9
     assert sdc.sdc_abft_workspace_size(128, 16384, 64) == (64 * 128 * 8 + 4 * 16384 * 8 + 4 * 1024 + 64 * 64 * 16
                                                            + 256)
 
