@@ -68,7 +68,10 @@ constexpr uint32_t kGemmThreads = 192;
 constexpr uint32_t kNumBars = 2 * kStages + 5;  // full[S], empty[S], tfull[2], tempty[2], done
 constexpr uint32_t kGemmSmem = kStages * (kStageA + kStageW) + 1024 + 8 * kNumBars + 16;
 constexpr uint32_t kColTileFloats = 32 * 33;  // one epilogue warp's column-sum tile (row pitch 33)
-constexpr uint32_t kGemmSmemCols = kGemmSmem + 4 * kColTileFloats * 4;
+// with columns: the four epilogue warps' column tiles, then their per-tile column partials [4][kBN]
+// (merged in the CTA, so one partial row per tile row reaches global memory)
+constexpr uint32_t kGemmSmemCols = kGemmSmem + 4 * kColTileFloats * 4 + 4 * kBN * 8;
+static_assert(kGemmSmemCols <= 232448, "shared memory per block");
 constexpr uint32_t kMaxK = 1u << 20;
 constexpr uint32_t kMaxSlabs = 64;
 constexpr uint32_t kCheckRows = 8;     // rows per block of the check
@@ -147,6 +150,18 @@ __device__ __forceinline__ void tc_commit_mc(uint32_t mbar, uint16_t mask) {
 }
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Barrier over `count` threads that also ORs `pred` across them: every warp of the group takes the
+// same branch afterwards.
+__device__ __forceinline__ bool bar_any(uint32_t id, uint32_t count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
 }
 
 // kMc: the CTAs run as clusters of two on vertically adjacent tiles (the same
@@ -271,11 +286,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t quarter = warp & 3u;  // the TMEM lanes this warp may read
         const uint32_t lane_base = (quarter * 32) << 16;
         float *coltile = (float *)(smem + pad + kStages * (kStageA + kStageW) + 8 * kNumBars + 16) + quarter * kColTileFloats;
+        double *cq = (double *)(smem + pad + kStages * (kStageA + kStageW) + 8 * kNumBars + 16 + 4 * kColTileFloats * 4);
+        const uint32_t et = tid - 64;  // thread index within the epilogue (warps 2-5)
         uint32_t lt = 0;
         for (uint32_t u = unit0; u < n_units; u += ustep, ++lt) {
             const uint32_t b = lt & 1u;
             const bool got = mbar_wait(tfull + 8 * b, (lt >> 1) & 1);
-            if (__any_sync(0xffffffffu, !got)) {
+            // with columns the four warps meet at barriers below: they leave together
+            if (kCols ? bar_any(1, 128, !got) : __any_sync(0xffffffffu, !got)) {
                 if (lane == 0) atomicOr(err, 1);
                 break;
             }
@@ -287,8 +305,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             __nv_bfloat16 *crow = C + (uint64_t)row * N + col0;
             const uint32_t acc = tmem + lane_base + b * kAccCols;
             float s = 0.0f, c = 0.0f;
-            // column partials of this warp's 32 rows: [4 tile_m + quarter][N]
-            double *cpart = colsum_part + ((uint64_t)tm * 4 + quarter) * N + (uint64_t)tile_n * kBN + lane;
+
             for (uint32_t c0 = 0; c0 < kBN; c0 += 64) {
                 uint32_t r0[32], r1[32];
                 tc_ld32(acc + c0, r0);
@@ -299,16 +316,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const uint32_t v1 = row >= M || col0 + c0 + 32 >= N ? 0u : min(32u, N - col0 - c0 - 32);
                 epilogue_chunk(r0, crow + c0, s, c, v0);
                 epilogue_chunk(r1, crow + c0 + 32, s, c, v1);
-                if (kCols) {
-                    const double cs0 = warp_column_sum(r0, lane, coltile), cs1 = warp_column_sum(r1, lane, coltile);
-                    if (col0 + c0 + lane < N) cpart[c0] = cs0;
-                    if (col0 + c0 + 32 + lane < N) cpart[c0 + 32] = cs1;
+                if (kCols) {  // this warp's 32 rows of the chunk's columns
+                    cq[quarter * kBN + c0 + lane] = warp_column_sum(r0, lane, coltile);
+                    cq[quarter * kBN + c0 + 32 + lane] = warp_column_sum(r1, lane, coltile);
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tempty + 8 * b) : "memory");
             if (row < M) rowsum_part[(uint64_t)tile_n * M + row] = (double)s + (double)c;
+            if (kCols) {  // the tile's column partials: the four lane quarters merged in order, one row per tile row
+                named_bar_sync(1, 128);
+#pragma unroll
+                for (uint32_t h = 0; h < kBN / 128; ++h) {
+                    const uint32_t cc = et + 128 * h;
+                    const double v = ((cq[cc] + cq[kBN + cc]) + cq[2 * kBN + cc]) + cq[3 * kBN + cc];
+                    if (col0 + cc < N) colsum_part[(uint64_t)tm * N + col0 + cc] = v;
+                }
+                named_bar_sync(1, 128);  // read before the next tile's partials overwrite them
+            }
         }
     }
     tc_fence_before();
@@ -553,7 +579,7 @@ uint32_t n_slabs_for(uint32_t rows, uint32_t K) {
     return n < 1 ? 1 : n;
 }
 
-// Workspace: row partials [ceil(N/256)][M] | column partials [4 ceil(M/128)][N] | W's column sums
+// Workspace: row partials [ceil(N/256)][M] | column partials [ceil(M/128)][N] | W's column sums
 // wcol [K] and their pair split wsplit [K] | A's, acol [K] and asplit [K] |
 // slabs [max(n_slabs(N, K), n_slabs(M, K))][K] (used for W, then for A) | abort word.
 struct AbftWs {
@@ -565,7 +591,7 @@ AbftWs abft_ws(uint32_t M, uint32_t N, uint32_t K) {
     w.part = 0;
     const size_t tiles_m = (M + kBM - 1) / kBM, tiles_n = (N + kBN - 1) / kBN;
     w.cpart = round_up256(tiles_n * M * sizeof(double));
-    w.wcol = w.cpart + round_up256(4 * tiles_m * N * sizeof(double));
+    w.wcol = w.cpart + round_up256(tiles_m * N * sizeof(double));
     w.wsplit = w.wcol + round_up256((size_t)K * sizeof(double2));
     w.acol = w.wsplit + round_up256((size_t)K * sizeof(float4));
     w.asplit = w.acol + round_up256((size_t)K * sizeof(double2));
@@ -653,7 +679,7 @@ sdc_status sdc_abft_gemm(const void *d_A, const void *d_W, void *d_C, uint32_t M
     e = cudaLaunchKernelEx(&cfg, kernel, mapA, mapW, (__nv_bfloat16 *)d_C, M, N, K, band_m, part, cpart, err);
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_gemm launch");
     abft_sum_parts_kernel<<<(M + 31) / 32, 256, 0, s>>>(part, M, tiles_n, d_rowsum, err, d_aborted);
-    if (cols) abft_sum_parts_kernel<<<(N + 31) / 32, 256, 0, s>>>(cpart, N, 4 * tiles_m, d_colsum, nullptr, nullptr);
+    if (cols) abft_sum_parts_kernel<<<(N + 31) / 32, 256, 0, s>>>(cpart, N, tiles_m, d_colsum, nullptr, nullptr);
     e = cudaGetLastError();
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_abft_gemm launch");
 }

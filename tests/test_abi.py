@@ -109,12 +109,12 @@ def test_host_validation_without_gpu(sdc):
         with pytest.raises(sdc.SdcError) as ei:
             sdc.sdc_abft_verify(4096, 8192, M, N, K, 0, 0, 1.0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0)
         assert ei.value.status == 9, (M, N, K)
-    # row partials (ceil(N/256) per row), column partials (4 ceil(M/128) per column), W's and A's column sums
+    # row partials (ceil(N/256) per row), column partials (ceil(M/128) per column), W's and A's column sums
     # (K float64 pairs) and their float32 pair splits (K x 16 bytes), slabs of K x 16 bytes for the
     # larger of the two column sums (slabs = min(608 / ceil(K / 256), 64, rows / 8)), the abort
     # word; each rounded up to 256 bytes
-    assert sdc.sdc_abft_workspace_size(128, 512, 64) == 2048 + 4 * 512 * 8 + 4 * 1024 + 64 * 64 * 16 + 256
-    assert sdc.sdc_abft_workspace_size(1000, 256, 100) == 8192 + 32 * 256 * 8 + 4 * 1792 + 64 * 100 * 16 + 256
+    assert sdc.sdc_abft_workspace_size(128, 512, 64) == 2048 + 1 * 512 * 8 + 4 * 1024 + 64 * 64 * 16 + 256
+    assert sdc.sdc_abft_workspace_size(1000, 256, 100) == 8192 + 8 * 256 * 8 + 4 * 1792 + 64 * 100 * 16 + 256
     # bounded-wait self-test: arguments checked before the launch
     with pytest.raises(sdc.SdcError) as ei:
         sdc.sdc_selftest_bounded_wait(10, 0, 0)
@@ -154,7 +154,7 @@ def test_host_validation_without_gpu(sdc):
         sdc.sdc_attn_dv_check_grouped(4096, 8192, 16384, 32768, 1024, 1024, 65536 + 128, 128, 0.088, 0, 1.0, *outs,
                                       0, 0, 0)
     assert ei.value.status == 9
-    assert sdc.sdc_abft_workspace_size(128, 16384, 64) == (64 * 128 * 8 + 4 * 16384 * 8 + 4 * 1024 + 64 * 64 * 16
+    assert sdc.sdc_abft_workspace_size(128, 16384, 64) == (64 * 128 * 8 + 1 * 16384 * 8 + 4 * 1024 + 64 * 64 * 16
                                                            + 256)
 
 
