@@ -21,7 +21,10 @@
  *    call allocates device memory except sdc_plan_create.
  *  - `stream` is a cudaStream_t (same type; NULL = the legacy default stream).
  *  - Errors are returned as sdc_status codes, checked before anything is
- *    enqueued; nothing is enqueued when a call fails.  sdc_last_error()
+ *    enqueued; nothing is enqueued when a call fails.  Every d_* array a call
+ *    reads or writes, and its workspace, is checked against the allocation
+ *    that holds it (SDC_ERR_BAD_POINTER when it is not device memory of the
+ *    current device or the bytes the call touches run past its end).  sdc_last_error()
  *    returns a one-line detail for the calling thread's last failure.  No
  *    kernel traps or asserts.
  *  - A workspace (d_ws) holds a call's intermediate values and counters,
@@ -280,7 +283,8 @@ size_t sdc_abft_workspace_size(uint32_t M, uint32_t N, uint32_t K);
  * 256-column tile, tile partials added in a fixed order in float64).
  * d_colsum: NULL, or device double [N] for the page's row + column
  * configuration: sum over i of the fp32 accumulator of C[i][j] (float32 pairs
- * per 32 rows, partials added in a fixed order).  d_aborted: device uint32,
+ * per 32 rows, merged per 128-row tile in a fixed order, tile partials added
+ * in a fixed order in float64).  d_aborted: device uint32,
  * 1 if a bounded wait of the GEMM gave up (results then invalid). */
 sdc_status sdc_abft_gemm(const void *d_A, const void *d_W, void *d_C, uint32_t M, uint32_t N, uint32_t K,
                          double *d_rowsum, double *d_colsum, uint32_t *d_aborted, void *d_ws, size_t ws_bytes,

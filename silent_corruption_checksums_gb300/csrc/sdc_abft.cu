@@ -625,7 +625,7 @@ static sdc_status abft_args(const void *d_A, const void *d_W, uint32_t M, uint32
     if (!d_ws || ws_bytes < sdc_abft_workspace_size(M, N, K))
         return fail(SDC_ERR_WS_TOO_SMALL, "workspace smaller than sdc_abft_workspace_size");
     if ((uint64_t)d_ws & 255u) return fail(SDC_ERR_BAD_POINTER, "workspace is not 256-byte aligned");
-    return SDC_OK;
+    return check_device_range(d_ws, sdc_abft_workspace_size(M, N, K), *dev, "d_ws");
 }
 
 sdc_status sdc_abft_gemm(const void *d_A, const void *d_W, void *d_C, uint32_t M, uint32_t N, uint32_t K,
@@ -635,7 +635,11 @@ sdc_status sdc_abft_gemm(const void *d_A, const void *d_W, void *d_C, uint32_t M
     sdc_status st = abft_args(d_A, d_W, M, N, K, d_ws, ws_bytes, &dev);
     if (st != SDC_OK) return st;
     if (!d_C || !d_rowsum || !d_aborted) return fail(SDC_ERR_NULL, "NULL output");
-    st = check_device_range(d_C, (uint64_t)M * N * 2, dev, "d_C");
+    st = check_spans({{d_C, (uint64_t)M * N * 2, "d_C"},
+                      {d_rowsum, (uint64_t)M * 8, "d_rowsum"},
+                      {d_colsum, d_colsum ? (uint64_t)N * 8 : 0, "d_colsum"},
+                      {d_aborted, 4, "d_aborted"}},
+                     dev);
     if (st != SDC_OK) return st;
     if ((uint64_t)d_C & 15u) return fail(SDC_ERR_BAD_POINTER, "C must be 16-byte aligned");
     const uint32_t tiles_m = (M + kBM - 1) / kBM, tiles_n = (N + kBN - 1) / kBN, sms = (uint32_t)sm_count(dev);
@@ -695,6 +699,18 @@ sdc_status sdc_abft_verify(const void *d_A, const void *d_W, uint32_t M, uint32_
     const bool cols = d_colsum != nullptr;
     if (cols && (!d_residual_col || !d_bound_col || !d_flag_col)) return fail(SDC_ERR_NULL, "NULL column output");
     if (!(tol_scale > 0.0f)) return fail(SDC_ERR_BAD_ARG, "tol_scale must be positive");
+    const uint64_t nc = cols ? N : 0;
+    st = check_spans({{d_rowsum, (uint64_t)M * 8, "d_rowsum"},
+                      {d_residual, (uint64_t)M * 8, "d_residual"},
+                      {d_bound, (uint64_t)M * 8, "d_bound"},
+                      {d_flag, M, "d_flag"},
+                      {d_colsum, nc * 8, "d_colsum"},
+                      {d_residual_col, nc * 8, "d_residual_col"},
+                      {d_bound_col, nc * 8, "d_bound_col"},
+                      {d_flag_col, nc, "d_flag_col"},
+                      {d_summary, sizeof(sdc_abft_summary), "d_summary"}},
+                     dev);
+    if (st != SDC_OK) return st;
     const AbftWs w = abft_ws(M, N, K);
     double2 *wcol = (double2 *)((char *)d_ws + w.wcol), *acol = (double2 *)((char *)d_ws + w.acol);
     float4 *wsplit = (float4 *)((char *)d_ws + w.wsplit), *asplit = (float4 *)((char *)d_ws + w.asplit);

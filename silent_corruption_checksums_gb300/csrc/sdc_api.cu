@@ -89,6 +89,14 @@ sdc_status check_device_range(const void *ptr, uint64_t bytes, int device, const
     return SDC_OK;
 }
 
+sdc_status check_spans(std::initializer_list<DevSpan> spans, int device) {
+    for (const DevSpan &sp : spans) {
+        const sdc_status st = check_device_range(sp.ptr, sp.bytes, device, sp.what);
+        if (st != SDC_OK) return st;
+    }
+    return SDC_OK;
+}
+
 sdc_status check_plan_device(const sdc_plan *plan) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
@@ -136,14 +144,15 @@ cudaError_t upload(T **dst, const std::vector<T> &src) {
     return cudaMemcpy(*dst, src.data(), src.size() * sizeof(T), cudaMemcpyHostToDevice);
 }
 
-sdc_status check_ws(const void *ws, size_t ws_bytes, size_t need) {
+// device < 0: the workspace is this library's own static scratch (no range query).
+sdc_status check_ws(const void *ws, size_t ws_bytes, size_t need, int device) {
     if (need == 0) return SDC_OK;
     if (!ws) return fail(SDC_ERR_NULL, "workspace is NULL");
     if (ws_bytes < need)
         return fail(SDC_ERR_WS_TOO_SMALL, "workspace of " + std::to_string(ws_bytes) + " bytes, need " +
                                               std::to_string(need));
     if (((uint64_t)ws & 255u) != 0) return fail(SDC_ERR_BAD_POINTER, "workspace is not 256-byte aligned");
-    return SDC_OK;
+    return device < 0 ? SDC_OK : check_device_range(ws, need, device, "d_ws");
 }
 
 // Workspace: per-chunk partials, then the statistics combine's group sums.
@@ -366,7 +375,8 @@ sdc_status sdc_fingerprint(const sdc_plan *plan, uint64_t *d_out, void *d_ws, si
     sdc_status st = check_plan_device(plan);
     if (st != SDC_OK) return st;
     if (plan->n_desc && !d_out) return fail(SDC_ERR_NULL, "d_out is NULL");
-    st = check_ws(d_ws, ws_bytes, plan_ws_bytes(plan));
+    st = check_device_range(d_out, plan->n_desc * 16, plan->device, "d_out");
+    if (st == SDC_OK) st = check_ws(d_ws, ws_bytes, plan_ws_bytes(plan), plan->device);
     if (st != SDC_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     FpPartial *part = (FpPartial *)d_ws;
@@ -380,7 +390,8 @@ sdc_status sdc_xorsum(const sdc_plan *plan, uint64_t *d_out, void *d_ws, size_t 
     sdc_status st = check_plan_device(plan);
     if (st != SDC_OK) return st;
     if (plan->n_desc && !d_out) return fail(SDC_ERR_NULL, "d_out is NULL");
-    st = check_ws(d_ws, ws_bytes, plan_ws_bytes(plan));
+    st = check_device_range(d_out, plan->n_desc * 8, plan->device, "d_out");
+    if (st == SDC_OK) st = check_ws(d_ws, ws_bytes, plan_ws_bytes(plan), plan->device);
     if (st != SDC_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     uint64_t *part = (uint64_t *)d_ws;
@@ -393,7 +404,16 @@ sdc_status sdc_xorsum_compare(const uint64_t *d_a, const uint64_t *d_b, uint32_t
                               uint64_t *d_diff, sdc_stream_t stream) {
     if (n == 0) return SDC_OK;
     if (!d_a || !d_b || !d_mismatch) return fail(SDC_ERR_NULL, "NULL input or output");
-    cudaError_t e = launch_xor_compare(d_a, d_b, n, d_mismatch, d_diff, (cudaStream_t)stream);
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    const sdc_status st = check_spans({{d_a, (uint64_t)n * 8, "d_a"},
+                                       {d_b, (uint64_t)n * 8, "d_b"},
+                                       {d_mismatch, n, "d_mismatch"},
+                                       {d_diff, d_diff ? (uint64_t)n * 8 : 0, "d_diff"}},
+                                      dev);
+    if (st != SDC_OK) return st;
+    e = launch_xor_compare(d_a, d_b, n, d_mismatch, d_diff, (cudaStream_t)stream);
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_xorsum_compare launch");
 }
 
@@ -403,7 +423,16 @@ sdc_status sdc_vote(const uint64_t *d_fp, uint32_t R, uint32_t T, int32_t *d_sus
         return fail(SDC_ERR_TOO_MANY_REPLICAS, "R = " + std::to_string(R) + ", must be 1..64");
     if (!d_summary) return fail(SDC_ERR_NULL, "d_summary is NULL");
     if (T && (!d_fp || !d_suspect || !d_mask)) return fail(SDC_ERR_NULL, "NULL table or output");
-    cudaError_t e = launch_vote(d_fp, R, T, d_suspect, d_mask, d_summary, (cudaStream_t)stream);
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    const sdc_status st = check_spans({{d_fp, (uint64_t)R * T * 16, "d_fp"},
+                                       {d_suspect, (uint64_t)T * 4, "d_suspect"},
+                                       {d_mask, (uint64_t)T * 8, "d_mask"},
+                                       {d_summary, sizeof(sdc_vote_summary), "d_summary"}},
+                                      dev);
+    if (st != SDC_OK) return st;
+    e = launch_vote(d_fp, R, T, d_suspect, d_mask, d_summary, (cudaStream_t)stream);
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_vote launch");
 }
 
@@ -414,7 +443,8 @@ sdc_status sdc_grad_scan(const sdc_plan *plan, sdc_grad_stats *d_stats, void *d_
     if (st != SDC_OK) return st;
     if (!d_stats) return fail(SDC_ERR_NULL, "d_stats is NULL");
     if (!plan->all_float) return fail(SDC_ERR_BAD_DTYPE, "sdc_grad_scan needs F32, BF16 or F16 descriptors");
-    st = check_ws(d_ws, ws_bytes, plan_ws_bytes(plan));
+    st = check_device_range(d_stats, (uint64_t)plan->R * sizeof(sdc_grad_stats), plan->device, "d_stats");
+    if (st == SDC_OK) st = check_ws(d_ws, ws_bytes, plan_ws_bytes(plan), plan->device);
     if (st != SDC_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     StatPartial *part = (StatPartial *)d_ws;
@@ -432,9 +462,13 @@ size_t sdc_grad_average_scan_workspace_size(uint64_t numel, uint32_t n_bufs, uin
            round_up((size_t)(n_bufs + 1) * kStatGroups * sizeof(StatPartial), 256);
 }
 
-sdc_status sdc_grad_average_scan(const void *const *bufs, uint32_t n_bufs, void *d_avg, uint64_t numel,
-                                 uint32_t dtype, sdc_grad_stats *d_pre, sdc_grad_stats *d_post, void *d_ws,
-                                 size_t ws_bytes, sdc_stream_t stream) {
+}  // extern "C"
+
+// ws_is_scratch: d_ws is this library's static scratch (sdc_noalloc.cu), whose
+// extent needs no range query.
+sdc_status sdc::grad_average_scan(const void *const *bufs, uint32_t n_bufs, void *d_avg, uint64_t numel,
+                                  uint32_t dtype, sdc_grad_stats *d_pre, sdc_grad_stats *d_post, void *d_ws,
+                                  size_t ws_bytes, bool ws_is_scratch, sdc_stream_t stream) {
     if (n_bufs == 0 || n_bufs > 8) return fail(SDC_ERR_TOO_MANY_REPLICAS, "n_bufs must be 1..8");
     if (dtype != SDC_DTYPE_F32 && dtype != SDC_DTYPE_BF16 && dtype != SDC_DTYPE_F16)
         return fail(SDC_ERR_BAD_DTYPE, "dtype must be F32, BF16 or F16");
@@ -457,10 +491,13 @@ sdc_status sdc_grad_average_scan(const void *const *bufs, uint32_t n_bufs, void 
         if (numel && lo < ohi && olo < hi) return fail(SDC_ERR_BAD_ARG, "d_avg overlaps an input");
     }
     if ((uint64_t)d_avg % es) return fail(SDC_ERR_BAD_POINTER, "d_avg not aligned to the element size");
-    sdc_status st = check_device_range(d_avg, bytes, dev, "d_avg");
+    sdc_status st = check_spans({{d_avg, bytes, "d_avg"},
+                                 {d_pre, (uint64_t)n_bufs * sizeof(sdc_grad_stats), "d_pre"},
+                                 {d_post, sizeof(sdc_grad_stats), "d_post"}},
+                                dev);
     if (st != SDC_OK) return st;
     const size_t nc = avg_chunks(numel, dtype);
-    st = check_ws(d_ws, ws_bytes, sdc_grad_average_scan_workspace_size(numel, n_bufs, dtype));
+    st = check_ws(d_ws, ws_bytes, sdc_grad_average_scan_workspace_size(numel, n_bufs, dtype), ws_is_scratch ? -1 : dev);
     if (st != SDC_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     StatPartial *part = (StatPartial *)d_ws;
@@ -470,4 +507,8 @@ sdc_status sdc_grad_average_scan(const void *const *bufs, uint32_t n_bufs, void 
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_grad_average_scan launch");
 }
 
-}  // extern "C"
+extern "C" sdc_status sdc_grad_average_scan(const void *const *bufs, uint32_t n_bufs, void *d_avg, uint64_t numel,
+                                            uint32_t dtype, sdc_grad_stats *d_pre, sdc_grad_stats *d_post,
+                                            void *d_ws, size_t ws_bytes, sdc_stream_t stream) {
+    return sdc::grad_average_scan(bufs, n_bufs, d_avg, numel, dtype, d_pre, d_post, d_ws, ws_bytes, false, stream);
+}

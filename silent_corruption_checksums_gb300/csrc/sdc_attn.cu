@@ -731,12 +731,23 @@ sdc_status sdc_attn_dv_check_grouped(const void *d_Q, const void *d_K, const voi
     if (st == SDC_OK) st = check_device_range(d_dO, tbytes, dev, "d_dO");
     if (st == SDC_OK) st = check_device_range(d_dV, kvbytes, dev, "d_dV");
     if (st == SDC_OK) st = check_device_range(d_lse, (uint64_t)BH * L * 4, dev, "d_lse");
+    if (st == SDC_OK)
+        st = check_spans({{d_colsum_dv, (uint64_t)n_kv * kHD * 8, "d_colsum_dv"},
+                          {d_colsum_do, (uint64_t)n_kv * kHD * 8, "d_colsum_do"},
+                          {d_residual, (uint64_t)n_kv * kHD * 8, "d_residual"},
+                          {d_bound, (uint64_t)n_kv * kHD * 8, "d_bound"},
+                          {d_flag, (uint64_t)n_kv * kHD, "d_flag"},
+                          {d_summary, sizeof(sdc_abft_summary), "d_summary"},
+                          {d_aborted, 4, "d_aborted"}},
+                         dev);
     if (st != SDC_OK) return st;
     if (((uint64_t)d_Q | (uint64_t)d_K | (uint64_t)d_dO | (uint64_t)d_dV | (uint64_t)d_lse) & 15u)
         return fail(SDC_ERR_BAD_POINTER, "Q, K, dO, dV and lse must be 16-byte aligned");
     if (!d_ws || ws_bytes < sdc_attn_workspace_size(BH, L, D))
         return fail(SDC_ERR_WS_TOO_SMALL, "workspace smaller than sdc_attn_workspace_size");
     if ((uint64_t)d_ws & 255u) return fail(SDC_ERR_BAD_POINTER, "workspace is not 256-byte aligned");
+    st = check_device_range(d_ws, sdc_attn_workspace_size(BH, L, D), dev, "d_ws");
+    if (st != SDC_OK) return st;
     const AttnWs w = attn_ws(BH, L);
     float4 *pdo = (float4 *)((char *)d_ws + w.pdo);
     float2 *pdv = (float2 *)((char *)d_ws + w.pdv);

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <initializer_list>
 #include <string>
 #include <vector>
 
@@ -84,7 +85,7 @@ struct sdc_plan {
 namespace sdc {
 
 // ---------------------------------------------------------------------------
-// Host-side helpers (sdc_plan.cu)
+// Host-side helpers (sdc_api.cu)
 // ---------------------------------------------------------------------------
 void set_error(const std::string &msg);
 sdc_status fail(sdc_status st, const std::string &msg);
@@ -92,6 +93,19 @@ sdc_status cuda_fail(cudaError_t e, const char *what);
 sdc_status check_plan_device(const sdc_plan *plan);
 // Check [ptr, ptr + bytes) is device memory of `device` inside one allocation.
 sdc_status check_device_range(const void *ptr, uint64_t bytes, int device, const char *what);
+// One array a call reads or writes; ptr may be NULL only when bytes == 0.
+struct DevSpan {
+    const void *ptr;
+    uint64_t bytes;
+    const char *what;
+};
+// check_device_range for each span in order; the first failure is returned.
+sdc_status check_spans(std::initializer_list<DevSpan> spans, int device);
+// sdc_grad_average_scan; ws_is_scratch skips the workspace's range query (the
+// no-allocation entry point passes this library's own static scratch).
+sdc_status grad_average_scan(const void *const *bufs, uint32_t n_bufs, void *d_avg, uint64_t numel, uint32_t dtype,
+                             sdc_grad_stats *d_pre, sdc_grad_stats *d_post, void *d_ws, size_t ws_bytes,
+                             bool ws_is_scratch, sdc_stream_t stream);
 int sm_count(int device);
 
 // Launchers (one per translation unit that holds the kernel).

@@ -64,6 +64,6 @@ extern "C" sdc_status sdc_grad_average_scan_noalloc(const void *const *bufs, uin
     if (st != SDC_OK) return st;
     // Nothing in the scratch needs to start at zero: every partial and group
     // sum is written by this call before it is read.
-    return sdc_grad_average_scan(bufs, n_bufs, d_avg, numel, dtype, d_pre, d_post, scratch,
-                                 (size_t)SDC_NOALLOC_SCRATCH_BYTES, stream);
+    return sdc::grad_average_scan(bufs, n_bufs, d_avg, numel, dtype, d_pre, d_post, scratch,
+                                  (size_t)SDC_NOALLOC_SCRATCH_BYTES, true, stream);
 }

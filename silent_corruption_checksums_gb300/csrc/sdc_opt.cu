@@ -278,6 +278,10 @@ sdc_status sdc_adamw_fingerprint(const sdc_plan *plan, const sdc_opt_state *stat
     }
     if (plan->n_chunks && (!d_ws || ws_bytes < plan->n_chunks * sizeof(FpPartial)))
         return fail(SDC_ERR_WS_TOO_SMALL, "workspace smaller than sdc_workspace_size(plan)");
+    st = check_spans({{d_fp_out, plan->n_desc * 16, "d_fp_out"},
+                      {d_ws, plan->n_chunks * sizeof(FpPartial), "d_ws"}},
+                     plan->device);
+    if (st != SDC_OK) return st;
     // float32 scalars, each formed in double from the float32 inputs and rounded once
     const double lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2, t = (double)hp->step;
     AdamK k;

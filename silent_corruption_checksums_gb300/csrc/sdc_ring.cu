@@ -102,6 +102,14 @@ extern "C" sdc_status sdc_ring_audit(const uint64_t *d_table, uint32_t n, uint32
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return sdc::cuda_fail(e, "cudaGetDevice");
+    const sdc_status st = sdc::check_spans({{d_table, (uint64_t)n * 2 * L * 8, "d_table"},
+                                            {d_mismatch, n, "d_mismatch"},
+                                            {d_hits, (uint64_t)n * 4, "d_hits"},
+                                            {d_culprit, n, "d_culprit"},
+                                            {d_ambiguous, n, "d_ambiguous"},
+                                            {d_summary, sizeof(sdc_ring_summary), "d_summary"}},
+                                           dev);
+    if (st != SDC_OK) return st;
     const uint32_t off = n ? offset % n : 0;
     e = sdc::launch_ring_audit(d_table, n, L, off, d_mismatch, d_hits, d_culprit, d_ambiguous, d_summary, dev,
                                (cudaStream_t)stream);

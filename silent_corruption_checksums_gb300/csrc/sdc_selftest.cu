@@ -31,6 +31,11 @@ __global__ void bounded_wait_selftest_kernel(uint32_t polls, uint32_t *__restric
 extern "C" sdc_status sdc_selftest_bounded_wait(uint32_t polls, uint32_t *d_status, sdc_stream_t stream) {
     if (!d_status) return sdc::fail(SDC_ERR_NULL, "NULL status");
     if (polls == 0 || polls > (1u << 24)) return sdc::fail(SDC_ERR_BAD_ARG, "polls must be 1 .. 2^24");
+    int dev = -1;
+    const cudaError_t de = cudaGetDevice(&dev);
+    if (de != cudaSuccess) return sdc::cuda_fail(de, "cudaGetDevice");
+    const sdc_status st = sdc::check_device_range(d_status, 4, dev, "d_status");
+    if (st != SDC_OK) return st;
     sdc::bounded_wait_selftest_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(polls, d_status);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? SDC_OK : sdc::cuda_fail(e, "sdc_selftest_bounded_wait launch");
