@@ -22,7 +22,8 @@
 // Kernels:
 //   attn_do_prep_kernel -- lse log2(e), and float32-pair column sums of dO
 //     and |dO| per 128-row block (dO itself feeds the dV product as it is:
-//     its B operand, MN-major);
+//     its B operand, MN-major); persistent CTAs, each block's rows brought in
+//     by a bulk copy that overlaps the previous block's sums;
 //   attn_dv_kernel -- persistent, one CTA per SM; a work item is one
 //     (K/V head, 128-key block), taken from a counter heaviest first (causal:
 //     key block 0 of every head first), its steps running over the query
@@ -633,39 +634,100 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 // block (x, y) takes rows 128x .. 128x + 127 of head y.  The tile goes through
 // shared memory (row-major, read back column-wise for the sums);
 // part_do[y][x][c] = {pair of sum_i dO[i, c], pair of sum_i |dO[i, c]|}.
-__global__ void __launch_bounds__(256) attn_do_prep_kernel(const __nv_bfloat16 *__restrict__ dO,
-                                                           const float *__restrict__ lse, uint32_t L,
-                                                           float4 *__restrict__ part_do, float *__restrict__ lse2) {
-    __shared__ __align__(16) uint16_t tile[kBlk][kHD];
+// The prep pass: one work unit per (head, 128-row block) of dO.  Persistent
+// CTAs take units round-robin; a unit's rows (contiguous, rows x 256 bytes)
+// arrive by one bulk copy into one of two shared-memory buffers, so the next
+// unit's copy runs while this one is summed; the unit's log-sum-exps come with
+// the same copy (rows x 4 bytes), so no thread waits on a global load.  Thread (column pair p, row
+// quarter h) sums columns 2p and 2p + 1 over rows 32h .. 32h + 31 as packed
+// float32 pairs (TwoSum), for dO and |dO|; quarters 1-3 are then merged into
+// quarter 0 in that order.
+constexpr uint32_t kPrepThreads = 256, kPrepQuarters = kPrepThreads / (kHD / 2);
+constexpr uint32_t kPrepScr = 2 * kTile;                                      // [3][64] x (dO pair, |dO| pair)
+constexpr uint32_t kPrepLse = kPrepScr + (kPrepQuarters - 1) * (kHD / 2) * 32;  // [2][128] float
+constexpr uint32_t kPrepBar = kPrepLse + 2 * kBlk * 4;                            // two mbarriers
+constexpr uint32_t kPrepSmem = kPrepBar + 16;
+constexpr uint32_t kPrepCtasPerSm = 3;
+static_assert(kPrepCtasPerSm * (kPrepSmem + 1024) <= 233472, "prep CTAs per SM exceed shared memory");
+
+__global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
+    attn_do_prep_kernel(const __nv_bfloat16 *__restrict__ dO, const float *__restrict__ lse, uint32_t L, uint32_t nb,
+                        uint32_t n_units, float4 *__restrict__ part_do, float *__restrict__ lse2, int *__restrict__ err) {
+    extern __shared__ __align__(128) uint8_t psm[];
     grid_dep_launch();  // the dV kernel may start its set-up now
-    const uint32_t qb = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
-    const uint64_t row0 = (uint64_t)bh * L + (uint64_t)qb * kBlk;
-    const uint32_t rows = L - qb * kBlk < kBlk ? L - qb * kBlk : kBlk;  // the block's rows inside the sequence
-    if (tid < rows) lse2[row0 + tid] = lse[row0 + tid] * kLog2e;  // the exponent's offset in base 2
-#pragma unroll
-    for (uint32_t v = tid; v < kBlk * kHD / 8; v += 256) {  // 16-byte vectors, row-major; zeros past the rows
-        const uint32_t r = v / (kHD / 8), c8 = v % (kHD / 8);
-        *(uint4 *)&tile[r][c8 * 8] = r < rows ? ld_stream(dO + (row0 + r) * kHD + c8 * 8) : make_uint4(0, 0, 0, 0);
+    const uint32_t tid = threadIdx.x, cp = tid & (kHD / 2 - 1), h = tid / (kHD / 2);
+    const uint32_t first = blockIdx.x, stride = gridDim.x;
+    const uint32_t n_mine = first < n_units ? (n_units - 1 - first) / stride + 1 : 0;
+    const uint32_t bar0 = smem_addr(psm + kPrepBar);
+    auto unit_rows = [&](uint32_t u) {  // the unit's rows inside the sequence
+        const uint32_t qb = u % nb;
+        return L - qb * kBlk < kBlk ? L - qb * kBlk : kBlk;
+    };
+    auto issue = [&](uint32_t i) {  // copy the CTA's i-th unit into buffer i & 1
+        const uint32_t u = first + i * stride, rows = unit_rows(u), bar = bar0 + 8 * (i & 1);
+        const uint64_t row0 = (uint64_t)(u / nb) * L + (u % nb) * kBlk;  // a multiple of 4: 16-byte aligned lse
+        mbar_arrive_expect_tx(bar, rows * (kHD * 2 + 4));
+        bulk_g2s(smem_addr(psm + (i & 1) * kTile), dO + row0 * kHD, rows * kHD * 2, bar);
+        bulk_g2s(smem_addr(psm + kPrepLse + (i & 1) * kBlk * 4), lse + row0, rows * 4, bar);
+    };
+    if (tid == 0) {
+        mbar_init(bar0, 1);
+        mbar_init(bar0 + 8, 1);
+        fence_mbar_init();
     }
     __syncthreads();
-    // column sums: thread (column c, row half h) sums rows 64h .. 64h + 63 of dO and |dO|
-    // (two independent chains); the half-1 pairs are merged into the half-0 ones in that order
-    __shared__ float4 half1[kHD];
-    const uint32_t c = tid & (kHD - 1), h = tid >> 7;
-    float s = 0.0f, e = 0.0f, sa = 0.0f, ea = 0.0f;
+    if (tid == 0 && n_mine) issue(0);
+    for (uint32_t i = 0; i < n_mine; ++i) {
+        // buffer (i + 1) & 1 was last read in iteration i - 1, whose closing barrier every thread has passed
+        if (tid == 0 && i + 1 < n_mine) issue(i + 1);
+        const uint32_t u = first + i * stride, bh = u / nb, qb = u % nb, rows = unit_rows(u);
+        const uint64_t row0 = (uint64_t)bh * L + (uint64_t)qb * kBlk;
+        const bool got = mbar_wait(bar0 + 8 * (i & 1), (i >> 1) & 1u);
+        if (!__syncthreads_and(got)) {  // a copy that never landed: record it, let the copies in flight end
+            if (tid == 0) {
+                atomicOr(err, 1);
+                mbar_wait(bar0 + 8 * (i & 1), (i >> 1) & 1u);
+                if (i + 1 < n_mine) mbar_wait(bar0 + 8 * ((i + 1) & 1), ((i + 1) >> 1) & 1u);
+            }
+            return;
+        }
+        if (tid < rows)  // the exponent's offset in base 2
+            lse2[row0 + tid] = ((const float *)(psm + kPrepLse))[(i & 1) * kBlk + tid] * kLog2e;
+        const uint32_t *tile = (const uint32_t *)(psm + (i & 1) * kTile);  // [128 rows][64 column pairs]
+        uint64_t s = 0, c = 0, sa = 0, ca = 0;
+        const uint32_t r0 = h * (kBlk / kPrepQuarters), r1 = min(r0 + kBlk / kPrepQuarters, rows);
 #pragma unroll 8
-    for (uint32_t r = h * 64; r < h * 64 + 64; ++r) {
-        const float x = __uint_as_float((uint32_t)tile[r][c] << 16);
-        pair_add(s, e, x);
-        pair_add(sa, ea, fabsf(x));
-    }
-    if (h == 1) half1[c] = make_float4(s, e, sa, ea);
-    __syncthreads();
-    if (h == 0) {
-        const float4 o = half1[c];
-        pair_merge(s, e, o.x, o.y);
-        pair_merge(sa, ea, o.z, o.w);
-        part_do[((uint64_t)bh * gridDim.x + qb) * kHD + c] = make_float4(s, e, sa, ea);
+        for (uint32_t r = r0; r < r1; ++r) {
+            const uint32_t w = tile[r * (kHD / 2) + cp], wa = w & 0x7FFF7FFFu;
+            pair2_add(s, c, f2_pack_bits(w << 16, w & 0xFFFF0000u));
+            pair2_add(sa, ca, f2_pack_bits(wa << 16, wa & 0xFFFF0000u));
+        }
+        ulonglong2 *scr = (ulonglong2 *)(psm + kPrepScr);  // [quarter - 1][pair][2]
+        if (h > 0) {
+            scr[((h - 1) * (kHD / 2) + cp) * 2] = make_ulonglong2(s, c);
+            scr[((h - 1) * (kHD / 2) + cp) * 2 + 1] = make_ulonglong2(sa, ca);
+        }
+        __syncthreads();
+        if (h == 0) {
+#pragma unroll
+            for (uint32_t q = 0; q + 1 < kPrepQuarters; ++q) {
+                const ulonglong2 o = scr[(q * (kHD / 2) + cp) * 2], oa = scr[(q * (kHD / 2) + cp) * 2 + 1];
+                pair2_add(s, c, o.x);
+                c = f2_add(c, o.y);
+                pair2_add(sa, ca, oa.x);
+                ca = f2_add(ca, oa.y);
+            }
+            float s0, s1, c0, c1, a0, a1, e0, e1;
+            f2_unpack(s, s0, s1);
+            f2_unpack(c, c0, c1);
+            f2_unpack(sa, a0, a1);
+            f2_unpack(ca, e0, e1);
+            float4 *o = part_do + ((uint64_t)bh * nb + qb) * kHD + 2 * cp;
+            o[0] = make_float4(s0, c0, a0, e0);
+            o[1] = make_float4(s1, c1, a1, e1);
+        }
+        // quarter 0's scratch reads end before the next iteration's first barrier, after which the
+        // other quarters write the scratch again
     }
 }
 
@@ -770,10 +832,15 @@ sdc_status sdc_attn_dv_check_grouped(const void *d_Q, const void *d_K, const voi
     if (e == cudaSuccess) e = cudaMemsetAsync(d_summary, 0, sizeof(sdc_abft_summary), s);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(attn_dv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAttnSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(attn_do_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
     if (e != cudaSuccess) return cuda_fail(e, "sdc_attn_dv_check setup");
     const uint32_t nb = (L + kBlk - 1) / kBlk;
     const AttnOut out{d_colsum_dv, d_colsum_do, d_residual, d_bound, d_flag, d_summary, d_aborted, tol_scale};
-    attn_do_prep_kernel<<<dim3(nb, BH), 256, 0, s>>>((const __nv_bfloat16 *)d_dO, d_lse, L, pdo, lse2);
+    const uint32_t prep_units = BH * nb;
+    const uint32_t prep_grid = prep_units < kPrepCtasPerSm * (uint32_t)n_sm ? prep_units : kPrepCtasPerSm * n_sm;
+    attn_do_prep_kernel<<<prep_grid, kPrepThreads, kPrepSmem, s>>>((const __nv_bfloat16 *)d_dO, d_lse, L, nb,
+                                                                   prep_units, pdo, lse2, err);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kAttnThreads);
