@@ -30,7 +30,9 @@
 //    the biased exponent of x is >= 76 (or x == 0); smaller values are caught
 //    by a running minimum of the lane's magnitudes.
 // A run whose float32 sum is not finite (NaN, Inf, big, |bf16| >= 32, or an
-// overflowing sum) or that holds a tiny f32 value is redone exactly: each
+// overflowing sum, including the sum of the two packed halves: bf16 values of
+// magnitude 2.9 .. 4 leave each half finite after the 2^118 scaling and
+// overflow their sum) or that holds a tiny f32 value is redone exactly: each
 // element classified and its square added in float64 (exact squares).
 // All reductions have a fixed shape, so results are identical on every run.
 #include <cuda_bf16.h>
@@ -141,8 +143,11 @@ __device__ __forceinline__ bool fast_flush(FastAcc &a, double &acc_scaled) {
         const float bb = t - sx;
         const float e = (sx - (t - bb)) + (sy - bb);
         const float cc = (cx + cy) + e;
-        acc_scaled = __dadd_rn(acc_scaled, (double)t);
-        acc_scaled = __dadd_rn(acc_scaled, (double)cc);
+        ok = isfinite(t);  // each half finite, their sum not: the run is redone exactly
+        if (ok) {
+            acc_scaled = __dadd_rn(acc_scaled, (double)t);
+            acc_scaled = __dadd_rn(acc_scaled, (double)cc);
+        }
     }
     a.s = 0;
     a.c = 0;

@@ -133,3 +133,29 @@ def test_repeatable(sdc):
         avg, pre, post = sdc.grad_average_scan(g["bufs"], ws=ws)
         results.append((host_bits(avg).tobytes(), pre.cpu().numpy().tobytes(), post.cpu().numpy().tobytes()))
     assert results[0] == results[1] == results[2]
+
+
+@pytest.mark.parametrize("dtype,magnitudes", [
+    (torch.bfloat16, (3.0, 3.0)),     # after the 2^118 scaling each packed half of a run stays finite,
+    (torch.bfloat16, (2.85, 3.98)),   # but the two halves' sum overflows float32
+    (torch.float32, (1.35e19, 1.35e19)),  # x^2 finite, two of them past FLT_MAX: the norm alarm
+])
+def test_run_halves_whose_sum_overflows(sdc, dtype, magnitudes):
+    gen = torch.Generator(device="cpu").manual_seed(41)
+    n = 3 * 8192 + 5
+    lo, hi = magnitudes
+    mag = lo + (hi - lo) * torch.rand(n, generator=gen, dtype=torch.float64)
+    sign = torch.where(torch.rand(n, generator=gen) < 0.5, -1.0, 1.0).to(torch.float64)
+    bufs = [(mag * sign).to(dtype).to(DEV) for _ in range(2)]
+    name = NAMES[dtype]
+    hb = [host_bits(b) for b in bufs]
+    ref = oracle.grad_stats(hb[0], name)
+    assert math.isfinite(ref["sumsq_finite"])
+    avg, pre, post = sdc.grad_average_scan(bufs)
+    for b in range(2):
+        stats_match(sdc.decode_stats(pre)[b], oracle.grad_stats(hb[b], name))
+    stats_match(sdc.decode_stats(post)[0], oracle.grad_stats(host_bits(avg), name))
+    plan = sdc.Plan([[bufs[0]], [bufs[1]]])
+    got = sdc.decode_stats(plan.grad_scan())
+    for b in range(2):
+        stats_match(got[b], oracle.grad_stats(hb[b], name))
