@@ -18,7 +18,10 @@
 // gamma_{n-1}^2 * sum, gamma_k = k u / (1 - k u), u = 2^-24 (Ogita, Rump and
 // Oishi, "Accurate sum and dot product", 2005); with n = 64 terms per lane
 // half between flushes that is 1.4e-11 relative.  Every 16 vectors the pair
-// is flushed into a float64 accumulator.
+// is added into the lane's own float32 pair (h, l) with TwoSum, and a warp's
+// lanes are added in a fixed xor tree of TwoSums; float64 is used only for the
+// warp's total (this part's FP64 pipe is slow, and per-run float64 adds kept
+// it a quarter busy), or for each lane's pair if the float32 tree overflows.
 //
 // Exactness of the float32 squares:
 //  - bf16: x is scaled by 2^59 before squaring, so every bf16 square -- down
@@ -128,25 +131,32 @@ __device__ __forceinline__ void fast_vec(const uint4 &v, FastAcc &a) {
     }
 }
 
-// Flush a run's (s, c) into the scaled float64 accumulator.  Returns false
-// when the run must be redone exactly.
+// A lane's runs summed as a float32 pair h + l (in the dtype's scaled domain).
+struct FF {
+    float h = 0.0f, l = 0.0f;
+};
+
+// Adds a finished run into f: the two packed halves merged error-free, then
+// TwoSum with f.h.  Returns false, leaving f unchanged, when the run must be
+// redone exactly: a half not finite, a tiny f32 value, or a sum that overflows.
 template <int DT>
-__device__ __forceinline__ bool fast_flush(FastAcc &a, double &acc_scaled) {
+__device__ __forceinline__ bool fast_flush_ff(FastAcc &a, FF &f) {
     float sx, sy, cx, cy;
     f2_unpack(a.s, sx, sy);
     f2_unpack(a.c, cx, cy);
     bool ok = isfinite(sx) && isfinite(sy);
     if (DT == SDC_DTYPE_F32) ok = ok && a.tmin >= kF32TinyLimit;
     if (ok) {
-        // error-free merge of the two lanes, then two float64 adds
         const float t = sx + sy;
         const float bb = t - sx;
         const float e = (sx - (t - bb)) + (sy - bb);
-        const float cc = (cx + cy) + e;
-        ok = isfinite(t);  // each half finite, their sum not: the run is redone exactly
+        const float h2 = f.h + t;  // Inf when t or the new sum overflows
+        const float b2 = h2 - f.h;
+        const float e2 = (f.h - (h2 - b2)) + (t - b2);
+        ok = isfinite(h2);
         if (ok) {
-            acc_scaled = __dadd_rn(acc_scaled, (double)t);
-            acc_scaled = __dadd_rn(acc_scaled, (double)cc);
+            f.h = h2;
+            f.l = __fadd_rn(f.l, __fadd_rn(__fadd_rn(__fadd_rn(cx, cy), e), e2));
         }
     }
     a.s = 0;
@@ -158,6 +168,32 @@ __device__ __forceinline__ bool fast_flush(FastAcc &a, double &acc_scaled) {
 template <int DT>
 __device__ __forceinline__ double unscale(double acc_scaled) {
     return DT == SDC_DTYPE_BF16 ? acc_scaled * kBf16Unscale : acc_scaled;
+}
+
+// The warp's total: the lanes' pairs added in a fixed xor tree (TwoSum's
+// error term is exact whichever operand comes first, so every lane ends with
+// the same bits); if that overflows float32, each lane's pair in float64
+// instead.  Then unscaled, plus the exactly summed elements (acc_e).
+template <int DT>
+__device__ __forceinline__ double warp_total(const FF &f, double acc_e) {
+    float h = f.h, l = f.l;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ho = __shfl_xor_sync(0xffffffffu, h, o), lo = __shfl_xor_sync(0xffffffffu, l, o);
+        const float t = __fadd_rn(h, ho);
+        const float bb = __fsub_rn(t, h);
+        const float e = __fadd_rn(__fsub_rn(h, __fsub_rn(t, bb)), __fsub_rn(ho, bb));
+        h = t;
+        l = __fadd_rn(__fadd_rn(l, lo), e);
+    }
+    double tot;
+    if (isfinite(h))  // the same on every lane
+        tot = __dadd_rn((double)h, (double)l);
+    else
+        tot = warp_sum_f64(__dadd_rn((double)f.h, (double)f.l));
+    tot = unscale<DT>(tot);
+    if (__any_sync(0xffffffffu, acc_e != 0.0)) tot = __dadd_rn(tot, warp_sum_f64(acc_e));
+    return tot;
 }
 
 template <int DT>
@@ -187,7 +223,8 @@ template <int DT, int U>
 __device__ __forceinline__ double grad_chunk(const GGeom &g, uint32_t lane, Counts &n) {
     const uint4 *vb = (const uint4 *)(g.addr + g.head);
     const uint32_t niter = (g.nvec + 31) >> 5;
-    double acc_scaled = 0.0, acc_exact = 0.0;
+    FF ff;
+    double acc_exact = 0.0;
     // one bulk L2 prefetch of the chunk's aligned body: the later runs of the
     // chunk then load from L2 while this run computes
     if (lane == 0 && g.nvec) prefetch_l2_bulk(vb, g.nvec * 16u);
@@ -204,7 +241,7 @@ __device__ __forceinline__ double grad_chunk(const GGeom &g, uint32_t lane, Coun
 #pragma unroll
             for (int u = 0; u < U; ++u) fast_vec<DT>(v[u], a);
         }
-        if (!fast_flush<DT>(a, acc_scaled)) {
+        if (!fast_flush_ff<DT>(a, ff)) {
             for (uint32_t i = r0; i < r1; ++i) {
                 const uint32_t vi = lane + (i << 5);
                 if (vi < g.nvec) exact_vec<DT>(vb[vi], acc_exact, n);
@@ -222,7 +259,7 @@ __device__ __forceinline__ double grad_chunk(const GGeom &g, uint32_t lane, Coun
         const uint32_t bits = g.l2 == 2 ? *(const uint32_t *)a : (uint32_t)(*(const uint16_t *)a);
         exact_elem(bits, DT, acc_exact, n);
     }
-    return __dadd_rn(unscale<DT>(acc_scaled), acc_exact);
+    return warp_total<DT>(ff, acc_exact);  // the warp's total, on every lane
 }
 
 template <int U>
@@ -241,7 +278,6 @@ __global__ void __launch_bounds__(kScanBlock) grad_scan_kernel(const Chunk *__re
             case SDC_DTYPE_BF16: acc = grad_chunk<SDC_DTYPE_BF16, U>(g, lane, n); break;
             default: acc = grad_chunk<SDC_DTYPE_F16, U>(g, lane, n); break;
         }
-        acc = warp_sum_f64(acc);
         const uint32_t nn = warp_sum_u32(n.nan), ni = warp_sum_u32(n.inf), nb = warp_sum_u32(n.big);
         if (lane == 0) partials[c] = StatPartial{acc, nn, ni, nb, 0u};
     }
@@ -390,10 +426,11 @@ __global__ void __launch_bounds__(kScanBlock) avg_scan_kernel(BufPtrs bp, void *
 #pragma unroll
         for (int b = 0; b < NB; ++b) in[b] = (const uint4 *)((const char *)bp.p[b] + e0 * ES);
         uint4 *out = (uint4 *)((char *)outp + e0 * ES);
-        double acc_s[NS], acc_e[NS];
+        FF ff[NS];
+        double acc_e[NS];
         Counts n[NS];
 #pragma unroll
-        for (int s = 0; s < NS; ++s) acc_s[s] = acc_e[s] = 0.0;
+        for (int s = 0; s < NS; ++s) acc_e[s] = 0.0;
         for (uint32_t r0 = 0; r0 < niter; r0 += kRunVec) {
             const uint32_t r1 = min(r0 + (uint32_t)kRunVec, niter);
             FastAcc a[NS];
@@ -432,7 +469,7 @@ __global__ void __launch_bounds__(kScanBlock) avg_scan_kernel(BufPtrs bp, void *
             }
 #pragma unroll
             for (int s = 0; s < NS; ++s) {
-                if (!fast_flush<DT>(a[s], acc_s[s])) {
+                if (!fast_flush_ff<DT>(a[s], ff[s])) {
                     const uint4 *src = s < NB ? in[s] : (const uint4 *)out;
                     for (uint32_t i = r0; i < r1; ++i) {
                         const uint32_t vi = lane + (i << 5);
@@ -453,8 +490,7 @@ __global__ void __launch_bounds__(kScanBlock) avg_scan_kernel(BufPtrs bp, void *
         }
 #pragma unroll
         for (int s = 0; s < NS; ++s) {
-            double acc = __dadd_rn(unscale<DT>(acc_s[s]), acc_e[s]);
-            acc = warp_sum_f64(acc);
+            const double acc = warp_total<DT>(ff[s], acc_e[s]);
             const uint32_t nn = warp_sum_u32(n[s].nan), ni = warp_sum_u32(n[s].inf), nbg = warp_sum_u32(n[s].big);
             if (lane == 0) partials[(uint64_t)s * n_chunks + c] = StatPartial{acc, nn, ni, nbg, 0u};
         }
