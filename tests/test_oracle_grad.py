@@ -193,3 +193,12 @@ def test_average_closed_forms():
         acc = (acc + _bf16_values(bb).astype(np.float32)).astype(np.float32)
     acc = (acc * np.float32(0.25)).astype(np.float32)
     assert np.array_equal(oracle.average(bufs, "bf16"), _bf16_bits(acc))
+
+
+def test_closed_form_magnitudes_three_to_four():
+    # n copies of c with |c| between 3 and 4 (exact in bf16): the sum of squares is exactly n c^2,
+    # nothing is big and no float32 alarm is raised
+    for c in (3.0, -3.5, 3.984375):
+        st = oracle.grad_stats(_bf16_bits(np.full(4099, c)), "bf16")
+        assert st["sumsq_finite"] == 4099 * c * c
+        assert st["n_big"] == 0 and st["nonfinite_fp32"] == 0
