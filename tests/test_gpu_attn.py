@@ -289,3 +289,20 @@ def test_length_not_a_multiple_of_4_is_rejected(sdc):
                               a.residual.data_ptr(), a.bound.data_ptr(), a.flag.data_ptr(), a.summary.data_ptr(),
                               a.aborted.data_ptr(), a.ws.data_ptr(), a.ws_bytes, 0)
     assert ei.value.status == 9
+
+
+@pytest.mark.parametrize("BH,L,causal", [(64, 2048, False), (40, 2052, True)])
+def test_prep_pass_several_blocks_per_cta(sdc, BH, L, causal):
+    # more (head, 128-row block) units than the prep pass's persistent CTAs (three per SM), so
+    # each CTA sums several blocks through its two alternating buffers; dO's column sums and the
+    # bound of every head against exact sums, dV's column sums within that bound
+    x = W.attn_inputs(BH, L, DEV, seed=39, causal=causal)
+    a = _run(sdc, x)
+    assert int(a.aborted[0]) == 0 and int(a.summary[0]) == 0
+    dO = oracle.bf16_to_f64(_bits(x["dO"]))  # [BH, L, 128]
+    colsum_do = a.colsum_do.cpu().numpy()
+    absd = np.abs(dO).sum(axis=1)
+    assert np.all(np.abs(colsum_do - dO.sum(axis=1)) <= 2.0 ** -40 * absd)
+    np.testing.assert_allclose(a.bound.cpu().numpy(), oracle.attn_bound(absd, L), rtol=2.0 ** -38)
+    assert np.all(np.abs(a.residual.cpu().numpy()) <= a.bound.cpu().numpy())
+    assert np.all(a.flag.cpu().numpy() == 0)
