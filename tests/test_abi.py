@@ -183,3 +183,65 @@ def test_binding_signatures_match_header(sdc):
         fn = getattr(lib, name)
         assert fn.argtypes is not None, name
         assert len(fn.argtypes) == n_c, (name, n_c, len(fn.argtypes))
+
+
+def test_header_compiles_alone_and_layouts_match_binding(sdc, tmp_path):
+    """include/sdc.h compiled as C11 on its own (no CUDA header on the path, warnings as errors): every
+    struct's size and field offsets, the dtype codes and the limits equal the Python binding's."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if not cc:
+        pytest.skip("no C compiler")
+
+    def np_layout(dt):
+        return dt.itemsize, {n: dt.fields[n][1] for n in dt.names}
+
+    def ct_layout(cls):
+        return ctypes.sizeof(cls), {n: getattr(cls, n).offset for n, _ in cls._fields_}
+
+    expect = {
+        "sdc_tensor_desc": np_layout(sdc.DESC_DTYPE),
+        "sdc_grad_stats": np_layout(sdc.GRAD_STATS_DTYPE),
+        "sdc_vote_summary": np_layout(sdc.VOTE_SUMMARY_DTYPE),
+        "sdc_ring_summary": np_layout(sdc.RING_SUMMARY_DTYPE),
+        "sdc_adamw_hparams": ct_layout(sdc.AdamWHparams),
+        "sdc_plan_opts": ct_layout(sdc._PlanOpts),
+        "sdc_abft_summary": (8, {"n_flagged": 0, "n_flagged_cols": 4}),  # read as int32[2] by the binding
+    }
+    lines = ["#include <stddef.h>", "#include <stdio.h>", '#include "sdc.h"', "int main(void) {"]
+    for s, (_, fields) in expect.items():
+        lines.append(f'    printf("S {s} %zu\\n", sizeof({s}));')
+        for f in fields:
+            lines.append(f'    printf("F {s} {f} %zu\\n", offsetof({s}, {f}));')
+    statuses = ["SDC_OK", "SDC_ERR_NULL", "SDC_ERR_BAD_ELEM_SIZE", "SDC_ERR_SHAPE_MISMATCH", "SDC_ERR_TOO_MANY_REPLICAS",
+                "SDC_ERR_WS_TOO_SMALL", "SDC_ERR_CUDA", "SDC_ERR_BAD_DTYPE", "SDC_ERR_BAD_POINTER", "SDC_ERR_BAD_ARG",
+                "SDC_ERR_WRONG_DEVICE"]
+    for c in statuses + ["SDC_DTYPE_RAW", "SDC_DTYPE_F32", "SDC_DTYPE_BF16", "SDC_DTYPE_F16", "SDC_MAX_REPLICAS"]:
+        lines.append(f'    printf("C {c} %lu\\n", (unsigned long)({c}));')
+    lines.append('    printf("C SDC_NOALLOC_SCRATCH_BYTES %lu\\n", (unsigned long)(SDC_NOALLOC_SCRATCH_BYTES));')
+    lines += ["    return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                    "-o", str(exe)], check=True)
+    got_size, got_off, consts = {}, {}, {}
+    for line in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.splitlines():
+        f = line.split()
+        if f[0] == "S":
+            got_size[f[1]] = int(f[2])
+        elif f[0] == "F":
+            got_off[(f[1], f[2])] = int(f[3])
+        else:
+            consts[f[1]] = int(f[2])
+    for s, (size, fields) in expect.items():
+        assert got_size[s] == size, s
+        for f, off in fields.items():
+            assert got_off[(s, f)] == off, (s, f)
+    assert [consts[k] for k in ("SDC_DTYPE_RAW", "SDC_DTYPE_F32", "SDC_DTYPE_BF16", "SDC_DTYPE_F16")] == \
+        [sdc.DTYPE_RAW, sdc.DTYPE_F32, sdc.DTYPE_BF16, sdc.DTYPE_F16]
+    assert consts["SDC_MAX_REPLICAS"] == sdc.MAX_REPLICAS
+    for name in statuses:  # each status code's string is its name in the header
+        assert sdc.sdc_status_string(consts[name]) == name
+    assert consts["SDC_NOALLOC_SCRATCH_BYTES"] == sdc.NOALLOC_SCRATCH_BYTES
