@@ -637,11 +637,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 // The prep pass: one work unit per (head, 128-row block) of dO.  Persistent
 // CTAs take units round-robin; a unit's rows (contiguous, rows x 256 bytes)
 // arrive by one bulk copy into one of two shared-memory buffers, so the next
-// unit's copy runs while this one is summed; the unit's log-sum-exps come with
-// the same copy (rows x 4 bytes), so no thread waits on a global load.  Thread (column pair p, row
-// quarter h) sums columns 2p and 2p + 1 over rows 32h .. 32h + 31 as packed
-// float32 pairs (TwoSum), for dO and |dO|; quarters 1-3 are then merged into
-// quarter 0 in that order.
+// unit's copy runs while this one is summed; the unit's log-sum-exps come on
+// the same barrier (rows x 4 bytes), so no thread waits on a global load.
+// Thread (column pair p, row quarter h) sums columns 2p and 2p + 1 over rows
+// 32h .. 32h + 31 as packed float32 pairs (TwoSum), for dO and |dO|; quarters
+// 1-3 are then merged into quarter 0 in that order.
 constexpr uint32_t kPrepThreads = 256, kPrepQuarters = kPrepThreads / (kHD / 2);
 constexpr uint32_t kPrepScr = 2 * kTile;                                      // [3][64] x (dO pair, |dO| pair)
 constexpr uint32_t kPrepLse = kPrepScr + (kPrepQuarters - 1) * (kHD / 2) * 32;  // [2][128] float
