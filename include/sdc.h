@@ -344,7 +344,7 @@ size_t sdc_attn_workspace_size(uint32_t BH, uint32_t L, uint32_t D);
  * = 1 if a bounded wait gave up (results then invalid).
  * Errors: SDC_ERR_NULL, SDC_ERR_BAD_ARG (shapes, scale, tol_scale, causal),
  * SDC_ERR_BAD_POINTER (alignment), SDC_ERR_WRONG_DEVICE, SDC_ERR_WS_TOO_SMALL.
- * The workspace (256-byte aligned) holds per-block partial sums, lse log2(e)
+ * The workspace (256-byte aligned) holds per-block partial sums, -lse log2(e)
  * and the kernels' abort word and work counter. */
 sdc_status sdc_attn_dv_check(const void *d_Q, const void *d_K, const void *d_dO, const float *d_lse, uint32_t BH,
                              uint32_t L, uint32_t D, float scale, uint32_t causal, float tol_scale, void *d_dV,

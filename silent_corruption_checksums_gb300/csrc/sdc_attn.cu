@@ -20,7 +20,7 @@
 //   (every row of every P_h sums to 1).  group = 1 is plain multi-head attention.
 //
 // Kernels:
-//   attn_do_prep_kernel -- lse log2(e), and float32-pair column sums of dO
+//   attn_do_prep_kernel -- -lse log2(e), and float32-pair column sums of dO
 //     and |dO| per 128-row block (dO itself feeds the dV product as it is:
 //     its B operand, MN-major); persistent CTAs, each block's rows brought in
 //     by a bulk copy that overlaps the previous block's sums;
@@ -32,7 +32,7 @@
 //       the next item, hands it to the other roles through a 4-slot ring,
 //       copies its K tile into one of two K stages (so the next item's K
 //       arrives while this one runs), then per 128-query step the Q tile and
-//       the step's 128 log-sum-exps (times log2(e)) into their rings;
+//       the step's 128 log-sum-exps (times -log2(e)) into their rings;
 //     warp 3 lane 0: the dO copies, per step into a ring of their own (one
 //       copy thread per ring: a Q copy never waits behind a dO stage);
 //     warp 1 lane 0: S^T = K Q^T (M = keys, N = queries, K = 128) into one of
@@ -527,6 +527,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const uint32_t qpart = (warp - kSoftBase) >> 2;   // which kQPer of a step's queries
         const uint32_t j = quarter * 32 + lane;           // this thread's key within the item (its TMEM lane)
         const uint32_t lane_base = (quarter * 32) << 16;
+        const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
         uint32_t g = 0;
         for (uint32_t i = 0; ok; ++i) {
             const uint32_t slot = i % kItemSlots;
@@ -554,7 +555,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t lsa = s0 + kOffLse + ls * kBlk * 4 + qpart * kQPer * 4;  // lse log2(e) of its queries
+                const uint32_t lsa = s0 + kOffLse + ls * kBlk * 4 + qpart * kQPer * 4;  // -lse log2(e) of its queries
                 // steps that need a mask: the causal diagonal block, a partial last query block, a key
                 // past L (a partial last key block)
                 const bool diag = causal && qb == kb;
@@ -575,8 +576,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         const float l8[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
 #pragma unroll
                         for (uint32_t q = 0; q < 8; q += 2) {
-                            float p0 = ex2(__fmaf_rn(__uint_as_float(r[q8 * 8 + q]), scale_log2, -l8[q]));
-                            float p1 = ex2(__fmaf_rn(__uint_as_float(r[q8 * 8 + q + 1]), scale_log2, -l8[q + 1]));
+                            // both exponents in one packed FMA (each lane rounded as a scalar fma.rn)
+                            float x0, x1;
+                            f2_unpack(f2_fma(f2_pack_bits(r[q8 * 8 + q], r[q8 * 8 + q + 1]), scale2,
+                                             f2_pack(l8[q], l8[q + 1])),
+                                      x0, x1);
+                            float p0 = ex2(x0);
+                            float p1 = ex2(x1);
                             if constexpr (decltype(masked)::value) {  // selected, not multiplied: a masked
                                 p0 = (mbits >> (q8 * 8 + q)) & 1u ? p0 : 0.0f;       // score may be anything
                                 p1 = (mbits >> (q8 * 8 + q + 1)) & 1u ? p1 : 0.0f;
@@ -630,10 +636,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #undef BAR
 }
 
-// lse log2(e), and the column sums of dO and |dO| over one block of 128 rows:
-// block (x, y) takes rows 128x .. 128x + 127 of head y.  The tile goes through
-// shared memory (row-major, read back column-wise for the sums);
-// part_do[y][x][c] = {pair of sum_i dO[i, c], pair of sum_i |dO[i, c]|}.
+// -lse log2(e), and the column sums of dO and |dO| over each block of 128 rows:
+// part_do[head][block][c] = {pair of sum_i dO[i, c], pair of sum_i |dO[i, c]|}.
 // The prep pass: one work unit per (head, 128-row block) of dO.  Persistent
 // CTAs take units round-robin; a unit's rows (contiguous, rows x 256 bytes)
 // arrive by one bulk copy into one of two shared-memory buffers, so the next
@@ -691,8 +695,8 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
             }
             return;
         }
-        if (tid < rows)  // the exponent's offset in base 2
-            lse2[row0 + tid] = ((const float *)(psm + kPrepLse))[(i & 1) * kBlk + tid] * kLog2e;
+        if (tid < rows)  // the exponent's offset in base 2, negated: -(lse log2(e)) exactly, added by the softmax
+            lse2[row0 + tid] = ((const float *)(psm + kPrepLse))[(i & 1) * kBlk + tid] * -kLog2e;
         const uint32_t *tile = (const uint32_t *)(psm + (i & 1) * kTile);  // [128 rows][64 column pairs]
         uint64_t s = 0, c = 0, sa = 0, ca = 0;
         const uint32_t r0 = h * (kBlk / kPrepQuarters), r1 = min(r0 + kBlk / kPrepQuarters, rows);
@@ -734,7 +738,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
 size_t round_up256(size_t x) { return (x + 255) / 256 * 256; }
 
 // Workspace: dO partials [BH][L/128][128] float4 |
-// dV partials [BH][L/128][128] float2 | lse log2(e) [BH][L] float | the abort word, the dV
+// dV partials [BH][L/128][128] float2 | -lse log2(e) [BH][L] float | the abort word, the dV
 // kernel's work counter, its count of finished blocks (one word of padding) and of finished
 // key blocks per head [BH].
 struct AttnWs {
