@@ -1,0 +1,44 @@
+"""The benchmark's clock record on CPU: nvidia-smi samples (csv, no header, no
+units) are reduced to the median SM clock under load, the maximum clock and
+the throttle reasons seen, so that a throttled or clock-locked run can be
+recognised and rejected."""
+import bench
+
+CLEAN = "0, 2070, 2070, 880.50, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active\n"
+
+
+def _summary(tmp_path, lines):
+    s = bench.ClockSampler(0)
+    p = tmp_path / "clocks.csv"
+    p.write_text("".join(lines))
+    s.path = str(p)
+    return s.summary()
+
+
+def test_clean_run(tmp_path):
+    got = _summary(tmp_path, [CLEAN] * 5)
+    assert got == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 5}
+
+
+def test_reasons_and_median(tmp_path):
+    lines = [CLEAN,
+             "0, 1980, 2070, 1390.00, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n",
+             "0, 1500, 2070, 900.00, 0x0000000000000008, Active, Not Active, Not Active, Not Active\n",
+             "0, 2070, 2070, 900.00, 0x0000000000000000, Not Active, Active, Active, Not Active\n"]
+    got = _summary(tmp_path, lines)
+    assert got["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_power_cap", "sw_thermal_slowdown"]
+    assert got["sm_mhz"] == 2025.0 and got["sm_max_mhz"] == 2070.0 and got["samples"] == 4
+
+
+def test_clock_stuck_low_without_a_reason_is_visible(tmp_path):
+    # a leftover clock lock shows as a median far below the maximum with no reason active
+    got = _summary(tmp_path, ["0, 1200, 2070, 600.00, 0x0000000000000000, Not Active, Not Active, Not Active, "
+                              "Not Active\n"] * 3)
+    assert got["reasons"] == [] and got["sm_mhz"] == 1200.0 and got["sm_max_mhz"] == 2070.0
+
+
+def test_malformed_lines_are_skipped_and_no_samples_is_none(tmp_path):
+    got = _summary(tmp_path, ["garbage\n", "0, [N/A], 2070, 1, 0x0, Not Active, Not Active, Not Active, Not Active\n",
+                              CLEAN])
+    assert got["samples"] == 1
+    assert _summary(tmp_path, ["garbage\n"]) is None
