@@ -42,3 +42,25 @@ def test_malformed_lines_are_skipped_and_no_samples_is_none(tmp_path):
                               CLEAN])
     assert got["samples"] == 1
     assert _summary(tmp_path, ["garbage\n"]) is None
+
+
+def test_roofline_traffic_is_tied_to_the_kernel_source(tmp_path, monkeypatch):
+    # the committed ncu traffic is reported only while the fingerprint kernel's source is the one it
+    # was measured on, and only for the workload it was scaled to
+    import json
+    import os
+    import shutil
+    full = bench.scan_traffic(24)
+    d = json.load(open(os.path.join(bench.ROOT, "profiles", "fp_scan_traffic.json")))
+    assert full == d["dram_bytes_per_launch"] * d["scale_to_full"]
+    assert bench.scan_traffic(0) is None
+    fake = tmp_path / "root"
+    shutil.copytree(os.path.join(bench.ROOT, "profiles"), fake / "profiles")
+    csrc = fake / "silent_corruption_checksums_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    src = open(os.path.join(bench.ROOT, "silent_corruption_checksums_gb300", "csrc", "sdc_fp.cu"), "rb").read()
+    (csrc / "sdc_fp.cu").write_bytes(src)
+    monkeypatch.setattr(bench, "ROOT", str(fake))
+    assert bench.scan_traffic(24) == full
+    (csrc / "sdc_fp.cu").write_bytes(src + b"\n// changed\n")
+    assert bench.scan_traffic(24) is None
