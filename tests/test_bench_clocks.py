@@ -1,7 +1,9 @@
-"""The benchmark's clock record on CPU: nvidia-smi samples (csv, no header, no
-units) are reduced to the median SM clock under load, the maximum clock and
-the throttle reasons seen, so that a throttled or clock-locked run can be
-recognised and rejected."""
+"""The benchmark's run records on CPU.  The clock record: nvidia-smi samples
+(csv, no header, no units) are reduced to the median SM clock under load, the
+maximum clock and the throttle reasons seen, so that a throttled or
+clock-locked run can be recognised and rejected.  The roofline traffic: the
+committed ncu figure is used only while the kernel it was measured on is
+unchanged."""
 import bench
 
 CLEAN = "0, 2070, 2070, 880.50, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active\n"
