@@ -111,7 +111,7 @@ static_assert(kOffBar % 8 == 0, "mbarrier alignment");
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Programmatic dependent launch: the prep kernel lets the dV kernel launch at once, and the dV
-// kernel's threads that read the prep's results (lse log2(e), dO's column sums) wait for the prep
+// kernel's threads that read the prep's results (-lse log2(e), dO's column sums) wait for the prep
 // grid to complete first; its other work (TMEM, barriers, the K and Q copies) overlaps the prep's tail.
 // Without a dependent launch the wait returns at once.
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (warp == 0) {
         if (lane == 0) {  // ------------------------------------------ work queue + TMA
             uint32_t nk = 0, tl = 0, tq = 0;  // K tiles and steps whose copies were issued
-            bool prep_done = false;           // the prep grid's lse log2(e) is complete
+            bool prep_done = false;           // the prep grid's -lse log2(e) is complete
             for (uint32_t i = 0; ok; ++i) {
                 const uint32_t slot = i % kItemSlots;
                 if (i >= kItemSlots && !mbar_wait(BAR(kBarIE + slot), ((i / kItemSlots) - 1) & 1)) {
