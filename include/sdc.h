@@ -17,8 +17,11 @@
  *    them.  Host arrays are named host_* or documented as host arrays.
  *  - Every compute call is asynchronous: it validates its arguments on the
  *    host, enqueues its kernels on `stream` and returns; results appear in
- *    device memory in stream order.  No call synchronises the device, and no
- *    call allocates device memory except sdc_plan_create.
+ *    device memory in stream order.  No compute call synchronises the device
+ *    or allocates device memory; only sdc_plan_create and
+ *    sdc_opt_state_create allocate (their tables, uploaded with a synchronous
+ *    cudaMemcpy), and only their destroy calls free (cudaFree, which may wait
+ *    for work queued on the device).
  *  - `stream` is a cudaStream_t (same type; NULL = the legacy default stream).
  *  - Errors are returned as sdc_status codes, checked before anything is
  *    enqueued; nothing is enqueued when a call fails.  Every d_* array a call
@@ -151,8 +154,9 @@ typedef struct {
 sdc_status sdc_plan_create(const sdc_tensor_desc *host_descs, uint32_t T, uint32_t R,
                            const sdc_plan_opts *opts, sdc_plan **out);
 
-/* Free a plan and its device tables (synchronises nothing; the caller must
- * not destroy a plan whose work is still queued).  NULL is accepted. */
+/* Free a plan and its device tables with cudaFree (which may wait for work
+ * queued on the device); the caller must not destroy a plan whose work is
+ * still queued or will be.  NULL is accepted. */
 sdc_status sdc_plan_destroy(sdc_plan *plan);
 
 /* Bytes of device workspace the plan's compute calls need: per-chunk partials
