@@ -126,32 +126,6 @@ __device__ __forceinline__ double warp_column_sum(const uint32_t (&r)[32], uint3
     return (double)s + (double)c;
 }
 
-// The cluster pair's helpers: this CTA's rank, a multicast tile load (the box
-// lands at the same offset in both CTAs and completes on each one's barrier at
-// that offset), a commit that arrives on both CTAs' barriers, a cluster barrier.
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap *map, int32_t c0, int32_t c1,
-                                               uint32_t mbar, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(map), "r"(c0), "r"(c1), "r"(mbar), "h"(mask)
-        : "memory");
-}
-__device__ __forceinline__ void tc_commit_mc(uint32_t mbar, uint16_t mask) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                     mbar),
-                 "h"(mask)
-                 : "memory");
-}
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // Barrier over `count` threads that also ORs `pred` across them: every warp of the group takes the
 // same branch afterwards.
 __device__ __forceinline__ bool bar_any(uint32_t id, uint32_t count, bool pred) {
@@ -164,12 +138,7 @@ __device__ __forceinline__ bool bar_any(uint32_t id, uint32_t count, bool pred) 
     return r != 0;
 }
 
-// kMc: the CTAs run as clusters of two on vertically adjacent tiles (the same
-// W tile): each loads its own A tile and one 128-row half of the W tile,
-// multicast into both CTAs' shared memory, so each SM pulls 32 instead of 48
-// KiB per stage from L2.  A stage is free once both CTAs' MMAs have read it:
-// each MMA warp's commit arrives on both CTAs' `empty` barriers.
-template <bool kCols, bool kMc>
+template <bool kCols>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     abft_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapW,
                      __nv_bfloat16 *__restrict__ C, uint32_t M, uint32_t N, uint32_t K, uint32_t band_m,
@@ -186,15 +155,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // tiles cover C with zeros past M, N and K: the copies fill the rows and columns outside A and
     // W with zeros, which add nothing to a product or a checksum; the epilogue stores only inside C
     const uint32_t tiles_m = (M + kBM - 1) / kBM, tiles_n = (N + kBN - 1) / kBN, nkb = (K + kBK - 1) / kBK;
-    // work units: tiles, or (with kMc) pairs of vertically adjacent tiles, one per cluster
-    const uint32_t rank = kMc ? cluster_rank() : 0u;
-    const uint32_t units_m = kMc ? tiles_m / 2 : tiles_m, n_units = units_m * tiles_n;
-    const uint32_t unit0 = kMc ? blockIdx.x >> 1 : blockIdx.x, ustep = kMc ? gridDim.x >> 1 : gridDim.x;
-    auto coords = [&](uint32_t u, uint32_t &tm, uint32_t &tn) {
-        uint32_t um;
-        tile_coords(u, units_m, tiles_n, band_m, um, tn);
-        tm = kMc ? 2 * um + rank : um;
-    };
+    const uint32_t n_units = tiles_m * tiles_n, unit0 = blockIdx.x, ustep = gridDim.x;
+    auto coords = [&](uint32_t u, uint32_t &tm, uint32_t &tn) { tile_coords(u, tiles_m, tiles_n, band_m, tm, tn); };
 
     if (warp == 1) {  // the MMA warp owns both accumulators' TMEM columns
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
@@ -205,7 +167,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(full + 8 * s, 1);
-            mbar_init(empty + 8 * s, kMc ? 2 : 1);  // with kMc: both CTAs' MMAs
+            mbar_init(empty + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull + 8 * b, 1);
@@ -216,7 +178,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (kMc) cluster_sync();  // the peer's barriers exist before any multicast or commit reaches them
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     bool ok = true;
@@ -236,11 +197,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     mbar_arrive_expect_tx(full + 8 * s, kStageA + kStageW);
                     tma_load_2d(sA + s * kStageA, &mapA, (int32_t)(kb * kBK), row_a, full + 8 * s);
-                    if (kMc)  // this CTA's half of the W tile, into both CTAs
-                        tma_load_2d_mc(sW + s * kStageW + rank * (kStageW / 2), &mapW, (int32_t)(kb * kBK),
-                                       row_w + (int32_t)(rank * (kBN / 2)), full + 8 * s, (uint16_t)3);
-                    else
-                        tma_load_2d(sW + s * kStageW, &mapW, (int32_t)(kb * kBK), row_w, full + 8 * s);
+                    tma_load_2d(sW + s * kStageW, &mapW, (int32_t)(kb * kBK), row_w, full + 8 * s);
                 }
             }
             // Let no copy land in shared memory after the block has left: wait
@@ -273,8 +230,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     for (uint32_t ks = 0; ks < kBK / 16; ++ks)
                         tc_mma(d, umma_desc_sw128(sA + s * kStageA + ks * 32), umma_desc_sw128(sW + s * kStageW + ks * 32),
                                idesc, (kb | ks) != 0 ? 1u : 0u);
-                    if (kMc) tc_commit_mc(empty + 8 * s, (uint16_t)3);  // both producers wait for both MMAs
-                    else tc_commit(empty + 8 * s);  // the stage is free once these MMAs have read it
+                    tc_commit(empty + 8 * s);  // the stage is free once these MMAs have read it
                 }
                 if (ok) tc_commit(tfull + 8 * b);
             }
@@ -341,9 +297,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncthreads();
     if (warp == 1 && lane == 0 && !mbar_wait(done, 0)) atomicOr(err, 1);
     __syncwarp();
-    // with kMc: every MMA of both CTAs (and so every arrival on the peer's barriers) is
-    // complete, and every copy into either CTA has landed, before either leaves
-    if (kMc) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * kAccCols) : "memory");
@@ -643,11 +596,9 @@ sdc_status sdc_abft_gemm(const void *d_A, const void *d_W, void *d_C, uint32_t M
     if (st != SDC_OK) return st;
     if ((uint64_t)d_C & 15u) return fail(SDC_ERR_BAD_POINTER, "C must be 16-byte aligned");
     const uint32_t tiles_m = (M + kBM - 1) / kBM, tiles_n = (N + kBN - 1) / kBN, sms = (uint32_t)sm_count(dev);
-    // clusters of two on vertically adjacent tiles (W multicast) when the tile rows pair up
-    const bool mc = tiles_m % 2 == 0 && sms >= 2;
     CUtensorMap mapA, mapW;
     st = make_map_sw128(&mapA, d_A, M, K, kBM);
-    if (st == SDC_OK) st = make_map_sw128(&mapW, d_W, N, K, mc ? kBN / 2 : kBN);
+    if (st == SDC_OK) st = make_map_sw128(&mapW, d_W, N, K, kBN);
     if (st != SDC_OK) return st;
     const AbftWs w = abft_ws(M, N, K);
     double *part = (double *)((char *)d_ws + w.part);
@@ -655,32 +606,18 @@ sdc_status sdc_abft_gemm(const void *d_A, const void *d_W, void *d_C, uint32_t M
     int *err = (int *)((char *)d_ws + w.err);
     cudaStream_t s = (cudaStream_t)stream;
     const bool cols = d_colsum != nullptr;
-    auto kernel = cols ? (mc ? abft_gemm_kernel<true, true> : abft_gemm_kernel<true, false>)
-                       : (mc ? abft_gemm_kernel<false, true> : abft_gemm_kernel<false, false>);
+    auto kernel = cols ? abft_gemm_kernel<true> : abft_gemm_kernel<false>;
     cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int), s);
     const uint32_t smem_bytes = cols ? kGemmSmemCols : kGemmSmem;
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_gemm setup");
-    const uint32_t units_m = mc ? tiles_m / 2 : tiles_m, n_units = units_m * tiles_n;
-    // one CTA per SM: mc -> one cluster (two CTAs) per SM pair and work unit
-    const uint32_t grid = mc ? 2 * (n_units < sms / 2 ? n_units : sms / 2) : (n_units < sms ? n_units : sms);
-    // A band of tile rows holds about 24 MiB of A, a fraction of the 126 MiB L2 (in work-unit rows).
+    const uint32_t n_units = tiles_m * tiles_n;
+    const uint32_t grid = n_units < sms ? n_units : sms;  // one CTA per SM
+    // A band of tile rows holds about 24 MiB of A, a fraction of the 126 MiB L2.
     uint32_t band_m = (uint32_t)((24u << 20) / ((size_t)kBM * K * 2));
-    if (mc) band_m /= 2;
-    band_m = band_m < 1 ? 1 : (band_m > units_m ? units_m : band_m);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kGemmThreads);
-    cfg.dynamicSmemBytes = smem_bytes;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = mc ? 2 : 1;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kernel, mapA, mapW, (__nv_bfloat16 *)d_C, M, N, K, band_m, part, cpart, err);
+    band_m = band_m < 1 ? 1 : (band_m > tiles_m ? tiles_m : band_m);
+    kernel<<<grid, kGemmThreads, smem_bytes, s>>>(mapA, mapW, (__nv_bfloat16 *)d_C, M, N, K, band_m, part, cpart, err);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_gemm launch");
     abft_sum_parts_kernel<<<(M + 31) / 32, 256, 0, s>>>(part, M, tiles_n, d_rowsum, err, d_aborted);
     if (cols) abft_sum_parts_kernel<<<(N + 31) / 32, 256, 0, s>>>(cpart, N, tiles_m, d_colsum, nullptr, nullptr);

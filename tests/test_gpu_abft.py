@@ -221,7 +221,7 @@ RAGGED = [(1, 8, 8), (100, 264, 72), (129, 520, 1000), (200, 776, 4104), (300, 2
 def test_ragged_shapes(sdc, M, N, K, columns):
     # shapes that are not multiples of the 128 x 256 x 64 tiles (any M, N and K multiples of 8): the
     # copies fill the tiles' rows and columns outside A and W with zeros, the epilogue stores
-    # only inside C; odd and even tile-row counts (with and without the cluster pairs)
+    # only inside C; odd and even tile-row counts
     ops = W.gemm_operands(M, N, K, DEV, seed=70 + M + N + K)
     g = sdc.AbftGemm(M, N, K, DEV, columns=columns)
     g(ops["A"], ops["W"])

@@ -1,8 +1,8 @@
 """The tensor-core checks inside a CUDA graph and on concurrent streams.
 
 The GEMM with row + column checksums and the attention invariant reset their own
-counters with memset nodes and launch persistent kernels (one with clusters of two
-CTAs, one with a work queue): captured once and replayed, and run at the same time
+counters with memset nodes and launch persistent kernels (one over a banded tile
+schedule, one with a work queue): captured once and replayed, and run at the same time
 on two streams with their own workspaces, they give results bit-identical to eager
 calls on the same inputs, and a replay after an in-place change of an input reads
 the new values.
