@@ -158,7 +158,7 @@ sdc_status check_ws(const void *ws, size_t ws_bytes, size_t need, int device) {
 // Workspace: per-chunk partials, then the statistics combine's group sums.
 size_t plan_partials_bytes(const sdc_plan *p) { return round_up((size_t)p->n_chunks * sizeof(StatPartial), 256); }
 size_t plan_ws_bytes(const sdc_plan *p) {
-    return plan_partials_bytes(p) + round_up((size_t)p->R * kStatGroups * sizeof(StatPartial), 256);
+    return plan_partials_bytes(p) + round_up((size_t)p->R * kStatGroups * sizeof(StatGroup), 256);
 }
 
 size_t avg_chunks(uint64_t numel, uint32_t dtype) {
@@ -448,7 +448,7 @@ sdc_status sdc_grad_scan(const sdc_plan *plan, sdc_grad_stats *d_stats, void *d_
     if (st != SDC_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     StatPartial *part = (StatPartial *)d_ws;
-    StatPartial *groups = (StatPartial *)((char *)d_ws + plan_partials_bytes(plan));
+    StatGroup *groups = (StatGroup *)((char *)d_ws + plan_partials_bytes(plan));
     cudaError_t e = launch_grad_scan(plan, part, s);
     if (e == cudaSuccess) e = launch_stats_combine_plan(plan, part, groups, d_stats, s);
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_grad_scan launch");
@@ -459,7 +459,7 @@ size_t sdc_grad_average_scan_workspace_size(uint64_t numel, uint32_t n_bufs, uin
     if (dtype != SDC_DTYPE_F32 && dtype != SDC_DTYPE_BF16 && dtype != SDC_DTYPE_F16) return 0;
     const size_t nc = avg_chunks(numel, dtype);
     return round_up(nc * (n_bufs + 1) * sizeof(StatPartial), 256) +
-           round_up((size_t)(n_bufs + 1) * kStatGroups * sizeof(StatPartial), 256);
+           round_up((size_t)(n_bufs + 1) * kStatGroups * sizeof(StatGroup), 256);
 }
 
 }  // extern "C"
@@ -501,7 +501,7 @@ sdc_status sdc::grad_average_scan(const void *const *bufs, uint32_t n_bufs, void
     if (st != SDC_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     StatPartial *part = (StatPartial *)d_ws;
-    StatPartial *groups = (StatPartial *)((char *)d_ws + round_up(nc * (n_bufs + 1) * sizeof(StatPartial), 256));
+    StatGroup *groups = (StatGroup *)((char *)d_ws + round_up(nc * (n_bufs + 1) * sizeof(StatPartial), 256));
     e = launch_avg_scan(bufs, n_bufs, d_avg, numel, dtype, part, nc, aligned, dev, s);
     if (e == cudaSuccess) e = launch_stats_combine_streams(part, groups, n_bufs + 1, nc, numel, d_pre, d_post, s);
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_grad_average_scan launch");

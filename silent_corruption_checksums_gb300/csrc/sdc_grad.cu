@@ -12,31 +12,27 @@
 //
 // Why not a float64 add per element: this part's FP64 rate is a small
 // fraction of its FP32 rate, far below what a bf16 stream at HBM speed needs.
-// Instead each lane accumulates x^2 in float32 with an error-free TwoSum
-// (Knuth) on packed f32x2 pairs: (s, c) with s + c = sum exactly up to the
-// rounding of c.  The error of such a sum of n terms is below
-// gamma_{n-1}^2 * sum, gamma_k = k u / (1 - k u), u = 2^-24 (Ogita, Rump and
-// Oishi, "Accurate sum and dot product", 2005); with n = 64 terms per lane
-// half between flushes that is 1.4e-11 relative.  Every 16 vectors the pair
-// is added into the lane's own float32 pair (h, l) with TwoSum, and a warp's
-// lanes are added in a fixed xor tree of TwoSums; float64 is used only for the
-// warp's total (this part's FP64 pipe is slow, and per-run float64 adds kept
-// it a quarter busy), or for each lane's pair if the float32 tree overflows.
-//
-// Exactness of the float32 squares:
-//  - bf16: x is scaled by 2^59 before squaring, so every bf16 square -- down
-//    to the smallest subnormal, (2^-133)^2 -- lands on a multiple of 2^-149
-//    and is exact; the flushed sums are scaled back by 2^-118 in float64.
-//    Values with |x| >= 32 overflow the scaled square to Inf.
-//  - f16: squares of f16 values (22 significant bits, >= 2^-48) are exact.
+// Every lane instead adds squares in float32 and captures each add's rounding
+// error exactly, on packed f32x2 pairs:
+//  - bf16 and f16 (the "offset runs" below): each square is a float32, added
+//    with one fused multiply-add whose rounding error a second one recovers,
+//    the run's sum started at a power-of-two offset so that Sterbenz's lemma
+//    makes every step exact (checked after the run; a run that fails the
+//    check is redone).  Error below 3.8e-11 of each run's sum.
 //  - f32: x^2 = p + e exactly with p = fl(x*x), e = fma(x, x, -p), provided
-//    the biased exponent of x is >= 76 (or x == 0); smaller values are caught
-//    by a running minimum of the lane's magnitudes.
-// A run whose float32 sum is not finite (NaN, Inf, big, |bf16| >= 32, or an
-// overflowing sum, including the sum of the two packed halves: bf16 values of
-// magnitude 2.9 .. 4 leave each half finite after the 2^118 scaling and
-// overflow their sum) or that holds a tiny f32 value is redone exactly: each
-// element classified and its square added in float64 (exact squares).
+//    the biased exponent of x is >= 76 (or x == 0; smaller values are caught
+//    by a running minimum of the lane's magnitudes); p is added with Dekker's
+//    Fast2Sum on the ordered pair.  The error of such a sum of n terms is
+//    below gamma_{n-1}^2 * sum, gamma_k = k u / (1 - k u), u = 2^-24 (Ogita,
+//    Rump and Oishi, "Accurate sum and dot product", 2005); with n = 64 terms
+//    per lane half between flushes that is 1.4e-11 relative.
+// Each run is added into the lane's own float32 pair (h, l) with TwoSum, and
+// a warp's lanes are added in a fixed xor tree of TwoSums; float64 is used
+// only for the warp's total, or for each lane's pair if the float32 tree
+// overflows.
+// A run whose float32 sum is not finite (NaN, Inf, big, an overflowing sum)
+// or that holds a tiny f32 value is redone exactly: each element classified
+// and its square added in float64 (exact squares).
 // All reductions have a fixed shape, so results are identical on every run.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -49,8 +45,6 @@ namespace {
 
 constexpr int kRunVec = 16;           // vectors per lane between flushes
 constexpr double kFltMax = 3.4028234663852886e38;
-constexpr float kBf16Scale = 0x1p59f;   // 2^59
-constexpr double kBf16Unscale = 0x1p-118;
 constexpr uint32_t kF32TinyLimit = (76u << 24) - 2u;  // (bits << 1) - 2 below this: tiny, non-zero
 
 // ---------------------------------------------------------------- exact element path
@@ -98,40 +92,22 @@ struct FastAcc {
     uint32_t tmin = 0xFFFFFFFFu;
 };
 
-template <int DT>
-__device__ __forceinline__ void fast_vec(const uint4 &v, FastAcc &a) {
+// The f32 fast path (bf16 and f16 take the offset runs below).
+__device__ __forceinline__ void fast_vec_f32(const uint4 &v, FastAcc &a) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    if (DT == SDC_DTYPE_BF16) {
-        const uint64_t k = f2_pack(kBf16Scale, kBf16Scale);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint64_t p = f2_pack_bits(w[j] << 16, w[j] & 0xFFFF0000u);
-            p = f2_mul(p, k);
-            f2_two_sum_acc(a.s, a.c, f2_mul(p, p));
-        }
-    } else if (DT == SDC_DTYPE_F16) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float lo = __half2float(__ushort_as_half((unsigned short)(w[j] & 0xFFFFu)));
-            const float hi = __half2float(__ushort_as_half((unsigned short)(w[j] >> 16)));
-            const uint64_t p = f2_pack(lo, hi);
-            f2_two_sum_acc(a.s, a.c, f2_mul(p, p));
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < 4; j += 2) {
-            const uint64_t p = f2_pack_bits(w[j], w[j + 1]);
-            const uint64_t sq = f2_mul(p, p);
-            const uint64_t e = f2_fma(p, p, sq ^ 0x8000000080000000ull);  // x*x - fl(x*x), exact
-            f2_two_sum_acc(a.s, a.c, sq);
-            a.c = f2_add(a.c, e);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) a.tmin = min(a.tmin, w[j] * 2u - 2u);
+    for (int j = 0; j < 4; j += 2) {
+        const uint64_t p = f2_pack_bits(w[j], w[j + 1]);
+        const uint64_t sq = f2_mul(p, p);
+        const uint64_t e = f2_fma(p, p, sq ^ 0x8000000080000000ull);  // x*x - fl(x*x), exact
+        f2_two_sum_acc(a.s, a.c, sq);
+        a.c = f2_add(a.c, e);
     }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) a.tmin = min(a.tmin, w[j] * 2u - 2u);
 }
 
-// A lane's runs summed as a float32 pair h + l (in the dtype's scaled domain).
+// A lane's runs summed as a float32 pair h + l.
 struct FF {
     float h = 0.0f, l = 0.0f;
 };
@@ -165,15 +141,10 @@ __device__ __forceinline__ bool fast_flush_ff(FastAcc &a, FF &f) {
     return ok;
 }
 
-template <int DT>
-__device__ __forceinline__ double unscale(double acc_scaled) {
-    return DT == SDC_DTYPE_BF16 ? acc_scaled * kBf16Unscale : acc_scaled;
-}
-
 // The warp's total: the lanes' pairs added in a fixed xor tree (TwoSum's
 // error term is exact whichever operand comes first, so every lane ends with
 // the same bits); if that overflows float32, each lane's pair in float64
-// instead.  Then unscaled, plus the exactly summed elements (acc_e).
+// instead.  Then plus the exactly summed elements (acc_e).
 template <int DT>
 __device__ __forceinline__ double warp_total(const FF &f, double acc_e) {
     float h = f.h, l = f.l;
@@ -191,7 +162,6 @@ __device__ __forceinline__ double warp_total(const FF &f, double acc_e) {
         tot = __dadd_rn((double)h, (double)l);
     else
         tot = warp_sum_f64(__dadd_rn((double)f.h, (double)f.l));
-    tot = unscale<DT>(tot);
     if (__any_sync(0xffffffffu, acc_e != 0.0)) tot = __dadd_rn(tot, warp_sum_f64(acc_e));
     return tot;
 }
@@ -199,6 +169,186 @@ __device__ __forceinline__ double warp_total(const FF &f, double acc_e) {
 template <int DT>
 __device__ __forceinline__ uint32_t elems_per_vec() {
     return DT == SDC_DTYPE_F32 ? 4u : 8u;
+}
+
+// ---------------------------------------------------------------- 16-bit path: offset runs
+// For bf16 and f16 each square x^2 is a float32 (8- and 11-bit significands
+// square to at most 22 bits) unless it leaves the float32 range, so a lane can
+// add it with one fused multiply-add and recover the rounding error of that
+// add exactly, without ordering the operands:
+//   s' = fl(s + x^2) = fma(x, x, s),   d = s - s',   e = fma(x, x, d) = s + x^2 - s'.
+// d is exact by Sterbenz's lemma whenever s <= s' <= 2s, which holds when
+// x^2 <= s; then d + x^2 is the exact rounding error, a float32, so the second
+// fma returns it exactly.  To make x^2 <= s hold for every term, a run of
+// kRun16 vectors per lane (64 terms per packed half) starts its sum at an
+// offset sigma, the power of two at or above 2.5 times the previous run's sum;
+// the run is accepted only when, afterwards,
+//   (1) s_final <= 1.96875 sigma: then the run's true sum is below sigma (the
+//       rounding errors of s are below 2^-24 s each), so every term was below
+//       the running sum, every d and e above were exact, and s_final - sigma is
+//       exact (Sterbenz again);
+//   (2) sigma <= 16 (s_final - sigma): the errors e are at most 2^-24 sigma
+//       each (s stays inside one binade), and each vector's four are added
+//       pairwise before their sum joins c, so c is off by at most
+//       16 * 8 + 4 * 135 = 668 units of 2^-48 sigma: below 3.8e-11 of the run's sum;
+//   (3) sigma >= 2^-100: a bf16 square below 2^-126 is not a float32, and
+//       the second fma then rounds e by at most 2^-150, negligible against a
+//       run sum of at least 2^-104.
+// A packed half with sigma == 0 is accepted only when a pass over the run has
+// seen every one of its elements be +-0 (a square below 2^-149 rounds to 0,
+// so s == 0 alone does not show that the sum is 0).
+// A run that fails is redone from its vectors with sigma from its own sum
+// estimate (which then satisfies (1) and (2)), and if that fails too (NaN,
+// Inf, a square or sum past FLT_MAX, a tiny sum) element by element exactly.
+// Accepted runs are added into the lane's float32 pair (h, l) with TwoSum.
+constexpr int kRun16 = 16;
+
+struct SAcc {
+    uint64_t s, c;  // packed running sum (starting at sigma) and error sum
+};
+
+// A lane's accepted runs, packed halves: h + l.
+struct FF2 {
+    uint64_t h = 0, l = 0;
+};
+
+template <int DT>
+__device__ __forceinline__ uint64_t widen16(uint32_t w) {
+    if constexpr (DT == SDC_DTYPE_BF16) {
+        return f2_pack_bits(w << 16, w & 0xFFFF0000u);
+    } else {
+        return f2_pack(__half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu))),
+                       __half2float(__ushort_as_half((unsigned short)(w >> 16))));
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ void sacc_vec(const uint4 &v, SAcc &a) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint64_t e[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint64_t x = widen16<DT>(w[j]);
+        const uint64_t s1 = f2_fma(x, x, a.s);  // fl(s + x^2)
+        const uint64_t d = f2_sub(a.s, s1);     // exact while x^2 <= s
+        e[j] = f2_fma(x, x, d);                 // s + x^2 - s1, exact
+        a.s = s1;
+    }
+    a.c = f2_add(a.c, f2_add(f2_add(e[0], e[1]), f2_add(e[2], e[3])));
+}
+
+// The offset for the run after one whose sum is about est: the power of two
+// at or above 2.5 est (0 when est is not a positive finite value).
+__device__ __forceinline__ float sigma_from(float est) {
+    const float y = 2.5f * est;
+    if (!(y > 0.0f) || !isfinite(y)) return 0.0f;
+    return __uint_as_float((__float_as_uint(y) + 0x007FFFFFu) & 0xFF800000u);
+}
+__device__ __forceinline__ uint64_t sigma_next(uint64_t est) {
+    float e0, e1;
+    f2_unpack(est, e0, e1);
+    return f2_pack(sigma_from(e0), sigma_from(e1));
+}
+
+// zero: every element of the half is known to be +-0 (then sigma is 0 too).
+__device__ __forceinline__ bool sigma_half_ok(float s, float g, float q, bool zero) {
+    return (g >= 0x1p-100f && s <= 1.96875f * g && g <= 16.0f * q) || (zero && g == 0.0f);
+}
+
+// Checks conditions (1)-(3) on both halves and, when they hold, adds the run
+// into f.  est receives the run's sum estimate (s - sigma + c) either way.
+// zero0 / zero1: the low / high half's elements are all known to be +-0.
+__device__ __forceinline__ bool sacc_accept(const SAcc &a, uint64_t sig, FF2 &f, uint64_t &est, bool zero0 = false,
+                                            bool zero1 = false) {
+    const uint64_t q = f2_sub(a.s, sig);  // exact when (1) holds
+    est = f2_add(q, a.c);
+    float s0, s1, g0, g1, q0, q1;
+    f2_unpack(a.s, s0, s1);
+    f2_unpack(sig, g0, g1);
+    f2_unpack(q, q0, q1);
+    if (!(sigma_half_ok(s0, g0, q0, zero0) && sigma_half_ok(s1, g1, q1, zero1))) return false;
+    const uint64_t t = f2_add(f.h, q);  // TwoSum(h, q)
+    const uint64_t bb = f2_sub(t, f.h);
+    const uint64_t err = f2_add(f2_sub(f.h, f2_sub(t, bb)), f2_sub(q, bb));
+    float t0, t1;
+    f2_unpack(t, t0, t1);
+    if (!(isfinite(t0) && isfinite(t1))) return false;
+    f.h = t;
+    f.l = f2_add(f.l, f2_add(a.c, err));
+    return true;
+}
+
+// A failed run again from its vectors (lane + 32 i for i in [r0, r1), below
+// nvec) with the offset sig.
+template <int DT>
+__device__ __forceinline__ bool sacc_redo(const uint4 *src, uint32_t lane, uint32_t r0, uint32_t r1, uint32_t nvec,
+                                          uint64_t sig, FF2 &f) {
+    SAcc b{sig, 0ull};
+    uint32_t mag = 0;  // OR of the magnitude bits of both halves' elements
+    for (uint32_t i = r0; i < r1; ++i) {
+        const uint32_t vi = lane + (i << 5);
+        if (vi < nvec) {
+            const uint4 v = src[vi];
+            sacc_vec<DT>(v, b);
+            mag |= v.x | v.y | v.z | v.w;
+        }
+    }
+    mag &= 0x7FFF7FFFu;
+    uint64_t est;
+    return sacc_accept(b, sig, f, est, (mag & 0xFFFFu) == 0, (mag >> 16) == 0);
+}
+
+// A run that the offset check refused, out of line (rare; keeping it out of
+// the scan loops keeps their code small): redone with the offset sig, else
+// element by element exactly into acc / cnt (the nan, inf and big counts at
+// cnt[0], cnt[stride], cnt[2 stride]).  Returns the lane's updated pair.
+template <int DT>
+__device__ __noinline__ FF2 run_fallback(const uint4 *src, uint32_t lane, uint32_t r0, uint32_t r1, uint32_t nvec,
+                                         uint64_t sig, FF2 f, double *acc, uint32_t *cnt, uint32_t stride) {
+    if (sacc_redo<DT>(src, lane, r0, r1, nvec, sig, f)) return f;
+    double a = *acc;
+    Counts n;
+    n.nan = cnt[0];
+    n.inf = cnt[stride];
+    n.big = cnt[2 * stride];
+    for (uint32_t i = r0; i < r1; ++i) {
+        const uint32_t vi = lane + (i << 5);
+        if (vi < nvec) exact_vec<DT>(src[vi], a, n);
+    }
+    *acc = a;
+    cnt[0] = n.nan;
+    cnt[stride] = n.inf;
+    cnt[2 * stride] = n.big;
+    return f;
+}
+
+// The warp's total from the lanes' packed pairs: each lane's halves merged
+// with TwoSum, then the same fixed xor tree as warp_total (float64 per lane if
+// the float32 sums overflow), plus the exactly summed elements acc_e.
+__device__ __forceinline__ double warp_total2(const FF2 &f, double acc_e) {
+    float h0, h1, l0, l1;
+    f2_unpack(f.h, h0, h1);
+    f2_unpack(f.l, l0, l1);
+    const float t = __fadd_rn(h0, h1);
+    const float bb = __fsub_rn(t, h0);
+    const float e = __fadd_rn(__fsub_rn(h0, __fsub_rn(t, bb)), __fsub_rn(h1, bb));
+    float h = t, l = __fadd_rn(__fadd_rn(l0, l1), e);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ho = __shfl_xor_sync(0xffffffffu, h, o), lo = __shfl_xor_sync(0xffffffffu, l, o);
+        const float t2 = __fadd_rn(h, ho);
+        const float b2 = __fsub_rn(t2, h);
+        const float e2 = __fadd_rn(__fsub_rn(h, __fsub_rn(t2, b2)), __fsub_rn(ho, b2));
+        h = t2;
+        l = __fadd_rn(__fadd_rn(l, lo), e2);
+    }
+    double tot;
+    if (isfinite(h))  // the same on every lane
+        tot = __dadd_rn((double)h, (double)l);
+    else
+        tot = warp_sum_f64(__dadd_rn(__dadd_rn((double)h0, (double)h1), __dadd_rn((double)l0, (double)l1)));
+    if (__any_sync(0xffffffffu, acc_e != 0.0)) tot = __dadd_rn(tot, warp_sum_f64(acc_e));
+    return tot;
 }
 
 // ---------------------------------------------------------------- plan-based scan
@@ -219,8 +369,25 @@ __device__ __forceinline__ GGeom ggeom(const Chunk &ch) {
     return g;
 }
 
+// A chunk's head and tail elements (fewer than 8 of each, outside its
+// 16-byte vectors), exactly: lanes 0..7 the head, lanes 16..23 the tail.
+template <int DT>
+__device__ __forceinline__ void grad_head_tail(const GGeom &g, uint32_t lane, double &acc_exact, Counts &n) {
+    const uint32_t he = g.head >> g.l2, te = g.tail >> g.l2;
+    if (lane < he) {
+        const uint64_t a = g.addr + ((uint64_t)lane << g.l2);
+        const uint32_t bits = g.l2 == 2 ? *(const uint32_t *)a : (uint32_t)(*(const uint16_t *)a);
+        exact_elem(bits, DT, acc_exact, n);
+    } else if (lane >= 16 && lane - 16 < te) {
+        const uint64_t a = g.addr + g.head + ((uint64_t)g.nvec << 4) + ((uint64_t)(lane - 16) << g.l2);
+        const uint32_t bits = g.l2 == 2 ? *(const uint32_t *)a : (uint32_t)(*(const uint16_t *)a);
+        exact_elem(bits, DT, acc_exact, n);
+    }
+}
+
 template <int DT, int U>
 __device__ __forceinline__ double grad_chunk(const GGeom &g, uint32_t lane, Counts &n) {
+    static_assert(DT == SDC_DTYPE_F32, "bf16 and f16 take grad_chunk16");
     const uint4 *vb = (const uint4 *)(g.addr + g.head);
     const uint32_t niter = (g.nvec + 31) >> 5;
     FF ff;
@@ -239,7 +406,7 @@ __device__ __forceinline__ double grad_chunk(const GGeom &g, uint32_t lane, Coun
                 v[u] = (i0 + u < r1 && vi < g.nvec) ? ld_stream(vb + vi) : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
-            for (int u = 0; u < U; ++u) fast_vec<DT>(v[u], a);
+            for (int u = 0; u < U; ++u) fast_vec_f32(v[u], a);
         }
         if (!fast_flush_ff<DT>(a, ff)) {
             for (uint32_t i = r0; i < r1; ++i) {
@@ -248,18 +415,51 @@ __device__ __forceinline__ double grad_chunk(const GGeom &g, uint32_t lane, Coun
             }
         }
     }
-    // head and tail elements (fewer than 8 of each), exactly
-    const uint32_t he = g.head >> g.l2, te = g.tail >> g.l2;
-    if (lane < he) {
-        const uint64_t a = g.addr + ((uint64_t)lane << g.l2);
-        const uint32_t bits = g.l2 == 2 ? *(const uint32_t *)a : (uint32_t)(*(const uint16_t *)a);
-        exact_elem(bits, DT, acc_exact, n);
-    } else if (lane >= 16 && lane - 16 < te) {
-        const uint64_t a = g.addr + g.head + ((uint64_t)g.nvec << 4) + ((uint64_t)(lane - 16) << g.l2);
-        const uint32_t bits = g.l2 == 2 ? *(const uint32_t *)a : (uint32_t)(*(const uint16_t *)a);
-        exact_elem(bits, DT, acc_exact, n);
-    }
+    grad_head_tail<DT>(g, lane, acc_exact, n);
     return warp_total<DT>(ff, acc_exact);  // the warp's total, on every lane
+}
+
+// The 16-bit form: U vectors per lane in flight, taken as runs of kRun16 that
+// start at the lane's offset sig, which carries over from chunk to chunk.
+template <int DT, int U>
+__device__ __forceinline__ double grad_chunk16(const GGeom &g, uint32_t lane, Counts &n, uint64_t &sig) {
+    static_assert(U % kRun16 == 0, "whole runs per batch");
+    const uint4 *vb = (const uint4 *)(g.addr + g.head);
+    const uint32_t niter = (g.nvec + 31) >> 5;
+    FF2 ff;
+    double acc_exact = 0.0;
+    if (lane == 0 && g.nvec) prefetch_l2_bulk(vb, g.nvec * 16u);
+    for (uint32_t b0 = 0; b0 < niter; b0 += U) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t vi = lane + ((b0 + u) << 5);
+            v[u] = (b0 + u < niter && vi < g.nvec) ? ld_stream(vb + vi) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int r = 0; r < U; r += kRun16) {
+            const uint32_t r0 = b0 + r;
+            if (r0 < niter) {  // the same on every lane
+                const uint32_t r1 = min(r0 + (uint32_t)kRun16, niter);
+                SAcc a{sig, 0ull};
+#pragma unroll
+                for (int u = r; u < r + kRun16; ++u) sacc_vec<DT>(v[u], a);  // zeros past the end add nothing
+                uint64_t est;
+                const bool ok = sacc_accept(a, sig, ff, est);
+                const uint64_t sn = sigma_next(est);
+                if (!ok) {
+                    uint32_t cnt[3] = {n.nan, n.inf, n.big};
+                    ff = run_fallback<DT>(vb, lane, r0, r1, g.nvec, sn, ff, &acc_exact, cnt, 1);
+                    n.nan = cnt[0];
+                    n.inf = cnt[1];
+                    n.big = cnt[2];
+                }
+                sig = sn;
+            }
+        }
+    }
+    grad_head_tail<DT>(g, lane, acc_exact, n);
+    return warp_total2(ff, acc_exact);
 }
 
 template <int U>
@@ -268,6 +468,7 @@ __global__ void __launch_bounds__(kScanBlock) grad_scan_kernel(const Chunk *__re
     const uint32_t lane = threadIdx.x & 31u;
     const uint64_t warp = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const uint64_t nwarps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
+    uint64_t sig = 0ull;  // the 16-bit path's run offset, carried across the warp's chunks
     for (uint64_t c = warp; c < n_chunks; c += nwarps) {
         const Chunk ch = chunks[c];
         const GGeom g = ggeom(ch);
@@ -275,8 +476,8 @@ __global__ void __launch_bounds__(kScanBlock) grad_scan_kernel(const Chunk *__re
         double acc;
         switch (chunk_dtype(ch.tag)) {
             case SDC_DTYPE_F32: acc = grad_chunk<SDC_DTYPE_F32, U>(g, lane, n); break;
-            case SDC_DTYPE_BF16: acc = grad_chunk<SDC_DTYPE_BF16, U>(g, lane, n); break;
-            default: acc = grad_chunk<SDC_DTYPE_F16, U>(g, lane, n); break;
+            case SDC_DTYPE_BF16: acc = grad_chunk16<SDC_DTYPE_BF16, U>(g, lane, n, sig); break;
+            default: acc = grad_chunk16<SDC_DTYPE_F16, U>(g, lane, n, sig); break;
         }
         const uint32_t nn = warp_sum_u32(n.nan), ni = warp_sum_u32(n.inf), nb = warp_sum_u32(n.big);
         if (lane == 0) partials[c] = StatPartial{acc, nn, ni, nb, 0u};
@@ -410,8 +611,9 @@ __device__ __forceinline__ void store_bits(void *p, uint64_t i, uint32_t v) {
 template <int DT, int NB, int U>
 __global__ void __launch_bounds__(kScanBlock) avg_scan_kernel(BufPtrs bp, void *__restrict__ outp, uint64_t numel,
                                                               uint64_t n_chunks, StatPartial *__restrict__ partials) {
+    static_assert(DT == SDC_DTYPE_F32, "bf16 and f16 take avg_scan16_kernel");
     constexpr int NS = NB + 1;
-    constexpr uint32_t ES = DT == SDC_DTYPE_F32 ? 4u : 2u;
+    constexpr uint32_t ES = 4u;
     constexpr uint64_t CE = kAvgChunkBytes / ES;
     const float inv = 1.0f / (float)NB;
     const uint32_t lane = threadIdx.x & 31u;
@@ -457,14 +659,14 @@ __global__ void __launch_bounds__(kScanBlock) avg_scan_kernel(BufPtrs bp, void *
                     const uint32_t vi = lane + ((i0 + u) << 5);
                     const bool ok = i0 + u < r1 && vi < nvec;
 #pragma unroll
-                    for (int b = 0; b < NB; ++b) fast_vec<DT>(v[u][b], a[b]);
+                    for (int b = 0; b < NB; ++b) fast_vec_f32(v[u][b], a[b]);
                     uint4 o = avg_vec<DT, NB>(v[u], inv);
                     if (ok) {
                         __stcs(out + vi, o);
                     } else {
                         o = make_uint4(0, 0, 0, 0);
                     }
-                    fast_vec<DT>(o, a[NB]);
+                    fast_vec_f32(o, a[NB]);
                 }
             }
 #pragma unroll
@@ -492,6 +694,120 @@ __global__ void __launch_bounds__(kScanBlock) avg_scan_kernel(BufPtrs bp, void *
         for (int s = 0; s < NS; ++s) {
             const double acc = warp_total<DT>(ff[s], acc_e[s]);
             const uint32_t nn = warp_sum_u32(n[s].nan), ni = warp_sum_u32(n[s].inf), nbg = warp_sum_u32(n[s].big);
+            if (lane == 0) partials[(uint64_t)s * n_chunks + c] = StatPartial{acc, nn, ni, nbg, 0u};
+        }
+    }
+}
+
+// The 16-bit form of avg_scan_kernel (bf16, f16): every stream accumulated in
+// offset runs of kRun16 vectors per lane, each stream's offset carried across
+// the warp's tasks.  The exact path's sums and counts, touched only by runs
+// that fail and by the tail, live in shared memory ([stream][thread]) so that
+// two blocks of 256 threads fit on an SM.
+template <int DT, int NB, int U>
+__global__ void __launch_bounds__(kScanBlock) avg_scan16_kernel(BufPtrs bp, void *__restrict__ outp, uint64_t numel,
+                                                                uint64_t n_chunks, StatPartial *__restrict__ partials) {
+    static_assert(kRun16 % U == 0, "whole batches per run");
+    constexpr int NS = NB + 1;
+    constexpr uint64_t CE = kAvgChunkBytes / 2;
+    __shared__ double sh_acc[NS][kScanBlock];
+    __shared__ uint32_t sh_cnt[NS][3][kScanBlock];
+    const float inv = 1.0f / (float)NB;
+    const uint32_t tid = threadIdx.x, lane = tid & 31u;
+    const uint64_t warp = ((uint64_t)blockIdx.x * blockDim.x + tid) >> 5;
+    const uint64_t nwarps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
+    uint64_t sig[NS];
+#pragma unroll
+    for (int s = 0; s < NS; ++s) sig[s] = 0ull;
+    for (uint64_t c = warp; c < n_chunks; c += nwarps) {
+        const uint64_t e0 = c * CE;
+        const uint64_t ne = min(CE, numel - e0);
+        const uint32_t nvec = (uint32_t)((ne * 2u) >> 4);
+        const uint32_t niter = (nvec + 31) >> 5;
+        const uint4 *in[NB];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) in[b] = (const uint4 *)((const char *)bp.p[b] + e0 * 2u);
+        uint4 *out = (uint4 *)((char *)outp + e0 * 2u);
+        FF2 ff[NS];
+#pragma unroll
+        for (int s = 0; s < NS; ++s) {
+            sh_acc[s][tid] = 0.0;
+            sh_cnt[s][0][tid] = sh_cnt[s][1][tid] = sh_cnt[s][2][tid] = 0u;
+        }
+        for (uint32_t r0 = 0; r0 < niter; r0 += kRun16) {
+            const uint32_t r1 = min(r0 + (uint32_t)kRun16, niter);
+            SAcc a[NS];
+#pragma unroll
+            for (int s = 0; s < NS; ++s) a[s] = SAcc{sig[s], 0ull};
+            for (uint32_t i0 = r0; i0 < r1; i0 += U) {  // not unrolled: the body stays in the instruction cache
+                // L2 prefetch of the batch after next: lanes 0, 8, 16, 24 touch the
+                // four 128-byte lines of each input's 512-byte warp slice
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const uint32_t vi = lane + ((i0 + 2 * U + u) << 5);
+                    if ((lane & 7u) == 0 && vi < nvec)
+#pragma unroll
+                        for (int b = 0; b < NB; ++b) prefetch_l2(in[b] + vi);
+                }
+                uint4 v[U][NB];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const uint32_t vi = lane + ((i0 + u) << 5);
+                    const bool ok = i0 + u < r1 && vi < nvec;
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) v[u][b] = ok ? ld_stream(in[b] + vi) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const uint32_t vi = lane + ((i0 + u) << 5);
+                    const bool ok = i0 + u < r1 && vi < nvec;
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) sacc_vec<DT>(v[u][b], a[b]);
+                    uint4 o = avg_vec<DT, NB>(v[u], inv);
+                    if (ok) {
+                        __stcs(out + vi, o);
+                    } else {
+                        o = make_uint4(0, 0, 0, 0);
+                    }
+                    sacc_vec<DT>(o, a[NB]);
+                }
+            }
+#pragma unroll
+            for (int s = 0; s < NS; ++s) {
+                uint64_t est;
+                const bool ok = sacc_accept(a[s], sig[s], ff[s], est);
+                const uint64_t sn = sigma_next(est);
+                if (!ok)
+                    ff[s] = run_fallback<DT>(s < NB ? in[s] : (const uint4 *)out, lane, r0, r1, nvec, sn, ff[s],
+                                             &sh_acc[s][tid], &sh_cnt[s][0][tid], kScanBlock);
+                sig[s] = sn;
+            }
+        }
+        // tail elements of the last chunk (fewer than one vector)
+        const uint64_t done = (uint64_t)nvec * 8u;
+        if (lane < ne - done) {
+            const uint64_t i = e0 + done + lane;
+            const uint32_t r = avg_elem<DT>(bp, NB, i);
+            store_bits<DT>(outp, i, r);
+#pragma unroll
+            for (int s = 0; s < NS; ++s) {
+                double acc = sh_acc[s][tid];
+                Counts cn;
+                cn.nan = sh_cnt[s][0][tid];
+                cn.inf = sh_cnt[s][1][tid];
+                cn.big = sh_cnt[s][2][tid];
+                exact_elem(s < NB ? load_bits<DT>(bp.p[s], i) : r, DT, acc, cn);
+                sh_acc[s][tid] = acc;
+                sh_cnt[s][0][tid] = cn.nan;
+                sh_cnt[s][1][tid] = cn.inf;
+                sh_cnt[s][2][tid] = cn.big;
+            }
+        }
+#pragma unroll
+        for (int s = 0; s < NS; ++s) {
+            const double acc = warp_total2(ff[s], sh_acc[s][tid]);
+            const uint32_t nn = warp_sum_u32(sh_cnt[s][0][tid]), ni = warp_sum_u32(sh_cnt[s][1][tid]),
+                           nbg = warp_sum_u32(sh_cnt[s][2][tid]);
             if (lane == 0) partials[(uint64_t)s * n_chunks + c] = StatPartial{acc, nn, ni, nbg, 0u};
         }
     }
@@ -588,7 +904,7 @@ __device__ __forceinline__ Acc block_reduce(Acc a) {
 }
 
 __global__ void __launch_bounds__(kCombineBlock) stats_combine1_kernel(const StatPartial *__restrict__ partials,
-                                                                       StreamSel sel, StatPartial *__restrict__ groups) {
+                                                                       StreamSel sel, StatGroup *__restrict__ groups) {
     const uint32_t s = blockIdx.y, g = blockIdx.x;
     uint64_t base, count;
     stream_range(sel, s, base, count);
@@ -603,16 +919,16 @@ __global__ void __launch_bounds__(kCombineBlock) stats_combine1_kernel(const Sta
     }
     a = block_reduce(a);
     if (threadIdx.x == 0)
-        groups[(uint64_t)s * kStatGroups + g] = StatPartial{a.sum, (uint32_t)a.nan, (uint32_t)a.inf, (uint32_t)a.big, 0u};
+        groups[(uint64_t)s * kStatGroups + g] = StatGroup{a.sum, a.nan, a.inf, a.big};
 }
 
-__global__ void __launch_bounds__(kCombineBlock) stats_combine2_kernel(const StatPartial *__restrict__ groups,
+__global__ void __launch_bounds__(kCombineBlock) stats_combine2_kernel(const StatGroup *__restrict__ groups,
                                                                        StreamSel sel, sdc_grad_stats *out_pre,
                                                                        sdc_grad_stats *out_post) {
     const uint32_t s = blockIdx.x;
     Acc a{0.0, 0, 0, 0};
     for (uint32_t g = threadIdx.x; g < kStatGroups; g += kCombineBlock) {
-        const StatPartial p = groups[(uint64_t)s * kStatGroups + g];
+        const StatGroup p = groups[(uint64_t)s * kStatGroups + g];
         a.sum = __dadd_rn(a.sum, p.sumsq);
         a.nan += p.n_nan;
         a.inf += p.n_inf;
@@ -636,7 +952,7 @@ __global__ void __launch_bounds__(kCombineBlock) stats_combine2_kernel(const Sta
     }
 }
 
-cudaError_t launch_combine(const StatPartial *partials, StatPartial *groups, const StreamSel &sel,
+cudaError_t launch_combine(const StatPartial *partials, StatGroup *groups, const StreamSel &sel,
                            sdc_grad_stats *out_pre, sdc_grad_stats *out_post, cudaStream_t st) {
     stats_combine1_kernel<<<dim3(kStatGroups, sel.n_streams), kCombineBlock, 0, st>>>(partials, sel, groups);
     cudaError_t e = cudaGetLastError();
@@ -647,17 +963,21 @@ cudaError_t launch_combine(const StatPartial *partials, StatPartial *groups, con
 
 constexpr int kGradUnroll = 16;  // a whole run (kRunVec vectors per lane) in flight
 constexpr int kAvgUnroll = 2;
+constexpr int kAvg16Unroll = 2;
 
 template <int DT, int NB>
 cudaError_t launch_avg_t(const BufPtrs &bp, void *avg, uint64_t numel, StatPartial *partials, uint64_t n_chunks,
                          int device, cudaStream_t st) {
+    void (*kernel)(BufPtrs, void *, uint64_t, uint64_t, StatPartial *);
+    if constexpr (DT == SDC_DTYPE_F32) kernel = avg_scan_kernel<DT, NB, kAvgUnroll>;
+    else kernel = avg_scan16_kernel<DT, NB, kAvg16Unroll>;
     int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, avg_scan_kernel<DT, NB, kAvgUnroll>, kScanBlock, 0);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kScanBlock, 0);
     if (per_sm < 1) per_sm = 1;
     uint64_t grid = (uint64_t)sm_count(device) * per_sm;
     const uint64_t need = (n_chunks * 32 + kScanBlock - 1) / kScanBlock;
     if (need < grid) grid = need;
-    avg_scan_kernel<DT, NB, kAvgUnroll><<<(unsigned)grid, kScanBlock, 0, st>>>(bp, avg, numel, n_chunks, partials);
+    kernel<<<(unsigned)grid, kScanBlock, 0, st>>>(bp, avg, numel, n_chunks, partials);
     return cudaGetLastError();
 }
 
@@ -693,7 +1013,7 @@ cudaError_t launch_grad_scan(const sdc_plan *plan, StatPartial *partials, cudaSt
     return cudaGetLastError();
 }
 
-cudaError_t launch_stats_combine_plan(const sdc_plan *plan, const StatPartial *partials, StatPartial *groups,
+cudaError_t launch_stats_combine_plan(const sdc_plan *plan, const StatPartial *partials, StatGroup *groups,
                                       sdc_grad_stats *out, cudaStream_t st) {
     StreamSel sel{plan->d_replica_first_chunk, plan->d_replica_numel, 0, 0, plan->R, plan->R};
     return launch_combine(partials, groups, sel, out, out, st);
@@ -729,7 +1049,7 @@ cudaError_t launch_avg_scan(const void *const *bufs, uint32_t n_bufs, void *avg,
     return cudaGetLastError();
 }
 
-cudaError_t launch_stats_combine_streams(const StatPartial *partials, StatPartial *groups, uint32_t n_streams,
+cudaError_t launch_stats_combine_streams(const StatPartial *partials, StatGroup *groups, uint32_t n_streams,
                                          uint64_t n_chunks, uint64_t numel, sdc_grad_stats *out_pre,
                                          sdc_grad_stats *out_post, cudaStream_t st) {
     StreamSel sel{nullptr, nullptr, n_chunks, numel, n_streams, n_streams - 1};

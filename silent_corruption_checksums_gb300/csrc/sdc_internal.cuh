@@ -62,6 +62,16 @@ struct StatPartial {
 };
 static_assert(sizeof(StatPartial) == 24, "StatPartial is 24 bytes");
 
+// One of the statistics combine's fixed groups: counts in 64 bits (a group
+// may cover more than 2^32 elements of one stream).
+struct StatGroup {
+    double sumsq;
+    uint64_t n_nan;
+    uint64_t n_inf;
+    uint64_t n_big;
+};
+static_assert(sizeof(StatGroup) == 32, "StatGroup is 32 bytes");
+
 }  // namespace sdc
 
 // The plan (opaque to callers).
@@ -116,12 +126,12 @@ cudaError_t launch_xor_scan(const sdc_plan *plan, uint64_t *partials, cudaStream
 cudaError_t launch_xor_combine(const sdc_plan *plan, const uint64_t *partials, uint64_t *out,
                                cudaStream_t st);
 cudaError_t launch_grad_scan(const sdc_plan *plan, StatPartial *partials, cudaStream_t st);
-cudaError_t launch_stats_combine_plan(const sdc_plan *plan, const StatPartial *partials, StatPartial *groups,
+cudaError_t launch_stats_combine_plan(const sdc_plan *plan, const StatPartial *partials, StatGroup *groups,
                                       sdc_grad_stats *out, cudaStream_t st);
 cudaError_t launch_avg_scan(const void *const *bufs, uint32_t n_bufs, void *avg, uint64_t numel,
                             uint32_t dtype, StatPartial *partials, uint64_t n_chunks, bool vector_path,
                             int device, cudaStream_t st);
-cudaError_t launch_stats_combine_streams(const StatPartial *partials, StatPartial *groups, uint32_t n_streams,
+cudaError_t launch_stats_combine_streams(const StatPartial *partials, StatGroup *groups, uint32_t n_streams,
                                          uint64_t n_chunks, uint64_t numel, sdc_grad_stats *out_pre,
                                          sdc_grad_stats *out_post, cudaStream_t st);
 cudaError_t launch_vote(const uint64_t *fp, uint32_t R, uint32_t T, int32_t *suspect, uint64_t *mask,

@@ -93,8 +93,9 @@ def test_host_validation_without_gpu(sdc):
         sdc.sdc_grad_average_scan([4096], 8192, 10, 0, 8, 8, 0, 0, 0)
     assert ei.value.status == 7
     # per-task partials (one 16 KiB task x 5 streams x 24 B, rounded to 256) + 128 group sums per stream
-    assert sdc.sdc_grad_average_scan_workspace_size(0, 4, 2) == 5 * 128 * 24
-    assert sdc.sdc_grad_average_scan_workspace_size(8192, 4, 2) == 256 + 5 * 128 * 24
+    # (32 B each: the counts are 64-bit)
+    assert sdc.sdc_grad_average_scan_workspace_size(0, 4, 2) == 5 * 128 * 32
+    assert sdc.sdc_grad_average_scan_workspace_size(8192, 4, 2) == 256 + 5 * 128 * 32
     assert sdc.sdc_grad_average_scan_workspace_size(8192, 9, 2) == 0  # more than 8 buffers
     sdc.sdc_xorsum_compare(0, 0, 0, 0, 0, 0)  # n == 0 is a no-op
     # GEMM checksum: operands checked, then shapes, before any CUDA call

@@ -159,3 +159,58 @@ def test_run_halves_whose_sum_overflows(sdc, dtype, magnitudes):
     got = sdc.decode_stats(plan.grad_scan())
     for b in range(2):
         stats_match(got[b], oracle.grad_stats(hb[b], name))
+
+
+def _block_pattern(kind: str, n: int, dtype, seed: int) -> torch.Tensor:
+    """Magnitude patterns in blocks of 2,048 elements (one 8-vector run of every lane of a
+    warp task) that defeat an offset taken from the previous run: jumps by 2^20 both ways,
+    steady growth, zero blocks, squares below float32's range, sums past FLT_MAX,
+    single spikes inside a run and subnormals."""
+    gen = torch.Generator(device="cpu").manual_seed(seed)
+    x = torch.randn(n, generator=gen, dtype=torch.float64)
+    blk = torch.arange(n) // 2048
+    f16 = dtype == torch.float16
+    if kind == "alternate":
+        scale = torch.where(blk % 2 == 0, 1.0, 2.0 ** (-12 if f16 else -20)).to(torch.float64)
+    elif kind == "grow":
+        scale = torch.pow(torch.tensor(2.0, dtype=torch.float64), (blk % 8).to(torch.float64) * (1 if f16 else 3))
+        scale = scale * (2.0 ** -8 if f16 else 1.0)
+    elif kind == "zero_blocks":
+        scale = torch.where(blk % 3 == 1, 0.0, 1e-3).to(torch.float64)
+    elif kind == "tiny":
+        scale = torch.where(blk % 2 == 0, 2.0 ** (-20 if f16 else -70), 1e-3).to(torch.float64)
+    elif kind == "near_overflow":
+        scale = torch.full((n,), 2.0 ** (10 if f16 else 62), dtype=torch.float64)
+    elif kind == "spikes":
+        scale = torch.full((n,), 1e-3, dtype=torch.float64)
+        idx = torch.arange(5, n, 997)
+        scale[idx] = 1e-3 * 2.0 ** (8 if f16 else 16)
+    elif kind == "subnormal":
+        scale = torch.full((n,), 2.0 ** (-20 if f16 else -130), dtype=torch.float64)
+    else:
+        raise ValueError(kind)
+    return (x * scale).to(dtype)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("kind", ["alternate", "grow", "zero_blocks", "tiny", "near_overflow", "spikes",
+                                  "subnormal"])
+def test_offset_runs_adversarial(sdc, dtype, kind):
+    # the 16-bit scans start each run's sum at an offset from the previous run; runs whose
+    # magnitudes break that guess must be redone (or summed exactly), never accepted inexactly
+    n = 4 * 8192 + 5
+    bufs = [_block_pattern(kind, n, dtype, 60 + i).to(DEV) for i in range(2)]
+    bufs.append(torch.flip(bufs[0], dims=[0]).contiguous())
+    name = NAMES[dtype]
+    hb = [host_bits(b) for b in bufs]
+    avg, pre, post = sdc.grad_average_scan(bufs)
+    ref_avg = oracle.average(hb, name)
+    assert np.array_equal(host_bits(avg), ref_avg)
+    got = sdc.decode_stats(pre)
+    for b in range(3):
+        stats_match(got[b], oracle.grad_stats(hb[b], name))
+    stats_match(sdc.decode_stats(post)[0], oracle.grad_stats(ref_avg, name))
+    plan = sdc.Plan([[b] for b in bufs])
+    got = sdc.decode_stats(plan.grad_scan())
+    for b in range(3):
+        stats_match(got[b], oracle.grad_stats(hb[b], name))
