@@ -468,8 +468,11 @@ sdc_status sdc_grad_average_scan(const void *const *bufs, uint32_t n_bufs, void 
  * dtype) exceeds it are rejected with SDC_ERR_BAD_ARG and a message giving
  * the limit (with 4 bf16 buffers that is about 1.14e9 elements).  The first
  * call on each device looks up the array's device address (a
- * cudaGetSymbolAddress with that device current) and caches it; make that
- * first call before any stream capture.  All calls share the one array and
+ * cudaGetSymbolAddress with that device current) and caches it with the ID
+ * of the current context; a call that finds another context current (after
+ * cudaDeviceReset, for example, which loads the library's device code anew)
+ * looks it up again.  Make the first call on a device, and the first after
+ * such a reset, before any stream capture.  All calls share the one array and
  * it keeps the last call's contents (nothing in it needs to start at zero):
  * calls whose GPU work overlaps -- on different streams, or from several host
  * threads -- race on it and must be ordered by the caller. */

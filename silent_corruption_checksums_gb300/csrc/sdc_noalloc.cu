@@ -13,7 +13,14 @@
 // every GPU that loads this library holds it until the process exits.  Host
 // code cannot use the array's name as a device address (in host code it is a
 // host-side shadow), so the first call on each device looks up the device
-// address with cudaGetSymbolAddress, with that device current, and caches it.
+// address with cudaGetSymbolAddress, with that device current, and caches it
+// together with the ID of the context it belongs to.  If that context is
+// destroyed and another one made current on the device (cudaDeviceReset, or a
+// primary context released and retained again), the module is loaded anew and
+// the array may sit elsewhere: a call that finds a different current context
+// looks the address up again instead of using the stale one.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "sdc_internal.cuh"
@@ -23,21 +30,56 @@ namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SDC_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
+struct CachedAddr {
+    unsigned long long ctx_id;  // 0: nothing cached
+    void *addr;
+};
 std::mutex g_mu;
-void *g_scratch_addr[kMaxDevices] = {nullptr};
+CachedAddr g_cache[kMaxDevices] = {};
 
-// Device address of the scratch array on `device` (the current device).
+typedef CUresult (*PFN_ctx_current)(CUcontext *ctx);
+typedef CUresult (*PFN_ctx_id)(CUcontext ctx, unsigned long long *id);
+
+// The unique ID of the calling thread's current context, 0 when no context is
+// current or the driver cannot say (then nothing is cached: every call looks
+// the address up).  Driver calls reached through the runtime's entry points.
+unsigned long long current_ctx_id() {
+    static std::once_flag once;
+    static PFN_ctx_current get_current = nullptr;
+    static PFN_ctx_id get_id = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = (PFN_ctx_current)p;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = (PFN_ctx_id)p;
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Device address of the scratch array on `device` (the current device) in
+// the current context.
 sdc_status scratch_address(int device, void **out) {
     if (device < 0 || device >= kMaxDevices)
         return sdc::fail(SDC_ERR_BAD_ARG, "device ordinal out of range for the static scratch");
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_addr[device]) {
-        void *p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return sdc::cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
-        g_scratch_addr[device] = p;
+    const unsigned long long id = current_ctx_id();
+    if (id != 0 && g_cache[device].ctx_id == id) {
+        *out = g_cache[device].addr;
+        return SDC_OK;
     }
-    *out = g_scratch_addr[device];
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return sdc::cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+    g_cache[device] = CachedAddr{current_ctx_id(), p};  // the lookup made the device's context current
+    *out = p;
     return SDC_OK;
 }
 
