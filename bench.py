@@ -5,9 +5,10 @@ Metric: fingerprint-scan GB/s (and % of HBM peak, ms per pass) on the
 ~1.04e9-parameter layout (24 layers, d=1792, ffn=7168, vocab=32000, untied
 embedding and head), float32 weights, 3 replicas resident in HBM.
 
-One step = one weight check: sdc_fingerprint over the 3 replicas (the
-persistent scan kernel plus its combine) and sdc_vote on the resulting
-[3, 195, 2] table.  Algorithmic bytes per step = every weight byte of every
+One step = one data-parallel weight check: every rank fingerprints its 3
+local copies (sdc_fingerprint: the persistent scan kernel plus its combine),
+the [3, 195, 2] tables are all-gathered (no exchange with one rank), and
+sdc_vote runs on the gathered table on every rank.  Algorithmic bytes per step = every weight byte of every
 replica read once = 12,475,438,080 bytes; inputs are ~97x the 129 MB L2, so
 no flush is needed between steps.  The other hot-path rows (fused gradient
 average-scan on 4 bf16 buffers of the same layout, xorsum with pair compare)
@@ -16,8 +17,10 @@ are timed in the same run and reported under "rows".
 Usage:
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 For N > 1 it is launched with torch.distributed.run, one rank per GPU; every
-rank checks its own 3 replicas (no collective on the data path: weak scaling),
-and rank 0 prints one JSON line with the whole-job throughput.
+rank holds 3 copies of the same weights (weak scaling: the work per GPU is
+fixed), rank 0's copies hold the one flipped bit, the tables are all-gathered
+with NCCL and every rank votes over all 3N copies; rank 0 prints one JSON
+line with the whole-job throughput.
 """
 from __future__ import annotations
 
@@ -149,6 +152,80 @@ def measured_peaks() -> dict:
 
 
 # ---------------------------------------------------------------- CPU baseline (the oracle)
+def cpu_info() -> dict:
+    """Host cores and CPU model (lscpu's model name, else the platform's processor string)."""
+    import platform
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    return {"nproc": os.cpu_count() or 1, "model": model or platform.processor() or platform.machine()}
+
+
+def host_bits(t):
+    """A device tensor's raw bits as a host numpy array (uint16 for 2-byte, uint32 for 4-byte elements)."""
+    import numpy as np
+    import torch
+    t = t.contiguous()
+    if t.element_size() == 2:
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    if t.element_size() == 4:
+        return t.view(torch.int32).cpu().numpy().view(np.uint32)
+    return t.cpu().numpy()
+
+
+def oracle_rate(work, nbytes: int, sample: str, unit: str = "GB/s", single=None, single_bytes: int = 0,
+                single_sample: str = "") -> dict:
+    """Time the oracle on all host cores (work(threads)) and single-threaded (single(1), a smaller sample)."""
+    threads = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    work(threads)
+    dt = time.perf_counter() - t0
+    out = {"value": nbytes / dt / (1e9 if unit == "GB/s" else 1e12), "unit": unit, "cores": threads,
+           "kind": "oracle", "seconds": dt, "sample": sample, "cpu": cpu_info()}
+    if single is not None:
+        t0 = time.perf_counter()
+        single(1)
+        ds = time.perf_counter() - t0
+        out["single_thread"] = {"value": single_bytes / ds / (1e9 if unit == "GB/s" else 1e12), "unit": unit,
+                                "cores": 1, "seconds": ds, "sample": single_sample}
+    return out
+
+
+def oracle_stream_rate(tensors, fn, limit_bytes: int, single_limit: int, what: str) -> dict:
+    """The oracle over device tensors streamed to the host one at a time (the copies are not
+    timed): fn(host_bits, threads) on all cores for the first ~limit_bytes, and on one core
+    for the first ~single_limit bytes."""
+    threads = os.cpu_count() or 1
+    t_all = t_one = 0.0
+    nb_all = nb_one = n_all = n_one = 0
+    for t in tensors:
+        if nb_all >= limit_bytes:
+            break
+        h = host_bits(t)
+        t0 = time.perf_counter()
+        fn(h, threads)
+        t_all += time.perf_counter() - t0
+        nb_all += h.nbytes
+        n_all += 1
+        if nb_one < single_limit:
+            t0 = time.perf_counter()
+            fn(h, 1)
+            t_one += time.perf_counter() - t0
+            nb_one += h.nbytes
+            n_one += 1
+    return {"value": nb_all / t_all / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle", "seconds": t_all,
+            "sample": f"{what}: the first {n_all} tensors ({nb_all} bytes), each copied to the host before "
+                      "its timed compute", "cpu": cpu_info(),
+            "single_thread": {"value": nb_one / t_one / 1e9, "unit": "GB/s", "cores": 1, "seconds": t_one,
+                              "sample": f"the first {n_one} tensors ({nb_one} bytes)"}}
+
+
 def cpu_baseline_sample(host_tensors, threads: int) -> dict:
     """Time the oracle's fingerprint over host copies of a sample of the workload."""
     import oracle
@@ -164,7 +241,8 @@ def cpu_baseline_sample(host_tensors, threads: int) -> dict:
 
 
 def run_reference(args) -> None:
-    """The reference arm: the CPU oracle on a bounded sample of the same workload."""
+    """The reference arm: the CPU oracle on the whole step of the same workload (3 float32
+    copies of the 1b layout, 12.5 GB per step) on all host cores."""
     rank, world, local = dist_env()
     if world > 1 and rank != 0:
         return
@@ -173,21 +251,23 @@ def run_reference(args) -> None:
     import sdc_workloads as W
     import oracle
     threads = os.cpu_count() or 1
-    # sample: the first tensors of one replica, up to ~1 GB of float32 weights, generated on the host
-    layout = W.layout_1b()
-    g = W.generator(1, "cpu")
-    sample, nbytes = [], 0
-    for _, shape in layout:
-        t = W.normal(shape, 0.02, torch.float32, g, "cpu")
-        sample.append(t.numpy().view(np.uint32))
-        nbytes += t.numel() * 4
-        if nbytes >= 1 << 30:
-            break
     oracle.build()
+    # the workload, made on the GPU when there is one (faster), then held in host memory
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    layout = W.layout_1b(args.layers)
+    copies = []
+    for r in range(3):
+        g = W.generator(1 + r, dev)
+        copies.append([W.normal(shape, 0.02, torch.float32, g, dev).cpu().numpy().view(np.uint32)
+                       for _, shape in layout])
+        if dev.type == "cuda":
+            torch.cuda.empty_cache()
+    nbytes = sum(a.nbytes for c in copies for a in c)
 
     def step():
-        for a in sample:
-            oracle.fingerprint(a, threads=threads)
+        for c in copies:
+            for a in c:
+                oracle.fingerprint(a, threads=threads)
 
     for _ in range(args.warmup):
         step()
@@ -196,14 +276,15 @@ def run_reference(args) -> None:
         step()
     dt = (time.perf_counter() - t0) / args.steps
     value = nbytes / dt / 1e9
+    sample = f"the whole step: 3 copies x {len(layout)} tensors, {nbytes} bytes of float32 weights"
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "int64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "sample": f"{len(sample)} tensors of replica 0 ({nbytes} bytes) "
-                       "per step; the full step is 3 replicas x 195 tensors"},
+            "config": {"workload": WORKLOAD if args.layers == 24 else f"{WORKLOAD}_{args.layers}layers",
+                       "sample": sample},
             "impl": "reference",
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                             "sample": f"{nbytes} bytes of float32 weights per step"},
+                             "sample": sample, "cpu": cpu_info()},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -227,6 +308,7 @@ def run_ours(args) -> None:
     import torch
     import sdc_workloads as W
     import silent_corruption_checksums_gb300 as sdc
+    from silent_corruption_checksums_gb300 import dp
 
     if args.only:
         return run_only_row(args)
@@ -239,26 +321,29 @@ def run_ours(args) -> None:
     peaks = measured_peaks()
     stream = torch.cuda.current_stream()
 
-    # ---- workload: 3 float32 replicas of the 1b layout, one bit flipped
-    w = W.weights_1b(dev, seed=1 + rank, n_layers=args.layers)
-    reps = w["replicas"]
+    # ---- workload: every rank holds the same 3 float32 copies of the 1b layout (data parallelism keeps
+    # the copies bit-identical); one seeded bit flip in one copy, on rank 0 only
+    w = W.weights_1b(dev, seed=1, n_layers=args.layers)
+    reps, truth = w["replicas"], w["truth"]
+    if rank != 0:  # this rank's copies are all clean
+        W.xor_element(reps[truth["replica"]][truth["tensor"]], truth["element"], 1 << truth["bit"])
     R, T = len(reps), len(reps[0])
     bytes_per_step = sum(t.numel() * t.element_size() for ts in reps for t in ts)
-    plan = sdc.Plan(reps, chunk_bytes=args.chunk_bytes)
-    fp = torch.empty((R, T, 2), dtype=torch.int64, device=dev)
-    vote_out = (torch.empty(T, dtype=torch.int32, device=dev), torch.empty(T, dtype=torch.int64, device=dev),
-                torch.empty(sdc.VOTE_SUMMARY_DTYPE.itemsize, dtype=torch.uint8, device=dev))
+    # the data-parallel weight check: fingerprint the local copies, all-gather the [T, 2] tables (none
+    # with one rank), the same strict-majority vote on every rank
+    wc = dp.WeightCheck(reps, chunk_bytes=args.chunk_bytes)
+    plan = wc.plan
 
     def step():
-        plan.fingerprint(out=fp, stream=stream)
-        sdc.vote(fp, stream=stream, out=vote_out)
+        wc.fingerprint(stream)
+        wc.gather_and_vote(stream)
 
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
-    # correctness of what is timed: the vote names the flipped replica
-    verdict = sdc.pages_verdict(sdc.decode_summary(vote_out[2]))
-    ok = verdict == {"diverged": True, "suspects": [w["truth"]["replica"]]}
+    # correctness of what is timed: every rank names rank 0 and the flipped copy
+    res = wc.result()
+    ok = res == {"diverged": True, "suspects": [0], "suspect_replicas": [truth["replica"]]}
 
     # ---- timed region: K steps, events around each fingerprint call
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -269,15 +354,16 @@ def run_ours(args) -> None:
         start.record(stream)
         for i in range(args.steps):
             ev[i][0].record(stream)
-            plan.fingerprint(out=fp, stream=stream)
+            wc.fingerprint(stream)
             ev[i][1].record(stream)
-            sdc.vote(fp, stream=stream, out=vote_out)
+            wc.gather_and_vote(stream)
         stop.record(stream)
         torch.cuda.synchronize()
     barrier(world)
     elapsed_ms = start.elapsed_time(stop)
     ms_step = max_over_ranks(elapsed_ms / args.steps, world, dev)
-    fp_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    fp_times = [a.elapsed_time(b) for a, b in ev]
+    fp_ms = statistics.median(fp_times)
     clocks = clk.summary()
     value = whole_job_rate(bytes_per_step, world, ms_step)
     achieved = bytes_per_step / (fp_ms * 1e-3) / 1e9
@@ -287,11 +373,12 @@ def run_ours(args) -> None:
     e2e = None
     cpu = None
     if not args.quick:
-        e2e_set = E2E(args, reps, sdc, torch) if rank == 0 else None
-        rows = bench_rows(args, dev, stream, peaks, sdc, W, torch, np)
-        if rank == 0:
-            e2e = e2e_set.run(args, fp, vote_out, stream, sdc, torch, bytes_per_step)
-            e2e_set.close(torch)
+        e2e_set = E2E(args, reps, dp, torch)
+        if world == 1:  # the other rows are single-GPU workloads, measured once
+            rows = bench_rows(args, dev, stream, peaks, sdc, W, torch, np)
+        e2e = e2e_set.run(args, wc.table, stream, torch, bytes_per_step, world, dev)
+        e2e_set.close(torch)
+        if rank == 0 and world == 1:
             cpu = bench_cpu(reps, torch)
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -300,6 +387,9 @@ def run_ours(args) -> None:
                 "config": {"workload": WORKLOAD if args.layers == 24 else f"{WORKLOAD}_{args.layers}layers",
                            "params_per_replica": W.layout_numel(w["layout"]),
                            "replicas": R, "tensors": T, "weights": "float32 N(0,0.02), one seeded bit flip",
+                           "parallelism": f"data-parallel weight check: {world} rank(s) x {R} local copies, "
+                                          "all-gather of the [T, 2] tables, the same vote on every rank",
+                           "copies_voted": world * R,
                            "bytes_per_step": bytes_per_step, "chunk_bytes": plan_chunk_bytes(args),
                            "grid": plan.grid, "block": plan.block, "n_chunks": plan.n_chunks,
                            "l2": "inputs 12.5 GB per step >> 129 MB L2; no flush between steps",
@@ -309,10 +399,13 @@ def run_ours(args) -> None:
                              "frac": achieved / peaks["hbm_gbs"],
                              "traffic": args.traffic if args.traffic is not None else scan_traffic(args.layers),
                              "kernel": "fp_scan_kernel (+ fp_combine_kernel, timed together as sdc_fingerprint)",
+                             "timing": f"median of {args.steps} per-call CUDA-event durations",
+                             "mean_ms": statistics.mean(fp_times), "median_ms": fp_ms,
                              "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)"},
                 "kernel_ms": fp_ms, "gpu_launches": launches_per_step * args.steps,
                 "clocks": clocks, "rows": rows, "e2e": e2e, "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)
+    wc.close()
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -344,6 +437,8 @@ def bench_rows(args, dev, stream, peaks, sdc, W, torch, np, only=None) -> dict:
         return bench_abft_row(args, dev, stream, peaks, sdc, W, torch)
     if only == "attn_invariant":
         return bench_attn_row(args, dev, stream, peaks, sdc, W, torch)
+    import oracle
+    oracle.build()
     # fused gradient average-scan on 4 bf16 buffers of the 1b layout
     g = W.grads_flat(W.layout_numel(W.layout_1b(args.layers)), 4, torch.bfloat16, 1e-3, dev, seed=3)
     bufs = g["bufs"]
@@ -358,10 +453,27 @@ def bench_rows(args, dev, stream, peaks, sdc, W, torch, np, only=None) -> dict:
     ms = _time_loop(avg_step, max(5, args.steps // 10), stream, torch) if only in (None, "grad_average_scan") \
         else None
     nbytes = 5 * n * 2
+    # the oracle's samples: the first elements of every buffer (all cores), a quarter of that (one core)
+    ns = min(n, 1 << 26)
+    hb = [host_bits(b[:ns]) for b in bufs]
+
+    def oracle_avg(k):
+        def run(threads):
+            avg = oracle.average([h[:k] for h in hb], "bf16", threads=threads)
+            for h in hb:
+                oracle.grad_stats(h[:k], "bf16", threads=threads)
+            oracle.grad_stats(avg, "bf16", threads=threads)
+        return run
+
     if ms is not None:
         rows["grad_average_scan"] = {"workload": "4 x bf16 local grads of the 1b layout (N(0,1e-3), rate-1e-7 "
                                      "NaN/Inf/2^70 in buffer 2)", "ms": ms, "bytes": nbytes,
-                                     "GB_s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"]}
+                                     "GB_s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"],
+                                     "cpu_baseline": oracle_rate(
+                                         oracle_avg(ns), 5 * ns * 2,
+                                         f"average + 5 scans of the first {ns} elements of each buffer",
+                                         single=oracle_avg(ns // 4), single_bytes=5 * (ns // 4) * 2,
+                                         single_sample=f"the first {ns // 4} elements")}
     # the same buffers as one plan: pre-average scan only
     if only in (None, "grad_scan"):
         gplan = sdc.Plan([[b] for b in bufs])
@@ -369,8 +481,16 @@ def bench_rows(args, dev, stream, peaks, sdc, W, torch, np, only=None) -> dict:
         ms = _time_loop(lambda: gplan.grad_scan(out=stats, stream=stream), max(5, args.steps // 10), stream,
                         torch)
         nbytes = 4 * n * 2
+
+        def oracle_scan(k):
+            return lambda threads: [oracle.grad_stats(h[:k], "bf16", threads=threads) for h in hb]
+
         rows["grad_scan"] = {"workload": "4 x bf16 local grads of the 1b layout", "ms": ms, "bytes": nbytes,
-                             "GB_s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"]}
+                             "GB_s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"],
+                             "cpu_baseline": oracle_rate(
+                                 oracle_scan(ns), 4 * ns * 2, f"scans of the first {ns} elements of each buffer",
+                                 single=oracle_scan(ns // 4), single_bytes=4 * (ns // 4) * 2,
+                                 single_sample=f"the first {ns // 4} elements")}
         del gplan
     if only in (None, "adamw_fingerprint"):
         rows.update(bench_adamw_row(args, dev, stream, peaks, sdc, W, torch))
@@ -387,11 +507,24 @@ def bench_rows(args, dev, stream, peaks, sdc, W, torch, np, only=None) -> dict:
 
         ms = _time_loop(xor_step, max(5, args.steps // 10), stream, torch)
         nbytes = 8 * n * 2
+        hr = host_bits(rec[1][:ns])
+
+        def oracle_xor(k):
+            def run(threads):
+                xa = [oracle.xorsum(h[:k], threads=threads) for h in hb]
+                xb = [oracle.xorsum(h[:k], threads=threads) for h in (hb[0], hr, hb[2], hb[3])]
+                oracle.xorsum_compare(xa, xb)
+            return run
+
         rows["xorsum"] = {"workload": "xorsum of 4 bf16 grad buffers and their recomputed copies + compare",
                           "ms": ms, "bytes": nbytes, "GB_s": nbytes / ms / 1e6,
-                          "frac_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"]}
+                          "frac_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"],
+                          "cpu_baseline": oracle_rate(
+                              oracle_xor(ns), 8 * ns * 2, f"the first {ns} elements of the 4 buffers and 4 copies",
+                              single=oracle_xor(ns // 4), single_bytes=8 * (ns // 4) * 2,
+                              single_sample=f"the first {ns // 4} elements")}
         del xplan, rec
-    del g, bufs, out, ws
+    del g, bufs, out, ws, hb
     torch.cuda.empty_cache()
     if only in (None, "abft_gemm"):
         rows.update(bench_abft_row(args, dev, stream, peaks, sdc, W, torch))
@@ -424,6 +557,20 @@ def bench_adamw_row(args, dev, stream, peaks, sdc, W, torch) -> dict:
                                  "ms": ms, "bytes": nbytes, "GB_s": nbytes / ms / 1e6,
                                  "frac_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"],
                                  "separate_fingerprint_reread_ms": ms_fp}}
+    # the oracle (one core: it is plain scalar C) on the first 2^24 elements of the first tensor
+    import numpy as np
+    import oracle
+    k = min(1 << 24, weights[0][0].numel())
+    p_h = host_bits(weights[0][0]).reshape(-1)[:k].view(np.float32).copy()
+    g_h = host_bits(grads[0]).reshape(-1)[:k].copy()
+    m_h, v_h = np.zeros(k, dtype=np.float32), np.zeros(k, dtype=np.float32)
+    t0 = time.perf_counter()
+    oracle.adamw_step(p_h, g_h, "bf16", m_h, v_h, hp, None)
+    dt = time.perf_counter() - t0
+    out["adamw_fingerprint"]["cpu_baseline"] = {
+        "value": k * 26 / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle", "seconds": dt,
+        "sample": f"the AdamW update of the first {k} elements of the first tensor (the oracle is single-threaded)",
+        "cpu": cpu_info()}
     opt.close()
     del plan, weights, grads, m, v
     torch.cuda.empty_cache()
@@ -462,7 +609,21 @@ def bench_abft_row(args, dev, stream, peaks, sdc, W, torch) -> dict:
                          "cublas_tflops": flops / (ms_cublas * 1e-3) / 1e12,
                          "clean_rows_flagged": int(g.summary[0]), "aborted": int(g.aborted[0]),
                          "max_residual_over_bound": float((g.residual.abs() / g.bound).max())}}
-    del g, gc, ops, A, Wt
+    # the oracle (float64, numpy's BLAS on all host cores) on the first 64 rows of A
+    import oracle
+    ms_rows = 64
+    A_h = host_bits(A[:ms_rows]).reshape(ms_rows, K)
+    W_h = host_bits(Wt).reshape(N, K)
+    t0 = time.perf_counter()
+    C_ref = oracle.abft_product(A_h, W_h)
+    oracle.abft_verify(oracle.abft_row_checksum(C_ref), A_h, W_h)
+    dt = time.perf_counter() - t0
+    out["abft_gemm"]["cpu_baseline"] = {
+        "value": 2.0 * ms_rows * N * K / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count() or 1,
+        "kind": "oracle", "seconds": dt, "cpu": cpu_info(),
+        "sample": f"the product, row checksums and check of the first {ms_rows} rows of A (float64; the "
+                  "matrix product runs on numpy's BLAS with its default threads)"}
+    del g, gc, ops, A, Wt, A_h, W_h, C_ref
     torch.cuda.empty_cache()
     return out
 
@@ -490,7 +651,20 @@ def bench_attn_row(args, dev, stream, peaks, sdc, W, torch) -> dict:
                               "clean_columns_flagged": int(a.summary[0]), "aborted": int(a.aborted[0]),
                               "max_residual_over_bound": float((a.residual.abs() / a.bound).max()),
                               "torch_fused_backward_dq_dk_dv_ms": ms_ref}}
-    del a, x, q, k, v, o
+    # the oracle (float64, numpy's BLAS on all host cores) on the first head
+    import oracle
+    Qh, Kh, dOh = (host_bits(x[n][0]).reshape(L, 128) for n in ("Q", "K", "dO"))
+    lse_h = x["lse"][0].float().cpu().numpy()
+    t0 = time.perf_counter()
+    P = oracle.attn_probs(Qh, Kh, lse_h, x["scale"], True)
+    oracle.attn_invariant(oracle.attn_dv(P, dOh).sum(axis=0), dOh)
+    dt = time.perf_counter() - t0
+    out["attn_invariant"]["cpu_baseline"] = {
+        "value": flops / BH / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count() or 1, "kind": "oracle",
+        "seconds": dt, "cpu": cpu_info(),
+        "sample": "the first head: P rebuilt, dV = P^T dO and the invariant (float64, numpy's BLAS with its "
+                  "default threads; FLOPs counted as for the GPU row, the causal half)"}
+    del a, x, q, k, v, o, P
     torch.cuda.empty_cache()
     # the 8b layout's grouped-query form: its 32 query heads over 8 K/V heads, dV per K/V head
     group = 4
@@ -512,6 +686,8 @@ def bench_attn_row(args, dev, stream, peaks, sdc, W, torch) -> dict:
 
 def bench_big_rows(args, dev, stream, peaks, sdc, W, torch, only) -> dict:
     """Fingerprint rows on the 8b and stress workloads (tens of GB each)."""
+    import oracle
+    oracle.build()
     rows = {}
     if only in (None, "fingerprint_8b"):
         L8, R8 = getattr(args, "layers_8b", 32), getattr(args, "replicas_8b", 8)
@@ -519,6 +695,9 @@ def bench_big_rows(args, dev, stream, peaks, sdc, W, torch, only) -> dict:
         rows["fingerprint_8b"] = bench_fp_row(
             w8["replicas"], f"8b bf16 layout (T={len(w8['layout'])}, {L8} layers), {R8} replicas, 16-element "
             "perturbation", args, stream, peaks, sdc, torch)
+        rows["fingerprint_8b"]["cpu_baseline"] = oracle_stream_rate(
+            [t for ts in w8["replicas"] for t in ts], lambda h, th: oracle.fingerprint(h, threads=th), 8 << 30,
+            1 << 30, "fingerprint, replica-major")
         del w8
         torch.cuda.empty_cache()
     if only in (None, "fingerprint_stress"):
@@ -527,6 +706,9 @@ def bench_big_rows(args, dev, stream, peaks, sdc, W, torch, only) -> dict:
         rows["fingerprint_stress"] = bench_fp_row(
             w["replicas"], f"{nt:,} tensors (1..1e6 elements, fp32/bf16/fp16, element-aligned packing), 3 replicas",
             args, stream, peaks, sdc, torch)
+        rows["fingerprint_stress"]["cpu_baseline"] = oracle_stream_rate(
+            [t for ts in w["replicas"] for t in ts], lambda h, th: oracle.fingerprint(h, threads=th), 2 << 30,
+            256 << 20, "fingerprint, replica-major")
         p = w["pairs"]
         xplan = sdc.Plan([p["orig"], p["recomp"]])
         xo = torch.empty((2, len(p["orig"])), dtype=torch.int64, device=dev)
@@ -537,10 +719,18 @@ def bench_big_rows(args, dev, stream, peaks, sdc, W, torch, only) -> dict:
 
         ms = _time_loop(xs_step, 20, stream, torch)
         nbytes = sum(t.numel() * t.element_size() for t in p["orig"]) * 2
+        ho, hr = [host_bits(t) for t in p["orig"]], [host_bits(t) for t in p["recomp"]]
+
+        def oracle_pairs(threads):
+            oracle.xorsum_compare([oracle.xorsum(h, threads=threads) for h in ho],
+                                  [oracle.xorsum(h, threads=threads) for h in hr])
         rows["xorsum_pairs_stress"] = {"workload": "1,000 (original, recomputed) pairs, sizes 1..1e6, half with a "
                                        "one-bit difference: xorsum + compare", "ms": ms, "bytes": nbytes,
-                                       "GB_s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"]}
-        del w, xplan, p
+                                       "GB_s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"],
+                                       "cpu_baseline": oracle_rate(oracle_pairs, nbytes, "all 1,000 pairs",
+                                                                   single=oracle_pairs, single_bytes=nbytes,
+                                                                   single_sample="all 1,000 pairs")}
+        del w, xplan, p, ho, hr
         torch.cuda.empty_cache()
     return rows
 
@@ -567,16 +757,17 @@ def bench_fp_row(reps, workload, args, stream, peaks, sdc, torch) -> dict:
 
 
 class E2E:
-    """The same metric through the public API with the replicas in pinned host memory:
-    every step copies them to the device, checks them, and reads the verdict back.
+    """The same metric through the public API with the copies in pinned host memory:
+    every step copies them to the device, runs the data-parallel weight check
+    (fingerprint, all-gather, vote) and reads the table and verdict back.
 
-    Each replica's tensors sit back to back (256-byte aligned) in one host buffer
+    Each copy's tensors sit back to back (256-byte aligned) in one host buffer
     allocated pinned and one device buffer; a step moves them in 256 MiB copies.
     The host buffers are written by the CPU, as a caller's host data would be
-    (set-up, outside the timed region).  The host link bounds the rate.  The plan
-    covers views of the device buffers."""
+    (set-up, outside the timed region).  The host link bounds the rate.  The
+    check covers views of the device buffers."""
 
-    def __init__(self, args, reps, sdc, torch):
+    def __init__(self, args, reps, dp, torch):
         align = 256
         self.offs, total = [], 0
         for t in reps[0]:
@@ -601,13 +792,14 @@ class E2E:
             self.dev.append(d)
             views.append(vs)
         self.views = views
-        self.plan = sdc.Plan(views, chunk_bytes=args.chunk_bytes)
+        self.wc = dp.WeightCheck(views, chunk_bytes=args.chunk_bytes)
 
-    def run(self, args, fp, vote_out, stream, sdc, torch, bytes_per_step) -> dict:
-        fp_ref = fp.cpu()  # the device-resident pass's table: the copied replicas must give the same one
-        fp_host = torch.empty(fp.shape, dtype=fp.dtype).pin_memory()
-        sum_host = torch.empty(vote_out[2].shape, dtype=torch.uint8).pin_memory()
-        sus_host = torch.empty(vote_out[0].shape, dtype=torch.int32).pin_memory()
+    def run(self, args, table_ref, stream, torch, bytes_per_step, world, dev) -> dict:
+        ref = table_ref.cpu()  # the device-resident pass's gathered table: the copied replicas give the same one
+        wc = self.wc
+        fp_host = torch.empty(wc.table.shape, dtype=wc.table.dtype).pin_memory()
+        sum_host = torch.empty(wc.vote_out[2].shape, dtype=torch.uint8).pin_memory()
+        sus_host = torch.empty(wc.vote_out[0].shape, dtype=torch.int32).pin_memory()
         piece, total = 256 << 20, self.total
 
         def e2e_step():
@@ -615,30 +807,31 @@ class E2E:
                 for o in range(0, total, piece):
                     e = min(total, o + piece)
                     d[o:e].copy_(h[o:e], non_blocking=True)
-            self.plan.fingerprint(out=fp, stream=stream)
-            sdc.vote(fp, stream=stream, out=vote_out)
-            fp_host.copy_(fp, non_blocking=True)
-            sus_host.copy_(vote_out[0], non_blocking=True)
-            sum_host.copy_(vote_out[2], non_blocking=True)
+            wc.enqueue(stream)
+            fp_host.copy_(wc.table, non_blocking=True)
+            sus_host.copy_(wc.vote_out[0], non_blocking=True)
+            sum_host.copy_(wc.vote_out[2], non_blocking=True)
 
         steps = max(3, min(10, args.steps // 50))
         e2e_step()
         torch.cuda.synchronize()
+        barrier(world)
         t0 = time.perf_counter()
         for _ in range(steps):
             e2e_step()
         torch.cuda.synchronize()
-        dt = (time.perf_counter() - t0) / steps
-        same = bool(torch.equal(fp_host, fp_ref))
-        d2h = fp.numel() * 8 + vote_out[0].numel() * 4 + vote_out[2].numel()
-        return {"value": bytes_per_step / dt / 1e9, "unit": "GB/s", "ms_per_step": dt * 1e3,
+        dt = max_over_ranks((time.perf_counter() - t0) / steps, world, dev)
+        same = bool(torch.equal(fp_host, ref))
+        d2h = wc.table.numel() * 8 + wc.vote_out[0].numel() * 4 + wc.vote_out[2].numel()
+        return {"value": bytes_per_step * world / dt / 1e9, "unit": "GB/s", "ms_per_step": dt * 1e3,
                 "h2d_bytes_per_step": total * self.n_rep, "d2h_bytes_per_step": d2h, "steps": steps,
                 "copies_per_step": self.n_rep * ((total + piece - 1) // piece) + 3,
+                "per_rank": "h2d and d2h bytes per rank; value = all ranks' bytes over the slowest rank's time",
                 "layout": "one pinned buffer per replica, tensors 256-byte aligned, 256 MiB copies",
                 "table_matches_device_pass": same}
 
     def close(self, torch) -> None:
-        self.plan.close()
+        self.wc.close()
         del self.host, self.dev, self.views
         torch.cuda.empty_cache()
 
@@ -651,6 +844,7 @@ def bench_cpu(reps, torch) -> dict:
     threads = os.cpu_count() or 1
     r = cpu_baseline_sample([t for ts in host for t in ts], threads)
     r["sample"] = f"the whole step: {len(host)} replicas x {len(host[0])} tensors, {nbytes} bytes"
+    r["cpu"] = cpu_info()
     one, nb1 = [], 0
     for t in host[0]:
         one.append(t)
