@@ -470,15 +470,18 @@ def abft_reference(A_bits: np.ndarray, W_bits: np.ndarray) -> tuple[np.ndarray, 
 
 def abft_bound(mag: np.ndarray, N: int, K: int) -> np.ndarray:
     """Rounding bound of a checksum of N outputs taken from their float32 accumulators
-    (N: the columns a row checksum sums, or the rows a column checksum sums).
+    (N: the columns a row checksum sums, or the rows a column checksum sums), against
+    exact check sums.
 
     Each of the K float32 accumulation steps of one output may lose up to two
     units in the last place of its partial sum (g = K 2^-22 per output to first
-    order, g^2 beyond it); the sums of the check, carried as float32 pairs of
-    about 48 bits, lose at most (N + K + 64) 2^-44 of the magnitude; subnormals
-    flushed to zero lose 2^-126 per product and per step."""
+    order, g^2 beyond it); subnormals flushed to zero lose 2^-126 per product and
+    per step.  The check's own sums are taken as exact: here they are float64,
+    whose rounding (below (N + K) 2^-53 of the magnitude) is far under one float32
+    unit of the bound.  A check that carries its sums in less precision adds its
+    own term on top."""
     g = K * 2.0 ** -22
-    return (g * (1.0 + g) + (N + K + 64) * 2.0 ** -44) * np.asarray(mag, dtype=np.float64) + 2.0 * K * N * 2.0 ** -126
+    return g * (1.0 + g) * np.asarray(mag, dtype=np.float64) + 2.0 * K * N * 2.0 ** -126
 
 
 def abft_reference_cols(A_bits: np.ndarray, W_bits: np.ndarray) -> tuple[np.ndarray, np.ndarray]:

@@ -54,3 +54,11 @@ def stats_match(gpu: dict, ref: dict, rtol: float = 1e-10) -> None:
     import oracle
     if abs(ref["sumsq_finite"] - oracle.FLT_MAX) > 1e-9 * oracle.FLT_MAX:
         assert gpu["nonfinite_fp32"] == ref["nonfinite_fp32"]
+
+
+def verifier_pair_slack(n_sum: int, K: int) -> float:
+    """The GEMM check kernel's own term, relative to the magnitude: it carries A(W^T 1),
+    the magnitude and its column sums as float32 pairs (about 48 bits), so its bound adds
+    (n_sum + K + 64) 2^-44 of the magnitude to the method's bound, and its residual and
+    bound agree with exact float64 sums to that term."""
+    return (n_sum + K + 64) * 2.0 ** -44
