@@ -294,13 +294,16 @@ sdc_status sdc_abft_gemm(const void *d_A, const void *d_W, void *d_C, uint32_t M
                          double *d_rowsum, double *d_colsum, uint32_t *d_aborted, void *d_ws, size_t ws_bytes,
                          sdc_stream_t stream);
 
-/* The checksum verifier: per row, the reference A(W^T 1) in float64, the
- * residual d_residual[i] = d_rowsum[i] - reference, the rounding bound
+/* The checksum verifier: per row, the reference A(W^T 1) (float32 pairs,
+ * about 48 bits, returned in float64), the residual d_residual[i] =
+ * d_rowsum[i] - reference, the rounding bound
  * d_bound[i] = (g (1 + g) + (N + K + 64) 2^-44) mag + 2 K N 2^-126 with
- * g = K 2^-22 and mag = sum_k |A[i][k]| sum_j |W[j][k]| (each float32
+ * g = K 2^-22 and mag an upper bound on sum_k |A[i][k]| sum_j |W[j][k]|
+ * (summed in plain float32 and raised by twice its chains' length in units of
+ * 2^-24, at most 2 (N/8 + K/4 + 32) 2^-24 of itself).  Each float32
  * accumulation step may lose two units in the last place of its partial sum;
- * the check's own sums, carried as float32 pairs, and flushed subnormals are
- * covered; so a correct product stays inside it), and d_flag[i] = 1 unless
+ * the check's own sums and flushed subnormals are covered; so a correct
+ * product stays inside the bound.  d_flag[i] = 1 unless
  * |residual| <= tol_scale * bound (a NaN residual flags; tol_scale > 0; the
  * page's adaptive threshold has no published constants).  With d_colsum
  * (from sdc_abft_gemm) the columns are checked too, against (1^T A) W^T:

@@ -74,8 +74,6 @@ constexpr uint32_t kGemmSmemCols = kGemmSmem + 4 * kColTileFloats * 4 + 4 * kBN 
 static_assert(kGemmSmemCols <= 232448, "shared memory per block");
 constexpr uint32_t kMaxK = 1u << 20;
 constexpr uint32_t kMaxSlabs = 64;
-constexpr uint32_t kCheckRows = 8;     // rows per block of the check
-constexpr uint32_t kCheckThreads = 128;  // threads per block of the check
 
 // Converts 32 accumulators to bf16 (round to nearest even), stores them at
 // dst (64 bytes, 16-byte aligned) and adds them to the row's pair sum.
@@ -331,58 +329,97 @@ __global__ void __launch_bounds__(256) abft_sum_parts_kernel(const double *__res
 }
 
 // ---------------------------------------------------------------- the check
+//
+// The check's sums need far less than float32-pair precision: it compares a
+// checksum with a reference under a bound of about K 2^-22 of the magnitude
+// mag = sum_k |A[i, k]| sum_j |W[j, k]|, so its own rounding only has to stay
+// well below that and be counted in the bound.  Plain float32 chains of at
+// most 8 terms are folded into float32 pairs with TwoSum:
+//  - W's column sums: 8-row chains per lane, each off by at most 8.01 2^-24
+//    of its rows' |W| sum;
+//  - the reference A (W^T 1): 8-term fused multiply-add chains (one vector
+//    of 8 columns), each off by at most 8.01 2^-24 of its |a| |w| sum, against
+//    the column sums rounded to float32 (2^-24 more);
+//  - the pairs and their merges: below (n + K + 64) 2^-44 of the magnitude.
+// Together the reference is within (20 2^-24 + (n_sum + K + 64) 2^-44) mag of
+// A (W^T 1), and that term is added to the bound.  The magnitude itself is
+// summed in plain float32 and raised by 1 + 2 (L1 + L2 + S + 8) 2^-24, where L1
+// is the longest plain float32 chain of the column sums of |W|, L2 that of a
+// lane's magnitude dot product and S the K splits merged after them.  Each
+// chain of non-negative terms is off by at most (its length) 2^-24 of its sum,
+// so the raised value is an upper bound on the exact magnitude, and the bound
+// stays rigorous.
+constexpr uint32_t kChain = 8;  // terms of a plain float32 chain before it is folded into a pair
 
-// Column sums of W over one slab of its rows: block (x, y) covers columns
-// 256x .. 256x + 255 (8 per lane, one 16-byte load per row) and slab y; the 8
-// warps take the slab's rows in turn.  Writes slabs[y][k] = the float32 pairs
-// of sum_j W[j, k] and sum_j |W[j, k]|, warps merged in order.
-__global__ void __launch_bounds__(256) abft_colsum_slab_kernel(const __nv_bfloat16 *__restrict__ W, uint32_t N,
+// Column sums of X [rows][K] over one slab of its rows: block (x, y) covers
+// columns 256x .. 256x + 255 (8 per lane, one 16-byte load per row) and slab
+// y; the 8 warps take the slab's rows in turn.  Writes slabs[y][k] =
+// {s, c, a, e}: the float32 pair of sum_j X[j, k], and the plain float32 sum of
+// |X[j, k]| (its chain: the warp's rows) as a pair a + e after the warps'
+// merge; warps merged in order.  The last block of each column block (a
+// counter per column block in `done`, zero at launch) merges the slabs into
+// split[] = {h, m} per column.
+__global__ void __launch_bounds__(256, 3) abft_colsum_slab_kernel(const __nv_bfloat16 *__restrict__ X, uint32_t rows,
                                                                uint32_t K, uint32_t n_slabs,
-                                                               float4 *__restrict__ slabs) {
+                                                               float4 *__restrict__ slabs, float2 *__restrict__ split,
+                                                               uint32_t *__restrict__ done) {
     __shared__ float4 part[8][256];
+    __shared__ uint32_t last;
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
     const uint32_t k = blockIdx.x * 256 + lane * 8;
-    const uint32_t j0 = (uint32_t)((uint64_t)blockIdx.y * N / n_slabs),
-                   j1 = (uint32_t)((uint64_t)(blockIdx.y + 1) * N / n_slabs);
-    // columns 2q and 2q + 1 of the lane's 8 share packed registers
-    uint64_t s[4], c[4], sa[4], ca[4];
+    const uint32_t j0 = (uint32_t)((uint64_t)blockIdx.y * rows / n_slabs),
+                   j1 = (uint32_t)((uint64_t)(blockIdx.y + 1) * rows / n_slabs);
+    // columns 2q and 2q + 1 of the lane's 8 share packed registers: the pair (s, c) of the sum,
+    // the running chain t of up to kChain rows folded into it, the plain sum a of |x|
+    uint64_t s[4], c[4], a[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) s[q] = c[q] = sa[q] = ca[q] = 0ull;
-    auto add_row = [&](const uint4 v) {
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    for (int q = 0; q < 4; ++q) s[q] = c[q] = a[q] = 0ull;
+    auto add_rows = [&](const uint4 (&v)[kChain], uint32_t n) {  // n <= kChain rows, in row order
+        uint64_t t[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint64_t x = f2_pack_bits(w[q] << 16, w[q] & 0xFFFF0000u);
-            pair2_add(s[q], c[q], x);
-            pair2_add(sa[q], ca[q], x & kF2Abs);
+        for (uint32_t u = 0; u < kChain; ++u) {
+            if (u < n) {
+                const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint64_t x = f2_pack_bits(w[q] << 16, w[q] & 0xFFFF0000u);
+                    t[q] = f2_add(t[q], x);
+                    a[q] = f2_add(a[q], x & kF2Abs);
+                }
+            }
         }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) pair2_add(s[q], c[q], t[q]);
     };
     if (k < K) {
         uint32_t j = j0 + warp;
-        for (; j + 24 < j1; j += 32) {  // four rows in flight per lane, added in row order
-            if ((lane & 7u) == 0) {  // the next four rows into L2: lanes 0, 8, 16, 24 touch the warp's 4 lines
+        uint4 v[kChain];
+        for (; j + 8 * (kChain - 1) < j1; j += 8 * kChain) {  // kChain rows in flight per lane, added in row order
+            if ((lane & 7u) == 0) {  // the next chain's rows into L2: lanes 0, 8, 16, 24 touch the warp's 4 lines
 #pragma unroll
-                for (uint32_t d = 32; d < 64; d += 8)
-                    if (j + d < j1) prefetch_l2(W + (uint64_t)(j + d) * K + k);
+                for (uint32_t u = kChain; u < 2 * kChain; ++u)
+                    if (j + 8 * u < j1) prefetch_l2(X + (uint64_t)(j + 8 * u) * K + k);
             }
-            const uint4 v0 = ld_stream(W + (uint64_t)j * K + k), v1 = ld_stream(W + (uint64_t)(j + 8) * K + k),
-                        v2 = ld_stream(W + (uint64_t)(j + 16) * K + k), v3 = ld_stream(W + (uint64_t)(j + 24) * K + k);
-            add_row(v0);
-            add_row(v1);
-            add_row(v2);
-            add_row(v3);
+#pragma unroll
+            for (uint32_t u = 0; u < kChain; ++u) v[u] = ld_stream(X + (uint64_t)(j + 8 * u) * K + k);
+            add_rows(v, kChain);
         }
-        for (; j < j1; j += 8) add_row(ld_stream(W + (uint64_t)j * K + k));
+        if (j < j1) {  // fewer than kChain rows left
+            const uint32_t n = (j1 - j + 7) / 8;
+#pragma unroll
+            for (uint32_t u = 0; u < kChain; ++u)
+                v[u] = u < n ? ld_stream(X + (uint64_t)(j + 8 * u) * K + k) : make_uint4(0, 0, 0, 0);
+            add_rows(v, n);
+        }
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        float s0, s1, c0, c1, a0, a1, e0, e1;
+        float s0, s1, c0, c1, a0, a1;
         f2_unpack(s[q], s0, s1);
         f2_unpack(c[q], c0, c1);
-        f2_unpack(sa[q], a0, a1);
-        f2_unpack(ca[q], e0, e1);
-        part[warp][lane * 8 + 2 * q] = make_float4(s0, c0, a0, e0);
-        part[warp][lane * 8 + 2 * q + 1] = make_float4(s1, c1, a1, e1);
+        f2_unpack(a[q], a0, a1);
+        part[warp][lane * 8 + 2 * q] = make_float4(s0, c0, a0, 0.0f);
+        part[warp][lane * 8 + 2 * q + 1] = make_float4(s1, c1, a1, 0.0f);
     }
     __syncthreads();
     const uint32_t kk = blockIdx.x * 256 + threadIdx.x;
@@ -395,161 +432,220 @@ __global__ void __launch_bounds__(256) abft_colsum_slab_kernel(const __nv_bfloat
         }
         slabs[(uint64_t)blockIdx.y * K + kk] = acc;
     }
-}
-
-// The slabs merged: for the check, W^T 1 and |W|^T 1 as normalised float32
-// pairs wsplit[k] = {hi, lo, hi_abs, lo_abs} (hi the float nearest the pair's
-// sum), and wcol[k] = the same values in float64.  Block = 32 columns (one per
-// lane) x 8 warps; warp w merges slabs w, w + 8, ... in order, then the warps'
-// pairs are merged in warp order (a fixed order: the result is reproducible).
-__global__ void __launch_bounds__(256) abft_colsum_final_kernel(const float4 *__restrict__ slabs, uint32_t K,
-                                                                uint32_t n_slabs, double2 *__restrict__ wcol,
-                                                                float4 *__restrict__ wsplit) {
-    __shared__ float4 part[8][32];
-    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
-    const uint32_t k = blockIdx.x * 32 + lane;
-    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    if (k < K) {
-#pragma unroll 8
-        for (uint32_t y = warp; y < n_slabs; y += 8) {
-            const float4 q = slabs[(uint64_t)y * K + k];
+    // The last slab block of this column block merges the column block's slabs (in slab order:
+    // the same result whichever block is last) into split[k] = {h, m}: h the float nearest
+    // sum_j X[j, k] (the merged pair's sum), m = sum_j |X[j, k]| rounded to float32.
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        last = atomicAdd(done + blockIdx.x, 1u) == n_slabs - 1 ? 1u : 0u;
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    if (kk < K) {
+        float4 acc = __ldcg(slabs + kk);
+        for (uint32_t y = 1; y < n_slabs; ++y) {
+            const float4 q = __ldcg(slabs + (uint64_t)y * K + kk);
             pair_merge(acc.x, acc.y, q.x, q.y);
             pair_merge(acc.z, acc.w, q.z, q.w);
         }
+        float h = 0.0f, l = 0.0f;  // renormalise: TwoSum of the two parts
+        pair_add(h, l, acc.x);
+        pair_add(h, l, acc.y);
+        split[kk] = make_float2(__fadd_rn(h, l), __fadd_rn(acc.z, acc.w));
     }
-    part[warp][lane] = acc;
-    __syncthreads();
-    if (warp != 0 || k >= K) return;
-    for (int w = 1; w < 8; ++w) {
-        const float4 q = part[w][lane];
-        pair_merge(acc.x, acc.y, q.x, q.y);
-        pair_merge(acc.z, acc.w, q.z, q.w);
-    }
-    float h = 0.0f, l = 0.0f, ha = 0.0f, la = 0.0f;  // renormalise: TwoSum of the two parts
-    pair_add(h, l, acc.x);
-    pair_add(h, l, acc.y);
-    pair_add(ha, la, acc.z);
-    pair_add(ha, la, acc.w);
-    wsplit[k] = make_float4(h, l, ha, la);
-    wcol[k] = make_double2((double)h + (double)l, (double)ha + (double)la);
+    if (threadIdx.x == 0) done[blockIdx.x] = 0u;  // ready for the next call
 }
 
-// Per row of X (A for the row check, W for the column check): the reference
-// X . split (A (W^T 1), or W (A^T 1)) and the magnitude |X| . split_abs as
-// float32 pairs, the bound over n_sum summed outputs, the residual against the
-// accumulator checksum, and the flag.  One block of kCheckThreads threads per kCheckRows rows: the threads stride over
-// the 8-column vectors (each column pair loaded once for all the rows), then
-// the pairs are merged across lanes (butterfly) and across warps (in order).
-__global__ void __launch_bounds__(kCheckThreads) abft_check_kernel(const __nv_bfloat16 *__restrict__ A, uint32_t n_rows,
-                                                         uint32_t n_sum, uint32_t K, const double *__restrict__ rowsum,
-                                                         const float4 *__restrict__ wsplit, float tol_scale,
-                                                         double *__restrict__ residual, double *__restrict__ bound,
-                                                         uint8_t *__restrict__ flag, uint32_t *__restrict__ n_flagged) {
-    __shared__ float4 red[kCheckThreads / 32][kCheckRows];
+// The check of X [n_rows][K] (A for the row check, W for the column check)
+// against split[] = {h, m} (the other operand's column sums), one K split per
+// block: part[y][i] = {s, c, m, 0} with s + c = sum_k X[i, k] h_k over split y's
+// columns (8-term chains folded into a float32 pair), and
+// m = sum_k |X[i, k]| m_k in plain float32.  Block = 4 warps over 32 rows; a
+// warp holds 4 packed row pairs, 8 lanes per pair.  The 8 lanes of a group read
+// a whole 128-byte line of each of their two rows per vector step (lane j takes
+// the split's vectors j, j + 8, ...) and the 512 contiguous bytes of those
+// vectors' column sums, which the warp's 4 groups share through L1; their sums
+// meet in 3 butterfly steps.  The block starts a bulk L2 prefetch of its 32
+// rows' segments first.  The last split block of a row block (a counter per
+// row block) merges the row block's partials in split order (the same result
+// whichever block is last) and writes, per row: the reference ref = s + c, the
+// magnitude raised by (1 + delta) to an upper bound, the bound over n_sum
+// summed outputs, the residual against the accumulator checksum and the flag
+// (a NaN residual flags).
+constexpr uint32_t kChkRows = 32;  // rows per block of the check
+
+struct CheckOut {
+    const double *checksum;
+    double *residual, *bound;
+    uint8_t *flag;
+    uint32_t *n_flagged;
+    uint32_t *done;  // a counter per row block
+    double delta;
+    float tol_scale;
+    uint32_t n_sum, n_splits;
+};
+
+// 8 columns of two rows (packed) against the column sums hm[0..7] = {h, m}: an
+// 8-term fused multiply-add chain folded into the pair (rs, rc) with TwoSum,
+// and the magnitude's plain chain m.
+__device__ __forceinline__ void check_vec(const uint4 &a0, const uint4 &a1, const float2 *hm, uint64_t &rs,
+                                          uint64_t &rc, uint64_t &m) {
+    const uint4 *p = (const uint4 *)hm;  // {h, m, h, m} of two columns per 16 bytes
+    uint64_t t = 0ull;
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) {
+        const uint4 w = __ldg(p + qq);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int q = 2 * qq + e;
+            const uint32_t w0 = (&a0.x)[q >> 1], w1 = (&a1.x)[q >> 1];
+            const uint64_t a2 = (q & 1) ? f2_pack_bits(w0 & 0xFFFF0000u, w1 & 0xFFFF0000u)
+                                        : f2_pack_bits(w0 << 16, w1 << 16);
+            const uint32_t h = e ? w.z : w.x, mm = e ? w.w : w.y;
+            t = f2_fma(a2, f2_pack_bits(h, h), t);
+            m = f2_fma(a2 & kF2Abs, f2_pack_bits(mm, mm), m);
+        }
+    }
+    pair2_add(rs, rc, t);
+}
+
+__global__ void __launch_bounds__(128) abft_check_kernel(const __nv_bfloat16 *__restrict__ X, uint32_t n_rows,
+                                                         uint32_t K, uint32_t vec_per_split,
+                                                         const float2 *__restrict__ split, float4 *__restrict__ part,
+                                                         CheckOut o) {
+    __shared__ uint32_t last;
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
-    const uint64_t row0 = (uint64_t)blockIdx.x * kCheckRows;
-    const uint32_t nr = n_rows - (uint32_t)row0 < kCheckRows ? n_rows - (uint32_t)row0 : kCheckRows;  // rows present
-    // rows (0, 1) and (2, 3) share packed registers
-    uint64_t rs2[kCheckRows / 2], rc2[kCheckRows / 2], ms2[kCheckRows / 2], mc2[kCheckRows / 2];
-#pragma unroll
-    for (uint32_t r = 0; r < kCheckRows / 2; ++r) rs2[r] = rc2[r] = ms2[r] = mc2[r] = 0ull;
-    for (uint32_t v = tid; v < K / 8; v += kCheckThreads) {
-        if ((lane & 7u) == 0 && v + kCheckThreads < K / 8) {  // the next vectors of every row into L2
-#pragma unroll
-            for (uint32_t r = 0; r < kCheckRows; ++r)
-                if (r < nr) prefetch_l2(A + (row0 + r) * K + (uint64_t)(v + kCheckThreads) * 8);
-        }
-        uint4 av[kCheckRows];
-#pragma unroll
-        for (uint32_t r = 0; r < kCheckRows; ++r)
-            av[r] = r < nr ? ld_stream(A + (row0 + r) * K + (uint64_t)v * 8) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {  // column 8 v + q
-            const float4 w = wsplit[v * 8 + q];
-            const uint64_t h2 = f2_pack(w.x, w.x), l2 = f2_pack(w.y, w.y);
-            const uint64_t ha2 = f2_pack(w.z, w.z), la2 = f2_pack(w.w, w.w);
-#pragma unroll
-            for (uint32_t rp = 0; rp < kCheckRows / 2; ++rp) {
-                const uint32_t w0 = (&av[2 * rp].x)[q >> 1], w1 = (&av[2 * rp + 1].x)[q >> 1];
-                const uint64_t a2 = (q & 1) ? f2_pack_bits(w0 & 0xFFFF0000u, w1 & 0xFFFF0000u)
-                                            : f2_pack_bits(w0 << 16, w1 << 16);
-                pair2_fma(rs2[rp], rc2[rp], a2, h2, l2);
-                pair2_fma(ms2[rp], mc2[rp], a2 & kF2Abs, ha2, la2);
-            }
-        }
+    const uint32_t v0 = blockIdx.y * vec_per_split, v1 = min(K / 8, v0 + vec_per_split), nv = v1 > v0 ? v1 - v0 : 0;
+    const uint32_t row0 = blockIdx.x * kChkRows;
+    if (tid < kChkRows && row0 + tid < n_rows && nv)  // this block's segment of each of its rows into L2
+        prefetch_l2_bulk(X + (uint64_t)(row0 + tid) * K + (uint64_t)v0 * 8, nv * 16u);
+    const float2 *hm = split + (uint64_t)v0 * 8;
+    const uint32_t g = lane >> 3, j = lane & 7u;
+    const uint32_t r = row0 + warp * 8 + g * 2;  // this group's rows r, r + 1
+    const bool ok0 = r < n_rows, ok1 = r + 1 < n_rows;
+    const uint4 *x0 = (const uint4 *)(X + (uint64_t)(ok0 ? r : 0) * K) + v0;
+    const uint4 *x1 = (const uint4 *)(X + (uint64_t)(ok1 ? r + 1 : 0) * K) + v0;
+    uint64_t rs = 0ull, rc = 0ull, m = 0ull;
+    uint32_t v = j;
+    for (; v + 8 < nv; v += 16) {  // two vector steps in flight
+        const uint4 a0 = ok0 ? ld_stream(x0 + v) : make_uint4(0, 0, 0, 0);
+        const uint4 a1 = ok1 ? ld_stream(x1 + v) : make_uint4(0, 0, 0, 0);
+        const uint4 b0 = ok0 ? ld_stream(x0 + v + 8) : make_uint4(0, 0, 0, 0);
+        const uint4 b1 = ok1 ? ld_stream(x1 + v + 8) : make_uint4(0, 0, 0, 0);
+        check_vec(a0, a1, hm + 8 * v, rs, rc, m);
+        check_vec(b0, b1, hm + 8 * (v + 8), rs, rc, m);
     }
-    float rs[kCheckRows], rc[kCheckRows], ms[kCheckRows], mc[kCheckRows];
-#pragma unroll
-    for (uint32_t rp = 0; rp < kCheckRows / 2; ++rp) {
-        f2_unpack(rs2[rp], rs[2 * rp], rs[2 * rp + 1]);
-        f2_unpack(rc2[rp], rc[2 * rp], rc[2 * rp + 1]);
-        f2_unpack(ms2[rp], ms[2 * rp], ms[2 * rp + 1]);
-        f2_unpack(mc2[rp], mc[2 * rp], mc[2 * rp + 1]);
+    if (v < nv) {
+        const uint4 a0 = ok0 ? ld_stream(x0 + v) : make_uint4(0, 0, 0, 0);
+        const uint4 a1 = ok1 ? ld_stream(x1 + v) : make_uint4(0, 0, 0, 0);
+        check_vec(a0, a1, hm + 8 * v, rs, rc, m);
     }
+    float s0, s1, c0, c1, m0, m1;
+    f2_unpack(rs, s0, s1);
+    f2_unpack(rc, c0, c1);
+    f2_unpack(m, m0, m1);
 #pragma unroll
-    for (uint32_t r = 0; r < kCheckRows; ++r) {
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float s2 = __shfl_xor_sync(0xffffffffu, rs[r], off), c2 = __shfl_xor_sync(0xffffffffu, rc[r], off);
-            const float t2 = __shfl_xor_sync(0xffffffffu, ms[r], off), d2 = __shfl_xor_sync(0xffffffffu, mc[r], off);
-            pair_merge(rs[r], rc[r], s2, c2);
-            pair_merge(ms[r], mc[r], t2, d2);
-        }
-        if (lane == 0) red[warp][r] = make_float4(rs[r], rc[r], ms[r], mc[r]);
+    for (int off = 4; off > 0; off >>= 1) {  // the group's 8 lanes, a fixed butterfly
+        pair_merge(s0, c0, __shfl_xor_sync(0xffffffffu, s0, off), __shfl_xor_sync(0xffffffffu, c0, off));
+        pair_merge(s1, c1, __shfl_xor_sync(0xffffffffu, s1, off), __shfl_xor_sync(0xffffffffu, c1, off));
+        m0 = __fadd_rn(m0, __shfl_xor_sync(0xffffffffu, m0, off));
+        m1 = __fadd_rn(m1, __shfl_xor_sync(0xffffffffu, m1, off));
+    }
+    if (j == 0) {
+        float4 *dst = part + (uint64_t)blockIdx.y * n_rows;
+        if (ok0) dst[r] = make_float4(s0, c0, m0, 0.0f);
+        if (ok1) dst[r + 1] = make_float4(s1, c1, m1, 0.0f);
     }
     __syncthreads();
-    if (tid < nr) {
-        float4 p = red[0][tid];
-        for (uint32_t w = 1; w < kCheckThreads / 32; ++w) {
-            const float4 q = red[w][tid];
-            pair_merge(p.x, p.y, q.x, q.y);
-            pair_merge(p.z, p.w, q.z, q.w);
-        }
-        const double ref = (double)p.x + (double)p.y, mag = (double)p.z + (double)p.w;
-        const uint64_t i = row0 + tid;
-        const double g = (double)K * 0x1p-22;
-        const double b =
-            (g * (1.0 + g) + (double)(n_sum + K + 64) * 0x1p-44) * mag + 2.0 * (double)K * (double)n_sum * 0x1p-126;
-        const double d = rowsum[i] - ref;
-        residual[i] = d;
-        bound[i] = b;
-        const uint8_t f = fabs(d) <= (double)tol_scale * b ? 0 : 1;  // NaN flags
-        flag[i] = f;
-        if (f) atomicAdd(n_flagged, 1u);
+    if (tid == 0) {
+        __threadfence();
+        last = atomicAdd(o.done + blockIdx.x, 1u) == o.n_splits - 1 ? 1u : 0u;
     }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    const uint32_t i = row0 + tid;
+    if (tid < kChkRows && i < n_rows) {
+        float s = 0.0f, c = 0.0f;
+        double mag = 0.0;
+        for (uint32_t y = 0; y < o.n_splits; ++y) {
+            const float4 p = __ldcg(part + (uint64_t)y * n_rows + i);
+            pair_merge(s, c, p.x, p.y);
+            mag = __dadd_rn(mag, (double)p.z);
+        }
+        const double ref = (double)s + (double)c;
+        mag *= 1.0 + o.delta;
+        const double gk = (double)K * 0x1p-22;
+        const double b = (gk * (1.0 + gk) + 20.0 * 0x1p-24 + (double)(o.n_sum + K + 64) * 0x1p-44) * mag +
+                         2.0 * (double)K * (double)o.n_sum * 0x1p-126;
+        const double d = o.checksum[i] - ref;
+        o.residual[i] = d;
+        o.bound[i] = b;
+        const uint8_t f = fabs(d) <= (double)o.tol_scale * b ? 0 : 1;  // NaN flags
+        o.flag[i] = f;
+        if (f) atomicAdd(o.n_flagged, 1u);
+    }
+    if (tid == 0) o.done[blockIdx.x] = 0u;  // ready for the next call
 }
 
 size_t round_up256(size_t x) { return (x + 255) / 256 * 256; }
 
-// Row slabs of a column sum over `rows` rows of K columns: about 608 blocks in all
-// (4 resident blocks on each of 152 SMs: one wave), at most kMaxSlabs, at least
+// Row slabs of a column sum over `rows` rows of K columns: about 456 blocks in all
+// (3 resident blocks on each of 152 SMs: one wave), at most kMaxSlabs, at least
 // 8 rows per slab.  A function of the shapes only, so the workspace size is too.
 uint32_t n_slabs_for(uint32_t rows, uint32_t K) {
     const uint32_t col_blocks = (K + 255) / 256;
-    uint32_t n = 608 / col_blocks;
+    uint32_t n = 456 / col_blocks;
     if (n > kMaxSlabs) n = kMaxSlabs;
     if (n > rows / 8) n = rows / 8;
     return n < 1 ? 1 : n;
 }
 
-// Workspace: row partials [ceil(N/256)][M] | column partials [ceil(M/128)][N] | W's column sums
-// wcol [K] and their pair split wsplit [K] | A's, acol [K] and asplit [K] |
-// slabs [max(n_slabs(N, K), n_slabs(M, K))][K] (used for W, then for A) | abort word.
+// K splits of the check of `rows` rows: enough blocks of kChkRows rows for
+// about three waves of 16 blocks on each of 152 SMs, with at least 16 vectors
+// per lane and split.  A function of the shapes only, so the workspace size is
+// too.
+uint32_t n_splits_for(uint32_t rows, uint32_t K) {
+    const uint32_t nvec = K / 8, row_blocks = (rows + kChkRows - 1) / kChkRows;
+    uint32_t n = (3u * 16u * 152u + row_blocks - 1) / row_blocks;
+    const uint32_t most = nvec / 128 > 0 ? nvec / 128 : 1;  // 16 vectors per lane
+    return n > most ? most : (n < 1 ? 1 : n);
+}
+
+// The plain float32 chains behind the magnitude, for its raise factor: the
+// longest run of rows one warp sums in a column-sum slab, and the longest run
+// of columns one lane group sums in a check split.
+double mag_delta(uint32_t rows_summed, uint32_t K, uint32_t n_slabs, uint32_t n_splits) {
+    const uint32_t slab_rows = (rows_summed + n_slabs - 1) / n_slabs;
+    const double l1 = (double)((slab_rows + 7) / 8);
+    const uint32_t vps = (K / 8 + n_splits - 1) / n_splits;
+    const double l2 = (double)((vps + 7) / 8) * 8.0;
+    return 2.0 * (l1 + l2 + (double)n_splits + 8.0) * 0x1p-24;
+}
+
+// Workspace: row partials [ceil(N/256)][M] | column partials [ceil(M/128)][N] | W's column sums wsplit [K] |
+// A's, asplit [K] | slabs [max(n_slabs(N, K), n_slabs(M, K))][K] (used for W, then for A) | the check's
+// split partials [max(S(M) M, S(N) N)] | the verifier's last-block counters (one per row block of the
+// check, or per 256-column block of the column sums: zeroed by each verify call) | abort word.
 struct AbftWs {
-    size_t part, cpart, wcol, wsplit, acol, asplit, slabs, err, total;
+    size_t part, cpart, wsplit, asplit, slabs, chk, done, err, total;
 };
 AbftWs abft_ws(uint32_t M, uint32_t N, uint32_t K) {
     AbftWs w;
     const size_t ns = n_slabs_for(N, K) > n_slabs_for(M, K) ? n_slabs_for(N, K) : n_slabs_for(M, K);
+    const size_t nc_r = (size_t)n_splits_for(M, K) * M, nc_c = (size_t)n_splits_for(N, K) * N;
     w.part = 0;
     const size_t tiles_m = (M + kBM - 1) / kBM, tiles_n = (N + kBN - 1) / kBN;
     w.cpart = round_up256(tiles_n * M * sizeof(double));
-    w.wcol = w.cpart + round_up256(tiles_m * N * sizeof(double));
-    w.wsplit = w.wcol + round_up256((size_t)K * sizeof(double2));
-    w.acol = w.wsplit + round_up256((size_t)K * sizeof(float4));
-    w.asplit = w.acol + round_up256((size_t)K * sizeof(double2));
-    w.slabs = w.asplit + round_up256((size_t)K * sizeof(float4));
-    w.err = w.slabs + round_up256(ns * K * sizeof(float4));
+    w.wsplit = w.cpart + round_up256(tiles_m * N * sizeof(double));
+    w.asplit = w.wsplit + round_up256((size_t)K * sizeof(float2));
+    w.slabs = w.asplit + round_up256((size_t)K * sizeof(float2));
+    w.chk = w.slabs + round_up256(ns * K * sizeof(float4));
+    w.done = w.chk + round_up256((nc_r > nc_c ? nc_r : nc_c) * sizeof(float4));
+    const size_t row_blocks = ((M > N ? M : N) + kChkRows - 1) / kChkRows, col_blocks = (K + 255) / 256;
+    w.err = w.done + round_up256((row_blocks > col_blocks ? row_blocks : col_blocks) * sizeof(uint32_t));
     w.total = w.err + 256;
     return w;
 }
@@ -649,30 +745,35 @@ sdc_status sdc_abft_verify(const void *d_A, const void *d_W, uint32_t M, uint32_
                      dev);
     if (st != SDC_OK) return st;
     const AbftWs w = abft_ws(M, N, K);
-    double2 *wcol = (double2 *)((char *)d_ws + w.wcol), *acol = (double2 *)((char *)d_ws + w.acol);
-    float4 *wsplit = (float4 *)((char *)d_ws + w.wsplit), *asplit = (float4 *)((char *)d_ws + w.asplit);
-    float4 *slabs = (float4 *)((char *)d_ws + w.slabs);
+    float2 *wsplit = (float2 *)((char *)d_ws + w.wsplit), *asplit = (float2 *)((char *)d_ws + w.asplit);
+    float4 *slabs = (float4 *)((char *)d_ws + w.slabs), *chk = (float4 *)((char *)d_ws + w.chk);
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = cudaMemsetAsync(d_summary, 0, sizeof(sdc_abft_summary), s);
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_verify setup");
+    uint32_t *done = (uint32_t *)((char *)d_ws + w.done);
+    const size_t done_bytes = w.err - w.done;
+    // One side of the check: the column sums of Y [n_sum][K] over its rows, then X [n_rows][K] against them.
+    auto side = [&](const void *X, uint32_t n_rows, const void *Y, uint32_t n_sum, float2 *split,
+                    const double *checksum, double *res, double *bnd, uint8_t *flg, uint32_t *count) -> cudaError_t {
+        // vps vectors per split; nsp re-derived from it, so that no split is empty
+        const uint32_t ns = n_slabs_for(n_sum, K), vps = (K / 8 + n_splits_for(n_rows, K) - 1) / n_splits_for(n_rows, K);
+        const uint32_t nsp = (K / 8 + vps - 1) / vps;
+        cudaError_t err = cudaMemsetAsync(done, 0, done_bytes, s);
+        if (err != cudaSuccess) return err;
+        abft_colsum_slab_kernel<<<dim3((K + 255) / 256, ns), 256, 0, s>>>((const __nv_bfloat16 *)Y, n_sum, K, ns,
+                                                                         slabs, split, done);
+        CheckOut o{checksum, res, bnd, flg, count, done, mag_delta(n_sum, K, ns, nsp), tol_scale, n_sum, nsp};
+        abft_check_kernel<<<dim3((n_rows + kChkRows - 1) / kChkRows, nsp), 128, 0, s>>>(
+            (const __nv_bfloat16 *)X, n_rows, K, vps, split, chk, o);
+        return cudaGetLastError();
+    };
     // rows: A (W^T 1) over the N columns each row checksum sums
-    const uint32_t nsw = n_slabs_for(N, K);
-    abft_colsum_slab_kernel<<<dim3((K + 255) / 256, nsw), 256, 0, s>>>((const __nv_bfloat16 *)d_W, N, K, nsw, slabs);
-    abft_colsum_final_kernel<<<(K + 31) / 32, 256, 0, s>>>(slabs, K, nsw, wcol, wsplit);
-    abft_check_kernel<<<(M + kCheckRows - 1) / kCheckRows, kCheckThreads, 0, s>>>((const __nv_bfloat16 *)d_A, M, N, K,
-                                                                                d_rowsum, wsplit,
-                                                               tol_scale, d_residual, d_bound, d_flag,
-                                                               &d_summary->n_flagged);
-    if (cols) {  // columns: W (A^T 1) over the M rows each column checksum sums
-        const uint32_t nsa = n_slabs_for(M, K);
-        abft_colsum_slab_kernel<<<dim3((K + 255) / 256, nsa), 256, 0, s>>>((const __nv_bfloat16 *)d_A, M, K, nsa,
-                                                                          slabs);
-        abft_colsum_final_kernel<<<(K + 31) / 32, 256, 0, s>>>(slabs, K, nsa, acol, asplit);
-        abft_check_kernel<<<(N + kCheckRows - 1) / kCheckRows, kCheckThreads, 0, s>>>((const __nv_bfloat16 *)d_W, N, M,
-                                                                                    K, d_colsum, asplit,
-                                                                   tol_scale, d_residual_col, d_bound_col, d_flag_col,
-                                                                   &d_summary->n_flagged_cols);
-    }
+    e = side(d_A, M, d_W, N, wsplit, d_rowsum, d_residual, d_bound, d_flag, &d_summary->n_flagged);
+    // columns: W (A^T 1) over the M rows each column checksum sums
+    if (e == cudaSuccess && cols)
+        e = side(d_W, N, d_A, M, asplit, d_colsum, d_residual_col, d_bound_col, d_flag_col,
+                 &d_summary->n_flagged_cols);
+    if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_verify launch");
     e = cudaGetLastError();
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_abft_verify launch");
 }

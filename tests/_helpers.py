@@ -56,9 +56,28 @@ def stats_match(gpu: dict, ref: dict, rtol: float = 1e-10) -> None:
         assert gpu["nonfinite_fp32"] == ref["nonfinite_fp32"]
 
 
-def verifier_pair_slack(n_sum: int, K: int) -> float:
-    """The GEMM check kernel's own term, relative to the magnitude: it carries A(W^T 1),
-    the magnitude and its column sums as float32 pairs (about 48 bits), so its bound adds
-    (n_sum + K + 64) 2^-44 of the magnitude to the method's bound, and its residual and
-    bound agree with exact float64 sums to that term."""
-    return (n_sum + K + 64) * 2.0 ** -44
+def verifier_own_slack(n_sum: int, K: int) -> float:
+    """The GEMM check kernel's own term, relative to the magnitude: it sums in plain float32
+    chains of at most 8 terms folded into float32 pairs (below 20 2^-24 of the magnitude in
+    all) and carries the pairs and their merges at about 48 bits ((n_sum + K + 64) 2^-44).
+    Its bound adds this term, and its residual agrees with exact sums to it."""
+    return 20.0 * 2.0 ** -24 + (n_sum + K + 64) * 2.0 ** -44
+
+
+def verifier_mag_slack(n_sum: int, K: int) -> float:
+    """How far above the exact magnitude the GEMM check's raised magnitude may sit, relative:
+    it sums |W| and |A| |W^T 1| in plain float32 chains (at most n_sum / 8 rows and K / 8 + 8
+    columns long, at most K / 64 + 1 splits) and raises the result by twice their length in
+    units of 2^-24, so that it is never below the exact magnitude."""
+    return 2.0 * (n_sum / 8 + K / 4 + 32) * 2.0 ** -24
+
+
+def assert_verifier_bound(kernel_bound, method_bound, mag, n_sum: int, K: int) -> None:
+    """The kernel's bound is never below the method's (no clean output can flag for the
+    kernel's own rounding), and above it by no more than the kernel's own terms: its own
+    sums (verifier_own_slack) and its raised magnitude (verifier_mag_slack)."""
+    import numpy as np
+    kb, mb, mg = (np.asarray(x, dtype=np.float64) for x in (kernel_bound, method_bound, mag))
+    assert np.all(kb >= mb * (1.0 - 1e-12)), float(np.min(kb / mb))
+    top = (mb + verifier_own_slack(n_sum, K) * mg) * (1.0 + verifier_mag_slack(n_sum, K)) * (1.0 + 1e-12)
+    assert np.all(kb <= top), float(np.max(kb / top))

@@ -111,11 +111,14 @@ def test_host_validation_without_gpu(sdc):
             sdc.sdc_abft_verify(4096, 8192, M, N, K, 0, 0, 1.0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0)
         assert ei.value.status == 9, (M, N, K)
     # row partials (ceil(N/256) per row), column partials (ceil(M/128) per column), W's and A's column sums
-    # (K float64 pairs) and their float32 pair splits (K x 16 bytes), slabs of K x 16 bytes for the
-    # larger of the two column sums (slabs = min(608 / ceil(K / 256), 64, rows / 8)), the abort
-    # word; each rounded up to 256 bytes
-    assert sdc.sdc_abft_workspace_size(128, 512, 64) == 2048 + 1 * 512 * 8 + 4 * 1024 + 64 * 64 * 16 + 256
-    assert sdc.sdc_abft_workspace_size(1000, 256, 100) == 8192 + 8 * 256 * 8 + 4 * 1792 + 64 * 100 * 16 + 256
+    # (K x 8 bytes each: the sum and the magnitude in float32), slabs of K x 16 bytes for the
+    # larger of the two column sums (slabs = min(456 / ceil(K / 256), 64, rows / 8)), the check's split
+    # partials (16 bytes per row and split; one split when K / 8 < 64), the last-block counters (a word
+    # per 32-row block of the larger side, or per 256 columns), the abort word; each rounded up to 256 bytes
+    assert sdc.sdc_abft_workspace_size(128, 512, 64) == (2048 + 1 * 512 * 8 + 2 * 512 + 64 * 64 * 16
+                                                         + 512 * 16 + 256 + 256)
+    assert sdc.sdc_abft_workspace_size(1000, 256, 100) == (8192 + 8 * 256 * 8 + 2 * 1024 + 64 * 100 * 16
+                                                           + 16128 + 256 + 256)
     # bounded-wait self-test: arguments checked before the launch
     with pytest.raises(sdc.SdcError) as ei:
         sdc.sdc_selftest_bounded_wait(10, 0, 0)
@@ -155,8 +158,8 @@ def test_host_validation_without_gpu(sdc):
         sdc.sdc_attn_dv_check_grouped(4096, 8192, 16384, 32768, 1024, 1024, 65536 + 128, 128, 0.088, 0, 1.0, *outs,
                                       0, 0, 0)
     assert ei.value.status == 9
-    assert sdc.sdc_abft_workspace_size(128, 16384, 64) == (64 * 128 * 8 + 1 * 16384 * 8 + 4 * 1024 + 64 * 64 * 16
-                                                           + 256)
+    assert sdc.sdc_abft_workspace_size(128, 16384, 64) == (64 * 128 * 8 + 1 * 16384 * 8 + 2 * 512 + 64 * 64 * 16
+                                                           + 16384 * 16 + 16384 // 32 * 4 + 256)
 
 
 def test_pages_verdict_decoding(sdc):

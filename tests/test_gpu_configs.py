@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import sdc_workloads as W
-from tests._helpers import fp_table, host_bits, stats_match, verifier_pair_slack
+from tests._helpers import assert_verifier_bound, fp_table, host_bits, stats_match
 
 pytestmark = [pytest.mark.gpu, pytest.mark.big]
 DEV = "cuda"
@@ -182,8 +182,7 @@ def test_gemm_checksum_bench_shape(sdc):
     bound_r = oracle.abft_bound(mag_r, N, K)
     rs = g.rowsum.cpu().numpy()[rows]
     assert np.all(np.abs(rs - exact.sum(axis=1)) <= bound_r)
-    eps = verifier_pair_slack(N, K)
-    np.testing.assert_allclose(g.bound.cpu().numpy()[rows], bound_r + eps * mag_r, rtol=eps)
+    assert_verifier_bound(g.bound.cpu().numpy()[rows], bound_r, mag_r, N, K)
     cols = np.sort(rng.choice(N, 8, replace=False))
     exact_c = (A64 @ W64[cols].T).sum(axis=0)
     bound_c = oracle.abft_bound(np.abs(W64[cols]) @ np.abs(A64).sum(axis=0), M, K)
