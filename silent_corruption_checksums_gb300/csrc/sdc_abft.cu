@@ -445,7 +445,18 @@ __global__ void __launch_bounds__(256, 3) abft_colsum_slab_kernel(const __nv_bfl
     __threadfence();
     if (kk < K) {
         float4 acc = __ldcg(slabs + kk);
-        for (uint32_t y = 1; y < n_slabs; ++y) {
+        uint32_t y = 1;
+        for (; y + 8 <= n_slabs; y += 8) {  // 8 slabs' loads in flight, merged in slab order
+            float4 q[8];
+#pragma unroll
+            for (uint32_t u = 0; u < 8; ++u) q[u] = __ldcg(slabs + (uint64_t)(y + u) * K + kk);
+#pragma unroll
+            for (uint32_t u = 0; u < 8; ++u) {
+                pair_merge(acc.x, acc.y, q[u].x, q[u].y);
+                pair_merge(acc.z, acc.w, q[u].z, q[u].w);
+            }
+        }
+        for (; y < n_slabs; ++y) {
             const float4 q = __ldcg(slabs + (uint64_t)y * K + kk);
             pair_merge(acc.x, acc.y, q.x, q.y);
             pair_merge(acc.z, acc.w, q.z, q.w);
@@ -570,7 +581,18 @@ __global__ void __launch_bounds__(128) abft_check_kernel(const __nv_bfloat16 *__
     if (tid < kChkRows && i < n_rows) {
         float s = 0.0f, c = 0.0f;
         double mag = 0.0;
-        for (uint32_t y = 0; y < o.n_splits; ++y) {
+        uint32_t y = 0;
+        for (; y + 4 <= o.n_splits; y += 4) {  // 4 splits' loads in flight, merged in split order
+            float4 p[4];
+#pragma unroll
+            for (uint32_t u = 0; u < 4; ++u) p[u] = __ldcg(part + (uint64_t)(y + u) * n_rows + i);
+#pragma unroll
+            for (uint32_t u = 0; u < 4; ++u) {
+                pair_merge(s, c, p[u].x, p[u].y);
+                mag = __dadd_rn(mag, (double)p[u].z);
+            }
+        }
+        for (; y < o.n_splits; ++y) {
             const float4 p = __ldcg(part + (uint64_t)y * n_rows + i);
             pair_merge(s, c, p.x, p.y);
             mag = __dadd_rn(mag, (double)p.z);
