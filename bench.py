@@ -431,7 +431,7 @@ def _time_loop(fn, steps, stream, torch):
 def bench_rows(args, dev, stream, peaks, sdc, W, torch, np, only=None) -> dict:
     """The other rows of the hot path, each timed on its own workload."""
     rows = {}
-    if only in ("fingerprint_8b", "fingerprint_stress"):
+    if only in ("fingerprint_8b", "fingerprint_stress", "xorsum_pairs"):
         return bench_big_rows(args, dev, stream, peaks, sdc, W, torch, only)
     if only == "abft_gemm":
         return bench_abft_row(args, dev, stream, peaks, sdc, W, torch)
@@ -700,6 +700,10 @@ def bench_big_rows(args, dev, stream, peaks, sdc, W, torch, only) -> dict:
             1 << 30, "fingerprint, replica-major")
         del w8
         torch.cuda.empty_cache()
+    if only == "xorsum_pairs":  # the pairs alone (profiling): the stress set's pairs, one tensor beside them
+        w = W.stress(dev, seed=5, n_tensors=1)
+        rows.update(bench_xor_pairs_row(w["pairs"], stream, peaks, sdc, torch, oracle))
+        return rows
     if only in (None, "fingerprint_stress"):
         nt = getattr(args, "stress_tensors", 100_000)
         w = W.stress(dev, seed=5, n_tensors=nt)
@@ -709,29 +713,37 @@ def bench_big_rows(args, dev, stream, peaks, sdc, W, torch, only) -> dict:
         rows["fingerprint_stress"]["cpu_baseline"] = oracle_stream_rate(
             [t for ts in w["replicas"] for t in ts], lambda h, th: oracle.fingerprint(h, threads=th), 2 << 30,
             256 << 20, "fingerprint, replica-major")
-        p = w["pairs"]
-        xplan = sdc.Plan([p["orig"], p["recomp"]])
-        xo = torch.empty((2, len(p["orig"])), dtype=torch.int64, device=dev)
-
-        def xs_step():
-            xplan.xorsum(out=xo, stream=stream)
-            sdc.xorsum_compare(xo[0], xo[1], stream=stream)
-
-        ms = _time_loop(xs_step, 20, stream, torch)
-        nbytes = sum(t.numel() * t.element_size() for t in p["orig"]) * 2
-        ho, hr = [host_bits(t) for t in p["orig"]], [host_bits(t) for t in p["recomp"]]
-
-        def oracle_pairs(threads):
-            oracle.xorsum_compare([oracle.xorsum(h, threads=threads) for h in ho],
-                                  [oracle.xorsum(h, threads=threads) for h in hr])
-        rows["xorsum_pairs_stress"] = {"workload": "1,000 (original, recomputed) pairs, sizes 1..1e6, half with a "
-                                       "one-bit difference: xorsum + compare", "ms": ms, "bytes": nbytes,
-                                       "GB_s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"],
-                                       "cpu_baseline": oracle_rate(oracle_pairs, nbytes, "all 1,000 pairs",
-                                                                   single=oracle_pairs, single_bytes=nbytes,
-                                                                   single_sample="all 1,000 pairs")}
-        del w, xplan, p, ho, hr
+        rows.update(bench_xor_pairs_row(w["pairs"], stream, peaks, sdc, torch, oracle))
+        del w
         torch.cuda.empty_cache()
+    return rows
+
+
+def bench_xor_pairs_row(p, stream, peaks, sdc, torch, oracle) -> dict:
+    """Xorsum + compare of the stress set's 1,000 (original, recomputed) pairs."""
+    rows = {}
+    xplan = sdc.Plan([p["orig"], p["recomp"]])
+    xo = torch.empty((2, len(p["orig"])), dtype=torch.int64, device=p["orig"][0].device)
+
+    def xs_step():
+        xplan.xorsum(out=xo, stream=stream)
+        sdc.xorsum_compare(xo[0], xo[1], stream=stream)
+
+    ms = _time_loop(xs_step, 20, stream, torch)
+    nbytes = sum(t.numel() * t.element_size() for t in p["orig"]) * 2
+    ho, hr = [host_bits(t) for t in p["orig"]], [host_bits(t) for t in p["recomp"]]
+
+    def oracle_pairs(threads):
+        oracle.xorsum_compare([oracle.xorsum(h, threads=threads) for h in ho],
+                              [oracle.xorsum(h, threads=threads) for h in hr])
+
+    rows["xorsum_pairs_stress"] = {"workload": "1,000 (original, recomputed) pairs, sizes 1..1e6, half with a "
+                                   "one-bit difference: xorsum + compare", "ms": ms, "bytes": nbytes,
+                                   "GB_s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"],
+                                   "cpu_baseline": oracle_rate(oracle_pairs, nbytes, "all 1,000 pairs",
+                                                               single=oracle_pairs, single_bytes=nbytes,
+                                                               single_sample="all 1,000 pairs")}
+    del xplan, ho, hr
     return rows
 
 
@@ -868,7 +880,7 @@ def main(argv=None) -> None:
     ap.add_argument("--quick", action="store_true", help="only the timed fingerprint step (no rows/e2e/cpu)")
     ap.add_argument("--no-big-rows", action="store_true", help="skip the 8b and stress rows")
     ap.add_argument("--only", choices=["grad_average_scan", "grad_scan", "xorsum", "abft_gemm", "attn_invariant",
-                                       "fingerprint_8b",
+                                       "fingerprint_8b", "xorsum_pairs",
                                        "fingerprint_stress", "adamw_fingerprint"], default=None,
                     help="time one row alone (profiling)")
     ap.add_argument("--layers-8b", type=int, default=32,

@@ -85,7 +85,9 @@ typedef struct {
 } sdc_tensor_desc;
 
 /* Plan options; a zero field takes its default.  chunk_bytes: bytes of one
- * warp task, a power of two in [4096, 32768] (default 16384); ctas_per_sm:
+ * warp task, a power of two in [4096, 32768] (default 16384, halved down to
+ * 4096 while the plan would give fewer than 16 tasks per warp of the
+ * persistent grid: 32 warps per SM); ctas_per_sm:
  * resident CTAs per SM of the persistent kernels (default: the occupancy
  * limit); skip_pointer_checks: 1 skips the driver queries that check every
  * descriptor's range lies inside one device allocation of this device. */

@@ -203,14 +203,16 @@ sdc_status sdc_plan_create(const sdc_tensor_desc *host_descs, uint32_t T, uint32
     if (n_desc >= kMaxDescs) return fail(SDC_ERR_BAD_ARG, "R * T too large");
     if (n_desc && !host_descs) return fail(SDC_ERR_NULL, "host_descs is NULL");
 
-    uint32_t chunk_bytes = 16384;
+    uint32_t chunk_bytes = 0;  // 0: chosen below from the plan's size
     uint32_t ctas_per_sm = 0;
     bool check_ptrs = true;
     if (opts) {
-        if (opts->chunk_bytes) chunk_bytes = opts->chunk_bytes;
+        chunk_bytes = opts->chunk_bytes;
         ctas_per_sm = opts->ctas_per_sm;
         check_ptrs = opts->skip_pointer_checks == 0;
     }
+    const bool auto_chunk = chunk_bytes == 0;
+    if (auto_chunk) chunk_bytes = 16384;
     if (chunk_bytes < 4096 || chunk_bytes > 32768 || (chunk_bytes & (chunk_bytes - 1)))
         return fail(SDC_ERR_BAD_ARG, "chunk_bytes must be a power of two in [4096, 32768]");
 
@@ -242,6 +244,16 @@ sdc_status sdc_plan_create(const sdc_tensor_desc *host_descs, uint32_t T, uint32
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+
+    // The default chunk: 16 KiB, halved (down to 4 KiB) while the plan would give fewer than 16 warp
+    // tasks per warp of the persistent grid (32 warps per SM), so that a small plan still spreads
+    // evenly over the SMs (its last wave of tasks is then a small part of the pass).
+    if (auto_chunk) {
+        uint64_t total = 0;
+        for (uint64_t d = 0; d < n_desc; ++d) total += host_descs[d].numel * host_descs[d].elem_size;
+        const uint64_t want = 16ull * 32ull * (uint64_t)sm_count(dev);
+        while (chunk_bytes > 4096 && total / chunk_bytes < want) chunk_bytes >>= 1;
+    }
 
     // every descriptor's byte range must lie in one allocation of this device;
     // ranges already proven by an earlier query are reused (sorted scan)
