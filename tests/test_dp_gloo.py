@@ -134,3 +134,45 @@ def test_two_ranks_two_copies_each():
         assert o["verdict"] == {"diverged": True, "suspects": [2]}
         assert o["ranks"] == [1]  # every rank names the same rank
         assert o["nonfinite"] == [1]
+
+
+def _worker_groups(rank, world, port, q):
+    import torch
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import oracle
+    from silent_corruption_checksums_gb300 import dp
+    # two data-parallel groups of two ranks each: {0, 2} and {1, 3} (the page's function takes any
+    # group that holds copies of the same shard); every rank holds 2 copies, global rank 3's first
+    # copy is corrupted, so only group {1, 3} diverges and it names global rank 3
+    groups = [dist.new_group([0, 2]), dist.new_group([1, 3])]
+    g = groups[rank % 2]
+    copies = [_replica(9, (0, 5, 30) if (rank == 3 and c == 0) else None) for c in range(2)]
+    gathered = dp.gather_rows(torch.from_numpy(_table(copies)), g)
+    _, _, summary = oracle.vote(gathered.numpy().view(np.uint64).tolist())
+    verdict = oracle.pages_verdict(summary)
+    ranks = dp.replica_ranks(verdict["suspects"], 2, g) if verdict["suspects"] else verdict["suspects"]
+    q.put({"rank": rank, "world": dp.world_of(g), "verdict": verdict, "ranks": ranks,
+           "first_copy_rank": dp.global_rank(0, g)})
+    dist.destroy_process_group()
+
+
+def test_subgroups_name_global_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker_groups, args=(r, 4, port, q)) for r in range(4)]
+    for p in procs:
+        p.start()
+    outs = sorted((q.get(timeout=180) for _ in procs), key=lambda o: o["rank"])
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for o in outs:
+        assert o["world"] == (o["rank"] // 2, 2)  # the rank within its group, the group's size
+        assert o["first_copy_rank"] == o["rank"] % 2
+        if o["rank"] % 2 == 0:  # group {0, 2}: all four copies agree
+            assert o["verdict"] == {"diverged": False, "suspects": []} and o["ranks"] == []
+        else:  # group {1, 3}: gathered copy 2 (group rank 1's first copy) is global rank 3's
+            assert o["verdict"] == {"diverged": True, "suspects": [2]} and o["ranks"] == [3]
