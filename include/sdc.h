@@ -344,10 +344,13 @@ size_t sdc_attn_workspace_size(uint32_t BH, uint32_t L, uint32_t D);
  *   d_colsum_dv[h][c] = sum_j of dV's float32 accumulator [j][c],
  *   d_colsum_do[h][c] = sum_i dO[i][c],
  *   d_residual = colsum_dv - colsum_do,
- *   d_bound = (2^-8 rho + g (1 + g) rho + 2^-40) sum_i |dO[i][c]| + 2^-100,
- *     g = L 2^-22, rho = 1 + 2^-7 (each probability within 2^-8 of itself:
- *     its bf16 rounding and up to 2^-9 for the recomputed scores, exp and the
- *     float32 log-sum-exp; each float32 accumulation step within two ulps),
+ *   d_bound = (2^-8 rho + g (1 + g) rho + own) A (1 + 2^-21) + 2^-100,
+ *     A = sum_i |dO[i][c]| (as summed here), g = L 2^-22, rho = 1 + 2^-7
+ *     (each probability within 2^-8 of itself: its bf16 rounding and up to
+ *     2^-9 for the recomputed scores, exp and the float32 log-sum-exp; each
+ *     float32 accumulation step within two ulps); own = 2^-40 + 2^-20 covers
+ *     this library's own column sums (float32 pairs of plain 8-row chains),
+ *     and the factor 1 + 2^-21 keeps A above the exact sum,
  *   d_flag[h][c] = 1 unless |residual| <= tol_scale * bound (NaN flags),
  * all double/uint8 [BH][D]; d_summary counts the flagged columns; *d_aborted
  * = 1 if a bounded wait gave up (results then invalid).

@@ -548,10 +548,12 @@ def attn_bound(abs_colsum_do: np.ndarray, L: int) -> np.ndarray:
     to 2^-9 for the recomputed scores, the exponential and the forward's float32
     log-sum-exp), so a row of P sums to 1 within 2^-8 (1 + 2^-7); each float32
     accumulation step may lose two units in the last place of its partial sum
-    (g = L 2^-22); the column sums themselves are float32 pairs (2^-40)."""
+    (g = L 2^-22).  The column sums of the check itself are taken as exact (the
+    oracle's are float64); a check that carries them in less precision adds its
+    own term on top."""
     g = L * 2.0 ** -22
     rho = 1.0 + 2.0 ** -7
-    return (2.0 ** -8 * rho + g * (1.0 + g) * rho + 2.0 ** -40) * np.asarray(abs_colsum_do, dtype=np.float64) + 2.0 ** -100
+    return (2.0 ** -8 * rho + g * (1.0 + g) * rho) * np.asarray(abs_colsum_do, dtype=np.float64) + 2.0 ** -100
 
 
 def attn_invariant(colsum_dv: np.ndarray, dO_bits: np.ndarray, tol_scale: float = 1.0) -> dict:

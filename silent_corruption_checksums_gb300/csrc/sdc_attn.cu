@@ -175,9 +175,13 @@ __device__ void head_invariant(const float2 *part_dv, const float4 *part_do, uin
         }
     }
     const double dv = (double)vs + (double)vc, dsum = (double)os + (double)oc, dabs = (double)as + (double)ac;
-    // dV's accumulation runs over the group's group * L query rows
+    // dV's accumulation runs over the group's group * L query rows.  Beyond the method's terms the
+    // bound carries this kernel's own: the float32 pairs of both column sums (2^-40) and the prep's
+    // plain chains of kPrepChain rows (below kPrepChain 2^-24 each, twice over: 16 2^-24), and it
+    // takes sum |dO| raised by kPrepChain 2^-24, above the exact sum whatever the chains lost.
     const double g = (double)group * (double)L * 0x1p-22, rho = 1.0 + 0x1p-7;
-    const double bnd = (0x1p-8 * rho + g * (1.0 + g) * rho + 0x1p-40) * dabs + 0x1p-100;
+    const double own = 0x1p-40 + 16.0 * 0x1p-24;
+    const double bnd = (0x1p-8 * rho + g * (1.0 + g) * rho + own) * dabs * (1.0 + 8.0 * 0x1p-24) + 0x1p-100;
     const double d = dv - dsum;
     const uint32_t i = kvh * kHD + c;
     o.colsum_dv[i] = dv;
@@ -644,14 +648,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 // unit's copy runs while this one is summed; the unit's log-sum-exps come on
 // the same barrier (rows x 4 bytes), so no thread waits on a global load.
 // Thread (column pair p, row quarter h) sums columns 2p and 2p + 1 over rows
-// 32h .. 32h + 31 as packed float32 pairs (TwoSum), for dO and |dO|; quarters
-// 1-3 are then merged into quarter 0 in that order.
+// 32h .. 32h + 31, for dO and |dO|: plain float32 chains of kPrepChain rows
+// folded into packed float32 pairs with TwoSum (each chain is off by at most
+// kPrepChain 2^-24 of its rows' |dO| sum, counted in the invariant's bound);
+// quarters 1-3 are then merged into quarter 0 in that order.
 constexpr uint32_t kPrepThreads = 256, kPrepQuarters = kPrepThreads / (kHD / 2);
 constexpr uint32_t kPrepScr = 2 * kTile;                                      // [3][64] x (dO pair, |dO| pair)
 constexpr uint32_t kPrepLse = kPrepScr + (kPrepQuarters - 1) * (kHD / 2) * 32;  // [2][128] float
 constexpr uint32_t kPrepBar = kPrepLse + 2 * kBlk * 4;                            // two mbarriers
 constexpr uint32_t kPrepSmem = kPrepBar + 16;
 constexpr uint32_t kPrepCtasPerSm = 3;
+constexpr uint32_t kPrepChain = 8;  // rows of a plain float32 chain before it is folded into a pair
 static_assert(kPrepCtasPerSm * (kPrepSmem + 1024) <= 233472, "prep CTAs per SM exceed shared memory");
 
 __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
@@ -700,11 +707,16 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
         const uint32_t *tile = (const uint32_t *)(psm + (i & 1) * kTile);  // [128 rows][64 column pairs]
         uint64_t s = 0, c = 0, sa = 0, ca = 0;
         const uint32_t r0 = h * (kBlk / kPrepQuarters), r1 = min(r0 + kBlk / kPrepQuarters, rows);
-#pragma unroll 8
-        for (uint32_t r = r0; r < r1; ++r) {
-            const uint32_t w = tile[r * (kHD / 2) + cp], wa = w & 0x7FFF7FFFu;
-            pair2_add(s, c, f2_pack_bits(w << 16, w & 0xFFFF0000u));
-            pair2_add(sa, ca, f2_pack_bits(wa << 16, wa & 0xFFFF0000u));
+        for (uint32_t rc = r0; rc < r1; rc += kPrepChain) {  // plain chains of kPrepChain rows, folded into pairs
+            uint64_t t = 0, ta = 0;
+#pragma unroll
+            for (uint32_t u = 0; u < kPrepChain; ++u) {
+                const uint32_t w = rc + u < r1 ? tile[(rc + u) * (kHD / 2) + cp] : 0u, wa = w & 0x7FFF7FFFu;
+                t = f2_add(t, f2_pack_bits(w << 16, w & 0xFFFF0000u));
+                ta = f2_add(ta, f2_pack_bits(wa << 16, wa & 0xFFFF0000u));
+            }
+            pair2_add(s, c, t);
+            pair2_add(sa, ca, ta);
         }
         ulonglong2 *scr = (ulonglong2 *)(psm + kPrepScr);  // [quarter - 1][pair][2]
         if (h > 0) {

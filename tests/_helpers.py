@@ -81,3 +81,20 @@ def assert_verifier_bound(kernel_bound, method_bound, mag, n_sum: int, K: int) -
     assert np.all(kb >= mb * (1.0 - 1e-12)), float(np.min(kb / mb))
     top = (mb + verifier_own_slack(n_sum, K) * mg) * (1.0 + verifier_mag_slack(n_sum, K)) * (1.0 + 1e-12)
     assert np.all(kb <= top), float(np.max(kb / top))
+
+
+# The attention check's own terms, relative to A = sum_i |dO[i, c]|: its column sums are float32
+# pairs (2^-40) of plain 8-row chains (below 8 2^-24 each, counted twice: 2^-20), and it raises A by
+# 2^-21 so that its bound never falls below the method's whatever the chains lost.
+ATTN_OWN_SLACK = 2.0 ** -40 + 2.0 ** -20
+ATTN_MAG_RAISE = 2.0 ** -21
+
+
+def assert_attn_bound(kernel_bound, method_bound, abs_colsum) -> None:
+    """The attention check's bound is never below the method's and above it by at most its own
+    terms (ATTN_OWN_SLACK of sum |dO|, and the raise of sum |dO|)."""
+    import numpy as np
+    kb, mb, a = (np.asarray(x, dtype=np.float64) for x in (kernel_bound, method_bound, abs_colsum))
+    assert np.all(kb >= mb * (1.0 - 1e-12)), float(np.min(kb / mb))
+    top = (mb + ATTN_OWN_SLACK * a) * (1.0 + 2.0 * ATTN_MAG_RAISE) * (1.0 + 1e-12)
+    assert np.all(kb <= top), float(np.max(kb / top))
