@@ -519,6 +519,55 @@ def abft_verify(rowsum: np.ndarray, A_bits: np.ndarray, W_bits: np.ndarray, tol_
 
 
 # --------------------------------------------------------------------------
+# Weight-gradient configuration  ([AEGIS] method section 2: the row
+# configuration leaves wgrad partly uncovered, the row + column configuration
+# covers every matmul class, wgrad included).  A linear layer's weight gradient
+# is dW = dY^T X, with the output gradient dY [T, N] and the layer's input
+# X [T, K] held token-major, as the backward pass has them; the contraction
+# runs over the T tokens.
+# --------------------------------------------------------------------------
+def wgrad_product(dY_bits: np.ndarray, X_bits: np.ndarray) -> np.ndarray:
+    """dW = dY^T X in float64 for bf16 dY [T, N] and X [T, K]: dW [N, K]."""
+    return bf16_to_f64(dY_bits).T @ bf16_to_f64(X_bits)
+
+
+def wgrad_reference(dY_bits: np.ndarray, X_bits: np.ndarray) -> dict:
+    """The two sides of the check of dW = dY^T X, float64.
+
+    Rows: dW 1 = dY^T (X 1), and the magnitude sum_t |dY[t, n]| sum_k |X[t, k]|.
+    Columns: 1^T dW = (1^T dY^T) X = (dY 1)^T X, and the magnitude
+    sum_t (sum_n |dY[t, n]|) |X[t, k]|."""
+    dY = bf16_to_f64(dY_bits)
+    X = bf16_to_f64(X_bits)
+    r, ra = X.sum(axis=1), np.abs(X).sum(axis=1)    # X 1 and |X| 1, one per token
+    q, qa = dY.sum(axis=1), np.abs(dY).sum(axis=1)  # dY 1 and |dY| 1
+    return {"row_ref": dY.T @ r, "row_mag": np.abs(dY).T @ ra, "col_ref": X.T @ q, "col_mag": np.abs(X).T @ qa}
+
+
+def wgrad_verify(rowsum: np.ndarray, colsum, dY_bits: np.ndarray, X_bits: np.ndarray,
+                 tol_scale: float = 1.0) -> dict:
+    """The check of one weight-gradient product: per output row n, residual = the
+    accumulator checksum - dY^T (X 1), bound over the K outputs the row sums with a
+    contraction of T; per output column (colsum given), the same over the N rows.
+    A row or column flags unless |residual| <= tol_scale * bound (NaN flags)."""
+    T, N = dY_bits.shape
+    K = X_bits.shape[1]
+    ref = wgrad_reference(dY_bits, X_bits)
+    out = {}
+    sides = [("", rowsum, ref["row_ref"], ref["row_mag"], K)]
+    if colsum is not None:
+        sides.append(("_col", colsum, ref["col_ref"], ref["col_mag"], N))
+    for tag, got, want, mag, n_sum in sides:
+        residual = np.asarray(got, dtype=np.float64) - want
+        bound = abft_bound(mag, n_sum, T)
+        with np.errstate(invalid="ignore"):
+            flag = ~(np.abs(residual) <= tol_scale * bound)
+        out.update({"residual" + tag: residual, "bound" + tag: bound, "flag" + tag: flag.astype(np.uint8),
+                    "n_flagged" + tag: int(flag.sum())})
+    return out
+
+
+# --------------------------------------------------------------------------
 # Attention invariant  ([AEGIS] method section 3: in the attention backward
 # dV = P^T dO and every row of the softmax P sums to 1, so 1^T dV = 1^T dO;
 # the column sums of dV come from its float32 accumulator)

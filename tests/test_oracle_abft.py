@@ -204,3 +204,98 @@ def test_column_bound_covers_float32_accumulation(mode):
     v = oracle.abft_verify_cols(acc.sum(axis=0), Ab, Wb)
     assert v["n_flagged"] == 0
     assert np.max(np.abs(v["residual"]) / v["bound"]) <= 1.0
+
+
+# ---------------------------------------------------------------- weight-gradient configuration
+# dW = dY^T X with dY [T, N] and X [T, K] token-major; the row + column configuration covers it
+# ([AEGIS] method section 2).
+
+def test_wgrad_product_and_both_sides_brute_force():
+    T, N, K = 9, 7, 12
+    rng = np.random.default_rng(21)
+    dY, X = rng.integers(-9, 10, size=(T, N)), rng.integers(-9, 10, size=(T, K))
+    dYb, Xb = _bf16_bits(dY.astype(np.float32)), _bf16_bits(X.astype(np.float32))
+    brute = [[sum(int(dY[t, n]) * int(X[t, k]) for t in range(T)) for k in range(K)] for n in range(N)]
+    dW = oracle.wgrad_product(dYb, Xb)
+    assert dW.tolist() == brute
+    ref = oracle.wgrad_reference(dYb, Xb)
+    assert ref["row_ref"].tolist() == [sum(r) for r in brute]
+    assert ref["col_ref"].tolist() == [sum(brute[n][k] for n in range(N)) for k in range(K)]
+    assert ref["row_mag"].tolist() == [sum(abs(int(dY[t, n])) * sum(abs(int(x)) for x in X[t]) for t in range(T))
+                                       for n in range(N)]
+    assert ref["col_mag"].tolist() == [sum(sum(abs(int(y)) for y in dY[t]) * abs(int(X[t, k])) for t in range(T))
+                                       for k in range(K)]
+    v = oracle.wgrad_verify(dW.sum(axis=1), dW.sum(axis=0), dYb, Xb)
+    assert v["n_flagged"] == 0 and v["n_flagged_col"] == 0
+    assert np.all(v["residual"] == 0) and np.all(v["residual_col"] == 0)
+
+
+def test_wgrad_single_token_is_an_outer_product():
+    rng = np.random.default_rng(22)
+    dY, X = rng.integers(-5, 6, size=(1, 6)), rng.integers(-5, 6, size=(1, 10))
+    dYb, Xb = _bf16_bits(dY.astype(np.float32)), _bf16_bits(X.astype(np.float32))
+    assert np.array_equal(oracle.wgrad_product(dYb, Xb), np.outer(dY[0], X[0]).astype(float))
+
+
+@pytest.mark.parametrize("operand", ["dY", "X"])
+def test_wgrad_planted_fault_closed_form(operand):
+    # the product reads a faulty operand, the check the clean one: a change delta at (t, j) moves
+    # dY fault (t, n): row n by delta sum_k X[t, k], column k by delta X[t, k]
+    # X fault (t, k): column k by delta sum_n dY[t, n], row n by delta dY[t, n]
+    T, N, K = 11, 8, 16
+    rng = np.random.default_rng(23)
+    dY, X = rng.integers(-8, 9, size=(T, N)), rng.integers(-8, 9, size=(T, K))
+    dYb, Xb = _bf16_bits(dY.astype(np.float32)), _bf16_bits(X.astype(np.float32))
+    t, delta = 5, 3
+    if operand == "dY":
+        n = 6
+        dYf = dY.copy()
+        dYf[t, n] += delta
+        dW = oracle.wgrad_product(_bf16_bits(dYf.astype(np.float32)), Xb)
+        er = np.zeros(N)
+        er[n] = delta * X[t].sum()
+        ec = np.zeros(K)
+        ec[:] = delta * X[t]
+    else:
+        k = 13
+        Xf = X.copy()
+        Xf[t, k] += delta
+        dW = oracle.wgrad_product(dYb, _bf16_bits(Xf.astype(np.float32)))
+        er = (delta * dY[t]).astype(float)
+        ec = np.zeros(K)
+        ec[k] = delta * dY[t].sum()
+    v = oracle.wgrad_verify(dW.sum(axis=1), dW.sum(axis=0), dYb, Xb)
+    assert np.array_equal(v["residual"], er)
+    assert np.array_equal(v["residual_col"], ec)
+
+
+@pytest.mark.parametrize("mode", ["rn", "trunc", "block16"])
+def test_wgrad_bound_covers_float32_accumulation(mode):
+    # accumulation over the tokens, emulated on dW = (dY^T)(X^T)^T; both sides within their bounds
+    T, N, K = 512, 16, 24
+    rng = np.random.default_rng(24)
+    dY32 = (rng.uniform(0.5, 1.0, (T, N)) * 2.0 ** -rng.integers(0, 12, (T, N))).astype(np.float32)
+    X32 = (rng.uniform(0.5, 1.0, (T, K)) * 2.0 ** -rng.integers(0, 12, (T, K))).astype(np.float32)
+    dY32[0], X32[0] = 2.0 ** 9, 2.0 ** 5
+    dYb, Xb = _bf16_round(dY32), _bf16_round(X32)
+    acc = _emulate_fp32(oracle.bf16_to_f64(dYb).T.copy(), oracle.bf16_to_f64(Xb).T.copy(), mode)
+    v = oracle.wgrad_verify(acc.sum(axis=1), acc.sum(axis=0), dYb, Xb)
+    assert v["n_flagged"] == 0 and v["n_flagged_col"] == 0
+    assert np.max(np.abs(v["residual"]) / v["bound"]) <= 1.0
+    assert np.max(np.abs(v["residual_col"]) / v["bound_col"]) <= 1.0
+    ref = oracle.wgrad_reference(dYb, Xb)  # not vacuous: about T 2^-22 of the magnitude
+    assert np.all(v["bound"] <= 1.01 * T * 2.0 ** -22 * ref["row_mag"] + 1e-30)
+    if mode == "trunc":
+        assert np.max(np.abs(v["residual"]) / v["bound"]) > 0.05
+
+
+def test_wgrad_flag_rule_edges():
+    T, N, K = 3, 8, 16
+    dYb = np.zeros((T, N), dtype=np.uint16)
+    Xb = _bf16_round(np.ones((T, K), np.float32))
+    b, bc = 2.0 * T * K * 2.0 ** -126, 2.0 * T * N * 2.0 ** -126
+    rowsum = np.array([b, 2 * b, np.nan, -np.inf, 0, 0, 0, 0])
+    v = oracle.wgrad_verify(rowsum, np.zeros(K), dYb, Xb)
+    assert np.all(v["bound"] == b) and np.all(v["bound_col"] == bc)
+    assert list(v["flag"]) == [0, 1, 1, 1, 0, 0, 0, 0] and v["n_flagged_col"] == 0
+    assert "residual_col" not in oracle.wgrad_verify(rowsum, None, dYb, Xb)
