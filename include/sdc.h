@@ -299,7 +299,7 @@ sdc_status sdc_abft_gemm(const void *d_A, const void *d_W, void *d_C, uint32_t M
 /* The checksum verifier: per row, the reference A(W^T 1) (float32 pairs,
  * about 48 bits, returned in float64), the residual d_residual[i] =
  * d_rowsum[i] - reference, the rounding bound
- * d_bound[i] = (g (1 + g) + (N + K + 64) 2^-44) mag + 2 K N 2^-126 with
+ * d_bound[i] = (g (1 + g) + 20 2^-24 + (N + K + 64) 2^-44) mag + 2 K N 2^-126 with
  * g = K 2^-22 and mag an upper bound on sum_k |A[i][k]| sum_j |W[j][k]|
  * (summed in plain float32 and raised by twice its chains' length in units of
  * 2^-24, at most 2 (N/8 + K/4 + 32) 2^-24 of itself).  Each float32
@@ -320,6 +320,47 @@ sdc_status sdc_abft_verify(const void *d_A, const void *d_W, uint32_t M, uint32_
                            const double *d_colsum, float tol_scale, double *d_residual, double *d_bound,
                            uint8_t *d_flag, double *d_residual_col, double *d_bound_col, uint8_t *d_flag_col,
                            sdc_abft_summary *d_summary, void *d_ws, size_t ws_bytes, sdc_stream_t stream);
+
+/* Workspace bytes of sdc_abft_gemm_wgrad / sdc_abft_verify_wgrad (one buffer
+ * may serve both when they are ordered on one stream). */
+size_t sdc_abft_wgrad_workspace_size(uint32_t T, uint32_t N, uint32_t K);
+
+/* The checksum sensor on the weight-gradient product: dW = dY^T . X on the
+ * tensor cores, with row and column checksums from the float32 accumulator.
+ * [AEGIS] method section 2: the row configuration leaves wgrad partly
+ * uncovered; the row + column configuration covers every matmul class.
+ * d_dY: device bf16 [T][N], the layer's output gradient; d_X: device bf16
+ * [T][K], its input (both token-major, as the backward pass holds them:
+ * row-major, 16-byte aligned; the operands reach the tensor cores MN-major,
+ * no transposed copy is made); d_dW: device bf16 [N][K].  T >= 1 tokens (the
+ * contraction), T <= 2^20; N and K positive multiples of 8.  d_rowsum: device
+ * double [N], sum over k of the fp32 accumulator of dW[n][k]; d_colsum: NULL
+ * (rows only) or device double [K], sum over n (the same orders as
+ * sdc_abft_gemm).  d_aborted: device uint32, 1 if a bounded wait gave up. */
+sdc_status sdc_abft_gemm_wgrad(const void *d_dY, const void *d_X, void *d_dW, uint32_t T, uint32_t N, uint32_t K,
+                               double *d_rowsum, double *d_colsum, uint32_t *d_aborted, void *d_ws, size_t ws_bytes,
+                               sdc_stream_t stream);
+
+/* The checksum verifier of the weight-gradient product.  Rows: X's row sums
+ * r[t] = sum_k X[t][k] weight dY's column sums, the reference of row n is
+ * sum_t dY[t][n] r[t] = (dY^T (X 1))[n] and its magnitude
+ * sum_t |dY[t][n]| sum_k |X[t][k]|.  Columns (d_colsum given): dY's row sums
+ * q[t] weight X's column sums, reference sum_t q[t] X[t][k] and magnitude
+ * sum_t (sum_n |dY[t][n]|) |X[t][k]|.  Both in float32 pairs (8-term chains
+ * folded in with TwoSum), the magnitudes in plain float32 raised to an upper
+ * bound.  The bound is sdc_abft_verify's with the T tokens as the contraction
+ * and the outputs a checksum sums (K for a row, N for a column):
+ * (g (1 + g) + 20 2^-24 + (n_sum + T + 64) 2^-44) mag + 2 T n_sum 2^-126,
+ * g = T 2^-22.  Flags, residuals and d_summary as sdc_abft_verify (rows: N
+ * entries; columns: K).  Same shapes and workspace as sdc_abft_gemm_wgrad.
+ * Errors: SDC_ERR_BAD_ARG for shapes or tol_scale <= 0, SDC_ERR_NULL,
+ * SDC_ERR_BAD_POINTER for misalignment, SDC_ERR_WS_TOO_SMALL,
+ * SDC_ERR_WRONG_DEVICE. */
+sdc_status sdc_abft_verify_wgrad(const void *d_dY, const void *d_X, uint32_t T, uint32_t N, uint32_t K,
+                                 const double *d_rowsum, const double *d_colsum, float tol_scale, double *d_residual,
+                                 double *d_bound, uint8_t *d_flag, double *d_residual_col, double *d_bound_col,
+                                 uint8_t *d_flag_col, sdc_abft_summary *d_summary, void *d_ws, size_t ws_bytes,
+                                 sdc_stream_t stream);
 
 /* ---------------------------------------------------------------- attention invariant (AEGIS) */
 

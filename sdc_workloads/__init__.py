@@ -275,6 +275,16 @@ def gemm_operands(M: int, N: int, K: int, device, seed: int = 6, a_std: float = 
     return {"A": A, "W": W}
 
 
+def wgrad_operands(T: int, N: int, K: int, device, seed: int = 10, dy_std: float = 2.0 ** -10,
+                   x_std: float = 1.0) -> dict:
+    """Seeded bf16 dY [T, N] (a linear layer's output gradient) and X [T, K] (its input),
+    token-major: the operands of its weight gradient dW = dY^T X."""
+    gen = generator(seed, device)
+    dY = normal((T, N), dy_std, torch.bfloat16, gen, device)
+    X = normal((T, K), x_std, torch.bfloat16, gen, device)
+    return {"dY": dY, "X": X}
+
+
 def gemm_fault(A: torch.Tensor, rows: list[int], seed: int = 7, mask: int = 0x4000) -> tuple[torch.Tensor, list]:
     """A copy of A with one seeded element of each listed row XORed with `mask`
     (default: the top exponent bit of a bf16).  Returns (faulty A, [(row, col)])."""

@@ -98,6 +98,10 @@ def _load() -> ctypes.CDLL:
         "sdc_abft_gemm": ([vp, vp, vp, u32, u32, u32, vp, vp, vp, vp, sz, vp], ctypes.c_int),
         "sdc_abft_verify": ([vp, vp, u32, u32, u32, vp, vp, ctypes.c_float, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
                             ctypes.c_int),
+        "sdc_abft_wgrad_workspace_size": ([u32, u32, u32], sz),
+        "sdc_abft_gemm_wgrad": ([vp, vp, vp, u32, u32, u32, vp, vp, vp, vp, sz, vp], ctypes.c_int),
+        "sdc_abft_verify_wgrad": ([vp, vp, u32, u32, u32, vp, vp, ctypes.c_float, vp, vp, vp, vp, vp, vp, vp, vp, sz,
+                                   vp], ctypes.c_int),
         "sdc_attn_workspace_size": ([u32, u32, u32], sz),
         "sdc_attn_dv_check": ([vp, vp, vp, vp, u32, u32, u32, ctypes.c_float, u32, ctypes.c_float, vp, vp, vp, vp,
                                vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
@@ -255,6 +259,26 @@ def sdc_abft_gemm(d_A: int, d_W: int, d_C: int, M: int, N: int, K: int, d_rowsum
                   d_aborted: int, d_ws: int, ws_bytes: int, stream: int) -> None:
     _check("sdc_abft_gemm", _lib.sdc_abft_gemm(d_A, d_W, d_C, M, N, K, d_rowsum, d_colsum or None, d_aborted, d_ws,
                                                ws_bytes, stream))
+
+
+def sdc_abft_wgrad_workspace_size(T: int, N: int, K: int) -> int:
+    return int(_lib.sdc_abft_wgrad_workspace_size(T, N, K))
+
+
+def sdc_abft_gemm_wgrad(d_dY: int, d_X: int, d_dW: int, T: int, N: int, K: int, d_rowsum: int, d_colsum: int,
+                        d_aborted: int, d_ws: int, ws_bytes: int, stream: int) -> None:
+    _check("sdc_abft_gemm_wgrad", _lib.sdc_abft_gemm_wgrad(d_dY, d_X, d_dW, T, N, K, d_rowsum, d_colsum or None,
+                                                           d_aborted, d_ws, ws_bytes, stream))
+
+
+def sdc_abft_verify_wgrad(d_dY: int, d_X: int, T: int, N: int, K: int, d_rowsum: int, d_colsum: int,
+                          tol_scale: float, d_residual: int, d_bound: int, d_flag: int, d_residual_col: int,
+                          d_bound_col: int, d_flag_col: int, d_summary: int, d_ws: int, ws_bytes: int,
+                          stream: int) -> None:
+    _check("sdc_abft_verify_wgrad", _lib.sdc_abft_verify_wgrad(d_dY, d_X, T, N, K, d_rowsum, d_colsum or None,
+                                                               tol_scale, d_residual, d_bound, d_flag,
+                                                               d_residual_col or None, d_bound_col or None,
+                                                               d_flag_col or None, d_summary, d_ws, ws_bytes, stream))
 
 
 def sdc_abft_verify(d_A: int, d_W: int, M: int, N: int, K: int, d_rowsum: int, d_colsum: int, tol_scale: float,
@@ -580,6 +604,62 @@ class AbftGemm:
         self.gemm(A, W, stream)
         self.verify(A, W, tol_scale, stream=stream)
         return self.C
+
+
+class AbftWgrad:
+    """dW = dY^T . X (a linear layer's weight gradient) on the tensor cores with the
+    accumulator's row checksums and, with columns=True (the default: the page's
+    row + column configuration, which covers wgrad), column checksums, and their
+    check against dY^T (X 1) and (dY 1)^T X.  dY: bf16 [T, N], X: bf16 [T, K], both
+    token-major contiguous CUDA tensors; T >= 1, N and K multiples of 8.  Outputs
+    and scratch are allocated once per shape and reused by every call."""
+
+    def __init__(self, T: int, N: int, K: int, device, columns: bool = True):
+        torch = _torch()
+        self.T, self.N, self.K = T, N, K
+        self.dW = torch.empty((N, K), dtype=torch.bfloat16, device=device)
+        f64 = dict(dtype=torch.float64, device=device)
+        self.rowsum, self.residual, self.bound = (torch.empty(N, **f64) for _ in range(3))
+        self.flag = torch.empty(N, dtype=torch.uint8, device=device)
+        self.aborted = torch.zeros(1, dtype=torch.int32, device=device)
+        self.summary = torch.zeros(2, dtype=torch.int32, device=device)
+        self.columns = columns
+        if columns:
+            self.colsum, self.residual_col, self.bound_col = (torch.empty(K, **f64) for _ in range(3))
+            self.flag_col = torch.empty(K, dtype=torch.uint8, device=device)
+        self.ws_bytes = sdc_abft_wgrad_workspace_size(T, N, K)
+        self.ws = _ws(self.ws_bytes, device)
+
+    def _ptr(self, name):
+        return getattr(self, name).data_ptr() if self.columns else 0
+
+    def _shape(self, dY, X):
+        if tuple(dY.shape) != (self.T, self.N) or tuple(X.shape) != (self.T, self.K):
+            raise ValueError(f"expected dY [{self.T}, {self.N}] and X [{self.T}, {self.K}]")
+
+    def gemm(self, dY, X, stream=None):
+        """dW and its checksums (self.dW, self.rowsum, self.colsum; self.aborted != 0 if a wait gave up)."""
+        self._shape(dY, X)
+        sdc_abft_gemm_wgrad(dY.data_ptr(), X.data_ptr(), self.dW.data_ptr(), self.T, self.N, self.K,
+                            self.rowsum.data_ptr(), self._ptr("colsum"), self.aborted.data_ptr(), self.ws.data_ptr(),
+                            self.ws_bytes, _stream_handle(stream))
+        return self.dW
+
+    def verify(self, dY, X, tol_scale: float = 1.0, stream=None):
+        """The check (self.residual, self.bound, self.flag, self.summary[0] = flagged rows; with
+        columns, self.residual_col, self.bound_col, self.flag_col, self.summary[1])."""
+        self._shape(dY, X)
+        sdc_abft_verify_wgrad(dY.data_ptr(), X.data_ptr(), self.T, self.N, self.K, self.rowsum.data_ptr(),
+                              self._ptr("colsum"), tol_scale, self.residual.data_ptr(), self.bound.data_ptr(),
+                              self.flag.data_ptr(), self._ptr("residual_col"), self._ptr("bound_col"),
+                              self._ptr("flag_col"), self.summary.data_ptr(), self.ws.data_ptr(), self.ws_bytes,
+                              _stream_handle(stream))
+        return self.flag
+
+    def __call__(self, dY, X, tol_scale: float = 1.0, stream=None):
+        self.gemm(dY, X, stream)
+        self.verify(dY, X, tol_scale, stream=stream)
+        return self.dW
 
 
 class AttnDvCheck:

@@ -64,6 +64,7 @@ constexpr int kStages = 4;
 constexpr uint32_t kStageA = kBM * kBK * 2;  // 16 KiB
 constexpr uint32_t kStageW = kBN * kBK * 2;  // 32 KiB
 constexpr uint32_t kAccCols = 256;           // one accumulator; two are allocated
+constexpr uint32_t kMnBlock = kBK * 128;      // 8 KiB: kBK contraction rows of 64 bf16 (MN-major operands)
 constexpr uint32_t kGemmThreads = 192;
 constexpr uint32_t kNumBars = 2 * kStages + 5;  // full[S], empty[S], tfull[2], tempty[2], done
 constexpr uint32_t kGemmSmem = kStages * (kStageA + kStageW) + 1024 + 8 * kNumBars + 16;
@@ -136,7 +137,8 @@ __device__ __forceinline__ bool bar_any(uint32_t id, uint32_t count, bool pred) 
     return r != 0;
 }
 
-template <bool kCols>
+// kMN: both operands MN-major (the weight-gradient form, below); otherwise both K-major.
+template <bool kCols, bool kMN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     abft_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapW,
                      __nv_bfloat16 *__restrict__ C, uint32_t M, uint32_t N, uint32_t K, uint32_t band_m,
@@ -194,8 +196,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(full + 8 * s, kStageA + kStageW);
-                    tma_load_2d(sA + s * kStageA, &mapA, (int32_t)(kb * kBK), row_a, full + 8 * s);
-                    tma_load_2d(sW + s * kStageW, &mapW, (int32_t)(kb * kBK), row_w, full + 8 * s);
+                    if constexpr (kMN) {  // 64 x 64 boxes: kBK contraction rows of 64 output rows or columns
+#pragma unroll
+                        for (uint32_t j = 0; j < kBM / 64; ++j)
+                            tma_load_2d(sA + s * kStageA + j * kMnBlock, &mapA, row_a + (int32_t)(64 * j),
+                                        (int32_t)(kb * kBK), full + 8 * s);
+#pragma unroll
+                        for (uint32_t j = 0; j < kBN / 64; ++j)
+                            tma_load_2d(sW + s * kStageW + j * kMnBlock, &mapW, row_w + (int32_t)(64 * j),
+                                        (int32_t)(kb * kBK), full + 8 * s);
+                    } else {
+                        tma_load_2d(sA + s * kStageA, &mapA, (int32_t)(kb * kBK), row_a, full + 8 * s);
+                        tma_load_2d(sW + s * kStageW, &mapW, (int32_t)(kb * kBK), row_w, full + 8 * s);
+                    }
                 }
             }
             // Let no copy land in shared memory after the block has left: wait
@@ -207,7 +220,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {  // ------------------------------------------ MMA issuer
-            constexpr uint32_t idesc = umma_idesc(kBM, kBN);
+            constexpr uint32_t idesc = kMN ? umma_idesc_mn(kBM, kBN) : umma_idesc(kBM, kBN);
             uint32_t it = 0, lt = 0;
             for (uint32_t u = unit0; u < n_units && ok; u += ustep, ++lt) {
                 const uint32_t b = lt & 1u;
@@ -225,9 +238,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     tc_fence_after();
 #pragma unroll
-                    for (uint32_t ks = 0; ks < kBK / 16; ++ks)
-                        tc_mma(d, umma_desc_sw128(sA + s * kStageA + ks * 32), umma_desc_sw128(sW + s * kStageW + ks * 32),
-                               idesc, (kb | ks) != 0 ? 1u : 0u);
+                    for (uint32_t ks = 0; ks < kBK / 16; ++ks) {
+                        // K-major: a K16 step is 32 bytes inside each 128-byte row; MN-major: 16 rows of
+                        // 128 bytes (2 KiB), the 64-wide blocks kMnBlock apart
+                        const uint64_t da = kMN ? umma_desc_sw128_mn(sA + s * kStageA + ks * 2048, kMnBlock)
+                                                : umma_desc_sw128(sA + s * kStageA + ks * 32);
+                        const uint64_t db = kMN ? umma_desc_sw128_mn(sW + s * kStageW + ks * 2048, kMnBlock)
+                                                : umma_desc_sw128(sW + s * kStageW + ks * 32);
+                        tc_mma(d, da, db, idesc, (kb | ks) != 0 ? 1u : 0u);
+                    }
                     tc_commit(empty + 8 * s);  // the stage is free once these MMAs have read it
                 }
                 if (ok) tc_commit(tfull + 8 * b);
@@ -359,10 +378,27 @@ constexpr uint32_t kChain = 8;  // terms of a plain float32 chain before it is f
 // merge; warps merged in order.  The last block of each column block (a
 // counter per column block in `done`, zero at launch) merges the slabs into
 // split[] = {h, m} per column.
+//
+// The weight-gradient check (kWeighted) runs the same kernel over dY or X [T][n] with a weight
+// wt[t] = {h, m} per token row (X's or dY's row sums, below): s + c = sum_t X[t, k] h_t from 8-term
+// fused multiply-add chains, a = sum_t |X[t, k]| m_t, and its last block compares the merged sums
+// with the accumulator checksums (ColCheck) instead of writing split[].
+struct ColCheck {
+    const float2 *wt;  // {h, m} per row
+    const double *checksum;
+    double *residual, *bound;
+    uint8_t *flag;
+    uint32_t *n_flagged;
+    double delta;      // the magnitude's raise
+    float tol_scale;
+    uint32_t n_sum;    // outputs each checksum sums
+};
+
+template <bool kWeighted>
 __global__ void __launch_bounds__(256, 3) abft_colsum_slab_kernel(const __nv_bfloat16 *__restrict__ X, uint32_t rows,
                                                                uint32_t K, uint32_t n_slabs,
                                                                float4 *__restrict__ slabs, float2 *__restrict__ split,
-                                                               uint32_t *__restrict__ done) {
+                                                               uint32_t *__restrict__ done, ColCheck o) {
     __shared__ float4 part[8][256];
     __shared__ uint32_t last;
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
@@ -374,17 +410,29 @@ __global__ void __launch_bounds__(256, 3) abft_colsum_slab_kernel(const __nv_bfl
     uint64_t s[4], c[4], a[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) s[q] = c[q] = a[q] = 0ull;
-    auto add_rows = [&](const uint4 (&v)[kChain], uint32_t n) {  // n <= kChain rows, in row order
+    // n <= kChain rows from row j0r on (every 8th row), in row order
+    auto add_rows = [&](const uint4 (&v)[kChain], uint32_t n, uint32_t j0r) {
         uint64_t t[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
         for (uint32_t u = 0; u < kChain; ++u) {
             if (u < n) {
                 const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                uint64_t hh = 0ull, mm = 0ull;
+                if constexpr (kWeighted) {
+                    const float2 wt = __ldg(o.wt + j0r + 8 * u);
+                    hh = f2_pack_bits(__float_as_uint(wt.x), __float_as_uint(wt.x));
+                    mm = f2_pack_bits(__float_as_uint(wt.y), __float_as_uint(wt.y));
+                }
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const uint64_t x = f2_pack_bits(w[q] << 16, w[q] & 0xFFFF0000u);
-                    t[q] = f2_add(t[q], x);
-                    a[q] = f2_add(a[q], x & kF2Abs);
+                    if constexpr (kWeighted) {
+                        t[q] = f2_fma(x, hh, t[q]);
+                        a[q] = f2_fma(x & kF2Abs, mm, a[q]);
+                    } else {
+                        t[q] = f2_add(t[q], x);
+                        a[q] = f2_add(a[q], x & kF2Abs);
+                    }
                 }
             }
         }
@@ -402,14 +450,14 @@ __global__ void __launch_bounds__(256, 3) abft_colsum_slab_kernel(const __nv_bfl
             }
 #pragma unroll
             for (uint32_t u = 0; u < kChain; ++u) v[u] = ld_stream(X + (uint64_t)(j + 8 * u) * K + k);
-            add_rows(v, kChain);
+            add_rows(v, kChain, j);
         }
         if (j < j1) {  // fewer than kChain rows left
             const uint32_t n = (j1 - j + 7) / 8;
 #pragma unroll
             for (uint32_t u = 0; u < kChain; ++u)
                 v[u] = u < n ? ld_stream(X + (uint64_t)(j + 8 * u) * K + k) : make_uint4(0, 0, 0, 0);
-            add_rows(v, n);
+            add_rows(v, n, j);
         }
     }
 #pragma unroll
@@ -461,12 +509,77 @@ __global__ void __launch_bounds__(256, 3) abft_colsum_slab_kernel(const __nv_bfl
             pair_merge(acc.x, acc.y, q.x, q.y);
             pair_merge(acc.z, acc.w, q.z, q.w);
         }
-        float h = 0.0f, l = 0.0f;  // renormalise: TwoSum of the two parts
-        pair_add(h, l, acc.x);
-        pair_add(h, l, acc.y);
-        split[kk] = make_float2(__fadd_rn(h, l), __fadd_rn(acc.z, acc.w));
+        if constexpr (kWeighted) {  // the check of column kk's accumulator checksum (contraction: the rows)
+            const double ref = (double)acc.x + (double)acc.y;
+            const double mag = ((double)acc.z + (double)acc.w) * (1.0 + o.delta);
+            const double g = (double)rows * 0x1p-22;
+            const double b = (g * (1.0 + g) + 20.0 * 0x1p-24 + (double)(o.n_sum + rows + 64) * 0x1p-44) * mag +
+                             2.0 * (double)rows * (double)o.n_sum * 0x1p-126;
+            const double d = o.checksum[kk] - ref;
+            o.residual[kk] = d;
+            o.bound[kk] = b;
+            const uint8_t f = fabs(d) <= (double)o.tol_scale * b ? 0 : 1;  // NaN flags
+            o.flag[kk] = f;
+            if (f) atomicAdd(o.n_flagged, 1u);
+        } else {
+            float h = 0.0f, l = 0.0f;  // renormalise: TwoSum of the two parts
+            pair_add(h, l, acc.x);
+            pair_add(h, l, acc.y);
+            split[kk] = make_float2(__fadd_rn(h, l), __fadd_rn(acc.z, acc.w));
+        }
     }
     if (threadIdx.x == 0) done[blockIdx.x] = 0u;  // ready for the next call
+}
+
+// Row sums of X [T][n] for the weight-gradient check: out[t] = {h, m}, h the float nearest
+// sum_k X[t, k] (4-term plain chains, one per packed half of a 16-byte vector, folded into a
+// float32 pair with TwoSum) and m = sum_k |X[t, k]| in plain float32 (its chain: a lane's
+// 4 ceil(n / 256) terms, then 6 merges).  One warp per row, the lanes over the row's vectors in
+// turn with 8 loads in flight; the lanes' sums meet in a fixed butterfly and lane 0 writes.
+__global__ void __launch_bounds__(256) abft_rowsum_kernel(const __nv_bfloat16 *__restrict__ X, uint32_t T, uint32_t n,
+                                                          float2 *__restrict__ out) {
+    const uint32_t lane = threadIdx.x & 31u, t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= T) return;  // the whole warp
+    const uint4 *x = (const uint4 *)(X + (uint64_t)t * n);
+    const uint32_t nv = n / 8;
+    uint64_t s = 0ull, c = 0ull, a = 0ull;
+    auto add = [&](const uint4 &v) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint64_t tt = 0ull;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint64_t xx = f2_pack_bits(w[q] << 16, w[q] & 0xFFFF0000u);
+            tt = f2_add(tt, xx);
+            a = f2_add(a, xx & kF2Abs);
+        }
+        pair2_add(s, c, tt);
+    };
+    uint32_t v = lane;
+    for (; v + 32 * 7 < nv; v += 32 * 8) {
+        uint4 q[8];
+#pragma unroll
+        for (uint32_t u = 0; u < 8; ++u) q[u] = ld_stream(x + v + 32 * u);
+#pragma unroll
+        for (uint32_t u = 0; u < 8; ++u) add(q[u]);
+    }
+    for (; v < nv; v += 32) add(ld_stream(x + v));
+    float s0, s1, c0, c1, a0, a1;
+    f2_unpack(s, s0, s1);
+    f2_unpack(c, c0, c1);
+    f2_unpack(a, a0, a1);
+    pair_merge(s0, c0, s1, c1);
+    float m = __fadd_rn(a0, a1);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        pair_merge(s0, c0, __shfl_xor_sync(0xffffffffu, s0, off), __shfl_xor_sync(0xffffffffu, c0, off));
+        m = __fadd_rn(m, __shfl_xor_sync(0xffffffffu, m, off));
+    }
+    if (lane == 0) {
+        float h = 0.0f, l = 0.0f;  // renormalise: TwoSum of the two parts
+        pair_add(h, l, s0);
+        pair_add(h, l, c0);
+        out[t] = make_float2(__fadd_rn(h, l), m);
+    }
 }
 
 // The check of X [n_rows][K] (A for the row check, W for the column check)
@@ -672,6 +785,38 @@ AbftWs abft_ws(uint32_t M, uint32_t N, uint32_t K) {
     return w;
 }
 
+// The plain float32 chains behind a weight-gradient magnitude, for its raise factor: a row-sum
+// lane's 4 ceil(n_rowsum / 256) terms and its 6 merges, then a slab warp's rows of the weighted
+// column sums (their later merges run on float32 pairs).
+double wgrad_mag_delta(uint32_t T, uint32_t n_rowsum, uint32_t n_slabs) {
+    const uint32_t slab_rows = (T + n_slabs - 1) / n_slabs;
+    const double l1 = 4.0 * (double)((n_rowsum + 255) / 256) + 6.0;
+    const double l2 = (double)((slab_rows + 7) / 8);
+    return 2.0 * (l1 + l2 + 8.0) * 0x1p-24;
+}
+
+// Workspace of the weight-gradient form (dW [N][K] = dY^T X over T tokens): the GEMM's row
+// partials [ceil(K/256)][N] | column partials [ceil(N/128)][K] | X's row sums [T] float2 | dY's
+// [T] float2 | slabs [max(n_slabs(T, N), n_slabs(T, K))][max(N, K)] float4 | the last-block
+// counters (one per 256-column block: zeroed by each verify call) | abort word.
+struct WgradWs {
+    size_t part, cpart, rsplit, qsplit, slabs, done, err, total;
+};
+WgradWs wgrad_ws(uint32_t T, uint32_t N, uint32_t K) {
+    WgradWs w;
+    const size_t tiles_m = (N + kBM - 1) / kBM, tiles_n = (K + kBN - 1) / kBN, nmax = N > K ? N : K;
+    const size_t ns = n_slabs_for(T, N) > n_slabs_for(T, K) ? n_slabs_for(T, N) : n_slabs_for(T, K);
+    w.part = 0;
+    w.cpart = round_up256(tiles_n * N * sizeof(double));
+    w.rsplit = w.cpart + round_up256(tiles_m * K * sizeof(double));
+    w.qsplit = w.rsplit + round_up256((size_t)T * sizeof(float2));
+    w.slabs = w.qsplit + round_up256((size_t)T * sizeof(float2));
+    w.done = w.slabs + round_up256(ns * nmax * sizeof(float4));
+    w.err = w.done + round_up256((nmax + 255) / 256 * sizeof(uint32_t));
+    w.total = w.err + 256;
+    return w;
+}
+
 }  // namespace
 
 }  // namespace sdc
@@ -724,7 +869,7 @@ sdc_status sdc_abft_gemm(const void *d_A, const void *d_W, void *d_C, uint32_t M
     int *err = (int *)((char *)d_ws + w.err);
     cudaStream_t s = (cudaStream_t)stream;
     const bool cols = d_colsum != nullptr;
-    auto kernel = cols ? abft_gemm_kernel<true> : abft_gemm_kernel<false>;
+    auto kernel = cols ? abft_gemm_kernel<true, false> : abft_gemm_kernel<false, false>;
     cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int), s);
     const uint32_t smem_bytes = cols ? kGemmSmemCols : kGemmSmem;
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
@@ -782,8 +927,8 @@ sdc_status sdc_abft_verify(const void *d_A, const void *d_W, uint32_t M, uint32_
         const uint32_t nsp = (K / 8 + vps - 1) / vps;
         cudaError_t err = cudaMemsetAsync(done, 0, done_bytes, s);
         if (err != cudaSuccess) return err;
-        abft_colsum_slab_kernel<<<dim3((K + 255) / 256, ns), 256, 0, s>>>((const __nv_bfloat16 *)Y, n_sum, K, ns,
-                                                                         slabs, split, done);
+        abft_colsum_slab_kernel<false><<<dim3((K + 255) / 256, ns), 256, 0, s>>>((const __nv_bfloat16 *)Y, n_sum, K,
+                                                                                ns, slabs, split, done, ColCheck{});
         CheckOut o{checksum, res, bnd, flg, count, done, mag_delta(n_sum, K, ns, nsp), tol_scale, n_sum, nsp};
         abft_check_kernel<<<dim3((n_rows + kChkRows - 1) / kChkRows, nsp), 128, 0, s>>>(
             (const __nv_bfloat16 *)X, n_rows, K, vps, split, chk, o);
@@ -798,6 +943,126 @@ sdc_status sdc_abft_verify(const void *d_A, const void *d_W, uint32_t M, uint32_
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_verify launch");
     e = cudaGetLastError();
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_abft_verify launch");
+}
+
+size_t sdc_abft_wgrad_workspace_size(uint32_t T, uint32_t N, uint32_t K) { return wgrad_ws(T, N, K).total; }
+
+static sdc_status wgrad_args(const void *d_dY, const void *d_X, uint32_t T, uint32_t N, uint32_t K, void *d_ws,
+                             size_t ws_bytes, int *dev) {
+    if (!d_dY || !d_X) return fail(SDC_ERR_NULL, "NULL operand");
+    if (T == 0 || N == 0 || K == 0 || N % 8 || K % 8 || T > kMaxK)
+        return fail(SDC_ERR_BAD_ARG, "T must be positive and <= 2^20, N and K positive multiples of 8");
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    sdc_status st = check_device_range(d_dY, (uint64_t)T * N * 2, *dev, "d_dY");
+    if (st == SDC_OK) st = check_device_range(d_X, (uint64_t)T * K * 2, *dev, "d_X");
+    if (st != SDC_OK) return st;
+    if (((uint64_t)d_dY | (uint64_t)d_X) & 15u) return fail(SDC_ERR_BAD_POINTER, "dY and X must be 16-byte aligned");
+    if (!d_ws || ws_bytes < sdc_abft_wgrad_workspace_size(T, N, K))
+        return fail(SDC_ERR_WS_TOO_SMALL, "workspace smaller than sdc_abft_wgrad_workspace_size");
+    if ((uint64_t)d_ws & 255u) return fail(SDC_ERR_BAD_POINTER, "workspace is not 256-byte aligned");
+    return check_device_range(d_ws, sdc_abft_wgrad_workspace_size(T, N, K), *dev, "d_ws");
+}
+
+sdc_status sdc_abft_gemm_wgrad(const void *d_dY, const void *d_X, void *d_dW, uint32_t T, uint32_t N, uint32_t K,
+                               double *d_rowsum, double *d_colsum, uint32_t *d_aborted, void *d_ws, size_t ws_bytes,
+                               sdc_stream_t stream) {
+    int dev = -1;
+    sdc_status st = wgrad_args(d_dY, d_X, T, N, K, d_ws, ws_bytes, &dev);
+    if (st != SDC_OK) return st;
+    if (!d_dW || !d_rowsum || !d_aborted) return fail(SDC_ERR_NULL, "NULL output");
+    st = check_spans({{d_dW, (uint64_t)N * K * 2, "d_dW"},
+                      {d_rowsum, (uint64_t)N * 8, "d_rowsum"},
+                      {d_colsum, d_colsum ? (uint64_t)K * 8 : 0, "d_colsum"},
+                      {d_aborted, 4, "d_aborted"}},
+                     dev);
+    if (st != SDC_OK) return st;
+    if ((uint64_t)d_dW & 15u) return fail(SDC_ERR_BAD_POINTER, "dW must be 16-byte aligned");
+    // the GEMM kernel on dW [N][K] = A . W^T with A = dY^T and W = X^T, both MN-major, contraction T
+    const uint32_t tiles_m = (N + kBM - 1) / kBM, tiles_n = (K + kBN - 1) / kBN, sms = (uint32_t)sm_count(dev);
+    CUtensorMap mapA, mapW;
+    st = make_map_sw128(&mapA, d_dY, T, N, kBK);
+    if (st == SDC_OK) st = make_map_sw128(&mapW, d_X, T, K, kBK);
+    if (st != SDC_OK) return st;
+    const WgradWs w = wgrad_ws(T, N, K);
+    double *part = (double *)((char *)d_ws + w.part);
+    double *cpart = (double *)((char *)d_ws + w.cpart);
+    int *err = (int *)((char *)d_ws + w.err);
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool cols = d_colsum != nullptr;
+    auto kernel = cols ? abft_gemm_kernel<true, true> : abft_gemm_kernel<false, true>;
+    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int), s);
+    const uint32_t smem_bytes = cols ? kGemmSmemCols : kGemmSmem;
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_gemm_wgrad setup");
+    const uint32_t n_units = tiles_m * tiles_n;
+    const uint32_t grid = n_units < sms ? n_units : sms;  // one CTA per SM
+    // a band of tile rows holds about 24 MiB of dY's columns
+    uint32_t band_m = (uint32_t)((24u << 20) / ((size_t)kBM * T * 2));
+    band_m = band_m < 1 ? 1 : (band_m > tiles_m ? tiles_m : band_m);
+    kernel<<<grid, kGemmThreads, smem_bytes, s>>>(mapA, mapW, (__nv_bfloat16 *)d_dW, N, K, T, band_m, part, cpart, err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_gemm_wgrad launch");
+    abft_sum_parts_kernel<<<(N + 31) / 32, 256, 0, s>>>(part, N, tiles_n, d_rowsum, err, d_aborted);
+    if (cols) abft_sum_parts_kernel<<<(K + 31) / 32, 256, 0, s>>>(cpart, K, tiles_m, d_colsum, nullptr, nullptr);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_abft_gemm_wgrad launch");
+}
+
+sdc_status sdc_abft_verify_wgrad(const void *d_dY, const void *d_X, uint32_t T, uint32_t N, uint32_t K,
+                                 const double *d_rowsum, const double *d_colsum, float tol_scale, double *d_residual,
+                                 double *d_bound, uint8_t *d_flag, double *d_residual_col, double *d_bound_col,
+                                 uint8_t *d_flag_col, sdc_abft_summary *d_summary, void *d_ws, size_t ws_bytes,
+                                 sdc_stream_t stream) {
+    int dev = -1;
+    sdc_status st = wgrad_args(d_dY, d_X, T, N, K, d_ws, ws_bytes, &dev);
+    if (st != SDC_OK) return st;
+    if (!d_rowsum || !d_residual || !d_bound || !d_flag || !d_summary) return fail(SDC_ERR_NULL, "NULL output");
+    const bool cols = d_colsum != nullptr;
+    if (cols && (!d_residual_col || !d_bound_col || !d_flag_col)) return fail(SDC_ERR_NULL, "NULL column output");
+    if (!(tol_scale > 0.0f)) return fail(SDC_ERR_BAD_ARG, "tol_scale must be positive");
+    const uint64_t nc = cols ? K : 0;
+    st = check_spans({{d_rowsum, (uint64_t)N * 8, "d_rowsum"},
+                      {d_residual, (uint64_t)N * 8, "d_residual"},
+                      {d_bound, (uint64_t)N * 8, "d_bound"},
+                      {d_flag, N, "d_flag"},
+                      {d_colsum, nc * 8, "d_colsum"},
+                      {d_residual_col, nc * 8, "d_residual_col"},
+                      {d_bound_col, nc * 8, "d_bound_col"},
+                      {d_flag_col, nc, "d_flag_col"},
+                      {d_summary, sizeof(sdc_abft_summary), "d_summary"}},
+                     dev);
+    if (st != SDC_OK) return st;
+    const WgradWs w = wgrad_ws(T, N, K);
+    float2 *rsplit = (float2 *)((char *)d_ws + w.rsplit), *qsplit = (float2 *)((char *)d_ws + w.qsplit);
+    float4 *slabs = (float4 *)((char *)d_ws + w.slabs);
+    uint32_t *done = (uint32_t *)((char *)d_ws + w.done);
+    const size_t done_bytes = w.err - w.done;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaMemsetAsync(d_summary, 0, sizeof(sdc_abft_summary), s);
+    if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_verify_wgrad setup");
+    // One side: R [T][n_r]'s row sums weight the column sums of Y [T][n_y], which are checked
+    // against the n_y accumulator checksums (each of them sums n_r outputs).
+    auto side = [&](const void *R, uint32_t n_r, const void *Y, uint32_t n_y, float2 *wt, const double *checksum,
+                    double *res, double *bnd, uint8_t *flg, uint32_t *count) -> cudaError_t {
+        abft_rowsum_kernel<<<(T + 7) / 8, 256, 0, s>>>((const __nv_bfloat16 *)R, T, n_r, wt);
+        cudaError_t err = cudaMemsetAsync(done, 0, done_bytes, s);
+        if (err != cudaSuccess) return err;
+        const uint32_t ns = n_slabs_for(T, n_y);
+        const ColCheck o{wt, checksum, res, bnd, flg, count, wgrad_mag_delta(T, n_r, ns), tol_scale, n_r};
+        abft_colsum_slab_kernel<true><<<dim3((n_y + 255) / 256, ns), 256, 0, s>>>((const __nv_bfloat16 *)Y, T, n_y,
+                                                                                 ns, slabs, nullptr, done, o);
+        return cudaGetLastError();
+    };
+    // rows of dW (one per column n of dY): X's row sums weight dY's column sums; each checksum sums K outputs
+    e = side(d_X, K, d_dY, N, rsplit, d_rowsum, d_residual, d_bound, d_flag, &d_summary->n_flagged);
+    // columns of dW (one per column k of X): dY's row sums weight X's column sums; each sums N outputs
+    if (e == cudaSuccess && cols)
+        e = side(d_dY, N, d_X, K, qsplit, d_colsum, d_residual_col, d_bound_col, d_flag_col,
+                 &d_summary->n_flagged_cols);
+    if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_verify_wgrad launch");
+    e = cudaGetLastError();
+    return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_abft_verify_wgrad launch");
 }
 
 }  // extern "C"

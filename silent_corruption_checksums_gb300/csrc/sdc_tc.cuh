@@ -45,6 +45,8 @@ __host__ __device__ constexpr uint32_t umma_idesc(uint32_t m, uint32_t n) {
 }
 // The same with B MN-major (bit 16).
 __host__ __device__ constexpr uint32_t umma_idesc_bmn(uint32_t m, uint32_t n) { return umma_idesc(m, n) | (1u << 16); }
+// The same with A and B MN-major (bits 15 and 16).
+__host__ __device__ constexpr uint32_t umma_idesc_mn(uint32_t m, uint32_t n) { return umma_idesc_bmn(m, n) | (1u << 15); }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int32_t c0, int32_t c1, int32_t c2,
                                             uint32_t mbar) {

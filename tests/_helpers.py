@@ -83,6 +83,18 @@ def assert_verifier_bound(kernel_bound, method_bound, mag, n_sum: int, K: int) -
     assert np.all(kb <= top), float(np.max(kb / top))
 
 
+def assert_wgrad_bound(kernel_bound, method_bound, mag, n_sum: int, T: int) -> None:
+    """The weight-gradient check's bound against the method's: its own sums as the forward
+    check's with the T tokens as the contraction, and its magnitude raised by at most
+    2 (T / 8 + n_sum / 64 + 20) 2^-24 (a slab warp's rows, a row-sum lane's terms, merges)."""
+    import numpy as np
+    kb, mb, mg = (np.asarray(x, dtype=np.float64) for x in (kernel_bound, method_bound, mag))
+    assert np.all(kb >= mb * (1.0 - 1e-12)), float(np.min(kb / mb))
+    raise_ = 2.0 * (T / 8 + n_sum / 64 + 20) * 2.0 ** -24
+    top = (mb + verifier_own_slack(n_sum, T) * mg) * (1.0 + raise_) * (1.0 + 1e-12)
+    assert np.all(kb <= top), float(np.max(kb / top))
+
+
 # The attention check's own terms, relative to A = sum_i |dO[i, c]|: its column sums are float32
 # pairs (2^-40) of plain 8-row chains (below 8 2^-24 each, counted twice: 2^-20), and it raises A by
 # 2^-21 so that its bound never falls below the method's whatever the chains lost.

@@ -119,6 +119,25 @@ def test_host_validation_without_gpu(sdc):
                                                          + 512 * 16 + 256 + 256)
     assert sdc.sdc_abft_workspace_size(1000, 256, 100) == (8192 + 8 * 256 * 8 + 2 * 1024 + 64 * 100 * 16
                                                            + 16128 + 256 + 256)
+    # weight-gradient GEMM checksum: operands, then shapes (T tokens in 1..2^20, N and K multiples of 8)
+    with pytest.raises(sdc.SdcError) as ei:
+        sdc.sdc_abft_gemm_wgrad(0, 4096, 8192, 128, 256, 64, 0, 0, 0, 0, 0, 0)
+    assert ei.value.status == 1
+    for T, N, K in [(0, 256, 64), (128, 0, 64), (128, 256, 0), (128, 260, 64), (128, 256, 60), ((1 << 20) + 1, 256, 64)]:
+        with pytest.raises(sdc.SdcError) as ei:
+            sdc.sdc_abft_gemm_wgrad(4096, 8192, 16384, T, N, K, 0, 0, 0, 0, 0, 0)
+        assert ei.value.status == 9, (T, N, K)
+        with pytest.raises(sdc.SdcError) as ei:
+            sdc.sdc_abft_verify_wgrad(4096, 8192, T, N, K, 0, 0, 1.0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0)
+        assert ei.value.status == 9, (T, N, K)
+    # row partials (ceil(K/256) per dW row), column partials (ceil(N/128) per column), X's and dY's row
+    # sums (8 bytes per token each), slabs of 16 bytes per column of the wider operand
+    # (min(456 / ceil(n / 256), 64, T / 8) slabs, the larger of the two), the last-block counters (a word
+    # per 256 columns), the abort word; each rounded up to 256 bytes
+    assert sdc.sdc_abft_wgrad_workspace_size(512, 256, 128) == (2048 + 2048 + 4096 + 4096 + 64 * 256 * 16
+                                                                + 256 + 256)
+    assert sdc.sdc_abft_wgrad_workspace_size(100, 8, 1000) == (256 + 8192 + 1024 + 1024 + 12 * 1000 * 16
+                                                               + 256 + 256)
     # bounded-wait self-test: arguments checked before the launch
     with pytest.raises(sdc.SdcError) as ei:
         sdc.sdc_selftest_bounded_wait(10, 0, 0)

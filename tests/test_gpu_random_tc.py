@@ -57,6 +57,34 @@ def test_gemm_random(sdc, case):
         assert vc["n_flagged"] == 0 and int(g.summary[1]) == 0 and np.all(g.flag_col.cpu().numpy() == 0)
 
 
+@pytest.mark.parametrize("case", range(6))
+def test_wgrad_random(sdc, case):
+    # the weight-gradient form over random shapes (multiples of 8, rarely tile-aligned), token
+    # counts from one to a few thousand and random input scales, rows and columns checked
+    rng = np.random.default_rng(5000 + case)
+    T = int(rng.integers(1, 3000))
+    N = 8 * int(rng.integers(1, 100))
+    K = 8 * int(rng.integers(1, 100))
+    dy_std = float(2.0 ** rng.integers(-16, 0))
+    x_std = float(2.0 ** rng.integers(-4, 5))
+    ops = W.wgrad_operands(T, N, K, DEV, seed=6000 + case, dy_std=dy_std, x_std=x_std)
+    a = sdc.AbftWgrad(T, N, K, DEV)
+    a(ops["dY"], ops["X"])
+    torch.cuda.synchronize()
+    assert int(a.aborted[0]) == 0
+    dYb, Xb = _bits(ops["dY"]), _bits(ops["X"])
+    exact = oracle.wgrad_product(dYb, Xb)
+    g = T * 2.0 ** -22
+    e = g * (1.0 + g) * (np.abs(oracle.bf16_to_f64(dYb)).T @ np.abs(oracle.bf16_to_f64(Xb))) + 2.0 * T * 2.0 ** -126
+    dW = a.dW.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(dW - exact) <= 2.0 ** -8 * (np.abs(exact) + e) + e + 2.0 ** -134), (T, N, K)
+    v = oracle.wgrad_verify(a.rowsum.cpu().numpy(), a.colsum.cpu().numpy(), dYb, Xb)
+    assert np.all(np.abs(a.rowsum.cpu().numpy() - exact.sum(axis=1)) <= v["bound"])
+    assert np.all(np.abs(a.colsum.cpu().numpy() - exact.sum(axis=0)) <= v["bound_col"])
+    assert v["n_flagged"] == 0 and v["n_flagged_col"] == 0
+    assert int(a.summary[0]) == 0 and int(a.summary[1]) == 0
+
+
 @pytest.mark.parametrize("case", range(14))
 def test_attention_random(sdc, case):
     # heads and lengths drawn so that the (head, key block) items range from one to a few
