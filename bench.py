@@ -435,6 +435,8 @@ def bench_rows(args, dev, stream, peaks, sdc, W, torch, np, only=None) -> dict:
         return bench_big_rows(args, dev, stream, peaks, sdc, W, torch, only)
     if only == "abft_gemm":
         return bench_abft_row(args, dev, stream, peaks, sdc, W, torch)
+    if only == "abft_wgrad":
+        return bench_wgrad_row(args, dev, stream, peaks, sdc, W, torch)
     if only == "attn_invariant":
         return bench_attn_row(args, dev, stream, peaks, sdc, W, torch)
     import oracle
@@ -528,6 +530,8 @@ def bench_rows(args, dev, stream, peaks, sdc, W, torch, np, only=None) -> dict:
     torch.cuda.empty_cache()
     if only in (None, "abft_gemm"):
         rows.update(bench_abft_row(args, dev, stream, peaks, sdc, W, torch))
+    if only in (None, "abft_wgrad"):
+        rows.update(bench_wgrad_row(args, dev, stream, peaks, sdc, W, torch))
     if only in (None, "attn_invariant"):
         rows.update(bench_attn_row(args, dev, stream, peaks, sdc, W, torch))
     if not getattr(args, "no_big_rows", False):
@@ -624,6 +628,50 @@ def bench_abft_row(args, dev, stream, peaks, sdc, W, torch) -> dict:
         "sample": f"the product, row checksums and check of the first {ms_rows} rows of A (float64; the "
                   "matrix product runs on numpy's BLAS with its default threads)"}
     del g, gc, ops, A, Wt, A_h, W_h, C_ref
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_wgrad_row(args, dev, stream, peaks, sdc, W, torch) -> dict:
+    """The weight-gradient form of the GEMM checksum, dW = dY^T X from token-major operands, with
+    row and column checksums (the configuration that covers wgrad) and their check, on the 8b
+    layout's MLP up-projection, with cuBLAS's plain dY^T X beside it."""
+    T, N, K = W.GEMM_8B_UP
+    ops = W.wgrad_operands(T, N, K, dev, seed=10)
+    dY, X = ops["dY"], ops["X"]
+    a = sdc.AbftWgrad(T, N, K, dev)
+    reps = max(10, args.steps // 10)
+    ms_gemm = _time_loop(lambda: a.gemm(dY, X, stream=stream), reps, stream, torch)
+    ms_verify = _time_loop(lambda: a.verify(dY, X, stream=stream), reps, stream, torch)
+    ms_cublas = _time_loop(lambda: torch.matmul(dY.t(), X), reps, stream, torch)
+    torch.cuda.synchronize()
+    flops = 2.0 * T * N * K
+    tf = flops / (ms_gemm * 1e-3) / 1e12
+    vbytes = 2 * (N + K) * T * 2  # each operand read twice: once for its row sums, once for its column sums
+    out = {"abft_wgrad": {"workload": f"dW = dY^T X, bf16, T={T} tokens, dY [T, N={N}] N(0, 2^-10), X [T, K={K}] "
+                          "N(0,1), token-major (8b MLP up-projection's weight gradient); row + column checksums from "
+                          "the fp32 accumulator + check vs dY^T (X 1) and (dY 1)^T X",
+                          "gemm_ms": ms_gemm, "tflops": tf, "frac_bf16_peak": tf / peaks["bf16_tflops"],
+                          "verify_ms": ms_verify, "verify_GB_s": vbytes / ms_verify / 1e6,
+                          "verify_frac_hbm": vbytes / ms_verify / 1e6 / peaks["hbm_gbs"],
+                          "cublas_plain_gemm_ms": ms_cublas, "cublas_tflops": flops / (ms_cublas * 1e-3) / 1e12,
+                          "clean_flagged": [int(a.summary[0]), int(a.summary[1])], "aborted": int(a.aborted[0]),
+                          "max_residual_over_bound": max(float((a.residual.abs() / a.bound).max()),
+                                                         float((a.residual_col.abs() / a.bound_col).max()))}}
+    # the oracle on the first 512 tokens: the product and both sides of the check
+    import oracle
+    ts = 512
+    dY_h, X_h = host_bits(dY[:ts]).reshape(ts, N), host_bits(X[:ts]).reshape(ts, K)
+    t0 = time.perf_counter()
+    dW_ref = oracle.wgrad_product(dY_h, X_h)
+    oracle.wgrad_verify(dW_ref.sum(axis=1), dW_ref.sum(axis=0), dY_h, X_h)
+    dt = time.perf_counter() - t0
+    out["abft_wgrad"]["cpu_baseline"] = {
+        "value": 2.0 * ts * N * K / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count() or 1,
+        "kind": "oracle", "seconds": dt, "cpu": cpu_info(),
+        "sample": f"the product over the first {ts} tokens and both sides of its check (float64; the matrix "
+                  "product runs on numpy's BLAS with its default threads)"}
+    del a, ops, dY, X, dY_h, X_h, dW_ref
     torch.cuda.empty_cache()
     return out
 
@@ -879,7 +927,8 @@ def main(argv=None) -> None:
     ap.add_argument("--chunk-bytes", type=int, default=0)
     ap.add_argument("--quick", action="store_true", help="only the timed fingerprint step (no rows/e2e/cpu)")
     ap.add_argument("--no-big-rows", action="store_true", help="skip the 8b and stress rows")
-    ap.add_argument("--only", choices=["grad_average_scan", "grad_scan", "xorsum", "abft_gemm", "attn_invariant",
+    ap.add_argument("--only", choices=["grad_average_scan", "grad_scan", "xorsum", "abft_gemm", "abft_wgrad",
+                                       "attn_invariant",
                                        "fingerprint_8b", "xorsum_pairs",
                                        "fingerprint_stress", "adamw_fingerprint"], default=None,
                     help="time one row alone (profiling)")

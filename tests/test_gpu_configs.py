@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import sdc_workloads as W
-from tests._helpers import assert_attn_bound, assert_verifier_bound, fp_table, host_bits, stats_match
+from tests._helpers import assert_attn_bound, assert_verifier_bound, assert_wgrad_bound, fp_table, host_bits, stats_match
 
 pytestmark = [pytest.mark.gpu, pytest.mark.big]
 DEV = "cuda"
@@ -187,6 +187,38 @@ def test_gemm_checksum_bench_shape(sdc):
     exact_c = (A64 @ W64[cols].T).sum(axis=0)
     bound_c = oracle.abft_bound(np.abs(W64[cols]) @ np.abs(A64).sum(axis=0), M, K)
     assert np.all(np.abs(g.colsum.cpu().numpy()[cols] - exact_c) <= bound_c)
+
+
+def test_wgrad_checksum_bench_shape(sdc):
+    # the benchmark's weight gradient (dW = dY^T X, 8192 tokens, dY [8192, 14336], X [8192, 4096],
+    # rows + columns, the same seed) in its launch configuration; sampled rows and columns of dW
+    # against the oracle one by one, no flag anywhere
+    T, N, K = W.GEMM_8B_UP
+    ops = W.wgrad_operands(T, N, K, DEV, seed=10)
+    a = sdc.AbftWgrad(T, N, K, DEV)
+    a(ops["dY"], ops["X"])
+    torch.cuda.synchronize()
+    assert int(a.aborted[0]) == 0 and int(a.summary[0]) == 0 and int(a.summary[1]) == 0
+    dY64 = oracle.bf16_to_f64(_bf16_bits(ops["dY"]))
+    X64 = oracle.bf16_to_f64(_bf16_bits(ops["X"]))
+    ra, qa = np.abs(X64).sum(axis=1), np.abs(dY64).sum(axis=1)  # per token: sum |X|, sum |dY|
+    rng = np.random.default_rng(62)
+    g = T * 2.0 ** -22
+    rows = np.sort(rng.choice(N, 12, replace=False))
+    exact = dY64[:, rows].T @ X64  # rows of dW [12, K]
+    e = g * (1 + g) * (np.abs(dY64[:, rows]).T @ np.abs(X64)) + 2.0 * T * 2.0 ** -126
+    dW = a.dW[torch.as_tensor(rows, device=DEV)].float().cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(dW - exact) <= 2.0 ** -8 * (np.abs(exact) + e) + e + 2.0 ** -134)
+    mag_r = np.abs(dY64[:, rows]).T @ ra
+    bound_r = oracle.abft_bound(mag_r, K, T)
+    assert np.all(np.abs(a.rowsum.cpu().numpy()[rows] - exact.sum(axis=1)) <= bound_r)
+    assert_wgrad_bound(a.bound.cpu().numpy()[rows], bound_r, mag_r, K, T)
+    cols = np.sort(rng.choice(K, 8, replace=False))
+    exact_c = (dY64.T @ X64[:, cols]).sum(axis=0)
+    mag_c = np.abs(X64[:, cols]).T @ qa
+    bound_c = oracle.abft_bound(mag_c, N, T)
+    assert np.all(np.abs(a.colsum.cpu().numpy()[cols] - exact_c) <= bound_c)
+    assert_wgrad_bound(a.bound_col.cpu().numpy()[cols], bound_c, mag_c, N, T)
 
 
 def test_attention_invariant_bench_shape(sdc):
