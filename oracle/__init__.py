@@ -568,6 +568,73 @@ def wgrad_verify(rowsum: np.ndarray, colsum, dY_bits: np.ndarray, X_bits: np.nda
 
 
 # --------------------------------------------------------------------------
+# Replay context and replay  ([AEGIS] method sections 1 and 2: when a check
+# fires, the sensor packs its evidence and the least context a replay needs
+# into a vTask; a verifier replays it off the critical path and confirms.  For
+# the forward product the context is the flagged row of A and the output row;
+# for wgrad, A's rows, B's columns and the matching results.)
+# --------------------------------------------------------------------------
+def capture_index(flag: np.ndarray, cap: int) -> tuple[np.ndarray, int]:
+    """The flagged positions in increasing order, at most cap of them, and how many were flagged."""
+    idx = np.nonzero(np.asarray(flag) != 0)[0]
+    return idx[:cap].astype(np.uint32), int(idx.size)
+
+
+def abft_capture(flag, flag_col, A_bits, W_bits, C_bits, cap_rows: int, cap_cols: int) -> dict:
+    """The replay context of C = A W^T: per flagged row i, A[i, :] and C[i, :]; per flagged column
+    j, W[j, :] (B's column j, as W is stored) and C[:, j].  The first cap rows and columns in index
+    order are kept; the counts are of everything flagged."""
+    ri, nr = capture_index(flag, cap_rows)
+    out = {"row_idx": ri, "row_A": A_bits[ri], "row_C": C_bits[ri], "n_rows": nr}
+    if flag_col is not None:
+        ci, nc = capture_index(flag_col, cap_cols)
+        out.update({"col_idx": ci, "col_W": W_bits[ci], "col_C": C_bits[:, ci].T.copy(), "n_cols": nc})
+    return out
+
+
+def wgrad_capture(flag, flag_col, dY_bits, X_bits, dW_bits, cap_rows: int, cap_cols: int) -> dict:
+    """The replay context of dW = dY^T X: per flagged row n of dW, dY[:, n] (A's row) and dW[n, :];
+    per flagged column k, X[:, k] (B's column) and dW[:, k]."""
+    ri, nr = capture_index(flag, cap_rows)
+    ci, nc = capture_index(flag_col, cap_cols)
+    return {"row_idx": ri, "row_dY": dY_bits[:, ri].T.copy(), "row_dW": dW_bits[ri], "n_rows": nr,
+            "col_idx": ci, "col_X": X_bits[:, ci].T.copy(), "col_dW": dW_bits[:, ci].T.copy(), "n_cols": nc}
+
+
+def output_consistent(C_bits: np.ndarray, exact: np.ndarray, mag: np.ndarray, K: int) -> np.ndarray:
+    """Whether each saved bf16 output can come from a correct product: within the float32
+    accumulation bound g (1 + g) mag + 2 K 2^-126 (g = K 2^-22, mag = sum_k |a| |b|) of the exact
+    value, then rounded to bf16 (2^-8 of the value, or 2^-134 if subnormal).  A replay of a
+    correct computation reproduces such values; an output outside it was computed wrongly."""
+    g = K * 2.0 ** -22
+    e = g * (1.0 + g) * np.asarray(mag, dtype=np.float64) + 2.0 * K * 2.0 ** -126
+    got = bf16_to_f64(C_bits)
+    with np.errstate(invalid="ignore"):
+        return np.abs(got - exact) <= 2.0 ** -8 * (np.abs(exact) + e) + e + 2.0 ** -134
+
+
+def abft_replay_rows(row_A_bits, W_bits, row_C_bits) -> np.ndarray:
+    """Per captured row: how many of its saved outputs a correct product cannot give (0: the
+    saved row is consistent with its inputs; a replay confirms a fault where this is > 0)."""
+    K = W_bits.shape[1]
+    A = bf16_to_f64(row_A_bits)
+    W = bf16_to_f64(W_bits)
+    ok = output_consistent(row_C_bits, A @ W.T, np.abs(A) @ np.abs(W).T, K)
+    return (~ok).sum(axis=1)
+
+
+def wgrad_replay_pairs(cap: dict) -> np.ndarray:
+    """Per captured (row r, column c) pair of a weight-gradient product: whether the saved
+    dW[n_r, k_c] is inconsistent with the saved operands dY[:, n_r] and X[:, k_c] (1) or not (0)."""
+    dY = bf16_to_f64(cap["row_dY"])  # [rows, T]
+    X = bf16_to_f64(cap["col_X"])    # [cols, T]
+    T = dY.shape[1]
+    saved = cap["row_dW"][:, cap["col_idx"]]  # [rows, cols]: dW[n_r, k_c]
+    ok = output_consistent(saved, dY @ X.T, np.abs(dY) @ np.abs(X).T, T)
+    return (~ok).astype(np.uint8)
+
+
+# --------------------------------------------------------------------------
 # Attention invariant  ([AEGIS] method section 3: in the attention backward
 # dV = P^T dO and every row of the softmax P sums to 1, so 1^T dV = 1^T dO;
 # the column sums of dV come from its float32 accumulator)

@@ -299,3 +299,81 @@ def test_wgrad_flag_rule_edges():
     assert np.all(v["bound"] == b) and np.all(v["bound_col"] == bc)
     assert list(v["flag"]) == [0, 1, 1, 1, 0, 0, 0, 0] and v["n_flagged_col"] == 0
     assert "residual_col" not in oracle.wgrad_verify(rowsum, None, dYb, Xb)
+
+
+# ---------------------------------------------------------------- replay context and replay
+
+def test_capture_index_order_cap_and_count():
+    idx, n = oracle.capture_index(np.array([0, 1, 0, 1, 1, 0, 1], np.uint8), 3)
+    assert idx.tolist() == [1, 3, 4] and n == 4
+    idx, n = oracle.capture_index(np.zeros(5, np.uint8), 4)
+    assert idx.tolist() == [] and n == 0
+
+
+def test_capture_copies_rows_and_columns_by_hand():
+    M, N, K = 5, 6, 4
+    A = np.arange(M * K, dtype=np.uint16).reshape(M, K)
+    Wb = (1000 + np.arange(N * K, dtype=np.uint16)).reshape(N, K)
+    C = (5000 + np.arange(M * N, dtype=np.uint16)).reshape(M, N)
+    cap = oracle.abft_capture(np.array([0, 1, 0, 0, 1], np.uint8), np.array([1, 0, 0, 1, 0, 1], np.uint8),
+                              A, Wb, C, cap_rows=4, cap_cols=2)
+    assert cap["n_rows"] == 2 and cap["n_cols"] == 3
+    assert cap["row_idx"].tolist() == [1, 4] and cap["col_idx"].tolist() == [0, 3]
+    assert cap["row_A"].tolist() == [[4, 5, 6, 7], [16, 17, 18, 19]]
+    assert cap["row_C"].tolist() == [[5006 + j for j in range(6)], [5024 + j for j in range(6)]]
+    assert cap["col_W"].tolist() == [[1000, 1001, 1002, 1003], [1012, 1013, 1014, 1015]]
+    assert cap["col_C"].tolist() == [[5000 + 6 * i for i in range(5)], [5003 + 6 * i for i in range(5)]]
+    # the weight-gradient form: dY's and X's columns, dW's rows and columns
+    T = 3
+    dY = np.arange(T * N, dtype=np.uint16).reshape(T, N)
+    X = (100 + np.arange(T * K, dtype=np.uint16)).reshape(T, K)
+    dW = (7000 + np.arange(N * K, dtype=np.uint16)).reshape(N, K)
+    w = oracle.wgrad_capture(np.array([0, 0, 1, 0, 0, 1], np.uint8), np.array([0, 1, 0, 0], np.uint8),
+                             dY, X, dW, cap_rows=1, cap_cols=4)
+    assert w["n_rows"] == 2 and w["row_idx"].tolist() == [2] and w["n_cols"] == 1 and w["col_idx"].tolist() == [1]
+    assert w["row_dY"].tolist() == [[2, 8, 14]] and w["row_dW"].tolist() == [[7008, 7009, 7010, 7011]]
+    assert w["col_X"].tolist() == [[101, 105, 109]]
+    assert w["col_dW"].tolist() == [[7001 + 4 * n for n in range(N)]]
+
+
+def test_replay_consistency_exact_and_planted():
+    # integer operands: every product and sum is exact, so C (bf16 of small integers) equals the
+    # exact product; one element moved by more than the rounding bound is the only one flagged
+    M, N, K = 4, 16, 32
+    A, W, Ab, Wb = _int_operands(M, N, K, 31, lo=-3, hi=3)
+    C = (A @ W.T).astype(np.float32)
+    Cb = _bf16_bits(C)
+    assert oracle.abft_replay_rows(Ab, Wb, Cb).tolist() == [0, 0, 0, 0]
+    bad = C.copy()
+    bad[2, 7] += 64.0  # |C| <= 288: exact in bf16 after the move, far beyond the bound
+    assert oracle.abft_replay_rows(Ab, Wb, _bf16_bits(bad)).tolist() == [0, 0, 1, 0]
+
+
+@pytest.mark.parametrize("mode", ["rn", "trunc", "block16"])
+def test_replay_consistency_covers_float32_accumulation(mode):
+    # a correct computation (float32 accumulation in any order, then bf16 rounding) is consistent
+    # everywhere; a value two bounds away is not
+    M, N, K = 6, 24, 512
+    rng = np.random.default_rng(32)
+    A32 = (rng.uniform(0.5, 1.0, (M, K)) * 2.0 ** -rng.integers(0, 12, (M, K))).astype(np.float32)
+    W32 = (rng.uniform(0.5, 1.0, (N, K)) * 2.0 ** -rng.integers(0, 12, (N, K))).astype(np.float32)
+    Ab, Wb = _bf16_round(A32), _bf16_round(W32)
+    acc = _emulate_fp32(oracle.bf16_to_f64(Ab), oracle.bf16_to_f64(Wb), mode)
+    Cb = _bf16_round(acc.astype(np.float32))
+    assert np.all(oracle.abft_replay_rows(Ab, Wb, Cb) == 0)
+    exact = oracle.abft_product(Ab, Wb)
+    shifted = _bf16_round((exact * (1.0 + 2.0 ** -5)).astype(np.float32))  # 2^-5: four times the bf16 step
+    assert np.all(oracle.abft_replay_rows(Ab, Wb, shifted) == N)
+
+
+def test_wgrad_replay_pairs_flags_only_the_planted_element():
+    T, N, K = 10, 8, 12
+    rng = np.random.default_rng(33)
+    dY, X = rng.integers(-4, 5, size=(T, N)), rng.integers(-4, 5, size=(T, K))
+    dYb, Xb = _bf16_bits(dY.astype(np.float32)), _bf16_bits(X.astype(np.float32))
+    dW = (dY.T @ X).astype(np.float32)
+    dW[5, 3] += 32.0
+    cap = oracle.wgrad_capture(np.array([0, 1, 0, 0, 0, 1, 0, 0], np.uint8),
+                               np.array([0, 0, 0, 1, 0, 0, 0, 0, 0, 1, 0, 0], np.uint8),
+                               dYb, Xb, _bf16_bits(dW), cap_rows=2, cap_cols=2)
+    assert oracle.wgrad_replay_pairs(cap).tolist() == [[0, 0], [1, 0]]
