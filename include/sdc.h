@@ -362,6 +362,75 @@ sdc_status sdc_abft_verify_wgrad(const void *d_dY, const void *d_X, uint32_t T, 
                                  uint8_t *d_flag_col, sdc_abft_summary *d_summary, void *d_ws, size_t ws_bytes,
                                  sdc_stream_t stream);
 
+/* ---------------------------------------------------------------- replay context and replay (AEGIS) */
+
+/* The replay context of a checked product C = A . W^T.  [AEGIS] method
+ * sections 1 and 2: a check that fires packs its evidence and the least
+ * context a replay needs into a vTask; for the forward (and dgrad) product
+ * that is the flagged row of A and its output row; with the row + column
+ * configuration also each flagged column's operand (W's row j, which is B's
+ * column j) and output column.  d_flag: device uint8 [M] (sdc_abft_verify's
+ * d_flag, or any selection); d_flag_col: device uint8 [N] or NULL (no
+ * columns).  The first cap_rows flagged rows in increasing index are copied:
+ * d_row_idx [cap_rows] uint32, d_row_A [cap_rows][K] bf16 (A[i][:]),
+ * d_row_C [cap_rows][N] bf16 (C[i][:]); the first cap_cols flagged columns:
+ * d_col_idx [cap_cols], d_col_W [cap_cols][K] (W[j][:]), d_col_C
+ * [cap_cols][M] (C[:][j]).  d_counts: device uint32 [2], how many rows and
+ * columns were flagged (all of them, also past the caps; 0 columns without
+ * d_flag_col).  Entries past the counts are not written.  Shapes as
+ * sdc_abft_gemm; A, W, C, d_row_A, d_row_C and d_col_W 16-byte aligned. */
+sdc_status sdc_abft_capture(const void *d_A, const void *d_W, const void *d_C, uint32_t M, uint32_t N, uint32_t K,
+                            const uint8_t *d_flag, const uint8_t *d_flag_col, uint32_t cap_rows, uint32_t *d_row_idx,
+                            void *d_row_A, void *d_row_C, uint32_t cap_cols, uint32_t *d_col_idx, void *d_col_W,
+                            void *d_col_C, uint32_t *d_counts, sdc_stream_t stream);
+
+/* The replay context of a checked weight gradient dW = dY^T . X (see
+ * sdc_abft_gemm_wgrad): per flagged row n of dW, dY's column n (A's row:
+ * d_row_dY [cap_rows][T]) and dW[n][:] (d_row_dW [cap_rows][K]); per flagged
+ * column k, X's column k (B's column: d_col_X [cap_cols][T]) and dW[:][k]
+ * (d_col_dW [cap_cols][N]).  d_flag [N], d_flag_col [K] or NULL; indices,
+ * caps and d_counts as sdc_abft_capture.  dW and d_row_dW 16-byte aligned. */
+sdc_status sdc_abft_capture_wgrad(const void *d_dY, const void *d_X, const void *d_dW, uint32_t T, uint32_t N,
+                                  uint32_t K, const uint8_t *d_flag, const uint8_t *d_flag_col, uint32_t cap_rows,
+                                  uint32_t *d_row_idx, void *d_row_dY, void *d_row_dW, uint32_t cap_cols,
+                                  uint32_t *d_col_idx, void *d_col_X, void *d_col_dW, uint32_t *d_counts,
+                                  sdc_stream_t stream);
+
+/* Workspace bytes of sdc_abft_replay (0 for cap_rows outside 1..1024 or bad
+ * N, K): cap_rows x 128 staged rows of K and of N bf16, plus a GEMM's. */
+size_t sdc_abft_replay_workspace_size(uint32_t cap_rows, uint32_t N, uint32_t K);
+
+/* The replay of captured rows (the verifier's confirmation): each captured
+ * row of A is recomputed against W (the same weights: [N][K] bf16) by the
+ * same tensor-core GEMM at the same lane of a 128-row tile (the rest of the
+ * tile zero), so a healthy GPU reproduces its output row bit for bit.
+ * d_ndiff [cap_rows] uint32: per captured row, how many of its N outputs
+ * differ from the captured d_row_C (0 for rows past the count).  d_summary:
+ * device uint32 [2], the rows with any difference, and 1 if a bounded wait
+ * of the replay's GEMM gave up.  d_row_idx, d_row_A, d_row_C and d_counts
+ * (its first word) as sdc_abft_capture wrote them with the same cap_rows. */
+sdc_status sdc_abft_replay(const void *d_W, uint32_t N, uint32_t K, uint32_t cap_rows, const uint32_t *d_row_idx,
+                           const void *d_row_A, const void *d_row_C, const uint32_t *d_counts, uint32_t *d_ndiff,
+                           uint32_t *d_summary, void *d_ws, size_t ws_bytes, sdc_stream_t stream);
+
+/* Workspace bytes of sdc_abft_replay_wgrad (0 for caps outside 1..64). */
+size_t sdc_abft_replay_wgrad_workspace_size(uint32_t T, uint32_t cap_rows, uint32_t cap_cols);
+
+/* The replay of a weight gradient's captured rows and columns: every
+ * (row n_r, column k_c) pair's output dW[n_r][k_c] is recomputed from the
+ * captured dY column and X column alone, by the same tensor-core kernel at
+ * the same position in its tile.  d_differs [cap_rows][cap_cols] uint8: 1
+ * unless the replay equals, bit for bit, both captured copies of that output
+ * (row r's element k_c and column c's element n_r); 0 past the counts.
+ * d_summary [2]: the pairs that differ, and the replay GEMM's abort flag.
+ * The captured buffers and d_counts as sdc_abft_capture_wgrad wrote them
+ * with the same caps (1..64 each). */
+sdc_status sdc_abft_replay_wgrad(uint32_t T, uint32_t N, uint32_t K, uint32_t cap_rows, uint32_t cap_cols,
+                                 const uint32_t *d_row_idx, const void *d_row_dY, const void *d_row_dW,
+                                 const uint32_t *d_col_idx, const void *d_col_X, const void *d_col_dW,
+                                 const uint32_t *d_counts, uint8_t *d_differs, uint32_t *d_summary, void *d_ws,
+                                 size_t ws_bytes, sdc_stream_t stream);
+
 /* ---------------------------------------------------------------- attention invariant (AEGIS) */
 
 /* Workspace bytes of sdc_attn_dv_check (0 unless D == 128). */

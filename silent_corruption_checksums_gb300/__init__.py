@@ -102,6 +102,15 @@ def _load() -> ctypes.CDLL:
         "sdc_abft_gemm_wgrad": ([vp, vp, vp, u32, u32, u32, vp, vp, vp, vp, sz, vp], ctypes.c_int),
         "sdc_abft_verify_wgrad": ([vp, vp, u32, u32, u32, vp, vp, ctypes.c_float, vp, vp, vp, vp, vp, vp, vp, vp, sz,
                                    vp], ctypes.c_int),
+        "sdc_abft_capture": ([vp, vp, vp, u32, u32, u32, vp, vp, u32, vp, vp, vp, u32, vp, vp, vp, vp, vp],
+                             ctypes.c_int),
+        "sdc_abft_capture_wgrad": ([vp, vp, vp, u32, u32, u32, vp, vp, u32, vp, vp, vp, u32, vp, vp, vp, vp, vp],
+                                   ctypes.c_int),
+        "sdc_abft_replay_workspace_size": ([u32, u32, u32], sz),
+        "sdc_abft_replay": ([vp, u32, u32, u32, vp, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
+        "sdc_abft_replay_wgrad_workspace_size": ([u32, u32, u32], sz),
+        "sdc_abft_replay_wgrad": ([u32, u32, u32, u32, u32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
+                                  ctypes.c_int),
         "sdc_attn_workspace_size": ([u32, u32, u32], sz),
         "sdc_attn_dv_check": ([vp, vp, vp, vp, u32, u32, u32, ctypes.c_float, u32, ctypes.c_float, vp, vp, vp, vp,
                                vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
@@ -279,6 +288,46 @@ def sdc_abft_verify_wgrad(d_dY: int, d_X: int, T: int, N: int, K: int, d_rowsum:
                                                                tol_scale, d_residual, d_bound, d_flag,
                                                                d_residual_col or None, d_bound_col or None,
                                                                d_flag_col or None, d_summary, d_ws, ws_bytes, stream))
+
+
+def sdc_abft_capture(d_A: int, d_W: int, d_C: int, M: int, N: int, K: int, d_flag: int, d_flag_col: int,
+                     cap_rows: int, d_row_idx: int, d_row_A: int, d_row_C: int, cap_cols: int, d_col_idx: int,
+                     d_col_W: int, d_col_C: int, d_counts: int, stream: int) -> None:
+    _check("sdc_abft_capture", _lib.sdc_abft_capture(d_A, d_W, d_C, M, N, K, d_flag, d_flag_col or None, cap_rows,
+                                                     d_row_idx or None, d_row_A or None, d_row_C or None, cap_cols,
+                                                     d_col_idx or None, d_col_W or None, d_col_C or None, d_counts,
+                                                     stream))
+
+
+def sdc_abft_capture_wgrad(d_dY: int, d_X: int, d_dW: int, T: int, N: int, K: int, d_flag: int, d_flag_col: int,
+                           cap_rows: int, d_row_idx: int, d_row_dY: int, d_row_dW: int, cap_cols: int,
+                           d_col_idx: int, d_col_X: int, d_col_dW: int, d_counts: int, stream: int) -> None:
+    _check("sdc_abft_capture_wgrad",
+           _lib.sdc_abft_capture_wgrad(d_dY, d_X, d_dW, T, N, K, d_flag, d_flag_col or None, cap_rows,
+                                       d_row_idx or None, d_row_dY or None, d_row_dW or None, cap_cols,
+                                       d_col_idx or None, d_col_X or None, d_col_dW or None, d_counts, stream))
+
+
+def sdc_abft_replay_workspace_size(cap_rows: int, N: int, K: int) -> int:
+    return int(_lib.sdc_abft_replay_workspace_size(cap_rows, N, K))
+
+
+def sdc_abft_replay(d_W: int, N: int, K: int, cap_rows: int, d_row_idx: int, d_row_A: int, d_row_C: int,
+                    d_counts: int, d_ndiff: int, d_summary: int, d_ws: int, ws_bytes: int, stream: int) -> None:
+    _check("sdc_abft_replay", _lib.sdc_abft_replay(d_W, N, K, cap_rows, d_row_idx, d_row_A, d_row_C, d_counts,
+                                                   d_ndiff, d_summary, d_ws, ws_bytes, stream))
+
+
+def sdc_abft_replay_wgrad_workspace_size(T: int, cap_rows: int, cap_cols: int) -> int:
+    return int(_lib.sdc_abft_replay_wgrad_workspace_size(T, cap_rows, cap_cols))
+
+
+def sdc_abft_replay_wgrad(T: int, N: int, K: int, cap_rows: int, cap_cols: int, d_row_idx: int, d_row_dY: int,
+                          d_row_dW: int, d_col_idx: int, d_col_X: int, d_col_dW: int, d_counts: int, d_differs: int,
+                          d_summary: int, d_ws: int, ws_bytes: int, stream: int) -> None:
+    _check("sdc_abft_replay_wgrad",
+           _lib.sdc_abft_replay_wgrad(T, N, K, cap_rows, cap_cols, d_row_idx, d_row_dY, d_row_dW, d_col_idx, d_col_X,
+                                      d_col_dW, d_counts, d_differs, d_summary, d_ws, ws_bytes, stream))
 
 
 def sdc_abft_verify(d_A: int, d_W: int, M: int, N: int, K: int, d_rowsum: int, d_colsum: int, tol_scale: float,
@@ -605,6 +654,47 @@ class AbftGemm:
         self.verify(A, W, tol_scale, stream=stream)
         return self.C
 
+    def capture(self, A, W, cap_rows: int = 8, cap_cols: int = 8, flag=None, flag_col=None, stream=None) -> dict:
+        """The replay context of the flagged rows (and, with columns, columns) of the last product:
+        {"row_idx", "row_A", "row_C", "col_idx", "col_W", "col_C", "counts"} as device tensors
+        (counts: flagged rows and columns, also past the caps).  flag / flag_col select other
+        rows or columns than the check's flags."""
+        torch = _torch()
+        self._shape(A, W)
+        dev = self.C.device
+        f = self.flag if flag is None else flag
+        fc = (self.flag_col if self.columns else None) if flag_col is None else flag_col
+        out = {"row_idx": torch.zeros(cap_rows, dtype=torch.int32, device=dev),
+               "row_A": torch.zeros((cap_rows, self.K), dtype=torch.bfloat16, device=dev),
+               "row_C": torch.zeros((cap_rows, self.N), dtype=torch.bfloat16, device=dev),
+               "col_idx": torch.zeros(cap_cols, dtype=torch.int32, device=dev),
+               "col_W": torch.zeros((cap_cols, self.K), dtype=torch.bfloat16, device=dev),
+               "col_C": torch.zeros((cap_cols, self.M), dtype=torch.bfloat16, device=dev),
+               "counts": torch.zeros(2, dtype=torch.int32, device=dev), "cap_rows": cap_rows}
+        c = cap_cols if fc is not None else 0
+        sdc_abft_capture(A.data_ptr(), W.data_ptr(), self.C.data_ptr(), self.M, self.N, self.K, f.data_ptr(),
+                         fc.data_ptr() if fc is not None else 0, cap_rows, out["row_idx"].data_ptr(),
+                         out["row_A"].data_ptr(), out["row_C"].data_ptr(), c, out["col_idx"].data_ptr() if c else 0,
+                         out["col_W"].data_ptr() if c else 0, out["col_C"].data_ptr() if c else 0,
+                         out["counts"].data_ptr(), _stream_handle(stream))
+        return out
+
+    def replay(self, W, cap: dict, stream=None):
+        """Recompute the captured rows against W with the same tensor-core kernel: (ndiff [cap_rows],
+        summary [2]) as device tensors -- per row the outputs not reproduced bit for bit; summary:
+        rows with any, and the replay GEMM's abort flag."""
+        torch = _torch()
+        n = cap["cap_rows"]
+        dev = W.device
+        ndiff = torch.zeros(n, dtype=torch.int32, device=dev)
+        summary = torch.zeros(2, dtype=torch.int32, device=dev)
+        wsb = sdc_abft_replay_workspace_size(n, self.N, self.K)
+        ws = _ws(wsb, dev)
+        sdc_abft_replay(W.data_ptr(), self.N, self.K, n, cap["row_idx"].data_ptr(), cap["row_A"].data_ptr(),
+                        cap["row_C"].data_ptr(), cap["counts"].data_ptr(), ndiff.data_ptr(), summary.data_ptr(),
+                        ws.data_ptr(), wsb, _stream_handle(stream))
+        return ndiff, summary
+
 
 class AbftWgrad:
     """dW = dY^T . X (a linear layer's weight gradient) on the tensor cores with the
@@ -660,6 +750,46 @@ class AbftWgrad:
         self.gemm(dY, X, stream)
         self.verify(dY, X, tol_scale, stream=stream)
         return self.dW
+
+    def capture(self, dY, X, cap_rows: int = 8, cap_cols: int = 8, flag=None, flag_col=None, stream=None) -> dict:
+        """The replay context of the flagged rows and columns of the last dW: {"row_idx", "row_dY"
+        (dY's columns), "row_dW", "col_idx", "col_X" (X's columns), "col_dW", "counts"}."""
+        torch = _torch()
+        self._shape(dY, X)
+        dev = self.dW.device
+        f = self.flag if flag is None else flag
+        fc = (self.flag_col if self.columns else None) if flag_col is None else flag_col
+        out = {"row_idx": torch.zeros(cap_rows, dtype=torch.int32, device=dev),
+               "row_dY": torch.zeros((cap_rows, self.T), dtype=torch.bfloat16, device=dev),
+               "row_dW": torch.zeros((cap_rows, self.K), dtype=torch.bfloat16, device=dev),
+               "col_idx": torch.zeros(cap_cols, dtype=torch.int32, device=dev),
+               "col_X": torch.zeros((cap_cols, self.T), dtype=torch.bfloat16, device=dev),
+               "col_dW": torch.zeros((cap_cols, self.N), dtype=torch.bfloat16, device=dev),
+               "counts": torch.zeros(2, dtype=torch.int32, device=dev), "cap_rows": cap_rows,
+               "cap_cols": cap_cols}
+        c = cap_cols if fc is not None else 0
+        sdc_abft_capture_wgrad(dY.data_ptr(), X.data_ptr(), self.dW.data_ptr(), self.T, self.N, self.K, f.data_ptr(),
+                               fc.data_ptr() if fc is not None else 0, cap_rows, out["row_idx"].data_ptr(),
+                               out["row_dY"].data_ptr(), out["row_dW"].data_ptr(), c,
+                               out["col_idx"].data_ptr() if c else 0, out["col_X"].data_ptr() if c else 0,
+                               out["col_dW"].data_ptr() if c else 0, out["counts"].data_ptr(), _stream_handle(stream))
+        return out
+
+    def replay(self, cap: dict, stream=None):
+        """Recompute every captured (row, column) output from the captured dY and X columns alone:
+        (differs [cap_rows, cap_cols] uint8, summary [2]) as device tensors."""
+        torch = _torch()
+        nr, nc = cap["cap_rows"], cap["cap_cols"]
+        dev = self.dW.device
+        differs = torch.zeros((nr, nc), dtype=torch.uint8, device=dev)
+        summary = torch.zeros(2, dtype=torch.int32, device=dev)
+        wsb = sdc_abft_replay_wgrad_workspace_size(self.T, nr, nc)
+        ws = _ws(wsb, dev)
+        sdc_abft_replay_wgrad(self.T, self.N, self.K, nr, nc, cap["row_idx"].data_ptr(), cap["row_dY"].data_ptr(),
+                              cap["row_dW"].data_ptr(), cap["col_idx"].data_ptr(), cap["col_X"].data_ptr(),
+                              cap["col_dW"].data_ptr(), cap["counts"].data_ptr(), differs.data_ptr(),
+                              summary.data_ptr(), ws.data_ptr(), wsb, _stream_handle(stream))
+        return differs, summary
 
 
 class AttnDvCheck:

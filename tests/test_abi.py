@@ -138,6 +138,36 @@ def test_host_validation_without_gpu(sdc):
                                                                 + 256 + 256)
     assert sdc.sdc_abft_wgrad_workspace_size(100, 8, 1000) == (256 + 8192 + 1024 + 1024 + 12 * 1000 * 16
                                                                + 256 + 256)
+    # replay context and replay: arguments and shapes before any CUDA call
+    with pytest.raises(sdc.SdcError) as ei:
+        sdc.sdc_abft_capture(0, 4096, 8192, 128, 256, 64, 12288, 0, 4, 16384, 20480, 24576, 0, 0, 0, 0, 28672, 0)
+    assert ei.value.status == 1
+    for M, N, K in [(0, 256, 64), (128, 260, 64), (128, 256, 60)]:
+        with pytest.raises(sdc.SdcError) as ei:
+            sdc.sdc_abft_capture(4096, 8192, 12288, M, N, K, 16384, 0, 4, 16384, 20480, 24576, 0, 0, 0, 0, 28672, 0)
+        assert ei.value.status == 9, (M, N, K)
+        with pytest.raises(sdc.SdcError) as ei:
+            sdc.sdc_abft_capture_wgrad(4096, 8192, 12288, M, N, K, 16384, 0, 4, 16384, 20480, 24576, 0, 0, 0, 0,
+                                       28672, 0)
+        assert ei.value.status == 9, (M, N, K)
+    with pytest.raises(sdc.SdcError) as ei:  # a cap with no buffer
+        sdc.sdc_abft_capture(4096, 8192, 12288, 128, 256, 64, 16384, 0, 4, 0, 0, 0, 0, 0, 0, 0, 28672, 0)
+    assert ei.value.status == 1
+    for cap, N, K in [(0, 256, 64), (1025, 256, 64), (4, 260, 64)]:
+        assert sdc.sdc_abft_replay_workspace_size(cap, N, K) == 0
+        with pytest.raises(sdc.SdcError) as ei:
+            sdc.sdc_abft_replay(4096, N, K, cap, 8192, 12288, 16384, 20480, 24576, 28672, 32768, 1 << 20, 0)
+        assert ei.value.status == 9, (cap, N, K)
+    for T, cr, cc in [(0, 4, 4), (128, 0, 4), (128, 4, 65)]:
+        assert sdc.sdc_abft_replay_wgrad_workspace_size(T, cr, cc) == 0
+        with pytest.raises(sdc.SdcError) as ei:
+            sdc.sdc_abft_replay_wgrad(T, 256, 64, cr, cc, *[4096 * (i + 1) for i in range(10)], 1 << 20, 0)
+        assert ei.value.status == 9, (T, cr, cc)
+    # staged rows (cap x 128 rows of K and of N bf16), their row checksums, the abort word, a GEMM's workspace
+    assert sdc.sdc_abft_replay_workspace_size(1, 256, 64) == (128 * 64 * 2 + 128 * 256 * 2 + 1024 + 256
+                                                              + sdc.sdc_abft_workspace_size(128, 256, 64))
+    assert sdc.sdc_abft_replay_wgrad_workspace_size(512, 2, 1) == (
+        512 * 256 * 2 + 512 * 256 * 2 + 256 * 256 * 2 + 256 * 8 + 256 + sdc.sdc_abft_wgrad_workspace_size(512, 256, 256))
     # bounded-wait self-test: arguments checked before the launch
     with pytest.raises(sdc.SdcError) as ei:
         sdc.sdc_selftest_bounded_wait(10, 0, 0)
