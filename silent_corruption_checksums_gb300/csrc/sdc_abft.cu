@@ -394,17 +394,36 @@ struct ColCheck {
     uint32_t n_sum;    // outputs each checksum sums
 };
 
+// One launch serves one or two independent column sums (the two sides of a check): column blocks
+// below cb0 are side s0's, the rest side s1's; each side has its own slabs and counters, and a
+// block whose slab index is past its side's slab count leaves at once.
+struct SlabSide {
+    const __nv_bfloat16 *X;
+    uint32_t rows, K, n_slabs;
+    float4 *slabs;
+    float2 *split;   // unweighted: the output
+    uint32_t *done;  // a counter per column block
+    ColCheck o;      // weighted: the check
+};
+
 template <bool kWeighted>
-__global__ void __launch_bounds__(256, 3) abft_colsum_slab_kernel(const __nv_bfloat16 *__restrict__ X, uint32_t rows,
-                                                               uint32_t K, uint32_t n_slabs,
-                                                               float4 *__restrict__ slabs, float2 *__restrict__ split,
-                                                               uint32_t *__restrict__ done, ColCheck o) {
+__global__ void __launch_bounds__(256, 3) abft_colsum_slab_kernel(const SlabSide s0, const SlabSide s1, uint32_t cb0) {
+    const bool second = blockIdx.x >= cb0;
+    const uint32_t bx = second ? blockIdx.x - cb0 : blockIdx.x, by = blockIdx.y;
+    const __nv_bfloat16 *__restrict__ X = second ? s1.X : s0.X;
+    const uint32_t rows = second ? s1.rows : s0.rows, K = second ? s1.K : s0.K,
+                   n_slabs = second ? s1.n_slabs : s0.n_slabs;
+    float4 *__restrict__ slabs = second ? s1.slabs : s0.slabs;
+    float2 *__restrict__ split = second ? s1.split : s0.split;
+    uint32_t *__restrict__ done = second ? s1.done : s0.done;
+    const ColCheck o = second ? s1.o : s0.o;
+    if (by >= n_slabs) return;  // the whole block
     __shared__ float4 part[8][256];
     __shared__ uint32_t last;
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
-    const uint32_t k = blockIdx.x * 256 + lane * 8;
-    const uint32_t j0 = (uint32_t)((uint64_t)blockIdx.y * rows / n_slabs),
-                   j1 = (uint32_t)((uint64_t)(blockIdx.y + 1) * rows / n_slabs);
+    const uint32_t k = bx * 256 + lane * 8;
+    const uint32_t j0 = (uint32_t)((uint64_t)by * rows / n_slabs),
+                   j1 = (uint32_t)((uint64_t)(by + 1) * rows / n_slabs);
     // columns 2q and 2q + 1 of the lane's 8 share packed registers: the pair (s, c) of the sum,
     // the running chain t of up to kChain rows folded into it, the plain sum a of |x|
     uint64_t s[4], c[4], a[4];
@@ -470,7 +489,7 @@ __global__ void __launch_bounds__(256, 3) abft_colsum_slab_kernel(const __nv_bfl
         part[warp][lane * 8 + 2 * q + 1] = make_float4(s1, c1, a1, 0.0f);
     }
     __syncthreads();
-    const uint32_t kk = blockIdx.x * 256 + threadIdx.x;
+    const uint32_t kk = bx * 256 + threadIdx.x;
     if (kk < K) {
         float4 acc = part[0][threadIdx.x];
         for (int w = 1; w < 8; ++w) {
@@ -478,7 +497,7 @@ __global__ void __launch_bounds__(256, 3) abft_colsum_slab_kernel(const __nv_bfl
             pair_merge(acc.x, acc.y, q.x, q.y);
             pair_merge(acc.z, acc.w, q.z, q.w);
         }
-        slabs[(uint64_t)blockIdx.y * K + kk] = acc;
+        slabs[(uint64_t)by * K + kk] = acc;
     }
     // The last slab block of this column block merges the column block's slabs (in slab order:
     // the same result whichever block is last) into split[k] = {h, m}: h the float nearest
@@ -486,7 +505,7 @@ __global__ void __launch_bounds__(256, 3) abft_colsum_slab_kernel(const __nv_bfl
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
-        last = atomicAdd(done + blockIdx.x, 1u) == n_slabs - 1 ? 1u : 0u;
+        last = atomicAdd(done + bx, 1u) == n_slabs - 1 ? 1u : 0u;
     }
     __syncthreads();
     if (!last) return;
@@ -528,7 +547,7 @@ __global__ void __launch_bounds__(256, 3) abft_colsum_slab_kernel(const __nv_bfl
             split[kk] = make_float2(__fadd_rn(h, l), __fadd_rn(acc.z, acc.w));
         }
     }
-    if (threadIdx.x == 0) done[blockIdx.x] = 0u;  // ready for the next call
+    if (threadIdx.x == 0) done[bx] = 0u;  // ready for the next call
 }
 
 // Row sums of X [T][n] for the weight-gradient check: out[t] = {h, m}, h the float nearest
@@ -536,8 +555,14 @@ __global__ void __launch_bounds__(256, 3) abft_colsum_slab_kernel(const __nv_bfl
 // float32 pair with TwoSum) and m = sum_k |X[t, k]| in plain float32 (its chain: a lane's
 // 4 ceil(n / 256) terms, then 6 merges).  One warp per row, the lanes over the row's vectors in
 // turn with 8 loads in flight; the lanes' sums meet in a fixed butterfly and lane 0 writes.
-__global__ void __launch_bounds__(256) abft_rowsum_kernel(const __nv_bfloat16 *__restrict__ X, uint32_t T, uint32_t n,
-                                                          float2 *__restrict__ out) {
+// blockIdx.y picks the matrix: (X0, n0, out0) or (X1, n1, out1), both with T rows.
+__global__ void __launch_bounds__(256) abft_rowsum_kernel(const __nv_bfloat16 *__restrict__ X0, uint32_t n0,
+                                                          float2 *__restrict__ out0, const __nv_bfloat16 *__restrict__ X1,
+                                                          uint32_t n1, float2 *__restrict__ out1, uint32_t T) {
+    const bool second = blockIdx.y != 0;
+    const __nv_bfloat16 *__restrict__ X = second ? X1 : X0;
+    const uint32_t n = second ? n1 : n0;
+    float2 *__restrict__ out = second ? out1 : out0;
     const uint32_t lane = threadIdx.x & 31u, t = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (t >= T) return;  // the whole warp
     const uint4 *x = (const uint4 *)(X + (uint64_t)t * n);
@@ -635,14 +660,30 @@ __device__ __forceinline__ void check_vec(const uint4 &a0, const uint4 &a1, cons
     pair2_add(rs, rc, t);
 }
 
-__global__ void __launch_bounds__(128) abft_check_kernel(const __nv_bfloat16 *__restrict__ X, uint32_t n_rows,
-                                                         uint32_t K, uint32_t vec_per_split,
-                                                         const float2 *__restrict__ split, float4 *__restrict__ part,
-                                                         CheckOut o) {
+// One launch serves one or two independent checks: row blocks below rb0 are side0's, the rest
+// side1's; a block whose split index is past its side's split count leaves at once.
+struct CheckSide {
+    const __nv_bfloat16 *X;
+    uint32_t n_rows, K, vec_per_split;
+    const float2 *split;
+    float4 *part;
+    CheckOut o;
+};
+
+__global__ void __launch_bounds__(128) abft_check_kernel(const CheckSide side0, const CheckSide side1, uint32_t rb0) {
+    const bool second = blockIdx.x >= rb0;
+    const uint32_t bx = second ? blockIdx.x - rb0 : blockIdx.x, by = blockIdx.y;
+    const __nv_bfloat16 *__restrict__ X = second ? side1.X : side0.X;
+    const uint32_t n_rows = second ? side1.n_rows : side0.n_rows, K = second ? side1.K : side0.K,
+                   vec_per_split = second ? side1.vec_per_split : side0.vec_per_split;
+    const float2 *__restrict__ split = second ? side1.split : side0.split;
+    float4 *__restrict__ part = second ? side1.part : side0.part;
+    const CheckOut o = second ? side1.o : side0.o;
+    if (by >= o.n_splits) return;  // the whole block
     __shared__ uint32_t last;
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
-    const uint32_t v0 = blockIdx.y * vec_per_split, v1 = min(K / 8, v0 + vec_per_split), nv = v1 > v0 ? v1 - v0 : 0;
-    const uint32_t row0 = blockIdx.x * kChkRows;
+    const uint32_t v0 = by * vec_per_split, v1 = min(K / 8, v0 + vec_per_split), nv = v1 > v0 ? v1 - v0 : 0;
+    const uint32_t row0 = bx * kChkRows;
     if (tid < kChkRows && row0 + tid < n_rows && nv)  // this block's segment of each of its rows into L2
         prefetch_l2_bulk(X + (uint64_t)(row0 + tid) * K + (uint64_t)v0 * 8, nv * 16u);
     const float2 *hm = split + (uint64_t)v0 * 8;
@@ -678,14 +719,14 @@ __global__ void __launch_bounds__(128) abft_check_kernel(const __nv_bfloat16 *__
         m1 = __fadd_rn(m1, __shfl_xor_sync(0xffffffffu, m1, off));
     }
     if (j == 0) {
-        float4 *dst = part + (uint64_t)blockIdx.y * n_rows;
+        float4 *dst = part + (uint64_t)by * n_rows;
         if (ok0) dst[r] = make_float4(s0, c0, m0, 0.0f);
         if (ok1) dst[r + 1] = make_float4(s1, c1, m1, 0.0f);
     }
     __syncthreads();
     if (tid == 0) {
         __threadfence();
-        last = atomicAdd(o.done + blockIdx.x, 1u) == o.n_splits - 1 ? 1u : 0u;
+        last = atomicAdd(o.done + bx, 1u) == o.n_splits - 1 ? 1u : 0u;
     }
     __syncthreads();
     if (!last) return;
@@ -722,7 +763,7 @@ __global__ void __launch_bounds__(128) abft_check_kernel(const __nv_bfloat16 *__
         o.flag[i] = f;
         if (f) atomicAdd(o.n_flagged, 1u);
     }
-    if (tid == 0) o.done[blockIdx.x] = 0u;  // ready for the next call
+    if (tid == 0) o.done[bx] = 0u;  // ready for the next call
 }
 
 size_t round_up256(size_t x) { return (x + 255) / 256 * 256; }
@@ -761,16 +802,17 @@ double mag_delta(uint32_t rows_summed, uint32_t K, uint32_t n_slabs, uint32_t n_
 }
 
 // Workspace: row partials [ceil(N/256)][M] | column partials [ceil(M/128)][N] | W's column sums wsplit [K] |
-// A's, asplit [K] | slabs [max(n_slabs(N, K), n_slabs(M, K))][K] (used for W, then for A) | the check's
-// split partials [max(S(M) M, S(N) N)] | the verifier's last-block counters (one per row block of the
-// check, or per 256-column block of the column sums: zeroed by each verify call) | abort word.
+// A's, asplit [K] | slabs [n_slabs(N, K) + n_slabs(M, K)][K] (W's, then A's) | the check's split
+// partials [S(M) M + S(N) N] (A's rows, then W's) | the verifier's last-block counters (one per 256-column
+// block of each side's column sums, then one per row block of each side's check: zeroed by each verify
+// call) | abort word.
 struct AbftWs {
     size_t part, cpart, wsplit, asplit, slabs, chk, done, err, total;
 };
 AbftWs abft_ws(uint32_t M, uint32_t N, uint32_t K) {
     AbftWs w;
-    const size_t ns = n_slabs_for(N, K) > n_slabs_for(M, K) ? n_slabs_for(N, K) : n_slabs_for(M, K);
-    const size_t nc_r = (size_t)n_splits_for(M, K) * M, nc_c = (size_t)n_splits_for(N, K) * N;
+    const size_t ns = (size_t)n_slabs_for(N, K) + n_slabs_for(M, K);  // both sides' slabs
+    const size_t nc = (size_t)n_splits_for(M, K) * M + (size_t)n_splits_for(N, K) * N;  // both sides' partials
     w.part = 0;
     const size_t tiles_m = (M + kBM - 1) / kBM, tiles_n = (N + kBN - 1) / kBN;
     w.cpart = round_up256(tiles_n * M * sizeof(double));
@@ -778,8 +820,9 @@ AbftWs abft_ws(uint32_t M, uint32_t N, uint32_t K) {
     w.asplit = w.wsplit + round_up256((size_t)K * sizeof(float2));
     w.slabs = w.asplit + round_up256((size_t)K * sizeof(float2));
     w.chk = w.slabs + round_up256(ns * K * sizeof(float4));
-    w.done = w.chk + round_up256((nc_r > nc_c ? nc_r : nc_c) * sizeof(float4));
-    const size_t row_blocks = ((M > N ? M : N) + kChkRows - 1) / kChkRows, col_blocks = (K + 255) / 256;
+    w.done = w.chk + round_up256(nc * sizeof(float4));
+    const size_t row_blocks = (M + kChkRows - 1) / kChkRows + (N + kChkRows - 1) / kChkRows,
+                 col_blocks = 2 * ((K + 255) / 256);
     w.err = w.done + round_up256((row_blocks > col_blocks ? row_blocks : col_blocks) * sizeof(uint32_t));
     w.total = w.err + 256;
     return w;
@@ -797,22 +840,21 @@ double wgrad_mag_delta(uint32_t T, uint32_t n_rowsum, uint32_t n_slabs) {
 
 // Workspace of the weight-gradient form (dW [N][K] = dY^T X over T tokens): the GEMM's row
 // partials [ceil(K/256)][N] | column partials [ceil(N/128)][K] | X's row sums [T] float2 | dY's
-// [T] float2 | slabs [max(n_slabs(T, N), n_slabs(T, K))][max(N, K)] float4 | the last-block
-// counters (one per 256-column block: zeroed by each verify call) | abort word.
+// [T] float2 | slabs: dY's [n_slabs(T, N)][N], then X's [n_slabs(T, K)][K] float4 | the last-block
+// counters (one per 256-column block of each: zeroed by each verify call) | abort word.
 struct WgradWs {
     size_t part, cpart, rsplit, qsplit, slabs, done, err, total;
 };
 WgradWs wgrad_ws(uint32_t T, uint32_t N, uint32_t K) {
     WgradWs w;
-    const size_t tiles_m = (N + kBM - 1) / kBM, tiles_n = (K + kBN - 1) / kBN, nmax = N > K ? N : K;
-    const size_t ns = n_slabs_for(T, N) > n_slabs_for(T, K) ? n_slabs_for(T, N) : n_slabs_for(T, K);
+    const size_t tiles_m = (N + kBM - 1) / kBM, tiles_n = (K + kBN - 1) / kBN;
     w.part = 0;
     w.cpart = round_up256(tiles_n * N * sizeof(double));
     w.rsplit = w.cpart + round_up256(tiles_m * K * sizeof(double));
     w.qsplit = w.rsplit + round_up256((size_t)T * sizeof(float2));
     w.slabs = w.qsplit + round_up256((size_t)T * sizeof(float2));
-    w.done = w.slabs + round_up256(ns * nmax * sizeof(float4));
-    w.err = w.done + round_up256((nmax + 255) / 256 * sizeof(uint32_t));
+    w.done = w.slabs + round_up256(((size_t)n_slabs_for(T, N) * N + (size_t)n_slabs_for(T, K) * K) * sizeof(float4));
+    w.err = w.done + round_up256(((N + 255) / 256 + (K + 255) / 256) * sizeof(uint32_t));
     w.total = w.err + 256;
     return w;
 }
@@ -919,27 +961,37 @@ sdc_status sdc_abft_verify(const void *d_A, const void *d_W, uint32_t M, uint32_
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_verify setup");
     uint32_t *done = (uint32_t *)((char *)d_ws + w.done);
     const size_t done_bytes = w.err - w.done;
-    // One side of the check: the column sums of Y [n_sum][K] over its rows, then X [n_rows][K] against them.
-    auto side = [&](const void *X, uint32_t n_rows, const void *Y, uint32_t n_sum, float2 *split,
-                    const double *checksum, double *res, double *bnd, uint8_t *flg, uint32_t *count) -> cudaError_t {
-        // vps vectors per split; nsp re-derived from it, so that no split is empty
-        const uint32_t ns = n_slabs_for(n_sum, K), vps = (K / 8 + n_splits_for(n_rows, K) - 1) / n_splits_for(n_rows, K);
-        const uint32_t nsp = (K / 8 + vps - 1) / vps;
-        cudaError_t err = cudaMemsetAsync(done, 0, done_bytes, s);
-        if (err != cudaSuccess) return err;
-        abft_colsum_slab_kernel<false><<<dim3((K + 255) / 256, ns), 256, 0, s>>>((const __nv_bfloat16 *)Y, n_sum, K,
-                                                                                ns, slabs, split, done, ColCheck{});
-        CheckOut o{checksum, res, bnd, flg, count, done, mag_delta(n_sum, K, ns, nsp), tol_scale, n_sum, nsp};
-        abft_check_kernel<<<dim3((n_rows + kChkRows - 1) / kChkRows, nsp), 128, 0, s>>>(
-            (const __nv_bfloat16 *)X, n_rows, K, vps, split, chk, o);
-        return cudaGetLastError();
+    // Both sides at once, in two launches: the column sums of W (for the rows) and of A (for the
+    // columns), then A's rows against W's sums and W's rows against A's.  Each side has its own
+    // slabs, split partials and counters; without columns each launch serves the row side alone.
+    const uint32_t cb = (K + 255) / 256, ns_w = n_slabs_for(N, K), ns_a = n_slabs_for(M, K);
+    auto vps_for = [&](uint32_t n_rows) {  // vectors per split; the split count re-derived, so none is empty
+        const uint32_t sp = n_splits_for(n_rows, K);
+        return (K / 8 + sp - 1) / sp;
     };
-    // rows: A (W^T 1) over the N columns each row checksum sums
-    e = side(d_A, M, d_W, N, wsplit, d_rowsum, d_residual, d_bound, d_flag, &d_summary->n_flagged);
-    // columns: W (A^T 1) over the M rows each column checksum sums
-    if (e == cudaSuccess && cols)
-        e = side(d_W, N, d_A, M, asplit, d_colsum, d_residual_col, d_bound_col, d_flag_col,
-                 &d_summary->n_flagged_cols);
+    const uint32_t vps_a = vps_for(M), nsp_a = (K / 8 + vps_a - 1) / vps_a;
+    const uint32_t vps_w = vps_for(N), nsp_w = (K / 8 + vps_w - 1) / vps_w;
+    const uint32_t rb_a = (M + kChkRows - 1) / kChkRows, rb_w = (N + kChkRows - 1) / kChkRows;
+    const SlabSide sw{(const __nv_bfloat16 *)d_W, N, K, ns_w, slabs, wsplit, done, ColCheck{}};
+    const SlabSide sa{(const __nv_bfloat16 *)d_A, M, K, ns_a, slabs + (size_t)ns_w * K, asplit, done + cb, ColCheck{}};
+    e = cudaMemsetAsync(done, 0, done_bytes, s);
+    if (e == cudaSuccess) {
+        abft_colsum_slab_kernel<false><<<dim3(cols ? 2 * cb : cb, cols && ns_a > ns_w ? ns_a : ns_w), 256, 0, s>>>(
+            sw, cols ? sa : sw, cb);
+        e = cudaMemsetAsync(done, 0, done_bytes, s);
+    }
+    if (e == cudaSuccess) {
+        // rows: A (W^T 1) over the N columns each row checksum sums; columns: W (A^T 1) over the M rows
+        const CheckSide ca{(const __nv_bfloat16 *)d_A, M, K, vps_a, wsplit, chk,
+                           CheckOut{d_rowsum, d_residual, d_bound, d_flag, &d_summary->n_flagged, done,
+                                    mag_delta(N, K, ns_w, nsp_a), tol_scale, N, nsp_a}};
+        const CheckSide cw{(const __nv_bfloat16 *)d_W, N, K, vps_w, asplit, chk + (size_t)nsp_a * M,
+                           CheckOut{d_colsum, d_residual_col, d_bound_col, d_flag_col, &d_summary->n_flagged_cols,
+                                    done + rb_a, mag_delta(M, K, ns_a, nsp_w), tol_scale, M, nsp_w}};
+        abft_check_kernel<<<dim3(cols ? rb_a + rb_w : rb_a, cols && nsp_w > nsp_a ? nsp_w : nsp_a), 128, 0, s>>>(
+            ca, cols ? cw : ca, rb_a);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_verify launch");
     e = cudaGetLastError();
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_abft_verify launch");
@@ -1041,25 +1093,25 @@ sdc_status sdc_abft_verify_wgrad(const void *d_dY, const void *d_X, uint32_t T, 
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = cudaMemsetAsync(d_summary, 0, sizeof(sdc_abft_summary), s);
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_verify_wgrad setup");
-    // One side: R [T][n_r]'s row sums weight the column sums of Y [T][n_y], which are checked
-    // against the n_y accumulator checksums (each of them sums n_r outputs).
-    auto side = [&](const void *R, uint32_t n_r, const void *Y, uint32_t n_y, float2 *wt, const double *checksum,
-                    double *res, double *bnd, uint8_t *flg, uint32_t *count) -> cudaError_t {
-        abft_rowsum_kernel<<<(T + 7) / 8, 256, 0, s>>>((const __nv_bfloat16 *)R, T, n_r, wt);
-        cudaError_t err = cudaMemsetAsync(done, 0, done_bytes, s);
-        if (err != cudaSuccess) return err;
-        const uint32_t ns = n_slabs_for(T, n_y);
-        const ColCheck o{wt, checksum, res, bnd, flg, count, wgrad_mag_delta(T, n_r, ns), tol_scale, n_r};
-        abft_colsum_slab_kernel<true><<<dim3((n_y + 255) / 256, ns), 256, 0, s>>>((const __nv_bfloat16 *)Y, T, n_y,
-                                                                                 ns, slabs, nullptr, done, o);
-        return cudaGetLastError();
-    };
-    // rows of dW (one per column n of dY): X's row sums weight dY's column sums; each checksum sums K outputs
-    e = side(d_X, K, d_dY, N, rsplit, d_rowsum, d_residual, d_bound, d_flag, &d_summary->n_flagged);
-    // columns of dW (one per column k of X): dY's row sums weight X's column sums; each sums N outputs
-    if (e == cudaSuccess && cols)
-        e = side(d_dY, N, d_X, K, qsplit, d_colsum, d_residual_col, d_bound_col, d_flag_col,
-                 &d_summary->n_flagged_cols);
+    // Both sides at once, in two launches: X's row sums (the weights of dY's column sums: the rows of
+    // dW, each checksum summing K outputs) and dY's (the weights of X's: the columns, each summing N),
+    // then both weighted column sums, each compared in its last blocks with its checksums.
+    abft_rowsum_kernel<<<dim3((T + 7) / 8, cols ? 2 : 1), 256, 0, s>>>((const __nv_bfloat16 *)d_X, K, rsplit,
+                                                                      (const __nv_bfloat16 *)d_dY, N, qsplit, T);
+    e = cudaMemsetAsync(done, 0, done_bytes, s);
+    if (e == cudaSuccess) {
+        const uint32_t cb_n = (N + 255) / 256, ns_n = n_slabs_for(T, N), ns_k = n_slabs_for(T, K);
+        const SlabSide sr{(const __nv_bfloat16 *)d_dY, T, N, ns_n, slabs, nullptr, done,
+                          ColCheck{rsplit, d_rowsum, d_residual, d_bound, d_flag, &d_summary->n_flagged,
+                                   wgrad_mag_delta(T, K, ns_n), tol_scale, K}};
+        const SlabSide sc{(const __nv_bfloat16 *)d_X, T, K, ns_k, slabs + (size_t)ns_n * N, nullptr, done + cb_n,
+                          ColCheck{qsplit, d_colsum, d_residual_col, d_bound_col, d_flag_col,
+                                   &d_summary->n_flagged_cols, wgrad_mag_delta(T, N, ns_k), tol_scale, N}};
+        abft_colsum_slab_kernel<true>
+            <<<dim3(cols ? cb_n + (K + 255) / 256 : cb_n, cols && ns_k > ns_n ? ns_k : ns_n), 256, 0, s>>>(
+                sr, cols ? sc : sr, cb_n);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_verify_wgrad launch");
     e = cudaGetLastError();
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_abft_verify_wgrad launch");

@@ -111,14 +111,14 @@ def test_host_validation_without_gpu(sdc):
             sdc.sdc_abft_verify(4096, 8192, M, N, K, 0, 0, 1.0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0)
         assert ei.value.status == 9, (M, N, K)
     # row partials (ceil(N/256) per row), column partials (ceil(M/128) per column), W's and A's column sums
-    # (K x 8 bytes each: the sum and the magnitude in float32), slabs of K x 16 bytes for the
-    # larger of the two column sums (slabs = min(456 / ceil(K / 256), 64, rows / 8)), the check's split
-    # partials (16 bytes per row and split; one split when K / 8 < 64), the last-block counters (a word
-    # per 32-row block of the larger side, or per 256 columns), the abort word; each rounded up to 256 bytes
-    assert sdc.sdc_abft_workspace_size(128, 512, 64) == (2048 + 1 * 512 * 8 + 2 * 512 + 64 * 64 * 16
-                                                         + 512 * 16 + 256 + 256)
-    assert sdc.sdc_abft_workspace_size(1000, 256, 100) == (8192 + 8 * 256 * 8 + 2 * 1024 + 64 * 100 * 16
-                                                           + 16128 + 256 + 256)
+    # (K x 8 bytes each: the sum and the magnitude in float32), slabs of K x 16 bytes for both column
+    # sums (slabs = min(456 / ceil(K / 256), 64, rows / 8) each), both checks' split partials (16 bytes per
+    # row and split; one split when K / 8 < 64), the last-block counters (a word per 32-row block of both
+    # sides, or per 256 columns of both), the abort word; each rounded up to 256 bytes
+    assert sdc.sdc_abft_workspace_size(128, 512, 64) == (2048 + 1 * 512 * 8 + 2 * 512 + (64 + 16) * 64 * 16
+                                                         + (128 + 512) * 16 + 256 + 256)
+    assert sdc.sdc_abft_workspace_size(1000, 256, 100) == (8192 + 8 * 256 * 8 + 2 * 1024 + (32 + 64) * 100 * 16
+                                                           + 20224 + 256 + 256)
     # weight-gradient GEMM checksum: operands, then shapes (T tokens in 1..2^20, N and K multiples of 8)
     with pytest.raises(sdc.SdcError) as ei:
         sdc.sdc_abft_gemm_wgrad(0, 4096, 8192, 128, 256, 64, 0, 0, 0, 0, 0, 0)
@@ -131,12 +131,12 @@ def test_host_validation_without_gpu(sdc):
             sdc.sdc_abft_verify_wgrad(4096, 8192, T, N, K, 0, 0, 1.0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0)
         assert ei.value.status == 9, (T, N, K)
     # row partials (ceil(K/256) per dW row), column partials (ceil(N/128) per column), X's and dY's row
-    # sums (8 bytes per token each), slabs of 16 bytes per column of the wider operand
-    # (min(456 / ceil(n / 256), 64, T / 8) slabs, the larger of the two), the last-block counters (a word
-    # per 256 columns), the abort word; each rounded up to 256 bytes
-    assert sdc.sdc_abft_wgrad_workspace_size(512, 256, 128) == (2048 + 2048 + 4096 + 4096 + 64 * 256 * 16
+    # sums (8 bytes per token each), slabs of 16 bytes per column of each operand
+    # (min(456 / ceil(n / 256), 64, T / 8) slabs each), the last-block counters (a word per 256 columns of
+    # each), the abort word; each rounded up to 256 bytes
+    assert sdc.sdc_abft_wgrad_workspace_size(512, 256, 128) == (2048 + 2048 + 4096 + 4096 + 64 * (256 + 128) * 16
                                                                 + 256 + 256)
-    assert sdc.sdc_abft_wgrad_workspace_size(100, 8, 1000) == (256 + 8192 + 1024 + 1024 + 12 * 1000 * 16
+    assert sdc.sdc_abft_wgrad_workspace_size(100, 8, 1000) == (256 + 8192 + 1024 + 1024 + 12 * (8 + 1000) * 16
                                                                + 256 + 256)
     # replay context and replay: arguments and shapes before any CUDA call
     with pytest.raises(sdc.SdcError) as ei:
@@ -207,8 +207,8 @@ def test_host_validation_without_gpu(sdc):
         sdc.sdc_attn_dv_check_grouped(4096, 8192, 16384, 32768, 1024, 1024, 65536 + 128, 128, 0.088, 0, 1.0, *outs,
                                       0, 0, 0)
     assert ei.value.status == 9
-    assert sdc.sdc_abft_workspace_size(128, 16384, 64) == (64 * 128 * 8 + 1 * 16384 * 8 + 2 * 512 + 64 * 64 * 16
-                                                           + 16384 * 16 + 16384 // 32 * 4 + 256)
+    assert sdc.sdc_abft_workspace_size(128, 16384, 64) == (64 * 128 * 8 + 1 * 16384 * 8 + 2 * 512 + (64 + 16) * 64 * 16
+                                                           + (128 + 16384) * 16 + 2304 + 256)
 
 
 def test_pages_verdict_decoding(sdc):
