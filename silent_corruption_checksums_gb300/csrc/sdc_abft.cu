@@ -503,6 +503,10 @@ __global__ void __launch_bounds__(256, 3) abft_colsum_slab_kernel(const SlabSide
     // the same result whichever block is last) into split[k] = {h, m}: h the float nearest
     // sum_j X[j, k] (the merged pair's sum), m = sum_j |X[j, k]| rounded to float32.
     __syncthreads();
+    // Once every block has passed its rows, the check of the other operand's rows may launch: it
+    // prefetches its rows into L2 during this grid's last-block merges, then waits for the grid to
+    // complete before it reads the column sums.  Without a dependent launch a no-op.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) {
         __threadfence();
         last = atomicAdd(done + bx, 1u) == n_slabs - 1 ? 1u : 0u;
@@ -686,6 +690,10 @@ __global__ void __launch_bounds__(128) abft_check_kernel(const CheckSide side0, 
     const uint32_t row0 = bx * kChkRows;
     if (tid < kChkRows && row0 + tid < n_rows && nv)  // this block's segment of each of its rows into L2
         prefetch_l2_bulk(X + (uint64_t)(row0 + tid) * K + (uint64_t)v0 * 8, nv * 16u);
+    // Launched as a dependent of the column sums: their grid has completed (and its writes are
+    // visible) once this returns.  The prefetch above overlaps the grid's tail.  Without a dependent
+    // launch a no-op.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const float2 *hm = split + (uint64_t)v0 * 8;
     const uint32_t g = lane >> 3, j = lane & 7u;
     const uint32_t r = row0 + warp * 8 + g * 2;  // this group's rows r, r + 1
@@ -803,9 +811,9 @@ double mag_delta(uint32_t rows_summed, uint32_t K, uint32_t n_slabs, uint32_t n_
 
 // Workspace: row partials [ceil(N/256)][M] | column partials [ceil(M/128)][N] | W's column sums wsplit [K] |
 // A's, asplit [K] | slabs [n_slabs(N, K) + n_slabs(M, K)][K] (W's, then A's) | the check's split
-// partials [S(M) M + S(N) N] (A's rows, then W's) | the verifier's last-block counters (one per 256-column
-// block of each side's column sums, then one per row block of each side's check: zeroed by each verify
-// call) | abort word.
+// partials [S(M) M + S(N) N] (A's rows, then W's) | the verifier's last-block counters: one per 256-column
+// block of each side's column sums, then one per row block of each side's check (apart, so that the
+// check may launch before the column sums complete; zeroed by each verify call) | abort word.
 struct AbftWs {
     size_t part, cpart, wsplit, asplit, slabs, chk, done, err, total;
 };
@@ -823,7 +831,7 @@ AbftWs abft_ws(uint32_t M, uint32_t N, uint32_t K) {
     w.done = w.chk + round_up256(nc * sizeof(float4));
     const size_t row_blocks = (M + kChkRows - 1) / kChkRows + (N + kChkRows - 1) / kChkRows,
                  col_blocks = 2 * ((K + 255) / 256);
-    w.err = w.done + round_up256((row_blocks > col_blocks ? row_blocks : col_blocks) * sizeof(uint32_t));
+    w.err = w.done + round_up256((col_blocks + row_blocks) * sizeof(uint32_t));
     w.total = w.err + 256;
     return w;
 }
@@ -978,19 +986,29 @@ sdc_status sdc_abft_verify(const void *d_A, const void *d_W, uint32_t M, uint32_
     if (e == cudaSuccess) {
         abft_colsum_slab_kernel<false><<<dim3(cols ? 2 * cb : cb, cols && ns_a > ns_w ? ns_a : ns_w), 256, 0, s>>>(
             sw, cols ? sa : sw, cb);
-        e = cudaMemsetAsync(done, 0, done_bytes, s);
+        e = cudaGetLastError();
     }
     if (e == cudaSuccess) {
-        // rows: A (W^T 1) over the N columns each row checksum sums; columns: W (A^T 1) over the M rows
+        // rows: A (W^T 1) over the N columns each row checksum sums; columns: W (A^T 1) over the M rows.
+        // A programmatic dependent launch: its blocks start once the column sums' blocks have passed
+        // their rows, prefetch their own rows into L2 and wait for that grid before they read the sums.
+        uint32_t *cdone = done + 2 * cb;
         const CheckSide ca{(const __nv_bfloat16 *)d_A, M, K, vps_a, wsplit, chk,
-                           CheckOut{d_rowsum, d_residual, d_bound, d_flag, &d_summary->n_flagged, done,
+                           CheckOut{d_rowsum, d_residual, d_bound, d_flag, &d_summary->n_flagged, cdone,
                                     mag_delta(N, K, ns_w, nsp_a), tol_scale, N, nsp_a}};
         const CheckSide cw{(const __nv_bfloat16 *)d_W, N, K, vps_w, asplit, chk + (size_t)nsp_a * M,
                            CheckOut{d_colsum, d_residual_col, d_bound_col, d_flag_col, &d_summary->n_flagged_cols,
-                                    done + rb_a, mag_delta(M, K, ns_a, nsp_w), tol_scale, M, nsp_w}};
-        abft_check_kernel<<<dim3(cols ? rb_a + rb_w : rb_a, cols && nsp_w > nsp_a ? nsp_w : nsp_a), 128, 0, s>>>(
-            ca, cols ? cw : ca, rb_a);
-        e = cudaGetLastError();
+                                    cdone + rb_a, mag_delta(M, K, ns_a, nsp_w), tol_scale, M, nsp_w}};
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(cols ? rb_a + rb_w : rb_a, cols && nsp_w > nsp_a ? nsp_w : nsp_a);
+        cfg.blockDim = dim3(128);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, abft_check_kernel, ca, cols ? cw : ca, rb_a);
     }
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_verify launch");
     e = cudaGetLastError();
