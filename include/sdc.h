@@ -321,6 +321,41 @@ sdc_status sdc_abft_verify(const void *d_A, const void *d_W, uint32_t M, uint32_
                            uint8_t *d_flag, double *d_residual_col, double *d_bound_col, uint8_t *d_flag_col,
                            sdc_abft_summary *d_summary, void *d_ws, size_t ws_bytes, sdc_stream_t stream);
 
+/* Workspace bytes of sdc_abft_weight_sums (0 for shapes it rejects). */
+size_t sdc_abft_weight_sums_workspace_size(uint32_t N, uint32_t K);
+
+/* W's column sums for the fused check: d_wsums[2k] = h, the float nearest
+ * sum_j W[j][k] (float32 pairs over 8-row chains), d_wsums[2k + 1] = the
+ * plain float32 sum of |W[j][k]|.  d_W: device bf16 [N][K] (16-byte aligned);
+ * d_wsums: device float [K][2].  They depend on W alone: one call serves
+ * every product with the same weights (a training step's micro-batches, its
+ * forward and dgrad products) until the weights change. */
+sdc_status sdc_abft_weight_sums(const void *d_W, uint32_t N, uint32_t K, float *d_wsums, void *d_ws, size_t ws_bytes,
+                                sdc_stream_t stream);
+
+/* The GEMM with its row check fused into it: C = A . W^T with each row's
+ * accumulator checksum (as sdc_abft_gemm), and the reference A[i][:] (W^T 1)
+ * formed in the same kernel by four more warps on the CUDA cores from the
+ * A tiles the product stages in shared memory (one tile of each tile row,
+ * against d_wsums from sdc_abft_weight_sums for this W).  [AEGIS] method
+ * section 2: the checksum and its check inside the GEMM kernel.  The check
+ * reads no operand again from HBM; its reference covers the tensor cores and
+ * the accumulator, not the copies into shared memory (which sdc_abft_verify,
+ * reading A and W from HBM, also covers).  d_residual, d_bound, d_flag and
+ * d_summary->n_flagged as sdc_abft_verify's rows, with the same bound (the
+ * magnitude's raise from W's column sums and a 32-term chain per 64-column
+ * stage); d_summary->n_flagged_cols = 0.  Tile (m, n) of the product forms
+ * the references of its 128 rows over the K blocks kb with
+ * kb mod ceil(N/256) = n, so the work spreads over all tiles; the partials
+ * are merged per row in tile order.  Shapes, d_rowsum and d_aborted as
+ * sdc_abft_gemm; tol_scale > 0; the workspace is
+ * sdc_abft_gemm_checked_workspace_size bytes. */
+size_t sdc_abft_gemm_checked_workspace_size(uint32_t M, uint32_t N, uint32_t K);
+sdc_status sdc_abft_gemm_checked(const void *d_A, const void *d_W, void *d_C, uint32_t M, uint32_t N, uint32_t K,
+                                 const float *d_wsums, float tol_scale, double *d_rowsum, double *d_residual,
+                                 double *d_bound, uint8_t *d_flag, sdc_abft_summary *d_summary, uint32_t *d_aborted,
+                                 void *d_ws, size_t ws_bytes, sdc_stream_t stream);
+
 /* Workspace bytes of sdc_abft_gemm_wgrad / sdc_abft_verify_wgrad (one buffer
  * may serve both when they are ordered on one stream). */
 size_t sdc_abft_wgrad_workspace_size(uint32_t T, uint32_t N, uint32_t K);

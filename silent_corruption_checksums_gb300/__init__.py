@@ -98,6 +98,11 @@ def _load() -> ctypes.CDLL:
         "sdc_abft_gemm": ([vp, vp, vp, u32, u32, u32, vp, vp, vp, vp, sz, vp], ctypes.c_int),
         "sdc_abft_verify": ([vp, vp, u32, u32, u32, vp, vp, ctypes.c_float, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
                             ctypes.c_int),
+        "sdc_abft_weight_sums_workspace_size": ([u32, u32], sz),
+        "sdc_abft_weight_sums": ([vp, u32, u32, vp, vp, sz, vp], ctypes.c_int),
+        "sdc_abft_gemm_checked_workspace_size": ([u32, u32, u32], sz),
+        "sdc_abft_gemm_checked": ([vp, vp, vp, u32, u32, u32, vp, ctypes.c_float, vp, vp, vp, vp, vp, vp, vp, sz, vp],
+                                  ctypes.c_int),
         "sdc_abft_wgrad_workspace_size": ([u32, u32, u32], sz),
         "sdc_abft_gemm_wgrad": ([vp, vp, vp, u32, u32, u32, vp, vp, vp, vp, sz, vp], ctypes.c_int),
         "sdc_abft_verify_wgrad": ([vp, vp, u32, u32, u32, vp, vp, ctypes.c_float, vp, vp, vp, vp, vp, vp, vp, vp, sz,
@@ -268,6 +273,26 @@ def sdc_abft_gemm(d_A: int, d_W: int, d_C: int, M: int, N: int, K: int, d_rowsum
                   d_aborted: int, d_ws: int, ws_bytes: int, stream: int) -> None:
     _check("sdc_abft_gemm", _lib.sdc_abft_gemm(d_A, d_W, d_C, M, N, K, d_rowsum, d_colsum or None, d_aborted, d_ws,
                                                ws_bytes, stream))
+
+
+def sdc_abft_weight_sums_workspace_size(N: int, K: int) -> int:
+    return int(_lib.sdc_abft_weight_sums_workspace_size(N, K))
+
+
+def sdc_abft_weight_sums(d_W: int, N: int, K: int, d_wsums: int, d_ws: int, ws_bytes: int, stream: int) -> None:
+    _check("sdc_abft_weight_sums", _lib.sdc_abft_weight_sums(d_W, N, K, d_wsums, d_ws, ws_bytes, stream))
+
+
+def sdc_abft_gemm_checked_workspace_size(M: int, N: int, K: int) -> int:
+    return int(_lib.sdc_abft_gemm_checked_workspace_size(M, N, K))
+
+
+def sdc_abft_gemm_checked(d_A: int, d_W: int, d_C: int, M: int, N: int, K: int, d_wsums: int, tol_scale: float,
+                          d_rowsum: int, d_residual: int, d_bound: int, d_flag: int, d_summary: int, d_aborted: int,
+                          d_ws: int, ws_bytes: int, stream: int) -> None:
+    _check("sdc_abft_gemm_checked",
+           _lib.sdc_abft_gemm_checked(d_A, d_W, d_C, M, N, K, d_wsums, tol_scale, d_rowsum, d_residual, d_bound,
+                                      d_flag, d_summary, d_aborted, d_ws, ws_bytes, stream))
 
 
 def sdc_abft_wgrad_workspace_size(T: int, N: int, K: int) -> int:
@@ -652,6 +677,34 @@ class AbftGemm:
     def __call__(self, A, W, tol_scale: float = 1.0, stream=None):
         self.gemm(A, W, stream)
         self.verify(A, W, tol_scale, stream=stream)
+        return self.C
+
+    def weight_sums(self, W, stream=None):
+        """W's column sums for the fused check (self.wsums, float32 [K, 2]); valid until W changes."""
+        torch = _torch()
+        if tuple(W.shape) != (self.N, self.K):
+            raise ValueError(f"expected W [{self.N}, {self.K}]")
+        if not hasattr(self, "wsums"):
+            self.wsums = torch.empty((self.K, 2), dtype=torch.float32, device=self.C.device)
+            self._wsb = sdc_abft_weight_sums_workspace_size(self.N, self.K)
+            self._wsws = _ws(self._wsb, self.C.device)
+        sdc_abft_weight_sums(W.data_ptr(), self.N, self.K, self.wsums.data_ptr(), self._wsws.data_ptr(), self._wsb,
+                             _stream_handle(stream))
+        return self.wsums
+
+    def gemm_checked(self, A, W, tol_scale: float = 1.0, stream=None):
+        """The GEMM with its row check fused into it, against self.wsums (weight_sums(W) first):
+        self.C, self.rowsum, self.residual, self.bound, self.flag, self.summary[0]."""
+        self._shape(A, W)
+        if not hasattr(self, "wsums"):
+            raise ValueError("call weight_sums(W) first")
+        if not hasattr(self, "_cws"):
+            self._cwsb = sdc_abft_gemm_checked_workspace_size(self.M, self.N, self.K)
+            self._cws = _ws(self._cwsb, self.C.device)
+        sdc_abft_gemm_checked(A.data_ptr(), W.data_ptr(), self.C.data_ptr(), self.M, self.N, self.K,
+                              self.wsums.data_ptr(), tol_scale, self.rowsum.data_ptr(), self.residual.data_ptr(),
+                              self.bound.data_ptr(), self.flag.data_ptr(), self.summary.data_ptr(),
+                              self.aborted.data_ptr(), self._cws.data_ptr(), self._cwsb, _stream_handle(stream))
         return self.C
 
     def capture(self, A, W, cap_rows: int = 8, cap_cols: int = 8, flag=None, flag_col=None, stream=None) -> dict:

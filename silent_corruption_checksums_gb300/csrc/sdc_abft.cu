@@ -66,8 +66,14 @@ constexpr uint32_t kStageW = kBN * kBK * 2;  // 32 KiB
 constexpr uint32_t kAccCols = 256;           // one accumulator; two are allocated
 constexpr uint32_t kMnBlock = kBK * 128;      // 8 KiB: kBK contraction rows of 64 bf16 (MN-major operands)
 constexpr uint32_t kGemmThreads = 192;
+constexpr uint32_t kRefThreads = 128;  // the fused check's reference warps (one row of the tile each)
 constexpr uint32_t kNumBars = 2 * kStages + 5;  // full[S], empty[S], tfull[2], tempty[2], done
 constexpr uint32_t kGemmSmem = kStages * (kStageA + kStageW) + 1024 + 8 * kNumBars + 16;
+// with the reference warps: a selected K block's column sums (64 x {h, m}, 512 bytes) after the barriers
+// and the TMEM slot, at a 16-byte boundary (128-bit loads)
+constexpr uint32_t kRefSumsOff = (kStages * (kStageA + kStageW) + 8 * kNumBars + 16 + 15) / 16 * 16;
+constexpr uint32_t kGemmSmemRef = 1024 + kRefSumsOff + kBK * 8;
+static_assert(kRefSumsOff % 16 == 0 && kGemmSmemRef <= 232448, "reference sums: alignment and shared memory");
 constexpr uint32_t kColTileFloats = 32 * 33;  // one epilogue warp's column-sum tile (row pitch 33)
 // with columns: the four epilogue warps' column tiles, then their per-tile column partials [4][kBN]
 // (merged in the CTA, so one partial row per tile row reaches global memory)
@@ -138,11 +144,18 @@ __device__ __forceinline__ bool bar_any(uint32_t id, uint32_t count, bool pred) 
 }
 
 // kMN: both operands MN-major (the weight-gradient form, below); otherwise both K-major.
-template <bool kCols, bool kMN>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+// kRef (K-major only): four more warps form the check's reference of each row, A[i, :] (W^T 1), on
+// the CUDA cores beside the product, against W's column sums wsums[k] = {h, m}.  Tile (m, n) takes
+// the K blocks kb with kb mod tiles_n = n, so every K block of every tile row is taken once and the
+// work spreads over all tiles; ref[n][i] = {s, c, mh, ml} is the tile's partial (the reference and
+// the magnitude, each a float32 pair).  They read A's rows from global memory (Ag), where the
+// banded schedule keeps them in L2 for the product's copies, and touch none of its barriers.
+template <bool kCols, bool kMN, bool kRef>
+__global__ void __launch_bounds__(kRef ? kGemmThreads + kRefThreads : kGemmThreads, 1)
     abft_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapW,
                      __nv_bfloat16 *__restrict__ C, uint32_t M, uint32_t N, uint32_t K, uint32_t band_m,
-                     double *__restrict__ rowsum_part, double *__restrict__ colsum_part, int *__restrict__ err) {
+                     double *__restrict__ rowsum_part, double *__restrict__ colsum_part, int *__restrict__ err,
+                     const float2 *__restrict__ wsums, float4 *__restrict__ ref, const __nv_bfloat16 *__restrict__ Ag) {
     extern __shared__ __align__(1024) unsigned char smem[];
     const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
     const uint32_t base = smem_addr(smem), pad = ((base + 1023u) & ~1023u) - base;
@@ -255,7 +268,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tc_commit(done);
             if (!ok) atomicOr(err, 1);
         }
-    } else {  // ------------------------------------------------------- epilogue
+    } else if (warp < kGemmThreads / 32) {  // ------------------------ epilogue
         const uint32_t quarter = warp & 3u;  // the TMEM lanes this warp may read
         const uint32_t lane_base = (quarter * 32) << 16;
         float *coltile = (float *)(smem + pad + kStages * (kStageA + kStageW) + 8 * kNumBars + 16) + quarter * kColTileFloats;
@@ -308,6 +321,54 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 named_bar_sync(1, 128);  // read before the next tile's partials overwrite them
             }
+        }
+    } else if constexpr (kRef) {  // ----------------------------------- reference warps
+        // Thread rt takes row rt of each tile; the tiles come in the CTA's order.  Per selected K block
+        // the group stages the block's 64 column sums in shared memory (one word per thread), each
+        // thread reads its row's 64 values of A (eight 16-byte loads of one 128-byte line) and forms
+        // its part of the reference.  The named barriers keep the staged sums whole while they are read.
+        const uint32_t rt = tid - kGemmThreads;
+        float *hsm = (float *)(smem + pad + kRefSumsOff);
+        const uint32_t hm = smem_addr(hsm);  // {h, m, h, m}: two columns per 16 bytes
+        for (uint32_t u = unit0; u < n_units; u += ustep) {
+            uint32_t tm, tn;
+            coords(u, tm, tn);
+            const uint32_t row = tm * kBM + rt;
+            const uint4 *arow = (const uint4 *)(Ag + (uint64_t)(row < M ? row : 0) * K);
+            // packed float32 pairs over even and odd columns: the reference (s2, c2), the magnitude (a2, e2)
+            uint64_t s2 = 0ull, c2 = 0ull, a2 = 0ull, e2 = 0ull;
+            for (uint32_t kb = tn; kb < nkb; kb += tiles_n) {
+                named_bar_sync(2, kRefThreads);  // the previous block's sums have been read
+                hsm[rt] = kb * kBK + rt / 2 < K ? __ldg((const float *)(wsums + (uint64_t)kb * kBK) + rt) : 0.0f;
+                uint4 av[kBK / 8];
+#pragma unroll
+                for (uint32_t q = 0; q < kBK / 8; ++q)  // past M or K (a multiple of 8): zero
+                    av[q] = row < M && kb * kBK + 8 * q < K ? __ldg(arow + kb * (kBK / 8) + q) : make_uint4(0, 0, 0, 0);
+                named_bar_sync(2, kRefThreads);  // the staged sums are whole
+                uint64_t m2 = 0ull;  // this block's magnitude: a plain chain of 32 terms per half
+#pragma unroll
+                for (uint32_t q = 0; q < kBK / 8; ++q) {  // 8 columns: a chain of 4 per half
+                    uint64_t t = 0ull;
+#pragma unroll
+                    for (uint32_t e = 0; e < 4; ++e) {
+                        const uint32_t w = (&av[q].x)[e];
+                        const uint64_t x = f2_pack_bits(w << 16, w & 0xFFFF0000u);
+                        const uint4 h = ld_shared_u4(hm + (4 * q + e) * 16);
+                        t = f2_fma(x, f2_pack_bits(h.x, h.z), t);
+                        m2 = f2_fma(x & kF2Abs, f2_pack_bits(h.y, h.w), m2);
+                    }
+                    pair2_add(s2, c2, t);
+                }
+                pair2_add(a2, e2, m2);
+            }
+            float s0, s1, c0, c1, a0, a1, e0, e1;
+            f2_unpack(s2, s0, s1);
+            f2_unpack(c2, c0, c1);
+            f2_unpack(a2, a0, a1);
+            f2_unpack(e2, e0, e1);
+            pair_merge(s0, c0, s1, c1);
+            pair_merge(a0, e0, a1, e1);
+            if (row < M) ref[(uint64_t)tn * M + row] = make_float4(s0, c0, a0, e0);
         }
     }
     tc_fence_before();
@@ -774,6 +835,37 @@ __global__ void __launch_bounds__(128) abft_check_kernel(const CheckSide side0, 
     if (tid == 0) o.done[bx] = 0u;  // ready for the next call
 }
 
+// The fused check's verdict per row: the reference the GEMM's reference warps formed (the partials
+// ref[p][i] = {s, c, mh, ml} of the n_parts tiles of the row's tile row: A[i, :] (W^T 1) over their K
+// blocks and its magnitude, each a float32 pair, merged in tile order) against the row's
+// accumulator checksum, with the verifier's bound (the magnitude raised by 1 + delta).
+__global__ void __launch_bounds__(256) abft_ref_finalize_kernel(const double *__restrict__ rowsum,
+                                                                const float4 *__restrict__ ref, uint32_t n_parts,
+                                                                uint32_t M, uint32_t N, uint32_t K, double delta,
+                                                                float tol_scale, double *__restrict__ residual,
+                                                                double *__restrict__ bound, uint8_t *__restrict__ flag,
+                                                                uint32_t *__restrict__ n_flagged) {
+    const uint32_t i = blockIdx.x * 256 + threadIdx.x;
+    if (i >= M) return;
+    float s = 0.0f, c = 0.0f, a = 0.0f, e = 0.0f;
+    for (uint32_t p = 0; p < n_parts; ++p) {
+        const float4 r = ref[(uint64_t)p * M + i];
+        pair_merge(s, c, r.x, r.y);
+        pair_merge(a, e, r.z, r.w);
+    }
+    const double refv = (double)s + (double)c;
+    const double mag = ((double)a + (double)e) * (1.0 + delta);
+    const double gk = (double)K * 0x1p-22;
+    const double b = (gk * (1.0 + gk) + 20.0 * 0x1p-24 + (double)(N + K + 64) * 0x1p-44) * mag +
+                     2.0 * (double)K * (double)N * 0x1p-126;
+    const double d = rowsum[i] - refv;
+    residual[i] = d;
+    bound[i] = b;
+    const uint8_t f = fabs(d) <= (double)tol_scale * b ? 0 : 1;  // NaN flags
+    flag[i] = f;
+    if (f) atomicAdd(n_flagged, 1u);
+}
+
 size_t round_up256(size_t x) { return (x + 255) / 256 * 256; }
 
 // Row slabs of a column sum over `rows` rows of K columns: about 456 blocks in all
@@ -919,7 +1011,7 @@ sdc_status sdc_abft_gemm(const void *d_A, const void *d_W, void *d_C, uint32_t M
     int *err = (int *)((char *)d_ws + w.err);
     cudaStream_t s = (cudaStream_t)stream;
     const bool cols = d_colsum != nullptr;
-    auto kernel = cols ? abft_gemm_kernel<true, false> : abft_gemm_kernel<false, false>;
+    auto kernel = cols ? abft_gemm_kernel<true, false, false> : abft_gemm_kernel<false, false, false>;
     cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int), s);
     const uint32_t smem_bytes = cols ? kGemmSmemCols : kGemmSmem;
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
@@ -929,7 +1021,8 @@ sdc_status sdc_abft_gemm(const void *d_A, const void *d_W, void *d_C, uint32_t M
     // A band of tile rows holds about 24 MiB of A, a fraction of the 126 MiB L2.
     uint32_t band_m = (uint32_t)((24u << 20) / ((size_t)kBM * K * 2));
     band_m = band_m < 1 ? 1 : (band_m > tiles_m ? tiles_m : band_m);
-    kernel<<<grid, kGemmThreads, smem_bytes, s>>>(mapA, mapW, (__nv_bfloat16 *)d_C, M, N, K, band_m, part, cpart, err);
+    kernel<<<grid, kGemmThreads, smem_bytes, s>>>(mapA, mapW, (__nv_bfloat16 *)d_C, M, N, K, band_m, part, cpart, err,
+                                                  nullptr, nullptr, nullptr);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_gemm launch");
     abft_sum_parts_kernel<<<(M + 31) / 32, 256, 0, s>>>(part, M, tiles_n, d_rowsum, err, d_aborted);
@@ -1060,7 +1153,7 @@ sdc_status sdc_abft_gemm_wgrad(const void *d_dY, const void *d_X, void *d_dW, ui
     int *err = (int *)((char *)d_ws + w.err);
     cudaStream_t s = (cudaStream_t)stream;
     const bool cols = d_colsum != nullptr;
-    auto kernel = cols ? abft_gemm_kernel<true, true> : abft_gemm_kernel<false, true>;
+    auto kernel = cols ? abft_gemm_kernel<true, true, false> : abft_gemm_kernel<false, true, false>;
     cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int), s);
     const uint32_t smem_bytes = cols ? kGemmSmemCols : kGemmSmem;
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
@@ -1070,7 +1163,8 @@ sdc_status sdc_abft_gemm_wgrad(const void *d_dY, const void *d_X, void *d_dW, ui
     // a band of tile rows holds about 24 MiB of dY's columns
     uint32_t band_m = (uint32_t)((24u << 20) / ((size_t)kBM * T * 2));
     band_m = band_m < 1 ? 1 : (band_m > tiles_m ? tiles_m : band_m);
-    kernel<<<grid, kGemmThreads, smem_bytes, s>>>(mapA, mapW, (__nv_bfloat16 *)d_dW, N, K, T, band_m, part, cpart, err);
+    kernel<<<grid, kGemmThreads, smem_bytes, s>>>(mapA, mapW, (__nv_bfloat16 *)d_dW, N, K, T, band_m, part, cpart, err,
+                                                  nullptr, nullptr, nullptr);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_gemm_wgrad launch");
     abft_sum_parts_kernel<<<(N + 31) / 32, 256, 0, s>>>(part, N, tiles_n, d_rowsum, err, d_aborted);
@@ -1133,6 +1227,112 @@ sdc_status sdc_abft_verify_wgrad(const void *d_dY, const void *d_X, uint32_t T, 
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_verify_wgrad launch");
     e = cudaGetLastError();
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_abft_verify_wgrad launch");
+}
+
+size_t sdc_abft_weight_sums_workspace_size(uint32_t N, uint32_t K) {
+    if (N == 0 || K == 0 || N % 8 || K % 8 || K > kMaxK) return 0;
+    return round_up256((size_t)n_slabs_for(N, K) * K * sizeof(float4)) + round_up256((K + 255) / 256 * sizeof(uint32_t));
+}
+
+sdc_status sdc_abft_weight_sums(const void *d_W, uint32_t N, uint32_t K, float *d_wsums, void *d_ws, size_t ws_bytes,
+                                sdc_stream_t stream) {
+    if (!d_W || !d_wsums || !d_ws) return fail(SDC_ERR_NULL, "NULL argument");
+    if (N == 0 || K == 0 || N % 8 || K % 8 || K > kMaxK)
+        return fail(SDC_ERR_BAD_ARG, "N and K positive multiples of 8, K <= 2^20");
+    const size_t need = sdc_abft_weight_sums_workspace_size(N, K);
+    if (ws_bytes < need) return fail(SDC_ERR_WS_TOO_SMALL, "workspace smaller than sdc_abft_weight_sums_workspace_size");
+    if ((uint64_t)d_ws & 255u) return fail(SDC_ERR_BAD_POINTER, "workspace is not 256-byte aligned");
+    if ((uint64_t)d_W & 15u) return fail(SDC_ERR_BAD_POINTER, "W must be 16-byte aligned");
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    sdc_status st = check_spans({{d_W, (uint64_t)N * K * 2, "d_W"}, {d_wsums, (uint64_t)K * 8, "d_wsums"},
+                                 {d_ws, need, "d_ws"}},
+                                dev);
+    if (st != SDC_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    const uint32_t ns = n_slabs_for(N, K), cb = (K + 255) / 256;
+    float4 *slabs = (float4 *)d_ws;
+    uint32_t *done = (uint32_t *)((char *)d_ws + round_up256((size_t)ns * K * sizeof(float4)));
+    e = cudaMemsetAsync(done, 0, cb * sizeof(uint32_t), s);
+    if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_weight_sums setup");
+    const SlabSide sw{(const __nv_bfloat16 *)d_W, N, K, ns, slabs, (float2 *)d_wsums, done, ColCheck{}};
+    abft_colsum_slab_kernel<false><<<dim3(cb, ns), 256, 0, s>>>(sw, sw, cb);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_abft_weight_sums launch");
+}
+
+// Workspace of the fused check: the row checksums' tile partials [ceil(N/256)][M] double | the
+// reference partials [ceil(N/256)][M] float4 | abort word.
+size_t sdc_abft_gemm_checked_workspace_size(uint32_t M, uint32_t N, uint32_t K) {
+    if (M == 0 || N == 0 || K == 0 || N % 8 || K % 8 || K > kMaxK) return 0;
+    const size_t tiles_n = (N + kBN - 1) / kBN;
+    return round_up256(tiles_n * M * sizeof(double)) + round_up256(tiles_n * M * sizeof(float4)) + 256;
+}
+
+sdc_status sdc_abft_gemm_checked(const void *d_A, const void *d_W, void *d_C, uint32_t M, uint32_t N, uint32_t K,
+                                 const float *d_wsums, float tol_scale, double *d_rowsum, double *d_residual,
+                                 double *d_bound, uint8_t *d_flag, sdc_abft_summary *d_summary, uint32_t *d_aborted,
+                                 void *d_ws, size_t ws_bytes, sdc_stream_t stream) {
+    if (!d_A || !d_W || !d_C || !d_wsums || !d_rowsum || !d_residual || !d_bound || !d_flag || !d_summary ||
+        !d_aborted || !d_ws)
+        return fail(SDC_ERR_NULL, "NULL argument");
+    if (M == 0 || N == 0 || K == 0 || N % 8 || K % 8 || K > kMaxK)
+        return fail(SDC_ERR_BAD_ARG, "M must be positive, N and K positive multiples of 8, K <= 2^20");
+    const size_t need = sdc_abft_gemm_checked_workspace_size(M, N, K);
+    if (ws_bytes < need) return fail(SDC_ERR_WS_TOO_SMALL, "workspace smaller than sdc_abft_gemm_checked_workspace_size");
+    if ((uint64_t)d_ws & 255u) return fail(SDC_ERR_BAD_POINTER, "workspace is not 256-byte aligned");
+    if (((uint64_t)d_A | (uint64_t)d_W) & 15u) return fail(SDC_ERR_BAD_POINTER, "A and W must be 16-byte aligned");
+    int dev = -1;
+    cudaError_t e0 = cudaGetDevice(&dev);
+    if (e0 != cudaSuccess) return cuda_fail(e0, "cudaGetDevice");
+    sdc_status st = check_spans({{d_A, (uint64_t)M * K * 2, "d_A"}, {d_W, (uint64_t)N * K * 2, "d_W"},
+                                 {d_ws, need, "d_ws"}},
+                                dev);
+    if (st != SDC_OK) return st;
+    if (!(tol_scale > 0.0f)) return fail(SDC_ERR_BAD_ARG, "tol_scale must be positive");
+    st = check_spans({{d_C, (uint64_t)M * N * 2, "d_C"},
+                      {d_wsums, (uint64_t)K * 8, "d_wsums"},
+                      {d_rowsum, (uint64_t)M * 8, "d_rowsum"},
+                      {d_residual, (uint64_t)M * 8, "d_residual"},
+                      {d_bound, (uint64_t)M * 8, "d_bound"},
+                      {d_flag, M, "d_flag"},
+                      {d_summary, sizeof(sdc_abft_summary), "d_summary"},
+                      {d_aborted, 4, "d_aborted"}},
+                     dev);
+    if (st != SDC_OK) return st;
+    if (((uint64_t)d_C | (uint64_t)d_wsums) & 15u) return fail(SDC_ERR_BAD_POINTER, "C and wsums must be 16-byte aligned");
+    const uint32_t tiles_m = (M + kBM - 1) / kBM, tiles_n = (N + kBN - 1) / kBN, sms = (uint32_t)sm_count(dev);
+    CUtensorMap mapA, mapW;
+    st = make_map_sw128(&mapA, d_A, M, K, kBM);
+    if (st == SDC_OK) st = make_map_sw128(&mapW, d_W, N, K, kBN);
+    if (st != SDC_OK) return st;
+    double *part = (double *)d_ws;
+    float4 *ref = (float4 *)((char *)d_ws + round_up256((size_t)tiles_n * M * sizeof(double)));
+    int *err = (int *)((char *)d_ws + need - 256);
+    cudaStream_t s = (cudaStream_t)stream;
+    auto kernel = abft_gemm_kernel<false, false, true>;
+    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(d_summary, 0, sizeof(sdc_abft_summary), s);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmemRef);
+    if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_gemm_checked setup");
+    const uint32_t n_units = tiles_m * tiles_n;
+    const uint32_t grid = n_units < sms ? n_units : sms;
+    uint32_t band_m = (uint32_t)((24u << 20) / ((size_t)kBM * K * 2));
+    band_m = band_m < 1 ? 1 : (band_m > tiles_m ? tiles_m : band_m);
+    kernel<<<grid, kGemmThreads + kRefThreads, kGemmSmemRef, s>>>(mapA, mapW, (__nv_bfloat16 *)d_C, M, N, K, band_m,
+                                                                part, nullptr, err, (const float2 *)d_wsums, ref,
+                                                                (const __nv_bfloat16 *)d_A);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_gemm_checked launch");
+    abft_sum_parts_kernel<<<(M + 31) / 32, 256, 0, s>>>(part, M, tiles_n, d_rowsum, err, d_aborted);
+    // the magnitude's plain chains: W's column sums (a slab warp's rows), a stage's 32 terms per half
+    const uint32_t ns = n_slabs_for(N, K), slab_rows = (N + ns - 1) / ns;
+    const double delta = 2.0 * ((double)((slab_rows + 7) / 8) + 32.0 + 8.0) * 0x1p-24;
+    abft_ref_finalize_kernel<<<(M + 255) / 256, 256, 0, s>>>(d_rowsum, ref, tiles_n, M, N, K, delta, tol_scale,
+                                                            d_residual, d_bound, d_flag, &d_summary->n_flagged);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_abft_gemm_checked launch");
 }
 
 }  // extern "C"
