@@ -595,6 +595,14 @@ def bench_abft_row(args, dev, stream, peaks, sdc, W, torch) -> dict:
     ms_gemm_rc = _time_loop(lambda: gc.gemm(A, Wt, stream=stream), reps, stream, torch)
     ms_verify_rc = _time_loop(lambda: gc.verify(A, Wt, stream=stream), reps, stream, torch)
     ms_cublas = _time_loop(lambda: torch.matmul(A, Wt.t()), reps, stream, torch)
+    # the row check fused into the GEMM: W's column sums once per weight version, then the GEMM whose
+    # extra warps form the reference beside the product
+    ms_wsums = _time_loop(lambda: g.weight_sums(Wt, stream=stream), reps, stream, torch)
+    ms_fused = _time_loop(lambda: g.gemm_checked(A, Wt, stream=stream), reps, stream, torch)
+    torch.cuda.synchronize()
+    fused_flagged = int(g.summary[0])
+    g.gemm(A, Wt, stream=stream)
+    g.verify(A, Wt, stream=stream)
     torch.cuda.synchronize()
     flops = 2.0 * M * N * K
     tf = flops / (ms_gemm * 1e-3) / 1e12
@@ -611,6 +619,9 @@ def bench_abft_row(args, dev, stream, peaks, sdc, W, torch) -> dict:
                          "row_col_clean_flagged": [int(gc.summary[0]), int(gc.summary[1])],
                          "cublas_plain_gemm_ms": ms_cublas,
                          "cublas_tflops": flops / (ms_cublas * 1e-3) / 1e12,
+                         "fused_row_check_gemm_ms": ms_fused, "fused_over_gemm": ms_fused / ms_gemm - 1.0,
+                         "separate_row_check_over_gemm": ms_verify / ms_gemm,
+                         "weight_sums_ms": ms_wsums, "fused_clean_rows_flagged": fused_flagged,
                          "clean_rows_flagged": int(g.summary[0]), "aborted": int(g.aborted[0]),
                          "max_residual_over_bound": float((g.residual.abs() / g.bound).max())}}
     # the oracle (float64, numpy's BLAS on all host cores) on the first 64 rows of A
