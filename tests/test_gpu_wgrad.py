@@ -157,3 +157,20 @@ def test_rejects_misaligned_and_short_workspace(sdc):
         sdc.sdc_abft_gemm_wgrad(ops["dY"].data_ptr(), ops["X"].data_ptr(), a.dW.data_ptr(), T, N, K,
                                 a.rowsum.data_ptr(), 0, a.aborted.data_ptr(), a.ws.data_ptr(), a.ws_bytes - 256, 0)
     assert ei.value.status == 5
+
+
+def test_wgrad_largest_contraction(sdc):
+    # the most tokens the kernel accepts (2^20), where the rounding bound is at its loosest
+    # (g = T 2^-22 = 1/4): one tile, rows and columns, against the oracle
+    T, N, K = 1 << 20, 8, 64
+    ops = W.wgrad_operands(T, N, K, DEV, seed=36)
+    a = sdc.AbftWgrad(T, N, K, DEV)
+    a(ops["dY"], ops["X"])
+    torch.cuda.synchronize()
+    dYb, Xb = _bits(ops["dY"]), _bits(ops["X"])
+    del ops
+    _check_clean(a, dYb, Xb, T, N, K)
+    with pytest.raises(sdc.SdcError) as ei:  # one token more is rejected
+        sdc.AbftWgrad(T + 8, N, K, DEV).gemm(torch.empty((T + 8, N), dtype=torch.bfloat16, device=DEV),
+                                             torch.empty((T + 8, K), dtype=torch.bfloat16, device=DEV))
+    assert ei.value.status == 9
