@@ -20,10 +20,7 @@
 //   (every row of every P_h sums to 1).  group = 1 is plain multi-head attention.
 //
 // Kernels:
-//   attn_do_prep_kernel -- -lse log2(e), and float32-pair column sums of dO
-//     and |dO| per 128-row block (dO itself feeds the dV product as it is:
-//     its B operand, MN-major); persistent CTAs, each block's rows brought in
-//     by a bulk copy that overlaps the previous block's sums;
+//   attn_lse2_kernel -- -lse log2(e) of every (head, token), elementwise;
 //   attn_dv_kernel -- persistent, one CTA per SM; a work item is one
 //     (K/V head, 128-key block), taken from a counter heaviest first (causal:
 //     key block 0 of every head first), its steps running over the query
@@ -41,9 +38,14 @@
 //       two 128-column TMEM accumulators (alternate items), its A operand P^T
 //       read from TMEM.  Two issuing threads: one thread's tcgen05.mma issue
 //       rate, not the tensor pipe, bounds products with N = 128;
-//     warps 4..7: epilogue -- when an item's dV is complete, each thread
-//       stores its key's row as bf16 and the warps sum dV's columns (float32
-//       pairs) through shared memory, while the next item's products run;
+//     warps 4..7: epilogue -- while an item's products run, they sum the
+//       columns of dO and |dO| over the item's share of each of the group's
+//       query heads' rows (float32 pairs; the shares cover every row once:
+//       query block kb without a mask, causal a share in proportion to the
+//       item's steps); when the item's dV is complete, each
+//       thread stores its key's row as bf16 and the warps sum dV's columns
+//       (float32 pairs) through shared memory, while the next item's
+//       products run;
 //     warps 8..23: softmax -- each thread owns one key (a TMEM lane) and 32
 //       of the step's queries (four warps per lane quarter), reads those 32
 //       scores, forms exp2(s scale log2(e) - lse log2(e)) (masked when
@@ -109,10 +111,11 @@ constexpr uint32_t kAttnSmem = 1024 + kOffSlot + 16;
 static_assert(kAttnSmem <= 232448, "shared memory per block");
 static_assert(kOffBar % 8 == 0, "mbarrier alignment");
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t kDoChain = 8;  // rows of dO's plain float32 chains before each is folded into a pair
 
-// Programmatic dependent launch: the prep kernel lets the dV kernel launch at once, and the dV
-// kernel's threads that read the prep's results (-lse log2(e), dO's column sums) wait for the prep
-// grid to complete first; its other work (TMEM, barriers, the K and Q copies) overlaps the prep's tail.
+// Programmatic dependent launch: the lse2 kernel lets the dV kernel launch at once, and the dV
+// kernel's thread that copies -lse log2(e) waits for that grid to complete first; its other work
+// (TMEM, barriers, the K and Q copies) overlaps the lse2 kernel.
 // Without a dependent launch the wait returns at once.
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -135,9 +138,9 @@ __device__ __forceinline__ bool bar_any(uint32_t id, uint32_t count, bool pred) 
     return r != 0;
 }
 
-// The invariant of head bh, column c, once every key block's partial is in part_dv: dV's column
-// sum (the blocks' partials merged in order), dO's and |dO|'s (the prep pass's partials merged in
-// order), the residual, the bound and the flag.
+// The invariant of K/V head kvh, column c, once every key block's partials are in part_dv and
+// part_do: dV's column sum and dO's and |dO|'s (the blocks' partials merged in order), the
+// residual, the bound and the flag.
 struct AttnOut {
     double *colsum_dv, *colsum_do, *residual, *bound;
     uint8_t *flag;
@@ -148,37 +151,21 @@ struct AttnOut {
 __device__ void head_invariant(const float2 *part_dv, const float4 *part_do, uint32_t kvh, uint32_t c, uint32_t nb,
                                uint32_t group, uint32_t L, const AttnOut &o) {
     float vs = 0.0f, vc = 0.0f, os = 0.0f, oc = 0.0f, as = 0.0f, ac = 0.0f;
-    // L2 reads: other blocks wrote these partials
-    if (group == 1) {  // one pass over the key blocks: both partials of block b together
+    // L2 reads: other blocks wrote these partials; block b's dO partial covers query block b of every
+    // query head of the group
 #pragma unroll 8
-        for (uint32_t b = 0; b < nb; ++b) {
-            const float2 pv = __ldcg(part_dv + ((uint64_t)kvh * nb + b) * kHD + c);
-            const float4 po = __ldcg(part_do + ((uint64_t)kvh * nb + b) * kHD + c);
-            pair_merge(vs, vc, pv.x, pv.y);
-            pair_merge(os, oc, po.x, po.y);
-            pair_merge(as, ac, po.z, po.w);
-        }
-    } else {  // dV's key blocks, then the group's query heads, each over its query blocks, in order
-#pragma unroll 8
-        for (uint32_t b = 0; b < nb; ++b) {
-            const float2 pv = __ldcg(part_dv + ((uint64_t)kvh * nb + b) * kHD + c);
-            pair_merge(vs, vc, pv.x, pv.y);
-        }
-        for (uint32_t h = 0; h < group; ++h) {
-            const float4 *pd = part_do + (uint64_t)(kvh * group + h) * nb * kHD + c;
-#pragma unroll 8
-            for (uint32_t b = 0; b < nb; ++b) {
-                const float4 po = __ldcg(pd + (uint64_t)b * kHD);
-                pair_merge(os, oc, po.x, po.y);
-                pair_merge(as, ac, po.z, po.w);
-            }
-        }
+    for (uint32_t b = 0; b < nb; ++b) {
+        const float2 pv = __ldcg(part_dv + ((uint64_t)kvh * nb + b) * kHD + c);
+        const float4 po = __ldcg(part_do + ((uint64_t)kvh * nb + b) * kHD + c);
+        pair_merge(vs, vc, pv.x, pv.y);
+        pair_merge(os, oc, po.x, po.y);
+        pair_merge(as, ac, po.z, po.w);
     }
     const double dv = (double)vs + (double)vc, dsum = (double)os + (double)oc, dabs = (double)as + (double)ac;
     // dV's accumulation runs over the group's group * L query rows.  Beyond the method's terms the
-    // bound carries this kernel's own: the float32 pairs of both column sums (2^-40) and the prep's
-    // plain chains of kPrepChain rows (below kPrepChain 2^-24 each, twice over: 16 2^-24), and it
-    // takes sum |dO| raised by kPrepChain 2^-24, above the exact sum whatever the chains lost.
+    // bound carries this kernel's own: the float32 pairs of both column sums (2^-40) and dO's plain
+    // chains of at most 8 rows (below 8 2^-24 each, twice over: 16 2^-24), and it takes sum |dO| raised
+    // by 8 2^-24, above the exact sum whatever the chains lost.
     const double g = (double)group * (double)L * 0x1p-22, rho = 1.0 + 0x1p-7;
     const double own = 0x1p-40 + 16.0 * 0x1p-24;
     const double bnd = (0x1p-8 * rho + g * (1.0 + g) * rho + own) * dabs * (1.0 + 8.0 * 0x1p-24) + 0x1p-100;
@@ -200,8 +187,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_dv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                    const __grid_constant__ CUtensorMap mapDo, const float *__restrict__ lse2, uint32_t L,
                    uint32_t n_kv, uint32_t group, float scale_log2, uint32_t causal, __nv_bfloat16 *__restrict__ dV,
-                   float2 *__restrict__ part_dv, const float4 *__restrict__ part_do, const AttnOut out,
-                   int *__restrict__ err, uint32_t *__restrict__ ctr) {
+                   float2 *__restrict__ part_dv, float4 *__restrict__ part_do, const AttnOut out,
+                   int *__restrict__ err, uint32_t *__restrict__ ctr, const __nv_bfloat16 *__restrict__ dO) {
     // ctr: [0] the work counter, [1] blocks finished, [3 + h] key blocks of head h finished
     uint32_t *next_item = ctr;
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -264,7 +251,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (warp == 0) {
         if (lane == 0) {  // ------------------------------------------ work queue + TMA
             uint32_t nk = 0, tl = 0, tq = 0;  // K tiles and steps whose copies were issued
-            bool prep_done = false;           // the prep grid's -lse log2(e) is complete
+            bool lse2_done = false;           // the lse2 grid's -lse log2(e) is complete
             for (uint32_t i = 0; ok; ++i) {
                 const uint32_t slot = i % kItemSlots;
                 if (i >= kItemSlots && !mbar_wait(BAR(kBarIE + slot), ((i / kItemSlots) - 1) & 1)) {
@@ -298,9 +285,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         ok = false;
                         break;
                     }
-                    if (!prep_done) {
+                    if (!lse2_done) {
                         grid_dep_wait();
-                        prep_done = true;
+                        lse2_done = true;
                     }
                     // the block's queries inside the sequence (a multiple of 4: 16-byte copies)
                     const uint32_t lbytes = (L - qb * kBlk < kBlk ? L - qb * kBlk : kBlk) * 4;
@@ -457,7 +444,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         float *scr = (float *)(sm + kOffScr) + (warp - kEpiBase) * 32 * kScrPitch;
         float2 *cpart = (float2 *)(sm + kOffCp);  // [lane quarter][column]
         volatile uint32_t *last = (volatile uint32_t *)(sm + kOffFlag);
-        grid_dep_wait();  // the head invariant reads the prep grid's column sums of dO
+        const uint32_t et = tid - kEpiBase * 32, cp = et & (kHD / 2 - 1), half = et / (kHD / 2);
+        static_assert(kEpiWarps * 32 == kHD, "the dO sums: one thread per column pair and half of the share");
         for (uint32_t i = 0;; ++i) {
             const uint32_t slot = i % kItemSlots;
             bool got = mbar_wait(BAR(kBarIF + slot), (i / kItemSlots) & 1);
@@ -470,6 +458,68 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (lane == 0) mbar_arrive(BAR(kBarIE + slot));
             if (w == kNoItem) break;
             const uint32_t kb = w / n_kv, kvh = w % n_kv, db = i % kDvBufs;
+            {  // dO's column sums over this item's share of the rows of each of the group's query heads,
+               // while the item's products run.  The shares cover every row of a head once: without a
+               // mask the item on the diagonal takes query block kb; causal, item kb takes rows in
+               // proportion to its steps (nkb - kb), in units of whole chains, so that the short items
+               // at the end of the schedule carry only a few rows.  Thread (column pair cp, half) sums
+               // columns 2cp, 2cp + 1 over its half of the share: plain float32 chains of kDoChain rows
+               // folded into packed float32 pairs; the halves meet through the scratch (free until the
+               // dV epilogue below).
+                uint32_t lo, hi;
+                if (causal) {
+                    const uint32_t steps = nkb * (nkb + 1) / 2;
+                    const uint32_t unit = kDoChain * ((L + kDoChain * steps - 1) / (kDoChain * steps));
+                    const uint32_t before = kb * nkb - kb * (kb - 1) / 2;  // steps of the items kb' < kb
+                    lo = min(L, unit * before);
+                    hi = min(L, unit * (before + nkb - kb));
+                } else {
+                    lo = kb * kBlk;
+                    hi = min(L, lo + kBlk);
+                }
+                const uint32_t mid = lo + (hi - lo + 2 * kDoChain - 1) / (2 * kDoChain) * kDoChain;
+                const uint32_t r0 = half ? min(mid, hi) : lo, r1 = half ? hi : min(mid, hi);
+                uint64_t ds = 0ull, dc = 0ull, das = 0ull, dac = 0ull;
+                for (uint32_t h = 0; h < group; ++h) {
+                    const uint32_t *src = (const uint32_t *)(dO + (uint64_t)(kvh * group + h) * L * kHD) + cp;
+                    for (uint32_t rc = r0; rc < r1; rc += kDoChain) {
+                        uint32_t wv[kDoChain];
+#pragma unroll
+                        for (uint32_t u = 0; u < kDoChain; ++u) wv[u] = rc + u < r1 ? __ldg(src + (rc + u) * (kHD / 2)) : 0u;
+                        uint64_t t = 0ull, ta = 0ull;
+#pragma unroll
+                        for (uint32_t u = 0; u < kDoChain; ++u) {
+                            const uint32_t wa = wv[u] & 0x7FFF7FFFu;
+                            t = f2_add(t, f2_pack_bits(wv[u] << 16, wv[u] & 0xFFFF0000u));
+                            ta = f2_add(ta, f2_pack_bits(wa << 16, wa & 0xFFFF0000u));
+                        }
+                        pair2_add(ds, dc, t);
+                        pair2_add(das, dac, ta);
+                    }
+                }
+                ulonglong2 *xs = (ulonglong2 *)(sm + kOffScr);  // [column pair][2]
+                if (half == 1) {
+                    xs[cp * 2] = make_ulonglong2(ds, dc);
+                    xs[cp * 2 + 1] = make_ulonglong2(das, dac);
+                }
+                named_bar_sync(2, 32 * kEpiWarps);
+                if (half == 0) {
+                    const ulonglong2 o = xs[cp * 2], oa = xs[cp * 2 + 1];
+                    pair2_add(ds, dc, o.x);
+                    dc = f2_add(dc, o.y);
+                    pair2_add(das, dac, oa.x);
+                    dac = f2_add(dac, oa.y);
+                    float s0, s1, c0, c1, a0, a1, e0, e1;
+                    f2_unpack(ds, s0, s1);
+                    f2_unpack(dc, c0, c1);
+                    f2_unpack(das, a0, a1);
+                    f2_unpack(dac, e0, e1);
+                    float4 *o4 = part_do + ((uint64_t)kvh * nkb + kb) * kHD + 2 * cp;
+                    o4[0] = make_float4(s0, c0, a0, e0);
+                    o4[1] = make_float4(s1, c1, a1, e1);
+                }
+                named_bar_sync(2, 32 * kEpiWarps);  // the scratch is read before the dV epilogue writes it
+            }
             got = mbar_wait(BAR(kBarVF + db), (i / kDvBufs) & 1);
             if (bar_any(2, 32 * kEpiWarps, !got)) {
                 ok = false;
@@ -640,110 +690,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #undef BAR
 }
 
-// -lse log2(e), and the column sums of dO and |dO| over each block of 128 rows:
-// part_do[head][block][c] = {pair of sum_i dO[i, c], pair of sum_i |dO[i, c]|}.
-// The prep pass: one work unit per (head, 128-row block) of dO.  Persistent
-// CTAs take units round-robin; a unit's rows (contiguous, rows x 256 bytes)
-// arrive by one bulk copy into one of two shared-memory buffers, so the next
-// unit's copy runs while this one is summed; the unit's log-sum-exps come on
-// the same barrier (rows x 4 bytes), so no thread waits on a global load.
-// Thread (column pair p, row quarter h) sums columns 2p and 2p + 1 over rows
-// 32h .. 32h + 31, for dO and |dO|: plain float32 chains of kPrepChain rows
-// folded into packed float32 pairs with TwoSum (each chain is off by at most
-// kPrepChain 2^-24 of its rows' |dO| sum, counted in the invariant's bound);
-// quarters 1-3 are then merged into quarter 0 in that order.
-constexpr uint32_t kPrepThreads = 256, kPrepQuarters = kPrepThreads / (kHD / 2);
-constexpr uint32_t kPrepScr = 2 * kTile;                                      // [3][64] x (dO pair, |dO| pair)
-constexpr uint32_t kPrepLse = kPrepScr + (kPrepQuarters - 1) * (kHD / 2) * 32;  // [2][128] float
-constexpr uint32_t kPrepBar = kPrepLse + 2 * kBlk * 4;                            // two mbarriers
-constexpr uint32_t kPrepSmem = kPrepBar + 16;
-constexpr uint32_t kPrepCtasPerSm = 3;
-constexpr uint32_t kPrepChain = 8;  // rows of a plain float32 chain before it is folded into a pair
-static_assert(kPrepCtasPerSm * (kPrepSmem + 1024) <= 233472, "prep CTAs per SM exceed shared memory");
-
-__global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm)
-    attn_do_prep_kernel(const __nv_bfloat16 *__restrict__ dO, const float *__restrict__ lse, uint32_t L, uint32_t nb,
-                        uint32_t n_units, float4 *__restrict__ part_do, float *__restrict__ lse2, int *__restrict__ err) {
-    extern __shared__ __align__(128) uint8_t psm[];
+// -lse log2(e) of every (head, token): the exponent's offset in base 2, negated, which the softmax
+// adds (one float32 product per value, four values per thread and step).  The dV kernel is launched as
+// its programmatic dependent: its set-up and its K and Q copies overlap this grid.
+__global__ void __launch_bounds__(256) attn_lse2_kernel(const float4 *__restrict__ lse, uint32_t n4,
+                                                        float4 *__restrict__ lse2) {
     grid_dep_launch();  // the dV kernel may start its set-up now
-    const uint32_t tid = threadIdx.x, cp = tid & (kHD / 2 - 1), h = tid / (kHD / 2);
-    const uint32_t first = blockIdx.x, stride = gridDim.x;
-    const uint32_t n_mine = first < n_units ? (n_units - 1 - first) / stride + 1 : 0;
-    const uint32_t bar0 = smem_addr(psm + kPrepBar);
-    auto unit_rows = [&](uint32_t u) {  // the unit's rows inside the sequence
-        const uint32_t qb = u % nb;
-        return L - qb * kBlk < kBlk ? L - qb * kBlk : kBlk;
-    };
-    auto issue = [&](uint32_t i) {  // copy the CTA's i-th unit into buffer i & 1
-        const uint32_t u = first + i * stride, rows = unit_rows(u), bar = bar0 + 8 * (i & 1);
-        const uint64_t row0 = (uint64_t)(u / nb) * L + (u % nb) * kBlk;  // a multiple of 4: 16-byte aligned lse
-        mbar_arrive_expect_tx(bar, rows * (kHD * 2 + 4));
-        bulk_g2s(smem_addr(psm + (i & 1) * kTile), dO + row0 * kHD, rows * kHD * 2, bar);
-        bulk_g2s(smem_addr(psm + kPrepLse + (i & 1) * kBlk * 4), lse + row0, rows * 4, bar);
-    };
-    if (tid == 0) {
-        mbar_init(bar0, 1);
-        mbar_init(bar0 + 8, 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-    if (tid == 0 && n_mine) issue(0);
-    for (uint32_t i = 0; i < n_mine; ++i) {
-        // buffer (i + 1) & 1 was last read in iteration i - 1, whose closing barrier every thread has passed
-        if (tid == 0 && i + 1 < n_mine) issue(i + 1);
-        const uint32_t u = first + i * stride, bh = u / nb, qb = u % nb, rows = unit_rows(u);
-        const uint64_t row0 = (uint64_t)bh * L + (uint64_t)qb * kBlk;
-        const bool got = mbar_wait(bar0 + 8 * (i & 1), (i >> 1) & 1u);
-        if (!__syncthreads_and(got)) {  // a copy that never landed: record it, let the copies in flight end
-            if (tid == 0) {
-                atomicOr(err, 1);
-                mbar_wait(bar0 + 8 * (i & 1), (i >> 1) & 1u);
-                if (i + 1 < n_mine) mbar_wait(bar0 + 8 * ((i + 1) & 1), ((i + 1) >> 1) & 1u);
-            }
-            return;
-        }
-        if (tid < rows)  // the exponent's offset in base 2, negated: -(lse log2(e)) exactly, added by the softmax
-            lse2[row0 + tid] = ((const float *)(psm + kPrepLse))[(i & 1) * kBlk + tid] * -kLog2e;
-        const uint32_t *tile = (const uint32_t *)(psm + (i & 1) * kTile);  // [128 rows][64 column pairs]
-        uint64_t s = 0, c = 0, sa = 0, ca = 0;
-        const uint32_t r0 = h * (kBlk / kPrepQuarters), r1 = min(r0 + kBlk / kPrepQuarters, rows);
-        for (uint32_t rc = r0; rc < r1; rc += kPrepChain) {  // plain chains of kPrepChain rows, folded into pairs
-            uint64_t t = 0, ta = 0;
-#pragma unroll
-            for (uint32_t u = 0; u < kPrepChain; ++u) {
-                const uint32_t w = rc + u < r1 ? tile[(rc + u) * (kHD / 2) + cp] : 0u, wa = w & 0x7FFF7FFFu;
-                t = f2_add(t, f2_pack_bits(w << 16, w & 0xFFFF0000u));
-                ta = f2_add(ta, f2_pack_bits(wa << 16, wa & 0xFFFF0000u));
-            }
-            pair2_add(s, c, t);
-            pair2_add(sa, ca, ta);
-        }
-        ulonglong2 *scr = (ulonglong2 *)(psm + kPrepScr);  // [quarter - 1][pair][2]
-        if (h > 0) {
-            scr[((h - 1) * (kHD / 2) + cp) * 2] = make_ulonglong2(s, c);
-            scr[((h - 1) * (kHD / 2) + cp) * 2 + 1] = make_ulonglong2(sa, ca);
-        }
-        __syncthreads();
-        if (h == 0) {
-#pragma unroll
-            for (uint32_t q = 0; q + 1 < kPrepQuarters; ++q) {
-                const ulonglong2 o = scr[(q * (kHD / 2) + cp) * 2], oa = scr[(q * (kHD / 2) + cp) * 2 + 1];
-                pair2_add(s, c, o.x);
-                c = f2_add(c, o.y);
-                pair2_add(sa, ca, oa.x);
-                ca = f2_add(ca, oa.y);
-            }
-            float s0, s1, c0, c1, a0, a1, e0, e1;
-            f2_unpack(s, s0, s1);
-            f2_unpack(c, c0, c1);
-            f2_unpack(sa, a0, a1);
-            f2_unpack(ca, e0, e1);
-            float4 *o = part_do + ((uint64_t)bh * nb + qb) * kHD + 2 * cp;
-            o[0] = make_float4(s0, c0, a0, e0);
-            o[1] = make_float4(s1, c1, a1, e1);
-        }
-        // quarter 0's scratch reads end before the next iteration's first barrier, after which the
-        // other quarters write the scratch again
+    for (uint32_t i = blockIdx.x * 256 + threadIdx.x; i < n4; i += gridDim.x * 256) {
+        const float4 v = lse[i];
+        lse2[i] = make_float4(v.x * -kLog2e, v.y * -kLog2e, v.z * -kLog2e, v.w * -kLog2e);
     }
 }
 
@@ -848,27 +803,24 @@ sdc_status sdc_attn_dv_check_grouped(const void *d_Q, const void *d_K, const voi
     if (e == cudaSuccess) e = cudaMemsetAsync(d_summary, 0, sizeof(sdc_abft_summary), s);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(attn_dv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAttnSmem);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(attn_do_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
     if (e != cudaSuccess) return cuda_fail(e, "sdc_attn_dv_check setup");
-    const uint32_t nb = (L + kBlk - 1) / kBlk;
     const AttnOut out{d_colsum_dv, d_colsum_do, d_residual, d_bound, d_flag, d_summary, d_aborted, tol_scale};
-    const uint32_t prep_units = BH * nb;
-    const uint32_t prep_grid = prep_units < kPrepCtasPerSm * (uint32_t)n_sm ? prep_units : kPrepCtasPerSm * n_sm;
-    attn_do_prep_kernel<<<prep_grid, kPrepThreads, kPrepSmem, s>>>((const __nv_bfloat16 *)d_dO, d_lse, L, nb,
-                                                                   prep_units, pdo, lse2, err);
+    const uint32_t n4 = BH * L / 4;  // L is a multiple of 4
+    const uint32_t lse_grid = (n4 + 255) / 256 < 4u * (uint32_t)n_sm ? (n4 + 255) / 256 : 4u * (uint32_t)n_sm;
+    attn_lse2_kernel<<<lse_grid, 256, 0, s>>>((const float4 *)d_lse, n4, (float4 *)lse2);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kAttnThreads);
     cfg.dynamicSmemBytes = kAttnSmem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start before the prep completes
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start before lse2 is complete
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, attn_dv_kernel, mapQ, mapK, mapDo, (const float *)lse2, L, n_kv, group,
-                           scale * kLog2e, causal, (__nv_bfloat16 *)d_dV, pdv, (const float4 *)pdo, out, err, ctr);
+                           scale * kLog2e, causal, (__nv_bfloat16 *)d_dV, pdv, pdo, out, err, ctr,
+                           (const __nv_bfloat16 *)d_dO);
     if (e != cudaSuccess) return cuda_fail(e, "sdc_attn_dv_check launch");
     e = cudaGetLastError();
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_attn_dv_check launch");
