@@ -448,6 +448,26 @@ sdc_status sdc_abft_replay(const void *d_W, uint32_t N, uint32_t K, uint32_t cap
                            const void *d_row_A, const void *d_row_C, const uint32_t *d_counts, uint32_t *d_ndiff,
                            uint32_t *d_summary, void *d_ws, size_t ws_bytes, sdc_stream_t stream);
 
+/* Workspace bytes of sdc_abft_replay_pairs (0 for caps outside 1..64 or a
+ * bad K). */
+size_t sdc_abft_replay_pairs_workspace_size(uint32_t K, uint32_t cap_rows, uint32_t cap_cols);
+
+/* The replay of a forward product's captured rows and columns (the row +
+ * column configuration): every (row i_r, column j_c) pair's output C[i_r][j_c]
+ * is recomputed from the captured row of A and the captured row of W (B's
+ * column) alone, by the same tensor-core kernel at the same position in its
+ * tile.  d_differs [cap_rows][cap_cols] uint8: 1 unless the replay equals, bit
+ * for bit, both captured copies of that output (d_row_C's element j_c and
+ * d_col_C's element i_r); 0 past the counts.  d_summary [2]: the pairs that
+ * differ, and the replay GEMM's abort flag.  The captured buffers and
+ * d_counts as sdc_abft_capture wrote them for this M, N, K with the same caps
+ * (1..64 each). */
+sdc_status sdc_abft_replay_pairs(uint32_t M, uint32_t N, uint32_t K, uint32_t cap_rows, uint32_t cap_cols,
+                                 const uint32_t *d_row_idx, const void *d_row_A, const void *d_row_C,
+                                 const uint32_t *d_col_idx, const void *d_col_W, const void *d_col_C,
+                                 const uint32_t *d_counts, uint8_t *d_differs, uint32_t *d_summary, void *d_ws,
+                                 size_t ws_bytes, sdc_stream_t stream);
+
 /* Workspace bytes of sdc_abft_replay_wgrad (0 for caps outside 1..64). */
 size_t sdc_abft_replay_wgrad_workspace_size(uint32_t T, uint32_t cap_rows, uint32_t cap_cols);
 

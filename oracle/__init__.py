@@ -623,6 +623,17 @@ def abft_replay_rows(row_A_bits, W_bits, row_C_bits) -> np.ndarray:
     return (~ok).sum(axis=1)
 
 
+def abft_replay_pairs(cap: dict) -> np.ndarray:
+    """Per captured (row r, column c) pair of a forward product: whether the saved C[i_r, j_c] is
+    inconsistent with the saved operands A[i_r, :] and W[j_c, :] (1) or not (0)."""
+    A = bf16_to_f64(cap["row_A"])  # [rows, K]
+    W = bf16_to_f64(cap["col_W"])  # [cols, K]
+    K = A.shape[1]
+    saved = cap["row_C"][:, cap["col_idx"]]  # [rows, cols]: C[i_r, j_c]
+    ok = output_consistent(saved, A @ W.T, np.abs(A) @ np.abs(W).T, K)
+    return (~ok).astype(np.uint8)
+
+
 def wgrad_replay_pairs(cap: dict) -> np.ndarray:
     """Per captured (row r, column c) pair of a weight-gradient product: whether the saved
     dW[n_r, k_c] is inconsistent with the saved operands dY[:, n_r] and X[:, k_c] (1) or not (0)."""

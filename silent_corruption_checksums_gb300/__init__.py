@@ -113,6 +113,9 @@ def _load() -> ctypes.CDLL:
                                    ctypes.c_int),
         "sdc_abft_replay_workspace_size": ([u32, u32, u32], sz),
         "sdc_abft_replay": ([vp, u32, u32, u32, vp, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
+        "sdc_abft_replay_pairs_workspace_size": ([u32, u32, u32], sz),
+        "sdc_abft_replay_pairs": ([u32, u32, u32, u32, u32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
+                                  ctypes.c_int),
         "sdc_abft_replay_wgrad_workspace_size": ([u32, u32, u32], sz),
         "sdc_abft_replay_wgrad": ([u32, u32, u32, u32, u32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
                                   ctypes.c_int),
@@ -341,6 +344,18 @@ def sdc_abft_replay(d_W: int, N: int, K: int, cap_rows: int, d_row_idx: int, d_r
                     d_counts: int, d_ndiff: int, d_summary: int, d_ws: int, ws_bytes: int, stream: int) -> None:
     _check("sdc_abft_replay", _lib.sdc_abft_replay(d_W, N, K, cap_rows, d_row_idx, d_row_A, d_row_C, d_counts,
                                                    d_ndiff, d_summary, d_ws, ws_bytes, stream))
+
+
+def sdc_abft_replay_pairs_workspace_size(K: int, cap_rows: int, cap_cols: int) -> int:
+    return int(_lib.sdc_abft_replay_pairs_workspace_size(K, cap_rows, cap_cols))
+
+
+def sdc_abft_replay_pairs(M: int, N: int, K: int, cap_rows: int, cap_cols: int, d_row_idx: int, d_row_A: int,
+                          d_row_C: int, d_col_idx: int, d_col_W: int, d_col_C: int, d_counts: int, d_differs: int,
+                          d_summary: int, d_ws: int, ws_bytes: int, stream: int) -> None:
+    _check("sdc_abft_replay_pairs",
+           _lib.sdc_abft_replay_pairs(M, N, K, cap_rows, cap_cols, d_row_idx, d_row_A, d_row_C, d_col_idx, d_col_W,
+                                      d_col_C, d_counts, d_differs, d_summary, d_ws, ws_bytes, stream))
 
 
 def sdc_abft_replay_wgrad_workspace_size(T: int, cap_rows: int, cap_cols: int) -> int:
@@ -723,7 +738,8 @@ class AbftGemm:
                "col_idx": torch.zeros(cap_cols, dtype=torch.int32, device=dev),
                "col_W": torch.zeros((cap_cols, self.K), dtype=torch.bfloat16, device=dev),
                "col_C": torch.zeros((cap_cols, self.M), dtype=torch.bfloat16, device=dev),
-               "counts": torch.zeros(2, dtype=torch.int32, device=dev), "cap_rows": cap_rows}
+               "counts": torch.zeros(2, dtype=torch.int32, device=dev), "cap_rows": cap_rows,
+               "cap_cols": cap_cols}
         c = cap_cols if fc is not None else 0
         sdc_abft_capture(A.data_ptr(), W.data_ptr(), self.C.data_ptr(), self.M, self.N, self.K, f.data_ptr(),
                          fc.data_ptr() if fc is not None else 0, cap_rows, out["row_idx"].data_ptr(),
@@ -747,6 +763,22 @@ class AbftGemm:
                         cap["row_C"].data_ptr(), cap["counts"].data_ptr(), ndiff.data_ptr(), summary.data_ptr(),
                         ws.data_ptr(), wsb, _stream_handle(stream))
         return ndiff, summary
+
+    def replay_pairs(self, cap: dict, stream=None):
+        """Recompute every captured (row, column) output from the captured A row and W row alone (the
+        row + column configuration): (differs [cap_rows, cap_cols] uint8, summary [2]) as device tensors."""
+        torch = _torch()
+        nr, nc = cap["cap_rows"], cap["cap_cols"]
+        dev = self.C.device
+        differs = torch.zeros((nr, nc), dtype=torch.uint8, device=dev)
+        summary = torch.zeros(2, dtype=torch.int32, device=dev)
+        wsb = sdc_abft_replay_pairs_workspace_size(self.K, nr, nc)
+        ws = _ws(wsb, dev)
+        sdc_abft_replay_pairs(self.M, self.N, self.K, nr, nc, cap["row_idx"].data_ptr(), cap["row_A"].data_ptr(),
+                              cap["row_C"].data_ptr(), cap["col_idx"].data_ptr(), cap["col_W"].data_ptr(),
+                              cap["col_C"].data_ptr(), cap["counts"].data_ptr(), differs.data_ptr(),
+                              summary.data_ptr(), ws.data_ptr(), wsb, _stream_handle(stream))
+        return differs, summary
 
 
 class AbftWgrad:

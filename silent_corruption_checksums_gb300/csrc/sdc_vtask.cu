@@ -32,7 +32,7 @@ namespace {
 
 constexpr uint32_t kRowTile = 128, kColTile = 256;  // the GEMM kernel's output tile
 constexpr uint32_t kMaxCapture = 1024;              // captured rows (forward replay)
-constexpr uint32_t kMaxPairs = 64;                  // captured rows and columns (weight-gradient replay)
+constexpr uint32_t kMaxPairs = 64;                  // captured rows and columns (the pairs replays)
 
 // idx[0 .. min(total, cap)) = the positions of the non-zero flags in increasing order; *count = total.
 // One block of 1024 threads, each over a contiguous run of the flags, an exclusive scan of the runs'
@@ -92,16 +92,17 @@ __global__ void __launch_bounds__(256) capture_cols_kernel(const uint16_t *__res
     dst[(uint64_t)c * rows + i] = src[(uint64_t)i * ld + idx[c]];
 }
 
-// staged[r * 128 + idx[r] % 128][0 .. K) = rows[r][0 .. K) for r < min(count, cap) (the rest of
-// staged is zero): each captured row of A at its own lane of its own tile.
+// staged[r * tile + idx[r] % tile][0 .. K) = rows[r][0 .. K) for r < min(count, cap) (the rest of
+// staged is zero): each captured row of A at its own lane of its own 128-row tile (tile = 128), or
+// each captured row of W at its own column of its own 256-column tile of the product (tile = 256).
 __global__ void __launch_bounds__(256) stage_rows_kernel(const __nv_bfloat16 *__restrict__ rows, uint32_t K,
                                                          const uint32_t *__restrict__ idx,
                                                          const uint32_t *__restrict__ count, uint32_t cap,
-                                                         __nv_bfloat16 *__restrict__ staged) {
+                                                         uint32_t tile, __nv_bfloat16 *__restrict__ staged) {
     const uint32_t r = blockIdx.x;
     if (r >= min(*count, cap)) return;
     const uint4 *s = (const uint4 *)(rows + (uint64_t)r * K);
-    uint4 *d = (uint4 *)(staged + ((uint64_t)r * kRowTile + idx[r] % kRowTile) * K);
+    uint4 *d = (uint4 *)(staged + ((uint64_t)r * tile + idx[r] % tile) * K);
     for (uint32_t v = threadIdx.x; v < K / 8; v += blockDim.x) d[v] = s[v];
 }
 
@@ -189,6 +190,26 @@ ReplayWs replay_ws(uint32_t cap, uint32_t N, uint32_t K) {
     w.aborted = w.rowsum + round_up256(M * 8);
     w.gemm = w.aborted + 256;
     w.gemm_bytes = sdc_abft_workspace_size((uint32_t)M, N, K);
+    w.total = w.gemm + round_up256(w.gemm_bytes);
+    return w;
+}
+
+// Forward pairs replay workspace: staged A rows [cap_r * 128][K] | staged W rows [cap_c * 256][K] |
+// replayed C [cap_r * 128][cap_c * 256] | row checksums [cap_r * 128] double | aborted word | the GEMM's
+// workspace.
+struct ReplayPairsWs {
+    size_t sa, sw, out, rowsum, aborted, gemm, gemm_bytes, total;
+};
+ReplayPairsWs replay_pairs_ws(uint32_t K, uint32_t cap_r, uint32_t cap_c) {
+    ReplayPairsWs w;
+    const size_t m = (size_t)cap_r * kRowTile, n = (size_t)cap_c * kColTile;
+    w.sa = 0;
+    w.sw = round_up256(m * K * 2);
+    w.out = w.sw + round_up256(n * K * 2);
+    w.rowsum = w.out + round_up256(m * n * 2);
+    w.aborted = w.rowsum + round_up256(m * 8);
+    w.gemm = w.aborted + 256;
+    w.gemm_bytes = sdc_abft_workspace_size((uint32_t)m, (uint32_t)n, K);
     w.total = w.gemm + round_up256(w.gemm_bytes);
     return w;
 }
@@ -363,7 +384,7 @@ sdc_status sdc_abft_replay(const void *d_W, uint32_t N, uint32_t K, uint32_t cap
     if (e == cudaSuccess) e = cudaMemsetAsync(d_summary, 0, 8, s);
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_replay setup");
     stage_rows_kernel<<<cap_rows, 256, 0, s>>>((const __nv_bfloat16 *)d_row_A, K, d_row_idx, d_counts, cap_rows,
-                                               (__nv_bfloat16 *)(ws + w.staged));
+                                               kRowTile, (__nv_bfloat16 *)(ws + w.staged));
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_replay launch");
     st = sdc_abft_gemm(ws + w.staged, d_W, ws + w.out, M, N, K, (double *)(ws + w.rowsum), nullptr,
@@ -433,6 +454,69 @@ sdc_status sdc_abft_replay_wgrad(uint32_t T, uint32_t N, uint32_t K, uint32_t ca
     copy_word_kernel<<<1, 1, 0, s>>>((const uint32_t *)(ws + w.aborted), d_summary + 1);
     e = cudaGetLastError();
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_abft_replay_wgrad launch");
+}
+
+size_t sdc_abft_replay_pairs_workspace_size(uint32_t K, uint32_t cap_rows, uint32_t cap_cols) {
+    if (K == 0 || K % 8 || K > (1u << 20) || cap_rows == 0 || cap_cols == 0 || cap_rows > kMaxPairs ||
+        cap_cols > kMaxPairs)
+        return 0;
+    return replay_pairs_ws(K, cap_rows, cap_cols).total;
+}
+
+sdc_status sdc_abft_replay_pairs(uint32_t M, uint32_t N, uint32_t K, uint32_t cap_rows, uint32_t cap_cols,
+                                 const uint32_t *d_row_idx, const void *d_row_A, const void *d_row_C,
+                                 const uint32_t *d_col_idx, const void *d_col_W, const void *d_col_C,
+                                 const uint32_t *d_counts, uint8_t *d_differs, uint32_t *d_summary, void *d_ws,
+                                 size_t ws_bytes, sdc_stream_t stream) {
+    if (!d_row_idx || !d_row_A || !d_row_C || !d_col_idx || !d_col_W || !d_col_C || !d_counts || !d_differs ||
+        !d_summary || !d_ws)
+        return fail(SDC_ERR_NULL, "NULL argument");
+    if (M == 0 || N == 0 || K == 0 || N % 8 || K % 8 || K > (1u << 20) || cap_rows == 0 || cap_cols == 0 ||
+        cap_rows > kMaxPairs || cap_cols > kMaxPairs)
+        return fail(SDC_ERR_BAD_ARG, "M positive, N and K multiples of 8, K <= 2^20, cap_rows and cap_cols in 1..64");
+    const ReplayPairsWs w = replay_pairs_ws(K, cap_rows, cap_cols);
+    if (ws_bytes < w.total) return fail(SDC_ERR_WS_TOO_SMALL, "workspace smaller than sdc_abft_replay_pairs_workspace_size");
+    if ((uint64_t)d_ws & 255u) return fail(SDC_ERR_BAD_POINTER, "workspace is not 256-byte aligned");
+    if (((uint64_t)d_row_A | (uint64_t)d_col_W) & 15u) return fail(SDC_ERR_BAD_POINTER, "row buffers must be 16-byte aligned");
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    sdc_status st = check_spans({{d_row_idx, (uint64_t)cap_rows * 4, "d_row_idx"},
+                                 {d_row_A, (uint64_t)cap_rows * K * 2, "d_row_A"},
+                                 {d_row_C, (uint64_t)cap_rows * N * 2, "d_row_C"},
+                                 {d_col_idx, (uint64_t)cap_cols * 4, "d_col_idx"},
+                                 {d_col_W, (uint64_t)cap_cols * K * 2, "d_col_W"},
+                                 {d_col_C, (uint64_t)cap_cols * M * 2, "d_col_C"},
+                                 {d_counts, 8, "d_counts"},
+                                 {d_differs, (uint64_t)cap_rows * cap_cols, "d_differs"},
+                                 {d_summary, 8, "d_summary"},
+                                 {d_ws, w.total, "d_ws"}},
+                                dev);
+    if (st != SDC_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    char *ws = (char *)d_ws;
+    const uint32_t m = cap_rows * kRowTile, n = cap_cols * kColTile;
+    e = cudaMemsetAsync(ws + w.sa, 0, w.out - w.sa, s);  // both staged operands
+    if (e == cudaSuccess) e = cudaMemsetAsync(d_summary, 0, 8, s);
+    if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_replay_pairs setup");
+    // row i of A at lane i mod 128 of tile r, row j of W (B's column j) at column j mod 256 of tile c
+    stage_rows_kernel<<<cap_rows, 256, 0, s>>>((const __nv_bfloat16 *)d_row_A, K, d_row_idx, d_counts, cap_rows,
+                                               kRowTile, (__nv_bfloat16 *)(ws + w.sa));
+    stage_rows_kernel<<<cap_cols, 256, 0, s>>>((const __nv_bfloat16 *)d_col_W, K, d_col_idx, d_counts + 1, cap_cols,
+                                               kColTile, (__nv_bfloat16 *)(ws + w.sw));
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_replay_pairs launch");
+    st = sdc_abft_gemm(ws + w.sa, ws + w.sw, ws + w.out, m, n, K, (double *)(ws + w.rowsum), nullptr,
+                       (uint32_t *)(ws + w.aborted), ws + w.gemm, w.gemm_bytes, stream);
+    if (st != SDC_OK) return st;
+    // the output at (row i, column j): row r's element j (d_row_C [cap_r][N]) and column c's element i
+    // (d_col_C [cap_c][M]), the layouts the weight-gradient pairs have with N, K in place of M, N
+    compare_pairs_kernel<<<(cap_rows * cap_cols + 255) / 256, 256, 0, s>>>(
+        (const uint16_t *)(ws + w.out), cap_rows, cap_cols, M, N, d_row_idx, (const uint16_t *)d_row_C, d_col_idx,
+        (const uint16_t *)d_col_C, d_counts, d_differs, d_summary);
+    copy_word_kernel<<<1, 1, 0, s>>>((const uint32_t *)(ws + w.aborted), d_summary + 1);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_abft_replay_pairs launch");
 }
 
 }  // extern "C"

@@ -163,6 +163,15 @@ def test_host_validation_without_gpu(sdc):
         with pytest.raises(sdc.SdcError) as ei:
             sdc.sdc_abft_replay_wgrad(T, 256, 64, cr, cc, *[4096 * (i + 1) for i in range(10)], 1 << 20, 0)
         assert ei.value.status == 9, (T, cr, cc)
+    for K, cr, cc in [(0, 4, 4), (60, 4, 4), (64, 0, 4), (64, 4, 65)]:
+        assert sdc.sdc_abft_replay_pairs_workspace_size(K, cr, cc) == 0
+        with pytest.raises(sdc.SdcError) as ei:
+            sdc.sdc_abft_replay_pairs(128, 256, K, cr, cc, *[4096 * (i + 1) for i in range(10)], 1 << 20, 0)
+        assert ei.value.status == 9, (K, cr, cc)
+    # staged A rows (cap_r x 128 of K) and W rows (cap_c x 256 of K), the replayed C, its row checksums, the
+    # abort word, a GEMM's workspace
+    assert sdc.sdc_abft_replay_pairs_workspace_size(64, 1, 1) == (128 * 64 * 2 + 256 * 64 * 2 + 128 * 256 * 2
+                                                                  + 1024 + 256 + sdc.sdc_abft_workspace_size(128, 256, 64))
     # staged rows (cap x 128 rows of K and of N bf16), their row checksums, the abort word, a GEMM's workspace
     assert sdc.sdc_abft_replay_workspace_size(1, 256, 64) == (128 * 64 * 2 + 128 * 256 * 2 + 1024 + 256
                                                               + sdc.sdc_abft_workspace_size(128, 256, 64))

@@ -160,3 +160,43 @@ def test_wgrad_fault_capture_and_replay_confirm(sdc):
     assert np.all(got[:1][want == 1] == 1) and want.sum() >= 4
     assert np.all(got[1:] == 0)  # past the captured rows
     assert int(summ[0]) == int(got.sum()) and int(summ[1]) == 0
+
+
+def test_forward_clean_pairs_replay_bit_for_bit(sdc):
+    # the row + column configuration: (row, column) outputs of a correct product, at the tile edges and
+    # in the ragged last tiles, recomputed from the captured A rows and W rows alone
+    M, N, K = 1000, 776, 1000
+    ops = W.gemm_operands(M, N, K, DEV, seed=48)
+    A, Wt = ops["A"], ops["W"]
+    g = sdc.AbftGemm(M, N, K, DEV, columns=True)
+    g(A, Wt)
+    rows, cols = [0, 127, 128, 999], [0, 255, 256, 775]
+    cap = g.capture(A, Wt, cap_rows=4, cap_cols=4, flag=_flags(M, rows), flag_col=_flags(N, cols))
+    differs, summ = g.replay_pairs(cap)
+    torch.cuda.synchronize()
+    ref = oracle.abft_capture(np.isin(np.arange(M), rows), np.isin(np.arange(N), cols), _bits(A), _bits(Wt),
+                              _bits(g.C), 4, 4)
+    assert differs.cpu().numpy().tolist() == [[0] * 4] * 4 and summ.cpu().tolist() == [0, 0]
+    assert np.all(oracle.abft_replay_pairs(ref) == 0)
+
+
+def test_forward_fault_pairs_replay_confirm(sdc):
+    # the product reads a W with one element of two chosen rows corrupted, the check the clean W: the
+    # corrupted rows of W are flagged columns of C; every captured (row, column) pair whose saved
+    # output the oracle finds inconsistent with the captured clean operands fails to reproduce
+    M, N, K = 512, 1024, 1024
+    ops = W.gemm_operands(M, N, K, DEV, seed=49)
+    A, Wt = ops["A"], ops["W"]
+    Wf, where = W.gemm_fault(Wt, [100, 700], seed=50, mask=0x4000)
+    g = sdc.AbftGemm(M, N, K, DEV, columns=True)
+    g.gemm(A, Wf)
+    g.verify(A, Wt)
+    cap = g.capture(A, Wt, cap_rows=4, cap_cols=2)
+    differs, summ = g.replay_pairs(cap)
+    torch.cuda.synchronize()
+    ref = oracle.abft_capture(g.flag.cpu().numpy(), g.flag_col.cpu().numpy(), _bits(A), _bits(Wt), _bits(g.C), 4, 2)
+    assert ref["n_cols"] >= 1 and set(ref["col_idx"].tolist()) <= {100, 700}
+    want = oracle.abft_replay_pairs(ref)
+    got = differs.cpu().numpy()[:len(ref["row_idx"]), :len(ref["col_idx"])]
+    assert np.all(got[want == 1] == 1) and want.sum() >= 1
+    assert int(summ[0]) == int(differs.sum()) and int(summ[1]) == 0

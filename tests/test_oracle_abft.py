@@ -377,3 +377,13 @@ def test_wgrad_replay_pairs_flags_only_the_planted_element():
                                np.array([0, 0, 0, 1, 0, 0, 0, 0, 0, 1, 0, 0], np.uint8),
                                dYb, Xb, _bf16_bits(dW), cap_rows=2, cap_cols=2)
     assert oracle.wgrad_replay_pairs(cap).tolist() == [[0, 0], [1, 0]]
+
+
+def test_forward_replay_pairs_flags_only_the_planted_element():
+    M, N, K = 9, 12, 10
+    A, W, Ab, Wb = _int_operands(M, N, K, 34, lo=-4, hi=4)
+    C = (A @ W.T).astype(np.float32)
+    C[2, 7] += 64.0
+    cap = oracle.abft_capture(np.isin(np.arange(M), [2, 5]), np.isin(np.arange(N), [3, 7]), Ab, Wb, _bf16_bits(C),
+                              cap_rows=2, cap_cols=2)
+    assert oracle.abft_replay_pairs(cap).tolist() == [[0, 1], [0, 0]]
