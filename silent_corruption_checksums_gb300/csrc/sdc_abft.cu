@@ -465,6 +465,8 @@ struct SlabSide {
     float2 *split;   // unweighted: the output
     uint32_t *done;  // a counter per column block
     ColCheck o;      // weighted: the check
+    uint32_t keep = 1;    // 0: X is read once here, and its lines are the first the L2 gives up
+    uint32_t planar = 0;  // unweighted: split[] in the check's planar layout instead of {h, m} per column
 };
 
 template <bool kWeighted>
@@ -482,6 +484,7 @@ __global__ void __launch_bounds__(256, 3) abft_colsum_slab_kernel(const SlabSide
     __shared__ float4 part[8][256];
     __shared__ uint32_t last;
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+    const uint64_t policy = l2_policy(!(second ? s1.keep : s0.keep));
     const uint32_t k = bx * 256 + lane * 8;
     const uint32_t j0 = (uint32_t)((uint64_t)by * rows / n_slabs),
                    j1 = (uint32_t)((uint64_t)(by + 1) * rows / n_slabs);
@@ -529,14 +532,14 @@ __global__ void __launch_bounds__(256, 3) abft_colsum_slab_kernel(const SlabSide
                     if (j + 8 * u < j1) prefetch_l2(X + (uint64_t)(j + 8 * u) * K + k);
             }
 #pragma unroll
-            for (uint32_t u = 0; u < kChain; ++u) v[u] = ld_stream(X + (uint64_t)(j + 8 * u) * K + k);
+            for (uint32_t u = 0; u < kChain; ++u) v[u] = ld_stream_hint(X + (uint64_t)(j + 8 * u) * K + k, policy);
             add_rows(v, kChain, j);
         }
         if (j < j1) {  // fewer than kChain rows left
             const uint32_t n = (j1 - j + 7) / 8;
 #pragma unroll
             for (uint32_t u = 0; u < kChain; ++u)
-                v[u] = u < n ? ld_stream(X + (uint64_t)(j + 8 * u) * K + k) : make_uint4(0, 0, 0, 0);
+                v[u] = u < n ? ld_stream_hint(X + (uint64_t)(j + 8 * u) * K + k, policy) : make_uint4(0, 0, 0, 0);
             add_rows(v, n, j);
         }
     }
@@ -609,7 +612,10 @@ __global__ void __launch_bounds__(256, 3) abft_colsum_slab_kernel(const SlabSide
             float h = 0.0f, l = 0.0f;  // renormalise: TwoSum of the two parts
             pair_add(h, l, acc.x);
             pair_add(h, l, acc.y);
-            split[kk] = make_float2(__fadd_rn(h, l), __fadd_rn(acc.z, acc.w));
+            const float2 hm = make_float2(__fadd_rn(h, l), __fadd_rn(acc.z, acc.w));
+            const bool planar = second ? s1.planar : s0.planar;
+            // planar: plane (kk mod 8) / 2 of vector kk / 8, half kk mod 2 (float2 units)
+            split[planar ? ((kk & 7u) >> 1) * (K / 4) + (kk >> 3) * 2 + (kk & 1u) : kk] = hm;
         }
     }
     if (threadIdx.x == 0) done[bx] = 0u;  // ready for the next call
@@ -620,11 +626,14 @@ __global__ void __launch_bounds__(256, 3) abft_colsum_slab_kernel(const SlabSide
 // float32 pair with TwoSum) and m = sum_k |X[t, k]| in plain float32 (its chain: a lane's
 // 4 ceil(n / 256) terms, then 6 merges).  One warp per row, the lanes over the row's vectors in
 // turn with 8 loads in flight; the lanes' sums meet in a fixed butterfly and lane 0 writes.
-// blockIdx.y picks the matrix: (X0, n0, out0) or (X1, n1, out1), both with T rows.
+// blockIdx.y picks the matrix: (X0, n0, out0) or (X1, n1, out1), both with T rows.  Matrix i's
+// lines are the first the L2 gives up when bit i of read_once is set (it is not read again soon).
 __global__ void __launch_bounds__(256) abft_rowsum_kernel(const __nv_bfloat16 *__restrict__ X0, uint32_t n0,
                                                           float2 *__restrict__ out0, const __nv_bfloat16 *__restrict__ X1,
-                                                          uint32_t n1, float2 *__restrict__ out1, uint32_t T) {
+                                                          uint32_t n1, float2 *__restrict__ out1, uint32_t T,
+                                                          uint32_t read_once) {
     const bool second = blockIdx.y != 0;
+    const uint64_t policy = l2_policy((read_once >> (second ? 1 : 0)) & 1u);
     const __nv_bfloat16 *__restrict__ X = second ? X1 : X0;
     const uint32_t n = second ? n1 : n0;
     float2 *__restrict__ out = second ? out1 : out0;
@@ -648,11 +657,11 @@ __global__ void __launch_bounds__(256) abft_rowsum_kernel(const __nv_bfloat16 *_
     for (; v + 32 * 7 < nv; v += 32 * 8) {
         uint4 q[8];
 #pragma unroll
-        for (uint32_t u = 0; u < 8; ++u) q[u] = ld_stream(x + v + 32 * u);
+        for (uint32_t u = 0; u < 8; ++u) q[u] = ld_stream_hint(x + v + 32 * u, policy);
 #pragma unroll
         for (uint32_t u = 0; u < 8; ++u) add(q[u]);
     }
-    for (; v < nv; v += 32) add(ld_stream(x + v));
+    for (; v < nv; v += 32) add(ld_stream_hint(x + v, policy));
     float s0, s1, c0, c1, a0, a1;
     f2_unpack(s, s0, s1);
     f2_unpack(c, c0, c1);
@@ -673,21 +682,22 @@ __global__ void __launch_bounds__(256) abft_rowsum_kernel(const __nv_bfloat16 *_
 }
 
 // The check of X [n_rows][K] (A for the row check, W for the column check)
-// against split[] = {h, m} (the other operand's column sums), one K split per
-// block: part[y][i] = {s, c, m, 0} with s + c = sum_k X[i, k] h_k over split y's
+// against the other operand's column sums {h, m}, one K split per block:
+// part[y][i] = {s, c, m, 0} with s + c = sum_k X[i, k] h_k over split y's
 // columns (8-term chains folded into a float32 pair), and
 // m = sum_k |X[i, k]| m_k in plain float32.  Block = 4 warps over 32 rows; a
-// warp holds 4 packed row pairs, 8 lanes per pair.  The 8 lanes of a group read
-// a whole 128-byte line of each of their two rows per vector step (lane j takes
-// the split's vectors j, j + 8, ...) and the 512 contiguous bytes of those
-// vectors' column sums, which the warp's 4 groups share through L1; their sums
-// meet in 3 butterfly steps.  The block starts a bulk L2 prefetch of its 32
-// rows' segments first.  The last split block of a row block (a counter per
-// row block) merges the row block's partials in split order (the same result
-// whichever block is last) and writes, per row: the reference ref = s + c, the
-// magnitude raised by (1 + delta) to an upper bound, the bound over n_sum
-// summed outputs, the residual against the accumulator checksum and the flag
-// (a NaN residual flags).
+// warp holds its 8 rows as 4 packed row pairs in every lane, and its 32 lanes
+// take the split's vectors lane, lane + 32, ...: each load of a row reads 512
+// contiguous bytes, and the column sums come in the planar layout (plane q of
+// vector v = {h, m} of columns 8v + 2q and 8v + 2q + 1, 16 bytes, planes
+// [4][K / 8]), so that each of their loads reads 512 contiguous bytes too and
+// serves 8 rows.  The lanes' sums meet in 5 butterfly steps.  The last split
+// block of a row block (a counter per row block) merges the row block's
+// partials in split order (the same result whichever block is last) and
+// writes, per row: the reference ref = s + c, the magnitude raised by
+// (1 + delta) to an upper bound, the bound over n_sum summed outputs, the
+// residual against the accumulator checksum and the flag (a NaN residual
+// flags).
 constexpr uint32_t kChkRows = 32;  // rows per block of the check
 
 struct CheckOut {
@@ -701,23 +711,22 @@ struct CheckOut {
     uint32_t n_sum, n_splits;
 };
 
-// 8 columns of two rows (packed) against the column sums hm[0..7] = {h, m}: an
-// 8-term fused multiply-add chain folded into the pair (rs, rc) with TwoSum,
-// and the magnitude's plain chain m.
-__device__ __forceinline__ void check_vec(const uint4 &a0, const uint4 &a1, const float2 *hm, uint64_t &rs,
+// 8 columns of two rows (packed) against their column sums (the four planes
+// w[q] = {h, m, h, m} of columns 2q and 2q + 1): an 8-term fused multiply-add
+// chain folded into the pair (rs, rc) with TwoSum, and the magnitude's plain
+// chain m.
+__device__ __forceinline__ void check_vec(const uint4 &a0, const uint4 &a1, const uint4 (&w)[4], uint64_t &rs,
                                           uint64_t &rc, uint64_t &m) {
-    const uint4 *p = (const uint4 *)hm;  // {h, m, h, m} of two columns per 16 bytes
     uint64_t t = 0ull;
 #pragma unroll
     for (int qq = 0; qq < 4; ++qq) {
-        const uint4 w = __ldg(p + qq);
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int q = 2 * qq + e;
             const uint32_t w0 = (&a0.x)[q >> 1], w1 = (&a1.x)[q >> 1];
             const uint64_t a2 = (q & 1) ? f2_pack_bits(w0 & 0xFFFF0000u, w1 & 0xFFFF0000u)
                                         : f2_pack_bits(w0 << 16, w1 << 16);
-            const uint32_t h = e ? w.z : w.x, mm = e ? w.w : w.y;
+            const uint32_t h = e ? w[qq].z : w[qq].x, mm = e ? w[qq].w : w[qq].y;
             t = f2_fma(a2, f2_pack_bits(h, h), t);
             m = f2_fma(a2 & kF2Abs, f2_pack_bits(mm, mm), m);
         }
@@ -747,50 +756,46 @@ __global__ void __launch_bounds__(128) abft_check_kernel(const CheckSide side0, 
     if (by >= o.n_splits) return;  // the whole block
     __shared__ uint32_t last;
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
-    const uint32_t v0 = by * vec_per_split, v1 = min(K / 8, v0 + vec_per_split), nv = v1 > v0 ? v1 - v0 : 0;
+    const uint32_t v0 = by * vec_per_split, v1 = min(K / 8, v0 + vec_per_split);
     const uint32_t row0 = bx * kChkRows;
-    if (tid < kChkRows && row0 + tid < n_rows && nv)  // this block's segment of each of its rows into L2
-        prefetch_l2_bulk(X + (uint64_t)(row0 + tid) * K + (uint64_t)v0 * 8, nv * 16u);
     // Launched as a dependent of the column sums: their grid has completed (and its writes are
-    // visible) once this returns.  The prefetch above overlaps the grid's tail.  Without a dependent
-    // launch a no-op.
+    // visible) once this returns.  Without a dependent launch a no-op.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const float2 *hm = split + (uint64_t)v0 * 8;
-    const uint32_t g = lane >> 3, j = lane & 7u;
-    const uint32_t r = row0 + warp * 8 + g * 2;  // this group's rows r, r + 1
-    const bool ok0 = r < n_rows, ok1 = r + 1 < n_rows;
-    const uint4 *x0 = (const uint4 *)(X + (uint64_t)(ok0 ? r : 0) * K) + v0;
-    const uint4 *x1 = (const uint4 *)(X + (uint64_t)(ok1 ? r + 1 : 0) * K) + v0;
-    uint64_t rs = 0ull, rc = 0ull, m = 0ull;
-    uint32_t v = j;
-    for (; v + 8 < nv; v += 16) {  // two vector steps in flight
-        const uint4 a0 = ok0 ? ld_stream(x0 + v) : make_uint4(0, 0, 0, 0);
-        const uint4 a1 = ok1 ? ld_stream(x1 + v) : make_uint4(0, 0, 0, 0);
-        const uint4 b0 = ok0 ? ld_stream(x0 + v + 8) : make_uint4(0, 0, 0, 0);
-        const uint4 b1 = ok1 ? ld_stream(x1 + v + 8) : make_uint4(0, 0, 0, 0);
-        check_vec(a0, a1, hm + 8 * v, rs, rc, m);
-        check_vec(b0, b1, hm + 8 * (v + 8), rs, rc, m);
-    }
-    if (v < nv) {
-        const uint4 a0 = ok0 ? ld_stream(x0 + v) : make_uint4(0, 0, 0, 0);
-        const uint4 a1 = ok1 ? ld_stream(x1 + v) : make_uint4(0, 0, 0, 0);
-        check_vec(a0, a1, hm + 8 * v, rs, rc, m);
-    }
-    float s0, s1, c0, c1, m0, m1;
-    f2_unpack(rs, s0, s1);
-    f2_unpack(rc, c0, c1);
-    f2_unpack(m, m0, m1);
+    const uint4 *planes = (const uint4 *)split;  // [4][K / 8]
+    const uint32_t nvk = K / 8, r0 = row0 + warp * 8;  // this warp's rows r0 .. r0 + 7
+    const __nv_bfloat16 *xw = X + (uint64_t)r0 * K;
+    uint64_t rs[4], rc[4], m[4];
 #pragma unroll
-    for (int off = 4; off > 0; off >>= 1) {  // the group's 8 lanes, a fixed butterfly
-        pair_merge(s0, c0, __shfl_xor_sync(0xffffffffu, s0, off), __shfl_xor_sync(0xffffffffu, c0, off));
-        pair_merge(s1, c1, __shfl_xor_sync(0xffffffffu, s1, off), __shfl_xor_sync(0xffffffffu, c1, off));
-        m0 = __fadd_rn(m0, __shfl_xor_sync(0xffffffffu, m0, off));
-        m1 = __fadd_rn(m1, __shfl_xor_sync(0xffffffffu, m1, off));
+    for (int p = 0; p < 4; ++p) rs[p] = rc[p] = m[p] = 0ull;
+    for (uint32_t v = v0 + lane; v < v1; v += 32) {
+        uint4 a[8], w[4];
+#pragma unroll
+        for (uint32_t rr = 0; rr < 8; ++rr)
+            a[rr] = r0 + rr < n_rows ? ld_stream((const uint4 *)(xw + (uint64_t)rr * K) + v) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (uint32_t q = 0; q < 4; ++q) w[q] = __ldg(planes + (uint64_t)q * nvk + v);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) check_vec(a[2 * p], a[2 * p + 1], w, rs[p], rc[p], m[p]);
     }
-    if (j == 0) {
-        float4 *dst = part + (uint64_t)by * n_rows;
-        if (ok0) dst[r] = make_float4(s0, c0, m0, 0.0f);
-        if (ok1) dst[r + 1] = make_float4(s1, c1, m1, 0.0f);
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        float s0, s1, c0, c1, m0, m1;
+        f2_unpack(rs[p], s0, s1);
+        f2_unpack(rc[p], c0, c1);
+        f2_unpack(m[p], m0, m1);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {  // the warp's 32 lanes, a fixed butterfly
+            pair_merge(s0, c0, __shfl_xor_sync(0xffffffffu, s0, off), __shfl_xor_sync(0xffffffffu, c0, off));
+            pair_merge(s1, c1, __shfl_xor_sync(0xffffffffu, s1, off), __shfl_xor_sync(0xffffffffu, c1, off));
+            m0 = __fadd_rn(m0, __shfl_xor_sync(0xffffffffu, m0, off));
+            m1 = __fadd_rn(m1, __shfl_xor_sync(0xffffffffu, m1, off));
+        }
+        const uint32_t r = r0 + 2 * p;
+        if (lane == (uint32_t)p) {
+            float4 *dst = part + (uint64_t)by * n_rows;
+            if (r < n_rows) dst[r] = make_float4(s0, c0, m0, 0.0f);
+            if (r + 1 < n_rows) dst[r + 1] = make_float4(s1, c1, m1, 0.0f);
+        }
     }
     __syncthreads();
     if (tid == 0) {
@@ -879,27 +884,30 @@ uint32_t n_slabs_for(uint32_t rows, uint32_t K) {
     return n < 1 ? 1 : n;
 }
 
-// K splits of the check of `rows` rows: enough blocks of kChkRows rows for
-// about three waves of 16 blocks on each of 152 SMs, with at least 16 vectors
-// per lane and split.  A function of the shapes only, so the workspace size is
-// too.
+// K splits of the check of `rows` rows: as many as one wave of its blocks of
+// kChkRows rows holds (6 resident per SM on 152 SMs), with at least 128 vectors
+// (4 per lane) per split.  A function of the shapes only, so the workspace size
+// is too.
 uint32_t n_splits_for(uint32_t rows, uint32_t K) {
     const uint32_t nvec = K / 8, row_blocks = (rows + kChkRows - 1) / kChkRows;
-    uint32_t n = (3u * 16u * 152u + row_blocks - 1) / row_blocks;
-    const uint32_t most = nvec / 128 > 0 ? nvec / 128 : 1;  // 16 vectors per lane
+    const uint32_t n = 6u * 152u / row_blocks;
+    const uint32_t most = nvec / 128 > 0 ? nvec / 128 : 1;
     return n > most ? most : (n < 1 ? 1 : n);
 }
 
 // The plain float32 chains behind the magnitude, for its raise factor: the
 // longest run of rows one warp sums in a column-sum slab, and the longest run
-// of columns one lane group sums in a check split.
-double mag_delta(uint32_t rows_summed, uint32_t K, uint32_t n_slabs, uint32_t n_splits) {
+// of columns one lane sums in a check split (8 per vector, the split's vps
+// vectors dealt to 32 lanes) with the 5 butterfly steps after it.
+double mag_delta(uint32_t rows_summed, uint32_t n_slabs, uint32_t vps, uint32_t n_splits) {
     const uint32_t slab_rows = (rows_summed + n_slabs - 1) / n_slabs;
     const double l1 = (double)((slab_rows + 7) / 8);
-    const uint32_t vps = (K / 8 + n_splits - 1) / n_splits;
-    const double l2 = (double)((vps + 7) / 8) * 8.0;
+    const double l2 = 8.0 * (double)((vps + 31) / 32) + 5.0;
     return 2.0 * (l1 + l2 + (double)n_splits + 8.0) * 0x1p-24;
 }
+
+// Bytes of an operand the verifier keeps in L2 between its two launches: about half the 126 MiB L2.
+constexpr uint64_t kKeepL2 = 64ull << 20;
 
 // Workspace: row partials [ceil(N/256)][M] | column partials [ceil(M/128)][N] | W's column sums wsplit [K] |
 // A's, asplit [K] | slabs [n_slabs(N, K) + n_slabs(M, K)][K] (W's, then A's) | the check's split
@@ -1073,8 +1081,15 @@ sdc_status sdc_abft_verify(const void *d_A, const void *d_W, uint32_t M, uint32_
     const uint32_t vps_a = vps_for(M), nsp_a = (K / 8 + vps_a - 1) / vps_a;
     const uint32_t vps_w = vps_for(N), nsp_w = (K / 8 + vps_w - 1) / vps_w;
     const uint32_t rb_a = (M + kChkRows - 1) / kChkRows, rb_w = (N + kChkRows - 1) / kChkRows;
-    const SlabSide sw{(const __nv_bfloat16 *)d_W, N, K, ns_w, slabs, wsplit, done, ColCheck{}};
-    const SlabSide sa{(const __nv_bfloat16 *)d_A, M, K, ns_a, slabs + (size_t)ns_w * K, asplit, done + cb, ColCheck{}};
+    SlabSide sw{(const __nv_bfloat16 *)d_W, N, K, ns_w, slabs, wsplit, done, ColCheck{}};
+    SlabSide sa{(const __nv_bfloat16 *)d_A, M, K, ns_a, slabs + (size_t)ns_w * K, asplit, done + cb, ColCheck{}};
+    sw.planar = sa.planar = 1;  // the layout the check reads
+    // L2 use: rows only, the column sums read W once (its lines leave L2 first, so that they do not
+    // push out lines the check's A rows may still find).  Rows and columns: the check re-reads both
+    // operands; the smaller keeps its lines if it fits in about half the L2, the other leaves first.
+    const uint64_t a_bytes = (uint64_t)M * K * 2, w_bytes = (uint64_t)N * K * 2;
+    sw.keep = cols && w_bytes < a_bytes && w_bytes <= kKeepL2;
+    sa.keep = cols && !sw.keep && a_bytes <= kKeepL2;
     e = cudaMemsetAsync(done, 0, done_bytes, s);
     if (e == cudaSuccess) {
         abft_colsum_slab_kernel<false><<<dim3(cols ? 2 * cb : cb, cols && ns_a > ns_w ? ns_a : ns_w), 256, 0, s>>>(
@@ -1088,10 +1103,10 @@ sdc_status sdc_abft_verify(const void *d_A, const void *d_W, uint32_t M, uint32_
         uint32_t *cdone = done + 2 * cb;
         const CheckSide ca{(const __nv_bfloat16 *)d_A, M, K, vps_a, wsplit, chk,
                            CheckOut{d_rowsum, d_residual, d_bound, d_flag, &d_summary->n_flagged, cdone,
-                                    mag_delta(N, K, ns_w, nsp_a), tol_scale, N, nsp_a}};
+                                    mag_delta(N, ns_w, vps_a, nsp_a), tol_scale, N, nsp_a}};
         const CheckSide cw{(const __nv_bfloat16 *)d_W, N, K, vps_w, asplit, chk + (size_t)nsp_a * M,
                            CheckOut{d_colsum, d_residual_col, d_bound_col, d_flag_col, &d_summary->n_flagged_cols,
-                                    cdone + rb_a, mag_delta(M, K, ns_a, nsp_w), tol_scale, M, nsp_w}};
+                                    cdone + rb_a, mag_delta(M, ns_a, vps_w, nsp_w), tol_scale, M, nsp_w}};
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(cols ? rb_a + rb_w : rb_a, cols && nsp_w > nsp_a ? nsp_w : nsp_a);
         cfg.blockDim = dim3(128);
@@ -1208,17 +1223,22 @@ sdc_status sdc_abft_verify_wgrad(const void *d_dY, const void *d_X, uint32_t T, 
     // Both sides at once, in two launches: X's row sums (the weights of dY's column sums: the rows of
     // dW, each checksum summing K outputs) and dY's (the weights of X's: the columns, each summing N),
     // then both weighted column sums, each compared in its last blocks with its checksums.
+    // L2 use: the second launch reads both operands again; X (the smaller) keeps its lines if it fits in
+    // about half the L2, dY's leave first, then and in the second launch, which reads it last.
+    const bool keep_x = (uint64_t)T * K * 2 <= kKeepL2;
     abft_rowsum_kernel<<<dim3((T + 7) / 8, cols ? 2 : 1), 256, 0, s>>>((const __nv_bfloat16 *)d_X, K, rsplit,
-                                                                      (const __nv_bfloat16 *)d_dY, N, qsplit, T);
+                                                                      (const __nv_bfloat16 *)d_dY, N, qsplit, T,
+                                                                      (keep_x ? 0u : 1u) | 2u);
     e = cudaMemsetAsync(done, 0, done_bytes, s);
     if (e == cudaSuccess) {
         const uint32_t cb_n = (N + 255) / 256, ns_n = n_slabs_for(T, N), ns_k = n_slabs_for(T, K);
-        const SlabSide sr{(const __nv_bfloat16 *)d_dY, T, N, ns_n, slabs, nullptr, done,
+        SlabSide sr{(const __nv_bfloat16 *)d_dY, T, N, ns_n, slabs, nullptr, done,
                           ColCheck{rsplit, d_rowsum, d_residual, d_bound, d_flag, &d_summary->n_flagged,
                                    wgrad_mag_delta(T, K, ns_n), tol_scale, K}};
         const SlabSide sc{(const __nv_bfloat16 *)d_X, T, K, ns_k, slabs + (size_t)ns_n * N, nullptr, done + cb_n,
                           ColCheck{qsplit, d_colsum, d_residual_col, d_bound_col, d_flag_col,
                                    &d_summary->n_flagged_cols, wgrad_mag_delta(T, N, ns_k), tol_scale, N}};
+        sr.keep = 0;
         abft_colsum_slab_kernel<true>
             <<<dim3(cols ? cb_n + (K + 255) / 256 : cb_n, cols && ns_k > ns_n ? ns_k : ns_n), 256, 0, s>>>(
                 sr, cols ? sc : sr, cb_n);

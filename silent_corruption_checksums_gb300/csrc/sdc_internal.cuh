@@ -169,6 +169,26 @@ __device__ __forceinline__ uint4 ld_stream(const void *p) {
     return r;
 }
 
+// L2 eviction policies for ld_stream_hint: evict_first for data read once
+// (its lines are the first the L2 gives up), evict_normal for data read again.
+__device__ __forceinline__ uint64_t l2_policy(bool read_once) {
+    uint64_t p;
+    if (read_once)
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    else
+        asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// ld_stream with an L2 eviction policy from l2_policy.
+__device__ __forceinline__ uint4 ld_stream_hint(const void *p, uint64_t policy) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p), "l"(policy));
+    return r;
+}
+
 // Bulk prefetch of [p, p + bytes) into L2 (p 16-byte aligned, bytes a
 // multiple of 16); no data is returned and no completion is tracked.
 __device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {

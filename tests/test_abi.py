@@ -113,7 +113,7 @@ def test_host_validation_without_gpu(sdc):
     # row partials (ceil(N/256) per row), column partials (ceil(M/128) per column), W's and A's column sums
     # (K x 8 bytes each: the sum and the magnitude in float32), slabs of K x 16 bytes for both column
     # sums (slabs = min(456 / ceil(K / 256), 64, rows / 8) each), both checks' split partials (16 bytes per
-    # row and split; one split when K / 8 < 64), the last-block counters (a word per 32-row block of both
+    # row and split; one split when K / 8 < 128), the last-block counters (a word per 32-row block of both
     # sides, or per 256 columns of both), the abort word; each rounded up to 256 bytes
     assert sdc.sdc_abft_workspace_size(128, 512, 64) == (2048 + 1 * 512 * 8 + 2 * 512 + (64 + 16) * 64 * 16
                                                          + (128 + 512) * 16 + 256 + 256)
