@@ -428,6 +428,22 @@ def _time_loop(fn, steps, stream, torch):
     return a.elapsed_time(b) / steps
 
 
+def _graph_of(fn, torch):
+    """fn's launches captured once in a CUDA graph (fn launches on the current stream; warmed up on a
+    side stream first, as capture requires)."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            fn()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
 def _time_calls_evicted(fn, steps, stream, torch):
     """Median CUDA-event time of fn, each call timed alone after a read pass over a 512 MiB buffer
     that is not one of its inputs: whatever the call left in the 126 MiB L2 is evicted, and no dirty
@@ -610,7 +626,8 @@ def bench_abft_row(args, dev, stream, peaks, sdc, W, torch) -> dict:
     g = sdc.AbftGemm(M, N, K, dev)
     reps = max(10, args.steps // 10)
     ms_gemm = _time_loop(lambda: g.gemm(A, Wt, stream=stream), reps, stream, torch)
-    # the verifier reads 185 MB: each call timed alone with the L2 emptied of its inputs before it
+    # the verifier reads 185 MB: each call timed alone with the L2 emptied of its inputs before it (and
+    # back to back beside it)
     ms_verify = _time_calls_evicted(lambda: g.verify(A, Wt, stream=stream), reps, stream, torch)
     ms_verify_b2b = _time_loop(lambda: g.verify(A, Wt, stream=stream), reps, stream, torch)
     gc = sdc.AbftGemm(M, N, K, dev, columns=True)  # the row + column configuration
@@ -820,7 +837,12 @@ def bench_xor_pairs_row(p, stream, peaks, sdc, torch, oracle) -> dict:
         xplan.xorsum(out=xo, stream=stream)
         sdc.xorsum_compare(xo[0], xo[1], stream=stream)
 
-    ms = _time_loop(xs_step, 20, stream, torch)
+    # the step's four launches (scan, output reset, combine, compare) replayed from a CUDA graph; the same
+    # launched on the stream one by one beside it
+    gx = _graph_of(lambda: (xplan.xorsum(out=xo), sdc.xorsum_compare(xo[0], xo[1])), torch)
+    ms = _time_loop(gx.replay, 20, stream, torch)
+    ms_stream = _time_loop(xs_step, 20, stream, torch)
+    del gx
     nbytes = sum(t.numel() * t.element_size() for t in p["orig"]) * 2
     ho, hr = [host_bits(t) for t in p["orig"]], [host_bits(t) for t in p["recomp"]]
 
@@ -829,7 +851,9 @@ def bench_xor_pairs_row(p, stream, peaks, sdc, torch, oracle) -> dict:
                               [oracle.xorsum(h, threads=threads) for h in hr])
 
     rows["xorsum_pairs_stress"] = {"workload": "1,000 (original, recomputed) pairs, sizes 1..1e6, half with a "
-                                   "one-bit difference: xorsum + compare", "ms": ms, "bytes": nbytes,
+                                   "one-bit difference: xorsum + compare", "ms": ms,
+                                   "launch": "the step's launches replayed from a CUDA graph",
+                                   "stream_launch_ms": ms_stream, "bytes": nbytes,
                                    "GB_s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"],
                                    "cpu_baseline": oracle_rate(oracle_pairs, nbytes, "all 1,000 pairs",
                                                                single=oracle_pairs, single_bytes=nbytes,

@@ -5,7 +5,8 @@ counters with memset nodes and launch persistent kernels (one over a banded tile
 schedule, one with a work queue): captured once and replayed, and run at the same time
 on two streams with their own workspaces, they give results bit-identical to eager
 calls on the same inputs, and a replay after an in-place change of an input reads
-the new values.
+the new values.  The same holds for the weight-gradient GEMM with its check and for a
+plan's xorsum with the pair compare (the launches the benchmark replays from graphs).
 """
 import pytest
 import torch
@@ -113,3 +114,50 @@ def test_two_streams_at_once(sdc):
     torch.cuda.synchronize()
     _same(_bits(_outs_gemm(g)), ref_g)
     _same(_bits(_outs_attn(a)), ref_a)
+
+
+def test_wgrad_check_and_xorsum_pairs_in_a_cuda_graph(sdc):
+    # the weight-gradient GEMM and its check, and a plan's xorsum with the pair compare, captured once:
+    # replays are bit-identical to eager calls, and read inputs changed in place
+    T, N, K = 1024, 512, 768
+    ops = W.wgrad_operands(T, N, K, DEV, seed=55)
+    rng_tensors = [W.gemm_operands(8, 8 * (i + 1), 64, DEV, seed=56 + i)["W"] for i in range(5)]  # [8 (i + 1), 64]
+    copies = [t.clone() for t in rng_tensors]
+    W.xor_element(copies[3], 17, 0x0100)
+    e = sdc.AbftWgrad(T, N, K, DEV)
+    e(ops["dY"], ops["X"])
+    ep = sdc.Plan([rng_tensors, copies])
+    ex = ep.xorsum()
+    em, ed = sdc.xorsum_compare(ex[0], ex[1])
+    torch.cuda.synchronize()
+    outs = lambda a: [a.dW, a.rowsum, a.colsum, a.residual, a.bound, a.flag, a.residual_col, a.bound_col,
+                      a.flag_col, a.summary, a.aborted]
+    ref = _bits(outs(e)) + _bits([ex, em, ed])
+    a = sdc.AbftWgrad(T, N, K, DEV)
+    plan = sdc.Plan([rng_tensors, copies])
+    xo = torch.empty((2, 5), dtype=torch.int64, device=DEV)
+    s = torch.cuda.Stream()
+    res = {}
+
+    def work():
+        a(ops["dY"], ops["X"], stream=s)
+        plan.xorsum(out=xo, stream=s)
+        res["m"], res["d"] = sdc.xorsum_compare(xo[0], xo[1], stream=s)
+
+    with torch.cuda.stream(s):
+        work()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        work()
+    for t in outs(a) + [xo]:
+        t.zero_()
+    for _ in range(2):
+        graph.replay()
+        torch.cuda.synchronize()
+        _same(_bits(outs(a)) + _bits([xo, res["m"], res["d"]]), ref)
+    assert int(res["m"].sum()) == 1 and int(res["m"][3]) == 1
+    W.xor_element(copies[1], 5, 0x0001)  # a second pair now differs
+    graph.replay()
+    torch.cuda.synchronize()
+    assert res["m"].cpu().tolist() == [0, 1, 0, 1, 0]
