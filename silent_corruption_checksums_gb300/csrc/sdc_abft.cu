@@ -840,30 +840,74 @@ __global__ void __launch_bounds__(128) abft_check_kernel(const CheckSide side0, 
     if (tid == 0) o.done[bx] = 0u;  // ready for the next call
 }
 
-// The fused check's verdict per row: the reference the GEMM's reference warps formed (the partials
-// ref[p][i] = {s, c, mh, ml} of the n_parts tiles of the row's tile row: A[i, :] (W^T 1) over their K
-// blocks and its magnitude, each a float32 pair, merged in tile order) against the row's
-// accumulator checksum, with the verifier's bound (the magnitude raised by 1 + delta).
-__global__ void __launch_bounds__(256) abft_ref_finalize_kernel(const double *__restrict__ rowsum,
-                                                                const float4 *__restrict__ ref, uint32_t n_parts,
-                                                                uint32_t M, uint32_t N, uint32_t K, double delta,
-                                                                float tol_scale, double *__restrict__ residual,
-                                                                double *__restrict__ bound, uint8_t *__restrict__ flag,
-                                                                uint32_t *__restrict__ n_flagged) {
-    const uint32_t i = blockIdx.x * 256 + threadIdx.x;
-    if (i >= M) return;
+// The fused check's last pass, one launch: per row i, the accumulator checksum rowsum[i] from the
+// GEMM's tile partials part[p][i] (double) in abft_sum_parts_kernel's order (eight sums over
+// p = s, s + 8, ..., then added for s = 0 .. 7 in turn: the same bits), and the verdict from the
+// reference partials ref[p][i] = {s, c, mh, ml} (A[i, :] (W^T 1) over tile p's K blocks and its
+// magnitude, float32 pairs), merged over the same eight interleaved runs and then in run order,
+// against the row's checksum: the residual, the bound (the verifier's formula, the magnitude raised
+// by 1 + delta) and the flag.  Block = 32 rows x 8 threads (thread s of a row
+// takes the runs' s-th); block 0's thread 0 publishes the GEMM's abort flag.
+__global__ void __launch_bounds__(256) abft_fused_finalize_kernel(const double *__restrict__ part,
+                                                                  const float4 *__restrict__ ref, uint32_t n_parts,
+                                                                  uint32_t M, uint32_t N, uint32_t K, double delta,
+                                                                  float tol_scale, double *__restrict__ rowsum,
+                                                                  double *__restrict__ residual,
+                                                                  double *__restrict__ bound,
+                                                                  uint8_t *__restrict__ flag,
+                                                                  uint32_t *__restrict__ n_flagged,
+                                                                  const int *__restrict__ err,
+                                                                  uint32_t *__restrict__ aborted) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) *aborted = *err != 0 ? 1u : 0u;
+    const uint32_t sub = threadIdx.x & 7u, i = blockIdx.x * 32 + (threadIdx.x >> 3);
+    const bool in = i < M;
+    double acc = 0.0;
     float s = 0.0f, c = 0.0f, a = 0.0f, e = 0.0f;
-    for (uint32_t p = 0; p < n_parts; ++p) {
-        const float4 r = ref[(uint64_t)p * M + i];
-        pair_merge(s, c, r.x, r.y);
-        pair_merge(a, e, r.z, r.w);
+    if (in) {
+        uint32_t p = sub;
+        for (; p + 8 * 3 < n_parts; p += 8 * 4) {  // 4 partials of each kind in flight, merged in order
+            double pd[4];
+            float4 pr[4];
+#pragma unroll
+            for (uint32_t u = 0; u < 4; ++u) {
+                pd[u] = part[(uint64_t)(p + 8 * u) * M + i];
+                pr[u] = ref[(uint64_t)(p + 8 * u) * M + i];
+            }
+#pragma unroll
+            for (uint32_t u = 0; u < 4; ++u) {
+                acc = __dadd_rn(acc, pd[u]);
+                pair_merge(s, c, pr[u].x, pr[u].y);
+                pair_merge(a, e, pr[u].z, pr[u].w);
+            }
+        }
+        for (; p < n_parts; p += 8) {
+            acc = __dadd_rn(acc, part[(uint64_t)p * M + i]);
+            const float4 r = ref[(uint64_t)p * M + i];
+            pair_merge(s, c, r.x, r.y);
+            pair_merge(a, e, r.z, r.w);
+        }
     }
-    const double refv = (double)s + (double)c;
-    const double mag = ((double)a + (double)e) * (1.0 + delta);
+    // thread 0 of the row takes the eight runs in order (a row's threads are 8 consecutive lanes)
+    const uint32_t lane0 = (threadIdx.x & 31u) & ~7u;
+    double t = acc;
+    float ts = s, tc = c, ta = a, te = e;
+#pragma unroll
+    for (uint32_t k = 1; k < 8; ++k) {
+        const double ak = __shfl_sync(0xffffffffu, acc, lane0 + k);
+        const float sk = __shfl_sync(0xffffffffu, s, lane0 + k), ck = __shfl_sync(0xffffffffu, c, lane0 + k);
+        const float ak2 = __shfl_sync(0xffffffffu, a, lane0 + k), ek = __shfl_sync(0xffffffffu, e, lane0 + k);
+        t = __dadd_rn(t, ak);
+        pair_merge(ts, tc, sk, ck);
+        pair_merge(ta, te, ak2, ek);
+    }
+    if (!in || sub != 0) return;
+    rowsum[i] = t;
+    const double refv = (double)ts + (double)tc;
+    const double mag = ((double)ta + (double)te) * (1.0 + delta);
     const double gk = (double)K * 0x1p-22;
     const double b = (gk * (1.0 + gk) + 20.0 * 0x1p-24 + (double)(N + K + 64) * 0x1p-44) * mag +
                      2.0 * (double)K * (double)N * 0x1p-126;
-    const double d = rowsum[i] - refv;
+    const double d = t - refv;
     residual[i] = d;
     bound[i] = b;
     const uint8_t f = fabs(d) <= (double)tol_scale * b ? 0 : 1;  // NaN flags
@@ -1345,12 +1389,12 @@ sdc_status sdc_abft_gemm_checked(const void *d_A, const void *d_W, void *d_C, ui
                                                                 (const __nv_bfloat16 *)d_A);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_gemm_checked launch");
-    abft_sum_parts_kernel<<<(M + 31) / 32, 256, 0, s>>>(part, M, tiles_n, d_rowsum, err, d_aborted);
     // the magnitude's plain chains: W's column sums (a slab warp's rows), a stage's 32 terms per half
     const uint32_t ns = n_slabs_for(N, K), slab_rows = (N + ns - 1) / ns;
     const double delta = 2.0 * ((double)((slab_rows + 7) / 8) + 32.0 + 8.0) * 0x1p-24;
-    abft_ref_finalize_kernel<<<(M + 255) / 256, 256, 0, s>>>(d_rowsum, ref, tiles_n, M, N, K, delta, tol_scale,
-                                                            d_residual, d_bound, d_flag, &d_summary->n_flagged);
+    abft_fused_finalize_kernel<<<(M + 31) / 32, 256, 0, s>>>(part, ref, tiles_n, M, N, K, delta, tol_scale, d_rowsum,
+                                                            d_residual, d_bound, d_flag, &d_summary->n_flagged, err,
+                                                            d_aborted);
     e = cudaGetLastError();
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_abft_gemm_checked launch");
 }
