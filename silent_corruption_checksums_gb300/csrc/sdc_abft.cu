@@ -469,8 +469,16 @@ struct SlabSide {
     uint32_t planar = 0;  // unweighted: split[] in the check's planar layout instead of {h, m} per column
 };
 
+// zero[0 .. n_zero) and zero2[0 .. n_zero2) are set to 0 by block (0, 0) first: counters and counts
+// that only a later launch on the stream uses (null when there are none).
 template <bool kWeighted>
-__global__ void __launch_bounds__(256, 3) abft_colsum_slab_kernel(const SlabSide s0, const SlabSide s1, uint32_t cb0) {
+__global__ void __launch_bounds__(256, 3) abft_colsum_slab_kernel(const SlabSide s0, const SlabSide s1, uint32_t cb0,
+                                                                  uint32_t *__restrict__ zero, uint32_t n_zero,
+                                                                  uint32_t *__restrict__ zero2, uint32_t n_zero2) {
+    if (blockIdx.x == 0 && blockIdx.y == 0) {
+        for (uint32_t z = threadIdx.x; z < n_zero; z += blockDim.x) zero[z] = 0u;
+        for (uint32_t z = threadIdx.x; z < n_zero2; z += blockDim.x) zero2[z] = 0u;
+    }
     const bool second = blockIdx.x >= cb0;
     const uint32_t bx = second ? blockIdx.x - cb0 : blockIdx.x, by = blockIdx.y;
     const __nv_bfloat16 *__restrict__ X = second ? s1.X : s0.X;
@@ -628,10 +636,17 @@ __global__ void __launch_bounds__(256, 3) abft_colsum_slab_kernel(const SlabSide
 // turn with 8 loads in flight; the lanes' sums meet in a fixed butterfly and lane 0 writes.
 // blockIdx.y picks the matrix: (X0, n0, out0) or (X1, n1, out1), both with T rows.  Matrix i's
 // lines are the first the L2 gives up when bit i of read_once is set (it is not read again soon).
+// Block (0, 0) first sets zero[0 .. n_zero) and zero2[0 .. n_zero2) to 0 (as abft_colsum_slab_kernel).
 __global__ void __launch_bounds__(256) abft_rowsum_kernel(const __nv_bfloat16 *__restrict__ X0, uint32_t n0,
                                                           float2 *__restrict__ out0, const __nv_bfloat16 *__restrict__ X1,
                                                           uint32_t n1, float2 *__restrict__ out1, uint32_t T,
-                                                          uint32_t read_once) {
+                                                          uint32_t read_once, uint32_t *__restrict__ zero,
+                                                          uint32_t n_zero, uint32_t *__restrict__ zero2,
+                                                          uint32_t n_zero2) {
+    if (blockIdx.x == 0 && blockIdx.y == 0) {
+        for (uint32_t z = threadIdx.x; z < n_zero; z += blockDim.x) zero[z] = 0u;
+        for (uint32_t z = threadIdx.x; z < n_zero2; z += blockDim.x) zero2[z] = 0u;
+    }
     const bool second = blockIdx.y != 0;
     const uint64_t policy = l2_policy((read_once >> (second ? 1 : 0)) & 1u);
     const __nv_bfloat16 *__restrict__ X = second ? X1 : X0;
@@ -1110,10 +1125,7 @@ sdc_status sdc_abft_verify(const void *d_A, const void *d_W, uint32_t M, uint32_
     float2 *wsplit = (float2 *)((char *)d_ws + w.wsplit), *asplit = (float2 *)((char *)d_ws + w.asplit);
     float4 *slabs = (float4 *)((char *)d_ws + w.slabs), *chk = (float4 *)((char *)d_ws + w.chk);
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = cudaMemsetAsync(d_summary, 0, sizeof(sdc_abft_summary), s);
-    if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_verify setup");
     uint32_t *done = (uint32_t *)((char *)d_ws + w.done);
-    const size_t done_bytes = w.err - w.done;
     // Both sides at once, in two launches: the column sums of W (for the rows) and of A (for the
     // columns), then A's rows against W's sums and W's rows against A's.  Each side has its own
     // slabs, split partials and counters; without columns each launch serves the row side alone.
@@ -1134,10 +1146,13 @@ sdc_status sdc_abft_verify(const void *d_A, const void *d_W, uint32_t M, uint32_
     const uint64_t a_bytes = (uint64_t)M * K * 2, w_bytes = (uint64_t)N * K * 2;
     sw.keep = cols && w_bytes < a_bytes && w_bytes <= kKeepL2;
     sa.keep = cols && !sw.keep && a_bytes <= kKeepL2;
-    e = cudaMemsetAsync(done, 0, done_bytes, s);
+    // the column sums' counters are zeroed here; the check's counters and the summary by the column
+    // sums' first block (the check reads them only after that grid has completed)
+    cudaError_t e = cudaMemsetAsync(done, 0, 2 * cb * sizeof(uint32_t), s);
     if (e == cudaSuccess) {
         abft_colsum_slab_kernel<false><<<dim3(cols ? 2 * cb : cb, cols && ns_a > ns_w ? ns_a : ns_w), 256, 0, s>>>(
-            sw, cols ? sa : sw, cb);
+            sw, cols ? sa : sw, cb, done + 2 * cb, rb_a + rb_w, (uint32_t *)d_summary,
+            (uint32_t)(sizeof(sdc_abft_summary) / 4));
         e = cudaGetLastError();
     }
     if (e == cudaSuccess) {
@@ -1262,18 +1277,17 @@ sdc_status sdc_abft_verify_wgrad(const void *d_dY, const void *d_X, uint32_t T, 
     uint32_t *done = (uint32_t *)((char *)d_ws + w.done);
     const size_t done_bytes = w.err - w.done;
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = cudaMemsetAsync(d_summary, 0, sizeof(sdc_abft_summary), s);
-    if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_verify_wgrad setup");
     // Both sides at once, in two launches: X's row sums (the weights of dY's column sums: the rows of
     // dW, each checksum summing K outputs) and dY's (the weights of X's: the columns, each summing N),
     // then both weighted column sums, each compared in its last blocks with its checksums.
     // L2 use: the second launch reads both operands again; X (the smaller) keeps its lines if it fits in
     // about half the L2, dY's leave first, then and in the second launch, which reads it last.
     const bool keep_x = (uint64_t)T * K * 2 <= kKeepL2;
-    abft_rowsum_kernel<<<dim3((T + 7) / 8, cols ? 2 : 1), 256, 0, s>>>((const __nv_bfloat16 *)d_X, K, rsplit,
-                                                                      (const __nv_bfloat16 *)d_dY, N, qsplit, T,
-                                                                      (keep_x ? 0u : 1u) | 2u);
-    e = cudaMemsetAsync(done, 0, done_bytes, s);
+    // its first block also zeroes the second launch's counters and the summary
+    abft_rowsum_kernel<<<dim3((T + 7) / 8, cols ? 2 : 1), 256, 0, s>>>(
+        (const __nv_bfloat16 *)d_X, K, rsplit, (const __nv_bfloat16 *)d_dY, N, qsplit, T, (keep_x ? 0u : 1u) | 2u, done,
+        (uint32_t)(done_bytes / 4), (uint32_t *)d_summary, (uint32_t)(sizeof(sdc_abft_summary) / 4));
+    cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess) {
         const uint32_t cb_n = (N + 255) / 256, ns_n = n_slabs_for(T, N), ns_k = n_slabs_for(T, K);
         SlabSide sr{(const __nv_bfloat16 *)d_dY, T, N, ns_n, slabs, nullptr, done,
@@ -1285,7 +1299,7 @@ sdc_status sdc_abft_verify_wgrad(const void *d_dY, const void *d_X, uint32_t T, 
         sr.keep = 0;
         abft_colsum_slab_kernel<true>
             <<<dim3(cols ? cb_n + (K + 255) / 256 : cb_n, cols && ns_k > ns_n ? ns_k : ns_n), 256, 0, s>>>(
-                sr, cols ? sc : sr, cb_n);
+                sr, cols ? sc : sr, cb_n, nullptr, 0, nullptr, 0);
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_verify_wgrad launch");
@@ -1321,7 +1335,7 @@ sdc_status sdc_abft_weight_sums(const void *d_W, uint32_t N, uint32_t K, float *
     e = cudaMemsetAsync(done, 0, cb * sizeof(uint32_t), s);
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_weight_sums setup");
     const SlabSide sw{(const __nv_bfloat16 *)d_W, N, K, ns, slabs, (float2 *)d_wsums, done, ColCheck{}};
-    abft_colsum_slab_kernel<false><<<dim3(cb, ns), 256, 0, s>>>(sw, sw, cb);
+    abft_colsum_slab_kernel<false><<<dim3(cb, ns), 256, 0, s>>>(sw, sw, cb, nullptr, 0, nullptr, 0);
     e = cudaGetLastError();
     return e == cudaSuccess ? SDC_OK : cuda_fail(e, "sdc_abft_weight_sums launch");
 }
