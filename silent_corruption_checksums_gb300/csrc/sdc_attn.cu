@@ -692,9 +692,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
 // -lse log2(e) of every (head, token): the exponent's offset in base 2, negated, which the softmax
 // adds (one float32 product per value, four values per thread and step).  The dV kernel is launched as
-// its programmatic dependent: its set-up and its K and Q copies overlap this grid.
+// its programmatic dependent: its set-up and its K and Q copies overlap this grid.  Block 0 also zeroes
+// the call's summary, which the dV kernel touches only after it has waited for this grid.
 __global__ void __launch_bounds__(256) attn_lse2_kernel(const float4 *__restrict__ lse, uint32_t n4,
-                                                        float4 *__restrict__ lse2) {
+                                                        float4 *__restrict__ lse2, uint32_t *__restrict__ zero,
+                                                        uint32_t n_zero) {
+    if (blockIdx.x == 0)
+        for (uint32_t z = threadIdx.x; z < n_zero; z += blockDim.x) zero[z] = 0u;
     grid_dep_launch();  // the dV kernel may start its set-up now
     for (uint32_t i = blockIdx.x * 256 + threadIdx.x; i < n4; i += gridDim.x * 256) {
         const float4 v = lse[i];
@@ -799,15 +803,17 @@ sdc_status sdc_attn_dv_check_grouped(const void *d_Q, const void *d_K, const voi
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
     const uint32_t n_items = n_kv * ((L + kBlk - 1) / kBlk);
     const uint32_t grid = n_items < (uint32_t)n_sm ? n_items : (uint32_t)n_sm;
+    // the abort word and the counters (the work counter is taken before the dV kernel waits for the
+    // lse2 grid); the summary is zeroed by the lse2 grid
     e = cudaMemsetAsync(err, 0, 16 + (size_t)BH * 4, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(d_summary, 0, sizeof(sdc_abft_summary), s);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(attn_dv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAttnSmem);
     if (e != cudaSuccess) return cuda_fail(e, "sdc_attn_dv_check setup");
     const AttnOut out{d_colsum_dv, d_colsum_do, d_residual, d_bound, d_flag, d_summary, d_aborted, tol_scale};
     const uint32_t n4 = BH * L / 4;  // L is a multiple of 4
     const uint32_t lse_grid = (n4 + 255) / 256 < 4u * (uint32_t)n_sm ? (n4 + 255) / 256 : 4u * (uint32_t)n_sm;
-    attn_lse2_kernel<<<lse_grid, 256, 0, s>>>((const float4 *)d_lse, n4, (float4 *)lse2);
+    attn_lse2_kernel<<<lse_grid, 256, 0, s>>>((const float4 *)d_lse, n4, (float4 *)lse2, (uint32_t *)d_summary,
+                                              (uint32_t)(sizeof(sdc_abft_summary) / 4));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kAttnThreads);
