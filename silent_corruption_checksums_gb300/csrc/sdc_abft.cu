@@ -155,9 +155,12 @@ __global__ void __launch_bounds__(kRef ? kGemmThreads + kRefThreads : kGemmThrea
     abft_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapW,
                      __nv_bfloat16 *__restrict__ C, uint32_t M, uint32_t N, uint32_t K, uint32_t band_m,
                      double *__restrict__ rowsum_part, double *__restrict__ colsum_part, int *__restrict__ err,
-                     const float2 *__restrict__ wsums, float4 *__restrict__ ref, const __nv_bfloat16 *__restrict__ Ag) {
+                     const float2 *__restrict__ wsums, float4 *__restrict__ ref, const __nv_bfloat16 *__restrict__ Ag,
+                     uint32_t *__restrict__ zero, uint32_t n_zero) {
     extern __shared__ __align__(1024) unsigned char smem[];
     const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
+    // zero[0 .. n_zero): counts that only a later launch on the stream adds to (the fused check's summary)
+    if (blockIdx.x == 0 && tid < n_zero) zero[tid] = 0u;
     const uint32_t base = smem_addr(smem), pad = ((base + 1023u) & ~1023u) - base;
     const uint32_t sA = base + pad;                // kStages x 16 KiB, 1 KiB aligned (the swizzle atom)
     const uint32_t sW = sA + kStages * kStageA;    // kStages x 32 KiB
@@ -1089,7 +1092,7 @@ sdc_status sdc_abft_gemm(const void *d_A, const void *d_W, void *d_C, uint32_t M
     uint32_t band_m = (uint32_t)((24u << 20) / ((size_t)kBM * K * 2));
     band_m = band_m < 1 ? 1 : (band_m > tiles_m ? tiles_m : band_m);
     kernel<<<grid, kGemmThreads, smem_bytes, s>>>(mapA, mapW, (__nv_bfloat16 *)d_C, M, N, K, band_m, part, cpart, err,
-                                                  nullptr, nullptr, nullptr);
+                                                  nullptr, nullptr, nullptr, nullptr, 0);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_gemm launch");
     abft_sum_parts_kernel<<<(M + 31) / 32, 256, 0, s>>>(part, M, tiles_n, d_rowsum, err, d_aborted);
@@ -1238,7 +1241,7 @@ sdc_status sdc_abft_gemm_wgrad(const void *d_dY, const void *d_X, void *d_dW, ui
     uint32_t band_m = (uint32_t)((24u << 20) / ((size_t)kBM * T * 2));
     band_m = band_m < 1 ? 1 : (band_m > tiles_m ? tiles_m : band_m);
     kernel<<<grid, kGemmThreads, smem_bytes, s>>>(mapA, mapW, (__nv_bfloat16 *)d_dW, N, K, T, band_m, part, cpart, err,
-                                                  nullptr, nullptr, nullptr);
+                                                  nullptr, nullptr, nullptr, nullptr, 0);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_gemm_wgrad launch");
     abft_sum_parts_kernel<<<(N + 31) / 32, 256, 0, s>>>(part, N, tiles_n, d_rowsum, err, d_aborted);
@@ -1390,8 +1393,7 @@ sdc_status sdc_abft_gemm_checked(const void *d_A, const void *d_W, void *d_C, ui
     int *err = (int *)((char *)d_ws + need - 256);
     cudaStream_t s = (cudaStream_t)stream;
     auto kernel = abft_gemm_kernel<false, false, true>;
-    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int), s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(d_summary, 0, sizeof(sdc_abft_summary), s);
+    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int), s);  // the summary is zeroed by the GEMM kernel
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmemRef);
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_gemm_checked setup");
     const uint32_t n_units = tiles_m * tiles_n;
@@ -1400,7 +1402,8 @@ sdc_status sdc_abft_gemm_checked(const void *d_A, const void *d_W, void *d_C, ui
     band_m = band_m < 1 ? 1 : (band_m > tiles_m ? tiles_m : band_m);
     kernel<<<grid, kGemmThreads + kRefThreads, kGemmSmemRef, s>>>(mapA, mapW, (__nv_bfloat16 *)d_C, M, N, K, band_m,
                                                                 part, nullptr, err, (const float2 *)d_wsums, ref,
-                                                                (const __nv_bfloat16 *)d_A);
+                                                                (const __nv_bfloat16 *)d_A, (uint32_t *)d_summary,
+                                                                (uint32_t)(sizeof(sdc_abft_summary) / 4));
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "sdc_abft_gemm_checked launch");
     // the magnitude's plain chains: W's column sums (a slab warp's rows), a stage's 32 terms per half
