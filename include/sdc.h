@@ -347,7 +347,8 @@ sdc_status sdc_abft_weight_sums(const void *d_W, uint32_t N, uint32_t K, float *
  * stage); d_summary->n_flagged_cols = 0.  Tile (m, n) of the product forms
  * the references of its 128 rows over the K blocks kb with
  * kb mod ceil(N/256) = n, so the work spreads over all tiles; the partials
- * are merged per row in tile order.  Shapes, d_rowsum and d_aborted as
+ * are merged per row in a fixed order (eight interleaved runs of tiles, then
+ * the runs in order).  Shapes, d_rowsum and d_aborted as
  * sdc_abft_gemm; tol_scale > 0; the workspace is
  * sdc_abft_gemm_checked_workspace_size bytes. */
 size_t sdc_abft_gemm_checked_workspace_size(uint32_t M, uint32_t N, uint32_t K);
