@@ -762,7 +762,7 @@ struct CheckSide {
     CheckOut o;
 };
 
-__global__ void __launch_bounds__(128) abft_check_kernel(const CheckSide side0, const CheckSide side1, uint32_t rb0) {
+__global__ void __launch_bounds__(128, 7) abft_check_kernel(const CheckSide side0, const CheckSide side1, uint32_t rb0) {
     const bool second = blockIdx.x >= rb0;
     const uint32_t bx = second ? blockIdx.x - rb0 : blockIdx.x, by = blockIdx.y;
     const __nv_bfloat16 *__restrict__ X = second ? side1.X : side0.X;
@@ -947,12 +947,13 @@ uint32_t n_slabs_for(uint32_t rows, uint32_t K) {
 }
 
 // K splits of the check of `rows` rows: as many as one wave of its blocks of
-// kChkRows rows holds (6 resident per SM on 152 SMs), with at least 128 vectors
-// (4 per lane) per split.  A function of the shapes only, so the workspace size
+// kChkRows rows holds (7 resident per SM on 152 SMs: the kernel is held to 73
+// registers, a few spilled, for the warps), with at least 128 vectors (4 per
+// lane) per split.  A function of the shapes only, so the workspace size
 // is too.
 uint32_t n_splits_for(uint32_t rows, uint32_t K) {
     const uint32_t nvec = K / 8, row_blocks = (rows + kChkRows - 1) / kChkRows;
-    const uint32_t n = 6u * 152u / row_blocks;
+    const uint32_t n = 7u * 152u / row_blocks;
     const uint32_t most = nvec / 128 > 0 ? nvec / 128 : 1;
     return n > most ? most : (n < 1 ? 1 : n);
 }
