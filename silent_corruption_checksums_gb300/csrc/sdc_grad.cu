@@ -166,11 +166,6 @@ __device__ __forceinline__ double warp_total(const FF &f, double acc_e) {
     return tot;
 }
 
-template <int DT>
-__device__ __forceinline__ uint32_t elems_per_vec() {
-    return DT == SDC_DTYPE_F32 ? 4u : 8u;
-}
-
 // ---------------------------------------------------------------- 16-bit path: offset runs
 // For bf16 and f16 each square x^2 is a float32 (8- and 11-bit significands
 // square to at most 22 bits) unless it leaves the float32 range, so a lane can

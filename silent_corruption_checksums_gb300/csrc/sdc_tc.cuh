@@ -148,14 +148,8 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
                  "l"(src), "r"(bytes), "r"(mbar)
                  : "memory");
 }
-// Makes this thread's generic-proxy shared-memory writes visible to the
-// tensor core (async proxy) once a barrier orders them.
-__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mbar) : "memory");
-}
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 __device__ __forceinline__ uint4 ld_shared_u4(uint32_t addr) {
     uint4 v;
@@ -173,8 +167,8 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
 }
 
 // Two float32 pairs at once, one in each half of packed f32x2 registers: the
-// same TwoSum and product splitting as pair_add / pair_fma.
-constexpr uint64_t kF2Sign = 0x8000000080000000ull, kF2Abs = 0x7FFFFFFF7FFFFFFFull;
+// same TwoSum as pair_add.
+constexpr uint64_t kF2Abs = 0x7FFFFFFF7FFFFFFFull;  // clears both halves' sign bits
 __device__ __forceinline__ void pair2_add(uint64_t &s, uint64_t &c, uint64_t x) {
     const uint64_t t = f2_add(s, x);
     const uint64_t bp = f2_sub(t, s);
@@ -182,15 +176,6 @@ __device__ __forceinline__ void pair2_add(uint64_t &s, uint64_t &c, uint64_t x) 
     s = t;
     c = f2_add(c, e);
 }
-__device__ __forceinline__ void pair2_fma(uint64_t &s, uint64_t &c, uint64_t a, uint64_t h, uint64_t l) {
-    const uint64_t p = f2_mul(a, h);
-    const uint64_t e = f2_fma(a, h, p ^ kF2Sign);  // a h - fl(a h), exact
-    pair2_add(s, c, p);
-    c = f2_fma(a, l, f2_add(c, e));
-}
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 typedef CUresult (*PFN_encodeTiled)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                     const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
